@@ -1,0 +1,213 @@
+"""CPU oracle for MoE token layout -> dispatch -> combine (numpy front end).
+
+TEST INFRASTRUCTURE.  Only the test suite, ``__graft_entry__.smoke()`` and the
+benchmark's CPU-baseline / reference leg may import this package.  The product
+library never imports, links or executes anything here, and this package
+imports nothing from the product package: the two share no code.  The only
+shared module is the seeded input generator, which holds none of the method's
+arithmetic.
+
+The arithmetic lives in ``ep_oracle.c`` (plain single-threaded C, one loop per
+step, each function citing the passage it follows).  This module only
+marshals numpy arrays.
+
+Pins (CPU tests): an independent numpy filter-and-sort formulation of the
+layout on small inputs; the count invariants of "DeepEP Symmetric Memory"
+section 7.3; the expected-distinct-groups closed form of the
+``get_theoretical_num_sms`` fragment of "DeepEP V2 ElasticBuffer architecture";
+the exact dispatch -> identity -> combine closed form; the OCP E4M3 definition
+and torch's CPU float8 cast.
+"""
+import ctypes
+import numpy as np
+
+from . import build as _build
+
+_lib = None
+
+_i32p = ctypes.POINTER(ctypes.c_int32)
+
+
+def _load():
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = _build.build()
+    lib = ctypes.CDLL(path)
+    vp = ctypes.c_void_p
+    lib.ep_oracle_layout.restype = ctypes.c_int
+    lib.ep_oracle_layout.argtypes = [vp, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                     ctypes.c_int, ctypes.c_int] + [vp] * 10
+    lib.ep_oracle_dispatch.restype = ctypes.c_int
+    lib.ep_oracle_dispatch.argtypes = [vp, vp, vp, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                       ctypes.c_int, ctypes.c_int, vp, vp, ctypes.c_int,
+                                       ctypes.c_int, ctypes.c_int64, ctypes.c_int, ctypes.c_int,
+                                       ctypes.c_int64, vp, vp, vp, vp, vp, vp]
+    lib.ep_oracle_combine.restype = ctypes.c_int
+    lib.ep_oracle_combine.argtypes = [vp, ctypes.c_int64, vp, vp, ctypes.c_int, ctypes.c_int,
+                                      ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                      vp, vp, ctypes.c_int, vp]
+    lib.ep_oracle_fp8_cast_row.restype = None
+    lib.ep_oracle_fp8_cast_row.argtypes = [vp, ctypes.c_int, vp, vp]
+    lib.ep_oracle_e4m3_encode.restype = ctypes.c_uint8
+    lib.ep_oracle_e4m3_encode.argtypes = [ctypes.c_float]
+    lib.ep_oracle_e4m3_decode.restype = ctypes.c_float
+    lib.ep_oracle_e4m3_decode.argtypes = [ctypes.c_uint8]
+    lib.ep_oracle_float_to_bf16.restype = ctypes.c_uint16
+    lib.ep_oracle_float_to_bf16.argtypes = [ctypes.c_float]
+    lib.ep_oracle_bf16_to_float.restype = ctypes.c_float
+    lib.ep_oracle_bf16_to_float.argtypes = [ctypes.c_uint16]
+    _lib = lib
+    return lib
+
+
+def _p(a):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+EP_ERR_INVALID_INDEX = 4
+EP_ERR_CAPACITY = 8
+
+
+class Layout:
+    """Result of :func:`layout` (all numpy int32 / uint8 arrays)."""
+
+    def __init__(self, **kw):
+        self.__dict__.update(kw)
+
+    @property
+    def num_recv(self):
+        return int(self.rank_offset[-1])
+
+
+def layout(topk_idx, E, R, ranks_per_node=0, expert_alignment=1, with_src_dst=True):
+    """Routing layout of int64 ``topk_idx`` [T, K] (see ep_oracle_layout)."""
+    lib = _load()
+    topk_idx = np.ascontiguousarray(topk_idx, dtype=np.int64)
+    T, K = topk_idx.shape
+    nodes = R // ranks_per_node if ranks_per_node > 0 else 0
+    out = Layout(
+        num_tokens_per_rank=np.zeros(R, np.int32),
+        num_tokens_per_node=np.zeros(nodes, np.int32) if nodes else None,
+        num_tokens_per_expert=np.zeros(E, np.int32),
+        is_token_in_rank=np.zeros((T, R), np.uint8),
+        rank_offset=np.zeros(R + 1, np.int32),
+        expert_offset=np.zeros(E + 1, np.int32),
+        dst_row=np.zeros((T, R), np.int32),
+        src_dst_count=np.zeros((R, R), np.int32) if (with_src_dst and T % R == 0) else None,
+    )
+    scratch_local = np.zeros(max(T * R, 1), np.int32)
+    scratch_mark = np.zeros(R + max(nodes, 1), np.uint8)
+    status = lib.ep_oracle_layout(
+        _p(topk_idx), T, K, E, R, ranks_per_node, expert_alignment,
+        _p(out.num_tokens_per_rank), _p(out.num_tokens_per_node), _p(out.num_tokens_per_expert),
+        _p(out.is_token_in_rank), _p(out.rank_offset), _p(out.expert_offset), _p(out.dst_row),
+        _p(out.src_dst_count), _p(scratch_local), _p(scratch_mark))
+    out.status = status
+    return out
+
+
+def dispatch(x_bits, topk_idx, topk_weights, E, R, dst_row, capacity=None, fp8=False,
+             sf_col_major=False, sf_stride=None, tokens=None):
+    """Dispatch (see ep_oracle_dispatch).
+
+    ``x_bits``: uint16 [T, H] bf16 bit patterns.  With ``tokens`` given, the
+    result is compact: rows numbered in (listed token, rank) order and the
+    returned dict carries ``rows`` (each row's destination index).
+    """
+    lib = _load()
+    x_bits = np.ascontiguousarray(x_bits, dtype=np.uint16)
+    topk_idx = np.ascontiguousarray(topk_idx, dtype=np.int64)
+    topk_weights = np.ascontiguousarray(topk_weights, dtype=np.float32)
+    dst_row = np.ascontiguousarray(dst_row, dtype=np.int32)
+    T, H = x_bits.shape
+    K = topk_idx.shape[1]
+    compact = tokens is not None
+    if compact:
+        tokens = np.ascontiguousarray(tokens, dtype=np.int32)
+        n_rows = int((dst_row[tokens] >= 0).sum())
+    else:
+        n_rows = int(capacity if capacity is not None else (dst_row.max() + 1 if dst_row.size else 0))
+    n_alloc = max(n_rows, 1)
+    row_bytes = H if fp8 else 2 * H
+    nb = H // 128
+    if sf_stride is None:
+        sf_stride = n_alloc
+    recv_x = np.zeros((n_alloc, row_bytes), np.uint8)
+    recv_sf = None
+    if fp8:
+        recv_sf = np.zeros(nb * sf_stride if sf_col_major else n_alloc * nb, np.float32)
+    recv_topk_idx = np.zeros((n_alloc, K), np.int32)
+    recv_topk_weights = np.zeros((n_alloc, K), np.float32)
+    recv_src_idx = np.zeros(n_alloc, np.int32)
+    rows = np.zeros(n_alloc, np.int32) if compact else None
+    status = lib.ep_oracle_dispatch(
+        _p(x_bits), _p(topk_idx), _p(topk_weights), T, H, K, E, R, _p(dst_row),
+        _p(tokens), len(tokens) if compact else 0, 1 if compact else 0, n_rows,
+        1 if fp8 else 0, 1 if sf_col_major else 0, sf_stride,
+        _p(recv_x), _p(recv_sf), _p(recv_topk_idx), _p(recv_topk_weights), _p(recv_src_idx),
+        _p(rows))
+    res = dict(recv_x=recv_x[:n_rows], recv_topk_idx=recv_topk_idx[:n_rows],
+               recv_topk_weights=recv_topk_weights[:n_rows], recv_src_idx=recv_src_idx[:n_rows],
+               status=status)
+    if fp8:
+        res["recv_sf"] = recv_sf if sf_col_major else recv_sf.reshape(n_alloc, nb)[:n_rows]
+    if compact:
+        res["rows"] = rows[:n_rows]
+    return res
+
+
+def combine(y_bits, topk_idx, topk_weights, E, R, dst_row, weighted=False, tokens=None):
+    """Combine (see ep_oracle_combine); returns float64 [len(tokens) or T, H]."""
+    lib = _load()
+    y_bits = np.ascontiguousarray(y_bits, dtype=np.uint16)
+    topk_idx = np.ascontiguousarray(topk_idx, dtype=np.int64)
+    T, K = topk_idx.shape
+    H = y_bits.shape[1]
+    if topk_weights is None:
+        topk_weights = np.zeros((T, K), np.float32)
+    topk_weights = np.ascontiguousarray(topk_weights, dtype=np.float32)
+    dst_row = np.ascontiguousarray(dst_row, dtype=np.int32)
+    if tokens is not None:
+        tokens = np.ascontiguousarray(tokens, dtype=np.int32)
+        n = len(tokens)
+    else:
+        n = T
+    out = np.zeros((max(n, 1), H), np.float64)
+    status = lib.ep_oracle_combine(_p(y_bits), y_bits.shape[0], _p(topk_idx), _p(topk_weights),
+                                   1 if weighted else 0, T, H, K, E, R, _p(dst_row), _p(tokens),
+                                   n if tokens is not None else 0, _p(out))
+    return out[:n], status
+
+
+def fp8_cast_row(x_bits_row):
+    """FP8 e4m3 cast of one bf16 row: returns (codes uint8 [H], sf float32 [H/128])."""
+    lib = _load()
+    x = np.ascontiguousarray(x_bits_row, dtype=np.uint16)
+    H = x.shape[0]
+    q = np.zeros(H, np.uint8)
+    sf = np.zeros(H // 128, np.float32)
+    lib.ep_oracle_fp8_cast_row(_p(x), H, _p(q), _p(sf))
+    return q, sf
+
+
+def e4m3_encode(values):
+    lib = _load()
+    v = np.asarray(values, dtype=np.float32).ravel()
+    return np.array([lib.ep_oracle_e4m3_encode(float(a)) for a in v], np.uint8)
+
+
+def e4m3_decode(codes):
+    lib = _load()
+    c = np.asarray(codes, dtype=np.uint8).ravel()
+    return np.array([lib.ep_oracle_e4m3_decode(int(a)) for a in c], np.float32)
+
+
+def float_to_bf16(values):
+    lib = _load()
+    v = np.asarray(values, dtype=np.float32).ravel()
+    return np.array([lib.ep_oracle_float_to_bf16(float(a)) for a in v], np.uint16)
+
+
+def bf16_to_float(bits):
+    return (np.asarray(bits, dtype=np.uint16).astype(np.uint32) << 16).view(np.float32)

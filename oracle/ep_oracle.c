@@ -1,0 +1,370 @@
+/*
+ * ep_oracle.c -- plain, slow, single-threaded CPU oracle for MoE token
+ * layout -> dispatch -> combine.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing on the product path may link, load or
+ * call this file: only the test suite, the smoke check and the benchmark's
+ * CPU-baseline leg do.  It shares no code, header, table or constant with the
+ * CUDA library; it is written from the definitions alone, one obvious loop per
+ * step, with no blocking, fusion or reordering.
+ *
+ * Sources (page title, then section or code fragment):
+ *  [P1] "DeepEP Symmetric Memory" architecture analysis,
+ *       section 6.1 (the dispatch launch: per-rank / per-expert prefix sums,
+ *       destination slot index, expert alignment), section 7.3 (receive
+ *       counts read back per rank and per local expert), section 9.2
+ *       (dispatch returns recv_x, recv_topk_idx, recv_topk_weights; combine
+ *       takes topk_weights and returns the combined rows).
+ *  [P2] "DeepEP V2 ElasticBuffer architecture", the TokenLayout fragment
+ *       (each received token carries its hidden row, scale factors, top-k
+ *       indices, top-k weights and source token index) and the limits
+ *       fragment (kNumMaxRanks, kNumMaxExperts, kNumMaxExpertsPerRank).
+ *
+ * Readings where the pages are silent (each repeated at its use):
+ *  - T is the total token count; receive order inside a rank is ascending
+ *    global token index (source rank s owns tokens [s*T/R, (s+1)*T/R)).
+ *  - Expert e lives on rank e / (E/R) (contiguous blocks of local experts).
+ *  - topk_idx is int64 with -1 = masked; received indices are int32 local
+ *    expert ids, -1 where the expert is not on the receiving rank, with
+ *    weight 0.0f.
+ *  - FP8: per 128-channel block, amax = max|x|, sf = amax/448,
+ *    q = e4m3_rne_satfinite(x * (448/amax)) in fp32; an all-zero block has
+ *    sf = 1 and multiplier 0.
+ *  - Combine: out[t] = sum over ranks r holding t of c(t,r) * y[dst_row[t,r]],
+ *    c = 1 unweighted, else the sum of t's weights whose expert is on r.
+ *    The oracle accumulates in fp64 and returns fp64 (the exact sum up to
+ *    fp64 rounding); the parity test applies the fp32/bf16 tolerance.
+ *
+ * Parity pins for every function live in the CPU test suite (brute force,
+ * closed forms, invariants, the OCP FP8 definition, a library cast).
+ *
+ * Build: gcc -O2 -std=c11 -ffp-contract=off -shared -fPIC (see build.py).
+ * -ffp-contract=off keeps every multiply and add separately rounded on both
+ * x86-64 and aarch64.
+ */
+#include <stdint.h>
+#include <stddef.h>
+#include <string.h>
+#include <math.h>
+
+#define OR_OK            0
+#define OR_INVALID_INDEX 4
+#define OR_CAPACITY      8
+
+/* ------------------------------------------------------------------------ */
+/* bf16 <-> float.  A bf16 is the upper 16 bits of an IEEE binary32.        */
+/* ------------------------------------------------------------------------ */
+
+float ep_oracle_bf16_to_float(uint16_t b)
+{
+    uint32_t u = ((uint32_t)b) << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return f;
+}
+
+/* Round a binary32 to the nearest bf16, ties to even (finite inputs). */
+uint16_t ep_oracle_float_to_bf16(float f)
+{
+    uint32_t u;
+    memcpy(&u, &f, sizeof u);
+    if ((u & 0x7f800000u) == 0x7f800000u) {           /* inf / nan */
+        if (u & 0x007fffffu) return (uint16_t)((u >> 16) | 0x40u);
+        return (uint16_t)(u >> 16);
+    }
+    uint32_t upper = u >> 16;
+    uint32_t lower = u & 0xffffu;
+    if (lower > 0x8000u || (lower == 0x8000u && (upper & 1u))) upper += 1u;
+    return (uint16_t)upper;
+}
+
+/* ------------------------------------------------------------------------ */
+/* FP8 E4M3 (OCP 8-bit floating point, E4M3 variant):                       */
+/*   1 sign bit, 4 exponent bits (bias 7), 3 mantissa bits;                 */
+/*   exponent field 0 = subnormal, value (m/8) * 2^-6;                      */
+/*   S.1111.111 is NaN; no infinities; largest finite 1.75 * 2^8 = 448.     */
+/* ------------------------------------------------------------------------ */
+
+float ep_oracle_e4m3_decode(uint8_t code)
+{
+    int sign = (code >> 7) & 1;
+    int ex = (code >> 3) & 0xf;
+    int man = code & 7;
+    double v;
+    if (ex == 0xf && man == 7) return NAN;
+    if (ex == 0) v = ldexp((double)man / 8.0, -6);
+    else v = ldexp(1.0 + (double)man / 8.0, ex - 7);
+    return (float)(sign ? -v : v);
+}
+
+/* Round half to even of a non-negative double that is a multiple of 2^-k
+ * for small k (exact in double).  Returns an integer-valued double. */
+static double round_half_even(double q)
+{
+    double fl = floor(q);
+    double frac = q - fl;
+    if (frac > 0.5) return fl + 1.0;
+    if (frac < 0.5) return fl;
+    return (fmod(fl, 2.0) == 0.0) ? fl : fl + 1.0;
+}
+
+/* binary32 -> e4m3, round to nearest even, saturating to +-448 (satfinite).
+ * NaN -> 0x7f (with sign). */
+uint8_t ep_oracle_e4m3_encode(float v)
+{
+    uint8_t sign = signbit(v) ? 0x80 : 0x00;
+    double a = fabs((double)v);
+    if (isnan(v)) return (uint8_t)(sign | 0x7f);
+    if (a >= 448.0) return (uint8_t)(sign | 0x7e);
+    if (a < ldexp(1.0, -6)) {
+        /* subnormal spacing 2^-9; a result of 8 steps is the smallest
+         * normal, whose code is also 8 (exponent field 1, mantissa 0). */
+        double m = round_half_even(a / ldexp(1.0, -9));
+        return (uint8_t)(sign | (uint8_t)m);
+    }
+    int e;
+    frexp(a, &e);               /* a = f * 2^e, f in [0.5, 1) */
+    e -= 1;                     /* a in [2^e, 2^(e+1)) */
+    double m = round_half_even(a / ldexp(1.0, e - 3));  /* in [8, 16] */
+    if (m == 16.0) { m = 8.0; e += 1; }
+    int field = e + 7;
+    int code = (field << 3) | ((int)m - 8);
+    if (code > 0x7e) code = 0x7e;  /* 480 is not finite in E4M3 -> 448 */
+    return (uint8_t)(sign | code);
+}
+
+/* ------------------------------------------------------------------------ */
+/* Layout: routing counts, membership and prefix offsets.                   */
+/* [P1 section 6.1] psum_num_recv_tokens_per_scaleup_rank,                 */
+/* psum_num_recv_tokens_per_expert, dst_buffer_slot_idx, expert_alignment;  */
+/* [P1 section 7.3] per-rank and per-local-expert receive counts.           */
+/*                                                                          */
+/* Per token t in ascending order and per k: skip -1; flag and skip ids     */
+/* outside [0,E); count the expert; mark its rank and node.  Then each      */
+/* marked rank gives t the next local slot of that rank.  Offsets are the   */
+/* exclusive prefix sums; dst_row = rank_offset[r] + local slot, else -1.   */
+/* ------------------------------------------------------------------------ */
+
+int ep_oracle_layout(const int64_t* topk_idx, int T, int K, int E, int R,
+                     int ranks_per_node, int expert_alignment,
+                     int32_t* num_tokens_per_rank,     /* [R]            */
+                     int32_t* num_tokens_per_node,     /* [R/rpn] or NULL */
+                     int32_t* num_tokens_per_expert,   /* [E]            */
+                     uint8_t* is_token_in_rank,        /* [T,R]          */
+                     int32_t* rank_offset,             /* [R+1]          */
+                     int32_t* expert_offset,           /* [E+1]          */
+                     int32_t* dst_row,                 /* [T,R]          */
+                     int32_t* src_dst_count,           /* [R,R] or NULL  */
+                     int32_t* scratch_local,           /* [T,R] scratch  */
+                     uint8_t* scratch_mark)            /* [R + nodes]    */
+{
+    int status = OR_OK;
+    int experts_per_rank = E / R;
+    int num_nodes = (ranks_per_node > 0) ? R / ranks_per_node : 0;
+    int align = expert_alignment > 0 ? expert_alignment : 1;
+
+    for (int r = 0; r < R; ++r) num_tokens_per_rank[r] = 0;
+    for (int e = 0; e < E; ++e) num_tokens_per_expert[e] = 0;
+    if (num_tokens_per_node)
+        for (int n = 0; n < num_nodes; ++n) num_tokens_per_node[n] = 0;
+
+    uint8_t* mark = scratch_mark;
+    uint8_t* node_mark = scratch_mark + R;
+
+    for (int t = 0; t < T; ++t) {
+        for (int r = 0; r < R; ++r) mark[r] = 0;
+        for (int n = 0; n < num_nodes; ++n) node_mark[n] = 0;
+        for (int k = 0; k < K; ++k) {
+            int64_t e = topk_idx[(int64_t)t * K + k];
+            if (e == -1) continue;
+            if (e < -1 || e >= E) { status |= OR_INVALID_INDEX; continue; }
+            num_tokens_per_expert[e] += 1;
+            int r = (int)(e / experts_per_rank);
+            mark[r] = 1;
+            if (num_nodes > 0) node_mark[r / ranks_per_node] = 1;
+        }
+        for (int r = 0; r < R; ++r) {
+            is_token_in_rank[(int64_t)t * R + r] = mark[r];
+            if (mark[r]) {
+                scratch_local[(int64_t)t * R + r] = num_tokens_per_rank[r];
+                num_tokens_per_rank[r] += 1;
+            } else {
+                scratch_local[(int64_t)t * R + r] = -1;
+            }
+        }
+        if (num_tokens_per_node)
+            for (int n = 0; n < num_nodes; ++n)
+                num_tokens_per_node[n] += node_mark[n];
+    }
+
+    rank_offset[0] = 0;
+    for (int r = 0; r < R; ++r)
+        rank_offset[r + 1] = rank_offset[r] + num_tokens_per_rank[r];
+
+    expert_offset[0] = 0;
+    for (int e = 0; e < E; ++e) {
+        int c = num_tokens_per_expert[e];
+        int padded = ((c + align - 1) / align) * align;
+        expert_offset[e + 1] = expert_offset[e] + padded;
+    }
+
+    for (int t = 0; t < T; ++t)
+        for (int r = 0; r < R; ++r) {
+            int32_t l = scratch_local[(int64_t)t * R + r];
+            dst_row[(int64_t)t * R + r] = (l >= 0) ? rank_offset[r] + l : -1;
+        }
+
+    /* Source rank s owns tokens [s*T/R, (s+1)*T/R) (needs R | T). */
+    if (src_dst_count) {
+        for (int i = 0; i < R * R; ++i) src_dst_count[i] = 0;
+        int per_src = T / R;
+        for (int t = 0; t < T && per_src > 0; ++t) {
+            int s = t / per_src;
+            for (int r = 0; r < R; ++r)
+                if (is_token_in_rank[(int64_t)t * R + r])
+                    src_dst_count[s * R + r] += 1;
+        }
+    }
+    return status;
+}
+
+/* ------------------------------------------------------------------------ */
+/* FP8 cast of one row: [P1 section 6.1] / [P1 section 9.1]                 */
+/* use_fp8_dispatch with per-block scale factors (sf_ptr, num_sf_packs).    */
+/* ------------------------------------------------------------------------ */
+
+void ep_oracle_fp8_cast_row(const uint16_t* x_row, int H, uint8_t* q_row, float* sf_row)
+{
+    for (int b = 0; b < H / 128; ++b) {
+        float amax = 0.0f;
+        for (int i = 0; i < 128; ++i) {
+            float v = fabsf(ep_oracle_bf16_to_float(x_row[b * 128 + i]));
+            if (v > amax) amax = v;
+        }
+        float sf, mult;
+        if (amax > 0.0f) {
+            volatile float a = amax;        /* two separate fp32 divides */
+            sf = a / 448.0f;
+            mult = 448.0f / a;
+        } else {
+            sf = 1.0f;
+            mult = 0.0f;
+        }
+        sf_row[b] = sf;
+        for (int i = 0; i < 128; ++i) {
+            volatile float p = ep_oracle_bf16_to_float(x_row[b * 128 + i]) * mult;
+            q_row[b * 128 + i] = ep_oracle_e4m3_encode(p);
+        }
+    }
+}
+
+/* ------------------------------------------------------------------------ */
+/* Dispatch: [P1 section 9.2] recv_x, recv_topk_idx, recv_topk_weights;     */
+/* [P2 TokenLayout fragment] each received row carries hidden, sf,          */
+/* topk_idx, topk_weights and the source token index.                       */
+/*                                                                          */
+/* tokens: list of source tokens to dispatch (NULL = all T in order).       */
+/* compact = 0: output row = dst_row[t,r] (arrays sized by capacity).        */
+/* compact = 1: output rows are numbered 0,1,2,... in (listed token, rank)  */
+/*              order and out_rows[j] receives dst_row[t,r].               */
+/* fp8 = 0: recv_x rows are H bf16 (2H bytes); fp8 = 1: H e4m3 bytes and    */
+/* recv_sf rows of H/128 floats (row-major) or, when sf_col_major, element  */
+/* (j, b) at recv_sf[b * sf_stride + j].                                    */
+/* Returns status bits (invalid index, capacity).                           */
+/* ------------------------------------------------------------------------ */
+
+int ep_oracle_dispatch(const uint16_t* x, const int64_t* topk_idx, const float* topk_weights,
+                       int T, int H, int K, int E, int R, const int32_t* dst_row,
+                       const int32_t* tokens, int num_listed, int compact, int64_t capacity,
+                       int fp8, int sf_col_major, int64_t sf_stride,
+                       uint8_t* recv_x, float* recv_sf, int32_t* recv_topk_idx,
+                       float* recv_topk_weights, int32_t* recv_src_idx, int32_t* out_rows)
+{
+    int status = OR_OK;
+    int experts_per_rank = E / R;
+    int n_list = tokens ? num_listed : T;
+    int64_t j = 0;
+    size_t row_bytes = fp8 ? (size_t)H : (size_t)H * 2;
+    int nb = H / 128;
+    uint8_t q_tmp[65536];
+    float sf_tmp[512];
+
+    for (int i = 0; i < n_list; ++i) {
+        int t = tokens ? tokens[i] : i;
+        for (int r = 0; r < R; ++r) {
+            int32_t d = dst_row[(int64_t)t * R + r];
+            if (d < 0) continue;
+            int64_t row;
+            if (compact) { row = j; out_rows[j] = d; j += 1; }
+            else {
+                if ((int64_t)d >= capacity) { status |= OR_CAPACITY; continue; }
+                row = d;
+            }
+            const uint16_t* src = x + (int64_t)t * H;
+            if (fp8) {
+                ep_oracle_fp8_cast_row(src, H, q_tmp, sf_tmp);
+                memcpy(recv_x + row * (int64_t)row_bytes, q_tmp, row_bytes);
+                if (recv_sf)
+                    for (int b = 0; b < nb; ++b) {
+                        if (sf_col_major) recv_sf[(int64_t)b * sf_stride + row] = sf_tmp[b];
+                        else recv_sf[row * nb + b] = sf_tmp[b];
+                    }
+            } else {
+                memcpy(recv_x + row * (int64_t)row_bytes, src, row_bytes);
+            }
+            for (int k = 0; k < K; ++k) {
+                int64_t e = topk_idx[(int64_t)t * K + k];
+                int on_r = (e >= 0 && e < E && (int)(e / experts_per_rank) == r);
+                if (recv_topk_idx)
+                    recv_topk_idx[row * K + k] = on_r ? (int32_t)(e - (int64_t)r * experts_per_rank) : -1;
+                if (recv_topk_weights)
+                    recv_topk_weights[row * K + k] = on_r ? topk_weights[(int64_t)t * K + k] : 0.0f;
+                if (e < -1 || e >= E) status |= OR_INVALID_INDEX;
+            }
+            if (recv_src_idx) recv_src_idx[row] = t;
+        }
+    }
+    return status;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Combine: [P1 section 9.2] combine(x, handle, topk_weights) -> combined_x. */
+/* For each listed token t: out[t] = sum over r ascending with              */
+/* dst_row[t,r] >= 0 of c(t,r) * y[dst_row[t,r]], with c = 1 (weighted = 0) */
+/* or c = sum over k of topk_weights[t,k] whose expert is on r.             */
+/* fp64 accumulation; out row i belongs to the i-th listed token.           */
+/* Rows at or beyond num_y_rows are skipped and flagged.                    */
+/* ------------------------------------------------------------------------ */
+
+int ep_oracle_combine(const uint16_t* y, int64_t num_y_rows,
+                      const int64_t* topk_idx, const float* topk_weights, int weighted,
+                      int T, int H, int K, int E, int R, const int32_t* dst_row,
+                      const int32_t* tokens, int num_listed, double* out)
+{
+    int status = OR_OK;
+    int experts_per_rank = E / R;
+    int n_list = tokens ? num_listed : T;
+    for (int i = 0; i < n_list; ++i) {
+        int t = tokens ? tokens[i] : i;
+        double* o = out + (int64_t)i * H;
+        for (int h = 0; h < H; ++h) o[h] = 0.0;
+        for (int r = 0; r < R; ++r) {
+            int32_t d = dst_row[(int64_t)t * R + r];
+            if (d < 0) continue;
+            if ((int64_t)d >= num_y_rows) { status |= OR_CAPACITY; continue; }
+            double c = 1.0;
+            if (weighted) {
+                c = 0.0;
+                for (int k = 0; k < K; ++k) {
+                    int64_t e = topk_idx[(int64_t)t * K + k];
+                    if (e >= 0 && e < E && (int)(e / experts_per_rank) == r)
+                        c += (double)topk_weights[(int64_t)t * K + k];
+                }
+            }
+            const uint16_t* yr = y + (int64_t)d * H;
+            for (int h = 0; h < H; ++h)
+                o[h] += c * (double)ep_oracle_bf16_to_float(yr[h]);
+        }
+    }
+    return status;
+}
