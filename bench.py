@@ -1,0 +1,522 @@
+#!/usr/bin/env python
+"""Benchmark of the MoE dispatch / combine hot path on GB300.
+
+One step = routing layout (ep_get_layout) -> bf16 dispatch (ep_dispatch) ->
+identity expert (the combine reads the dispatched rows) -> unweighted combine
+(ep_combine), on the DeepSeek-V3-shaped prefill workload: T=4096 tokens,
+H=7168 bf16, E=256 experts, top-8 distinct uniform experts per token, R=8
+logical ranks in one GPU's memory.  Inputs are seeded synthetic data.
+
+The metric is throughput in GB/s of algorithmic bytes (what the method must
+read and write: see ``algorithmic_bytes``) per step, with tokens/s beside it
+and the dominant kernel's HBM roofline fraction against the measured copy
+bandwidth.  L2 (129 MB) is flushed by a 256 MiB write before the layout and
+again before the combine (in a real layer, expert GEMMs run between them), and
+the flushes are outside the timed events.
+
+Multi-GPU: the path does not shard (ranks are partitions of one GPU), so
+``--gpus N`` under torchrun runs N independent replicas; the time is the max
+over ranks and the value is the sum of all replicas' work ("weak" scaling).
+
+``--impl reference`` times the CPU oracle (the test suite's checker) on the
+host cores instead, on a bounded token sample per step.
+"""
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+L2_FLUSH_BYTES = 256 << 20
+KERNELS_PER_STEP = 5      # layout: count + scan + rows; dispatch: 1; combine: 1
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="dsv3")
+    ap.add_argument("--no-graph", action="store_true", help="launch eagerly instead of CUDA graphs")
+    ap.add_argument("--e2e-steps", type=int, default=30)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0,
+                    help="CPU time budget of the oracle baseline (rank 0, N=1)")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args(argv)
+
+
+# ---------------------------------------------------------------------------
+# algorithmic bytes
+# ---------------------------------------------------------------------------
+
+def algorithmic_bytes(T, H, K, E, R, N, weighted=False, fp8=False):
+    """Bytes the method must move per step (reads + writes), by kernel.
+
+    layout:   read topk_idx (8 B per entry), write dst_row (4 B) and
+              is_token_in_rank (1 B) per (token, rank), plus the O(E + R) counts.
+    dispatch: read x, topk_idx, topk_weights and dst_row; write N rows of
+              payload (+ FP8 scales), K remapped indices, K weights, 1 source index.
+    combine:  read dst_row and N expert-output rows (+ topk for weighting);
+              write T rows.
+    """
+    b_out = 1 if fp8 else 2
+    s = 4 * (H // 128) if fp8 else 0
+    layout = T * K * 8 + T * R * 5 + 4 * (3 * E + 3 * R + 2)
+    dispatch = T * H * 2 + T * K * 12 + T * R * 4 + N * (H * b_out + s + 8 * K + 4)
+    combine = N * H * 2 + T * R * 4 + T * H * 2 + (T * K * 12 if weighted else 0)
+    return dict(layout=layout, dispatch=dispatch, combine=combine,
+                total=layout + dispatch + combine)
+
+
+# ---------------------------------------------------------------------------
+# distributed helpers (replicas)
+# ---------------------------------------------------------------------------
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def reduce_max(value, world, device=None):
+    """Max of a float over all ranks (identity when world == 1)."""
+    if world <= 1:
+        return float(value)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def replica_value(units_per_step, steps, max_total_ms, world):
+    """Whole-job throughput: all replicas' units / the slowest replica's time."""
+    if max_total_ms <= 0:
+        return 0.0
+    return world * units_per_step * steps / (max_total_ms / 1e3)
+
+
+# ---------------------------------------------------------------------------
+# clocks
+# ---------------------------------------------------------------------------
+
+class ClockSampler:
+    """Samples nvidia-smi clocks and throttle reasons while running."""
+
+    QUERY = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "--query-gpu=" + self.QUERY, "--format=csv,noheader,nounits",
+                 "-lms", "100", "-i", str(self.gpu)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=5)
+        sm, mx, reasons = [], [], set()
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for name, val in zip(self.REASONS, parts[4:8]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# peaks and recorded DRAM traffic
+# ---------------------------------------------------------------------------
+
+def hbm_peak():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return 6800.0, "fallback"
+
+
+def kernel_source_hash(kernel):
+    path = os.path.join(ROOT, "combine_ep_get_gb300", "csrc", "%s.cu" % kernel)
+    with open(path, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def recorded_traffic(kernel, workload):
+    """DRAM bytes per launch from an ncu capture, if recorded for this source."""
+    try:
+        with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+            rec = json.load(f)[workload][kernel]
+    except (OSError, KeyError, ValueError):
+        return None
+    if rec.get("source_sha256_16") != kernel_source_hash(kernel):
+        return None
+    return rec.get("dram_bytes_per_launch")
+
+
+# ---------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------
+
+def run_ours(args):
+    import numpy as np
+    import torch
+
+    world, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group(backend="nccl")
+    from combine_ep_get_gb300 import build as lib_build
+    lib_build.build()
+    from combine_ep_get_gb300 import binding as B
+    from combine_ep_get_gb300.inputs import CONFIGS, make_config
+
+    cfg = CONFIGS[args.workload]
+    data = make_config(cfg)
+    T, H, E, K, R = cfg.T, cfg.H, cfg.E, cfg.K, cfg.R
+    dev = torch.device("cuda", local)
+
+    x_host = torch.from_numpy(data["x_bits"].view(np.int16)).view(torch.bfloat16)
+    idx_host = torch.from_numpy(data["topk_idx"])
+    w_host = torch.from_numpy(data["topk_weights"])
+    x = x_host.to(dev)
+    idx = idx_host.to(dev)
+    w = w_host.to(dev)
+
+    lay = B.alloc_layout(T, E, R, cfg.ranks_per_node, device=dev)
+    ws = torch.empty(B.ep_layout_workspace_bytes(T, K, E, R, cfg.ranks_per_node), dtype=torch.uint8,
+                     device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    B.ep_get_layout(idx, E, R, lay, ws, status, cfg.ranks_per_node)
+    N = lay.num_recv            # one host read of rank_offset[R], before any timing
+    recv_x = torch.empty((N, H), dtype=torch.bfloat16, device=dev)
+    recv_idx = torch.empty((N, K), dtype=torch.int32, device=dev)
+    recv_w = torch.empty((N, K), dtype=torch.float32, device=dev)
+    recv_src = torch.empty((N,), dtype=torch.int32, device=dev)
+    out = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    def do_layout():
+        B.ep_get_layout(idx, E, R, lay, ws, status, cfg.ranks_per_node)
+
+    def do_dispatch():
+        B.ep_dispatch(x, idx, w, E, R, lay, recv_x, recv_idx, recv_w, recv_src, status)
+
+    def do_combine():
+        B.ep_combine(recv_x, idx, None, E, R, lay, out, status)
+
+    # eager warm-up (sets kernel attributes outside any capture)
+    for _ in range(2):
+        do_layout()
+        do_dispatch()
+        do_combine()
+    torch.cuda.synchronize()
+    st = int(status.item())
+    if st != 0:
+        raise RuntimeError("device status after warm-up: %s" % B.ep_status_string(st))
+
+    use_graph = not args.no_graph
+    if use_graph:
+        graphs = []
+        for fn in (do_layout, do_dispatch, do_combine):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                fn()
+            graphs.append(g)
+        torch.cuda.synchronize()
+        run_layout, run_dispatch, run_combine = (g.replay for g in graphs)
+    else:
+        run_layout, run_dispatch, run_combine = do_layout, do_dispatch, do_combine
+
+    def one_step(ev=None):
+        flush.zero_()
+        if ev:
+            ev[0].record()
+        run_layout()
+        if ev:
+            ev[1].record()
+        run_dispatch()
+        if ev:
+            ev[2].record()
+        flush.zero_()
+        if ev:
+            ev[3].record()
+        run_combine()
+        if ev:
+            ev[4].record()
+
+    for _ in range(args.warmup):
+        one_step()
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.25)
+    barrier(world)
+    torch.cuda.synchronize()
+    for i in range(args.steps):
+        one_step(events[i])
+    torch.cuda.synchronize()
+    barrier(world)
+    time.sleep(0.15)
+    clocks = sampler.stop()
+    st = int(status.item())
+    if st != 0:
+        raise RuntimeError("device status after timing: %s" % B.ep_status_string(st))
+
+    t_layout = [e[0].elapsed_time(e[1]) for e in events]
+    t_dispatch = [e[1].elapsed_time(e[2]) for e in events]
+    t_combine = [e[3].elapsed_time(e[4]) for e in events]
+    local_total = sum(t_layout) + sum(t_dispatch) + sum(t_combine)
+    max_total = reduce_max(local_total, world, dev)
+
+    nbytes = algorithmic_bytes(T, H, K, E, R, N)
+    value_bps = replica_value(nbytes["total"], args.steps, max_total, world)
+    tokens_ps = replica_value(T, args.steps, max_total, world)
+    ms_per_step = max_total / args.steps
+
+    avg = {"layout": statistics.mean(t_layout), "dispatch": statistics.mean(t_dispatch),
+           "combine": statistics.mean(t_combine)}
+    dominant = "dispatch" if avg["dispatch"] >= avg["combine"] else "combine"
+    peak, peak_kind = hbm_peak()
+    achieved = nbytes[dominant] / (avg[dominant] * 1e-3) / 1e9
+    per_kernel = {k: {"ms": avg[k], "gbs": nbytes[k] / (avg[k] * 1e-3) / 1e9,
+                      "frac_of_" + peak_kind: nbytes[k] / (avg[k] * 1e-3) / 1e9 / peak}
+                  for k in avg}
+
+    # end to end through the public API with host buffers
+    e2e = run_e2e(args, B, torch, dev, x_host, idx_host, w_host, lay, ws, status, recv_x, recv_idx,
+                  recv_w, recv_src, out, cfg, nbytes, world)
+
+    result = {
+        "metric": "dispatch+combine GB/s and tokens/s on 1 GB300; % of HBM roofline",
+        "value": value_bps / 1e9,
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms_per_step,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic",
+        "tokens_per_s": tokens_ps,
+        "config": {
+            "workload": cfg.description,
+            "T": T, "H": H, "E": E, "K": K, "R": R, "N": N,
+            "bytes_per_step": nbytes,
+            "parallelism": "replicas" if world > 1 else "single",
+            "l2": "flushed (256 MiB write) before layout and before combine, outside the timed events",
+            "launch": "CUDA graphs" if use_graph else "eager",
+        },
+        "per_kernel": per_kernel,
+        "roofline": {"bound": "hbm", "kernel": dominant, "achieved": achieved, "peak": peak,
+                     "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / peak,
+                     "traffic": recorded_traffic(dominant, args.workload),
+                     "algorithmic_bytes_per_launch": nbytes[dominant]},
+        "e2e": e2e,
+        "gpu_launches": KERNELS_PER_STEP * args.steps,
+        "clocks": clocks,
+    }
+    if world == 1 and rank == 0 and not args.no_cpu_baseline:
+        result["cpu_baseline"] = cpu_baseline(cfg, data, nbytes, N, args.cpu_seconds)
+    if rank == 0:
+        print(json.dumps(result))
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def run_e2e(args, B, torch, dev, x_host, idx_host, w_host, lay, ws, status, recv_x, recv_idx, recv_w,
+            recv_src, out, cfg, nbytes, world):
+    """Host -> device inputs, the three public calls, device -> host output."""
+    xp = x_host.pin_memory()
+    ip = idx_host.pin_memory()
+    wp = w_host.pin_memory()
+    outp = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    xd = torch.empty_like(xp, device=dev)
+    idd = torch.empty_like(ip, device=dev)
+    wd = torch.empty_like(wp, device=dev)
+    E, R = cfg.E, cfg.R
+
+    def step():
+        xd.copy_(xp, non_blocking=True)
+        idd.copy_(ip, non_blocking=True)
+        wd.copy_(wp, non_blocking=True)
+        B.ep_get_layout(idd, E, R, lay, ws, status, cfg.ranks_per_node)
+        B.ep_dispatch(xd, idd, wd, E, R, lay, recv_x, recv_idx, recv_w, recv_src, status)
+        B.ep_combine(recv_x, idd, None, E, R, lay, out, status)
+        outp.copy_(out, non_blocking=True)
+
+    for _ in range(3):
+        step()
+    torch.cuda.synchronize()
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    start.record()
+    for _ in range(args.e2e_steps):
+        step()
+    end.record()
+    torch.cuda.synchronize()
+    barrier(world)
+    ms = reduce_max(start.elapsed_time(end), world, dev)
+    h2d = xp.numel() * xp.element_size() + ip.numel() * ip.element_size() + wp.numel() * wp.element_size()
+    d2h = outp.numel() * outp.element_size()
+    return {"value": replica_value(nbytes["total"], args.e2e_steps, ms, world) / 1e9, "unit": "GB/s",
+            "ms_per_step": ms / args.e2e_steps, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "launch": "eager through the binding"}
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle (baseline leg and reference arm)
+# ---------------------------------------------------------------------------
+
+def _oracle_step(oracle, np, data, cfg, tokens):
+    """The oracle's layout on all tokens, then dispatch and combine of `tokens`."""
+    idx, w, xb = data["topk_idx"], data["topk_weights"], data["x_bits"]
+    L = oracle.layout(idx, cfg.E, cfg.R, cfg.ranks_per_node)
+    d = oracle.dispatch(xb, idx, w, cfg.E, cfg.R, L.dst_row, tokens=tokens)
+    mask = L.dst_row[tokens] >= 0
+    local = np.full(mask.shape, -1, np.int32)
+    local[mask] = np.arange(int(mask.sum()), dtype=np.int32)
+    oracle.combine(d["recv_x"].view(np.uint16), idx[tokens], None, cfg.E, cfg.R, local)
+    return int(mask.sum())
+
+
+def _sample_bytes(cfg, n_tok, n_rows):
+    T, H, K, E, R = cfg.T, cfg.H, cfg.K, cfg.E, cfg.R
+    full = algorithmic_bytes(T, H, K, E, R, 0)
+    disp = n_tok * H * 2 + n_tok * K * 12 + n_tok * R * 4 + n_rows * (H * 2 + 8 * K + 4)
+    comb = n_rows * H * 2 + n_tok * R * 4 + n_tok * H * 2
+    return full["layout"] + disp + comb
+
+
+def cpu_baseline(cfg, data, nbytes, N, seconds):
+    import numpy as np
+    import oracle
+    tokens = np.arange(cfg.T, dtype=np.int32)
+    done, moved = 0, 0
+    t0 = time.perf_counter()
+    while True:
+        rows = _oracle_step(oracle, np, data, cfg, tokens)
+        done += 1
+        moved += _sample_bytes(cfg, cfg.T, rows)
+        if time.perf_counter() - t0 >= seconds:
+            break
+    el = time.perf_counter() - t0
+    return {"value": moved / el / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": "%d full step(s) of the workload (all %d tokens), single-threaded C oracle"
+                      % (done, cfg.T),
+            "tokens_per_s": done * cfg.T / el}
+
+
+def run_reference(args):
+    world, rank, local = dist_env()
+    if rank != 0:
+        return
+    import numpy as np
+    import oracle
+    from combine_ep_get_gb300.inputs import CONFIGS, make_config
+    cfg = CONFIGS[args.workload]
+    data = make_config(cfg)
+    # size each step's token sample so that warm-up + timed steps take ~2 minutes
+    probe = np.arange(64, dtype=np.int32)
+    t0 = time.perf_counter()
+    _oracle_step(oracle, np, data, cfg, probe)
+    per_tok = max((time.perf_counter() - t0) / 64, 1e-7)
+    budget = 120.0 / max(args.steps + args.warmup, 1)
+    n_tok = int(min(cfg.T, max(8, budget / per_tok)))
+    starts = [(i * n_tok) % cfg.T for i in range(args.steps + args.warmup)]
+
+    def toks(s):
+        return (np.arange(s, s + n_tok) % cfg.T).astype(np.int32)
+
+    for s in starts[:args.warmup]:
+        _oracle_step(oracle, np, data, cfg, toks(s))
+    moved = 0
+    t0 = time.perf_counter()
+    for s in starts[args.warmup:]:
+        rows = _oracle_step(oracle, np, data, cfg, toks(s))
+        moved += _sample_bytes(cfg, n_tok, rows)
+    el = time.perf_counter() - t0
+    value = moved / el / 1e9
+    sample = ("%d tokens per step (layout on all %d tokens, dispatch and combine of the sample), "
+              "single-threaded C oracle" % (n_tok, cfg.T))
+    print(json.dumps({
+        "impl": "reference",
+        "metric": "dispatch+combine GB/s and tokens/s on 1 GB300; % of HBM roofline",
+        "value": value, "unit": "GB/s", "n_gpus": args.gpus, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": el * 1e3 / max(args.steps, 1),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic", "tokens_per_s": args.steps * n_tok / el,
+        "config": {"workload": cfg.description, "T": cfg.T, "H": cfg.H, "E": cfg.E, "K": cfg.K,
+                   "R": cfg.R, "l2": "n/a (host)"},
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }))
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,158 @@
+"""ctypes binding of libep_get.so with the C ABI's entry-point names.
+
+Argument marshalling only: tensors become device pointers, the current torch
+CUDA stream becomes the cudaStream_t, and a non-zero host status raises.  All
+computation happens in the library's CUDA kernels.  Importing this module
+fails when the library has not been built (there is no CPU fallback).
+"""
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libep_get.so")
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError("libep_get.so is not built; run `python -c \"import __graft_entry__ as g; "
+                      "g.build()\"` or `python combine_ep_get_gb300/build.py`")
+
+_lib = ctypes.CDLL(LIB_PATH)
+
+EP_OK = 0
+EP_ERR_INVALID_ARG = 1
+EP_ERR_UNSUPPORTED = 2
+EP_ERR_INVALID_INDEX = 4
+EP_ERR_CAPACITY = 8
+EP_ERR_TIMEOUT = 16
+EP_ERR_CUDA = 32
+EP_BF16 = 0
+EP_FP8_E4M3 = 1
+
+_vp = ctypes.c_void_p
+_i = ctypes.c_int
+_i64 = ctypes.c_int64
+
+
+class ep_layout_t(ctypes.Structure):
+    _fields_ = [("num_tokens_per_rank", _vp), ("num_tokens_per_node", _vp),
+                ("num_tokens_per_expert", _vp), ("is_token_in_rank", _vp), ("rank_offset", _vp),
+                ("expert_offset", _vp), ("dst_row", _vp), ("src_dst_count", _vp)]
+
+
+_lib.ep_layout_workspace_bytes.restype = ctypes.c_size_t
+_lib.ep_layout_workspace_bytes.argtypes = [_i, _i, _i, _i, _i]
+_lib.ep_recv_capacity_bound.restype = _i64
+_lib.ep_recv_capacity_bound.argtypes = [_i, _i, _i]
+_lib.ep_get_layout.restype = ctypes.c_int32
+_lib.ep_get_layout.argtypes = [_vp, _i, _i, _i, _i, _i, _i, ctypes.POINTER(ep_layout_t), _vp,
+                               ctypes.c_size_t, _vp, _vp]
+_lib.ep_dispatch.restype = ctypes.c_int32
+_lib.ep_dispatch.argtypes = [_vp, _vp, _vp, _i, _i, _i, _i, _i, ctypes.POINTER(ep_layout_t), _i,
+                             _i64, _vp, _vp, _i, _vp, _vp, _vp, _vp, _vp]
+_lib.ep_combine.restype = ctypes.c_int32
+_lib.ep_combine.argtypes = [_vp, _i64, _vp, _vp, _i, _i, _i, _i, _i, ctypes.POINTER(ep_layout_t),
+                            _vp, _vp, _vp]
+_lib.ep_status_string.restype = ctypes.c_char_p
+_lib.ep_status_string.argtypes = [ctypes.c_int32]
+_lib.ep_abi_version.restype = _i
+_lib.ep_abi_version.argtypes = []
+
+
+def library():
+    """The loaded ctypes library (for callers that marshal raw pointers)."""
+    return _lib
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    return t.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream
+
+
+def _check(code, what):
+    if code != EP_OK:
+        raise RuntimeError("%s failed: %s" % (what, ep_status_string(code)))
+    return code
+
+
+def ep_status_string(status) -> str:
+    return _lib.ep_status_string(int(status)).decode()
+
+
+def ep_layout_workspace_bytes(num_tokens, num_topk, num_experts, num_ranks, ranks_per_node=0) -> int:
+    return int(_lib.ep_layout_workspace_bytes(num_tokens, num_topk, num_experts, num_ranks,
+                                              ranks_per_node))
+
+
+def ep_recv_capacity_bound(num_tokens, num_topk, num_ranks) -> int:
+    return int(_lib.ep_recv_capacity_bound(num_tokens, num_topk, num_ranks))
+
+
+class Layout:
+    """Device tensors of one routing layout plus their ep_layout_t view."""
+
+    def __init__(self, T, E, R, ranks_per_node=0, with_src_dst=True, device="cuda"):
+        i32 = dict(dtype=torch.int32, device=device)
+        nodes = R // ranks_per_node if ranks_per_node > 0 else 0
+        self.T, self.E, self.R, self.ranks_per_node = T, E, R, ranks_per_node
+        self.num_tokens_per_rank = torch.empty(R, **i32)
+        self.num_tokens_per_node = torch.empty(nodes, **i32) if nodes else None
+        self.num_tokens_per_expert = torch.empty(E, **i32)
+        self.is_token_in_rank = torch.empty((T, R), dtype=torch.uint8, device=device)
+        self.rank_offset = torch.empty(R + 1, **i32)
+        self.expert_offset = torch.empty(E + 1, **i32)
+        self.dst_row = torch.empty((T, R), **i32)
+        self.src_dst_count = torch.empty((R, R), **i32) if (with_src_dst and T % R == 0) else None
+        self.c = ep_layout_t(*[_ptr(getattr(self, f)) for f, _ in ep_layout_t._fields_])
+
+    @property
+    def num_recv(self) -> int:
+        """N = rank_offset[R] (one device-to-host read)."""
+        return int(self.rank_offset[-1].item())
+
+
+def alloc_layout(T, E, R, ranks_per_node=0, with_src_dst=True, device="cuda") -> Layout:
+    return Layout(T, E, R, ranks_per_node, with_src_dst, device)
+
+
+def ep_get_layout(topk_idx, num_experts, num_ranks, layout, workspace, d_status, ranks_per_node=0,
+                  expert_alignment=1, stream=None):
+    T, K = topk_idx.shape
+    assert topk_idx.dtype == torch.int64 and topk_idx.is_contiguous()
+    code = _lib.ep_get_layout(_ptr(topk_idx), T, K, num_experts, num_ranks, ranks_per_node,
+                              expert_alignment, ctypes.byref(layout.c), _ptr(workspace),
+                              workspace.numel() * workspace.element_size(), _ptr(d_status),
+                              _stream(stream))
+    return _check(code, "ep_get_layout")
+
+
+def ep_dispatch(x, topk_idx, topk_weights, num_experts, num_ranks, layout, recv_x, recv_topk_idx,
+                recv_topk_weights, recv_src_idx, d_status, recv_sf=None, out_dtype=EP_BF16,
+                sf_col_major=False, stream=None):
+    T, H = x.shape
+    K = topk_idx.shape[1]
+    assert x.element_size() == 2 and x.is_contiguous() and recv_x.is_contiguous()
+    capacity = recv_x.shape[0]
+    code = _lib.ep_dispatch(_ptr(x), _ptr(topk_idx), _ptr(topk_weights), T, H, K, num_experts,
+                            num_ranks, ctypes.byref(layout.c), out_dtype, capacity, _ptr(recv_x),
+                            _ptr(recv_sf), 1 if sf_col_major else 0, _ptr(recv_topk_idx),
+                            _ptr(recv_topk_weights), _ptr(recv_src_idx), _ptr(d_status),
+                            _stream(stream))
+    return _check(code, "ep_dispatch")
+
+
+def ep_combine(y, topk_idx, topk_weights, num_experts, num_ranks, layout, out, d_status, stream=None):
+    T, H = out.shape
+    K = topk_idx.shape[1]
+    assert y.element_size() == 2 and y.is_contiguous() and out.is_contiguous()
+    code = _lib.ep_combine(_ptr(y), y.shape[0], _ptr(topk_idx), _ptr(topk_weights), T, H, K,
+                           num_experts, num_ranks, ctypes.byref(layout.c), _ptr(out), _ptr(d_status),
+                           _stream(stream))
+    return _check(code, "ep_combine")

@@ -1,0 +1,224 @@
+// C ABI of libep_get.so: host-side argument checks, parameter blocks and
+// launches.  Declarations and the full contract are in include/ep_get.h.
+#include <mutex>
+#include <string>
+
+#include "ep_internal.cuh"
+
+namespace epg {
+
+const DeviceInfo& device_info() {
+    constexpr int kMaxDevices = 64;
+    static std::mutex mu;
+    static DeviceInfo infos[kMaxDevices];
+    static bool have[kMaxDevices] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) dev = 0;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!have[dev]) {
+        DeviceInfo d{dev, 0, 0};
+        cudaDeviceGetAttribute(&d.num_sms, cudaDevAttrMultiProcessorCount, dev);
+        cudaDeviceGetAttribute(&d.max_smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+        if (d.num_sms < 1) d.num_sms = 1;
+        infos[dev] = d;
+        have[dev] = true;
+    }
+    return infos[dev];
+}
+
+}  // namespace epg
+
+namespace {
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+inline bool ok_ptr(const void* p) { return p != nullptr && aligned16(p); }
+
+// Shape checks shared by the three calls.
+ep_status_t check_shape(int T, int K, int E, int R) {
+    if (T < 0 || K < 1 || E < 1 || R < 1) return EP_ERR_INVALID_ARG;
+    if (K > EP_MAX_TOPK || R > EP_MAX_RANKS || E > EP_MAX_EXPERTS) return EP_ERR_UNSUPPORTED;
+    if (E % R != 0) return EP_ERR_INVALID_ARG;
+    if (E / R > EP_MAX_EXPERTS_PER_RANK) return EP_ERR_UNSUPPORTED;
+    if (static_cast<int64_t>(T) * R > INT32_MAX || static_cast<int64_t>(T) * K > INT32_MAX)
+        return EP_ERR_UNSUPPORTED;
+    return EP_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int ep_abi_version(void) { return 1; }
+
+size_t ep_layout_workspace_bytes(int num_tokens, int num_topk, int num_experts, int num_ranks,
+                                 int ranks_per_node) {
+    (void)num_topk;
+    if (num_tokens < 0 || num_experts < 1 || num_ranks < 1) return 16;
+    const int nodes = ranks_per_node > 0 ? num_ranks / ranks_per_node : 0;
+    return epg::layout_workspace(num_tokens, num_experts, num_ranks, nodes).total;
+}
+
+int64_t ep_recv_capacity_bound(int num_tokens, int num_topk, int num_ranks) {
+    if (num_tokens <= 0 || num_topk <= 0 || num_ranks <= 0) return 0;
+    return static_cast<int64_t>(num_tokens) * (num_topk < num_ranks ? num_topk : num_ranks);
+}
+
+ep_status_t ep_get_layout(const int64_t* topk_idx, int T, int K, int E, int R, int ranks_per_node,
+                          int expert_alignment, const ep_layout_t* out, void* workspace,
+                          size_t ws_bytes, int32_t* d_status, void* cuda_stream) {
+    if (!out || !d_status) return EP_ERR_INVALID_ARG;
+    ep_status_t s = check_shape(T, K, E, R);
+    if (s != EP_OK) return s;
+    if (ranks_per_node < 0 || (ranks_per_node > 0 && R % ranks_per_node != 0))
+        return EP_ERR_INVALID_ARG;
+    if (expert_alignment < 1) return EP_ERR_INVALID_ARG;
+    if (!ok_ptr(out->num_tokens_per_rank) || !ok_ptr(out->num_tokens_per_expert) ||
+        !ok_ptr(out->rank_offset) || !ok_ptr(out->expert_offset))
+        return EP_ERR_INVALID_ARG;
+    if (T > 0 && (!ok_ptr(topk_idx) || !ok_ptr(out->is_token_in_rank) || !ok_ptr(out->dst_row)))
+        return EP_ERR_INVALID_ARG;
+    if (out->num_tokens_per_node && !aligned16(out->num_tokens_per_node)) return EP_ERR_INVALID_ARG;
+    if (out->src_dst_count && (!aligned16(out->src_dst_count) || T % R != 0)) return EP_ERR_INVALID_ARG;
+    const int nodes_ws = ranks_per_node > 0 ? R / ranks_per_node : 0;
+    const epg::LayoutWorkspace w = epg::layout_workspace(T, E, R, nodes_ws);
+    if (!ok_ptr(workspace) || ws_bytes < w.total) return EP_ERR_INVALID_ARG;
+
+    epg::LayoutParams p{};
+    p.topk_idx = topk_idx;
+    p.T = T;
+    p.K = K;
+    p.E = E;
+    p.R = R;
+    p.experts_per_rank = E / R;
+    p.ranks_per_node = ranks_per_node;
+    p.num_nodes = (ranks_per_node > 0 && out->num_tokens_per_node) ? R / ranks_per_node : 0;
+    p.alignment = expert_alignment;
+    p.num_tiles = (T + epg::kTileTokens - 1) / epg::kTileTokens;
+    p.num_tokens_per_rank = out->num_tokens_per_rank;
+    p.num_tokens_per_node = out->num_tokens_per_node;
+    p.num_tokens_per_expert = out->num_tokens_per_expert;
+    p.is_token_in_rank = out->is_token_in_rank;
+    p.rank_offset = out->rank_offset;
+    p.expert_offset = out->expert_offset;
+    p.dst_row = out->dst_row;
+    p.src_dst_count = out->src_dst_count;
+    char* ws = static_cast<char*>(workspace);
+    p.ws_rank = reinterpret_cast<int32_t*>(ws + w.off_rank);
+    p.ws_expert = reinterpret_cast<int32_t*>(ws + w.off_expert);
+    p.ws_node = reinterpret_cast<int32_t*>(ws + w.off_node);
+    p.ws_bitmap = reinterpret_cast<uint32_t*>(ws + w.off_bitmap);
+    p.status = d_status;
+    return epg::launch_layout(p, static_cast<cudaStream_t>(cuda_stream)) == cudaSuccess ? EP_OK
+                                                                                      : EP_ERR_CUDA;
+}
+
+ep_status_t ep_dispatch(const void* x, const int64_t* topk_idx, const float* topk_weights, int T,
+                        int H, int K, int E, int R, const ep_layout_t* layout, int out_dtype,
+                        int64_t recv_capacity, void* recv_x, float* recv_sf, int sf_col_major,
+                        int32_t* recv_topk_idx, float* recv_topk_weights, int32_t* recv_src_idx,
+                        int32_t* d_status, void* cuda_stream) {
+    if (!layout || !d_status) return EP_ERR_INVALID_ARG;
+    ep_status_t s = check_shape(T, K, E, R);
+    if (s != EP_OK) return s;
+    if (H < 1) return EP_ERR_INVALID_ARG;
+    if (out_dtype == EP_BF16) {
+        if (H % 8 != 0) return EP_ERR_INVALID_ARG;
+    } else if (out_dtype == EP_FP8_E4M3) {
+        if (H % 128 != 0) return EP_ERR_INVALID_ARG;
+        if (H > 65536) return EP_ERR_UNSUPPORTED;
+    } else {
+        return EP_ERR_INVALID_ARG;
+    }
+    if (recv_capacity < 0 || recv_capacity > INT32_MAX) return EP_ERR_INVALID_ARG;
+    if (static_cast<int64_t>(H) * 2 > UINT32_MAX / 2) return EP_ERR_UNSUPPORTED;
+    if (T > 0 && (!ok_ptr(x) || !ok_ptr(topk_idx) || !ok_ptr(layout->dst_row)))
+        return EP_ERR_INVALID_ARG;
+    if (recv_capacity > 0 && !ok_ptr(recv_x)) return EP_ERR_INVALID_ARG;
+    if (out_dtype == EP_FP8_E4M3 && recv_capacity > 0 && !ok_ptr(recv_sf)) return EP_ERR_INVALID_ARG;
+    if (recv_topk_weights && T > 0 && !ok_ptr(topk_weights)) return EP_ERR_INVALID_ARG;
+    if ((recv_topk_idx && !aligned16(recv_topk_idx)) ||
+        (recv_topk_weights && !aligned16(recv_topk_weights)) ||
+        (recv_src_idx && !aligned16(recv_src_idx)))
+        return EP_ERR_INVALID_ARG;
+    if (T == 0) return EP_OK;
+
+    epg::DispatchParams p{};
+    p.x = static_cast<const uint8_t*>(x);
+    p.topk_idx = topk_idx;
+    p.topk_weights = topk_weights;
+    p.dst_row = layout->dst_row;
+    p.T = T;
+    p.H = H;
+    p.K = K;
+    p.E = E;
+    p.R = R;
+    p.experts_per_rank = E / R;
+    p.capacity = recv_capacity;
+    p.recv_x = static_cast<uint8_t*>(recv_x);
+    p.recv_sf = recv_sf;
+    p.sf_col_major = sf_col_major ? 1 : 0;
+    p.sf_stride = (recv_capacity + 3) / 4 * 4;
+    p.recv_topk_idx = recv_topk_idx;
+    p.recv_topk_weights = recv_topk_weights;
+    p.recv_src_idx = recv_src_idx;
+    p.status = d_status;
+    cudaStream_t st = static_cast<cudaStream_t>(cuda_stream);
+    const cudaError_t e = out_dtype == EP_BF16 ? epg::launch_dispatch_bf16(p, st)
+                                               : epg::launch_dispatch_fp8(p, st);
+    return e == cudaSuccess ? EP_OK : EP_ERR_CUDA;
+}
+
+ep_status_t ep_combine(const void* y, int64_t num_y_rows, const int64_t* topk_idx,
+                       const float* topk_weights, int T, int H, int K, int E, int R,
+                       const ep_layout_t* layout, void* out, int32_t* d_status, void* cuda_stream) {
+    if (!layout || !d_status) return EP_ERR_INVALID_ARG;
+    ep_status_t s = check_shape(T, K, E, R);
+    if (s != EP_OK) return s;
+    if (H < 1 || H % 8 != 0) return EP_ERR_INVALID_ARG;
+    if (num_y_rows < 0 || num_y_rows > INT32_MAX) return EP_ERR_INVALID_ARG;
+    if (num_y_rows > 0 && !ok_ptr(y)) return EP_ERR_INVALID_ARG;
+    if (T > 0 && (!ok_ptr(out) || !ok_ptr(layout->dst_row))) return EP_ERR_INVALID_ARG;
+    if (topk_weights && T > 0 && (!ok_ptr(topk_weights) || !ok_ptr(topk_idx))) return EP_ERR_INVALID_ARG;
+    if (T == 0) return EP_OK;
+
+    epg::CombineParams p{};
+    p.y = static_cast<const uint8_t*>(y);
+    p.num_y_rows = num_y_rows;
+    p.topk_idx = topk_idx;
+    p.topk_weights = topk_weights;
+    p.dst_row = layout->dst_row;
+    p.T = T;
+    p.H = H;
+    p.K = K;
+    p.E = E;
+    p.R = R;
+    p.experts_per_rank = E / R;
+    p.out = static_cast<uint8_t*>(out);
+    p.status = d_status;
+    const cudaError_t e =
+        epg::launch_combine(p, topk_weights != nullptr, static_cast<cudaStream_t>(cuda_stream));
+    return e == cudaSuccess ? EP_OK : EP_ERR_CUDA;
+}
+
+const char* ep_status_string(int32_t status) {
+    static const char* const kNames[6] = {"invalid_arg", "unsupported", "invalid_index",
+                                          "capacity",    "timeout",     "cuda"};
+    static std::string table[64];
+    static std::once_flag once;
+    std::call_once(once, [] {
+        table[0] = "ok";
+        for (int v = 1; v < 64; ++v) {
+            std::string sname;
+            for (int b = 0; b < 6; ++b)
+                if (v & (1 << b)) {
+                    if (!sname.empty()) sname += "|";
+                    sname += kNames[b];
+                }
+            table[v] = sname;
+        }
+    });
+    if (status < 0 || status >= 64) return "unknown";
+    return table[status].c_str();
+}
+
+}  // extern "C"

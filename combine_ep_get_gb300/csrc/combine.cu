@@ -1,0 +1,151 @@
+// Combine: gather each token's expert-output rows back from the receive rows
+// and reduce them into token order ("DeepEP Symmetric Memory" section 9.2,
+// combine(x, handle, topk_weights) -> combined_x):
+//   out[t] = bf16_rne( sum over ranks r holding t of c(t,r) * y[dst_row[t,r]] )
+// with fp32 accumulation; c = 1 unweighted, else the sum of t's top-k weights
+// whose expert lives on r.
+//
+// One CTA of 128 threads per (token, piece of the row).  Warp 0 compacts the
+// token's receive rows (ascending rank) and coefficients into shared memory;
+// then every thread owns 16-byte vectors of the piece and issues the loads of
+// up to 8 source rows back to back (read-only, no L1 allocation) before
+// accumulating, so each thread keeps up to 128 bytes of reads in flight.  The
+// reduced vector is rounded to bf16 and stored once.  HBM-bound: reads are
+// ~n(t) times the writes.
+#include <cuda_bf16.h>
+
+#include "ep_internal.cuh"
+
+namespace epg {
+namespace {
+
+constexpr int kThreads = 128;
+constexpr int kBatch = 8;
+
+template <bool kWeighted>
+__global__ void __launch_bounds__(kThreads) combine_kernel(const CombineParams p) {
+    __shared__ int s_rows[EP_MAX_TOPK];
+    __shared__ float s_coef[EP_MAX_TOPK];
+    __shared__ int s_n;
+    const int64_t it = blockIdx.x;
+    const int t = static_cast<int>(it / p.chunks);
+    const int c = static_cast<int>(it - static_cast<int64_t>(t) * p.chunks);
+
+    if (threadIdx.x < 32) {
+        const int lane = threadIdx.x;
+        int64_t e_l = -1;
+        float w_l = 0.0f;
+        if (kWeighted && lane < p.K) {
+            e_l = p.topk_idx[static_cast<int64_t>(t) * p.K + lane];
+            w_l = p.topk_weights[static_cast<int64_t>(t) * p.K + lane];
+        }
+        int n = 0;
+        bool cap_bad = false;
+        for (int rb = 0; rb < p.R; rb += 32) {
+            const int r = rb + lane;
+            const int d = r < p.R ? p.dst_row[static_cast<int64_t>(t) * p.R + r] : -1;
+            const bool ok = d >= 0 && d < p.num_y_rows;
+            if (d >= p.num_y_rows) cap_bad = true;
+            float coef = 1.0f;
+            if (kWeighted) {
+                coef = 0.0f;
+                for (int k = 0; k < p.K; ++k) {
+                    const int64_t e = __shfl_sync(0xffffffffu, e_l, k);
+                    const float w = __shfl_sync(0xffffffffu, w_l, k);
+                    if (e >= 0 && e < p.E && static_cast<int>(e) / p.experts_per_rank == r) coef += w;
+                }
+            }
+            const unsigned m = __ballot_sync(0xffffffffu, ok);
+            const int pos = n + __popc(m & ((1u << lane) - 1u));
+            // A layout from ep_get_layout has at most K <= 32 ranks per token;
+            // a foreign dst_row with more is cut off and flagged.
+            if (ok && pos < EP_MAX_TOPK) {
+                s_rows[pos] = d;
+                s_coef[pos] = coef;
+            }
+            n += __popc(m);
+        }
+        if (n > EP_MAX_TOPK) {
+            if (lane == 0) atomicOr(p.status, EP_ERR_INVALID_INDEX);
+            n = EP_MAX_TOPK;
+        }
+        if (lane == 0) s_n = n;
+        if (__any_sync(0xffffffffu, cap_bad) && lane == 0 && c == 0) atomicOr(p.status, EP_ERR_CAPACITY);
+    }
+    __syncthreads();
+
+    const int n = s_n;
+    const int n_vec = p.H / 8;
+    const int v_begin = c * p.chunk_vecs;
+    const int v_end = min(n_vec, v_begin + p.chunk_vecs);
+    const int64_t row_bytes = static_cast<int64_t>(p.H) * 2;
+    for (int v = v_begin + threadIdx.x; v < v_end; v += kThreads) {
+        float acc[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) acc[q] = 0.0f;
+        const int64_t off = static_cast<int64_t>(v) * 16;
+        for (int m0 = 0; m0 < n; m0 += kBatch) {
+            uint4 buf[kBatch];
+#pragma unroll
+            for (int j = 0; j < kBatch; ++j)
+                if (m0 + j < n) buf[j] = ld_stream_v4(p.y + static_cast<int64_t>(s_rows[m0 + j]) * row_bytes + off);
+#pragma unroll
+            for (int j = 0; j < kBatch; ++j) {
+                if (m0 + j < n) {
+                    const uint32_t w[4] = {buf[j].x, buf[j].y, buf[j].z, buf[j].w};
+                    if (kWeighted) {
+                        const float cf = s_coef[m0 + j];
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            acc[2 * q] = fmaf(cf, __uint_as_float(w[q] << 16), acc[2 * q]);
+                            acc[2 * q + 1] = fmaf(cf, __uint_as_float(w[q] & 0xffff0000u), acc[2 * q + 1]);
+                        }
+                    } else {
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            acc[2 * q] += __uint_as_float(w[q] << 16);
+                            acc[2 * q + 1] += __uint_as_float(w[q] & 0xffff0000u);
+                        }
+                    }
+                }
+            }
+        }
+        uint4 o;
+        uint32_t* ow = reinterpret_cast<uint32_t*>(&o);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const __nv_bfloat162 h = __floats2bfloat162_rn(acc[2 * q], acc[2 * q + 1]);
+            ow[q] = *reinterpret_cast<const uint32_t*>(&h);
+        }
+        st_v4(p.out + static_cast<int64_t>(t) * row_bytes + off, o);
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_combine(CombineParams p, bool weighted, cudaStream_t stream) {
+    const DeviceInfo& di = device_info();
+    const int n_vec = p.H / 8;
+    // Pieces of up to 2 vectors per thread; more pieces when there are few tokens.
+    int chunks = (n_vec + 2 * kThreads - 1) / (2 * kThreads);
+    const int want_items = 4 * di.num_sms;
+    if (p.T > 0 && static_cast<int64_t>(p.T) * chunks < want_items) {
+        const int more = (want_items + p.T - 1) / p.T;
+        const int max_chunks = (n_vec + 31) / 32;
+        chunks = more < max_chunks ? more : max_chunks;
+        if (chunks < 1) chunks = 1;
+    }
+    int chunk_vecs = (n_vec + chunks - 1) / chunks;
+    chunks = (n_vec + chunk_vecs - 1) / chunk_vecs;
+    p.chunks = chunks;
+    p.chunk_vecs = chunk_vecs;
+    const int64_t grid = static_cast<int64_t>(p.T) * chunks;
+    if (grid < 1) return cudaSuccess;
+    if (weighted)
+        combine_kernel<true><<<static_cast<unsigned>(grid), kThreads, 0, stream>>>(p);
+    else
+        combine_kernel<false><<<static_cast<unsigned>(grid), kThreads, 0, stream>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace epg

@@ -1,0 +1,316 @@
+// Dispatch: scatter each token row once per destination rank into the
+// rank-contiguous receive rows, with the token's top-k indices remapped to
+// the receiving rank's local experts, its weights and its source index
+// ("DeepEP Symmetric Memory" sections 6.1 and 9.2; "DeepEP V2 ElasticBuffer
+// architecture", TokenLayout fragment).
+//
+// bf16 path (pure copy, HBM-bound, writes ~n(t) times the reads):
+//   persistent CTAs of 4 warps.  Warp 0 drives the bulk-copy engine: a ring
+//   of kStages shared-memory slots, each filled by one cp.async.bulk
+//   global->shared load of a token row (or a piece of it) that completes on an
+//   mbarrier; once it lands, the lanes that own a destination rank each issue
+//   one cp.async.bulk shared->global store of the slot, so a row is read from
+//   HBM once and written n(t) times without passing through registers.  A slot
+//   is refilled when the bulk group that reads it has finished reading.
+//   Warps 1-3 write the per-row metadata (remapped top-k, weights, source).
+//
+// FP8 path: one CTA per (token, piece of 128-channel blocks); each half-warp
+//   owns one 128-channel block, loads it with 16-byte vectors, takes amax by
+//   shuffles, scales with IEEE divides and converts with cvt.rn.satfinite
+//   e4m3x2, then stores the 8-byte code vectors and the scale to every
+//   destination row.
+#include "ep_internal.cuh"
+
+namespace epg {
+namespace {
+
+constexpr int kBf16Threads = 128;
+constexpr int kStages = 4;
+constexpr int kStoreDepth = 2;
+
+// Metadata of token t for every rank that receives it (one warp).
+__device__ __forceinline__ void write_metadata(const DispatchParams& p, int t, int lane,
+                                               bool& cap_bad) {
+    const int K = p.K;
+    const int64_t e_l = lane < K ? p.topk_idx[static_cast<int64_t>(t) * K + lane] : -1;
+    const float w_l =
+        (lane < K && p.recv_topk_weights) ? p.topk_weights[static_cast<int64_t>(t) * K + lane] : 0.0f;
+    for (int rb = 0; rb < p.R; rb += 32) {
+        const int r = rb + lane;
+        const int d = r < p.R ? p.dst_row[static_cast<int64_t>(t) * p.R + r] : -1;
+        const bool ok = d >= 0 && d < p.capacity;
+        if (d >= p.capacity) cap_bad = true;
+        unsigned m = __ballot_sync(0xffffffffu, ok);
+        while (m) {
+            const int src = __ffs(m) - 1;
+            m &= m - 1;
+            const int64_t dd = __shfl_sync(0xffffffffu, d, src);
+            const int rr = rb + src;
+            if (lane < K) {
+                const bool on = e_l >= 0 && e_l < p.E && static_cast<int>(e_l) / p.experts_per_rank == rr;
+                if (p.recv_topk_idx)
+                    p.recv_topk_idx[dd * K + lane] =
+                        on ? static_cast<int32_t>(e_l) - rr * p.experts_per_rank : -1;
+                if (p.recv_topk_weights) p.recv_topk_weights[dd * K + lane] = on ? w_l : 0.0f;
+            }
+            if (lane == 0 && p.recv_src_idx) p.recv_src_idx[dd] = t;
+        }
+    }
+}
+
+__global__ void __launch_bounds__(kBf16Threads) dispatch_bf16_kernel(const DispatchParams p) {
+    extern __shared__ __align__(128) uint8_t smem[];
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem);
+    uint8_t* stage = smem + 128;
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int64_t num_items = static_cast<int64_t>(p.T) * p.chunks;
+    const int64_t first = blockIdx.x;
+    const int64_t stride = gridDim.x;
+    const int64_t my_n = first < num_items ? (num_items - first + stride - 1) / stride : 0;
+    const uint32_t row_bytes = static_cast<uint32_t>(p.H) * 2u;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            for (int s = 0; s < kStages; ++s) mbar_init(&bars[s], 1);
+            fence_mbar_init();
+        }
+        __syncwarp();
+        int64_t issued = 0;  // lane 0 only
+        auto issue = [&](int64_t i) {
+            const int64_t it = first + i * stride;
+            const int64_t t = it / p.chunks;
+            const uint32_t off = static_cast<uint32_t>(it - t * p.chunks) * p.chunk_bytes;
+            const uint32_t bytes = min(p.chunk_bytes, row_bytes - off);
+            const int slot = static_cast<int>(i % kStages);
+            mbar_arrive_expect_tx(&bars[slot], bytes);
+            bulk_load(stage + static_cast<size_t>(slot) * p.chunk_bytes, p.x + t * row_bytes + off,
+                      bytes, &bars[slot]);
+        };
+        if (lane == 0) {
+            for (; issued < kStages && issued < my_n; ++issued) issue(issued);
+        }
+        bool ok = true;
+        bool cap_bad = false;
+        int64_t i = 0;
+        for (; i < my_n; ++i) {
+            const int slot = static_cast<int>(i % kStages);
+            const int64_t it = first + i * stride;
+            const int64_t t = it / p.chunks;
+            const uint32_t off = static_cast<uint32_t>(it - t * p.chunks) * p.chunk_bytes;
+            const uint32_t bytes = min(p.chunk_bytes, row_bytes - off);
+            const bool landed = mbar_wait_bounded(&bars[slot], static_cast<uint32_t>((i / kStages) & 1));
+            if (!__all_sync(0xffffffffu, landed)) {
+                ok = false;
+                break;
+            }
+            const uint8_t* src = stage + static_cast<size_t>(slot) * p.chunk_bytes;
+            for (int rb = 0; rb < p.R; rb += 32) {
+                const int r = rb + lane;
+                const int d = r < p.R ? p.dst_row[t * p.R + r] : -1;
+                if (d >= 0) {
+                    if (d < p.capacity)
+                        bulk_store(p.recv_x + static_cast<int64_t>(d) * row_bytes + off, src, bytes);
+                    else
+                        cap_bad = true;
+                }
+            }
+            bulk_commit();
+            bulk_wait_read<kStoreDepth - 1>();
+            __syncwarp();
+            const int64_t j = i - (kStoreDepth - 1);
+            if (lane == 0 && j >= 0 && j + kStages < my_n) {
+                issue(j + kStages);
+                ++issued;
+            }
+        }
+        bulk_wait_all<0>();
+        if (!ok) {
+            // Drain the loads still in flight (bounded) before shared memory is released.
+            if (lane == 0) {
+                for (int64_t k = i; k < issued; ++k)
+                    mbar_wait_bounded(&bars[k % kStages], static_cast<uint32_t>((k / kStages) & 1));
+                atomicOr(p.status, EP_ERR_TIMEOUT);
+            }
+        }
+        if (__any_sync(0xffffffffu, cap_bad) && lane == 0) atomicOr(p.status, EP_ERR_CAPACITY);
+    } else {
+        // Metadata: tokens of this CTA (piece 0 of each), round-robin over warps 1..3.
+        const int mw = warp - 1;
+        const int n_mw = kBf16Threads / 32 - 1;
+        bool cap_bad = false;
+        int64_t count = 0;
+        for (int64_t i = 0; i < my_n; ++i) {
+            const int64_t it = first + i * stride;
+            if (it % p.chunks != 0) continue;
+            if ((count++ % n_mw) != mw) continue;
+            write_metadata(p, static_cast<int>(it / p.chunks), lane, cap_bad);
+        }
+        (void)cap_bad;  // the copy warp reports capacity overflows
+    }
+}
+
+__device__ __forceinline__ uint32_t pack_e4m3x4(float a, float b, float c, float d) {
+    uint16_t lo, hi;
+    // cvt ... d, x, y puts x in the upper byte and y in the lower byte.
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(lo) : "f"(b), "f"(a));
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(hi) : "f"(d), "f"(c));
+    return static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
+}
+
+constexpr int kFp8Threads = 256;
+
+__global__ void __launch_bounds__(kFp8Threads) dispatch_fp8_kernel(const DispatchParams p) {
+    __shared__ int s_rows[EP_MAX_TOPK];
+    __shared__ int s_n;
+    const int64_t it = blockIdx.x;
+    const int t = static_cast<int>(it / p.chunks);
+    const int c = static_cast<int>(it - static_cast<int64_t>(t) * p.chunks);
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    if (warp == 0) {
+        int n = 0;
+        bool cap_bad = false;
+        for (int rb = 0; rb < p.R; rb += 32) {
+            const int r = rb + lane;
+            const int d = r < p.R ? p.dst_row[static_cast<int64_t>(t) * p.R + r] : -1;
+            const bool ok = d >= 0 && d < p.capacity;
+            if (d >= p.capacity) cap_bad = true;
+            const unsigned m = __ballot_sync(0xffffffffu, ok);
+            const int pos = n + __popc(m & ((1u << lane) - 1u));
+            // A layout from ep_get_layout has at most K <= 32 ranks per token;
+            // a foreign dst_row with more is cut off and flagged.
+            if (ok && pos < EP_MAX_TOPK) s_rows[pos] = d;
+            n += __popc(m);
+        }
+        if (n > EP_MAX_TOPK) {
+            if (lane == 0) atomicOr(p.status, EP_ERR_INVALID_INDEX);
+            n = EP_MAX_TOPK;
+        }
+        if (lane == 0) s_n = n;
+        if (__any_sync(0xffffffffu, cap_bad) && lane == 0 && c == 0) atomicOr(p.status, EP_ERR_CAPACITY);
+    } else if (warp == 1 && c == 0) {
+        bool cap_bad = false;
+        write_metadata(p, t, lane, cap_bad);
+    }
+    __syncthreads();
+
+    const int n = s_n;
+    const int nb = p.H / 128;
+    const int b_begin = c * p.chunk_blocks;
+    const int b_end = min(nb, b_begin + p.chunk_blocks);
+    const int half = lane >> 4;
+    const int sub = lane & 15;
+    const uint8_t* xrow = p.x + static_cast<int64_t>(t) * p.H * 2;
+    for (int b0 = b_begin + 2 * warp; b0 < b_end; b0 += 2 * (kFp8Threads / 32)) {
+        const int b = b0 + half;
+        const bool valid = b < b_end;
+        uint4 v = make_uint4(0, 0, 0, 0);
+        if (valid) v = ld_stream_v4(xrow + static_cast<size_t>(b) * 256 + sub * 16);
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+        float f[8];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            f[2 * q] = __uint_as_float(w[q] << 16);
+            f[2 * q + 1] = __uint_as_float(w[q] & 0xffff0000u);
+        }
+        float amax = 0.0f;
+#pragma unroll
+        for (int q = 0; q < 8; ++q) amax = fmaxf(amax, fabsf(f[q]));
+#pragma unroll
+        for (int o = 8; o >= 1; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+        float sf = 1.0f, mult = 0.0f;
+        if (amax > 0.0f) {
+            sf = __fdiv_rn(amax, 448.0f);
+            mult = __fdiv_rn(448.0f, amax);
+        }
+        float g[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) g[q] = __fmul_rn(f[q], mult);
+        uint2 code;
+        code.x = pack_e4m3x4(g[0], g[1], g[2], g[3]);
+        code.y = pack_e4m3x4(g[4], g[5], g[6], g[7]);
+        if (valid) {
+            for (int m = 0; m < n; ++m) {
+                const int64_t d = s_rows[m];
+                *reinterpret_cast<uint2*>(p.recv_x + d * p.H + static_cast<int64_t>(b) * 128 + sub * 8) = code;
+                if (sub == 0 && p.recv_sf) {
+                    const int64_t si = p.sf_col_major ? static_cast<int64_t>(b) * p.sf_stride + d
+                                                      : d * nb + b;
+                    p.recv_sf[si] = sf;
+                }
+            }
+        }
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_dispatch_bf16(DispatchParams p, cudaStream_t stream) {
+    const DeviceInfo& di = device_info();
+    const uint32_t row_bytes = static_cast<uint32_t>(p.H) * 2u;
+    // Pieces: at most 16 KB each; more pieces when there are few tokens so
+    // that every SM gets work.
+    int chunks = static_cast<int>((row_bytes + 16383u) / 16384u);
+    const int want_items = 2 * di.num_sms;
+    if (p.T > 0 && static_cast<int64_t>(p.T) * chunks < want_items) {
+        const int more = (want_items + p.T - 1) / p.T;
+        const int max_chunks = static_cast<int>(row_bytes / 1024u) > 0 ? static_cast<int>(row_bytes / 1024u) : 1;
+        chunks = more < max_chunks ? more : max_chunks;
+        if (chunks < 1) chunks = 1;
+    }
+    uint32_t chunk_bytes = (row_bytes + chunks - 1) / chunks;
+    chunk_bytes = (chunk_bytes + 15u) / 16u * 16u;
+    chunks = static_cast<int>((row_bytes + chunk_bytes - 1) / chunk_bytes);
+    p.chunks = chunks;
+    p.chunk_bytes = chunk_bytes;
+    const size_t smem = 128 + static_cast<size_t>(kStages) * chunk_bytes;
+
+    static thread_local int configured_device = -1;
+    static thread_local int blocks_per_sm = 1;
+    static thread_local size_t configured_smem = 0;
+    if (configured_device != di.device || configured_smem != smem) {
+        cudaError_t e = cudaFuncSetAttribute(dispatch_bf16_kernel,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             static_cast<int>(smem));
+        if (e != cudaSuccess) return e;
+        int nb = 0;
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, dispatch_bf16_kernel, kBf16Threads, smem);
+        if (e != cudaSuccess) return e;
+        blocks_per_sm = nb > 0 ? nb : 1;
+        configured_device = di.device;
+        configured_smem = smem;
+    }
+    const int64_t num_items = static_cast<int64_t>(p.T) * chunks;
+    int64_t grid = static_cast<int64_t>(di.num_sms) * blocks_per_sm;
+    if (grid > num_items) grid = num_items;
+    if (grid < 1) return cudaSuccess;
+    dispatch_bf16_kernel<<<static_cast<unsigned>(grid), kBf16Threads, smem, stream>>>(p);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_dispatch_fp8(DispatchParams p, cudaStream_t stream) {
+    const DeviceInfo& di = device_info();
+    const int nb = p.H / 128;
+    // One CTA per (token, piece); pieces of up to 16 blocks (2048 channels),
+    // split further when there are few tokens.
+    int chunks = (nb + 15) / 16;
+    const int want_items = 4 * di.num_sms;
+    if (p.T > 0 && static_cast<int64_t>(p.T) * chunks < want_items) {
+        const int more = (want_items + p.T - 1) / p.T;
+        const int max_chunks = (nb + 1) / 2;  // keep >= 2 blocks (one warp) per piece
+        chunks = more < max_chunks ? more : max_chunks;
+        if (chunks < 1) chunks = 1;
+    }
+    int chunk_blocks = (nb + chunks - 1) / chunks;
+    chunks = (nb + chunk_blocks - 1) / chunk_blocks;
+    p.chunks = chunks;
+    p.chunk_blocks = chunk_blocks;
+    const int64_t grid = static_cast<int64_t>(p.T) * chunks;
+    if (grid < 1) return cudaSuccess;
+    dispatch_fp8_kernel<<<static_cast<unsigned>(grid), kFp8Threads, 0, stream>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace epg

@@ -1,0 +1,213 @@
+// Internal declarations shared by the CUDA translation units of libep_get.so:
+// kernel parameter blocks, launchers, and thin inline-PTX wrappers for the
+// Blackwell bulk-copy engine (cp.async.bulk + mbarrier) and streaming loads.
+#pragma once
+
+#include <cstdint>
+#include <cstddef>
+#include <cuda_runtime.h>
+
+#include "../../include/ep_get.h"
+
+namespace epg {
+
+// ---------------------------------------------------------------------------
+// Parameter blocks
+// ---------------------------------------------------------------------------
+
+constexpr int kTileTokens = 256;               // tokens per layout tile (one per thread)
+constexpr int kTileWords = kTileTokens / 32;   // 32-bit membership words per rank per tile
+
+struct LayoutParams {
+    const int64_t* topk_idx;
+    int T, K, E, R, experts_per_rank, ranks_per_node, num_nodes, alignment, num_tiles;
+    int32_t* num_tokens_per_rank;
+    int32_t* num_tokens_per_node;
+    int32_t* num_tokens_per_expert;
+    uint8_t* is_token_in_rank;
+    int32_t* rank_offset;
+    int32_t* expert_offset;
+    int32_t* dst_row;
+    int32_t* src_dst_count;
+    // workspace
+    int32_t* ws_rank;      // [R][num_tiles]: tile counts, then exclusive tile prefix
+    int32_t* ws_expert;    // [E][num_tiles]
+    int32_t* ws_node;      // [num_nodes][num_tiles]
+    uint32_t* ws_bitmap;   // [num_tiles][R][kTileWords]
+    int32_t* status;
+};
+
+struct DispatchParams {
+    const uint8_t* x;
+    const int64_t* topk_idx;
+    const float* topk_weights;
+    const int32_t* dst_row;
+    int T, H, K, E, R, experts_per_rank;
+    int64_t capacity;
+    uint8_t* recv_x;
+    float* recv_sf;
+    int sf_col_major;
+    int64_t sf_stride;
+    int32_t* recv_topk_idx;
+    float* recv_topk_weights;
+    int32_t* recv_src_idx;
+    int32_t* status;
+    // work split: each token row is cut into `chunks` pieces
+    int chunks;
+    uint32_t chunk_bytes;   // bf16 path: bytes per piece (multiple of 16)
+    int chunk_blocks;       // fp8 path: 128-channel blocks per piece
+};
+
+struct CombineParams {
+    const uint8_t* y;
+    int64_t num_y_rows;
+    const int64_t* topk_idx;
+    const float* topk_weights;
+    const int32_t* dst_row;
+    int T, H, K, E, R, experts_per_rank;
+    uint8_t* out;
+    int32_t* status;
+    int chunks;             // pieces per token row
+    int chunk_vecs;         // 16-byte vectors per piece
+};
+
+struct DeviceInfo {
+    int device;
+    int num_sms;
+    int max_smem_optin;
+};
+
+// Cached per-device properties (host).
+const DeviceInfo& device_info();
+
+// Launchers (host).  Each returns cudaSuccess or the launch error.
+cudaError_t launch_layout(const LayoutParams& p, cudaStream_t stream);
+cudaError_t launch_dispatch_bf16(DispatchParams p, cudaStream_t stream);
+cudaError_t launch_dispatch_fp8(DispatchParams p, cudaStream_t stream);
+cudaError_t launch_combine(CombineParams p, bool weighted, cudaStream_t stream);
+
+// Workspace carve-up shared by the size query and the launcher.
+struct LayoutWorkspace {
+    size_t off_rank, off_expert, off_node, off_bitmap, total;
+};
+LayoutWorkspace layout_workspace(int T, int E, int R, int num_nodes);
+
+// ---------------------------------------------------------------------------
+// Device helpers
+// ---------------------------------------------------------------------------
+
+// A bounded wait gives up after this many nanoseconds of %globaltimer.
+constexpr uint64_t kWaitTimeoutNs = 2000000000ull;
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint64_t global_timer_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count)
+                 : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)),
+                 "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_addr(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Wait for the phase with the given parity to complete; false after the
+// timeout (the caller records EP_ERR_TIMEOUT and winds down).
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_timer_ns();
+    for (uint32_t i = 1; i < (1u << 30); ++i) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((i & 31u) == 0 && global_timer_ns() - t0 > kWaitTimeoutNs) return false;
+    }
+    return false;
+}
+
+// Bulk copy global -> shared; completion is signalled on `bar` as tx bytes.
+__device__ __forceinline__ void bulk_load(void* dst_smem, const void* src, uint32_t bytes,
+                                          uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+            "r"(smem_addr(dst_smem)),
+        "l"(src), "r"(bytes), "r"(smem_addr(bar))
+        : "memory");
+}
+
+// Bulk copy shared -> global, tracked by the issuing thread's bulk groups.
+__device__ __forceinline__ void bulk_store(void* dst, const void* src_smem, uint32_t bytes) {
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst),
+                 "r"(smem_addr(src_smem)), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void bulk_commit() {
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+
+// Wait until at most N of this thread's bulk groups are still reading smem.
+template <int N>
+__device__ __forceinline__ void bulk_wait_read() {
+    asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+
+// Wait until at most N of this thread's bulk groups are still in flight.
+template <int N>
+__device__ __forceinline__ void bulk_wait_all() {
+    asm volatile("cp.async.bulk.wait_group %0;" ::"n"(N) : "memory");
+}
+
+// 16-byte read-only streaming load that does not allocate in L1.
+__device__ __forceinline__ uint4 ld_stream_v4(const void* p) {
+    uint4 v;
+    asm("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+        : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+        : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ void st_v4(void* p, uint4 v) {
+    asm volatile("st.global.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z),
+                 "r"(v.w)
+                 : "memory");
+}
+
+__device__ __forceinline__ int warp_inclusive_scan(int v) {
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        int n = __shfl_up_sync(0xffffffffu, v, o);
+        if (lane >= o) v += n;
+    }
+    return v;
+}
+
+}  // namespace epg

@@ -1,0 +1,194 @@
+/*
+ * ep_get.h -- C ABI of the GB300 MoE token dispatch / combine library
+ * (libep_get.so, CUDA kernels for sm_103a).
+ *
+ * The hot path is routing layout -> dispatch -> combine for R expert-parallel
+ * ranks that are logical partitions of ONE GPU's memory: a "rank" is a
+ * contiguous block of E/R experts and a contiguous block of rows in the
+ * receive buffer.  There is no traffic between GPUs.
+ *
+ * Sources (page title, then section or code fragment):
+ *  - "DeepEP Symmetric Memory" architecture analysis, section 6.1: the
+ *    dispatch launch carries per-rank and per-expert prefix sums of receive
+ *    counts, a destination slot index per token, expert_alignment, FP8 scale
+ *    factor packs and strides, topk_idx and topk_weights;
+ *    section 7.3: the host learns the receive count per rank and per local
+ *    expert after dispatch; section 9.2: dispatch(x, topk_idx, topk_weights,
+ *    num_experts) returns recv_x, recv_topk_idx, recv_topk_weights and a
+ *    handle, and combine(x, handle, topk_weights) returns the combined rows.
+ *  - "DeepEP V2 ElasticBuffer architecture", TokenLayout fragment: a received
+ *    token carries its hidden row, its scale factors, its top-k indices
+ *    (4 bytes each), its top-k weights (4 bytes each) and its source token
+ *    index (4 bytes); limits fragment: at most 1024 ranks, 2048 experts and
+ *    256 experts per rank.
+ *
+ * Conventions shared by every entry point:
+ *  - All array arguments are DEVICE pointers owned by the caller; they must be
+ *    16-byte aligned.  The library allocates nothing and keeps no state
+ *    between calls other than per-device kernel attributes.
+ *  - Every call is asynchronous on `cuda_stream` (a cudaStream_t; NULL = the
+ *    legacy default stream).  The caller orders streams.
+ *  - Errors a host check can see (null or misaligned pointers, sizes out of
+ *    range, unsupported shapes) are returned before anything is launched.
+ *  - Errors only the device can see are OR-ed into the caller's device word
+ *    `*d_status` (int32, zero it before the first call); the offending entry
+ *    or row is skipped and every other result is still correct.  Read it after
+ *    the stream has synchronised.  Nothing ever traps.
+ *  - A return of EP_ERR_CUDA means a launch failed; cudaGetLastError() has
+ *    the CUDA error.
+ *
+ * Notation: T tokens (all source ranks together), H hidden channels, K top-k
+ * slots per token, E experts, R ranks, E_l = E/R experts per rank; expert e
+ * lives on rank e / E_l.  Token t's source rank is t / (T/R) when R divides
+ * T.  n(t) is the number of distinct ranks among t's valid experts and
+ * N = sum_t n(t) is the number of received rows.
+ */
+#ifndef EP_GET_H
+#define EP_GET_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Status bits (returned and/or OR-ed into *d_status). */
+typedef int32_t ep_status_t;
+#define EP_OK                0
+#define EP_ERR_INVALID_ARG   1   /* host: bad pointer, size or alignment        */
+#define EP_ERR_UNSUPPORTED   2   /* host: shape beyond the limits below         */
+#define EP_ERR_INVALID_INDEX 4   /* device: a topk_idx entry outside [-1, E)    */
+#define EP_ERR_CAPACITY      8   /* device: a row index >= the receive capacity */
+#define EP_ERR_TIMEOUT       16  /* device: a bounded wait gave up              */
+#define EP_ERR_CUDA          32  /* host: a CUDA launch failed                  */
+
+/* Payload types of the receive buffer. */
+#define EP_BF16      0
+#define EP_FP8_E4M3  1
+
+/* Limits ("DeepEP V2 ElasticBuffer architecture", limits fragment), plus the
+ * top-k width this library supports. */
+#define EP_MAX_RANKS            1024
+#define EP_MAX_EXPERTS          2048
+#define EP_MAX_EXPERTS_PER_RANK 256
+#define EP_MAX_TOPK             32
+
+/*
+ * The routing layout: the dispatch "handle".  All members are device pointers
+ * owned by the caller.  Filled by ep_get_layout, read by ep_dispatch and
+ * ep_combine; one layout serves any number of dispatch/combine calls (the
+ * pages' cached mode).
+ */
+typedef struct ep_layout {
+    int32_t* num_tokens_per_rank;   /* [R]   tokens received by each rank                 */
+    int32_t* num_tokens_per_node;   /* [R/ranks_per_node] tokens per node group, or NULL  */
+    int32_t* num_tokens_per_expert; /* [E]   valid top-k entries naming each expert       */
+    uint8_t* is_token_in_rank;      /* [T,R] 1 if any valid expert of t is on r, else 0   */
+    int32_t* rank_offset;           /* [R+1] exclusive prefix of num_tokens_per_rank;
+                                             rank_offset[R] = N                          */
+    int32_t* expert_offset;         /* [E+1] exclusive prefix of num_tokens_per_expert,
+                                             each rounded up to expert_alignment         */
+    int32_t* dst_row;               /* [T,R] receive row of (t, r) or -1; rows of rank r
+                                             are rank_offset[r] + 0, 1, ... in ascending t */
+    int32_t* src_dst_count;         /* [R,R] tokens of source rank s received by rank r,
+                                             or NULL; needs R | T                        */
+} ep_layout_t;
+
+/* Bytes of device workspace ep_get_layout needs for these sizes (>= 16). */
+size_t ep_layout_workspace_bytes(int num_tokens, int num_topk, int num_experts, int num_ranks,
+                                 int ranks_per_node);
+
+/* An upper bound on N: num_tokens * min(num_topk, num_ranks).  A receive
+ * buffer of this many rows never overflows ("DeepEP V2 ElasticBuffer
+ * architecture", calculate_buffer_size fragment: size buffers for the worst
+ * case so that no host wait is needed before dispatch). */
+int64_t ep_recv_capacity_bound(int num_tokens, int num_topk, int num_ranks);
+
+/*
+ * Routing layout ("DeepEP Symmetric Memory" sections 6.1 and 7.3).
+ *
+ * topk_idx        int64 [T,K]: expert of each top-k slot, -1 = masked.  Entries
+ *                 outside [-1, E) set EP_ERR_INVALID_INDEX and are skipped.
+ *                 A repeated expert counts once per entry in
+ *                 num_tokens_per_expert and once for its rank.
+ * ranks_per_node  0 = no node counts; else must divide R, and when
+ *                 out->num_tokens_per_node is non-NULL it receives, per group of
+ *                 ranks_per_node consecutive ranks, the tokens with any expert
+ *                 in that group.
+ * expert_alignment >= 1; only expert_offset uses it.
+ * out             the layout arrays (num_tokens_per_node and src_dst_count may
+ *                 be NULL; src_dst_count non-NULL needs R | T).
+ * workspace       device scratch of ws_bytes >= ep_layout_workspace_bytes(...);
+ *                 its contents need no initialisation and are garbage after.
+ * Results depend only on topk_idx (no atomics decide any order).
+ */
+ep_status_t ep_get_layout(const int64_t* topk_idx, int num_tokens, int num_topk, int num_experts,
+                          int num_ranks, int ranks_per_node, int expert_alignment,
+                          const ep_layout_t* out, void* workspace, size_t ws_bytes,
+                          int32_t* d_status, void* cuda_stream);
+
+/*
+ * Dispatch ("DeepEP Symmetric Memory" sections 6.1 and 9.2; "DeepEP V2
+ * ElasticBuffer architecture", TokenLayout fragment).  For every token t and
+ * rank r with dst_row[t,r] = d >= 0:
+ *   recv_x[d]               = x[t] (bf16 copy), or its FP8 E4M3 cast;
+ *   recv_sf[d, b]           = FP8 scale of 128-channel block b (FP8 only);
+ *   recv_topk_idx[d, k]     = topk_idx[t,k] - r*E_l if that expert is on r, else -1;
+ *   recv_topk_weights[d, k] = topk_weights[t,k] if that expert is on r, else 0;
+ *   recv_src_idx[d]         = t.
+ * FP8 cast per token and 128-channel block: amax = max |x|; scale
+ * sf = amax/448 and codes e4m3_rne_satfinite(x * (448/amax)), both fp32 IEEE;
+ * an all-zero block has sf = 1 and codes of +-0.
+ *
+ * x                 [T,H] bf16 (any 2-byte payload is copied bit for bit).
+ * topk_idx          int64 [T,K]; topk_weights fp32 [T,K] (may be NULL when
+ *                   recv_topk_weights is NULL).
+ * layout            from ep_get_layout for the same topk_idx (only dst_row is read).
+ * out_dtype         EP_BF16 (H % 8 == 0) or EP_FP8_E4M3 (H % 128 == 0).
+ * recv_capacity     rows allocated in every recv_* array; a row d >= capacity
+ *                   is skipped and sets EP_ERR_CAPACITY.
+ * recv_x            [capacity, H] of 2-byte (bf16) or 1-byte (FP8) elements.
+ * recv_sf           FP8 only: fp32 scales, row-major [capacity, H/128] when
+ *                   sf_col_major == 0, else element (d, b) at b*sf_stride + d
+ *                   with sf_stride = capacity rounded up to a multiple of 4
+ *                   (a column-major layout a following GEMM can load by TMA).
+ * recv_topk_idx     int32 [capacity, K] or NULL; recv_topk_weights fp32
+ *                   [capacity, K] or NULL; recv_src_idx int32 [capacity] or NULL.
+ */
+ep_status_t ep_dispatch(const void* x, const int64_t* topk_idx, const float* topk_weights,
+                        int num_tokens, int hidden, int num_topk, int num_experts, int num_ranks,
+                        const ep_layout_t* layout, int out_dtype, int64_t recv_capacity,
+                        void* recv_x, float* recv_sf, int sf_col_major,
+                        int32_t* recv_topk_idx, float* recv_topk_weights, int32_t* recv_src_idx,
+                        int32_t* d_status, void* cuda_stream);
+
+/*
+ * Combine ("DeepEP Symmetric Memory" section 9.2: combine(x, handle,
+ * topk_weights) -> combined_x).  For every token t:
+ *   out[t] = bf16_rne( sum over r with dst_row[t,r] = d >= 0 of c(t,r) * y[d] )
+ * accumulated in fp32, with c = 1 when topk_weights is NULL (unweighted), else
+ * c(t,r) = sum of topk_weights[t,k] over the k whose expert is on r.  A token
+ * in no rank gets a zero row.
+ *
+ * y           bf16 [num_y_rows, H]: the expert outputs, in the receive rows of
+ *             dispatch; a row d >= num_y_rows is skipped (EP_ERR_CAPACITY).
+ * topk_idx    int64 [T,K]; needed when topk_weights is non-NULL.
+ * out         bf16 [T,H].  H % 8 == 0.
+ */
+ep_status_t ep_combine(const void* y, int64_t num_y_rows, const int64_t* topk_idx,
+                       const float* topk_weights, int num_tokens, int hidden, int num_topk,
+                       int num_experts, int num_ranks, const ep_layout_t* layout, void* out,
+                       int32_t* d_status, void* cuda_stream);
+
+/* Text for a status word (bits joined by '|'); a static string. */
+const char* ep_status_string(int32_t status);
+
+/* ABI version of this header (bumped on any signature change). */
+int ep_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* EP_GET_H */

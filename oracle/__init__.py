@@ -57,6 +57,10 @@ def _load():
     lib.ep_oracle_float_to_bf16.argtypes = [ctypes.c_float]
     lib.ep_oracle_bf16_to_float.restype = ctypes.c_float
     lib.ep_oracle_bf16_to_float.argtypes = [ctypes.c_uint16]
+    for name in ("ep_oracle_e4m3_encode_array", "ep_oracle_e4m3_decode_array",
+                 "ep_oracle_float_to_bf16_array"):
+        getattr(lib, name).restype = None
+        getattr(lib, name).argtypes = [vp, ctypes.c_int64, vp]
     _lib = lib
     return lib
 
@@ -192,21 +196,30 @@ def fp8_cast_row(x_bits_row):
 
 
 def e4m3_encode(values):
+    """binary32 -> E4M3 codes (RNE, saturating), elementwise, flattened."""
     lib = _load()
-    v = np.asarray(values, dtype=np.float32).ravel()
-    return np.array([lib.ep_oracle_e4m3_encode(float(a)) for a in v], np.uint8)
+    v = np.ascontiguousarray(np.asarray(values, dtype=np.float32).ravel())
+    out = np.zeros(v.size, np.uint8)
+    lib.ep_oracle_e4m3_encode_array(_p(v), v.size, _p(out))
+    return out
 
 
 def e4m3_decode(codes):
+    """E4M3 codes -> binary32 values, elementwise, flattened."""
     lib = _load()
-    c = np.asarray(codes, dtype=np.uint8).ravel()
-    return np.array([lib.ep_oracle_e4m3_decode(int(a)) for a in c], np.float32)
+    c = np.ascontiguousarray(np.asarray(codes, dtype=np.uint8).ravel())
+    out = np.zeros(c.size, np.float32)
+    lib.ep_oracle_e4m3_decode_array(_p(c), c.size, _p(out))
+    return out
 
 
 def float_to_bf16(values):
+    """binary32 -> bf16 bit patterns (RNE), elementwise, flattened."""
     lib = _load()
-    v = np.asarray(values, dtype=np.float32).ravel()
-    return np.array([lib.ep_oracle_float_to_bf16(float(a)) for a in v], np.uint16)
+    v = np.ascontiguousarray(np.asarray(values, dtype=np.float32).ravel())
+    out = np.zeros(v.size, np.uint16)
+    lib.ep_oracle_float_to_bf16_array(_p(v), v.size, _p(out))
+    return out
 
 
 def bf16_to_float(bits):

@@ -368,3 +368,22 @@ int ep_oracle_combine(const uint16_t* y, int64_t num_y_rows,
     }
     return status;
 }
+
+/* ------------------------------------------------------------------------ */
+/* Array forms of the element conversions above (test convenience).         */
+/* ------------------------------------------------------------------------ */
+
+void ep_oracle_e4m3_encode_array(const float* v, int64_t n, uint8_t* out)
+{
+    for (int64_t i = 0; i < n; ++i) out[i] = ep_oracle_e4m3_encode(v[i]);
+}
+
+void ep_oracle_e4m3_decode_array(const uint8_t* c, int64_t n, float* out)
+{
+    for (int64_t i = 0; i < n; ++i) out[i] = ep_oracle_e4m3_decode(c[i]);
+}
+
+void ep_oracle_float_to_bf16_array(const float* v, int64_t n, uint16_t* out)
+{
+    for (int64_t i = 0; i < n; ++i) out[i] = ep_oracle_float_to_bf16(v[i]);
+}

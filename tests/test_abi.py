@@ -1,0 +1,124 @@
+"""The C ABI library on a machine without a GPU: it loads, exports every
+function include/ep_get.h declares, and its host-side checks reject bad
+arguments with the documented codes before any CUDA call."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "ep_get.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from combine_ep_get_gb300 import build
+    path = build.build()
+    return ctypes.CDLL(path)
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"^\s*(?:const\s+)?[A-Za-z_][A-Za-z0-9_]*\s*\*?\s*([a-z_][a-z0-9_]*)\s*\(",
+                       text, flags=re.M)
+    return sorted(set(n for n in names if n.startswith("ep_")))
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for n in ("ep_get_layout", "ep_dispatch", "ep_combine", "ep_layout_workspace_bytes",
+              "ep_recv_capacity_bound", "ep_status_string", "ep_abi_version"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for n in declared_functions():
+        assert hasattr(lib, n), n
+
+
+def test_status_strings_and_sizes(lib):
+    lib.ep_status_string.restype = ctypes.c_char_p
+    assert lib.ep_status_string(0) == b"ok"
+    assert lib.ep_status_string(4 | 8) == b"invalid_index|capacity"
+    assert lib.ep_status_string(999) == b"unknown"
+    lib.ep_recv_capacity_bound.restype = ctypes.c_int64
+    assert lib.ep_recv_capacity_bound(4096, 8, 8) == 4096 * 8
+    assert lib.ep_recv_capacity_bound(128, 8, 4) == 512
+    lib.ep_layout_workspace_bytes.restype = ctypes.c_size_t
+    ws = lib.ep_layout_workspace_bytes(4096, 8, 256, 8, 0)
+    tiles = 16
+    assert ws >= 4 * tiles * (8 + 256 + 8 * 8)
+    assert lib.ep_abi_version() == 1
+
+
+def test_host_checks_reject_before_any_launch(lib):
+    """Every call below fails a host check, so no CUDA call is made."""
+    from combine_ep_get_gb300 import binding as B
+    L = B.ep_layout_t()
+    vp = ctypes.c_void_p
+    st = vp(16)            # a stand-in device address; never dereferenced on these paths
+    # layout: null out / status, bad shapes, limits
+    f = lib.ep_get_layout
+    f.restype = ctypes.c_int32
+    f.argtypes = [vp, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                  ctypes.c_int, ctypes.POINTER(B.ep_layout_t), vp, ctypes.c_size_t, vp, vp]
+    assert f(None, 10, 8, 256, 8, 0, 1, None, None, 0, st, None) == B.EP_ERR_INVALID_ARG
+    assert f(None, 10, 8, 256, 7, 0, 1, ctypes.byref(L), None, 0, st, None) == B.EP_ERR_INVALID_ARG
+    assert f(None, 10, 8, 4096, 8, 0, 1, ctypes.byref(L), None, 0, st, None) == B.EP_ERR_UNSUPPORTED
+    assert f(None, 10, 33, 256, 8, 0, 1, ctypes.byref(L), None, 0, st, None) == B.EP_ERR_UNSUPPORTED
+    assert f(None, 10, 8, 2048, 4, 0, 1, ctypes.byref(L), None, 0, st, None) == B.EP_ERR_UNSUPPORTED
+    assert f(None, -1, 8, 256, 8, 0, 1, ctypes.byref(L), None, 0, st, None) == B.EP_ERR_INVALID_ARG
+    assert f(None, 10, 8, 256, 8, 3, 1, ctypes.byref(L), None, 0, st, None) == B.EP_ERR_INVALID_ARG
+    assert f(None, 10, 8, 256, 8, 0, 0, ctypes.byref(L), None, 0, st, None) == B.EP_ERR_INVALID_ARG
+    # layout: arrays missing / misaligned
+    L2 = B.ep_layout_t(16, None, 32, 48, 64, 80, 96, None)
+    assert f(vp(16), 10, 8, 256, 8, 0, 1, ctypes.byref(L2), None, 0, st, None) == B.EP_ERR_INVALID_ARG
+    L3 = B.ep_layout_t(16, None, 32, 48, 64, 80, 97, None)      # dst_row misaligned
+    assert f(vp(16), 10, 8, 256, 8, 0, 1, ctypes.byref(L3), vp(256), 1 << 20, st, None) == B.EP_ERR_INVALID_ARG
+    # workspace too small
+    assert f(vp(16), 10, 8, 256, 8, 0, 1, ctypes.byref(L2), vp(256), 8, st, None) == B.EP_ERR_INVALID_ARG
+    # src_dst_count needs R | T
+    L4 = B.ep_layout_t(16, None, 32, 48, 64, 80, 96, 112)
+    assert f(vp(16), 10, 8, 256, 8, 0, 1, ctypes.byref(L4), vp(256), 1 << 20, st, None) == B.EP_ERR_INVALID_ARG
+    # dispatch
+    d = lib.ep_dispatch
+    d.restype = ctypes.c_int32
+    d.argtypes = [vp, vp, vp, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                  ctypes.POINTER(B.ep_layout_t), ctypes.c_int, ctypes.c_int64, vp, vp, ctypes.c_int,
+                  vp, vp, vp, vp, vp]
+    args = [vp(16), vp(32), vp(48), 10, 7168, 8, 256, 8, ctypes.byref(L2), B.EP_BF16, 100,
+            vp(64), None, 0, None, None, None, st, None]
+    bad = list(args); bad[4] = 7164                      # H % 8
+    assert d(*bad) == B.EP_ERR_INVALID_ARG
+    bad = list(args); bad[9] = B.EP_FP8_E4M3; bad[4] = 7168 + 64   # H % 128 for FP8
+    assert d(*bad) == B.EP_ERR_INVALID_ARG
+    bad = list(args); bad[9] = B.EP_FP8_E4M3             # FP8 needs recv_sf
+    assert d(*bad) == B.EP_ERR_INVALID_ARG
+    bad = list(args); bad[9] = 7                         # unknown dtype
+    assert d(*bad) == B.EP_ERR_INVALID_ARG
+    bad = list(args); bad[0] = vp(18)                    # x misaligned
+    assert d(*bad) == B.EP_ERR_INVALID_ARG
+    bad = list(args); bad[10] = -1                       # capacity
+    assert d(*bad) == B.EP_ERR_INVALID_ARG
+    bad = list(args); bad[11] = None                     # recv_x missing
+    assert d(*bad) == B.EP_ERR_INVALID_ARG
+    bad = list(args); bad[15] = vp(80); bad[2] = None    # weights out without weights in
+    assert d(*bad) == B.EP_ERR_INVALID_ARG
+    bad = list(args); bad[17] = None                     # status missing
+    assert d(*bad) == B.EP_ERR_INVALID_ARG
+    # combine
+    c = lib.ep_combine
+    c.restype = ctypes.c_int32
+    c.argtypes = [vp, ctypes.c_int64, vp, vp, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                  ctypes.c_int, ctypes.POINTER(B.ep_layout_t), vp, vp, vp]
+    cargs = [vp(16), 100, vp(32), None, 10, 7168, 8, 256, 8, ctypes.byref(L2), vp(64), st, None]
+    bad = list(cargs); bad[5] = 100                      # H % 8
+    assert c(*bad) == B.EP_ERR_INVALID_ARG
+    bad = list(cargs); bad[10] = None                    # out missing
+    assert c(*bad) == B.EP_ERR_INVALID_ARG
+    bad = list(cargs); bad[3] = vp(48); bad[2] = None    # weighted without topk_idx
+    assert c(*bad) == B.EP_ERR_INVALID_ARG
+    bad = list(cargs); bad[0] = None                     # y missing with rows > 0
+    assert c(*bad) == B.EP_ERR_INVALID_ARG

@@ -1,0 +1,147 @@
+"""GPU parity of dispatch against the CPU oracle.
+
+* element by element (payload bytes, scales, remapped top-k, weights, source
+  index) at sizes the oracle finishes in seconds, spanning several tiles and a
+  ragged tail;
+* at the full workload sizes, in the bench's launch configuration: the
+  metadata of every row against the oracle run on a 16-channel stand-in row
+  (metadata does not depend on the payload), the payload of sampled tokens
+  against the oracle's sampled dispatch, and recv_x[d] == x[src[d]] for every
+  row;
+* FP8 (decode workload, full size): codes and scales bit-exact;
+* capacity overflow and invalid ids set the status and leave other rows right.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from combine_ep_get_gb300.inputs import CONFIGS, make_config, make_inputs
+
+pytestmark = pytest.mark.gpu
+
+
+def _run(d, E, R, fp8=False, sf_col_major=False, capacity=None, rpn=0):
+    from gpu_path import run_dispatch, run_layout, to_dev, x_tensor
+    idx = to_dev(d["topk_idx"])
+    w = to_dev(d["topk_weights"])
+    x = x_tensor(d["x_bits"])
+    lay, st = run_layout(idx, E, R, rpn)
+    n = lay.num_recv
+    cap = n if capacity is None else capacity
+    res = run_dispatch(x, idx, w, E, R, lay, cap, fp8=fp8, sf_col_major=sf_col_major)
+    torch.cuda.synchronize()
+    return lay, res, n, x, idx
+
+
+def _host(res, fp8, n):
+    from gpu_path import bf16_bits
+    out = dict(recv_topk_idx=res["recv_topk_idx"][:n].cpu().numpy(),
+               recv_topk_weights=res["recv_topk_weights"][:n].cpu().numpy(),
+               recv_src_idx=res["recv_src_idx"][:n].cpu().numpy())
+    if fp8:
+        out["recv_x"] = res["recv_x"][:n].cpu().numpy()
+    else:
+        out["recv_x"] = bf16_bits(res["recv_x"][:n]).view(np.uint8).reshape(n, -1)
+    return out
+
+
+@pytest.mark.parametrize("T,H,E,K,R,mask", [
+    (128, 256, 16, 4, 4, 0.0),        # the small workload's shape
+    (1000, 7168, 256, 8, 8, 0.0),     # 4 tiles, ragged tail, DeepSeek-V3 row
+    (777, 2048, 64, 6, 16, 0.1),
+    (300, 8, 32, 2, 32, 0.0),         # 16-byte rows
+    (33, 4096, 128, 8, 64, 0.05),     # few tokens: rows split into pieces
+    (1, 7168, 256, 8, 8, 0.0),
+])
+def test_dispatch_bf16_full_compare(T, H, E, K, R, mask):
+    d = make_inputs(T, H, E, K, R, seed=T * 3 + H, mask_frac=mask)
+    lay, res, n, _, _ = _run(d, E, R)
+    assert int(res["status"].item()) == 0
+    g = _host(res, False, n)
+    L = oracle.layout(d["topk_idx"], E, R)
+    o = oracle.dispatch(d["x_bits"], d["topk_idx"], d["topk_weights"], E, R, L.dst_row)
+    for k in ("recv_x", "recv_topk_idx", "recv_topk_weights", "recv_src_idx"):
+        np.testing.assert_array_equal(g[k], o[k], err_msg=k)
+
+
+@pytest.mark.parametrize("name", ["dsv3", "skewed", "large"])
+def test_dispatch_bf16_full_size_sampled(name):
+    d = make_config(name)
+    c = d["cfg"]
+    lay, res, n, x, idx = _run(d, c.E, c.R, rpn=c.ranks_per_node)
+    assert int(res["status"].item()) == 0
+    L = oracle.layout(d["topk_idx"], c.E, c.R)
+    assert n == L.num_recv
+    # metadata of every row: payload-independent, so the oracle runs on 16-channel rows
+    stand_in = np.zeros((c.T, 16), np.uint16)
+    om = oracle.dispatch(stand_in, d["topk_idx"], d["topk_weights"], c.E, c.R, L.dst_row)
+    np.testing.assert_array_equal(res["recv_src_idx"][:n].cpu().numpy(), om["recv_src_idx"])
+    np.testing.assert_array_equal(res["recv_topk_idx"][:n].cpu().numpy(), om["recv_topk_idx"])
+    np.testing.assert_array_equal(res["recv_topk_weights"][:n].cpu().numpy(), om["recv_topk_weights"])
+    # every payload row equals its source row (a property at any size)
+    src = res["recv_src_idx"][:n].long()
+    assert torch.equal(res["recv_x"][:n].view(torch.int16), x.view(torch.int16)[src])
+    # sampled tokens against the oracle's own dispatch of those tokens
+    rng = np.random.Generator(np.random.PCG64(99))
+    toks = np.unique(np.concatenate([[0, c.T - 1], rng.choice(c.T, 48, replace=False)])).astype(np.int32)
+    os_ = oracle.dispatch(d["x_bits"], d["topk_idx"], d["topk_weights"], c.E, c.R, L.dst_row, tokens=toks)
+    rows = torch.from_numpy(os_["rows"].astype(np.int64)).cuda()
+    from gpu_path import bf16_bits
+    got = bf16_bits(res["recv_x"][rows]).view(np.uint8).reshape(len(os_["rows"]), -1)
+    np.testing.assert_array_equal(got, os_["recv_x"])
+
+
+@pytest.mark.parametrize("sf_col_major", [False, True])
+def test_dispatch_fp8_decode_full_size(sf_col_major):
+    d = make_config("decode")
+    c = d["cfg"]
+    lay, res, n, _, _ = _run(d, c.E, c.R, fp8=True, sf_col_major=sf_col_major)
+    assert int(res["status"].item()) == 0
+    g = _host(res, True, n)
+    L = oracle.layout(d["topk_idx"], c.E, c.R)
+    stride = (n + 3) // 4 * 4
+    o = oracle.dispatch(d["x_bits"], d["topk_idx"], d["topk_weights"], c.E, c.R, L.dst_row, fp8=True,
+                        sf_col_major=sf_col_major, sf_stride=stride)
+    for k in ("recv_x", "recv_topk_idx", "recv_topk_weights", "recv_src_idx"):
+        np.testing.assert_array_equal(g[k], o[k], err_msg=k)
+    sf = res["recv_sf"].cpu().numpy()
+    if sf_col_major:
+        nb = c.H // 128
+        got = sf[:nb * stride].reshape(nb, stride)[:, :n]
+        want = o["recv_sf"][:nb * stride].reshape(nb, stride)[:, :n]
+    else:
+        got = sf[:n * (c.H // 128)].reshape(n, -1)
+        want = o["recv_sf"]
+    np.testing.assert_array_equal(got, want)
+
+
+def test_dispatch_fp8_special_blocks():
+    T, H, E, K, R = 300, 1024, 64, 8, 8
+    d = make_inputs(T, H, E, K, R, seed=8)
+    x = d["x_bits"]
+    x[0, :128] = 0                     # all-zero block
+    x[1, 128:256] = 0x8000             # negative zeros
+    x[2, :] = x[2, :] & 0x807F         # tiny values (exponent field 0: subnormal bf16)
+    x[2, :] |= 0x0080                  # smallest normal exponent
+    x[3, 256:384] = 0x4380             # constant 256.0
+    lay, res, n, _, _ = _run(d, E, R, fp8=True)
+    g = _host(res, True, n)
+    L = oracle.layout(d["topk_idx"], E, R)
+    o = oracle.dispatch(x, d["topk_idx"], d["topk_weights"], E, R, L.dst_row, fp8=True)
+    np.testing.assert_array_equal(g["recv_x"], o["recv_x"])
+    sf = res["recv_sf"].cpu().numpy()[:n * (H // 128)].reshape(n, -1)
+    np.testing.assert_array_equal(sf, o["recv_sf"])
+
+
+def test_dispatch_capacity_overflow():
+    T, H, E, K, R = 400, 512, 64, 4, 8
+    d = make_inputs(T, H, E, K, R, seed=12)
+    L = oracle.layout(d["topk_idx"], E, R)
+    cap = L.num_recv - 50
+    lay, res, n, _, _ = _run(d, E, R, capacity=cap)
+    assert int(res["status"].item()) & oracle.EP_ERR_CAPACITY
+    g = _host(res, False, cap)
+    o = oracle.dispatch(d["x_bits"], d["topk_idx"], d["topk_weights"], E, R, L.dst_row, capacity=cap)
+    for k in ("recv_x", "recv_topk_idx", "recv_topk_weights", "recv_src_idx"):
+        np.testing.assert_array_equal(g[k], o[k][:cap], err_msg=k)
