@@ -2,8 +2,8 @@
 
 Tolerance (fp32 accumulation, bf16 output): |gpu - oracle| <= 1e-2 *
 sum_r |c(t,r) * y_r| elementwise, where the oracle's result is the fp64 sum.
-The unweighted identity round trip has a closed form that must hold
-bit-exactly in any summation order: out[t] = bf16(n(t) * x[t]).
+The unweighted identity round trip has a closed form that must hold exactly
+(as values) in any summation order: out[t] = bf16(n(t) * x[t]).
 """
 import numpy as np
 import pytest
@@ -70,7 +70,9 @@ def test_round_trip_identity_closed_form(name):
     assert int(st.item()) == 0 and int(res["status"].item()) == 0
     nt = lay.is_token_in_rank.sum(dim=1, dtype=torch.int32).float()
     want = (x.float() * nt[:, None]).to(torch.bfloat16)
-    assert torch.equal(out.view(torch.int16), want.view(torch.int16))
+    # exact values (bf16 -> fp32 is exact); a sum of -0 terms started from +0 is
+    # +0 while n * (-0) is -0, so compare values, not sign bits of zeros
+    assert torch.equal(out.float(), want.float())
 
 
 @pytest.mark.parametrize("name", ["dsv3", "skewed", "large"])

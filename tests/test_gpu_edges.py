@@ -41,7 +41,7 @@ def test_degenerate_shapes_round_trip(T, H, E, K, R):
     out, st = run_combine(res["recv_x"], idx, None, E, R, lay, T, H)
     nt = L.is_token_in_rank.sum(axis=1)
     want = (x.float() * torch.from_numpy(nt).cuda().float()[:, None]).to(torch.bfloat16)
-    assert torch.equal(out.view(torch.int16), want.view(torch.int16))
+    assert torch.equal(out.float(), want.float())     # exact values; zeros compare unsigned
 
 
 def test_invalid_ids_whole_path():
