@@ -47,6 +47,9 @@ _lib.ep_recv_capacity_bound.argtypes = [_i, _i, _i]
 _lib.ep_get_layout.restype = ctypes.c_int32
 _lib.ep_get_layout.argtypes = [_vp, _i, _i, _i, _i, _i, _i, ctypes.POINTER(ep_layout_t), _vp,
                                ctypes.c_size_t, _vp, _vp]
+_lib.ep_get_layout_static_scratch.restype = ctypes.c_int32
+_lib.ep_get_layout_static_scratch.argtypes = [_vp, _i, _i, _i, _i, _i, _i, ctypes.POINTER(ep_layout_t),
+                                              _vp, _vp]
 _lib.ep_dispatch.restype = ctypes.c_int32
 _lib.ep_dispatch.argtypes = [_vp, _vp, _vp, _i, _i, _i, _i, _i, ctypes.POINTER(ep_layout_t), _i,
                              _i64, _vp, _vp, _i, _vp, _vp, _vp, _vp, _vp]
@@ -131,6 +134,19 @@ def ep_get_layout(topk_idx, num_experts, num_ranks, layout, workspace, d_status,
                               workspace.numel() * workspace.element_size(), _ptr(d_status),
                               _stream(stream))
     return _check(code, "ep_get_layout")
+
+
+def ep_get_layout_static_scratch(topk_idx, num_experts, num_ranks, layout, d_status, ranks_per_node=0,
+                                 expert_alignment=1, stream=None):
+    """ep_get_layout using the library's built-in scratch instead of a caller
+    workspace, for callers that cannot allocate device memory (see the C
+    header for the size limit and the ordering rule)."""
+    T, K = topk_idx.shape
+    assert topk_idx.dtype == torch.int64 and topk_idx.is_contiguous()
+    code = _lib.ep_get_layout_static_scratch(_ptr(topk_idx), T, K, num_experts, num_ranks,
+                                             ranks_per_node, expert_alignment, ctypes.byref(layout.c),
+                                             _ptr(d_status), _stream(stream))
+    return _check(code, "ep_get_layout_static_scratch")
 
 
 def ep_dispatch(x, topk_idx, topk_weights, num_experts, num_ranks, layout, recv_x, recv_topk_idx,

@@ -25,7 +25,8 @@
  * Conventions shared by every entry point:
  *  - All array arguments are DEVICE pointers owned by the caller; they must be
  *    16-byte aligned.  The library allocates nothing and keeps no state
- *    between calls other than per-device kernel attributes.
+ *    between calls other than per-device kernel attributes (and the built-in
+ *    scratch array of ep_get_layout_static_scratch).
  *  - Every call is asynchronous on `cuda_stream` (a cudaStream_t; NULL = the
  *    legacy default stream).  The caller orders streams.
  *  - Errors a host check can see (null or misaligned pointers, sizes out of
@@ -127,6 +128,38 @@ ep_status_t ep_get_layout(const int64_t* topk_idx, int num_tokens, int num_topk,
                           int num_ranks, int ranks_per_node, int expert_alignment,
                           const ep_layout_t* out, void* workspace, size_t ws_bytes,
                           int32_t* d_status, void* cuda_stream);
+
+/* Size of the library's built-in layout scratch (4 MiB). */
+#define EP_LAYOUT_STATIC_SCRATCH_BYTES (4u << 20)
+
+/*
+ * Routing layout without a caller workspace.  The pages have no counterpart:
+ * this is a library convenience.
+ *
+ * For callers that cannot allocate device memory: a plugin that a host
+ * framework hands only its input and output buffers, with no allocator of its
+ * own, or a process whose device memory is fully reserved up front by a
+ * pooling allocator, so that a further cudaMalloc fails or is not allowed.
+ * Same arguments and results as ep_get_layout minus `workspace` / `ws_bytes`:
+ * the scratch is a device array of EP_LAYOUT_STATIC_SCRATCH_BYTES built into
+ * the library, which every GPU that loads the library holds until the process
+ * exits.  The call allocates nothing.
+ *
+ * Limit: returns EP_ERR_UNSUPPORTED, before any launch, when
+ * ep_layout_workspace_bytes(num_tokens, num_topk, num_experts, num_ranks,
+ * ranks_per_node) > EP_LAYOUT_STATIC_SCRATCH_BYTES (for example T=32768,
+ * E=256, R=64 needs about 0.43 MB; T=16384, E=2048, R=1024 about 2.9 MB).
+ * The first call on a device looks up the array's device address (with that
+ * device current) and returns EP_ERR_CUDA if that fails; make that first call
+ * before any stream capture.  All calls share the one array, and every call
+ * overwrites the scratch words it reads, so nothing needs clearing between
+ * calls; but calls whose kernels overlap on the GPU (on unordered streams)
+ * race on it and give wrong layouts: order them.
+ */
+ep_status_t ep_get_layout_static_scratch(const int64_t* topk_idx, int num_tokens, int num_topk,
+                                         int num_experts, int num_ranks, int ranks_per_node,
+                                         int expert_alignment, const ep_layout_t* out,
+                                         int32_t* d_status, void* cuda_stream);
 
 /*
  * Dispatch ("DeepEP Symmetric Memory" sections 6.1 and 9.2; "DeepEP V2
