@@ -33,7 +33,7 @@ struct LayoutParams {
     int32_t* ws_rank;      // [R][num_tiles]: tile counts, then exclusive tile prefix
     int32_t* ws_expert;    // [E][num_tiles]
     int32_t* ws_node;      // [num_nodes][num_tiles]
-    uint32_t* ws_bitmap;   // [num_tiles][R][kTileWords]
+    uint32_t* ws_bitmap;   // [num_tiles][kTileWords][R]
     int32_t* status;
 };
 

@@ -7,8 +7,20 @@
 // expert).  Receive order inside a rank is ascending token index, so every
 // output is a pure function of topk_idx: no atomic decides an order.
 //
-// Three launches over tiles of 256 tokens:
-//   1. count:  per tile, a shared-memory membership bitmap [R][8 words]
+// Main path: ONE launch of one thread-block cluster (up to 16 CTAs of 1024
+// threads, one per SM).  CTA c owns a contiguous token range; it builds the
+// membership bitmaps [words][R] and the expert histogram of its range in
+// shared memory, then after a hardware cluster barrier every CTA reads the
+// other CTAs' per-rank counts through distributed shared memory to get its
+// base row per rank (rank_offset + earlier CTAs), CTA 0 writes the rank counts
+// and offsets and the last CTA the expert / node counts and expert offsets; a
+// second cluster barrier keeps every CTA's shared memory alive until all remote
+// reads are done, then each CTA writes dst_row and is_token_in_rank for its
+// range with 16-byte stores.  No global-memory synchronisation, no spin.
+//
+// Fallback (when a CTA's bitmaps would not fit in shared memory): three
+// launches over tiles of 256 tokens:
+//   1. count:  per tile, a shared-memory membership bitmap [8 words][R]
 //              (bit t of rank r set when token t has an expert on r), built
 //              from coalesced top-k loads with shared atomics; per-tile rank,
 //              expert and node counts go to the workspace, columns by tile.
@@ -18,19 +30,22 @@
 //              dst_row and is_token_in_rank for the tile's contiguous [256,R]
 //              block: base of (rank, tile) + popc of the bitmap below the
 //              token.  Block 0 also writes rank_offset and expert_offset.
+#include <cooperative_groups.h>
+
 #include "ep_internal.cuh"
 
 namespace epg {
 namespace {
 
 constexpr int kThreads = 256;
+constexpr int kUnroll = 4;
 
 __global__ void __launch_bounds__(kThreads) layout_count_kernel(const LayoutParams p) {
     extern __shared__ __align__(16) uint32_t smem[];
     __shared__ int s_bad;
     const int R = p.R;
-    uint32_t* s_bm = smem;                                       // [R][kTileWords]
-    uint32_t* s_bm_node = s_bm + R * kTileWords;                 // [num_nodes][kTileWords]
+    uint32_t* s_bm = smem;                                       // [kTileWords][R]
+    uint32_t* s_bm_node = s_bm + R * kTileWords;                 // [kTileWords][num_nodes]
     int* s_hist = reinterpret_cast<int*>(s_bm_node + p.num_nodes * kTileWords);  // [E]
     const int tile = blockIdx.x;
     const int n_words = R * kTileWords + p.num_nodes * kTileWords + p.E;
@@ -52,16 +67,25 @@ __global__ void __launch_bounds__(kThreads) layout_count_kernel(const LayoutPara
     const int n_entries = nt * p.K;
     const int64_t* src = p.topk_idx + static_cast<int64_t>(t0) * p.K;
     bool bad = false;
-    for (int i = threadIdx.x; i < n_entries; i += kThreads) {
-        const int64_t e = src[i];
-        if (e == -1) continue;
-        if (e < -1 || e >= p.E) { bad = true; continue; }
-        const int tl = i / p.K;
-        const int r = static_cast<int>(e) / p.experts_per_rank;
-        const uint32_t bit = 1u << (tl & 31);
-        atomicAdd(&s_hist[e], 1);
-        atomicOr(&s_bm[r * kTileWords + (tl >> 5)], bit);
-        if (p.num_nodes) atomicOr(&s_bm_node[(r / p.ranks_per_node) * kTileWords + (tl >> 5)], bit);
+    for (int base = 0; base < n_entries; base += kUnroll * kThreads) {
+        int64_t e[kUnroll];
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+            const int i = base + u * kThreads + threadIdx.x;
+            e[u] = i < n_entries ? src[i] : -1;     // all loads in flight before any use
+        }
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+            const int i = base + u * kThreads + threadIdx.x;
+            if (e[u] == -1) continue;
+            if (e[u] < -1 || e[u] >= p.E) { bad = true; continue; }
+            const int tl = i / p.K;
+            const int r = static_cast<int>(e[u]) / p.experts_per_rank;
+            const uint32_t bit = 1u << (tl & 31);
+            atomicAdd(&s_hist[e[u]], 1);
+            atomicOr(&s_bm[(tl >> 5) * R + r], bit);
+            if (p.num_nodes) atomicOr(&s_bm_node[(tl >> 5) * p.num_nodes + r / p.ranks_per_node], bit);
+        }
     }
     if (bad) s_bad = 1;
     __syncthreads();
@@ -71,7 +95,7 @@ __global__ void __launch_bounds__(kThreads) layout_count_kernel(const LayoutPara
     for (int r = threadIdx.x; r < R; r += kThreads) {
         int c = 0;
 #pragma unroll
-        for (int w = 0; w < kTileWords; ++w) c += __popc(s_bm[r * kTileWords + w]);
+        for (int w = 0; w < kTileWords; ++w) c += __popc(s_bm[w * R + r]);
         p.ws_rank[static_cast<size_t>(r) * p.num_tiles + tile] = c;
     }
     for (int e = threadIdx.x; e < p.E; e += kThreads)
@@ -79,7 +103,7 @@ __global__ void __launch_bounds__(kThreads) layout_count_kernel(const LayoutPara
     for (int n = threadIdx.x; n < p.num_nodes; n += kThreads) {
         int c = 0;
 #pragma unroll
-        for (int w = 0; w < kTileWords; ++w) c += __popc(s_bm_node[n * kTileWords + w]);
+        for (int w = 0; w < kTileWords; ++w) c += __popc(s_bm_node[w * p.num_nodes + n]);
         p.ws_node[static_cast<size_t>(n) * p.num_tiles + tile] = c;
     }
     if (threadIdx.x == 0 && s_bad) atomicOr(p.status, EP_ERR_INVALID_INDEX);
@@ -153,8 +177,8 @@ __global__ void __launch_bounds__(kThreads) layout_rows_kernel(const LayoutParam
     __shared__ int s_warp[kThreads / 32];
     const int R = p.R;
     int* s_base = reinterpret_cast<int*>(smem);                 // [R+1]
-    uint32_t* s_bm = smem + (R + 1);                             // [R][kTileWords]
-    int* s_wpre = reinterpret_cast<int*>(s_bm + R * kTileWords);  // [R][kTileWords]
+    uint32_t* s_bm = smem + (R + 1);                             // [kTileWords][R]
+    int* s_wpre = reinterpret_cast<int*>(s_bm + R * kTileWords);  // [kTileWords][R]
     const int tile = blockIdx.x;
 
     const int32_t* cnt = p.num_tokens_per_rank;
@@ -180,8 +204,8 @@ __global__ void __launch_bounds__(kThreads) layout_rows_kernel(const LayoutParam
         int run = 0;
 #pragma unroll
         for (int w = 0; w < kTileWords; ++w) {
-            s_wpre[r * kTileWords + w] = run;
-            run += __popc(s_bm[r * kTileWords + w]);
+            s_wpre[w * R + r] = run;
+            run += __popc(s_bm[w * R + r]);
         }
     }
     __syncthreads();
@@ -195,10 +219,10 @@ __global__ void __launch_bounds__(kThreads) layout_rows_kernel(const LayoutParam
         const int tl = j / R;
         const int r = j - tl * R;
         const int w = tl >> 5;
-        const uint32_t word = s_bm[r * kTileWords + w];
+        const uint32_t word = s_bm[w * R + r];
         const uint32_t b = static_cast<uint32_t>(tl & 31);
         const bool in = (word >> b) & 1u;
-        drow[j] = in ? s_base[r] + s_wpre[r * kTileWords + w] + __popc(word & ((1u << b) - 1u)) : -1;
+        drow[j] = in ? s_base[r] + s_wpre[w * R + r] + __popc(word & ((1u << b) - 1u)) : -1;
         inr[j] = in ? 1 : 0;
     }
 
@@ -219,7 +243,232 @@ __global__ void __launch_bounds__(kThreads) layout_rows_kernel(const LayoutParam
                 const int hi = min(b - w * 32, 32);
                 const uint32_t upper = hi >= 32 ? 0xffffffffu : ((1u << hi) - 1u);
                 const uint32_t mask = upper & ~((1u << lo) - 1u);
-                c += __popc(s_bm[r * kTileWords + w] & mask);
+                c += __popc(s_bm[w * R + r] & mask);
+            }
+            if (c) atomicAdd(&p.src_dst_count[s * R + r], c);
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Single-launch cluster path
+// ---------------------------------------------------------------------------
+
+constexpr int kClusterThreads = 1024;
+constexpr int kClusterUnroll = 4;
+constexpr int kMaxClusterCtas = 16;
+#ifndef EP_LAYOUT_CLUSTER_MAX_TOKEN_RANKS
+#define EP_LAYOUT_CLUSTER_MAX_TOKEN_RANKS (1 << 19)
+#endif
+// Above this many (token, rank) outputs the tiled path (one CTA per 256 tokens) is used.
+constexpr int64_t kClusterMaxTokenRanks = EP_LAYOUT_CLUSTER_MAX_TOKEN_RANKS;
+
+// Shared-memory words of one cluster CTA for W bitmap words per rank.
+size_t cluster_smem_words(int R, int E, int nodes, int W) {
+    return 2 * static_cast<size_t>(R) * W + static_cast<size_t>(nodes) * W + R + E + nodes + (R + 1) +
+           R + 64;
+}
+
+// In-place exclusive scan of a[0, n) in shared memory by all kClusterThreads
+// threads; returns the total.  s_warp holds 33 ints.
+__device__ int smem_exclusive_scan(int* a, int n, int* s_warp) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int per = (n + kClusterThreads - 1) / kClusterThreads;
+    const int begin = min(n, tid * per);
+    const int end = min(n, begin + per);
+    int local = 0;
+    for (int i = begin; i < end; ++i) local += a[i];
+    const int incl = warp_inclusive_scan(local);
+    if (lane == 31) s_warp[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+        const int v = s_warp[lane];
+        const int inc = warp_inclusive_scan(v);
+        s_warp[lane] = inc - v;
+        if (lane == 31) s_warp[32] = inc;
+    }
+    __syncthreads();
+    int run = s_warp[warp] + incl - local;
+    for (int i = begin; i < end; ++i) {
+        const int v = a[i];
+        a[i] = run;
+        run += v;
+    }
+    const int total = s_warp[32];
+    __syncthreads();
+    return total;
+}
+
+__global__ void __launch_bounds__(kClusterThreads, 1)
+    layout_cluster_kernel(const LayoutParams p, int tokens_per_cta) {
+    namespace cg = cooperative_groups;
+    cg::cluster_group cluster = cg::this_cluster();
+    const int C = static_cast<int>(cluster.num_blocks());
+    const int me = static_cast<int>(cluster.block_rank());
+    extern __shared__ __align__(16) uint32_t smem[];
+    __shared__ int s_warp[33];
+    __shared__ int s_bad;
+    const int R = p.R, E = p.E, NN = p.num_nodes;
+    const int W = tokens_per_cta / 32;
+    uint32_t* s_bm = smem;                                          // [W][R] membership
+    int* s_wbase = reinterpret_cast<int*>(s_bm + R * W);            // [W][R] row base per word
+    uint32_t* s_bmn = reinterpret_cast<uint32_t*>(s_wbase + R * W);  // [W][NN] node membership
+    int* s_cnt = reinterpret_cast<int*>(s_bmn + NN * W);            // [R]  read by every CTA
+    int* s_hist = s_cnt + R;                                        // [E]  read by the last CTA
+    int* s_ncnt = s_hist + E;                                       // [NN] read by the last CTA
+    int* s_tot = s_ncnt + NN;                                       // [R+1]
+    int* s_before = s_tot + R + 1;                                  // [R]
+    const int tid = threadIdx.x;
+    const int t0 = me * tokens_per_cta;
+    const int nt = max(0, min(tokens_per_cta, p.T - t0));
+
+    for (int i = tid; i < R * W; i += kClusterThreads) s_bm[i] = 0u;
+    for (int i = tid; i < NN * W; i += kClusterThreads) s_bmn[i] = 0u;
+    for (int i = tid; i < E; i += kClusterThreads) s_hist[i] = 0;
+    if (tid == 0) s_bad = 0;
+    if (p.src_dst_count) {
+        for (int i = me * kClusterThreads + tid; i < R * R; i += C * kClusterThreads)
+            p.src_dst_count[i] = 0;
+    }
+    __syncthreads();
+
+    // Phase 1: membership bitmaps and the expert histogram of this CTA's range.
+    const int n_ent = nt * p.K;
+    const int64_t* src = p.topk_idx + static_cast<int64_t>(t0) * p.K;
+    bool bad = false;
+    for (int base = 0; base < n_ent; base += kClusterUnroll * kClusterThreads) {
+        int64_t e[kClusterUnroll];
+#pragma unroll
+        for (int u = 0; u < kClusterUnroll; ++u) {
+            const int i = base + u * kClusterThreads + tid;
+            e[u] = i < n_ent ? src[i] : -1;
+        }
+#pragma unroll
+        for (int u = 0; u < kClusterUnroll; ++u) {
+            if (e[u] == -1) continue;
+            if (e[u] < -1 || e[u] >= E) { bad = true; continue; }
+            const int i = base + u * kClusterThreads + tid;
+            const int tl = i / p.K;
+            const int r = static_cast<int>(e[u]) / p.experts_per_rank;
+            const uint32_t bit = 1u << (tl & 31);
+            atomicAdd(&s_hist[e[u]], 1);
+            atomicOr(&s_bm[(tl >> 5) * R + r], bit);
+            if (NN) atomicOr(&s_bmn[(tl >> 5) * NN + r / p.ranks_per_node], bit);
+        }
+    }
+    if (bad) s_bad = 1;
+    __syncthreads();
+    for (int r = tid; r < R; r += kClusterThreads) {
+        int run = 0;
+        for (int w = 0; w < W; ++w) {
+            s_wbase[w * R + r] = run;
+            run += __popc(s_bm[w * R + r]);
+        }
+        s_cnt[r] = run;
+    }
+    for (int n = tid; n < NN; n += kClusterThreads) {
+        int c = 0;
+        for (int w = 0; w < W; ++w) c += __popc(s_bmn[w * NN + n]);
+        s_ncnt[n] = c;
+    }
+    if (tid == 0 && s_bad) atomicOr(p.status, EP_ERR_INVALID_INDEX);
+    cluster.sync();   // counts of every CTA visible; src_dst_count zeroed
+
+    // Phase 2: rank totals, this CTA's base per rank, and (two CTAs) the outputs.
+    for (int r = tid; r < R; r += kClusterThreads) {
+        int tot = 0, before = 0;
+        for (int c = 0; c < C; ++c) {
+            const int v = cluster.map_shared_rank(s_cnt, c)[r];
+            tot += v;
+            if (c < me) before += v;
+        }
+        s_tot[r] = tot;
+        s_before[r] = before;
+        if (me == 0) p.num_tokens_per_rank[r] = tot;
+    }
+    __syncthreads();
+    const int n_recv = smem_exclusive_scan(s_tot, R, s_warp);   // s_tot = rank_offset
+    if (me == 0) {
+        for (int r = tid; r < R; r += kClusterThreads) p.rank_offset[r] = s_tot[r];
+        if (tid == 0) p.rank_offset[R] = n_recv;
+    }
+    if (me == C - 1) {
+        for (int e = tid; e < E; e += kClusterThreads) {
+            int tot = 0;
+            for (int c = 0; c < C; ++c) tot += cluster.map_shared_rank(s_hist, c)[e];
+            p.num_tokens_per_expert[e] = tot;
+            s_hist[e] = (tot + p.alignment - 1) / p.alignment * p.alignment;   // own slot only
+        }
+        for (int n = tid; n < NN; n += kClusterThreads) {
+            int tot = 0;
+            for (int c = 0; c < C; ++c) tot += cluster.map_shared_rank(s_ncnt, c)[n];
+            p.num_tokens_per_node[n] = tot;
+        }
+    }
+    cluster.sync();   // every remote read done: shared memory may be reused / released
+    if (me == C - 1) {
+        const int tot = smem_exclusive_scan(s_hist, E, s_warp);
+        for (int e = tid; e < E; e += kClusterThreads) p.expert_offset[e] = s_hist[e];
+        if (tid == 0) p.expert_offset[E] = tot;
+    }
+
+    // Phase 3: dst_row and is_token_in_rank of this CTA's [nt, R] block.
+    for (int i = tid; i < R * W; i += kClusterThreads) {
+        const int r = i % R;
+        s_wbase[i] += s_tot[r] + s_before[r];
+    }
+    __syncthreads();
+    const int n_el = nt * R;
+    int32_t* drow = p.dst_row + static_cast<int64_t>(t0) * R;
+    uint8_t* inr = p.is_token_in_rank + static_cast<int64_t>(t0) * R;
+    for (int q = tid; q * 4 < n_el; q += kClusterThreads) {
+        const int j0 = q * 4;
+        int tl = j0 / R;
+        int r = j0 - tl * R;
+        int v[4];
+        uint32_t in4 = 0;
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            v[u] = -1;
+            if (j0 + u < n_el) {
+                const int w = tl >> 5;
+                const uint32_t word = s_bm[w * R + r];
+                const uint32_t b = static_cast<uint32_t>(tl & 31);
+                if ((word >> b) & 1u) {
+                    v[u] = s_wbase[w * R + r] + __popc(word & ((1u << b) - 1u));
+                    in4 |= 1u << (8 * u);
+                }
+            }
+            if (++r == R) { r = 0; ++tl; }
+        }
+        if (j0 + 4 <= n_el) {
+            *reinterpret_cast<int4*>(drow + j0) = make_int4(v[0], v[1], v[2], v[3]);
+            *reinterpret_cast<uint32_t*>(inr + j0) = in4;
+        } else {
+            for (int u = 0; u < 4 && j0 + u < n_el; ++u) {
+                drow[j0 + u] = v[u];
+                inr[j0 + u] = static_cast<uint8_t>((in4 >> (8 * u)) & 1u);
+            }
+        }
+    }
+
+    // src_dst_count[s][r] += tokens of source rank s in this range that rank r receives.
+    if (p.src_dst_count && nt > 0) {
+        const int ts = p.T / R;
+        const int s_lo = t0 / ts;
+        const int s_hi = (t0 + nt - 1) / ts;
+        const int n_pairs = (s_hi - s_lo + 1) * R;
+        for (int q = tid; q < n_pairs; q += kClusterThreads) {
+            const int s = s_lo + q / R;
+            const int r = q - (q / R) * R;
+            const int a = max(t0, s * ts) - t0;
+            const int b = min(t0 + nt, (s + 1) * ts) - t0;
+            int c = 0;
+            for (int w = a >> 5; w <= (b - 1) >> 5; ++w) {
+                const int lo = max(a - w * 32, 0);
+                const int hi = min(b - w * 32, 32);
+                const uint32_t upper = hi >= 32 ? 0xffffffffu : ((1u << hi) - 1u);
+                c += __popc(s_bm[w * R + r] & upper & ~((1u << lo) - 1u));
             }
             if (c) atomicAdd(&p.src_dst_count[s * R + r], c);
         }
@@ -227,6 +476,34 @@ __global__ void __launch_bounds__(kThreads) layout_rows_kernel(const LayoutParam
 }
 
 size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+// Cluster shape for the single-launch path, or C = 0 when it does not apply.
+struct ClusterPlan {
+    int ctas;
+    int tokens_per_cta;
+    size_t smem;
+};
+
+ClusterPlan plan_cluster(const LayoutParams& p, const DeviceInfo& di) {
+    ClusterPlan plan{0, 0, 0};
+    // One CTA per 256 tokens up to 16; ranges are whole 32-token words.
+    int ctas = (p.T + kTileTokens - 1) / kTileTokens;
+    if (ctas < 1) ctas = 1;
+    if (ctas > kMaxClusterCtas) ctas = kMaxClusterCtas;
+    int tpc = (p.T + ctas - 1) / ctas;
+    tpc = (tpc + 31) / 32 * 32;
+    if (tpc < 32) tpc = 32;
+    ctas = (p.T + tpc - 1) / tpc;
+    if (ctas < 1) ctas = 1;
+    const size_t smem = 4 * cluster_smem_words(p.R, p.E, p.num_nodes, tpc / 32);
+    if (smem > static_cast<size_t>(di.max_smem_optin) - 1024) return plan;
+    // Large [T, R] outputs are written faster by the many-CTA path.
+    if (static_cast<int64_t>(p.T) * p.R > kClusterMaxTokenRanks) return plan;
+    plan.ctas = ctas;
+    plan.tokens_per_cta = tpc;
+    plan.smem = smem;
+    return plan;
+}
 
 }  // namespace
 
@@ -248,10 +525,8 @@ LayoutWorkspace layout_workspace(int T, int E, int R, int num_nodes) {
 
 cudaError_t launch_layout(const LayoutParams& p, cudaStream_t stream) {
     const DeviceInfo& di = device_info();
-    const size_t smem_count =
-        4 * (static_cast<size_t>(p.R) * kTileWords + static_cast<size_t>(p.num_nodes) * kTileWords + p.E);
-    const size_t smem_rows = 4 * (static_cast<size_t>(p.R) + 1 + 2 * static_cast<size_t>(p.R) * kTileWords);
     static thread_local int configured_device = -1;
+    static thread_local bool cluster_ok = false;
     if (configured_device != di.device) {
         // Worst case over the supported limits (R = 1024, E = 2048): < 80 KB.
         const int cap = di.max_smem_optin < 100 * 1024 ? di.max_smem_optin : 100 * 1024;
@@ -259,8 +534,40 @@ cudaError_t launch_layout(const LayoutParams& p, cudaStream_t stream) {
         if (e != cudaSuccess) return e;
         e = cudaFuncSetAttribute(layout_rows_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, cap);
         if (e != cudaSuccess) return e;
+        cluster_ok =
+            cudaFuncSetAttribute(layout_cluster_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 di.max_smem_optin - 1024) == cudaSuccess &&
+            cudaFuncSetAttribute(layout_cluster_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed,
+                                 1) == cudaSuccess;
+        cudaGetLastError();   // a refused attribute only disables the cluster path
         configured_device = di.device;
     }
+
+    const ClusterPlan plan = cluster_ok ? plan_cluster(p, di) : ClusterPlan{0, 0, 0};
+    if (plan.ctas > 0) {
+        cudaLaunchConfig_t cfg = {};
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = plan.ctas;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.gridDim = dim3(plan.ctas);
+        cfg.blockDim = dim3(kClusterThreads);
+        cfg.dynamicSmemBytes = plan.smem;
+        cfg.stream = stream;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        int max_clusters = 0;
+        if (cudaOccupancyMaxActiveClusters(&max_clusters, layout_cluster_kernel, &cfg) == cudaSuccess &&
+            max_clusters >= 1) {
+            return cudaLaunchKernelEx(&cfg, layout_cluster_kernel, p, plan.tokens_per_cta);
+        }
+        cudaGetLastError();   // fall back to the tiled path
+    }
+
+    const size_t smem_count =
+        4 * (static_cast<size_t>(p.R) * kTileWords + static_cast<size_t>(p.num_nodes) * kTileWords + p.E);
+    const size_t smem_rows = 4 * (static_cast<size_t>(p.R) + 1 + 2 * static_cast<size_t>(p.R) * kTileWords);
     const int grid_tiles = p.num_tiles > 0 ? p.num_tiles : 1;
     layout_count_kernel<<<grid_tiles, kThreads, smem_count, stream>>>(p);
     const int n_cols = p.R + p.E + p.num_nodes;

@@ -44,6 +44,9 @@ def test_layout_workloads_full_size(name):
     (300, 3, 32, 1, 0, 1, 0.0),           # one rank
     (512, 32, 2048, 1024, 32, 1, 0.0),    # the limits: R=1024, E=2048, K=32
     (2048, 9, 2048, 8, 0, 16, 0.1),       # 256 experts per rank
+    (4096, 8, 2048, 1024, 0, 1, 0.0),     # many (token, rank) outputs: tiled path
+    (32768, 8, 256, 128, 16, 1, 0.01),    # tiled path with node and source counts
+    (9000, 8, 256, 256, 32, 3, 0.0),      # tiled path, ragged last tile
 ])
 def test_layout_shapes(T, K, E, R, rpn, align, mask):
     idx = make_inputs(T, 8, E, K, R, seed=T + K + E + R, mask_frac=mask, with_x=False)["topk_idx"]
