@@ -37,7 +37,8 @@ _i64 = ctypes.c_int64
 class ep_layout_t(ctypes.Structure):
     _fields_ = [("num_tokens_per_rank", _vp), ("num_tokens_per_node", _vp),
                 ("num_tokens_per_expert", _vp), ("is_token_in_rank", _vp), ("rank_offset", _vp),
-                ("expert_offset", _vp), ("dst_row", _vp), ("src_dst_count", _vp)]
+                ("expert_offset", _vp), ("dst_row", _vp), ("src_dst_count", _vp),
+                ("token_offset", _vp)]
 
 
 _lib.ep_layout_workspace_bytes.restype = ctypes.c_size_t
@@ -113,6 +114,7 @@ class Layout:
         self.expert_offset = torch.empty(E + 1, **i32)
         self.dst_row = torch.empty((T, R), **i32)
         self.src_dst_count = torch.empty((R, R), **i32) if (with_src_dst and T % R == 0) else None
+        self.token_offset = torch.empty(T + 1, **i32)
         self.c = ep_layout_t(*[_ptr(getattr(self, f)) for f, _ in ep_layout_t._fields_])
 
     @property

@@ -48,7 +48,7 @@ ep_status_t check_shape(int T, int K, int E, int R) {
 
 extern "C" {
 
-int ep_abi_version(void) { return 1; }
+int ep_abi_version(void) { return 2; }
 
 size_t ep_layout_workspace_bytes(int num_tokens, int num_topk, int num_experts, int num_ranks,
                                  int ranks_per_node) {
@@ -79,6 +79,7 @@ ep_status_t ep_get_layout(const int64_t* topk_idx, int T, int K, int E, int R, i
         return EP_ERR_INVALID_ARG;
     if (out->num_tokens_per_node && !aligned16(out->num_tokens_per_node)) return EP_ERR_INVALID_ARG;
     if (out->src_dst_count && (!aligned16(out->src_dst_count) || T % R != 0)) return EP_ERR_INVALID_ARG;
+    if (out->token_offset && !aligned16(out->token_offset)) return EP_ERR_INVALID_ARG;
     const int nodes_ws = ranks_per_node > 0 ? R / ranks_per_node : 0;
     const epg::LayoutWorkspace w = epg::layout_workspace(T, E, R, nodes_ws);
     if (!ok_ptr(workspace) || ws_bytes < w.total) return EP_ERR_INVALID_ARG;
@@ -102,6 +103,7 @@ ep_status_t ep_get_layout(const int64_t* topk_idx, int T, int K, int E, int R, i
     p.expert_offset = out->expert_offset;
     p.dst_row = out->dst_row;
     p.src_dst_count = out->src_dst_count;
+    p.token_offset = out->token_offset;
     char* ws = static_cast<char*>(workspace);
     p.ws_rank = reinterpret_cast<int32_t*>(ws + w.off_rank);
     p.ws_expert = reinterpret_cast<int32_t*>(ws + w.off_expert);
@@ -147,6 +149,7 @@ ep_status_t ep_dispatch(const void* x, const int64_t* topk_idx, const float* top
     p.topk_idx = topk_idx;
     p.topk_weights = topk_weights;
     p.dst_row = layout->dst_row;
+    p.token_offset = layout->token_offset;
     p.T = T;
     p.H = H;
     p.K = K;

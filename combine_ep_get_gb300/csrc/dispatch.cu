@@ -4,43 +4,151 @@
 // ("DeepEP Symmetric Memory" sections 6.1 and 9.2; "DeepEP V2 ElasticBuffer
 // architecture", TokenLayout fragment).
 //
-// bf16 path (pure copy, HBM-bound, writes ~n(t) times the reads):
-//   persistent CTAs of 4 warps.  Warp 0 drives the bulk-copy engine: a ring
-//   of kStages shared-memory slots, each filled by one cp.async.bulk
-//   global->shared load of a token row (or a piece of it) that completes on an
-//   mbarrier; once it lands, the lanes that own a destination rank each issue
-//   one cp.async.bulk shared->global store of the slot, so a row is read from
-//   HBM once and written n(t) times without passing through registers.  A slot
-//   is refilled when the bulk group that reads it has finished reading.
-//   Warps 1-3 write the per-row metadata (remapped top-k, weights, source).
+// bf16 path (pure copy, HBM-bound, writes ~n(t) times the reads), default:
+//   one CTA of 256 threads per (token, piece of <= 16 KB).  Every thread first
+//   issues its 16-byte streaming loads of the piece (up to 4), warp 0 meanwhile
+//   compacts the token's destination rows (one lane per rank, ballot) into
+//   shared memory, warp 1 writes the per-row metadata, and after one barrier
+//   every thread stores its vectors to every destination row.  Thousands of
+//   short CTAs let the block scheduler balance the uneven fan-out n(t).
+//
+// bf16 alternative (EP_DISPATCH_IMPL=0): persistent CTAs whose warp 0 drives
+//   the bulk-copy engine: a ring of kStages shared-memory slots, each filled by
+//   one cp.async.bulk global->shared load of a token row that completes on an
+//   mbarrier, then one cp.async.bulk shared->global store per destination, so
+//   a row never passes through registers; warps 1-3 write the metadata.  With
+//   token_offset it splits the receive rows evenly over the CTAs.  On GB300 it
+//   measured ~7% slower than the register path for every stage count, piece
+//   size and L2 hint tried, so it is not the default.
 //
 // FP8 path: one CTA per (token, piece of 128-channel blocks); each half-warp
 //   owns one 128-channel block, loads it with 16-byte vectors, takes amax by
 //   shuffles, scales with IEEE divides and converts with cvt.rn.satfinite
 //   e4m3x2, then stores the 8-byte code vectors and the scale to every
 //   destination row.
+#include <climits>
+
 #include "ep_internal.cuh"
 
 namespace epg {
 namespace {
 
-constexpr int kBf16Threads = 128;
-constexpr int kStages = 4;
-constexpr int kStoreDepth = 2;
+// Compile-time tuning of the bf16 path (defaults are the measured best).
+#ifndef EP_DISPATCH_STAGES
+#define EP_DISPATCH_STAGES 4          // shared-memory slots per CTA
+#endif
+#ifndef EP_DISPATCH_STORE_DEPTH
+#define EP_DISPATCH_STORE_DEPTH 2     // bulk-store groups in flight per CTA
+#endif
+#ifndef EP_DISPATCH_PIECE_MAX
+#define EP_DISPATCH_PIECE_MAX 16384   // bytes of a row moved by one bulk copy
+#endif
+#ifndef EP_DISPATCH_BALANCED
+#define EP_DISPATCH_BALANCED 1        // split rows evenly when token_offset is given
+#endif
+#ifndef EP_DISPATCH_EVICT_FIRST
+#define EP_DISPATCH_EVICT_FIRST 0     // L2 evict-first hint on the receive-row stores
+#endif
+#ifndef EP_DISPATCH_IMPL
+#define EP_DISPATCH_IMPL 1            // 1: 16-byte register copies, 0: bulk-copy engine
+#endif
+#ifndef EP_DISPATCH_STORE_CS
+#define EP_DISPATCH_STORE_CS 0        // register path: streaming (.cs) stores
+#endif
 
-// Metadata of token t for every rank that receives it (one warp).
+constexpr int kBf16Threads = 128;
+constexpr int kStages = EP_DISPATCH_STAGES;
+constexpr int kStoreDepth = EP_DISPATCH_STORE_DEPTH;
+
+// The work of one CTA.  Strided mode: items first, first + stride, ... of the
+// (token, piece) list, every destination stored.  Balanced mode (rows
+// numbered token by token are known, one piece per token): the CTA owns rows
+// [lo, hi) of that numbering, N / gridDim rows each, and the consecutive
+// tokens first .. first + count - 1 that hold them; only destinations whose
+// row number falls in [lo, hi) are stored by this CTA.
+struct CtaWork {
+    int64_t first, count, stride;
+    int lo, hi;
+    int balanced;
+};
+
+// Largest t in [0, T) with a[t] <= v, for a non-decreasing a with a[0] <= v,
+// searched by one warp in a 128-entry window around `guess` (one round trip of
+// loads); a binary search covers a guess that misses.
+__device__ int warp_last_le(const int32_t* a, int T, int v, int guess, int lane) {
+    int w0 = guess - 64;
+    if (w0 > T - 128) w0 = T - 128;
+    if (w0 < 0) w0 = 0;
+    int vals[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        const int idx = w0 + q * 32 + lane;
+        vals[q] = idx < T ? a[idx] : INT32_MAX;
+    }
+    int cnt = 0;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) cnt += __popc(__ballot_sync(0xffffffffu, vals[q] <= v));
+    if (cnt >= 1 && (cnt < 128 || w0 + 128 >= T)) return w0 + cnt - 1;
+    int res = 0;
+    if (lane == 0) {
+        int lo = 0, hi = T - 1;
+        while (lo < hi) {
+            const int mid = lo + (hi - lo + 1) / 2;
+            if (a[mid] <= v) lo = mid;
+            else hi = mid - 1;
+        }
+        res = lo;
+    }
+    return __shfl_sync(0xffffffffu, res, 0);
+}
+
+__device__ void cta_work(const DispatchParams& p, int lane, CtaWork& w) {
+    const int64_t num_items = static_cast<int64_t>(p.T) * p.chunks;
+    if (!EP_DISPATCH_BALANCED || p.token_offset == nullptr || p.chunks != 1) {
+        w.balanced = 0;
+        w.first = blockIdx.x;
+        w.stride = gridDim.x;
+        w.count = w.first < num_items ? (num_items - w.first + w.stride - 1) / w.stride : 0;
+        w.lo = INT32_MIN;
+        w.hi = INT32_MAX;
+        return;
+    }
+    w.balanced = 1;
+    w.stride = 1;
+    const int N = p.token_offset[p.T];
+    const int64_t G = gridDim.x, b = blockIdx.x;
+    w.lo = static_cast<int>(b * N / G);
+    w.hi = static_cast<int>((b + 1) * N / G);
+    if (w.lo >= w.hi) {
+        w.first = 0;
+        w.count = 0;
+        return;
+    }
+    const int g0 = static_cast<int>(static_cast<int64_t>(w.lo) * p.T / N);
+    const int g1 = static_cast<int>(static_cast<int64_t>(w.hi - 1) * p.T / N);
+    const int t0 = warp_last_le(p.token_offset, p.T, w.lo, g0, lane);
+    const int t1 = warp_last_le(p.token_offset, p.T, w.hi - 1, g1, lane);
+    w.first = t0;
+    w.count = t1 - t0 + 1;
+}
+
+// Metadata of token t for every destination row this CTA owns (one warp).
 __device__ __forceinline__ void write_metadata(const DispatchParams& p, int t, int lane,
-                                               bool& cap_bad) {
+                                               const CtaWork& w) {
     const int K = p.K;
     const int64_t e_l = lane < K ? p.topk_idx[static_cast<int64_t>(t) * K + lane] : -1;
     const float w_l =
         (lane < K && p.recv_topk_weights) ? p.topk_weights[static_cast<int64_t>(t) * K + lane] : 0.0f;
+    const int tok_off = w.balanced ? p.token_offset[t] : 0;
+    int m_base = 0;
     for (int rb = 0; rb < p.R; rb += 32) {
         const int r = rb + lane;
         const int d = r < p.R ? p.dst_row[static_cast<int64_t>(t) * p.R + r] : -1;
-        const bool ok = d >= 0 && d < p.capacity;
-        if (d >= p.capacity) cap_bad = true;
-        unsigned m = __ballot_sync(0xffffffffu, ok);
+        const unsigned members = __ballot_sync(0xffffffffu, d >= 0);
+        const int row_tm = tok_off + m_base + __popc(members & ((1u << lane) - 1u));
+        m_base += __popc(members);
+        const bool mine = d >= 0 && row_tm >= w.lo && row_tm < w.hi && d < p.capacity;
+        unsigned m = __ballot_sync(0xffffffffu, mine);
         while (m) {
             const int src = __ffs(m) - 1;
             m &= m - 1;
@@ -60,25 +168,33 @@ __device__ __forceinline__ void write_metadata(const DispatchParams& p, int t, i
 
 __global__ void __launch_bounds__(kBf16Threads) dispatch_bf16_kernel(const DispatchParams p) {
     extern __shared__ __align__(128) uint8_t smem[];
+    __shared__ CtaWork s_work;
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem);
     uint8_t* stage = smem + 128;
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int64_t num_items = static_cast<int64_t>(p.T) * p.chunks;
-    const int64_t first = blockIdx.x;
-    const int64_t stride = gridDim.x;
-    const int64_t my_n = first < num_items ? (num_items - first + stride - 1) / stride : 0;
     const uint32_t row_bytes = static_cast<uint32_t>(p.H) * 2u;
 
     if (warp == 0) {
+        CtaWork w;
+        cta_work(p, lane, w);
         if (lane == 0) {
+            s_work = w;
             for (int s = 0; s < kStages; ++s) mbar_init(&bars[s], 1);
             fence_mbar_init();
         }
-        __syncwarp();
+    }
+    __syncthreads();
+    const CtaWork w = s_work;
+    const int64_t my_n = w.count;
+
+    if (warp == 0) {
+#if EP_DISPATCH_EVICT_FIRST
+        const uint64_t policy = l2_policy_evict_first();
+#endif
         int64_t issued = 0;  // lane 0 only
         auto issue = [&](int64_t i) {
-            const int64_t it = first + i * stride;
+            const int64_t it = w.first + i * w.stride;
             const int64_t t = it / p.chunks;
             const uint32_t off = static_cast<uint32_t>(it - t * p.chunks) * p.chunk_bytes;
             const uint32_t bytes = min(p.chunk_bytes, row_bytes - off);
@@ -95,22 +211,36 @@ __global__ void __launch_bounds__(kBf16Threads) dispatch_bf16_kernel(const Dispa
         int64_t i = 0;
         for (; i < my_n; ++i) {
             const int slot = static_cast<int>(i % kStages);
-            const int64_t it = first + i * stride;
+            const int64_t it = w.first + i * w.stride;
             const int64_t t = it / p.chunks;
             const uint32_t off = static_cast<uint32_t>(it - t * p.chunks) * p.chunk_bytes;
             const uint32_t bytes = min(p.chunk_bytes, row_bytes - off);
+            // destination rows of the first 32 ranks and the token's first row
+            // number: loaded before the wait so their latency overlaps it
+            const int d0 = lane < p.R ? p.dst_row[t * p.R + lane] : -1;
+            const int tok_off = w.balanced ? p.token_offset[t] : 0;
             const bool landed = mbar_wait_bounded(&bars[slot], static_cast<uint32_t>((i / kStages) & 1));
             if (!__all_sync(0xffffffffu, landed)) {
                 ok = false;
                 break;
             }
             const uint8_t* src = stage + static_cast<size_t>(slot) * p.chunk_bytes;
+            int m_base = 0;
             for (int rb = 0; rb < p.R; rb += 32) {
                 const int r = rb + lane;
-                const int d = r < p.R ? p.dst_row[t * p.R + r] : -1;
-                if (d >= 0) {
-                    if (d < p.capacity)
+                const int d = rb == 0 ? d0 : (r < p.R ? p.dst_row[t * p.R + r] : -1);
+                const unsigned members = __ballot_sync(0xffffffffu, d >= 0);
+                const int row_tm = tok_off + m_base + __popc(members & ((1u << lane) - 1u));
+                m_base += __popc(members);
+                if (d >= 0 && row_tm >= w.lo && row_tm < w.hi) {
+                    if (d < p.capacity) {
+#if EP_DISPATCH_EVICT_FIRST
+                        bulk_store_evict_first(p.recv_x + static_cast<int64_t>(d) * row_bytes + off, src,
+                                               bytes, policy);
+#else
                         bulk_store(p.recv_x + static_cast<int64_t>(d) * row_bytes + off, src, bytes);
+#endif
+                    }
                     else
                         cap_bad = true;
                 }
@@ -135,20 +265,104 @@ __global__ void __launch_bounds__(kBf16Threads) dispatch_bf16_kernel(const Dispa
         }
         if (__any_sync(0xffffffffu, cap_bad) && lane == 0) atomicOr(p.status, EP_ERR_CAPACITY);
     } else {
-        // Metadata: tokens of this CTA (piece 0 of each), round-robin over warps 1..3.
+        // Metadata: this CTA's tokens (piece 0 of each), round-robin over warps 1..3.
         const int mw = warp - 1;
         const int n_mw = kBf16Threads / 32 - 1;
-        bool cap_bad = false;
         int64_t count = 0;
         for (int64_t i = 0; i < my_n; ++i) {
-            const int64_t it = first + i * stride;
+            const int64_t it = w.first + i * w.stride;
             if (it % p.chunks != 0) continue;
             if ((count++ % n_mw) != mw) continue;
-            write_metadata(p, static_cast<int>(it / p.chunks), lane, cap_bad);
+            write_metadata(p, static_cast<int>(it / p.chunks), lane, w);
         }
-        (void)cap_bad;  // the copy warp reports capacity overflows
     }
 }
+
+#if EP_DISPATCH_IMPL == 1
+constexpr int kRegThreads = 256;
+constexpr int kRegUnroll = 4;
+
+// Register path: one CTA per (token, piece); each thread loads up to
+// kRegUnroll 16-byte vectors of the piece, then stores each to every
+// destination row.
+__global__ void __launch_bounds__(kRegThreads) dispatch_bf16_regs_kernel(const DispatchParams p) {
+    __shared__ int s_rows[EP_MAX_TOPK];
+    __shared__ int s_n;
+    const int64_t it = blockIdx.x;
+    const int t = static_cast<int>(it / p.chunks);
+    const int c = static_cast<int>(it - static_cast<int64_t>(t) * p.chunks);
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const uint32_t row_bytes = static_cast<uint32_t>(p.H) * 2u;
+    const uint32_t off = static_cast<uint32_t>(c) * p.chunk_bytes;
+    const uint32_t bytes = min(p.chunk_bytes, row_bytes - off);
+    const int nvec = static_cast<int>(bytes / 16);
+    const uint8_t* src = p.x + static_cast<int64_t>(t) * row_bytes + off;
+    // issue this thread's loads before anything waits
+    uint4 u[kRegUnroll];
+#pragma unroll
+    for (int k = 0; k < kRegUnroll; ++k) {
+        const int v = threadIdx.x + k * kRegThreads;
+        if (v < nvec) u[k] = ld_stream_v4(src + static_cast<size_t>(v) * 16);
+    }
+    if (warp == 0) {
+        int n = 0;
+        bool cap_bad = false;
+        for (int rb = 0; rb < p.R; rb += 32) {
+            const int r = rb + lane;
+            const int d = r < p.R ? p.dst_row[static_cast<int64_t>(t) * p.R + r] : -1;
+            const bool ok = d >= 0 && d < p.capacity;
+            if (d >= p.capacity) cap_bad = true;
+            const unsigned m = __ballot_sync(0xffffffffu, ok);
+            const int pos = n + __popc(m & ((1u << lane) - 1u));
+            if (ok && pos < EP_MAX_TOPK) s_rows[pos] = d;
+            n += __popc(m);
+        }
+        if (n > EP_MAX_TOPK) {
+            if (lane == 0) atomicOr(p.status, EP_ERR_INVALID_INDEX);
+            n = EP_MAX_TOPK;
+        }
+        if (lane == 0) s_n = n;
+        if (__any_sync(0xffffffffu, cap_bad) && lane == 0 && c == 0) atomicOr(p.status, EP_ERR_CAPACITY);
+    } else if (warp == 1 && c == 0) {
+        CtaWork all;
+        all.first = 0;
+        all.count = 0;
+        all.stride = 1;
+        all.lo = INT32_MIN;
+        all.hi = INT32_MAX;
+        all.balanced = 0;
+        write_metadata(p, t, lane, all);
+    }
+    __syncthreads();
+    const int n = s_n;
+    for (int base = 0; base < nvec; base += kRegUnroll * kRegThreads) {
+        if (base > 0) {
+#pragma unroll
+            for (int k = 0; k < kRegUnroll; ++k) {
+                const int v = base + threadIdx.x + k * kRegThreads;
+                if (v < nvec) u[k] = ld_stream_v4(src + static_cast<size_t>(v) * 16);
+            }
+        }
+        for (int m = 0; m < n; ++m) {
+            uint8_t* dst = p.recv_x + static_cast<int64_t>(s_rows[m]) * row_bytes + off;
+#pragma unroll
+            for (int k = 0; k < kRegUnroll; ++k) {
+                const int v = base + threadIdx.x + k * kRegThreads;
+                if (v < nvec) {
+#if EP_DISPATCH_STORE_CS
+                    st_cs_v4(dst + static_cast<size_t>(v) * 16, u[k]);
+#else
+                    st_v4(dst + static_cast<size_t>(v) * 16, u[k]);
+#endif
+                }
+            }
+        }
+    }
+}
+
+#endif  // EP_DISPATCH_IMPL == 1
+
 
 __device__ __forceinline__ uint32_t pack_e4m3x4(float a, float b, float c, float d) {
     uint16_t lo, hi;
@@ -191,8 +405,14 @@ __global__ void __launch_bounds__(kFp8Threads) dispatch_fp8_kernel(const Dispatc
         if (lane == 0) s_n = n;
         if (__any_sync(0xffffffffu, cap_bad) && lane == 0 && c == 0) atomicOr(p.status, EP_ERR_CAPACITY);
     } else if (warp == 1 && c == 0) {
-        bool cap_bad = false;
-        write_metadata(p, t, lane, cap_bad);
+        CtaWork all;
+        all.first = 0;
+        all.count = 0;
+        all.stride = 1;
+        all.lo = INT32_MIN;
+        all.hi = INT32_MAX;
+        all.balanced = 0;
+        write_metadata(p, t, lane, all);
     }
     __syncthreads();
 
@@ -252,7 +472,28 @@ cudaError_t launch_dispatch_bf16(DispatchParams p, cudaStream_t stream) {
     const uint32_t row_bytes = static_cast<uint32_t>(p.H) * 2u;
     // Pieces: at most 16 KB each; more pieces when there are few tokens so
     // that every SM gets work.
-    int chunks = static_cast<int>((row_bytes + 16383u) / 16384u);
+#if EP_DISPATCH_IMPL == 1
+    {
+        // register path: one CTA per (token, piece of <= 16 KB); more pieces for few tokens
+        int chunks = static_cast<int>((row_bytes + 16383u) / 16384u);
+        const int want_items = 4 * di.num_sms;
+        if (p.T > 0 && static_cast<int64_t>(p.T) * chunks < want_items) {
+            const int more = (want_items + p.T - 1) / p.T;
+            const int max_chunks = static_cast<int>(row_bytes / 1024u) > 0 ? static_cast<int>(row_bytes / 1024u) : 1;
+            chunks = more < max_chunks ? more : max_chunks;
+            if (chunks < 1) chunks = 1;
+        }
+        uint32_t cb = (row_bytes + chunks - 1) / chunks;
+        cb = (cb + 15u) / 16u * 16u;
+        p.chunks = static_cast<int>((row_bytes + cb - 1) / cb);
+        p.chunk_bytes = cb;
+        const int64_t g = static_cast<int64_t>(p.T) * p.chunks;
+        if (g < 1) return cudaSuccess;
+        dispatch_bf16_regs_kernel<<<static_cast<unsigned>(g), kRegThreads, 0, stream>>>(p);
+        return cudaGetLastError();
+    }
+#endif
+    int chunks = static_cast<int>((row_bytes + EP_DISPATCH_PIECE_MAX - 1) / EP_DISPATCH_PIECE_MAX);
     const int want_items = 2 * di.num_sms;
     if (p.T > 0 && static_cast<int64_t>(p.T) * chunks < want_items) {
         const int more = (want_items + p.T - 1) / p.T;

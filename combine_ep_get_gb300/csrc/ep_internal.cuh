@@ -29,6 +29,7 @@ struct LayoutParams {
     int32_t* expert_offset;
     int32_t* dst_row;
     int32_t* src_dst_count;
+    int32_t* token_offset;
     // workspace
     int32_t* ws_rank;      // [R][num_tiles]: tile counts, then exclusive tile prefix
     int32_t* ws_expert;    // [E][num_tiles]
@@ -42,6 +43,7 @@ struct DispatchParams {
     const int64_t* topk_idx;
     const float* topk_weights;
     const int32_t* dst_row;
+    const int32_t* token_offset;   // may be null
     int T, H, K, E, R, experts_per_rank;
     int64_t capacity;
     uint8_t* recv_x;
@@ -169,6 +171,21 @@ __device__ __forceinline__ void bulk_store(void* dst, const void* src_smem, uint
                  : "memory");
 }
 
+// L2 policy that marks lines for early eviction.
+__device__ __forceinline__ uint64_t l2_policy_evict_first() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
+// Bulk copy shared -> global with an L2 cache policy.
+__device__ __forceinline__ void bulk_store_evict_first(void* dst, const void* src_smem, uint32_t bytes,
+                                                       uint64_t policy) {
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group.L2::cache_hint [%0], [%1], %2, %3;" ::"l"(dst),
+                 "r"(smem_addr(src_smem)), "r"(bytes), "l"(policy)
+                 : "memory");
+}
+
 __device__ __forceinline__ void bulk_commit() {
     asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }
@@ -196,6 +213,13 @@ __device__ __forceinline__ uint4 ld_stream_v4(const void* p) {
 
 __device__ __forceinline__ void st_v4(void* p, uint4 v) {
     asm volatile("st.global.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z),
+                 "r"(v.w)
+                 : "memory");
+}
+
+// 16-byte streaming store (evict-first at every cache level).
+__device__ __forceinline__ void st_cs_v4(void* p, uint4 v) {
+    asm volatile("st.global.cs.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z),
                  "r"(v.w)
                  : "memory");
 }

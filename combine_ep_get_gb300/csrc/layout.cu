@@ -40,6 +40,27 @@ namespace {
 constexpr int kThreads = 256;
 constexpr int kUnroll = 4;
 
+// Sum of v over the block (blockDim a multiple of 32, at most 1024); s_red
+// holds 33 ints.  Every thread gets the total.
+__device__ int block_sum(int v, int* s_red) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, n_warps = blockDim.x >> 5;
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    if (lane == 0) s_red[warp] = v;
+    __syncthreads();
+    if (warp == 0) {
+        int x = lane < n_warps ? s_red[lane] : 0;
+#pragma unroll
+        for (int o = 16; o >= 1; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+        if (lane == 0) s_red[32] = x;
+    }
+    __syncthreads();
+    const int total = s_red[32];
+    __syncthreads();
+    return total;
+}
+
+
 __global__ void __launch_bounds__(kThreads) layout_count_kernel(const LayoutParams p) {
     extern __shared__ __align__(16) uint32_t smem[];
     __shared__ int s_bad;
@@ -193,7 +214,10 @@ __global__ void __launch_bounds__(kThreads) layout_rows_kernel(const LayoutParam
             p.E, [&](int i) { return (ce[i] + a - 1) / a * a; }, [&](int i, int v) { eo[i] = v; },
             s_warp);
     }
-    if (tile >= p.num_tiles) return;
+    if (tile >= p.num_tiles) {
+        if (p.token_offset && p.num_tiles == 0 && threadIdx.x == 0) p.token_offset[0] = 0;
+        return;
+    }
 
     for (int r = threadIdx.x; r < R; r += kThreads)
         s_base[r] += p.ws_rank[static_cast<size_t>(r) * p.num_tiles + tile];
@@ -224,6 +248,33 @@ __global__ void __launch_bounds__(kThreads) layout_rows_kernel(const LayoutParam
         const bool in = (word >> b) & 1u;
         drow[j] = in ? s_base[r] + s_wpre[w * R + r] + __popc(word & ((1u << b) - 1u)) : -1;
         inr[j] = in ? 1 : 0;
+    }
+
+    // token_offset: rows numbered token by token.  The rows of tokens before
+    // this tile are the sum over ranks of the tile prefix of each rank.
+    if (p.token_offset) {
+        __shared__ int s_red[33];
+        __shared__ int s_ntok[kTileTokens];
+        int before = 0;
+        for (int r = threadIdx.x; r < R; r += kThreads)
+            before += p.ws_rank[static_cast<size_t>(r) * p.num_tiles + tile];
+        const int tile_base = block_sum(before, s_red);
+        if (threadIdx.x < nt) {
+            const int w = threadIdx.x >> 5;
+            const uint32_t b = threadIdx.x & 31;
+            int n = 0;
+            for (int r = 0; r < R; ++r) n += (s_bm[w * R + r] >> b) & 1u;
+            s_ntok[threadIdx.x] = n;
+        }
+        __syncthreads();
+        const bool last = tile == p.num_tiles - 1;
+        int32_t* to = p.token_offset + t0;
+        block_exclusive_scan(
+            nt, [&](int i) { return s_ntok[i]; },
+            [&](int i, int v) {
+                if (i < nt || last) to[i] = tile_base + v;
+            },
+            s_warp);
     }
 
     // src_dst_count[s][r]: tokens of source rank s (tokens [s*T/R, (s+1)*T/R)) in rank r.
@@ -266,7 +317,7 @@ constexpr int64_t kClusterMaxTokenRanks = EP_LAYOUT_CLUSTER_MAX_TOKEN_RANKS;
 // Shared-memory words of one cluster CTA for W bitmap words per rank.
 size_t cluster_smem_words(int R, int E, int nodes, int W) {
     return 2 * static_cast<size_t>(R) * W + static_cast<size_t>(nodes) * W + R + E + nodes + (R + 1) +
-           R + 64;
+           R + 32 * static_cast<size_t>(W) + 64;
 }
 
 // In-place exclusive scan of a[0, n) in shared memory by all kClusterThreads
@@ -318,6 +369,8 @@ __global__ void __launch_bounds__(kClusterThreads, 1)
     int* s_ncnt = s_hist + E;                                       // [NN] read by the last CTA
     int* s_tot = s_ncnt + NN;                                       // [R+1]
     int* s_before = s_tot + R + 1;                                  // [R]
+    int* s_ntok = s_before + R;                                     // [32 W] rows per token
+    __shared__ int s_red[33];
     const int tid = threadIdx.x;
     const int t0 = me * tokens_per_cta;
     const int nt = max(0, min(tokens_per_cta, p.T - t0));
@@ -450,6 +503,22 @@ __global__ void __launch_bounds__(kClusterThreads, 1)
                 inr[j0 + u] = static_cast<uint8_t>((in4 >> (8 * u)) & 1u);
             }
         }
+    }
+
+    // token_offset: rows of earlier CTAs' tokens + exclusive prefix of n(t) here.
+    if (p.token_offset) {
+        const int cta_base = block_sum(tid < R ? s_before[tid] : 0, s_red);
+        for (int tl = tid; tl < nt; tl += kClusterThreads) {
+            const int w = tl >> 5;
+            const uint32_t b = static_cast<uint32_t>(tl & 31);
+            int n = 0;
+            for (int r = 0; r < R; ++r) n += (s_bm[w * R + r] >> b) & 1u;
+            s_ntok[tl] = n;
+        }
+        __syncthreads();
+        smem_exclusive_scan(s_ntok, nt, s_warp);
+        for (int tl = tid; tl < nt; tl += kClusterThreads) p.token_offset[t0 + tl] = cta_base + s_ntok[tl];
+        if (me == C - 1 && tid == 0) p.token_offset[p.T] = n_recv;
     }
 
     // src_dst_count[s][r] += tokens of source rank s in this range that rank r receives.

@@ -94,6 +94,10 @@ typedef struct ep_layout {
                                              are rank_offset[r] + 0, 1, ... in ascending t */
     int32_t* src_dst_count;         /* [R,R] tokens of source rank s received by rank r,
                                              or NULL; needs R | T                        */
+    int32_t* token_offset;          /* [T+1] exclusive prefix over tokens of n(t) (rows
+                                             numbered token by token; [T] = N), or NULL.
+                                             When present, ep_dispatch uses it to give
+                                             every CTA the same number of rows          */
 } ep_layout_t;
 
 /* Bytes of device workspace ep_get_layout needs for these sizes (>= 16). */
@@ -118,8 +122,8 @@ int64_t ep_recv_capacity_bound(int num_tokens, int num_topk, int num_ranks);
  *                 ranks_per_node consecutive ranks, the tokens with any expert
  *                 in that group.
  * expert_alignment >= 1; only expert_offset uses it.
- * out             the layout arrays (num_tokens_per_node and src_dst_count may
- *                 be NULL; src_dst_count non-NULL needs R | T).
+ * out             the layout arrays (num_tokens_per_node, src_dst_count and
+ *                 token_offset may be NULL; src_dst_count non-NULL needs R | T).
  * workspace       device scratch of ws_bytes >= ep_layout_workspace_bytes(...);
  *                 its contents need no initialisation and are garbage after.
  * Results depend only on topk_idx (no atomics decide any order).

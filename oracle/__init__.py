@@ -37,7 +37,7 @@ def _load():
     vp = ctypes.c_void_p
     lib.ep_oracle_layout.restype = ctypes.c_int
     lib.ep_oracle_layout.argtypes = [vp, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
-                                     ctypes.c_int, ctypes.c_int] + [vp] * 10
+                                     ctypes.c_int, ctypes.c_int] + [vp] * 11
     lib.ep_oracle_dispatch.restype = ctypes.c_int
     lib.ep_oracle_dispatch.argtypes = [vp, vp, vp, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                        ctypes.c_int, ctypes.c_int, vp, vp, ctypes.c_int,
@@ -99,6 +99,7 @@ def layout(topk_idx, E, R, ranks_per_node=0, expert_alignment=1, with_src_dst=Tr
         expert_offset=np.zeros(E + 1, np.int32),
         dst_row=np.zeros((T, R), np.int32),
         src_dst_count=np.zeros((R, R), np.int32) if (with_src_dst and T % R == 0) else None,
+        token_offset=np.zeros(T + 1, np.int32),
     )
     scratch_local = np.zeros(max(T * R, 1), np.int32)
     scratch_mark = np.zeros(R + max(nodes, 1), np.uint8)
@@ -106,7 +107,7 @@ def layout(topk_idx, E, R, ranks_per_node=0, expert_alignment=1, with_src_dst=Tr
         _p(topk_idx), T, K, E, R, ranks_per_node, expert_alignment,
         _p(out.num_tokens_per_rank), _p(out.num_tokens_per_node), _p(out.num_tokens_per_expert),
         _p(out.is_token_in_rank), _p(out.rank_offset), _p(out.expert_offset), _p(out.dst_row),
-        _p(out.src_dst_count), _p(scratch_local), _p(scratch_mark))
+        _p(out.src_dst_count), _p(out.token_offset), _p(scratch_local), _p(scratch_mark))
     out.status = status
     return out
 

@@ -155,6 +155,7 @@ int ep_oracle_layout(const int64_t* topk_idx, int T, int K, int E, int R,
                      int32_t* expert_offset,           /* [E+1]          */
                      int32_t* dst_row,                 /* [T,R]          */
                      int32_t* src_dst_count,           /* [R,R] or NULL  */
+                     int32_t* token_offset,            /* [T+1] or NULL  */
                      int32_t* scratch_local,           /* [T,R] scratch  */
                      uint8_t* scratch_mark)            /* [R + nodes]    */
 {
@@ -213,6 +214,17 @@ int ep_oracle_layout(const int64_t* topk_idx, int T, int K, int E, int R,
             int32_t l = scratch_local[(int64_t)t * R + r];
             dst_row[(int64_t)t * R + r] = (l >= 0) ? rank_offset[r] + l : -1;
         }
+
+    /* Rows numbered token by token: token_offset[t] = sum over t' < t of
+     * the number of ranks that receive t'. */
+    if (token_offset) {
+        token_offset[0] = 0;
+        for (int t = 0; t < T; ++t) {
+            int n = 0;
+            for (int r = 0; r < R; ++r) n += is_token_in_rank[(int64_t)t * R + r];
+            token_offset[t + 1] = token_offset[t] + n;
+        }
+    }
 
     /* Source rank s owns tokens [s*T/R, (s+1)*T/R) (needs R | T). */
     if (src_dst_count) {

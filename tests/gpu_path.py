@@ -32,7 +32,7 @@ def run_layout(topk_idx, E, R, ranks_per_node=0, expert_alignment=1, with_src_ds
     # garbage in the workspace must not matter
     ws.fill_(0xA5)
     for t in (lay.num_tokens_per_rank, lay.num_tokens_per_expert, lay.rank_offset,
-              lay.expert_offset, lay.dst_row):
+              lay.expert_offset, lay.dst_row, lay.token_offset):
         t.fill_(-7)
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
     B.ep_get_layout(idx, E, R, lay, ws, status, ranks_per_node, expert_alignment)
@@ -42,7 +42,8 @@ def run_layout(topk_idx, E, R, ranks_per_node=0, expert_alignment=1, with_src_ds
 def layout_host(lay):
     out = {}
     for f in ("num_tokens_per_rank", "num_tokens_per_node", "num_tokens_per_expert",
-              "is_token_in_rank", "rank_offset", "expert_offset", "dst_row", "src_dst_count"):
+              "is_token_in_rank", "rank_offset", "expert_offset", "dst_row", "src_dst_count",
+              "token_offset"):
         v = getattr(lay, f)
         out[f] = None if v is None else v.cpu().numpy()
     return out

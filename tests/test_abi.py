@@ -50,7 +50,7 @@ def test_status_strings_and_sizes(lib):
     ws = lib.ep_layout_workspace_bytes(4096, 8, 256, 8, 0)
     tiles = 16
     assert ws >= 4 * tiles * (8 + 256 + 8 * 8)
-    assert lib.ep_abi_version() == 1
+    assert lib.ep_abi_version() == 2
 
 
 def test_host_checks_reject_before_any_launch(lib):
@@ -73,14 +73,14 @@ def test_host_checks_reject_before_any_launch(lib):
     assert f(None, 10, 8, 256, 8, 3, 1, ctypes.byref(L), None, 0, st, None) == B.EP_ERR_INVALID_ARG
     assert f(None, 10, 8, 256, 8, 0, 0, ctypes.byref(L), None, 0, st, None) == B.EP_ERR_INVALID_ARG
     # layout: arrays missing / misaligned
-    L2 = B.ep_layout_t(16, None, 32, 48, 64, 80, 96, None)
+    L2 = B.ep_layout_t(16, None, 32, 48, 64, 80, 96, None, None)
     assert f(vp(16), 10, 8, 256, 8, 0, 1, ctypes.byref(L2), None, 0, st, None) == B.EP_ERR_INVALID_ARG
-    L3 = B.ep_layout_t(16, None, 32, 48, 64, 80, 97, None)      # dst_row misaligned
+    L3 = B.ep_layout_t(16, None, 32, 48, 64, 80, 97, None, None)      # dst_row misaligned
     assert f(vp(16), 10, 8, 256, 8, 0, 1, ctypes.byref(L3), vp(256), 1 << 20, st, None) == B.EP_ERR_INVALID_ARG
     # workspace too small
     assert f(vp(16), 10, 8, 256, 8, 0, 1, ctypes.byref(L2), vp(256), 8, st, None) == B.EP_ERR_INVALID_ARG
     # src_dst_count needs R | T
-    L4 = B.ep_layout_t(16, None, 32, 48, 64, 80, 96, 112)
+    L4 = B.ep_layout_t(16, None, 32, 48, 64, 80, 96, 112, None)
     assert f(vp(16), 10, 8, 256, 8, 0, 1, ctypes.byref(L4), vp(256), 1 << 20, st, None) == B.EP_ERR_INVALID_ARG
     # dispatch
     d = lib.ep_dispatch

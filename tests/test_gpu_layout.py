@@ -9,7 +9,7 @@ from combine_ep_get_gb300.inputs import CONFIGS, make_config, make_inputs
 pytestmark = pytest.mark.gpu
 
 FIELDS = ("num_tokens_per_rank", "num_tokens_per_expert", "is_token_in_rank", "rank_offset",
-          "expert_offset", "dst_row")
+          "expert_offset", "dst_row", "token_offset")
 
 
 def _compare(idx, E, R, rpn=0, align=1):

@@ -49,7 +49,11 @@ def brute_layout(topk_idx, E, R, rpn=0, align=1):
     if T % R == 0:
         ts = T // R
         src_dst = np.array([member[s * ts:(s + 1) * ts].sum(axis=0) for s in range(R)]).reshape(R, R)
+    # rows numbered token by token: how many receive lists name each token
+    per_tok = np.bincount(np.concatenate(lists + [np.zeros(0, np.int64)]).astype(np.int64), minlength=T)
+    tok_off = np.concatenate([[0], np.cumsum(per_tok)])
     return dict(num_tokens_per_expert=cnt_e, num_tokens_per_rank=np.array([len(l) for l in lists]),
+                token_offset=tok_off,
                 rank_offset=np.array(starts), dst_row=dst, is_token_in_rank=member.astype(np.uint8),
                 expert_offset=exp_off, num_tokens_per_node=nodes, src_dst_count=src_dst,
                 invalid=bool(((topk_idx < -1) | (topk_idx >= E)).any()))
@@ -57,7 +61,7 @@ def brute_layout(topk_idx, E, R, rpn=0, align=1):
 
 def check_against(L, ref):
     for key in ("num_tokens_per_expert", "num_tokens_per_rank", "rank_offset", "dst_row",
-                "is_token_in_rank", "expert_offset"):
+                "is_token_in_rank", "expert_offset", "token_offset"):
         np.testing.assert_array_equal(getattr(L, key), ref[key], err_msg=key)
     if ref["num_tokens_per_node"] is not None:
         np.testing.assert_array_equal(L.num_tokens_per_node, ref["num_tokens_per_node"])
@@ -72,7 +76,7 @@ def test_handworked_example():
     L = oracle.layout(idx, g["E"], g["R"], g["ranks_per_node"], g["expert_alignment"])
     assert L.status == 0
     for key in ("num_tokens_per_expert", "num_tokens_per_rank", "num_tokens_per_node", "rank_offset",
-                "expert_offset", "is_token_in_rank", "dst_row", "src_dst_count"):
+                "expert_offset", "is_token_in_rank", "dst_row", "src_dst_count", "token_offset"):
         np.testing.assert_array_equal(getattr(L, key), np.array(g[key]), err_msg=key)
 
 
@@ -124,6 +128,7 @@ def _invariants(L, idx, E, R, rpn):
     n_t = L.is_token_in_rank.sum(axis=1)
     assert L.num_tokens_per_rank.sum() == L.rank_offset[-1] == n_t.sum()
     assert (np.diff(L.rank_offset) == L.num_tokens_per_rank).all()
+    assert (np.diff(L.token_offset) == n_t).all() and L.token_offset[-1] == L.rank_offset[-1]
     # each (t, r) in the rank has exactly one row; rows within a rank rise with t
     for r in range(R):
         rows = L.dst_row[:, r]

@@ -19,7 +19,7 @@ from combine_ep_get_gb300.inputs import make_inputs
 pytestmark = pytest.mark.gpu
 
 FIELDS = ("num_tokens_per_rank", "num_tokens_per_node", "num_tokens_per_expert", "is_token_in_rank",
-          "rank_offset", "expert_offset", "dst_row", "src_dst_count")
+          "rank_offset", "expert_offset", "dst_row", "src_dst_count", "token_offset")
 
 
 def _static_layout(B, idx, E, R, rpn):
