@@ -283,11 +283,11 @@ constexpr int kRegThreads = 256;
 constexpr int kRegUnroll = 4;
 
 // Register path: one CTA per (token, piece); each thread loads up to
-// kRegUnroll 16-byte vectors of the piece, then stores each to every
-// destination row.
-__global__ void __launch_bounds__(kRegThreads) dispatch_bf16_regs_kernel(const DispatchParams p) {
-    __shared__ int s_rows[EP_MAX_TOPK];
-    __shared__ int s_n;
+// kRegUnroll 16-byte vectors of the piece, its warp reads the token's
+// destination rows (one lane per rank) and broadcasts them by shuffles, and
+// the thread stores its vectors to every destination.  Warps never wait for
+// one another.
+__global__ void __launch_bounds__(kRegThreads, 6) dispatch_bf16_regs_kernel(const DispatchParams p) {
     const int64_t it = blockIdx.x;
     const int t = static_cast<int>(it / p.chunks);
     const int c = static_cast<int>(it - static_cast<int64_t>(t) * p.chunks);
@@ -298,33 +298,17 @@ __global__ void __launch_bounds__(kRegThreads) dispatch_bf16_regs_kernel(const D
     const uint32_t bytes = min(p.chunk_bytes, row_bytes - off);
     const int nvec = static_cast<int>(bytes / 16);
     const uint8_t* src = p.x + static_cast<int64_t>(t) * row_bytes + off;
-    // issue this thread's loads before anything waits
+    // this thread's loads and the warp's destination rows, all in flight together
     uint4 u[kRegUnroll];
 #pragma unroll
     for (int k = 0; k < kRegUnroll; ++k) {
         const int v = threadIdx.x + k * kRegThreads;
         if (v < nvec) u[k] = ld_stream_v4(src + static_cast<size_t>(v) * 16);
     }
-    if (warp == 0) {
-        int n = 0;
-        bool cap_bad = false;
-        for (int rb = 0; rb < p.R; rb += 32) {
-            const int r = rb + lane;
-            const int d = r < p.R ? p.dst_row[static_cast<int64_t>(t) * p.R + r] : -1;
-            const bool ok = d >= 0 && d < p.capacity;
-            if (d >= p.capacity) cap_bad = true;
-            const unsigned m = __ballot_sync(0xffffffffu, ok);
-            const int pos = n + __popc(m & ((1u << lane) - 1u));
-            if (ok && pos < EP_MAX_TOPK) s_rows[pos] = d;
-            n += __popc(m);
-        }
-        if (n > EP_MAX_TOPK) {
-            if (lane == 0) atomicOr(p.status, EP_ERR_INVALID_INDEX);
-            n = EP_MAX_TOPK;
-        }
-        if (lane == 0) s_n = n;
-        if (__any_sync(0xffffffffu, cap_bad) && lane == 0 && c == 0) atomicOr(p.status, EP_ERR_CAPACITY);
-    } else if (warp == 1 && c == 0) {
+    const int32_t* drow = p.dst_row + static_cast<int64_t>(t) * p.R;
+    const int d0 = lane < p.R ? drow[lane] : -1;
+    const int d1 = 32 + lane < p.R ? drow[32 + lane] : -1;   // ranks 32..63, same latency
+    if (warp == 1 && c == 0) {
         CtaWork all;
         all.first = 0;
         all.count = 0;
@@ -334,8 +318,7 @@ __global__ void __launch_bounds__(kRegThreads) dispatch_bf16_regs_kernel(const D
         all.balanced = 0;
         write_metadata(p, t, lane, all);
     }
-    __syncthreads();
-    const int n = s_n;
+    bool cap_bad = false;
     for (int base = 0; base < nvec; base += kRegUnroll * kRegThreads) {
         if (base > 0) {
 #pragma unroll
@@ -344,23 +327,31 @@ __global__ void __launch_bounds__(kRegThreads) dispatch_bf16_regs_kernel(const D
                 if (v < nvec) u[k] = ld_stream_v4(src + static_cast<size_t>(v) * 16);
             }
         }
-        for (int m = 0; m < n; ++m) {
-            uint8_t* dst = p.recv_x + static_cast<int64_t>(s_rows[m]) * row_bytes + off;
+        for (int rb = 0; rb < p.R; rb += 32) {
+            const int d = rb == 0 ? d0 : rb == 32 ? d1 : (rb + lane < p.R ? drow[rb + lane] : -1);
+            if (d >= p.capacity) cap_bad = true;
+            unsigned m = __ballot_sync(0xffffffffu, d >= 0 && d < p.capacity);
+            while (m) {
+                const int sl = __ffs(m) - 1;
+                m &= m - 1;
+                uint8_t* dst = p.recv_x + static_cast<int64_t>(__shfl_sync(0xffffffffu, d, sl)) * row_bytes + off;
 #pragma unroll
-            for (int k = 0; k < kRegUnroll; ++k) {
-                const int v = base + threadIdx.x + k * kRegThreads;
-                if (v < nvec) {
+                for (int k = 0; k < kRegUnroll; ++k) {
+                    const int v = base + threadIdx.x + k * kRegThreads;
+                    if (v < nvec) {
 #if EP_DISPATCH_STORE_CS
-                    st_cs_v4(dst + static_cast<size_t>(v) * 16, u[k]);
+                        st_cs_v4(dst + static_cast<size_t>(v) * 16, u[k]);
 #else
-                    st_v4(dst + static_cast<size_t>(v) * 16, u[k]);
+                        st_v4(dst + static_cast<size_t>(v) * 16, u[k]);
 #endif
+                    }
                 }
             }
         }
     }
+    if (warp == 0 && c == 0 && __any_sync(0xffffffffu, cap_bad) && lane == 0)
+        atomicOr(p.status, EP_ERR_CAPACITY);
 }
-
 #endif  // EP_DISPATCH_IMPL == 1
 
 

@@ -428,12 +428,16 @@ __global__ void __launch_bounds__(kClusterThreads, 1)
     cluster.sync();   // counts of every CTA visible; src_dst_count zeroed
 
     // Phase 2: rank totals, this CTA's base per rank, and (two CTAs) the outputs.
+    // Remote loads are issued for all CTAs before any is summed (one latency).
     for (int r = tid; r < R; r += kClusterThreads) {
+        int v[kMaxClusterCtas];
+#pragma unroll
+        for (int c = 0; c < kMaxClusterCtas; ++c) v[c] = c < C ? cluster.map_shared_rank(s_cnt, c)[r] : 0;
         int tot = 0, before = 0;
-        for (int c = 0; c < C; ++c) {
-            const int v = cluster.map_shared_rank(s_cnt, c)[r];
-            tot += v;
-            if (c < me) before += v;
+#pragma unroll
+        for (int c = 0; c < kMaxClusterCtas; ++c) {
+            tot += v[c];
+            if (c < me) before += v[c];
         }
         s_tot[r] = tot;
         s_before[r] = before;
@@ -447,14 +451,22 @@ __global__ void __launch_bounds__(kClusterThreads, 1)
     }
     if (me == C - 1) {
         for (int e = tid; e < E; e += kClusterThreads) {
+            int v[kMaxClusterCtas];
+#pragma unroll
+            for (int c = 0; c < kMaxClusterCtas; ++c) v[c] = c < C ? cluster.map_shared_rank(s_hist, c)[e] : 0;
             int tot = 0;
-            for (int c = 0; c < C; ++c) tot += cluster.map_shared_rank(s_hist, c)[e];
+#pragma unroll
+            for (int c = 0; c < kMaxClusterCtas; ++c) tot += v[c];
             p.num_tokens_per_expert[e] = tot;
             s_hist[e] = (tot + p.alignment - 1) / p.alignment * p.alignment;   // own slot only
         }
         for (int n = tid; n < NN; n += kClusterThreads) {
+            int v[kMaxClusterCtas];
+#pragma unroll
+            for (int c = 0; c < kMaxClusterCtas; ++c) v[c] = c < C ? cluster.map_shared_rank(s_ncnt, c)[n] : 0;
             int tot = 0;
-            for (int c = 0; c < C; ++c) tot += cluster.map_shared_rank(s_ncnt, c)[n];
+#pragma unroll
+            for (int c = 0; c < kMaxClusterCtas; ++c) tot += v[c];
             p.num_tokens_per_node[n] = tot;
         }
     }
