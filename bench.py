@@ -36,7 +36,10 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 L2_FLUSH_BYTES = 256 << 20
-KERNELS_PER_STEP = 5      # layout: count + scan + rows; dispatch: 1; combine: 1
+def kernels_per_step(T, R):
+    """Launches of this library per step: the layout is one cluster kernel, or
+    three tiled kernels when T*R is large; dispatch and combine one each."""
+    return (1 if T * R <= (1 << 19) else 3) + 2
 
 
 def parse_args(argv=None):
@@ -221,7 +224,7 @@ def run_ours(args):
     from combine_ep_get_gb300 import build as lib_build
     lib_build.build()
     from combine_ep_get_gb300 import binding as B
-    from combine_ep_get_gb300.inputs import CONFIGS, make_config
+    from combine_ep_get_gb300.inputs import CONFIGS, make_config, make_rows
 
     cfg = CONFIGS[args.workload]
     data = make_config(cfg)
@@ -241,21 +244,34 @@ def run_ours(args):
     status = torch.zeros(1, dtype=torch.int32, device=dev)
     B.ep_get_layout(idx, E, R, lay, ws, status, cfg.ranks_per_node)
     N = lay.num_recv            # one host read of rank_offset[R], before any timing
-    recv_x = torch.empty((N, H), dtype=torch.bfloat16, device=dev)
+    fp8, weighted = cfg.fp8, cfg.weighted
     recv_idx = torch.empty((N, K), dtype=torch.int32, device=dev)
     recv_w = torch.empty((N, K), dtype=torch.float32, device=dev)
     recv_src = torch.empty((N,), dtype=torch.int32, device=dev)
     out = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    if fp8:
+        # FP8 dispatch; the combine reads a bf16 stand-in for the expert outputs
+        recv_x = torch.empty((N, H), dtype=torch.uint8, device=dev)
+        recv_sf = torch.empty((N * (H // 128),), dtype=torch.float32, device=dev)
+        y = torch.from_numpy(make_rows(N, H, cfg.seed + 100).view(np.int16)).view(torch.bfloat16).to(dev)
+    else:
+        # identity expert: the combine reads the dispatched rows
+        recv_x = torch.empty((N, H), dtype=torch.bfloat16, device=dev)
+        recv_sf = None
+        y = recv_x
+    dtype_code = B.EP_FP8_E4M3 if fp8 else B.EP_BF16
+    w_comb = w if weighted else None
 
     def do_layout():
         B.ep_get_layout(idx, E, R, lay, ws, status, cfg.ranks_per_node)
 
     def do_dispatch():
-        B.ep_dispatch(x, idx, w, E, R, lay, recv_x, recv_idx, recv_w, recv_src, status)
+        B.ep_dispatch(x, idx, w, E, R, lay, recv_x, recv_idx, recv_w, recv_src, status, recv_sf=recv_sf,
+                      out_dtype=dtype_code)
 
     def do_combine():
-        B.ep_combine(recv_x, idx, None, E, R, lay, out, status)
+        B.ep_combine(y, idx, w_comb, E, R, lay, out, status)
 
     # eager warm-up (sets kernel attributes outside any capture)
     for _ in range(2):
@@ -269,17 +285,21 @@ def run_ours(args):
 
     use_graph = not args.no_graph
 
-    def step_body(ev):
+    def step_body(ev, split):
+        # split: an extra event between layout and dispatch (per-kernel
+        # breakdown); without it the dispatch launch overlaps the layout's
+        # tail (programmatic dependent launch), as in a real layer
         flush.zero_()
         ev[0].record()
         do_layout()
-        ev[1].record()
+        if split:
+            ev[4].record()
         do_dispatch()
-        ev[2].record()
+        ev[1].record()
         flush.zero_()
-        ev[3].record()
+        ev[2].record()
         do_combine()
-        ev[4].record()
+        ev[3].record()
 
     def new_events():
         if use_graph:
@@ -287,51 +307,65 @@ def run_ours(args):
         return [torch.cuda.Event(enable_timing=True) for _ in range(5)]
 
     # One CUDA graph per step holds the flushes, the three calls and the timing
-    # events; N_GRAPHS instances rotate so the GPU never waits for the host
+    # events; n_graphs instances rotate so the GPU never waits for the host
     # while the times of a finished instance are read.
     n_graphs = 4
-    slots = []
-    for _ in range(n_graphs):
-        ev = new_events()
-        g = None
-        if use_graph:
-            g = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(g):
-                step_body(ev)
-        slots.append((g, ev))
-    torch.cuda.synchronize()
 
-    times = []          # (layout, dispatch, combine) ms per timed step
+    def make_slots(split):
+        slots = []
+        for _ in range(n_graphs):
+            ev = new_events()
+            g = None
+            if use_graph:
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g):
+                    step_body(ev, split)
+            slots.append((g, ev))
+        return slots
 
-    def launch(k):
-        g, ev = slots[k]
-        if g is not None:
-            g.replay()
-        else:
-            step_body(ev)
+    def run(slots, split, steps, warm):
+        times = []
 
-    def harvest(k):
-        ev = slots[k][1]
-        ev[4].synchronize()
-        times.append((ev[0].elapsed_time(ev[1]), ev[1].elapsed_time(ev[2]), ev[3].elapsed_time(ev[4])))
+        def launch(k):
+            g, ev = slots[k]
+            if g is not None:
+                g.replay()
+            else:
+                step_body(ev, split)
 
-    for i in range(args.warmup):
-        launch(i % n_graphs)
+        def harvest(k):
+            ev = slots[k][1]
+            ev[3].synchronize()
+            t = [ev[0].elapsed_time(ev[1]), ev[2].elapsed_time(ev[3])]
+            if split:
+                t += [ev[0].elapsed_time(ev[4]), ev[4].elapsed_time(ev[1])]
+            times.append(t)
+
+        for i in range(warm):
+            launch(i % n_graphs)
+        torch.cuda.synchronize()
+        pending = []
+        for i in range(steps):
+            k = i % n_graphs
+            if len(pending) == n_graphs:
+                harvest(pending.pop(0))
+            launch(k)
+            pending.append(k)
+        for k in pending:
+            harvest(k)
+        torch.cuda.synchronize()
+        return times
+
+    main_slots = make_slots(False)
+    split_slots = make_slots(True)
     torch.cuda.synchronize()
     sampler = ClockSampler(local)
     sampler.start()
     time.sleep(0.25)
+    run(main_slots, False, 0, args.warmup)
     barrier(world)
     torch.cuda.synchronize()
-    pending = []
-    for i in range(args.steps):
-        k = i % n_graphs
-        if len(pending) == n_graphs:
-            harvest(pending.pop(0))
-        launch(k)
-        pending.append(k)
-    for k in pending:
-        harvest(k)
+    times = run(main_slots, False, args.steps, 0)          # the timed region
     torch.cuda.synchronize()
     barrier(world)
     time.sleep(0.15)
@@ -339,30 +373,38 @@ def run_ours(args):
     st = int(status.item())
     if st != 0:
         raise RuntimeError("device status after timing: %s" % B.ep_status_string(st))
+    # per-kernel breakdown (layout and dispatch apart), after the timed region
+    n_split = max(50, args.steps // 10)
+    split_times = run(split_slots, True, n_split, args.warmup)
 
-    t_layout = [t[0] for t in times]
-    t_dispatch = [t[1] for t in times]
-    t_combine = [t[2] for t in times]
-    local_total = sum(t_layout) + sum(t_dispatch) + sum(t_combine)
+    t_ld = [t[0] for t in times]
+    t_combine = [t[1] for t in times]
+    local_total = sum(t_ld) + sum(t_combine)
     max_total = reduce_max(local_total, world, dev)
 
-    nbytes = algorithmic_bytes(T, H, K, E, R, N)
+    nbytes = algorithmic_bytes(T, H, K, E, R, N, weighted=weighted, fp8=fp8)
     value_bps = replica_value(nbytes["total"], args.steps, max_total, world)
     tokens_ps = replica_value(T, args.steps, max_total, world)
     ms_per_step = max_total / args.steps
 
-    avg = {"layout": statistics.mean(t_layout), "dispatch": statistics.mean(t_dispatch),
-           "combine": statistics.mean(t_combine)}
+    avg = {"layout": statistics.mean(t[2] for t in split_times),
+           "dispatch": statistics.mean(t[3] for t in split_times),
+           "combine": statistics.mean(t_combine),
+           "layout+dispatch": statistics.mean(t_ld)}
+    source = {"layout": "breakdown pass", "dispatch": "breakdown pass", "combine": "timed region",
+              "layout+dispatch": "timed region"}
     dominant = "dispatch" if avg["dispatch"] >= avg["combine"] else "combine"
     peak, peak_kind = hbm_peak()
+    nbytes["layout+dispatch"] = nbytes["layout"] + nbytes["dispatch"]
     achieved = nbytes[dominant] / (avg[dominant] * 1e-3) / 1e9
     per_kernel = {k: {"ms": avg[k], "gbs": nbytes[k] / (avg[k] * 1e-3) / 1e9,
-                      "frac_of_" + peak_kind: nbytes[k] / (avg[k] * 1e-3) / 1e9 / peak}
+                      "frac_of_" + peak_kind: nbytes[k] / (avg[k] * 1e-3) / 1e9 / peak,
+                      "timed_in": source[k]}
                   for k in avg}
 
     # end to end through the public API with host buffers
-    e2e = run_e2e(args, B, torch, dev, x_host, idx_host, w_host, lay, ws, status, recv_x, recv_idx,
-                  recv_w, recv_src, out, cfg, nbytes, world)
+    e2e = run_e2e(args, B, torch, dev, x_host, idx_host, w_host, lay, ws, status, recv_x, recv_sf, y,
+                  recv_idx, recv_w, recv_src, out, cfg, nbytes, world)
 
     result = {
         "metric": "dispatch+combine GB/s and tokens/s on 1 GB300; % of HBM roofline",
@@ -375,7 +417,7 @@ def run_ours(args):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "bf16",
+        "dtype": "fp8_e4m3" if fp8 else "bf16",
         "data": "synthetic",
         "tokens_per_s": tokens_ps,
         "config": {
@@ -386,14 +428,18 @@ def run_ours(args):
             "l2": "flushed (256 MiB write) before layout and before combine, outside the timed events",
             "launch": ("one CUDA graph per step (flushes, calls and timing events inside)"
                        if use_graph else "eager"),
+            "arithmetic": ("fp8 e4m3 dispatch with fp32 per-128-channel scales; combine of bf16 "
+                           "stand-in expert rows, weighted, fp32 accumulate, bf16 out" if fp8 else
+                           "bf16 row copies; combine of the dispatched rows (identity expert), "
+                           "%s, fp32 accumulate, bf16 out" % ("weighted" if weighted else "unweighted")),
         },
         "per_kernel": per_kernel,
         "roofline": {"bound": "hbm", "kernel": dominant, "achieved": achieved, "peak": peak,
                      "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / peak,
                      "traffic": recorded_traffic(dominant, args.workload),
-                     "algorithmic_bytes_per_launch": nbytes[dominant]},
+                     "algorithmic_bytes_per_launch": nbytes[dominant], "timed_in": source[dominant]},
         "e2e": e2e,
-        "gpu_launches": KERNELS_PER_STEP * args.steps,
+        "gpu_launches": kernels_per_step(T, R) * args.steps,
         "clocks": clocks,
     }
     if world == 1 and rank == 0 and not args.no_cpu_baseline:
@@ -405,8 +451,8 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
-def run_e2e(args, B, torch, dev, x_host, idx_host, w_host, lay, ws, status, recv_x, recv_idx, recv_w,
-            recv_src, out, cfg, nbytes, world):
+def run_e2e(args, B, torch, dev, x_host, idx_host, w_host, lay, ws, status, recv_x, recv_sf, y, recv_idx,
+            recv_w, recv_src, out, cfg, nbytes, world):
     """End to end through the public calls with host buffers.
 
     Every step copies its inputs (x, topk_idx, topk_weights) from pinned host
@@ -442,8 +488,8 @@ def run_e2e(args, B, torch, dev, x_host, idx_host, w_host, lay, ws, status, recv
         s_comp.wait_event(ev_out[b])             # step i-2's output has been copied out
         B.ep_get_layout(idd[b], E, R, lay, ws, status, cfg.ranks_per_node, stream=s_comp)
         B.ep_dispatch(xd[b], idd[b], wd[b], E, R, lay, recv_x, recv_idx, recv_w, recv_src, status,
-                      stream=s_comp)
-        B.ep_combine(recv_x, idd[b], None, E, R, lay, outd[b], status, stream=s_comp)
+                      recv_sf=recv_sf, out_dtype=B.EP_FP8_E4M3 if cfg.fp8 else B.EP_BF16, stream=s_comp)
+        B.ep_combine(y, idd[b], wd[b] if cfg.weighted else None, E, R, lay, outd[b], status, stream=s_comp)
         ev_comp[b].record(s_comp)
         with torch.cuda.stream(s_out):
             s_out.wait_event(ev_comp[b])

@@ -43,6 +43,7 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(const CombineParams p
     const int64_t it = blockIdx.x;
     const int t = static_cast<int>(it / p.chunks);
     const int c = static_cast<int>(it - static_cast<int64_t>(t) * p.chunks);
+    pdl_wait();
 
     if (threadIdx.x < 32) {
         const int lane = threadIdx.x;
@@ -302,10 +303,8 @@ cudaError_t launch_combine(CombineParams p, bool weighted, cudaStream_t stream) 
     const int64_t grid = static_cast<int64_t>(p.T) * chunks;
     if (grid < 1) return cudaSuccess;
     if (weighted)
-        combine_kernel<true><<<static_cast<unsigned>(grid), kThreads, 0, stream>>>(p);
-    else
-        combine_kernel<false><<<static_cast<unsigned>(grid), kThreads, 0, stream>>>(p);
-    return cudaGetLastError();
+        return launch_pdl(combine_kernel<true>, dim3(static_cast<unsigned>(grid)), dim3(kThreads), 0, stream, p);
+    return launch_pdl(combine_kernel<false>, dim3(static_cast<unsigned>(grid)), dim3(kThreads), 0, stream, p);
 }
 
 }  // namespace epg

@@ -174,6 +174,7 @@ __global__ void __launch_bounds__(kBf16Threads) dispatch_bf16_kernel(const Dispa
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const uint32_t row_bytes = static_cast<uint32_t>(p.H) * 2u;
+    pdl_wait();
 
     if (warp == 0) {
         CtaWork w;
@@ -298,6 +299,7 @@ __global__ void __launch_bounds__(kRegThreads, 6) dispatch_bf16_regs_kernel(cons
     const uint32_t bytes = min(p.chunk_bytes, row_bytes - off);
     const int nvec = static_cast<int>(bytes / 16);
     const uint8_t* src = p.x + static_cast<int64_t>(t) * row_bytes + off;
+    pdl_wait();   // before any global access: the previous kernel may write x
     // this thread's loads and the warp's destination rows, all in flight together
     uint4 u[kRegUnroll];
 #pragma unroll
@@ -373,6 +375,7 @@ __global__ void __launch_bounds__(kFp8Threads) dispatch_fp8_kernel(const Dispatc
     const int c = static_cast<int>(it - static_cast<int64_t>(t) * p.chunks);
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+    pdl_wait();
 
     if (warp == 0) {
         int n = 0;
@@ -480,8 +483,8 @@ cudaError_t launch_dispatch_bf16(DispatchParams p, cudaStream_t stream) {
         p.chunk_bytes = cb;
         const int64_t g = static_cast<int64_t>(p.T) * p.chunks;
         if (g < 1) return cudaSuccess;
-        dispatch_bf16_regs_kernel<<<static_cast<unsigned>(g), kRegThreads, 0, stream>>>(p);
-        return cudaGetLastError();
+        return launch_pdl(dispatch_bf16_regs_kernel, dim3(static_cast<unsigned>(g)), dim3(kRegThreads), 0, stream,
+                          p);
     }
 #endif
     int chunks = static_cast<int>((row_bytes + EP_DISPATCH_PIECE_MAX - 1) / EP_DISPATCH_PIECE_MAX);
@@ -518,8 +521,8 @@ cudaError_t launch_dispatch_bf16(DispatchParams p, cudaStream_t stream) {
     int64_t grid = static_cast<int64_t>(di.num_sms) * blocks_per_sm;
     if (grid > num_items) grid = num_items;
     if (grid < 1) return cudaSuccess;
-    dispatch_bf16_kernel<<<static_cast<unsigned>(grid), kBf16Threads, smem, stream>>>(p);
-    return cudaGetLastError();
+    return launch_pdl(dispatch_bf16_kernel, dim3(static_cast<unsigned>(grid)), dim3(kBf16Threads), smem, stream,
+                      p);
 }
 
 cudaError_t launch_dispatch_fp8(DispatchParams p, cudaStream_t stream) {
@@ -541,8 +544,7 @@ cudaError_t launch_dispatch_fp8(DispatchParams p, cudaStream_t stream) {
     p.chunk_blocks = chunk_blocks;
     const int64_t grid = static_cast<int64_t>(p.T) * chunks;
     if (grid < 1) return cudaSuccess;
-    dispatch_fp8_kernel<<<static_cast<unsigned>(grid), kFp8Threads, 0, stream>>>(p);
-    return cudaGetLastError();
+    return launch_pdl(dispatch_fp8_kernel, dim3(static_cast<unsigned>(grid)), dim3(kFp8Threads), 0, stream, p);
 }
 
 }  // namespace epg

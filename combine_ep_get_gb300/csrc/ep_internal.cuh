@@ -5,6 +5,7 @@
 
 #include <cstdint>
 #include <cstddef>
+#include <utility>
 #include <cuda_runtime.h>
 
 #include "../../include/ep_get.h"
@@ -88,6 +89,26 @@ cudaError_t launch_dispatch_bf16(DispatchParams p, cudaStream_t stream);
 cudaError_t launch_dispatch_fp8(DispatchParams p, cudaStream_t stream);
 cudaError_t launch_combine(CombineParams p, bool weighted, cudaStream_t stream);
 
+// Launch with programmatic dependent launch allowed: the kernel may begin
+// while the previous kernel on the stream is still running, and must call
+// pdl_wait() before it reads anything that kernel writes.  After any other
+// stream operation the attribute has no effect.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                       Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
 // Workspace carve-up shared by the size query and the launcher.
 struct LayoutWorkspace {
     size_t off_rank, off_expert, off_node, off_bitmap, total;
@@ -100,6 +121,16 @@ LayoutWorkspace layout_workspace(int T, int E, int R, int num_nodes);
 
 // A bounded wait gives up after this many nanoseconds of %globaltimer.
 constexpr uint64_t kWaitTimeoutNs = 2000000000ull;
+
+// Wait until the kernel this one depends on (previous on the stream) has
+// completed and its writes are visible; returns at once without a dependency.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// Allow the next kernel on the stream to be scheduled now (it still waits in
+// pdl_wait() for this kernel to complete before reading its outputs).
+__device__ __forceinline__ void pdl_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
 
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));

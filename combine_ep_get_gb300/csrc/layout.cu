@@ -70,6 +70,7 @@ __global__ void __launch_bounds__(kThreads) layout_count_kernel(const LayoutPara
     int* s_hist = reinterpret_cast<int*>(s_bm_node + p.num_nodes * kTileWords);  // [E]
     const int tile = blockIdx.x;
     const int n_words = R * kTileWords + p.num_nodes * kTileWords + p.E;
+    pdl_wait();   // first: the previous kernel may write topk_idx or read our outputs
 
     // The src_dst_count output is accumulated by the rows kernel: zero it here.
     if (p.src_dst_count) {
@@ -132,6 +133,7 @@ __global__ void __launch_bounds__(kThreads) layout_count_kernel(const LayoutPara
 
 // One warp per column: ranks [0,R), experts [R, R+E), nodes [R+E, R+E+nodes).
 __global__ void __launch_bounds__(kThreads) layout_scan_kernel(const LayoutParams p) {
+    pdl_wait();
     const int col = (blockIdx.x * kThreads + threadIdx.x) >> 5;
     const int lane = threadIdx.x & 31;
     const int n_cols = p.R + p.E + p.num_nodes;
@@ -201,6 +203,8 @@ __global__ void __launch_bounds__(kThreads) layout_rows_kernel(const LayoutParam
     uint32_t* s_bm = smem + (R + 1);                             // [kTileWords][R]
     int* s_wpre = reinterpret_cast<int*>(s_bm + R * kTileWords);  // [kTileWords][R]
     const int tile = blockIdx.x;
+    pdl_wait();
+    pdl_launch_dependents();   // the next kernel may be scheduled; it waits for our completion
 
     const int32_t* cnt = p.num_tokens_per_rank;
     block_exclusive_scan(R, [&](int i) { return cnt[i]; }, [&](int i, int v) { s_base[i] = v; },
@@ -374,6 +378,8 @@ __global__ void __launch_bounds__(kClusterThreads, 1)
     const int tid = threadIdx.x;
     const int t0 = me * tokens_per_cta;
     const int nt = max(0, min(tokens_per_cta, p.T - t0));
+    pdl_wait();
+    pdl_launch_dependents();   // the next kernel may be scheduled; it waits for our completion
 
     for (int i = tid; i < R * W; i += kClusterThreads) s_bm[i] = 0u;
     for (int i = tid; i < NN * W; i += kClusterThreads) s_bmn[i] = 0u;
@@ -627,19 +633,24 @@ cudaError_t launch_layout(const LayoutParams& p, cudaStream_t stream) {
     const ClusterPlan plan = cluster_ok ? plan_cluster(p, di) : ClusterPlan{0, 0, 0};
     if (plan.ctas > 0) {
         cudaLaunchConfig_t cfg = {};
-        cudaLaunchAttribute attr[1];
+        cudaLaunchAttribute attr[2];
         attr[0].id = cudaLaunchAttributeClusterDimension;
         attr[0].val.clusterDim.x = plan.ctas;
         attr[0].val.clusterDim.y = 1;
         attr[0].val.clusterDim.z = 1;
+        attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[1].val.programmaticStreamSerializationAllowed = 1;
         cfg.gridDim = dim3(plan.ctas);
         cfg.blockDim = dim3(kClusterThreads);
         cfg.dynamicSmemBytes = plan.smem;
         cfg.stream = stream;
         cfg.attrs = attr;
-        cfg.numAttrs = 1;
+        cfg.numAttrs = 2;
         int max_clusters = 0;
-        if (cudaOccupancyMaxActiveClusters(&max_clusters, layout_cluster_kernel, &cfg) == cudaSuccess &&
+        cfg.numAttrs = 1;   // the occupancy query takes the cluster shape only
+        const bool fits = cudaOccupancyMaxActiveClusters(&max_clusters, layout_cluster_kernel, &cfg) == cudaSuccess;
+        cfg.numAttrs = 2;
+        if (fits &&
             max_clusters >= 1) {
             return cudaLaunchKernelEx(&cfg, layout_cluster_kernel, p, plan.tokens_per_cta);
         }
@@ -650,12 +661,13 @@ cudaError_t launch_layout(const LayoutParams& p, cudaStream_t stream) {
         4 * (static_cast<size_t>(p.R) * kTileWords + static_cast<size_t>(p.num_nodes) * kTileWords + p.E);
     const size_t smem_rows = 4 * (static_cast<size_t>(p.R) + 1 + 2 * static_cast<size_t>(p.R) * kTileWords);
     const int grid_tiles = p.num_tiles > 0 ? p.num_tiles : 1;
-    layout_count_kernel<<<grid_tiles, kThreads, smem_count, stream>>>(p);
+    cudaError_t e = launch_pdl(layout_count_kernel, dim3(grid_tiles), dim3(kThreads), smem_count, stream, p);
+    if (e != cudaSuccess) return e;
     const int n_cols = p.R + p.E + p.num_nodes;
     const int scan_blocks = (n_cols * 32 + kThreads - 1) / kThreads;
-    layout_scan_kernel<<<scan_blocks, kThreads, 0, stream>>>(p);
-    layout_rows_kernel<<<grid_tiles, kThreads, smem_rows, stream>>>(p);
-    return cudaGetLastError();
+    e = launch_pdl(layout_scan_kernel, dim3(scan_blocks), dim3(kThreads), 0, stream, p);
+    if (e != cudaSuccess) return e;
+    return launch_pdl(layout_rows_kernel, dim3(grid_tiles), dim3(kThreads), smem_rows, stream, p);
 }
 
 }  // namespace epg
