@@ -8,8 +8,8 @@
 // One CTA of 128 threads per (token, piece of the row).  Warp 0 compacts the
 // token's receive rows (ascending rank) and coefficients into shared memory;
 // then every thread owns 16-byte vectors of the piece and issues the loads of
-// up to 8 source rows back to back (read-only, no L1 allocation) before
-// accumulating, so each thread keeps up to 128 bytes of reads in flight.  The
+// up to 4 source rows back to back (read-only, no L1 allocation) before
+// accumulating (64 bytes of reads in flight per thread, 12 CTAs per SM).  The
 // reduced vector is rounded to bf16 and stored once.  HBM-bound: reads are
 // ~n(t) times the writes.
 #include <cuda_bf16.h>
@@ -19,24 +19,21 @@
 namespace epg {
 namespace {
 
-#ifndef EP_COMBINE_IMPL
-#define EP_COMBINE_IMPL 0            // 0: CTA per (token, piece); 1: warp per (token, piece)
+// Compile-time tuning (defaults are the measured best on GB300).
+#ifndef EP_COMBINE_THREADS
+#define EP_COMBINE_THREADS 128       // threads per CTA
 #endif
-#ifndef EP_COMBINE_WARP_VPL
-#define EP_COMBINE_WARP_VPL 2        // warp path: 16-byte vectors per lane per pass
+#ifndef EP_COMBINE_MIN_BLOCKS
+#define EP_COMBINE_MIN_BLOCKS 12     // __launch_bounds__ minimum resident CTAs per SM (<= 40 registers)
 #endif
-#ifndef EP_COMBINE_WARP_PASSES
-#define EP_COMBINE_WARP_PASSES 4     // warp path: passes per piece
-#endif
-
-constexpr int kThreads = 128;
+constexpr int kThreads = EP_COMBINE_THREADS;
 #ifndef EP_COMBINE_BATCH
-#define EP_COMBINE_BATCH 8
+#define EP_COMBINE_BATCH 4
 #endif
 constexpr int kBatch = EP_COMBINE_BATCH;
 
 template <bool kWeighted>
-__global__ void __launch_bounds__(kThreads) combine_kernel(const CombineParams p) {
+__global__ void __launch_bounds__(kThreads, EP_COMBINE_MIN_BLOCKS) combine_kernel(const CombineParams p) {
     __shared__ int s_rows[EP_MAX_TOPK];
     __shared__ float s_coef[EP_MAX_TOPK];
     __shared__ int s_n;
@@ -135,158 +132,12 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(const CombineParams p
     }
 }
 
-#if EP_COMBINE_IMPL == 1
-constexpr int kWarpThreads = 256;
-constexpr int kVpl = EP_COMBINE_WARP_VPL;
-constexpr int kPasses = EP_COMBINE_WARP_PASSES;
-
-// Warp path: each warp owns one (token, piece of 32 * kVpl * kPasses vectors).
-// Lane r of the warp reads the token's row on rank r (and its coefficient);
-// members are broadcast by shuffles; every lane keeps kVpl vectors x up to
-// kBatch members of loads in flight before accumulating.  No block barrier.
-template <bool kWeighted>
-__global__ void __launch_bounds__(kWarpThreads) combine_warp_kernel(const CombineParams p) {
-    const int warp = threadIdx.x >> 5;
-    const int lane = threadIdx.x & 31;
-    const int64_t it = static_cast<int64_t>(blockIdx.x) * (kWarpThreads / 32) + warp;
-    if (it >= static_cast<int64_t>(p.T) * p.chunks) return;
-    const int t = static_cast<int>(it / p.chunks);
-    const int c = static_cast<int>(it - static_cast<int64_t>(t) * p.chunks);
-    const int64_t row_bytes = static_cast<int64_t>(p.H) * 2;
-    const int n_vec = p.H / 8;
-    const int v_begin = c * p.chunk_vecs;
-    const int v_end = min(n_vec, v_begin + p.chunk_vecs);
-
-    int64_t e_l = -1;
-    float w_l = 0.0f;
-    if (kWeighted && lane < p.K) {
-        e_l = p.topk_idx[static_cast<int64_t>(t) * p.K + lane];
-        w_l = p.topk_weights[static_cast<int64_t>(t) * p.K + lane];
-    }
-    // rows and coefficients of the (at most 32) members, lane j holding member j
-    int my_row = 0;
-    float my_coef = 0.0f;
-    int n = 0;
-    bool cap_bad = false;
-    for (int rb = 0; rb < p.R; rb += 32) {
-        const int r = rb + lane;
-        const int d = r < p.R ? p.dst_row[static_cast<int64_t>(t) * p.R + r] : -1;
-        const bool ok = d >= 0 && d < p.num_y_rows;
-        if (d >= p.num_y_rows) cap_bad = true;
-        float coef = 1.0f;
-        if (kWeighted) {
-            coef = 0.0f;
-            for (int k = 0; k < p.K; ++k) {
-                const int64_t e = __shfl_sync(0xffffffffu, e_l, k);
-                const float w = __shfl_sync(0xffffffffu, w_l, k);
-                if (e >= 0 && e < p.E && static_cast<int>(e) / p.experts_per_rank == r) coef += w;
-            }
-        }
-        unsigned m = __ballot_sync(0xffffffffu, ok);
-        while (m) {
-            const int sl = __ffs(m) - 1;
-            m &= m - 1;
-            const int dd = __shfl_sync(0xffffffffu, d, sl);
-            const float cc = __shfl_sync(0xffffffffu, coef, sl);
-            if (lane == n) {
-                my_row = dd;
-                my_coef = cc;
-            }
-            ++n;
-            if (n > 32) break;
-        }
-        if (n > 32) break;
-    }
-    if (n > 32) {
-        if (lane == 0) atomicOr(p.status, EP_ERR_INVALID_INDEX);
-        n = 32;
-    }
-    if (__any_sync(0xffffffffu, cap_bad) && lane == 0 && c == 0) atomicOr(p.status, EP_ERR_CAPACITY);
-
-    for (int pass = 0; pass < kPasses; ++pass) {
-        const int v0 = v_begin + pass * 32 * kVpl + lane;
-        if (v_begin + pass * 32 * kVpl >= v_end) break;
-        float acc[kVpl][8];
-#pragma unroll
-        for (int q = 0; q < kVpl; ++q)
-#pragma unroll
-            for (int e = 0; e < 8; ++e) acc[q][e] = 0.0f;
-        for (int j0 = 0; j0 < n; j0 += kBatch) {
-            uint4 buf[kBatch][kVpl];
-#pragma unroll
-            for (int j = 0; j < kBatch; ++j) {
-                const int row = __shfl_sync(0xffffffffu, my_row, (j0 + j) & 31);
-                if (j0 + j < n) {
-                    const uint8_t* yr = p.y + static_cast<int64_t>(row) * row_bytes;
-#pragma unroll
-                    for (int q = 0; q < kVpl; ++q) {
-                        const int v = v0 + 32 * q;
-                        if (v < v_end) buf[j][q] = ld_stream_v4(yr + static_cast<int64_t>(v) * 16);
-                    }
-                }
-            }
-#pragma unroll
-            for (int j = 0; j < kBatch; ++j) {
-                const float cf = __shfl_sync(0xffffffffu, my_coef, (j0 + j) & 31);
-                if (j0 + j < n) {
-#pragma unroll
-                    for (int q = 0; q < kVpl; ++q) {
-                        const uint32_t w[4] = {buf[j][q].x, buf[j][q].y, buf[j][q].z, buf[j][q].w};
-#pragma unroll
-                        for (int h = 0; h < 4; ++h) {
-                            const float lo = __uint_as_float(w[h] << 16);
-                            const float hi = __uint_as_float(w[h] & 0xffff0000u);
-                            if (kWeighted) {
-                                acc[q][2 * h] = fmaf(cf, lo, acc[q][2 * h]);
-                                acc[q][2 * h + 1] = fmaf(cf, hi, acc[q][2 * h + 1]);
-                            } else {
-                                acc[q][2 * h] += lo;
-                                acc[q][2 * h + 1] += hi;
-                            }
-                        }
-                    }
-                }
-            }
-        }
-#pragma unroll
-        for (int q = 0; q < kVpl; ++q) {
-            const int v = v0 + 32 * q;
-            if (v < v_end) {
-                uint4 o;
-                uint32_t* ow = reinterpret_cast<uint32_t*>(&o);
-#pragma unroll
-                for (int h = 0; h < 4; ++h) {
-                    const __nv_bfloat162 b2 = __floats2bfloat162_rn(acc[q][2 * h], acc[q][2 * h + 1]);
-                    ow[h] = *reinterpret_cast<const uint32_t*>(&b2);
-                }
-                st_v4(p.out + static_cast<int64_t>(t) * row_bytes + static_cast<int64_t>(v) * 16, o);
-            }
-        }
-    }
-}
-#endif  // EP_COMBINE_IMPL == 1
 
 }  // namespace
 
 cudaError_t launch_combine(CombineParams p, bool weighted, cudaStream_t stream) {
     const DeviceInfo& di = device_info();
     const int n_vec = p.H / 8;
-#if EP_COMBINE_IMPL == 1
-    {
-        const int piece = 32 * kVpl * kPasses;
-        p.chunks = (n_vec + piece - 1) / piece;
-        p.chunk_vecs = piece;
-        (void)di;
-        const int64_t items = static_cast<int64_t>(p.T) * p.chunks;
-        const int64_t g = (items + kWarpThreads / 32 - 1) / (kWarpThreads / 32);
-        if (g < 1) return cudaSuccess;
-        if (weighted)
-            combine_warp_kernel<true><<<static_cast<unsigned>(g), kWarpThreads, 0, stream>>>(p);
-        else
-            combine_warp_kernel<false><<<static_cast<unsigned>(g), kWarpThreads, 0, stream>>>(p);
-        return cudaGetLastError();
-    }
-#endif
     // Pieces of up to 2 vectors per thread; more pieces when there are few tokens.
     int chunks = (n_vec + 2 * kThreads - 1) / (2 * kThreads);
     const int want_items = 4 * di.num_sms;
