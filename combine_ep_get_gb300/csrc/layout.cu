@@ -321,7 +321,7 @@ constexpr int64_t kClusterMaxTokenRanks = EP_LAYOUT_CLUSTER_MAX_TOKEN_RANKS;
 // Shared-memory words of one cluster CTA for W bitmap words per rank.
 size_t cluster_smem_words(int R, int E, int nodes, int W) {
     return 2 * static_cast<size_t>(R) * W + static_cast<size_t>(nodes) * W + R + E + nodes + (R + 1) +
-           R + 32 * static_cast<size_t>(W) + 64;
+           R + 33 * static_cast<size_t>(W) + 64;
 }
 
 // In-place exclusive scan of a[0, n) in shared memory by all kClusterThreads
@@ -373,8 +373,10 @@ __global__ void __launch_bounds__(kClusterThreads, 1)
     int* s_ncnt = s_hist + E;                                       // [NN] read by the last CTA
     int* s_tot = s_ncnt + NN;                                       // [R+1]
     int* s_before = s_tot + R + 1;                                  // [R]
-    int* s_ntok = s_before + R;                                     // [32 W] rows per token
-    __shared__ int s_red[33];
+    int* s_ntok = s_before + R;                                     // [32 W] token's row within its word
+    int* s_wtok = s_ntok + 32 * W;                                  // [W] rows of earlier words
+    __shared__ int s_rows_total;                                    // read by later CTAs
+    __shared__ int s_cta_base;
     const int tid = threadIdx.x;
     const int t0 = me * tokens_per_cta;
     const int nt = max(0, min(tokens_per_cta, p.T - t0));
@@ -430,7 +432,27 @@ __global__ void __launch_bounds__(kClusterThreads, 1)
         for (int w = 0; w < W; ++w) c += __popc(s_bmn[w * NN + n]);
         s_ncnt[n] = c;
     }
+    // Rows numbered token by token: one warp per 32-token word, lane = token.
+    const int warp_id = tid >> 5, lane = tid & 31;
+    for (int w = warp_id; w < W; w += kClusterThreads / 32) {
+        int n = 0;
+        for (int r = 0; r < R; ++r) n += (s_bm[w * R + r] >> lane) & 1u;
+        const int incl = warp_inclusive_scan(n);
+        s_ntok[w * 32 + lane] = incl - n;
+        if (lane == 31) s_wtok[w] = incl;
+    }
     if (tid == 0 && s_bad) atomicOr(p.status, EP_ERR_INVALID_INDEX);
+    __syncthreads();
+    if (warp_id == 0) {
+        int carry = 0;
+        for (int base = 0; base < W; base += 32) {
+            const int v = base + lane < W ? s_wtok[base + lane] : 0;
+            const int incl = warp_inclusive_scan(v);
+            if (base + lane < W) s_wtok[base + lane] = carry + incl - v;
+            carry += __shfl_sync(0xffffffffu, incl, 31);
+        }
+        if (lane == 0) s_rows_total = carry;
+    }
     cluster.sync();   // counts of every CTA visible; src_dst_count zeroed
 
     // Phase 2: rank totals, this CTA's base per rank, and (two CTAs) the outputs.
@@ -449,6 +471,21 @@ __global__ void __launch_bounds__(kClusterThreads, 1)
         s_before[r] = before;
         if (me == 0) p.num_tokens_per_rank[r] = tot;
     }
+    if (warp_id == 1) {
+        const int v = lane < me ? *cluster.map_shared_rank(&s_rows_total, lane) : 0;
+        const int sum = warp_inclusive_scan(v);
+        if (lane == 31) s_cta_base = sum;
+    }
+    // expert totals: CTA c sums experts [c E / C, (c+1) E / C) over all CTAs
+    for (int e = me * E / C + tid; e < (me + 1) * E / C; e += kClusterThreads) {
+        int v[kMaxClusterCtas];
+#pragma unroll
+        for (int c = 0; c < kMaxClusterCtas; ++c) v[c] = c < C ? cluster.map_shared_rank(s_hist, c)[e] : 0;
+        int tot = 0;
+#pragma unroll
+        for (int c = 0; c < kMaxClusterCtas; ++c) tot += v[c];
+        p.num_tokens_per_expert[e] = tot;
+    }
     __syncthreads();
     const int n_recv = smem_exclusive_scan(s_tot, R, s_warp);   // s_tot = rank_offset
     if (me == 0) {
@@ -456,16 +493,6 @@ __global__ void __launch_bounds__(kClusterThreads, 1)
         if (tid == 0) p.rank_offset[R] = n_recv;
     }
     if (me == C - 1) {
-        for (int e = tid; e < E; e += kClusterThreads) {
-            int v[kMaxClusterCtas];
-#pragma unroll
-            for (int c = 0; c < kMaxClusterCtas; ++c) v[c] = c < C ? cluster.map_shared_rank(s_hist, c)[e] : 0;
-            int tot = 0;
-#pragma unroll
-            for (int c = 0; c < kMaxClusterCtas; ++c) tot += v[c];
-            p.num_tokens_per_expert[e] = tot;
-            s_hist[e] = (tot + p.alignment - 1) / p.alignment * p.alignment;   // own slot only
-        }
         for (int n = tid; n < NN; n += kClusterThreads) {
             int v[kMaxClusterCtas];
 #pragma unroll
@@ -476,8 +503,13 @@ __global__ void __launch_bounds__(kClusterThreads, 1)
             p.num_tokens_per_node[n] = tot;
         }
     }
-    cluster.sync();   // every remote read done: shared memory may be reused / released
+    cluster.sync();   // every remote read done; every CTA's expert totals are in global memory
     if (me == C - 1) {
+        for (int e = tid; e < E; e += kClusterThreads) {
+            const int tot = __ldcg(p.num_tokens_per_expert + e);
+            s_hist[e] = (tot + p.alignment - 1) / p.alignment * p.alignment;
+        }
+        __syncthreads();
         const int tot = smem_exclusive_scan(s_hist, E, s_warp);
         for (int e = tid; e < E; e += kClusterThreads) p.expert_offset[e] = s_hist[e];
         if (tid == 0) p.expert_offset[E] = tot;
@@ -523,19 +555,11 @@ __global__ void __launch_bounds__(kClusterThreads, 1)
         }
     }
 
-    // token_offset: rows of earlier CTAs' tokens + exclusive prefix of n(t) here.
+    // token_offset: rows of earlier CTAs' tokens + rows of earlier words + row in word.
     if (p.token_offset) {
-        const int cta_base = block_sum(tid < R ? s_before[tid] : 0, s_red);
-        for (int tl = tid; tl < nt; tl += kClusterThreads) {
-            const int w = tl >> 5;
-            const uint32_t b = static_cast<uint32_t>(tl & 31);
-            int n = 0;
-            for (int r = 0; r < R; ++r) n += (s_bm[w * R + r] >> b) & 1u;
-            s_ntok[tl] = n;
-        }
-        __syncthreads();
-        smem_exclusive_scan(s_ntok, nt, s_warp);
-        for (int tl = tid; tl < nt; tl += kClusterThreads) p.token_offset[t0 + tl] = cta_base + s_ntok[tl];
+        const int cta_base = s_cta_base;
+        for (int tl = tid; tl < nt; tl += kClusterThreads)
+            p.token_offset[t0 + tl] = cta_base + s_wtok[tl >> 5] + s_ntok[tl];
         if (me == C - 1 && tid == 0) p.token_offset[p.T] = n_recv;
     }
 
