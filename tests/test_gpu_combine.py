@@ -37,6 +37,8 @@ def _check_close(gpu_bits, ref, bound):
     (777, 2048, 64, 6, 16, 0.2, True),
     (300, 8, 32, 2, 32, 0.0, False),
     (33, 4096, 128, 8, 64, 0.05, True),
+    (300, 512, 256, 8, 128, 0.0, True),      # more than 64 ranks
+    (200, 256, 2048, 32, 1024, 0.1, True),   # the limits: 1024 ranks, top-32
 ])
 def test_combine_random_rows(T, H, E, K, R, mask, weighted):
     from gpu_path import bf16_bits, combine_tolerance, run_combine, x_tensor

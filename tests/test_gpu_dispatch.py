@@ -53,6 +53,8 @@ def _host(res, fp8, n):
     (300, 8, 32, 2, 32, 0.0),         # 16-byte rows
     (33, 4096, 128, 8, 64, 0.05),     # few tokens: rows split into pieces
     (1, 7168, 256, 8, 8, 0.0),
+    (300, 512, 256, 8, 128, 0.0),     # more than 64 ranks
+    (200, 256, 2048, 32, 1024, 0.1),  # the limits: 1024 ranks, top-32
 ])
 def test_dispatch_bf16_full_compare(T, H, E, K, R, mask):
     d = make_inputs(T, H, E, K, R, seed=T * 3 + H, mask_frac=mask)
@@ -145,3 +147,17 @@ def test_dispatch_capacity_overflow():
     o = oracle.dispatch(d["x_bits"], d["topk_idx"], d["topk_weights"], E, R, L.dst_row, capacity=cap)
     for k in ("recv_x", "recv_topk_idx", "recv_topk_weights", "recv_src_idx"):
         np.testing.assert_array_equal(g[k], o[k][:cap], err_msg=k)
+
+
+@pytest.mark.parametrize("T,H,E,K,R", [(64, 1024, 256, 8, 128), (200, 512, 2048, 32, 1024), (7, 128, 16, 2, 4)])
+def test_dispatch_fp8_shapes(T, H, E, K, R):
+    d = make_inputs(T, H, E, K, R, seed=T + R)
+    lay, res, n, _, _ = _run(d, E, R, fp8=True)
+    assert int(res["status"].item()) == 0
+    g = _host(res, True, n)
+    L = oracle.layout(d["topk_idx"], E, R)
+    o = oracle.dispatch(d["x_bits"], d["topk_idx"], d["topk_weights"], E, R, L.dst_row, fp8=True)
+    for k in ("recv_x", "recv_topk_idx", "recv_topk_weights", "recv_src_idx"):
+        np.testing.assert_array_equal(g[k], o[k], err_msg=k)
+    sf = res["recv_sf"].cpu().numpy()[:n * (H // 128)].reshape(n, -1)
+    np.testing.assert_array_equal(sf, o["recv_sf"])
