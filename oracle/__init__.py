@@ -57,6 +57,14 @@ def _load():
     lib.ep_oracle_float_to_bf16.argtypes = [ctypes.c_float]
     lib.ep_oracle_bf16_to_float.restype = ctypes.c_float
     lib.ep_oracle_bf16_to_float.argtypes = [ctypes.c_uint16]
+    lib.ep_oracle_expanded_rows.restype = ctypes.c_int
+    lib.ep_oracle_expanded_rows.argtypes = [vp, ctypes.c_int, ctypes.c_int, ctypes.c_int, vp, vp, vp]
+    lib.ep_oracle_dispatch_expanded.restype = ctypes.c_int
+    lib.ep_oracle_dispatch_expanded.argtypes = [vp, vp, ctypes.c_int, ctypes.c_int, ctypes.c_int, vp,
+                                                ctypes.c_int64, ctypes.c_int, vp, vp, vp, vp]
+    lib.ep_oracle_combine_expanded.restype = ctypes.c_int
+    lib.ep_oracle_combine_expanded.argtypes = [vp, ctypes.c_int64, vp, ctypes.c_int, ctypes.c_int,
+                                               ctypes.c_int, ctypes.c_int, vp, vp]
     for name in ("ep_oracle_e4m3_encode_array", "ep_oracle_e4m3_decode_array",
                  "ep_oracle_float_to_bf16_array"):
         getattr(lib, name).restype = None
@@ -183,6 +191,58 @@ def combine(y_bits, topk_idx, topk_weights, E, R, dst_row, weighted=False, token
                                    1 if weighted else 0, T, H, K, E, R, _p(dst_row), _p(tokens),
                                    n if tokens is not None else 0, _p(out))
     return out[:n], status
+
+
+def expanded_rows(topk_idx, E, expert_offset):
+    """Expanded row of every (t, k) (see ep_oracle_expanded_rows): int32 [T, K], -1 if masked."""
+    lib = _load()
+    topk_idx = np.ascontiguousarray(topk_idx, dtype=np.int64)
+    T, K = topk_idx.shape
+    expert_offset = np.ascontiguousarray(expert_offset, dtype=np.int32)
+    out = np.zeros((T, K), np.int32)
+    scratch = np.zeros(max(E, 1), np.int32)
+    status = lib.ep_oracle_expanded_rows(_p(topk_idx), T, K, E, _p(expert_offset), _p(out), _p(scratch))
+    return out, status
+
+
+def dispatch_expanded(x_bits, topk_weights, expanded_row, capacity, fp8=False):
+    """Expanded dispatch (see ep_oracle_dispatch_expanded); arrays sized by capacity."""
+    lib = _load()
+    x_bits = np.ascontiguousarray(x_bits, dtype=np.uint16)
+    T, H = x_bits.shape
+    topk_weights = np.ascontiguousarray(topk_weights, dtype=np.float32)
+    expanded_row = np.ascontiguousarray(expanded_row, dtype=np.int32)
+    K = expanded_row.shape[1]
+    n = max(int(capacity), 1)
+    row_bytes = H if fp8 else 2 * H
+    recv_x = np.zeros((n, row_bytes), np.uint8)
+    recv_sf = np.zeros((n, H // 128), np.float32) if fp8 else None
+    recv_src_idx = np.full(n, -1, np.int32)
+    recv_weight = np.zeros(n, np.float32)
+    status = lib.ep_oracle_dispatch_expanded(_p(x_bits), _p(topk_weights), T, H, K, _p(expanded_row),
+                                             int(capacity), 1 if fp8 else 0, _p(recv_x), _p(recv_sf),
+                                             _p(recv_src_idx), _p(recv_weight))
+    res = dict(recv_x=recv_x[:capacity], recv_src_idx=recv_src_idx[:capacity],
+               recv_weight=recv_weight[:capacity], status=status)
+    if fp8:
+        res["recv_sf"] = recv_sf[:capacity]
+    return res
+
+
+def combine_expanded(y_bits, topk_weights, expanded_row, weighted=True):
+    """Expanded combine (see ep_oracle_combine_expanded); float64 [T, H]."""
+    lib = _load()
+    y_bits = np.ascontiguousarray(y_bits, dtype=np.uint16)
+    expanded_row = np.ascontiguousarray(expanded_row, dtype=np.int32)
+    T, K = expanded_row.shape
+    H = y_bits.shape[1]
+    if topk_weights is None:
+        topk_weights = np.zeros((T, K), np.float32)
+    topk_weights = np.ascontiguousarray(topk_weights, dtype=np.float32)
+    out = np.zeros((max(T, 1), H), np.float64)
+    status = lib.ep_oracle_combine_expanded(_p(y_bits), y_bits.shape[0], _p(topk_weights),
+                                            1 if weighted else 0, T, H, K, _p(expanded_row), _p(out))
+    return out[:T], status
 
 
 def fp8_cast_row(x_bits_row):

@@ -399,3 +399,87 @@ void ep_oracle_float_to_bf16_array(const float* v, int64_t n, uint16_t* out)
 {
     for (int64_t i = 0; i < n; ++i) out[i] = ep_oracle_float_to_bf16(v[i]);
 }
+
+/* ------------------------------------------------------------------------ */
+/* Expanded (per-expert) receive layout: [P2] dispatch_copy_epilogue and     */
+/* combine_reduce_epilogue, [P2 TokenLayout fragment] linked_list_idx,      */
+/* [P1 section 6.1] expert_alignment.  Every valid (t, k) gets its own row: */
+/* expert e's rows are expert_offset[e] + 0, 1, ... in (token, k) order,    */
+/* so rows are grouped by expert (ranks' experts in order) and each         */
+/* expert's block starts at its aligned offset.  Masked or invalid -> -1.   */
+/* ------------------------------------------------------------------------ */
+
+int ep_oracle_expanded_rows(const int64_t* topk_idx, int T, int K, int E,
+                            const int32_t* expert_offset, int32_t* expanded_row,
+                            int32_t* scratch_count /* [E] */)
+{
+    int status = OR_OK;
+    for (int e = 0; e < E; ++e) scratch_count[e] = 0;
+    for (int t = 0; t < T; ++t)
+        for (int k = 0; k < K; ++k) {
+            int64_t e = topk_idx[(int64_t)t * K + k];
+            int64_t i = (int64_t)t * K + k;
+            if (e < 0 || e >= E) {
+                expanded_row[i] = -1;
+                if (e < -1 || e >= E) status |= OR_INVALID_INDEX;
+                continue;
+            }
+            expanded_row[i] = expert_offset[e] + scratch_count[e];
+            scratch_count[e] += 1;
+        }
+    return status;
+}
+
+/* Expanded dispatch: row expanded_row[t,k] receives x[t] (bf16 copy or the  */
+/* FP8 cast), its source token t and its weight topk_weights[t,k].         */
+int ep_oracle_dispatch_expanded(const uint16_t* x, const float* topk_weights, int T, int H, int K,
+                                const int32_t* expanded_row, int64_t capacity, int fp8,
+                                uint8_t* recv_x, float* recv_sf, int32_t* recv_src_idx,
+                                float* recv_weight)
+{
+    int status = OR_OK;
+    size_t row_bytes = fp8 ? (size_t)H : (size_t)H * 2;
+    int nb = H / 128;
+    uint8_t q_tmp[65536];
+    float sf_tmp[512];
+    for (int t = 0; t < T; ++t)
+        for (int k = 0; k < K; ++k) {
+            int32_t d = expanded_row[(int64_t)t * K + k];
+            if (d < 0) continue;
+            if ((int64_t)d >= capacity) { status |= OR_CAPACITY; continue; }
+            const uint16_t* src = x + (int64_t)t * H;
+            if (fp8) {
+                ep_oracle_fp8_cast_row(src, H, q_tmp, sf_tmp);
+                memcpy(recv_x + (int64_t)d * (int64_t)row_bytes, q_tmp, row_bytes);
+                if (recv_sf)
+                    for (int b = 0; b < nb; ++b) recv_sf[(int64_t)d * nb + b] = sf_tmp[b];
+            } else {
+                memcpy(recv_x + (int64_t)d * (int64_t)row_bytes, src, row_bytes);
+            }
+            if (recv_src_idx) recv_src_idx[d] = t;
+            if (recv_weight) recv_weight[d] = topk_weights[(int64_t)t * K + k];
+        }
+    return status;
+}
+
+/* Expanded combine: out[t] = sum over valid k (ascending) of c * y[expanded_row[t,k]], */
+/* c = topk_weights[t,k] (weighted) or 1; fp64 accumulation.                         */
+int ep_oracle_combine_expanded(const uint16_t* y, int64_t num_y_rows, const float* topk_weights,
+                               int weighted, int T, int H, int K, const int32_t* expanded_row,
+                               double* out)
+{
+    int status = OR_OK;
+    for (int t = 0; t < T; ++t) {
+        double* o = out + (int64_t)t * H;
+        for (int h = 0; h < H; ++h) o[h] = 0.0;
+        for (int k = 0; k < K; ++k) {
+            int32_t d = expanded_row[(int64_t)t * K + k];
+            if (d < 0) continue;
+            if ((int64_t)d >= num_y_rows) { status |= OR_CAPACITY; continue; }
+            double c = weighted ? (double)topk_weights[(int64_t)t * K + k] : 1.0;
+            const uint16_t* yr = y + (int64_t)d * H;
+            for (int h = 0; h < H; ++h) o[h] += c * (double)ep_oracle_bf16_to_float(yr[h]);
+        }
+    }
+    return status;
+}
