@@ -38,7 +38,7 @@ class ep_layout_t(ctypes.Structure):
     _fields_ = [("num_tokens_per_rank", _vp), ("num_tokens_per_node", _vp),
                 ("num_tokens_per_expert", _vp), ("is_token_in_rank", _vp), ("rank_offset", _vp),
                 ("expert_offset", _vp), ("dst_row", _vp), ("src_dst_count", _vp),
-                ("token_offset", _vp)]
+                ("token_offset", _vp), ("expanded_row", _vp)]
 
 
 _lib.ep_layout_workspace_bytes.restype = ctypes.c_size_t
@@ -57,6 +57,14 @@ _lib.ep_dispatch.argtypes = [_vp, _vp, _vp, _i, _i, _i, _i, _i, ctypes.POINTER(e
 _lib.ep_combine.restype = ctypes.c_int32
 _lib.ep_combine.argtypes = [_vp, _i64, _vp, _vp, _i, _i, _i, _i, _i, ctypes.POINTER(ep_layout_t),
                             _vp, _vp, _vp]
+_lib.ep_expanded_capacity_bound.restype = _i64
+_lib.ep_expanded_capacity_bound.argtypes = [_i, _i, _i, _i]
+_lib.ep_dispatch_expanded.restype = ctypes.c_int32
+_lib.ep_dispatch_expanded.argtypes = [_vp, _vp, _vp, _i, _i, _i, _i, _i, ctypes.POINTER(ep_layout_t), _i,
+                                      _i64, _vp, _vp, _i, _vp, _vp, _vp, _vp]
+_lib.ep_combine_expanded.restype = ctypes.c_int32
+_lib.ep_combine_expanded.argtypes = [_vp, _i64, _vp, _i, _i, _i, _i, _i, ctypes.POINTER(ep_layout_t), _vp,
+                                     _vp, _vp]
 _lib.ep_status_string.restype = ctypes.c_char_p
 _lib.ep_status_string.argtypes = [ctypes.c_int32]
 _lib.ep_abi_version.restype = _i
@@ -102,7 +110,7 @@ def ep_recv_capacity_bound(num_tokens, num_topk, num_ranks) -> int:
 class Layout:
     """Device tensors of one routing layout plus their ep_layout_t view."""
 
-    def __init__(self, T, E, R, ranks_per_node=0, with_src_dst=True, device="cuda"):
+    def __init__(self, T, E, R, ranks_per_node=0, with_src_dst=True, device="cuda", K=None):
         i32 = dict(dtype=torch.int32, device=device)
         nodes = R // ranks_per_node if ranks_per_node > 0 else 0
         self.T, self.E, self.R, self.ranks_per_node = T, E, R, ranks_per_node
@@ -115,6 +123,8 @@ class Layout:
         self.dst_row = torch.empty((T, R), **i32)
         self.src_dst_count = torch.empty((R, R), **i32) if (with_src_dst and T % R == 0) else None
         self.token_offset = torch.empty(T + 1, **i32)
+        # expanded (per-expert) rows are produced when K is given
+        self.expanded_row = torch.empty((T, K), **i32) if K is not None else None
         self.c = ep_layout_t(*[_ptr(getattr(self, f)) for f, _ in ep_layout_t._fields_])
 
     @property
@@ -123,8 +133,13 @@ class Layout:
         return int(self.rank_offset[-1].item())
 
 
-def alloc_layout(T, E, R, ranks_per_node=0, with_src_dst=True, device="cuda") -> Layout:
-    return Layout(T, E, R, ranks_per_node, with_src_dst, device)
+def alloc_layout(T, E, R, ranks_per_node=0, with_src_dst=True, device="cuda", K=None) -> Layout:
+    """Device arrays of a layout; pass K to also get the expanded rows."""
+    return Layout(T, E, R, ranks_per_node, with_src_dst, device, K)
+
+
+def ep_expanded_capacity_bound(num_tokens, num_topk, num_experts, expert_alignment=1) -> int:
+    return int(_lib.ep_expanded_capacity_bound(num_tokens, num_topk, num_experts, expert_alignment))
 
 
 def ep_get_layout(topk_idx, num_experts, num_ranks, layout, workspace, d_status, ranks_per_node=0,
@@ -164,6 +179,29 @@ def ep_dispatch(x, topk_idx, topk_weights, num_experts, num_ranks, layout, recv_
                             _ptr(recv_topk_weights), _ptr(recv_src_idx), _ptr(d_status),
                             _stream(stream))
     return _check(code, "ep_dispatch")
+
+
+def ep_dispatch_expanded(x, topk_idx, topk_weights, num_experts, num_ranks, layout, recv_x, recv_src_idx,
+                         recv_weight, d_status, recv_sf=None, out_dtype=EP_BF16, sf_col_major=False,
+                         stream=None):
+    T, H = x.shape
+    K = topk_idx.shape[1]
+    assert x.element_size() == 2 and x.is_contiguous() and recv_x.is_contiguous()
+    code = _lib.ep_dispatch_expanded(_ptr(x), _ptr(topk_idx), _ptr(topk_weights), T, H, K, num_experts,
+                                     num_ranks, ctypes.byref(layout.c), out_dtype, recv_x.shape[0],
+                                     _ptr(recv_x), _ptr(recv_sf), 1 if sf_col_major else 0,
+                                     _ptr(recv_src_idx), _ptr(recv_weight), _ptr(d_status), _stream(stream))
+    return _check(code, "ep_dispatch_expanded")
+
+
+def ep_combine_expanded(y, topk_weights, num_topk, num_experts, num_ranks, layout, out, d_status,
+                        stream=None):
+    T, H = out.shape
+    assert y.element_size() == 2 and y.is_contiguous() and out.is_contiguous()
+    code = _lib.ep_combine_expanded(_ptr(y), y.shape[0], _ptr(topk_weights), T, H, num_topk, num_experts,
+                                    num_ranks, ctypes.byref(layout.c), _ptr(out), _ptr(d_status),
+                                    _stream(stream))
+    return _check(code, "ep_combine_expanded")
 
 
 def ep_combine(y, topk_idx, topk_weights, num_experts, num_ranks, layout, out, d_status, stream=None):

@@ -48,7 +48,7 @@ ep_status_t check_shape(int T, int K, int E, int R) {
 
 extern "C" {
 
-int ep_abi_version(void) { return 2; }
+int ep_abi_version(void) { return 3; }
 
 size_t ep_layout_workspace_bytes(int num_tokens, int num_topk, int num_experts, int num_ranks,
                                  int ranks_per_node) {
@@ -80,6 +80,7 @@ ep_status_t ep_get_layout(const int64_t* topk_idx, int T, int K, int E, int R, i
     if (out->num_tokens_per_node && !aligned16(out->num_tokens_per_node)) return EP_ERR_INVALID_ARG;
     if (out->src_dst_count && (!aligned16(out->src_dst_count) || T % R != 0)) return EP_ERR_INVALID_ARG;
     if (out->token_offset && !aligned16(out->token_offset)) return EP_ERR_INVALID_ARG;
+    if (out->expanded_row && !aligned16(out->expanded_row)) return EP_ERR_INVALID_ARG;
     const int nodes_ws = ranks_per_node > 0 ? R / ranks_per_node : 0;
     const epg::LayoutWorkspace w = epg::layout_workspace(T, E, R, nodes_ws);
     if (!ok_ptr(workspace) || ws_bytes < w.total) return EP_ERR_INVALID_ARG;
@@ -104,6 +105,7 @@ ep_status_t ep_get_layout(const int64_t* topk_idx, int T, int K, int E, int R, i
     p.dst_row = out->dst_row;
     p.src_dst_count = out->src_dst_count;
     p.token_offset = out->token_offset;
+    p.expanded_row = T > 0 ? out->expanded_row : nullptr;
     char* ws = static_cast<char*>(workspace);
     p.ws_rank = reinterpret_cast<int32_t*>(ws + w.off_rank);
     p.ws_expert = reinterpret_cast<int32_t*>(ws + w.off_expert);
@@ -190,6 +192,94 @@ ep_status_t ep_combine(const void* y, int64_t num_y_rows, const int64_t* topk_id
     p.topk_idx = topk_idx;
     p.topk_weights = topk_weights;
     p.dst_row = layout->dst_row;
+    p.T = T;
+    p.H = H;
+    p.K = K;
+    p.E = E;
+    p.R = R;
+    p.experts_per_rank = E / R;
+    p.out = static_cast<uint8_t*>(out);
+    p.status = d_status;
+    const cudaError_t e =
+        epg::launch_combine(p, topk_weights != nullptr, static_cast<cudaStream_t>(cuda_stream));
+    return e == cudaSuccess ? EP_OK : EP_ERR_CUDA;
+}
+
+int64_t ep_expanded_capacity_bound(int num_tokens, int num_topk, int num_experts, int expert_alignment) {
+    if (num_tokens < 0 || num_topk < 0 || num_experts < 0 || expert_alignment < 1) return 0;
+    return static_cast<int64_t>(num_tokens) * num_topk + static_cast<int64_t>(num_experts) * (expert_alignment - 1);
+}
+
+ep_status_t ep_dispatch_expanded(const void* x, const int64_t* topk_idx, const float* topk_weights, int T,
+                                 int H, int K, int E, int R, const ep_layout_t* layout, int out_dtype,
+                                 int64_t recv_capacity, void* recv_x, float* recv_sf, int sf_col_major,
+                                 int32_t* recv_src_idx, float* recv_weight, int32_t* d_status,
+                                 void* cuda_stream) {
+    if (!layout || !d_status) return EP_ERR_INVALID_ARG;
+    ep_status_t s = check_shape(T, K, E, R);
+    if (s != EP_OK) return s;
+    if (H < 1) return EP_ERR_INVALID_ARG;
+    if (out_dtype == EP_BF16) {
+        if (H % 8 != 0) return EP_ERR_INVALID_ARG;
+    } else if (out_dtype == EP_FP8_E4M3) {
+        if (H % 128 != 0) return EP_ERR_INVALID_ARG;
+        if (H > 65536) return EP_ERR_UNSUPPORTED;
+    } else {
+        return EP_ERR_INVALID_ARG;
+    }
+    if (recv_capacity < 0 || recv_capacity > INT32_MAX) return EP_ERR_INVALID_ARG;
+    if (static_cast<int64_t>(H) * 2 > UINT32_MAX / 2) return EP_ERR_UNSUPPORTED;
+    if (T > 0 && (!ok_ptr(x) || !ok_ptr(layout->expanded_row))) return EP_ERR_INVALID_ARG;
+    if (recv_capacity > 0 && !ok_ptr(recv_x)) return EP_ERR_INVALID_ARG;
+    if (out_dtype == EP_FP8_E4M3 && recv_capacity > 0 && !ok_ptr(recv_sf)) return EP_ERR_INVALID_ARG;
+    if (recv_weight && T > 0 && !ok_ptr(topk_weights)) return EP_ERR_INVALID_ARG;
+    if ((recv_src_idx && !aligned16(recv_src_idx)) || (recv_weight && !aligned16(recv_weight)))
+        return EP_ERR_INVALID_ARG;
+    if (T == 0) return EP_OK;
+
+    epg::DispatchParams p{};
+    p.x = static_cast<const uint8_t*>(x);
+    p.topk_idx = topk_idx;
+    p.topk_weights = topk_weights;
+    p.expanded_row = layout->expanded_row;
+    p.T = T;
+    p.H = H;
+    p.K = K;
+    p.E = E;
+    p.R = R;
+    p.experts_per_rank = E / R;
+    p.capacity = recv_capacity;
+    p.recv_x = static_cast<uint8_t*>(recv_x);
+    p.recv_sf = recv_sf;
+    p.sf_col_major = sf_col_major ? 1 : 0;
+    p.sf_stride = (recv_capacity + 3) / 4 * 4;
+    p.recv_src_idx = recv_src_idx;
+    p.recv_weight = recv_weight;
+    p.status = d_status;
+    cudaStream_t st = static_cast<cudaStream_t>(cuda_stream);
+    const cudaError_t e = out_dtype == EP_BF16 ? epg::launch_dispatch_bf16(p, st)
+                                               : epg::launch_dispatch_fp8(p, st);
+    return e == cudaSuccess ? EP_OK : EP_ERR_CUDA;
+}
+
+ep_status_t ep_combine_expanded(const void* y, int64_t num_y_rows, const float* topk_weights, int T, int H,
+                                int K, int E, int R, const ep_layout_t* layout, void* out, int32_t* d_status,
+                                void* cuda_stream) {
+    if (!layout || !d_status) return EP_ERR_INVALID_ARG;
+    ep_status_t s = check_shape(T, K, E, R);
+    if (s != EP_OK) return s;
+    if (H < 1 || H % 8 != 0) return EP_ERR_INVALID_ARG;
+    if (num_y_rows < 0 || num_y_rows > INT32_MAX) return EP_ERR_INVALID_ARG;
+    if (num_y_rows > 0 && !ok_ptr(y)) return EP_ERR_INVALID_ARG;
+    if (T > 0 && (!ok_ptr(out) || !ok_ptr(layout->expanded_row))) return EP_ERR_INVALID_ARG;
+    if (topk_weights && T > 0 && !ok_ptr(topk_weights)) return EP_ERR_INVALID_ARG;
+    if (T == 0) return EP_OK;
+
+    epg::CombineParams p{};
+    p.y = static_cast<const uint8_t*>(y);
+    p.num_y_rows = num_y_rows;
+    p.topk_weights = topk_weights;
+    p.expanded_row = layout->expanded_row;
     p.T = T;
     p.H = H;
     p.K = K;

@@ -32,7 +32,9 @@ constexpr int kThreads = EP_COMBINE_THREADS;
 #endif
 constexpr int kBatch = EP_COMBINE_BATCH;
 
-template <bool kWeighted>
+// kExpanded: the token's source rows are its expanded rows (one per valid
+// top-k slot, coefficient = that slot's weight) instead of one row per rank.
+template <bool kWeighted, bool kExpanded>
 __global__ void __launch_bounds__(kThreads, EP_COMBINE_MIN_BLOCKS) combine_kernel(const CombineParams p) {
     __shared__ int s_rows[EP_MAX_TOPK];
     __shared__ float s_coef[EP_MAX_TOPK];
@@ -47,18 +49,23 @@ __global__ void __launch_bounds__(kThreads, EP_COMBINE_MIN_BLOCKS) combine_kerne
         int64_t e_l = -1;
         float w_l = 0.0f;
         if (kWeighted && lane < p.K) {
-            e_l = p.topk_idx[static_cast<int64_t>(t) * p.K + lane];
+            if (!kExpanded) e_l = p.topk_idx[static_cast<int64_t>(t) * p.K + lane];
             w_l = p.topk_weights[static_cast<int64_t>(t) * p.K + lane];
         }
         int n = 0;
         bool cap_bad = false;
-        for (int rb = 0; rb < p.R; rb += 32) {
+        const int n_src = kExpanded ? p.K : p.R;
+        const int32_t* srow = kExpanded ? p.expanded_row + static_cast<int64_t>(t) * p.K
+                                        : p.dst_row + static_cast<int64_t>(t) * p.R;
+        for (int rb = 0; rb < n_src; rb += 32) {
             const int r = rb + lane;
-            const int d = r < p.R ? p.dst_row[static_cast<int64_t>(t) * p.R + r] : -1;
+            const int d = r < n_src ? srow[r] : -1;
             const bool ok = d >= 0 && d < p.num_y_rows;
             if (d >= p.num_y_rows) cap_bad = true;
             float coef = 1.0f;
-            if (kWeighted) {
+            if (kExpanded) {
+                if (kWeighted) coef = w_l;   // lane r holds slot r's weight (K <= 32)
+            } else if (kWeighted) {
                 coef = 0.0f;
                 for (int k = 0; k < p.K; ++k) {
                     const int64_t e = __shfl_sync(0xffffffffu, e_l, k);
@@ -153,9 +160,13 @@ cudaError_t launch_combine(CombineParams p, bool weighted, cudaStream_t stream) 
     p.chunk_vecs = chunk_vecs;
     const int64_t grid = static_cast<int64_t>(p.T) * chunks;
     if (grid < 1) return cudaSuccess;
-    if (weighted)
-        return launch_pdl(combine_kernel<true>, dim3(static_cast<unsigned>(grid)), dim3(kThreads), 0, stream, p);
-    return launch_pdl(combine_kernel<false>, dim3(static_cast<unsigned>(grid)), dim3(kThreads), 0, stream, p);
+    const dim3 g(static_cast<unsigned>(grid)), b(kThreads);
+    if (p.expanded_row) {
+        if (weighted) return launch_pdl(combine_kernel<true, true>, g, b, 0, stream, p);
+        return launch_pdl(combine_kernel<false, true>, g, b, 0, stream, p);
+    }
+    if (weighted) return launch_pdl(combine_kernel<true, false>, g, b, 0, stream, p);
+    return launch_pdl(combine_kernel<false, false>, g, b, 0, stream, p);
 }
 
 }  // namespace epg

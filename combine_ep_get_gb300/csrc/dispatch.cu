@@ -279,7 +279,16 @@ __global__ void __launch_bounds__(kBf16Threads) dispatch_bf16_kernel(const Dispa
     }
 }
 
-#if EP_DISPATCH_IMPL == 1
+// Expanded mode metadata of token t (one warp, lane k): every valid (t, k)
+// row gets the source token and the weight of that top-k slot.
+__device__ __forceinline__ void write_expanded_metadata(const DispatchParams& p, int t, int lane) {
+    if (lane >= p.K) return;
+    const int d = p.expanded_row[static_cast<int64_t>(t) * p.K + lane];
+    if (d < 0 || d >= p.capacity) return;
+    if (p.recv_src_idx) p.recv_src_idx[d] = t;
+    if (p.recv_weight) p.recv_weight[d] = p.topk_weights[static_cast<int64_t>(t) * p.K + lane];
+}
+
 constexpr int kRegThreads = 256;
 constexpr int kRegUnroll = 4;
 
@@ -287,7 +296,9 @@ constexpr int kRegUnroll = 4;
 // kRegUnroll 16-byte vectors of the piece, its warp reads the token's
 // destination rows (one lane per rank) and broadcasts them by shuffles, and
 // the thread stores its vectors to every destination.  Warps never wait for
-// one another.
+// one another.  kExpanded: the destinations are the token's expanded rows
+// (one per valid top-k slot) instead of one row per rank.
+template <bool kExpanded>
 __global__ void __launch_bounds__(kRegThreads, 6) dispatch_bf16_regs_kernel(const DispatchParams p) {
     const int64_t it = blockIdx.x;
     const int t = static_cast<int>(it / p.chunks);
@@ -307,18 +318,24 @@ __global__ void __launch_bounds__(kRegThreads, 6) dispatch_bf16_regs_kernel(cons
         const int v = threadIdx.x + k * kRegThreads;
         if (v < nvec) u[k] = ld_stream_v4(src + static_cast<size_t>(v) * 16);
     }
-    const int32_t* drow = p.dst_row + static_cast<int64_t>(t) * p.R;
-    const int d0 = lane < p.R ? drow[lane] : -1;
-    const int d1 = 32 + lane < p.R ? drow[32 + lane] : -1;   // ranks 32..63, same latency
+    const int n_dst = kExpanded ? p.K : p.R;
+    const int32_t* drow = kExpanded ? p.expanded_row + static_cast<int64_t>(t) * p.K
+                                    : p.dst_row + static_cast<int64_t>(t) * p.R;
+    const int d0 = lane < n_dst ? drow[lane] : -1;
+    const int d1 = 32 + lane < n_dst ? drow[32 + lane] : -1;   // ranks 32..63, same latency
     if (warp == 1 && c == 0) {
-        CtaWork all;
-        all.first = 0;
-        all.count = 0;
-        all.stride = 1;
-        all.lo = INT32_MIN;
-        all.hi = INT32_MAX;
-        all.balanced = 0;
-        write_metadata(p, t, lane, all);
+        if (kExpanded) {
+            write_expanded_metadata(p, t, lane);
+        } else {
+            CtaWork all;
+            all.first = 0;
+            all.count = 0;
+            all.stride = 1;
+            all.lo = INT32_MIN;
+            all.hi = INT32_MAX;
+            all.balanced = 0;
+            write_metadata(p, t, lane, all);
+        }
     }
     bool cap_bad = false;
     for (int base = 0; base < nvec; base += kRegUnroll * kRegThreads) {
@@ -329,8 +346,8 @@ __global__ void __launch_bounds__(kRegThreads, 6) dispatch_bf16_regs_kernel(cons
                 if (v < nvec) u[k] = ld_stream_v4(src + static_cast<size_t>(v) * 16);
             }
         }
-        for (int rb = 0; rb < p.R; rb += 32) {
-            const int d = rb == 0 ? d0 : rb == 32 ? d1 : (rb + lane < p.R ? drow[rb + lane] : -1);
+        for (int rb = 0; rb < n_dst; rb += 32) {
+            const int d = rb == 0 ? d0 : rb == 32 ? d1 : (rb + lane < n_dst ? drow[rb + lane] : -1);
             if (d >= p.capacity) cap_bad = true;
             unsigned m = __ballot_sync(0xffffffffu, d >= 0 && d < p.capacity);
             while (m) {
@@ -354,8 +371,6 @@ __global__ void __launch_bounds__(kRegThreads, 6) dispatch_bf16_regs_kernel(cons
     if (warp == 0 && c == 0 && __any_sync(0xffffffffu, cap_bad) && lane == 0)
         atomicOr(p.status, EP_ERR_CAPACITY);
 }
-#endif  // EP_DISPATCH_IMPL == 1
-
 
 __device__ __forceinline__ uint32_t pack_e4m3x4(float a, float b, float c, float d) {
     uint16_t lo, hi;
@@ -367,6 +382,7 @@ __device__ __forceinline__ uint32_t pack_e4m3x4(float a, float b, float c, float
 
 constexpr int kFp8Threads = 256;
 
+template <bool kExpanded>
 __global__ void __launch_bounds__(kFp8Threads) dispatch_fp8_kernel(const DispatchParams p) {
     __shared__ int s_rows[EP_MAX_TOPK];
     __shared__ int s_n;
@@ -380,9 +396,12 @@ __global__ void __launch_bounds__(kFp8Threads) dispatch_fp8_kernel(const Dispatc
     if (warp == 0) {
         int n = 0;
         bool cap_bad = false;
-        for (int rb = 0; rb < p.R; rb += 32) {
+        const int n_dst = kExpanded ? p.K : p.R;
+        const int32_t* drow = kExpanded ? p.expanded_row + static_cast<int64_t>(t) * p.K
+                                        : p.dst_row + static_cast<int64_t>(t) * p.R;
+        for (int rb = 0; rb < n_dst; rb += 32) {
             const int r = rb + lane;
-            const int d = r < p.R ? p.dst_row[static_cast<int64_t>(t) * p.R + r] : -1;
+            const int d = r < n_dst ? drow[r] : -1;
             const bool ok = d >= 0 && d < p.capacity;
             if (d >= p.capacity) cap_bad = true;
             const unsigned m = __ballot_sync(0xffffffffu, ok);
@@ -399,14 +418,18 @@ __global__ void __launch_bounds__(kFp8Threads) dispatch_fp8_kernel(const Dispatc
         if (lane == 0) s_n = n;
         if (__any_sync(0xffffffffu, cap_bad) && lane == 0 && c == 0) atomicOr(p.status, EP_ERR_CAPACITY);
     } else if (warp == 1 && c == 0) {
-        CtaWork all;
-        all.first = 0;
-        all.count = 0;
-        all.stride = 1;
-        all.lo = INT32_MIN;
-        all.hi = INT32_MAX;
-        all.balanced = 0;
-        write_metadata(p, t, lane, all);
+        if (kExpanded) {
+            write_expanded_metadata(p, t, lane);
+        } else {
+            CtaWork all;
+            all.first = 0;
+            all.count = 0;
+            all.stride = 1;
+            all.lo = INT32_MIN;
+            all.hi = INT32_MAX;
+            all.balanced = 0;
+            write_metadata(p, t, lane, all);
+        }
     }
     __syncthreads();
 
@@ -466,9 +489,8 @@ cudaError_t launch_dispatch_bf16(DispatchParams p, cudaStream_t stream) {
     const uint32_t row_bytes = static_cast<uint32_t>(p.H) * 2u;
     // Pieces: at most 16 KB each; more pieces when there are few tokens so
     // that every SM gets work.
-#if EP_DISPATCH_IMPL == 1
-    {
-        // register path: one CTA per (token, piece of <= 16 KB); more pieces for few tokens
+    if (EP_DISPATCH_IMPL == 1 || p.expanded_row != nullptr) {
+        // register path (the expanded mode always takes it): one CTA per (token, piece of <= 16 KB); more pieces for few tokens
         int chunks = static_cast<int>((row_bytes + 16383u) / 16384u);
         const int want_items = 4 * di.num_sms;
         if (p.T > 0 && static_cast<int64_t>(p.T) * chunks < want_items) {
@@ -483,10 +505,12 @@ cudaError_t launch_dispatch_bf16(DispatchParams p, cudaStream_t stream) {
         p.chunk_bytes = cb;
         const int64_t g = static_cast<int64_t>(p.T) * p.chunks;
         if (g < 1) return cudaSuccess;
-        return launch_pdl(dispatch_bf16_regs_kernel, dim3(static_cast<unsigned>(g)), dim3(kRegThreads), 0, stream,
-                          p);
+        if (p.expanded_row)
+            return launch_pdl(dispatch_bf16_regs_kernel<true>, dim3(static_cast<unsigned>(g)), dim3(kRegThreads),
+                              0, stream, p);
+        return launch_pdl(dispatch_bf16_regs_kernel<false>, dim3(static_cast<unsigned>(g)), dim3(kRegThreads),
+                          0, stream, p);
     }
-#endif
     int chunks = static_cast<int>((row_bytes + EP_DISPATCH_PIECE_MAX - 1) / EP_DISPATCH_PIECE_MAX);
     const int want_items = 2 * di.num_sms;
     if (p.T > 0 && static_cast<int64_t>(p.T) * chunks < want_items) {
@@ -544,7 +568,11 @@ cudaError_t launch_dispatch_fp8(DispatchParams p, cudaStream_t stream) {
     p.chunk_blocks = chunk_blocks;
     const int64_t grid = static_cast<int64_t>(p.T) * chunks;
     if (grid < 1) return cudaSuccess;
-    return launch_pdl(dispatch_fp8_kernel, dim3(static_cast<unsigned>(grid)), dim3(kFp8Threads), 0, stream, p);
+    if (p.expanded_row)
+        return launch_pdl(dispatch_fp8_kernel<true>, dim3(static_cast<unsigned>(grid)), dim3(kFp8Threads), 0, stream,
+                          p);
+    return launch_pdl(dispatch_fp8_kernel<false>, dim3(static_cast<unsigned>(grid)), dim3(kFp8Threads), 0, stream,
+                      p);
 }
 
 }  // namespace epg

@@ -31,6 +31,7 @@ struct LayoutParams {
     int32_t* dst_row;
     int32_t* src_dst_count;
     int32_t* token_offset;
+    int32_t* expanded_row;   // [T][K] or null
     // workspace
     int32_t* ws_rank;      // [R][num_tiles]: tile counts, then exclusive tile prefix
     int32_t* ws_expert;    // [E][num_tiles]
@@ -45,6 +46,8 @@ struct DispatchParams {
     const float* topk_weights;
     const int32_t* dst_row;
     const int32_t* token_offset;   // may be null
+    const int32_t* expanded_row;   // expanded mode: [T][K] destination rows instead of dst_row
+    float* recv_weight;            // expanded mode: weight of each received (token, k)
     int T, H, K, E, R, experts_per_rank;
     int64_t capacity;
     uint8_t* recv_x;
@@ -67,6 +70,7 @@ struct CombineParams {
     const int64_t* topk_idx;
     const float* topk_weights;
     const int32_t* dst_row;
+    const int32_t* expanded_row;   // expanded mode: [T][K] source rows instead of dst_row
     int T, H, K, E, R, experts_per_rank;
     uint8_t* out;
     int32_t* status;

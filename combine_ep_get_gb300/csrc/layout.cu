@@ -149,6 +149,7 @@ __global__ void __launch_bounds__(kThreads) layout_scan_kernel(const LayoutParam
         const int e = col - p.R;
         row = p.ws_expert + static_cast<size_t>(e) * p.num_tiles;
         total = p.num_tokens_per_expert + e;
+        scan = p.expanded_row != nullptr;   // tile prefix per expert for the expanded rows
     } else {
         const int n = col - p.R - p.E;
         row = p.ws_node + static_cast<size_t>(n) * p.num_tiles;
@@ -193,6 +194,71 @@ __device__ void block_exclusive_scan(int n, Get get, Put put, int* s_warp) {
     }
     if (tid == 0) put(n, total);
     __syncthreads();
+}
+
+// Expanded (per-expert) rows of one tile's (token, k) entries: expert e's
+// entries take rows expert_offset[e] + (entries of e in earlier tiles) + their
+// stable rank in the tile, in (token, k) order.  The tile's entries are staged
+// in shared memory; each warp ranks a contiguous slice of them twice with
+// __match_any_sync (count, then place) around a per-(warp, expert) prefix, so
+// the order never depends on timing.  Needs 256 K + E + 8 E shared ints.
+__device__ void expanded_rows_of_tile(const LayoutParams& p, int tile, int t0, int nt, int* sm, int* s_warp) {
+    constexpr int kWarps = kThreads / 32;
+    const int E = p.E;
+    const int n_ent = nt * p.K;
+    int* s_key = sm;                      // [256 K] expert of each entry, or a unique negative
+    int* s_eb = s_key + kTileTokens * p.K;  // [E] base row of each expert for this tile
+    int* s_wc = s_eb + E;                 // [kWarps][E] per-warp counts, then per-warp bases
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int64_t* src = p.topk_idx + static_cast<int64_t>(t0) * p.K;
+    for (int i = threadIdx.x; i < n_ent; i += kThreads) {
+        const int64_t e = src[i];
+        s_key[i] = (e >= 0 && e < E) ? static_cast<int>(e) : -1 - (i & 31);
+    }
+    for (int i = threadIdx.x; i < kWarps * E; i += kThreads) s_wc[i] = 0;
+    const int a = p.alignment;
+    const int32_t* ce = p.num_tokens_per_expert;
+    block_exclusive_scan(
+        E, [&](int i) { return (ce[i] + a - 1) / a * a; },
+        [&](int i, int v) {
+            if (i < E) s_eb[i] = v;
+        },
+        s_warp);
+    for (int e = threadIdx.x; e < E; e += kThreads) s_eb[e] += p.ws_expert[static_cast<size_t>(e) * p.num_tiles + tile];
+    __syncthreads();
+    // each warp owns entries [w0, w1), whole 32-entry chunks
+    const int chunks = (n_ent + 31) / 32;
+    const int per = (chunks + kWarps - 1) / kWarps;
+    const int c0 = min(chunks, warp * per), c1 = min(chunks, c0 + per);
+    for (int c = c0; c < c1; ++c) {                     // pass 1: per-(warp, expert) counts
+        const int i = c * 32 + lane;
+        const int key = i < n_ent ? s_key[i] : -1 - lane;
+        const unsigned g = __match_any_sync(0xffffffffu, key);
+        if (key >= 0 && lane == __ffs(g) - 1) s_wc[warp * E + key] += __popc(g);
+        __syncwarp();
+    }
+    __syncthreads();
+    for (int e = threadIdx.x; e < E; e += kThreads) {   // per-warp bases, warps in entry order
+        int run = s_eb[e];
+        for (int w = 0; w < kWarps; ++w) {
+            const int v = s_wc[w * E + e];
+            s_wc[w * E + e] = run;
+            run += v;
+        }
+    }
+    __syncthreads();
+    int32_t* out = p.expanded_row + static_cast<int64_t>(t0) * p.K;
+    for (int c = c0; c < c1; ++c) {                     // pass 2: place
+        const int i = c * 32 + lane;
+        const int key = i < n_ent ? s_key[i] : -1 - lane;
+        const unsigned g = __match_any_sync(0xffffffffu, key);
+        int pos = -1;
+        if (key >= 0) pos = s_wc[warp * E + key] + __popc(g & ((1u << lane) - 1u));
+        __syncwarp();
+        if (key >= 0 && lane == __ffs(g) - 1) s_wc[warp * E + key] += __popc(g);
+        __syncwarp();
+        if (i < n_ent) out[i] = pos;
+    }
 }
 
 __global__ void __launch_bounds__(kThreads) layout_rows_kernel(const LayoutParams p) {
@@ -303,6 +369,8 @@ __global__ void __launch_bounds__(kThreads) layout_rows_kernel(const LayoutParam
             if (c) atomicAdd(&p.src_dst_count[s * R + r], c);
         }
     }
+
+    if (p.expanded_row) expanded_rows_of_tile(p, tile, t0, nt, s_wpre + R * kTileWords, s_warp);
 }
 
 // ---------------------------------------------------------------------------
@@ -595,7 +663,7 @@ struct ClusterPlan {
     size_t smem;
 };
 
-ClusterPlan plan_cluster(const LayoutParams& p, const DeviceInfo& di) {
+ClusterPlan plan_cluster(const LayoutParams& p, int smem_max) {
     ClusterPlan plan{0, 0, 0};
     // One CTA per 256 tokens up to 16; ranges are whole 32-token words.
     int ctas = (p.T + kTileTokens - 1) / kTileTokens;
@@ -607,7 +675,7 @@ ClusterPlan plan_cluster(const LayoutParams& p, const DeviceInfo& di) {
     ctas = (p.T + tpc - 1) / tpc;
     if (ctas < 1) ctas = 1;
     const size_t smem = 4 * cluster_smem_words(p.R, p.E, p.num_nodes, tpc / 32);
-    if (smem > static_cast<size_t>(di.max_smem_optin) - 1024) return plan;
+    if (smem > static_cast<size_t>(smem_max)) return plan;
     // Large [T, R] outputs are written faster by the many-CTA path.
     if (static_cast<int64_t>(p.T) * p.R > kClusterMaxTokenRanks) return plan;
     plan.ctas = ctas;
@@ -638,23 +706,35 @@ cudaError_t launch_layout(const LayoutParams& p, cudaStream_t stream) {
     const DeviceInfo& di = device_info();
     static thread_local int configured_device = -1;
     static thread_local bool cluster_ok = false;
+    static thread_local int cluster_smem_max = 0;
     if (configured_device != di.device) {
         // Worst case over the supported limits (R = 1024, E = 2048): < 80 KB.
         const int cap = di.max_smem_optin < 100 * 1024 ? di.max_smem_optin : 100 * 1024;
         cudaError_t e = cudaFuncSetAttribute(layout_count_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, cap);
         if (e != cudaSuccess) return e;
-        e = cudaFuncSetAttribute(layout_rows_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, cap);
+        // the rows kernel needs up to ~220 KB with expanded rows: all the dynamic
+        // shared memory the block limit leaves beside its static shared memory
+        cudaFuncAttributes fa{};
+        e = cudaFuncGetAttributes(&fa, layout_rows_kernel);
         if (e != cudaSuccess) return e;
+        e = cudaFuncSetAttribute(layout_rows_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 di.max_smem_optin - static_cast<int>(fa.sharedSizeBytes));
+        if (e != cudaSuccess) return e;
+        e = cudaFuncGetAttributes(&fa, layout_cluster_kernel);
+        if (e != cudaSuccess) return e;
+        cluster_smem_max = di.max_smem_optin - static_cast<int>(fa.sharedSizeBytes);
         cluster_ok =
             cudaFuncSetAttribute(layout_cluster_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 di.max_smem_optin - 1024) == cudaSuccess &&
+                                 cluster_smem_max) == cudaSuccess &&
             cudaFuncSetAttribute(layout_cluster_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed,
                                  1) == cudaSuccess;
         cudaGetLastError();   // a refused attribute only disables the cluster path
         configured_device = di.device;
     }
 
-    const ClusterPlan plan = cluster_ok ? plan_cluster(p, di) : ClusterPlan{0, 0, 0};
+    // the expanded rows are produced by the tiled path only
+    const ClusterPlan plan =
+        (cluster_ok && p.expanded_row == nullptr) ? plan_cluster(p, cluster_smem_max) : ClusterPlan{0, 0, 0};
     if (plan.ctas > 0) {
         cudaLaunchConfig_t cfg = {};
         cudaLaunchAttribute attr[2];
@@ -683,7 +763,9 @@ cudaError_t launch_layout(const LayoutParams& p, cudaStream_t stream) {
 
     const size_t smem_count =
         4 * (static_cast<size_t>(p.R) * kTileWords + static_cast<size_t>(p.num_nodes) * kTileWords + p.E);
-    const size_t smem_rows = 4 * (static_cast<size_t>(p.R) + 1 + 2 * static_cast<size_t>(p.R) * kTileWords);
+    size_t smem_rows = 4 * (static_cast<size_t>(p.R) + 1 + 2 * static_cast<size_t>(p.R) * kTileWords);
+    if (p.expanded_row)
+        smem_rows += 4 * (static_cast<size_t>(kTileTokens) * p.K + 9 * static_cast<size_t>(p.E));
     const int grid_tiles = p.num_tiles > 0 ? p.num_tiles : 1;
     cudaError_t e = launch_pdl(layout_count_kernel, dim3(grid_tiles), dim3(kThreads), smem_count, stream, p);
     if (e != cudaSuccess) return e;

@@ -96,8 +96,11 @@ typedef struct ep_layout {
                                              or NULL; needs R | T                        */
     int32_t* token_offset;          /* [T+1] exclusive prefix over tokens of n(t) (rows
                                              numbered token by token; [T] = N), or NULL.
-                                             When present, ep_dispatch uses it to give
-                                             every CTA the same number of rows          */
+                                             The bulk-copy dispatch alternative uses it
+                                             to give every CTA the same number of rows  */
+    int32_t* expanded_row;          /* [T,K] expanded (per-expert) row of each valid
+                                             (t, k), -1 if masked, or NULL; see
+                                             ep_dispatch_expanded                        */
 } ep_layout_t;
 
 /* Bytes of device workspace ep_get_layout needs for these sizes (>= 16). */
@@ -122,8 +125,12 @@ int64_t ep_recv_capacity_bound(int num_tokens, int num_topk, int num_ranks);
  *                 ranks_per_node consecutive ranks, the tokens with any expert
  *                 in that group.
  * expert_alignment >= 1; only expert_offset uses it.
- * out             the layout arrays (num_tokens_per_node, src_dst_count and
- *                 token_offset may be NULL; src_dst_count non-NULL needs R | T).
+ * out             the layout arrays (num_tokens_per_node, src_dst_count,
+ *                 token_offset and expanded_row may be NULL; src_dst_count
+ *                 non-NULL needs R | T).  expanded_row: expert e's valid
+ *                 (t, k) entries take rows expert_offset[e] + 0, 1, ... in
+ *                 (token, k) order; rows between expert e's count and the next
+ *                 aligned offset are padding.
  * workspace       device scratch of ws_bytes >= ep_layout_workspace_bytes(...);
  *                 its contents need no initialisation and are garbage after.
  * Results depend only on topk_idx (no atomics decide any order).
@@ -217,6 +224,51 @@ ep_status_t ep_combine(const void* y, int64_t num_y_rows, const int64_t* topk_id
                        const float* topk_weights, int num_tokens, int hidden, int num_topk,
                        int num_experts, int num_ranks, const ep_layout_t* layout, void* out,
                        int32_t* d_status, void* cuda_stream);
+
+/*
+ * Expanded (per-expert) receive layout ("DeepEP V2 ElasticBuffer
+ * architecture": the dispatch_copy_epilogue and combine_reduce_epilogue
+ * kernels and the TokenLayout record's linked_list_idx; "DeepEP Symmetric
+ * Memory" section 6.1: expert_alignment and the unaligned per-expert counts).
+ * Every valid top-k slot (t, k) gets its own row, grouped by expert (the
+ * experts of rank 0, then rank 1, ...) and padded so that expert e's block
+ * starts at expert_offset[e] -- the input of a grouped GEMM.  In one GPU's
+ * memory the pages' two steps (rank rows, then a per-expert copy epilogue;
+ * a per-expert weighted reduce, then the rank return) are done directly.
+ *
+ * Bound on the rows: T*K + E*(expert_alignment - 1); the exact count is
+ * expert_offset[E].
+ */
+int64_t ep_expanded_capacity_bound(int num_tokens, int num_topk, int num_experts,
+                                   int expert_alignment);
+
+/*
+ * Expanded dispatch: for every (t, k) with d = layout->expanded_row[t,k] >= 0:
+ *   recv_x[d] = x[t] (bf16 copy) or its FP8 E4M3 cast (same cast as
+ *   ep_dispatch; recv_sf row-major or column-major as there);
+ *   recv_src_idx[d] = t; recv_weight[d] = topk_weights[t,k].
+ * Padding rows are not written.  layout must come from ep_get_layout with
+ * expanded_row set.  recv_src_idx / recv_weight may be NULL (recv_weight
+ * non-NULL needs topk_weights).  Other arguments and errors as ep_dispatch.
+ */
+ep_status_t ep_dispatch_expanded(const void* x, const int64_t* topk_idx, const float* topk_weights,
+                                 int num_tokens, int hidden, int num_topk, int num_experts,
+                                 int num_ranks, const ep_layout_t* layout, int out_dtype,
+                                 int64_t recv_capacity, void* recv_x, float* recv_sf, int sf_col_major,
+                                 int32_t* recv_src_idx, float* recv_weight, int32_t* d_status,
+                                 void* cuda_stream);
+
+/*
+ * Expanded combine: out[t] = bf16_rne( sum over k ascending with
+ * d = layout->expanded_row[t,k] >= 0 of c * y[d] ), fp32 accumulation,
+ * c = topk_weights[t,k], or 1 when topk_weights is NULL.  The per-(token,
+ * slot) weighting and the reduction over slots and ranks in one pass.
+ * y bf16 [num_y_rows, H]; rows >= num_y_rows are skipped (EP_ERR_CAPACITY).
+ */
+ep_status_t ep_combine_expanded(const void* y, int64_t num_y_rows, const float* topk_weights,
+                                int num_tokens, int hidden, int num_topk, int num_experts,
+                                int num_ranks, const ep_layout_t* layout, void* out, int32_t* d_status,
+                                void* cuda_stream);
 
 /* Text for a status word (bits joined by '|'); a static string. */
 const char* ep_status_string(int32_t status);

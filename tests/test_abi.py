@@ -29,7 +29,8 @@ def declared_functions():
 def test_header_declares_the_entry_points():
     names = declared_functions()
     for n in ("ep_get_layout", "ep_dispatch", "ep_combine", "ep_layout_workspace_bytes",
-              "ep_recv_capacity_bound", "ep_status_string", "ep_abi_version"):
+              "ep_recv_capacity_bound", "ep_status_string", "ep_abi_version", "ep_dispatch_expanded",
+              "ep_combine_expanded", "ep_expanded_capacity_bound"):
         assert n in names
 
 
@@ -50,7 +51,7 @@ def test_status_strings_and_sizes(lib):
     ws = lib.ep_layout_workspace_bytes(4096, 8, 256, 8, 0)
     tiles = 16
     assert ws >= 4 * tiles * (8 + 256 + 8 * 8)
-    assert lib.ep_abi_version() == 2
+    assert lib.ep_abi_version() == 3
 
 
 def test_host_checks_reject_before_any_launch(lib):
