@@ -36,10 +36,11 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 L2_FLUSH_BYTES = 256 << 20
-def kernels_per_step(T, R):
+def kernels_per_step(T, R, expanded=False):
     """Launches of this library per step: the layout is one cluster kernel, or
-    three tiled kernels when T*R is large; dispatch and combine one each."""
-    return (1 if T * R <= (1 << 19) else 3) + 2
+    three tiled kernels when T*R is large or expanded rows are wanted;
+    dispatch and combine one each."""
+    return (1 if T * R <= (1 << 19) and not expanded else 3) + 2
 
 
 def parse_args(argv=None):
@@ -49,6 +50,9 @@ def parse_args(argv=None):
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="dsv3")
+    ap.add_argument("--path", choices=["rank", "expanded"], default="rank",
+                    help="rank: one receive row per (token, rank); expanded: one per valid (token, k), "
+                         "grouped by expert (weighted combine)")
     ap.add_argument("--no-graph", action="store_true", help="launch eagerly instead of CUDA graphs")
     ap.add_argument("--e2e-steps", type=int, default=200)
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
@@ -60,6 +64,23 @@ def parse_args(argv=None):
 # ---------------------------------------------------------------------------
 # algorithmic bytes
 # ---------------------------------------------------------------------------
+
+def algorithmic_bytes_expanded(T, H, K, E, R, M, fp8=False):
+    """Bytes per step of the expanded path, M = valid (token, k) slots.
+
+    layout:   as the rank path, plus the [T, K] expanded rows written.
+    dispatch: read x, topk_idx, topk_weights and the expanded rows; write M
+              rows of payload (+ FP8 scales), a source index and a weight each.
+    combine:  read the expanded rows, the weights and M expert-output rows;
+              write T rows.
+    """
+    b_out = 1 if fp8 else 2
+    s = 4 * (H // 128) if fp8 else 0
+    layout = T * K * 8 + T * R * 5 + T * K * 4 + 4 * (3 * E + 3 * R + 2)
+    dispatch = T * H * 2 + T * K * 12 + T * K * 4 + M * (H * b_out + s + 8)
+    combine = M * H * 2 + T * K * 8 + T * H * 2
+    return dict(layout=layout, dispatch=dispatch, combine=combine, total=layout + dispatch + combine)
+
 
 def algorithmic_bytes(T, H, K, E, R, N, weighted=False, fp8=False):
     """Bytes the method must move per step (reads + writes), by kernel.
@@ -238,12 +259,15 @@ def run_ours(args):
     idx = idx_host.to(dev)
     w = w_host.to(dev)
 
-    lay = B.alloc_layout(T, E, R, cfg.ranks_per_node, device=dev)
+    expanded = args.path == "expanded"
+    lay = B.alloc_layout(T, E, R, cfg.ranks_per_node, device=dev, K=K if expanded else None)
     ws = torch.empty(B.ep_layout_workspace_bytes(T, K, E, R, cfg.ranks_per_node), dtype=torch.uint8,
                      device=dev)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
     B.ep_get_layout(idx, E, R, lay, ws, status, cfg.ranks_per_node)
-    N = lay.num_recv            # one host read of rank_offset[R], before any timing
+    # one host read of the row count (rank_offset[R], or expert_offset[E] for the
+    # expanded rows), before any timing
+    N = int(lay.expert_offset[-1].item()) if expanded else lay.num_recv
     fp8, weighted = cfg.fp8, cfg.weighted
     recv_idx = torch.empty((N, K), dtype=torch.int32, device=dev)
     recv_w = torch.empty((N, K), dtype=torch.float32, device=dev)
@@ -262,16 +286,26 @@ def run_ours(args):
         y = recv_x
     dtype_code = B.EP_FP8_E4M3 if fp8 else B.EP_BF16
     w_comb = w if weighted else None
+    if expanded:
+        weighted = True            # the expanded combine weights every (token, k) output
+        recv_weight = torch.empty((N,), dtype=torch.float32, device=dev)
 
     def do_layout():
         B.ep_get_layout(idx, E, R, lay, ws, status, cfg.ranks_per_node)
 
     def do_dispatch():
-        B.ep_dispatch(x, idx, w, E, R, lay, recv_x, recv_idx, recv_w, recv_src, status, recv_sf=recv_sf,
-                      out_dtype=dtype_code)
+        if expanded:
+            B.ep_dispatch_expanded(x, idx, w, E, R, lay, recv_x, recv_src, recv_weight, status,
+                                   recv_sf=recv_sf, out_dtype=dtype_code)
+        else:
+            B.ep_dispatch(x, idx, w, E, R, lay, recv_x, recv_idx, recv_w, recv_src, status,
+                          recv_sf=recv_sf, out_dtype=dtype_code)
 
     def do_combine():
-        B.ep_combine(y, idx, w_comb, E, R, lay, out, status)
+        if expanded:
+            B.ep_combine_expanded(y, w, K, E, R, lay, out, status)
+        else:
+            B.ep_combine(y, idx, w_comb, E, R, lay, out, status)
 
     # eager warm-up (sets kernel attributes outside any capture)
     for _ in range(2):
@@ -382,7 +416,10 @@ def run_ours(args):
     local_total = sum(t_ld) + sum(t_combine)
     max_total = reduce_max(local_total, world, dev)
 
-    nbytes = algorithmic_bytes(T, H, K, E, R, N, weighted=weighted, fp8=fp8)
+    if expanded:
+        nbytes = algorithmic_bytes_expanded(T, H, K, E, R, int((idx >= 0).sum().item()), fp8=fp8)
+    else:
+        nbytes = algorithmic_bytes(T, H, K, E, R, N, weighted=weighted, fp8=fp8)
     value_bps = replica_value(nbytes["total"], args.steps, max_total, world)
     tokens_ps = replica_value(T, args.steps, max_total, world)
     ms_per_step = max_total / args.steps
@@ -422,7 +459,7 @@ def run_ours(args):
         "tokens_per_s": tokens_ps,
         "config": {
             "workload": cfg.description,
-            "T": T, "H": H, "E": E, "K": K, "R": R, "N": N,
+            "T": T, "H": H, "E": E, "K": K, "R": R, "N": N, "path": args.path,
             "bytes_per_step": nbytes,
             "parallelism": "replicas" if world > 1 else "single",
             "l2": "flushed (256 MiB write) before layout and before combine, outside the timed events",
@@ -431,7 +468,8 @@ def run_ours(args):
             "arithmetic": ("fp8 e4m3 dispatch with fp32 per-128-channel scales; combine of bf16 "
                            "stand-in expert rows, weighted, fp32 accumulate, bf16 out" if fp8 else
                            "bf16 row copies; combine of the dispatched rows (identity expert), "
-                           "%s, fp32 accumulate, bf16 out" % ("weighted" if weighted else "unweighted")),
+                           "%s, fp32 accumulate, bf16 out" % ("weighted" if weighted else "unweighted")) +
+                          ("; expanded rows: one per valid (token, k), grouped by expert" if expanded else ""),
         },
         "per_kernel": per_kernel,
         "roofline": {"bound": "hbm", "kernel": dominant, "achieved": achieved, "peak": peak,
@@ -439,7 +477,7 @@ def run_ours(args):
                      "traffic": recorded_traffic(dominant, args.workload),
                      "algorithmic_bytes_per_launch": nbytes[dominant], "timed_in": source[dominant]},
         "e2e": e2e,
-        "gpu_launches": kernels_per_step(T, R) * args.steps,
+        "gpu_launches": kernels_per_step(T, R, expanded) * args.steps,
         "clocks": clocks,
     }
     if world == 1 and rank == 0 and not args.no_cpu_baseline:
@@ -487,9 +525,16 @@ def run_e2e(args, B, torch, dev, x_host, idx_host, w_host, lay, ws, status, recv
         s_comp.wait_event(ev_in[b])
         s_comp.wait_event(ev_out[b])             # step i-2's output has been copied out
         B.ep_get_layout(idd[b], E, R, lay, ws, status, cfg.ranks_per_node, stream=s_comp)
-        B.ep_dispatch(xd[b], idd[b], wd[b], E, R, lay, recv_x, recv_idx, recv_w, recv_src, status,
-                      recv_sf=recv_sf, out_dtype=B.EP_FP8_E4M3 if cfg.fp8 else B.EP_BF16, stream=s_comp)
-        B.ep_combine(y, idd[b], wd[b] if cfg.weighted else None, E, R, lay, outd[b], status, stream=s_comp)
+        dtype_code = B.EP_FP8_E4M3 if cfg.fp8 else B.EP_BF16
+        if args.path == "expanded":
+            B.ep_dispatch_expanded(xd[b], idd[b], wd[b], E, R, lay, recv_x, recv_src, None, status,
+                                   recv_sf=recv_sf, out_dtype=dtype_code, stream=s_comp)
+            B.ep_combine_expanded(y, wd[b], idd[b].shape[1], E, R, lay, outd[b], status, stream=s_comp)
+        else:
+            B.ep_dispatch(xd[b], idd[b], wd[b], E, R, lay, recv_x, recv_idx, recv_w, recv_src, status,
+                          recv_sf=recv_sf, out_dtype=dtype_code, stream=s_comp)
+            B.ep_combine(y, idd[b], wd[b] if cfg.weighted else None, E, R, lay, outd[b], status,
+                         stream=s_comp)
         ev_comp[b].record(s_comp)
         with torch.cuda.stream(s_out):
             s_out.wait_event(ev_comp[b])
