@@ -65,6 +65,11 @@ _lib.ep_dispatch_expanded.argtypes = [_vp, _vp, _vp, _i, _i, _i, _i, _i, ctypes.
 _lib.ep_combine_expanded.restype = ctypes.c_int32
 _lib.ep_combine_expanded.argtypes = [_vp, _i64, _vp, _i, _i, _i, _i, _i, ctypes.POINTER(ep_layout_t), _vp,
                                      _vp, _vp]
+_lib.ep_combine_topk_weights.restype = ctypes.c_int32
+_lib.ep_combine_topk_weights.argtypes = [_vp, _i64, _i, _i, _i, _i, ctypes.POINTER(ep_layout_t), _vp, _vp,
+                                         _vp]
+_lib.ep_accumulate_expert_stats.restype = ctypes.c_int32
+_lib.ep_accumulate_expert_stats.argtypes = [ctypes.POINTER(ep_layout_t), _i, _vp, _vp]
 _lib.ep_status_string.restype = ctypes.c_char_p
 _lib.ep_status_string.argtypes = [ctypes.c_int32]
 _lib.ep_abi_version.restype = _i
@@ -202,6 +207,22 @@ def ep_combine_expanded(y, topk_weights, num_topk, num_experts, num_ranks, layou
                                     num_ranks, ctypes.byref(layout.c), _ptr(out), _ptr(d_status),
                                     _stream(stream))
     return _check(code, "ep_combine_expanded")
+
+
+def ep_combine_topk_weights(recv_topk_weights, num_experts, num_ranks, layout, combined, d_status,
+                            stream=None):
+    T, K = combined.shape
+    assert recv_topk_weights.is_contiguous() and combined.is_contiguous()
+    code = _lib.ep_combine_topk_weights(_ptr(recv_topk_weights), recv_topk_weights.shape[0], T, K,
+                                        num_experts, num_ranks, ctypes.byref(layout.c), _ptr(combined),
+                                        _ptr(d_status), _stream(stream))
+    return _check(code, "ep_combine_topk_weights")
+
+
+def ep_accumulate_expert_stats(layout, num_experts, stats, stream=None):
+    assert stats.dtype == torch.int64 and stats.is_contiguous()
+    code = _lib.ep_accumulate_expert_stats(ctypes.byref(layout.c), num_experts, _ptr(stats), _stream(stream))
+    return _check(code, "ep_accumulate_expert_stats")
 
 
 def ep_combine(y, topk_idx, topk_weights, num_experts, num_ranks, layout, out, d_status, stream=None):

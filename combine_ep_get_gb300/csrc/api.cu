@@ -293,6 +293,40 @@ ep_status_t ep_combine_expanded(const void* y, int64_t num_y_rows, const float* 
     return e == cudaSuccess ? EP_OK : EP_ERR_CUDA;
 }
 
+ep_status_t ep_combine_topk_weights(const float* recv_topk_weights, int64_t num_rows, int T, int K, int E,
+                                   int R, const ep_layout_t* layout, float* combined_topk_weights,
+                                   int32_t* d_status, void* cuda_stream) {
+    if (!layout || !d_status) return EP_ERR_INVALID_ARG;
+    ep_status_t s = check_shape(T, K, E, R);
+    if (s != EP_OK) return s;
+    if (num_rows < 0 || num_rows > INT32_MAX) return EP_ERR_INVALID_ARG;
+    if (num_rows > 0 && !ok_ptr(recv_topk_weights)) return EP_ERR_INVALID_ARG;
+    if (T > 0 && (!ok_ptr(combined_topk_weights) || !ok_ptr(layout->dst_row))) return EP_ERR_INVALID_ARG;
+    if (T == 0) return EP_OK;
+    epg::CombineWeightsParams p{};
+    p.recv_topk_weights = recv_topk_weights;
+    p.num_rows = num_rows;
+    p.dst_row = layout->dst_row;
+    p.T = T;
+    p.K = K;
+    p.R = R;
+    p.combined = combined_topk_weights;
+    p.status = d_status;
+    return epg::launch_combine_topk_weights(p, static_cast<cudaStream_t>(cuda_stream)) == cudaSuccess
+               ? EP_OK
+               : EP_ERR_CUDA;
+}
+
+ep_status_t ep_accumulate_expert_stats(const ep_layout_t* layout, int E, int64_t* stats, void* cuda_stream) {
+    if (!layout || E < 1) return EP_ERR_INVALID_ARG;
+    if (E > EP_MAX_EXPERTS) return EP_ERR_UNSUPPORTED;
+    if (!ok_ptr(layout->num_tokens_per_expert) || !ok_ptr(stats)) return EP_ERR_INVALID_ARG;
+    return epg::launch_accumulate_expert_stats(layout->num_tokens_per_expert, E, stats,
+                                               static_cast<cudaStream_t>(cuda_stream)) == cudaSuccess
+               ? EP_OK
+               : EP_ERR_CUDA;
+}
+
 const char* ep_status_string(int32_t status) {
     static const char* const kNames[6] = {"invalid_arg", "unsupported", "invalid_index",
                                           "capacity",    "timeout",     "cuda"};

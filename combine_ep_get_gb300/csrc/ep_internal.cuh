@@ -78,6 +78,15 @@ struct CombineParams {
     int chunk_vecs;         // 16-byte vectors per piece
 };
 
+struct CombineWeightsParams {
+    const float* recv_topk_weights;
+    int64_t num_rows;
+    const int32_t* dst_row;
+    int T, K, R;
+    float* combined;
+    int32_t* status;
+};
+
 struct DeviceInfo {
     int device;
     int num_sms;
@@ -92,6 +101,8 @@ cudaError_t launch_layout(const LayoutParams& p, cudaStream_t stream);
 cudaError_t launch_dispatch_bf16(DispatchParams p, cudaStream_t stream);
 cudaError_t launch_dispatch_fp8(DispatchParams p, cudaStream_t stream);
 cudaError_t launch_combine(CombineParams p, bool weighted, cudaStream_t stream);
+cudaError_t launch_combine_topk_weights(const CombineWeightsParams& p, cudaStream_t stream);
+cudaError_t launch_accumulate_expert_stats(const int32_t* counts, int E, int64_t* stats, cudaStream_t stream);
 
 // Launch with programmatic dependent launch allowed: the kernel may begin
 // while the previous kernel on the stream is still running, and must call

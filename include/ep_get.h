@@ -270,6 +270,30 @@ ep_status_t ep_combine_expanded(const void* y, int64_t num_y_rows, const float* 
                                 int num_ranks, const ep_layout_t* layout, void* out, int32_t* d_status,
                                 void* cuda_stream);
 
+/*
+ * Combined top-k weights ("DeepEP Symmetric Memory" section 9.2: combine
+ * returns combined_topk_weights).  For every token t and slot k:
+ *   combined_topk_weights[t,k] = sum over ranks r holding t (ascending, fp32)
+ *                                of recv_topk_weights[dst_row[t,r], k].
+ * Each slot's weight travels only in the row of the rank holding its expert,
+ * so for received weights that were not modified this returns topk_weights for
+ * valid slots and 0 for masked ones.  recv_topk_weights fp32 [num_rows, K]
+ * (as written by ep_dispatch, possibly updated by the experts);
+ * combined_topk_weights fp32 [T, K].  Rows >= num_rows set EP_ERR_CAPACITY.
+ */
+ep_status_t ep_combine_topk_weights(const float* recv_topk_weights, int64_t num_rows, int num_tokens,
+                                    int num_topk, int num_experts, int num_ranks,
+                                    const ep_layout_t* layout, float* combined_topk_weights,
+                                    int32_t* d_status, void* cuda_stream);
+
+/*
+ * Cumulative receive statistics ("DeepEP Symmetric Memory" section 6.1:
+ * cumulative_local_expert_recv_stats, a load-balance monitor): adds the
+ * layout's num_tokens_per_expert to the caller's int64 counters stats[E].
+ */
+ep_status_t ep_accumulate_expert_stats(const ep_layout_t* layout, int num_experts, int64_t* stats,
+                                       void* cuda_stream);
+
 /* Text for a status word (bits joined by '|'); a static string. */
 const char* ep_status_string(int32_t status);
 

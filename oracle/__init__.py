@@ -65,6 +65,11 @@ def _load():
     lib.ep_oracle_combine_expanded.restype = ctypes.c_int
     lib.ep_oracle_combine_expanded.argtypes = [vp, ctypes.c_int64, vp, ctypes.c_int, ctypes.c_int,
                                                ctypes.c_int, ctypes.c_int, vp, vp]
+    lib.ep_oracle_combine_topk_weights.restype = ctypes.c_int
+    lib.ep_oracle_combine_topk_weights.argtypes = [vp, ctypes.c_int64, ctypes.c_int, ctypes.c_int,
+                                                   ctypes.c_int, vp, vp]
+    lib.ep_oracle_accumulate_expert_stats.restype = None
+    lib.ep_oracle_accumulate_expert_stats.argtypes = [vp, ctypes.c_int, vp]
     for name in ("ep_oracle_e4m3_encode_array", "ep_oracle_e4m3_decode_array",
                  "ep_oracle_float_to_bf16_array"):
         getattr(lib, name).restype = None
@@ -243,6 +248,27 @@ def combine_expanded(y_bits, topk_weights, expanded_row, weighted=True):
     status = lib.ep_oracle_combine_expanded(_p(y_bits), y_bits.shape[0], _p(topk_weights),
                                             1 if weighted else 0, T, H, K, _p(expanded_row), _p(out))
     return out[:T], status
+
+
+def combine_topk_weights(recv_topk_weights, dst_row):
+    """Combined top-k weights (see ep_oracle_combine_topk_weights): float32 [T, K]."""
+    lib = _load()
+    rw = np.ascontiguousarray(recv_topk_weights, dtype=np.float32)
+    dst_row = np.ascontiguousarray(dst_row, dtype=np.int32)
+    T, R = dst_row.shape
+    K = rw.shape[1]
+    out = np.zeros((max(T, 1), K), np.float32)
+    status = lib.ep_oracle_combine_topk_weights(_p(rw), rw.shape[0], T, K, R, _p(dst_row), _p(out))
+    return out[:T], status
+
+
+def accumulate_expert_stats(num_tokens_per_expert, stats):
+    """stats (int64, updated in place) += num_tokens_per_expert."""
+    lib = _load()
+    cnt = np.ascontiguousarray(num_tokens_per_expert, dtype=np.int32)
+    assert stats.dtype == np.int64 and stats.flags.c_contiguous
+    lib.ep_oracle_accumulate_expert_stats(_p(cnt), cnt.size, _p(stats))
+    return stats
 
 
 def fp8_cast_row(x_bits_row):

@@ -483,3 +483,35 @@ int ep_oracle_combine_expanded(const uint16_t* y, int64_t num_y_rows, const floa
     }
     return status;
 }
+
+/* ------------------------------------------------------------------------ */
+/* Combined top-k weights: [P1 section 9.2] combine returns                 */
+/* combined_topk_weights.  For every token t and slot k: the fp32 sum over  */
+/* the ranks r holding t (ascending) of the received row's weight in slot k. */
+/* Rows at or beyond num_rows are skipped and flagged.                      */
+/* ------------------------------------------------------------------------ */
+
+int ep_oracle_combine_topk_weights(const float* recv_topk_weights, int64_t num_rows, int T, int K,
+                                   int R, const int32_t* dst_row, float* combined)
+{
+    int status = OR_OK;
+    for (int t = 0; t < T; ++t)
+        for (int k = 0; k < K; ++k) {
+            float acc = 0.0f;
+            for (int r = 0; r < R; ++r) {
+                int32_t d = dst_row[(int64_t)t * R + r];
+                if (d < 0) continue;
+                if ((int64_t)d >= num_rows) { status |= OR_CAPACITY; continue; }
+                acc += recv_topk_weights[(int64_t)d * K + k];
+            }
+            combined[(int64_t)t * K + k] = acc;
+        }
+    return status;
+}
+
+/* Cumulative receive statistics: [P1 section 6.1]                          */
+/* cumulative_local_expert_recv_stats -- stats[e] += tokens routed to e.    */
+void ep_oracle_accumulate_expert_stats(const int32_t* num_tokens_per_expert, int E, int64_t* stats)
+{
+    for (int e = 0; e < E; ++e) stats[e] += num_tokens_per_expert[e];
+}

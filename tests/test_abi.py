@@ -30,7 +30,8 @@ def test_header_declares_the_entry_points():
     names = declared_functions()
     for n in ("ep_get_layout", "ep_dispatch", "ep_combine", "ep_layout_workspace_bytes",
               "ep_recv_capacity_bound", "ep_status_string", "ep_abi_version", "ep_dispatch_expanded",
-              "ep_combine_expanded", "ep_expanded_capacity_bound"):
+              "ep_combine_expanded", "ep_expanded_capacity_bound", "ep_combine_topk_weights",
+              "ep_accumulate_expert_stats"):
         assert n in names
 
 

@@ -137,3 +137,44 @@ def test_combine_capacity_flag():
     g = (bf16_bits(out).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
     # rows beyond the capacity are skipped on both sides
     assert np.allclose(g, ref, rtol=1e-2, atol=1e-2)
+
+
+@pytest.mark.parametrize("T,E,K,R,mask", [(4096, 256, 8, 8, 0.0), (777, 64, 6, 16, 0.2), (200, 2048, 32, 1024, 0.1)])
+def test_combined_topk_weights(T, E, K, R, mask):
+    """Bit-exact against the oracle (same fp32 order); for unmodified received
+    weights, exactly topk_weights on valid slots and 0 on masked ones."""
+    from gpu_path import B, run_dispatch, to_dev, x_tensor
+    d = make_inputs(T, 16, E, K, R, seed=T + E, mask_frac=mask)
+    idx, w, lay = _setup(d, E, R)
+    n = lay.num_recv
+    res = run_dispatch(x_tensor(d["x_bits"]), idx, w, E, R, lay, n)
+    rw = res["recv_topk_weights"]
+    rw_mod = (rw * 0.75 + 0.125).contiguous()          # weights an expert might rewrite
+    L = oracle.layout(d["topk_idx"], E, R)
+    for src, scale in ((rw, None), (rw_mod, True)):
+        comb = torch.full((T, K), -1.0, dtype=torch.float32, device="cuda")
+        st = torch.zeros(1, dtype=torch.int32, device="cuda")
+        B.ep_combine_topk_weights(src, E, R, lay, comb, st)
+        torch.cuda.synchronize()
+        assert int(st.item()) == 0
+        ref, _ = oracle.combine_topk_weights(src.cpu().numpy(), L.dst_row)
+        np.testing.assert_array_equal(comb.cpu().numpy(), ref)
+        if scale is None:
+            want = np.where(d["topk_idx"] >= 0, d["topk_weights"], 0.0).astype(np.float32)
+            np.testing.assert_array_equal(comb.cpu().numpy(), want)
+
+
+def test_expert_stats_accumulate():
+    from gpu_path import B
+    d = make_config("skewed", with_x=False)
+    c = d["cfg"]
+    idx, w, lay = _setup(d, c.E, c.R)
+    stats = torch.zeros(c.E, dtype=torch.int64, device="cuda")
+    B.ep_accumulate_expert_stats(lay, c.E, stats)
+    B.ep_accumulate_expert_stats(lay, c.E, stats)
+    torch.cuda.synchronize()
+    L = oracle.layout(d["topk_idx"], c.E, c.R)
+    ref = np.zeros(c.E, np.int64)
+    oracle.accumulate_expert_stats(L.num_tokens_per_expert, ref)
+    oracle.accumulate_expert_stats(L.num_tokens_per_expert, ref)
+    np.testing.assert_array_equal(stats.cpu().numpy(), ref)

@@ -154,3 +154,30 @@ def test_capacity_and_invalid_flags():
     good[3, 1] = -1
     L3 = oracle.layout(good, 16, 4)
     np.testing.assert_array_equal(L2.dst_row, L3.dst_row)
+
+
+def test_combined_topk_weights_closed_form():
+    """Each slot's weight travels only in the row of the rank holding its
+    expert, so combining the received weight rows returns topk_weights
+    exactly for valid slots and 0 for masked ones."""
+    T, H, E, K, R = 300, 64, 64, 6, 8
+    d, L = _case(T, H, E, K, R, seed=41, mask=0.15)
+    res = oracle.dispatch(d["x_bits"], d["topk_idx"], d["topk_weights"], E, R, L.dst_row)
+    comb, st = oracle.combine_topk_weights(res["recv_topk_weights"], L.dst_row)
+    assert st == 0
+    want = np.where(d["topk_idx"] >= 0, d["topk_weights"], 0.0).astype(np.float32)
+    np.testing.assert_array_equal(comb, want)
+    # scaled received weights combine to the scaled weights
+    comb2, _ = oracle.combine_topk_weights(res["recv_topk_weights"] * 2.0, L.dst_row)
+    np.testing.assert_array_equal(comb2, 2.0 * want)
+    # a short row count flags and skips
+    _, st = oracle.combine_topk_weights(res["recv_topk_weights"][:L.num_recv - 5], L.dst_row)
+    assert st & oracle.EP_ERR_CAPACITY
+
+
+def test_expert_stats_accumulate():
+    d, L = _case(64, 64, 16, 4, 4, seed=2)
+    stats = np.zeros(16, np.int64)
+    oracle.accumulate_expert_stats(L.num_tokens_per_expert, stats)
+    oracle.accumulate_expert_stats(L.num_tokens_per_expert, stats)
+    np.testing.assert_array_equal(stats, 2 * np.bincount(d["topk_idx"][d["topk_idx"] >= 0], minlength=16))
