@@ -54,6 +54,8 @@ def parse_args(argv=None):
                     help="rank: one receive row per (token, rank); expanded: one per valid (token, k), "
                          "grouped by expert (weighted combine)")
     ap.add_argument("--no-graph", action="store_true", help="launch eagerly instead of CUDA graphs")
+    ap.add_argument("--num-sms", type=int, default=0,
+                    help="SM-limited dispatch and combine (persistent grid of this many CTAs); 0 = whole GPU")
     ap.add_argument("--e2e-steps", type=int, default=200)
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
                     help="CPU time budget of the oracle baseline (rank 0, N=1)")
@@ -296,16 +298,16 @@ def run_ours(args):
     def do_dispatch():
         if expanded:
             B.ep_dispatch_expanded(x, idx, w, E, R, lay, recv_x, recv_src, recv_weight, status,
-                                   recv_sf=recv_sf, out_dtype=dtype_code)
+                                   recv_sf=recv_sf, out_dtype=dtype_code, num_sms=args.num_sms)
         else:
             B.ep_dispatch(x, idx, w, E, R, lay, recv_x, recv_idx, recv_w, recv_src, status,
-                          recv_sf=recv_sf, out_dtype=dtype_code)
+                          recv_sf=recv_sf, out_dtype=dtype_code, num_sms=args.num_sms)
 
     def do_combine():
         if expanded:
-            B.ep_combine_expanded(y, w, K, E, R, lay, out, status)
+            B.ep_combine_expanded(y, w, K, E, R, lay, out, status, num_sms=args.num_sms)
         else:
-            B.ep_combine(y, idx, w_comb, E, R, lay, out, status)
+            B.ep_combine(y, idx, w_comb, E, R, lay, out, status, num_sms=args.num_sms)
 
     # eager warm-up (sets kernel attributes outside any capture)
     for _ in range(2):
@@ -460,6 +462,7 @@ def run_ours(args):
         "config": {
             "workload": cfg.description,
             "T": T, "H": H, "E": E, "K": K, "R": R, "N": N, "path": args.path,
+            "num_sms": args.num_sms or "all",
             "bytes_per_step": nbytes,
             "parallelism": "replicas" if world > 1 else "single",
             "l2": "flushed (256 MiB write) before layout and before combine, outside the timed events",

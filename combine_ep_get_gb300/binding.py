@@ -53,18 +53,18 @@ _lib.ep_get_layout_static_scratch.argtypes = [_vp, _i, _i, _i, _i, _i, _i, ctype
                                               _vp, _vp]
 _lib.ep_dispatch.restype = ctypes.c_int32
 _lib.ep_dispatch.argtypes = [_vp, _vp, _vp, _i, _i, _i, _i, _i, ctypes.POINTER(ep_layout_t), _i,
-                             _i64, _vp, _vp, _i, _vp, _vp, _vp, _vp, _vp]
+                             _i64, _vp, _vp, _i, _vp, _vp, _vp, _i, _vp, _vp]
 _lib.ep_combine.restype = ctypes.c_int32
 _lib.ep_combine.argtypes = [_vp, _i64, _vp, _vp, _i, _i, _i, _i, _i, ctypes.POINTER(ep_layout_t),
-                            _vp, _vp, _vp]
+                            _vp, _i, _vp, _vp]
 _lib.ep_expanded_capacity_bound.restype = _i64
 _lib.ep_expanded_capacity_bound.argtypes = [_i, _i, _i, _i]
 _lib.ep_dispatch_expanded.restype = ctypes.c_int32
 _lib.ep_dispatch_expanded.argtypes = [_vp, _vp, _vp, _i, _i, _i, _i, _i, ctypes.POINTER(ep_layout_t), _i,
-                                      _i64, _vp, _vp, _i, _vp, _vp, _vp, _vp]
+                                      _i64, _vp, _vp, _i, _vp, _vp, _i, _vp, _vp]
 _lib.ep_combine_expanded.restype = ctypes.c_int32
 _lib.ep_combine_expanded.argtypes = [_vp, _i64, _vp, _i, _i, _i, _i, _i, ctypes.POINTER(ep_layout_t), _vp,
-                                     _vp, _vp]
+                                     _i, _vp, _vp]
 _lib.ep_combine_topk_weights.restype = ctypes.c_int32
 _lib.ep_combine_topk_weights.argtypes = [_vp, _i64, _i, _i, _i, _i, ctypes.POINTER(ep_layout_t), _vp, _vp,
                                          _vp]
@@ -173,7 +173,7 @@ def ep_get_layout_static_scratch(topk_idx, num_experts, num_ranks, layout, d_sta
 
 def ep_dispatch(x, topk_idx, topk_weights, num_experts, num_ranks, layout, recv_x, recv_topk_idx,
                 recv_topk_weights, recv_src_idx, d_status, recv_sf=None, out_dtype=EP_BF16,
-                sf_col_major=False, stream=None):
+                sf_col_major=False, num_sms=0, stream=None):
     T, H = x.shape
     K = topk_idx.shape[1]
     assert x.element_size() == 2 and x.is_contiguous() and recv_x.is_contiguous()
@@ -181,30 +181,31 @@ def ep_dispatch(x, topk_idx, topk_weights, num_experts, num_ranks, layout, recv_
     code = _lib.ep_dispatch(_ptr(x), _ptr(topk_idx), _ptr(topk_weights), T, H, K, num_experts,
                             num_ranks, ctypes.byref(layout.c), out_dtype, capacity, _ptr(recv_x),
                             _ptr(recv_sf), 1 if sf_col_major else 0, _ptr(recv_topk_idx),
-                            _ptr(recv_topk_weights), _ptr(recv_src_idx), _ptr(d_status),
+                            _ptr(recv_topk_weights), _ptr(recv_src_idx), num_sms, _ptr(d_status),
                             _stream(stream))
     return _check(code, "ep_dispatch")
 
 
 def ep_dispatch_expanded(x, topk_idx, topk_weights, num_experts, num_ranks, layout, recv_x, recv_src_idx,
                          recv_weight, d_status, recv_sf=None, out_dtype=EP_BF16, sf_col_major=False,
-                         stream=None):
+                         num_sms=0, stream=None):
     T, H = x.shape
     K = topk_idx.shape[1]
     assert x.element_size() == 2 and x.is_contiguous() and recv_x.is_contiguous()
     code = _lib.ep_dispatch_expanded(_ptr(x), _ptr(topk_idx), _ptr(topk_weights), T, H, K, num_experts,
                                      num_ranks, ctypes.byref(layout.c), out_dtype, recv_x.shape[0],
                                      _ptr(recv_x), _ptr(recv_sf), 1 if sf_col_major else 0,
-                                     _ptr(recv_src_idx), _ptr(recv_weight), _ptr(d_status), _stream(stream))
+                                     _ptr(recv_src_idx), _ptr(recv_weight), num_sms, _ptr(d_status),
+                                     _stream(stream))
     return _check(code, "ep_dispatch_expanded")
 
 
 def ep_combine_expanded(y, topk_weights, num_topk, num_experts, num_ranks, layout, out, d_status,
-                        stream=None):
+                        num_sms=0, stream=None):
     T, H = out.shape
     assert y.element_size() == 2 and y.is_contiguous() and out.is_contiguous()
     code = _lib.ep_combine_expanded(_ptr(y), y.shape[0], _ptr(topk_weights), T, H, num_topk, num_experts,
-                                    num_ranks, ctypes.byref(layout.c), _ptr(out), _ptr(d_status),
+                                    num_ranks, ctypes.byref(layout.c), _ptr(out), num_sms, _ptr(d_status),
                                     _stream(stream))
     return _check(code, "ep_combine_expanded")
 
@@ -225,11 +226,12 @@ def ep_accumulate_expert_stats(layout, num_experts, stats, stream=None):
     return _check(code, "ep_accumulate_expert_stats")
 
 
-def ep_combine(y, topk_idx, topk_weights, num_experts, num_ranks, layout, out, d_status, stream=None):
+def ep_combine(y, topk_idx, topk_weights, num_experts, num_ranks, layout, out, d_status, num_sms=0,
+               stream=None):
     T, H = out.shape
     K = topk_idx.shape[1]
     assert y.element_size() == 2 and y.is_contiguous() and out.is_contiguous()
     code = _lib.ep_combine(_ptr(y), y.shape[0], _ptr(topk_idx), _ptr(topk_weights), T, H, K,
-                           num_experts, num_ranks, ctypes.byref(layout.c), _ptr(out), _ptr(d_status),
-                           _stream(stream))
+                           num_experts, num_ranks, ctypes.byref(layout.c), _ptr(out), num_sms,
+                           _ptr(d_status), _stream(stream))
     return _check(code, "ep_combine")

@@ -48,7 +48,7 @@ ep_status_t check_shape(int T, int K, int E, int R) {
 
 extern "C" {
 
-int ep_abi_version(void) { return 3; }
+int ep_abi_version(void) { return 4; }
 
 size_t ep_layout_workspace_bytes(int num_tokens, int num_topk, int num_experts, int num_ranks,
                                  int ranks_per_node) {
@@ -120,8 +120,8 @@ ep_status_t ep_dispatch(const void* x, const int64_t* topk_idx, const float* top
                         int H, int K, int E, int R, const ep_layout_t* layout, int out_dtype,
                         int64_t recv_capacity, void* recv_x, float* recv_sf, int sf_col_major,
                         int32_t* recv_topk_idx, float* recv_topk_weights, int32_t* recv_src_idx,
-                        int32_t* d_status, void* cuda_stream) {
-    if (!layout || !d_status) return EP_ERR_INVALID_ARG;
+                        int num_sms, int32_t* d_status, void* cuda_stream) {
+    if (!layout || !d_status || num_sms < 0) return EP_ERR_INVALID_ARG;
     ep_status_t s = check_shape(T, K, E, R);
     if (s != EP_OK) return s;
     if (H < 1) return EP_ERR_INVALID_ARG;
@@ -166,6 +166,7 @@ ep_status_t ep_dispatch(const void* x, const int64_t* topk_idx, const float* top
     p.recv_topk_idx = recv_topk_idx;
     p.recv_topk_weights = recv_topk_weights;
     p.recv_src_idx = recv_src_idx;
+    p.num_sms = num_sms;
     p.status = d_status;
     cudaStream_t st = static_cast<cudaStream_t>(cuda_stream);
     const cudaError_t e = out_dtype == EP_BF16 ? epg::launch_dispatch_bf16(p, st)
@@ -175,8 +176,9 @@ ep_status_t ep_dispatch(const void* x, const int64_t* topk_idx, const float* top
 
 ep_status_t ep_combine(const void* y, int64_t num_y_rows, const int64_t* topk_idx,
                        const float* topk_weights, int T, int H, int K, int E, int R,
-                       const ep_layout_t* layout, void* out, int32_t* d_status, void* cuda_stream) {
-    if (!layout || !d_status) return EP_ERR_INVALID_ARG;
+                       const ep_layout_t* layout, void* out, int num_sms, int32_t* d_status,
+                       void* cuda_stream) {
+    if (!layout || !d_status || num_sms < 0) return EP_ERR_INVALID_ARG;
     ep_status_t s = check_shape(T, K, E, R);
     if (s != EP_OK) return s;
     if (H < 1 || H % 8 != 0) return EP_ERR_INVALID_ARG;
@@ -199,6 +201,7 @@ ep_status_t ep_combine(const void* y, int64_t num_y_rows, const int64_t* topk_id
     p.R = R;
     p.experts_per_rank = E / R;
     p.out = static_cast<uint8_t*>(out);
+    p.num_sms = num_sms;
     p.status = d_status;
     const cudaError_t e =
         epg::launch_combine(p, topk_weights != nullptr, static_cast<cudaStream_t>(cuda_stream));
@@ -213,9 +216,9 @@ int64_t ep_expanded_capacity_bound(int num_tokens, int num_topk, int num_experts
 ep_status_t ep_dispatch_expanded(const void* x, const int64_t* topk_idx, const float* topk_weights, int T,
                                  int H, int K, int E, int R, const ep_layout_t* layout, int out_dtype,
                                  int64_t recv_capacity, void* recv_x, float* recv_sf, int sf_col_major,
-                                 int32_t* recv_src_idx, float* recv_weight, int32_t* d_status,
+                                 int32_t* recv_src_idx, float* recv_weight, int num_sms, int32_t* d_status,
                                  void* cuda_stream) {
-    if (!layout || !d_status) return EP_ERR_INVALID_ARG;
+    if (!layout || !d_status || num_sms < 0) return EP_ERR_INVALID_ARG;
     ep_status_t s = check_shape(T, K, E, R);
     if (s != EP_OK) return s;
     if (H < 1) return EP_ERR_INVALID_ARG;
@@ -255,6 +258,7 @@ ep_status_t ep_dispatch_expanded(const void* x, const int64_t* topk_idx, const f
     p.sf_stride = (recv_capacity + 3) / 4 * 4;
     p.recv_src_idx = recv_src_idx;
     p.recv_weight = recv_weight;
+    p.num_sms = num_sms;
     p.status = d_status;
     cudaStream_t st = static_cast<cudaStream_t>(cuda_stream);
     const cudaError_t e = out_dtype == EP_BF16 ? epg::launch_dispatch_bf16(p, st)
@@ -263,9 +267,9 @@ ep_status_t ep_dispatch_expanded(const void* x, const int64_t* topk_idx, const f
 }
 
 ep_status_t ep_combine_expanded(const void* y, int64_t num_y_rows, const float* topk_weights, int T, int H,
-                                int K, int E, int R, const ep_layout_t* layout, void* out, int32_t* d_status,
-                                void* cuda_stream) {
-    if (!layout || !d_status) return EP_ERR_INVALID_ARG;
+                                int K, int E, int R, const ep_layout_t* layout, void* out, int num_sms,
+                                int32_t* d_status, void* cuda_stream) {
+    if (!layout || !d_status || num_sms < 0) return EP_ERR_INVALID_ARG;
     ep_status_t s = check_shape(T, K, E, R);
     if (s != EP_OK) return s;
     if (H < 1 || H % 8 != 0) return EP_ERR_INVALID_ARG;
@@ -287,6 +291,7 @@ ep_status_t ep_combine_expanded(const void* y, int64_t num_y_rows, const float* 
     p.R = R;
     p.experts_per_rank = E / R;
     p.out = static_cast<uint8_t*>(out);
+    p.num_sms = num_sms;
     p.status = d_status;
     const cudaError_t e =
         epg::launch_combine(p, topk_weights != nullptr, static_cast<cudaStream_t>(cuda_stream));

@@ -32,20 +32,20 @@ constexpr int kThreads = EP_COMBINE_THREADS;
 #endif
 constexpr int kBatch = EP_COMBINE_BATCH;
 
-// kExpanded: the token's source rows are its expanded rows (one per valid
-// top-k slot, coefficient = that slot's weight) instead of one row per rank.
-template <bool kWeighted, bool kExpanded>
-__global__ void __launch_bounds__(kThreads, EP_COMBINE_MIN_BLOCKS) combine_kernel(const CombineParams p) {
-    __shared__ int s_rows[EP_MAX_TOPK];
-    __shared__ float s_coef[EP_MAX_TOPK];
-    __shared__ int s_n;
-    const int64_t it = blockIdx.x;
+// SM-limited mode: CTAs of kSmGroups x kThreads threads, one per SM, each
+// group looping over (token, piece) items.
+constexpr int kSmGroups = 8;
+
+// One (token, piece) item, by one group of kThreads threads.  kExpanded: the
+// token's source rows are its expanded rows (one per valid top-k slot,
+// coefficient = that slot's weight) instead of one row per rank.
+template <bool kWeighted, bool kExpanded, int kGroups>
+__device__ __forceinline__ void combine_item(const CombineParams& p, int64_t it, int group, int gtid,
+                                             int* s_rows, float* s_coef, int* s_n) {
     const int t = static_cast<int>(it / p.chunks);
     const int c = static_cast<int>(it - static_cast<int64_t>(t) * p.chunks);
-    pdl_wait();
-
-    if (threadIdx.x < 32) {
-        const int lane = threadIdx.x;
+    if (gtid < 32) {
+        const int lane = gtid;
         int64_t e_l = -1;
         float w_l = 0.0f;
         if (kWeighted && lane < p.K) {
@@ -87,17 +87,20 @@ __global__ void __launch_bounds__(kThreads, EP_COMBINE_MIN_BLOCKS) combine_kerne
             if (lane == 0) atomicOr(p.status, EP_ERR_INVALID_INDEX);
             n = EP_MAX_TOPK;
         }
-        if (lane == 0) s_n = n;
+        if (lane == 0) *s_n = n;
         if (__any_sync(0xffffffffu, cap_bad) && lane == 0 && c == 0) atomicOr(p.status, EP_ERR_CAPACITY);
     }
-    __syncthreads();
+    if (kGroups > 1)
+        named_barrier(1 + group, kThreads);
+    else
+        __syncthreads();
 
-    const int n = s_n;
+    const int n = *s_n;
     const int n_vec = p.H / 8;
     const int v_begin = c * p.chunk_vecs;
     const int v_end = min(n_vec, v_begin + p.chunk_vecs);
     const int64_t row_bytes = static_cast<int64_t>(p.H) * 2;
-    for (int v = v_begin + threadIdx.x; v < v_end; v += kThreads) {
+    for (int v = v_begin + gtid; v < v_end; v += kThreads) {
         float acc[8];
 #pragma unroll
         for (int q = 0; q < 8; ++q) acc[q] = 0.0f;
@@ -139,6 +142,43 @@ __global__ void __launch_bounds__(kThreads, EP_COMBINE_MIN_BLOCKS) combine_kerne
     }
 }
 
+// kGroups == 1: one CTA per item.  kGroups > 1 (SM-limited mode): several
+// groups per CTA, each looping over items with a stride and synchronising on
+// its own named barrier.
+template <bool kWeighted, bool kExpanded, int kGroups>
+__global__ void __launch_bounds__(kThreads * kGroups, kGroups == 1 ? EP_COMBINE_MIN_BLOCKS : 1)
+    combine_kernel(const CombineParams p) {
+    __shared__ int s_rows_all[kGroups][EP_MAX_TOPK];
+    __shared__ float s_coef_all[kGroups][EP_MAX_TOPK];
+    __shared__ int s_n_all[kGroups];
+    pdl_wait();
+    if (kGroups == 1) {
+        combine_item<kWeighted, kExpanded, 1>(p, blockIdx.x, 0, threadIdx.x, s_rows_all[0], s_coef_all[0],
+                                               &s_n_all[0]);
+    } else {
+        const int group = static_cast<int>(threadIdx.x) / kThreads;
+        const int gtid = static_cast<int>(threadIdx.x) % kThreads;
+        const int64_t n_items = static_cast<int64_t>(p.T) * p.chunks;
+        for (int64_t it = static_cast<int64_t>(blockIdx.x) * kGroups + group; it < n_items;
+             it += static_cast<int64_t>(gridDim.x) * kGroups) {
+            named_barrier(1 + group, kThreads);   // the previous item's list is consumed
+            combine_item<kWeighted, kExpanded, kGroups>(p, it, group, gtid, s_rows_all[group], s_coef_all[group],
+                                                        &s_n_all[group]);
+        }
+    }
+}
+
+template <bool kWeighted, bool kExpanded>
+cudaError_t launch_combine_t(const CombineParams& p, int64_t items, int num_sms, cudaStream_t stream) {
+    if (num_sms > 0) {
+        int64_t grid = (items + kSmGroups - 1) / kSmGroups;
+        if (grid > num_sms) grid = num_sms;
+        return launch_pdl(combine_kernel<kWeighted, kExpanded, kSmGroups>, dim3(static_cast<unsigned>(grid)),
+                          dim3(kThreads * kSmGroups), 0, stream, p);
+    }
+    return launch_pdl(combine_kernel<kWeighted, kExpanded, 1>, dim3(static_cast<unsigned>(items)), dim3(kThreads), 0,
+                      stream, p);
+}
 
 }  // namespace
 
@@ -158,15 +198,15 @@ cudaError_t launch_combine(CombineParams p, bool weighted, cudaStream_t stream) 
     chunks = (n_vec + chunk_vecs - 1) / chunk_vecs;
     p.chunks = chunks;
     p.chunk_vecs = chunk_vecs;
-    const int64_t grid = static_cast<int64_t>(p.T) * chunks;
-    if (grid < 1) return cudaSuccess;
-    const dim3 g(static_cast<unsigned>(grid)), b(kThreads);
+    const int64_t items = static_cast<int64_t>(p.T) * chunks;
+    if (items < 1) return cudaSuccess;
+    const int num_sms = p.num_sms > 0 ? (p.num_sms < di.num_sms ? p.num_sms : di.num_sms) : 0;
     if (p.expanded_row) {
-        if (weighted) return launch_pdl(combine_kernel<true, true>, g, b, 0, stream, p);
-        return launch_pdl(combine_kernel<false, true>, g, b, 0, stream, p);
+        if (weighted) return launch_combine_t<true, true>(p, items, num_sms, stream);
+        return launch_combine_t<false, true>(p, items, num_sms, stream);
     }
-    if (weighted) return launch_pdl(combine_kernel<true, false>, g, b, 0, stream, p);
-    return launch_pdl(combine_kernel<false, false>, g, b, 0, stream, p);
+    if (weighted) return launch_combine_t<true, false>(p, items, num_sms, stream);
+    return launch_combine_t<false, false>(p, items, num_sms, stream);
 }
 
 }  // namespace epg

@@ -292,30 +292,33 @@ __device__ __forceinline__ void write_expanded_metadata(const DispatchParams& p,
 constexpr int kRegThreads = 256;
 constexpr int kRegUnroll = 4;
 
-// Register path: one CTA per (token, piece); each thread loads up to
-// kRegUnroll 16-byte vectors of the piece, its warp reads the token's
-// destination rows (one lane per rank) and broadcasts them by shuffles, and
-// the thread stores its vectors to every destination.  Warps never wait for
-// one another.  kExpanded: the destinations are the token's expanded rows
-// (one per valid top-k slot) instead of one row per rank.
+// SM-limited mode: CTAs of kSmGroups groups, one per SM, each group looping
+// over (token, piece) items.
+constexpr int kSmGroups = 4;
+
+// Register path: one group of 256 threads per (token, piece); each thread
+// loads up to kRegUnroll 16-byte vectors of the piece, its warp reads the
+// token's destination rows (one lane per rank) and broadcasts them by
+// shuffles, and the thread stores its vectors to every destination.  Warps
+// never wait for one another.  kExpanded: the destinations are the token's
+// expanded rows (one per valid top-k slot) instead of one row per rank.
+// kGroups > 1 (SM-limited mode): several groups per CTA looping over items.
+// One (token, piece) item of the register path, by one group of 256 threads.
 template <bool kExpanded>
-__global__ void __launch_bounds__(kRegThreads, 6) dispatch_bf16_regs_kernel(const DispatchParams p) {
-    const int64_t it = blockIdx.x;
+__device__ __forceinline__ void dispatch_regs_item(const DispatchParams& p, int64_t it, int gtid, int warp_g,
+                                                   int lane, bool& cap_bad) {
+    const uint32_t row_bytes = static_cast<uint32_t>(p.H) * 2u;
     const int t = static_cast<int>(it / p.chunks);
     const int c = static_cast<int>(it - static_cast<int64_t>(t) * p.chunks);
-    const int warp = threadIdx.x >> 5;
-    const int lane = threadIdx.x & 31;
-    const uint32_t row_bytes = static_cast<uint32_t>(p.H) * 2u;
     const uint32_t off = static_cast<uint32_t>(c) * p.chunk_bytes;
     const uint32_t bytes = min(p.chunk_bytes, row_bytes - off);
     const int nvec = static_cast<int>(bytes / 16);
     const uint8_t* src = p.x + static_cast<int64_t>(t) * row_bytes + off;
-    pdl_wait();   // before any global access: the previous kernel may write x
     // this thread's loads and the warp's destination rows, all in flight together
     uint4 u[kRegUnroll];
 #pragma unroll
     for (int k = 0; k < kRegUnroll; ++k) {
-        const int v = threadIdx.x + k * kRegThreads;
+        const int v = gtid + k * kRegThreads;
         if (v < nvec) u[k] = ld_stream_v4(src + static_cast<size_t>(v) * 16);
     }
     const int n_dst = kExpanded ? p.K : p.R;
@@ -323,7 +326,7 @@ __global__ void __launch_bounds__(kRegThreads, 6) dispatch_bf16_regs_kernel(cons
                                     : p.dst_row + static_cast<int64_t>(t) * p.R;
     const int d0 = lane < n_dst ? drow[lane] : -1;
     const int d1 = 32 + lane < n_dst ? drow[32 + lane] : -1;   // ranks 32..63, same latency
-    if (warp == 1 && c == 0) {
+    if (warp_g == 1 && c == 0) {
         if (kExpanded) {
             write_expanded_metadata(p, t, lane);
         } else {
@@ -337,18 +340,17 @@ __global__ void __launch_bounds__(kRegThreads, 6) dispatch_bf16_regs_kernel(cons
             write_metadata(p, t, lane, all);
         }
     }
-    bool cap_bad = false;
     for (int base = 0; base < nvec; base += kRegUnroll * kRegThreads) {
         if (base > 0) {
 #pragma unroll
             for (int k = 0; k < kRegUnroll; ++k) {
-                const int v = base + threadIdx.x + k * kRegThreads;
+                const int v = base + gtid + k * kRegThreads;
                 if (v < nvec) u[k] = ld_stream_v4(src + static_cast<size_t>(v) * 16);
             }
         }
         for (int rb = 0; rb < n_dst; rb += 32) {
             const int d = rb == 0 ? d0 : rb == 32 ? d1 : (rb + lane < n_dst ? drow[rb + lane] : -1);
-            if (d >= p.capacity) cap_bad = true;
+            if (d >= p.capacity && c == 0) cap_bad = true;
             unsigned m = __ballot_sync(0xffffffffu, d >= 0 && d < p.capacity);
             while (m) {
                 const int sl = __ffs(m) - 1;
@@ -356,7 +358,7 @@ __global__ void __launch_bounds__(kRegThreads, 6) dispatch_bf16_regs_kernel(cons
                 uint8_t* dst = p.recv_x + static_cast<int64_t>(__shfl_sync(0xffffffffu, d, sl)) * row_bytes + off;
 #pragma unroll
                 for (int k = 0; k < kRegUnroll; ++k) {
-                    const int v = base + threadIdx.x + k * kRegThreads;
+                    const int v = base + gtid + k * kRegThreads;
                     if (v < nvec) {
 #if EP_DISPATCH_STORE_CS
                         st_cs_v4(dst + static_cast<size_t>(v) * 16, u[k]);
@@ -368,8 +370,26 @@ __global__ void __launch_bounds__(kRegThreads, 6) dispatch_bf16_regs_kernel(cons
             }
         }
     }
-    if (warp == 0 && c == 0 && __any_sync(0xffffffffu, cap_bad) && lane == 0)
-        atomicOr(p.status, EP_ERR_CAPACITY);
+}
+
+template <bool kExpanded, int kGroups>
+__global__ void __launch_bounds__(kRegThreads * kGroups, kGroups == 1 ? 6 : 1)
+    dispatch_bf16_regs_kernel(const DispatchParams p) {
+    const int gtid = static_cast<int>(threadIdx.x) % kRegThreads;
+    const int warp_g = gtid >> 5;   // warp within the group
+    const int lane = threadIdx.x & 31;
+    bool cap_bad = false;
+    pdl_wait();   // before any global access: the previous kernel may write x
+    if (kGroups == 1) {
+        dispatch_regs_item<kExpanded>(p, blockIdx.x, gtid, warp_g, lane, cap_bad);
+    } else {
+        const int64_t n_items = static_cast<int64_t>(p.T) * p.chunks;
+        const int group = static_cast<int>(threadIdx.x) / kRegThreads;
+        for (int64_t it = static_cast<int64_t>(blockIdx.x) * kGroups + group; it < n_items;
+             it += static_cast<int64_t>(gridDim.x) * kGroups)
+            dispatch_regs_item<kExpanded>(p, it, gtid, warp_g, lane, cap_bad);
+    }
+    if (warp_g == 0 && __any_sync(0xffffffffu, cap_bad) && lane == 0) atomicOr(p.status, EP_ERR_CAPACITY);
 }
 
 __device__ __forceinline__ uint32_t pack_e4m3x4(float a, float b, float c, float d) {
@@ -382,100 +402,114 @@ __device__ __forceinline__ uint32_t pack_e4m3x4(float a, float b, float c, float
 
 constexpr int kFp8Threads = 256;
 
-template <bool kExpanded>
-__global__ void __launch_bounds__(kFp8Threads) dispatch_fp8_kernel(const DispatchParams p) {
-    __shared__ int s_rows[EP_MAX_TOPK];
-    __shared__ int s_n;
-    const int64_t it = blockIdx.x;
-    const int t = static_cast<int>(it / p.chunks);
-    const int c = static_cast<int>(it - static_cast<int64_t>(t) * p.chunks);
-    const int warp = threadIdx.x >> 5;
+// One group of kFp8Threads threads casts one (token, piece) item per
+// iteration; kGroups > 1 (SM-limited mode): several groups per CTA, each
+// looping over items and synchronising on its own named barrier.
+template <bool kExpanded, int kGroups>
+__global__ void __launch_bounds__(kFp8Threads * kGroups) dispatch_fp8_kernel(const DispatchParams p) {
+    __shared__ int s_rows_all[kGroups][EP_MAX_TOPK];
+    __shared__ int s_n_all[kGroups];
+    const int group = kGroups == 1 ? 0 : static_cast<int>(threadIdx.x) / kFp8Threads;
+    const int gtid = kGroups == 1 ? static_cast<int>(threadIdx.x) : static_cast<int>(threadIdx.x) % kFp8Threads;
+    const int warp = gtid >> 5;
     const int lane = threadIdx.x & 31;
+    int* s_rows = s_rows_all[group];
+    const int64_t n_items = static_cast<int64_t>(p.T) * p.chunks;
     pdl_wait();
 
-    if (warp == 0) {
-        int n = 0;
-        bool cap_bad = false;
-        const int n_dst = kExpanded ? p.K : p.R;
-        const int32_t* drow = kExpanded ? p.expanded_row + static_cast<int64_t>(t) * p.K
-                                        : p.dst_row + static_cast<int64_t>(t) * p.R;
-        for (int rb = 0; rb < n_dst; rb += 32) {
-            const int r = rb + lane;
-            const int d = r < n_dst ? drow[r] : -1;
-            const bool ok = d >= 0 && d < p.capacity;
-            if (d >= p.capacity) cap_bad = true;
-            const unsigned m = __ballot_sync(0xffffffffu, ok);
-            const int pos = n + __popc(m & ((1u << lane) - 1u));
-            // A layout from ep_get_layout has at most K <= 32 ranks per token;
-            // a foreign dst_row with more is cut off and flagged.
-            if (ok && pos < EP_MAX_TOPK) s_rows[pos] = d;
-            n += __popc(m);
-        }
-        if (n > EP_MAX_TOPK) {
-            if (lane == 0) atomicOr(p.status, EP_ERR_INVALID_INDEX);
-            n = EP_MAX_TOPK;
-        }
-        if (lane == 0) s_n = n;
-        if (__any_sync(0xffffffffu, cap_bad) && lane == 0 && c == 0) atomicOr(p.status, EP_ERR_CAPACITY);
-    } else if (warp == 1 && c == 0) {
-        if (kExpanded) {
-            write_expanded_metadata(p, t, lane);
-        } else {
-            CtaWork all;
-            all.first = 0;
-            all.count = 0;
-            all.stride = 1;
-            all.lo = INT32_MIN;
-            all.hi = INT32_MAX;
-            all.balanced = 0;
-            write_metadata(p, t, lane, all);
-        }
-    }
-    __syncthreads();
+    for (int64_t it = static_cast<int64_t>(blockIdx.x) * kGroups + group; it < n_items;
+         it += static_cast<int64_t>(gridDim.x) * kGroups) {
+        const int t = static_cast<int>(it / p.chunks);
+        const int c = static_cast<int>(it - static_cast<int64_t>(t) * p.chunks);
+        if (kGroups > 1) named_barrier(1 + group, kFp8Threads);   // previous list consumed
 
-    const int n = s_n;
-    const int nb = p.H / 128;
-    const int b_begin = c * p.chunk_blocks;
-    const int b_end = min(nb, b_begin + p.chunk_blocks);
-    const int half = lane >> 4;
-    const int sub = lane & 15;
-    const uint8_t* xrow = p.x + static_cast<int64_t>(t) * p.H * 2;
-    for (int b0 = b_begin + 2 * warp; b0 < b_end; b0 += 2 * (kFp8Threads / 32)) {
-        const int b = b0 + half;
-        const bool valid = b < b_end;
-        uint4 v = make_uint4(0, 0, 0, 0);
-        if (valid) v = ld_stream_v4(xrow + static_cast<size_t>(b) * 256 + sub * 16);
-        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-        float f[8];
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            f[2 * q] = __uint_as_float(w[q] << 16);
-            f[2 * q + 1] = __uint_as_float(w[q] & 0xffff0000u);
+        if (warp == 0) {
+            int n = 0;
+            bool cap_bad = false;
+            const int n_dst = kExpanded ? p.K : p.R;
+            const int32_t* drow = kExpanded ? p.expanded_row + static_cast<int64_t>(t) * p.K
+                                            : p.dst_row + static_cast<int64_t>(t) * p.R;
+            for (int rb = 0; rb < n_dst; rb += 32) {
+                const int r = rb + lane;
+                const int d = r < n_dst ? drow[r] : -1;
+                const bool ok = d >= 0 && d < p.capacity;
+                if (d >= p.capacity) cap_bad = true;
+                const unsigned m = __ballot_sync(0xffffffffu, ok);
+                const int pos = n + __popc(m & ((1u << lane) - 1u));
+                // A layout from ep_get_layout has at most K <= 32 ranks per token;
+                // a foreign dst_row with more is cut off and flagged.
+                if (ok && pos < EP_MAX_TOPK) s_rows[pos] = d;
+                n += __popc(m);
+            }
+            if (n > EP_MAX_TOPK) {
+                if (lane == 0) atomicOr(p.status, EP_ERR_INVALID_INDEX);
+                n = EP_MAX_TOPK;
+            }
+            if (lane == 0) s_n_all[group] = n;
+            if (__any_sync(0xffffffffu, cap_bad) && lane == 0 && c == 0) atomicOr(p.status, EP_ERR_CAPACITY);
+        } else if (warp == 1 && c == 0) {
+            if (kExpanded) {
+                write_expanded_metadata(p, t, lane);
+            } else {
+                CtaWork all;
+                all.first = 0;
+                all.count = 0;
+                all.stride = 1;
+                all.lo = INT32_MIN;
+                all.hi = INT32_MAX;
+                all.balanced = 0;
+                write_metadata(p, t, lane, all);
+            }
         }
-        float amax = 0.0f;
+        if (kGroups > 1)
+            named_barrier(1 + group, kFp8Threads);
+        else
+            __syncthreads();
+
+        const int n = s_n_all[group];
+        const int nb = p.H / 128;
+        const int b_begin = c * p.chunk_blocks;
+        const int b_end = min(nb, b_begin + p.chunk_blocks);
+        const int half = lane >> 4;
+        const int sub = lane & 15;
+        const uint8_t* xrow = p.x + static_cast<int64_t>(t) * p.H * 2;
+        for (int b0 = b_begin + 2 * warp; b0 < b_end; b0 += 2 * (kFp8Threads / 32)) {
+            const int b = b0 + half;
+            const bool valid = b < b_end;
+            uint4 v = make_uint4(0, 0, 0, 0);
+            if (valid) v = ld_stream_v4(xrow + static_cast<size_t>(b) * 256 + sub * 16);
+            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+            float f[8];
 #pragma unroll
-        for (int q = 0; q < 8; ++q) amax = fmaxf(amax, fabsf(f[q]));
+            for (int q = 0; q < 4; ++q) {
+                f[2 * q] = __uint_as_float(w[q] << 16);
+                f[2 * q + 1] = __uint_as_float(w[q] & 0xffff0000u);
+            }
+            float amax = 0.0f;
 #pragma unroll
-        for (int o = 8; o >= 1; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-        float sf = 1.0f, mult = 0.0f;
-        if (amax > 0.0f) {
-            sf = __fdiv_rn(amax, 448.0f);
-            mult = __fdiv_rn(448.0f, amax);
-        }
-        float g[8];
+            for (int q = 0; q < 8; ++q) amax = fmaxf(amax, fabsf(f[q]));
 #pragma unroll
-        for (int q = 0; q < 8; ++q) g[q] = __fmul_rn(f[q], mult);
-        uint2 code;
-        code.x = pack_e4m3x4(g[0], g[1], g[2], g[3]);
-        code.y = pack_e4m3x4(g[4], g[5], g[6], g[7]);
-        if (valid) {
-            for (int m = 0; m < n; ++m) {
-                const int64_t d = s_rows[m];
-                *reinterpret_cast<uint2*>(p.recv_x + d * p.H + static_cast<int64_t>(b) * 128 + sub * 8) = code;
-                if (sub == 0 && p.recv_sf) {
-                    const int64_t si = p.sf_col_major ? static_cast<int64_t>(b) * p.sf_stride + d
-                                                      : d * nb + b;
-                    p.recv_sf[si] = sf;
+            for (int o = 8; o >= 1; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+            float sf = 1.0f, mult = 0.0f;
+            if (amax > 0.0f) {
+                sf = __fdiv_rn(amax, 448.0f);
+                mult = __fdiv_rn(448.0f, amax);
+            }
+            float g[8];
+#pragma unroll
+            for (int q = 0; q < 8; ++q) g[q] = __fmul_rn(f[q], mult);
+            uint2 code;
+            code.x = pack_e4m3x4(g[0], g[1], g[2], g[3]);
+            code.y = pack_e4m3x4(g[4], g[5], g[6], g[7]);
+            if (valid) {
+                for (int m = 0; m < n; ++m) {
+                    const int64_t d = s_rows[m];
+                    *reinterpret_cast<uint2*>(p.recv_x + d * p.H + static_cast<int64_t>(b) * 128 + sub * 8) = code;
+                    if (sub == 0 && p.recv_sf) {
+                        const int64_t si = p.sf_col_major ? static_cast<int64_t>(b) * p.sf_stride + d
+                                                          : d * nb + b;
+                        p.recv_sf[si] = sf;
+                    }
                 }
             }
         }
@@ -503,13 +537,19 @@ cudaError_t launch_dispatch_bf16(DispatchParams p, cudaStream_t stream) {
         cb = (cb + 15u) / 16u * 16u;
         p.chunks = static_cast<int>((row_bytes + cb - 1) / cb);
         p.chunk_bytes = cb;
-        const int64_t g = static_cast<int64_t>(p.T) * p.chunks;
-        if (g < 1) return cudaSuccess;
-        if (p.expanded_row)
-            return launch_pdl(dispatch_bf16_regs_kernel<true>, dim3(static_cast<unsigned>(g)), dim3(kRegThreads),
-                              0, stream, p);
-        return launch_pdl(dispatch_bf16_regs_kernel<false>, dim3(static_cast<unsigned>(g)), dim3(kRegThreads),
-                          0, stream, p);
+        const int64_t items = static_cast<int64_t>(p.T) * p.chunks;
+        if (items < 1) return cudaSuccess;
+        const int num_sms = p.num_sms > 0 ? (p.num_sms < di.num_sms ? p.num_sms : di.num_sms) : 0;
+        if (num_sms > 0) {
+            int64_t g = (items + kSmGroups - 1) / kSmGroups;
+            if (g > num_sms) g = num_sms;
+            const dim3 grid(static_cast<unsigned>(g)), block(kRegThreads * kSmGroups);
+            if (p.expanded_row) return launch_pdl(dispatch_bf16_regs_kernel<true, kSmGroups>, grid, block, 0, stream, p);
+            return launch_pdl(dispatch_bf16_regs_kernel<false, kSmGroups>, grid, block, 0, stream, p);
+        }
+        const dim3 grid(static_cast<unsigned>(items)), block(kRegThreads);
+        if (p.expanded_row) return launch_pdl(dispatch_bf16_regs_kernel<true, 1>, grid, block, 0, stream, p);
+        return launch_pdl(dispatch_bf16_regs_kernel<false, 1>, grid, block, 0, stream, p);
     }
     int chunks = static_cast<int>((row_bytes + EP_DISPATCH_PIECE_MAX - 1) / EP_DISPATCH_PIECE_MAX);
     const int want_items = 2 * di.num_sms;
@@ -566,13 +606,19 @@ cudaError_t launch_dispatch_fp8(DispatchParams p, cudaStream_t stream) {
     chunks = (nb + chunk_blocks - 1) / chunk_blocks;
     p.chunks = chunks;
     p.chunk_blocks = chunk_blocks;
-    const int64_t grid = static_cast<int64_t>(p.T) * chunks;
-    if (grid < 1) return cudaSuccess;
-    if (p.expanded_row)
-        return launch_pdl(dispatch_fp8_kernel<true>, dim3(static_cast<unsigned>(grid)), dim3(kFp8Threads), 0, stream,
-                          p);
-    return launch_pdl(dispatch_fp8_kernel<false>, dim3(static_cast<unsigned>(grid)), dim3(kFp8Threads), 0, stream,
-                      p);
+    const int64_t items = static_cast<int64_t>(p.T) * chunks;
+    if (items < 1) return cudaSuccess;
+    const int num_sms = p.num_sms > 0 ? (p.num_sms < di.num_sms ? p.num_sms : di.num_sms) : 0;
+    if (num_sms > 0) {
+        int64_t g = (items + kSmGroups - 1) / kSmGroups;
+        if (g > num_sms) g = num_sms;
+        const dim3 grid(static_cast<unsigned>(g)), block(kFp8Threads * kSmGroups);
+        if (p.expanded_row) return launch_pdl(dispatch_fp8_kernel<true, kSmGroups>, grid, block, 0, stream, p);
+        return launch_pdl(dispatch_fp8_kernel<false, kSmGroups>, grid, block, 0, stream, p);
+    }
+    const dim3 grid(static_cast<unsigned>(items)), block(kFp8Threads);
+    if (p.expanded_row) return launch_pdl(dispatch_fp8_kernel<true, 1>, grid, block, 0, stream, p);
+    return launch_pdl(dispatch_fp8_kernel<false, 1>, grid, block, 0, stream, p);
 }
 
 }  // namespace epg

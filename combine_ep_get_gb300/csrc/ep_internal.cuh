@@ -58,6 +58,7 @@ struct DispatchParams {
     float* recv_topk_weights;
     int32_t* recv_src_idx;
     int32_t* status;
+    int num_sms;            // > 0: SM-limited mode (persistent CTAs, one per SM)
     // work split: each token row is cut into `chunks` pieces
     int chunks;
     uint32_t chunk_bytes;   // bf16 path: bytes per piece (multiple of 16)
@@ -76,6 +77,7 @@ struct CombineParams {
     int32_t* status;
     int chunks;             // pieces per token row
     int chunk_vecs;         // 16-byte vectors per piece
+    int num_sms;            // > 0: SM-limited mode (persistent CTAs, one per SM)
 };
 
 struct CombineWeightsParams {
@@ -261,6 +263,12 @@ __device__ __forceinline__ void st_v4(void* p, uint4 v) {
     asm volatile("st.global.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z),
                  "r"(v.w)
                  : "memory");
+}
+
+// Barrier over `threads` threads of the CTA on hardware barrier `id` (1..15;
+// 0 is __syncthreads).
+__device__ __forceinline__ void named_barrier(int id, int threads) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }
 
 // 16-byte streaming store (evict-first at every cache level).

@@ -199,13 +199,20 @@ ep_status_t ep_get_layout_static_scratch(const int64_t* topk_idx, int num_tokens
  *                   (a column-major layout a following GEMM can load by TMA).
  * recv_topk_idx     int32 [capacity, K] or NULL; recv_topk_weights fp32
  *                   [capacity, K] or NULL; recv_src_idx int32 [capacity] or NULL.
+ * num_sms           0 = use the whole GPU; n > 0 = SM-limited mode: a
+ *                   persistent grid of min(n, SMs) CTAs, one per SM, so the
+ *                   copy can overlap compute kernels on the other SMs ("DeepEP V2
+ *                   ElasticBuffer architecture", get_theoretical_num_sms: the
+ *                   SM count is chosen to leave the rest to compute).  Results
+ *                   are identical in both modes.  The same argument exists on
+ *                   ep_combine, ep_dispatch_expanded and ep_combine_expanded.
  */
 ep_status_t ep_dispatch(const void* x, const int64_t* topk_idx, const float* topk_weights,
                         int num_tokens, int hidden, int num_topk, int num_experts, int num_ranks,
                         const ep_layout_t* layout, int out_dtype, int64_t recv_capacity,
                         void* recv_x, float* recv_sf, int sf_col_major,
                         int32_t* recv_topk_idx, float* recv_topk_weights, int32_t* recv_src_idx,
-                        int32_t* d_status, void* cuda_stream);
+                        int num_sms, int32_t* d_status, void* cuda_stream);
 
 /*
  * Combine ("DeepEP Symmetric Memory" section 9.2: combine(x, handle,
@@ -223,7 +230,7 @@ ep_status_t ep_dispatch(const void* x, const int64_t* topk_idx, const float* top
 ep_status_t ep_combine(const void* y, int64_t num_y_rows, const int64_t* topk_idx,
                        const float* topk_weights, int num_tokens, int hidden, int num_topk,
                        int num_experts, int num_ranks, const ep_layout_t* layout, void* out,
-                       int32_t* d_status, void* cuda_stream);
+                       int num_sms, int32_t* d_status, void* cuda_stream);
 
 /*
  * Expanded (per-expert) receive layout ("DeepEP V2 ElasticBuffer
@@ -255,8 +262,8 @@ ep_status_t ep_dispatch_expanded(const void* x, const int64_t* topk_idx, const f
                                  int num_tokens, int hidden, int num_topk, int num_experts,
                                  int num_ranks, const ep_layout_t* layout, int out_dtype,
                                  int64_t recv_capacity, void* recv_x, float* recv_sf, int sf_col_major,
-                                 int32_t* recv_src_idx, float* recv_weight, int32_t* d_status,
-                                 void* cuda_stream);
+                                 int32_t* recv_src_idx, float* recv_weight, int num_sms,
+                                 int32_t* d_status, void* cuda_stream);
 
 /*
  * Expanded combine: out[t] = bf16_rne( sum over k ascending with
@@ -267,8 +274,8 @@ ep_status_t ep_dispatch_expanded(const void* x, const int64_t* topk_idx, const f
  */
 ep_status_t ep_combine_expanded(const void* y, int64_t num_y_rows, const float* topk_weights,
                                 int num_tokens, int hidden, int num_topk, int num_experts,
-                                int num_ranks, const ep_layout_t* layout, void* out, int32_t* d_status,
-                                void* cuda_stream);
+                                int num_ranks, const ep_layout_t* layout, void* out, int num_sms,
+                                int32_t* d_status, void* cuda_stream);
 
 /*
  * Combined top-k weights ("DeepEP Symmetric Memory" section 9.2: combine

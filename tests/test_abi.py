@@ -52,7 +52,7 @@ def test_status_strings_and_sizes(lib):
     ws = lib.ep_layout_workspace_bytes(4096, 8, 256, 8, 0)
     tiles = 16
     assert ws >= 4 * tiles * (8 + 256 + 8 * 8)
-    assert lib.ep_abi_version() == 3
+    assert lib.ep_abi_version() == 4
 
 
 def test_host_checks_reject_before_any_launch(lib):
@@ -89,9 +89,9 @@ def test_host_checks_reject_before_any_launch(lib):
     d.restype = ctypes.c_int32
     d.argtypes = [vp, vp, vp, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                   ctypes.POINTER(B.ep_layout_t), ctypes.c_int, ctypes.c_int64, vp, vp, ctypes.c_int,
-                  vp, vp, vp, vp, vp]
+                  vp, vp, vp, ctypes.c_int, vp, vp]
     args = [vp(16), vp(32), vp(48), 10, 7168, 8, 256, 8, ctypes.byref(L2), B.EP_BF16, 100,
-            vp(64), None, 0, None, None, None, st, None]
+            vp(64), None, 0, None, None, None, 0, st, None]
     bad = list(args); bad[4] = 7164                      # H % 8
     assert d(*bad) == B.EP_ERR_INVALID_ARG
     bad = list(args); bad[9] = B.EP_FP8_E4M3; bad[4] = 7168 + 64   # H % 128 for FP8
@@ -108,14 +108,16 @@ def test_host_checks_reject_before_any_launch(lib):
     assert d(*bad) == B.EP_ERR_INVALID_ARG
     bad = list(args); bad[15] = vp(80); bad[2] = None    # weights out without weights in
     assert d(*bad) == B.EP_ERR_INVALID_ARG
-    bad = list(args); bad[17] = None                     # status missing
+    bad = list(args); bad[18] = None                     # status missing
+    assert d(*bad) == B.EP_ERR_INVALID_ARG
+    bad = list(args); bad[17] = -1                       # negative SM count
     assert d(*bad) == B.EP_ERR_INVALID_ARG
     # combine
     c = lib.ep_combine
     c.restype = ctypes.c_int32
     c.argtypes = [vp, ctypes.c_int64, vp, vp, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
-                  ctypes.c_int, ctypes.POINTER(B.ep_layout_t), vp, vp, vp]
-    cargs = [vp(16), 100, vp(32), None, 10, 7168, 8, 256, 8, ctypes.byref(L2), vp(64), st, None]
+                  ctypes.c_int, ctypes.POINTER(B.ep_layout_t), vp, ctypes.c_int, vp, vp]
+    cargs = [vp(16), 100, vp(32), None, 10, 7168, 8, 256, 8, ctypes.byref(L2), vp(64), 0, st, None]
     bad = list(cargs); bad[5] = 100                      # H % 8
     assert c(*bad) == B.EP_ERR_INVALID_ARG
     bad = list(cargs); bad[10] = None                    # out missing
