@@ -54,8 +54,12 @@ def parse_args(argv=None):
                     help="rank: one receive row per (token, rank); expanded: one per valid (token, k), "
                          "grouped by expert (weighted combine)")
     ap.add_argument("--no-graph", action="store_true", help="launch eagerly instead of CUDA graphs")
-    ap.add_argument("--num-sms", type=int, default=0,
-                    help="SM-limited dispatch and combine (persistent grid of this many CTAs); 0 = whole GPU")
+    ap.add_argument("--num-sms", default="0",
+                    help="SM-limited dispatch and combine (persistent grid of this many CTAs); 0 = whole "
+                         "GPU; 'rule' = each phase's count from ep_theoretical_num_sms with the measured "
+                         "HBM peak and the per-SM rates below")
+    ap.add_argument("--sm-read-gbs", type=float, default=200.0, help="per-SM read rate of the SM count rule")
+    ap.add_argument("--sm-write-gbs", type=float, default=50.0, help="per-SM write rate of the SM count rule")
     ap.add_argument("--e2e-steps", type=int, default=200)
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
                     help="CPU time budget of the oracle baseline (rank 0, N=1)")
@@ -292,22 +296,35 @@ def run_ours(args):
         weighted = True            # the expanded combine weights every (token, k) output
         recv_weight = torch.empty((N,), dtype=torch.float32, device=dev)
 
+    if args.num_sms == "rule":
+        hbm, _ = hbm_peak()
+        rule = dict(H=H, K=K, E=E, R=R, hbm_gbs=hbm, sm_read_gbs=args.sm_read_gbs,
+                    sm_write_gbs=args.sm_write_gbs)
+        sms_dispatch = B.ep_theoretical_num_sms(H, K, E, R, hbm, out_dtype=dtype_code, is_combine=False,
+                                                sm_read_gbs=args.sm_read_gbs, sm_write_gbs=args.sm_write_gbs)
+        sms_combine = B.ep_theoretical_num_sms(H, K, E, R, hbm, is_combine=True, sm_read_gbs=args.sm_read_gbs,
+                                               sm_write_gbs=args.sm_write_gbs)
+        sms_config = {"dispatch": sms_dispatch, "combine": sms_combine, "rule": rule}
+    else:
+        sms_dispatch = sms_combine = int(args.num_sms)
+        sms_config = sms_dispatch or "all"
+
     def do_layout():
         B.ep_get_layout(idx, E, R, lay, ws, status, cfg.ranks_per_node)
 
     def do_dispatch():
         if expanded:
             B.ep_dispatch_expanded(x, idx, w, E, R, lay, recv_x, recv_src, recv_weight, status,
-                                   recv_sf=recv_sf, out_dtype=dtype_code, num_sms=args.num_sms)
+                                   recv_sf=recv_sf, out_dtype=dtype_code, num_sms=sms_dispatch)
         else:
             B.ep_dispatch(x, idx, w, E, R, lay, recv_x, recv_idx, recv_w, recv_src, status,
-                          recv_sf=recv_sf, out_dtype=dtype_code, num_sms=args.num_sms)
+                          recv_sf=recv_sf, out_dtype=dtype_code, num_sms=sms_dispatch)
 
     def do_combine():
         if expanded:
-            B.ep_combine_expanded(y, w, K, E, R, lay, out, status, num_sms=args.num_sms)
+            B.ep_combine_expanded(y, w, K, E, R, lay, out, status, num_sms=sms_combine)
         else:
-            B.ep_combine(y, idx, w_comb, E, R, lay, out, status, num_sms=args.num_sms)
+            B.ep_combine(y, idx, w_comb, E, R, lay, out, status, num_sms=sms_combine)
 
     # eager warm-up (sets kernel attributes outside any capture)
     for _ in range(2):
@@ -462,7 +479,7 @@ def run_ours(args):
         "config": {
             "workload": cfg.description,
             "T": T, "H": H, "E": E, "K": K, "R": R, "N": N, "path": args.path,
-            "num_sms": args.num_sms or "all",
+            "num_sms": sms_config,
             "bytes_per_step": nbytes,
             "parallelism": "replicas" if world > 1 else "single",
             "l2": "flushed (256 MiB write) before layout and before combine, outside the timed events",

@@ -74,6 +74,9 @@ _lib.ep_status_string.restype = ctypes.c_char_p
 _lib.ep_status_string.argtypes = [ctypes.c_int32]
 _lib.ep_abi_version.restype = _i
 _lib.ep_abi_version.argtypes = []
+_lib.ep_theoretical_num_sms.restype = _i
+_lib.ep_theoretical_num_sms.argtypes = [_i, _i, _i, _i, _i, _i, ctypes.c_double, ctypes.c_double,
+                                        ctypes.c_double, _i, _i]
 
 
 def library():
@@ -110,6 +113,21 @@ def ep_layout_workspace_bytes(num_tokens, num_topk, num_experts, num_ranks, rank
 
 def ep_recv_capacity_bound(num_tokens, num_topk, num_ranks) -> int:
     return int(_lib.ep_recv_capacity_bound(num_tokens, num_topk, num_ranks))
+
+
+def ep_theoretical_num_sms(hidden, num_topk, num_experts, num_ranks, hbm_gbs, out_dtype=EP_BF16,
+                           is_combine=False, sm_read_gbs=200.0, sm_write_gbs=50.0,
+                           prefer_overlap_with_compute=True, device_sms=None) -> int:
+    """SM count for the SM-limited mode; device_sms defaults to the current
+    device's SM count.  Raises ValueError for arguments the library rejects."""
+    if device_sms is None:
+        device_sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+    n = int(_lib.ep_theoretical_num_sms(hidden, num_topk, num_experts, num_ranks, out_dtype, int(is_combine),
+                                        float(hbm_gbs), float(sm_read_gbs), float(sm_write_gbs),
+                                        int(prefer_overlap_with_compute), int(device_sms)))
+    if n == 0:
+        raise ValueError("ep_theoretical_num_sms: invalid arguments")
+    return n
 
 
 class Layout:

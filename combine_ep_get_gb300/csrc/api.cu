@@ -1,5 +1,7 @@
 // C ABI of libep_get.so: host-side argument checks, parameter blocks and
 // launches.  Declarations and the full contract are in include/ep_get.h.
+#include <algorithm>
+#include <cmath>
 #include <mutex>
 #include <string>
 
@@ -48,7 +50,7 @@ ep_status_t check_shape(int T, int K, int E, int R) {
 
 extern "C" {
 
-int ep_abi_version(void) { return 4; }
+int ep_abi_version(void) { return 5; }
 
 size_t ep_layout_workspace_bytes(int num_tokens, int num_topk, int num_experts, int num_ranks,
                                  int ranks_per_node) {
@@ -56,6 +58,34 @@ size_t ep_layout_workspace_bytes(int num_tokens, int num_topk, int num_experts, 
     if (num_tokens < 0 || num_experts < 1 || num_ranks < 1) return 16;
     const int nodes = ranks_per_node > 0 ? num_ranks / ranks_per_node : 0;
     return epg::layout_workspace(num_tokens, num_experts, num_ranks, nodes).total;
+}
+
+int ep_theoretical_num_sms(int hidden, int num_topk, int num_experts, int num_ranks, int out_dtype,
+                           int is_combine, double hbm_gbs, double sm_read_gbs, double sm_write_gbs,
+                           int prefer_overlap_with_compute, int device_sms) {
+    const bool fp8 = out_dtype == EP_FP8_E4M3;
+    if (out_dtype != EP_BF16 && !fp8) return 0;
+    if (hidden <= 0 || hidden % (fp8 ? 128 : 8) != 0) return 0;
+    if (num_ranks < 1 || num_experts < num_ranks || num_experts % num_ranks != 0) return 0;
+    if (num_topk < 1 || num_topk > EP_MAX_TOPK || num_topk > num_experts) return 0;
+    if (!(hbm_gbs > 0.0) || !(sm_read_gbs > 0.0) || !(sm_write_gbs > 0.0) || device_sms < 1) return 0;
+    // C(E - E/R, K) / C(E, K) = prod_{i<K} (E - E/R - i) / (E - i): the chance
+    // that none of K distinct uniform experts lives on a given rank.
+    const int others = num_experts - num_experts / num_ranks;
+    double miss = 1.0;
+    for (int i = 0; i < num_topk; ++i)
+        miss *= others - i > 0 ? static_cast<double>(others - i) / (num_experts - i) : 0.0;
+    const double g = num_ranks * (1.0 - miss);
+    const double h = static_cast<double>(hidden);
+    const double row = fp8 ? h + 4.0 * (h / 128.0) : 2.0 * h;
+    const double read = is_combine ? g * 2.0 * h : 2.0 * h;
+    const double write = is_combine ? 2.0 * h : g * row;
+    const double per_byte = hbm_gbs / (read + write);
+    const double n = std::max(per_byte * read / sm_read_gbs, per_byte * write / sm_write_gbs);
+    int sms = std::max(4, static_cast<int>(std::ceil(n * 1.25)));
+    sms += sms & 1;
+    if (!prefer_overlap_with_compute) sms = std::max(sms, 64);
+    return std::min(sms, device_sms);
 }
 
 int64_t ep_recv_capacity_bound(int num_tokens, int num_topk, int num_ranks) {

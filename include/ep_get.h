@@ -301,6 +301,33 @@ ep_status_t ep_combine_topk_weights(const float* recv_topk_weights, int64_t num_
 ep_status_t ep_accumulate_expert_stats(const ep_layout_t* layout, int num_experts, int64_t* stats,
                                        void* cuda_stream);
 
+/*
+ * SM count rule for the SM-limited mode ("DeepEP V2 ElasticBuffer
+ * architecture", get_theoretical_num_sms and its get_expected_topk helper),
+ * restated for ranks that share one HBM.  Host-only arithmetic, no GPU call.
+ *
+ *   g     = R * (1 - C(E - E/R, K) / C(E, K))   expected ranks per token when
+ *           each token picks K distinct experts uniformly at random
+ *   bytes the SMs move per token (payload only):
+ *           dispatch: read 2H, write g * row, row = 2H (bf16) or
+ *                     H + 4*H/128 (FP8 codes + fp32 scales)
+ *           combine:  read g * 2H, write 2H
+ *   the bounding link is the HBM itself (hbm_gbs), carrying read + write, so
+ *   n     = max(hbm_gbs / (read + write) * read  / sm_read_gbs,
+ *               hbm_gbs / (read + write) * write / sm_write_gbs)
+ *   n     = max(4, ceil(1.25 * n)) rounded up to even; at least 64 when
+ *           prefer_overlap_with_compute == 0; at most device_sms.
+ *
+ * The pages' per-SM rates are sm_read_gbs = 200 and sm_write_gbs = 50.
+ * is_combine: 0 = dispatch, 1 = combine (combine reads bf16 rows whatever
+ * out_dtype is).  Returns the SM count, or 0 for invalid arguments (hidden not
+ * a positive multiple of 128 for FP8 or of 8 otherwise, K outside 1..min(E, 32),
+ * R not dividing E, a rate or device_sms not positive).
+ */
+int ep_theoretical_num_sms(int hidden, int num_topk, int num_experts, int num_ranks, int out_dtype,
+                           int is_combine, double hbm_gbs, double sm_read_gbs, double sm_write_gbs,
+                           int prefer_overlap_with_compute, int device_sms);
+
 /* Text for a status word (bits joined by '|'); a static string. */
 const char* ep_status_string(int32_t status);
 

@@ -9,7 +9,8 @@ arithmetic.
 
 The arithmetic lives in ``ep_oracle.c`` (plain single-threaded C, one loop per
 step, each function citing the passage it follows).  This module only
-marshals numpy arrays.
+marshals numpy arrays, except for the SM count rule, a few lines of host
+arithmetic written here in Python with exact binomial coefficients.
 
 Pins (CPU tests): an independent numpy filter-and-sort formulation of the
 layout on small inputs; the count invariants of "DeepEP Symmetric Memory"
@@ -19,6 +20,8 @@ the exact dispatch -> identity -> combine closed form; the OCP E4M3 definition
 and torch's CPU float8 cast.
 """
 import ctypes
+import math
+
 import numpy as np
 
 from . import build as _build
@@ -311,3 +314,45 @@ def float_to_bf16(values):
 
 def bf16_to_float(bits):
     return (np.asarray(bits, dtype=np.uint16).astype(np.uint32) << 16).view(np.float32)
+
+
+def expected_ranks_per_token(E, K, R):
+    """Expected number of distinct ranks a token reaches when it picks K
+    distinct experts uniformly among E, E/R experts per rank: the
+    ``get_expected_topk(num_groups)`` helper of the ``get_theoretical_num_sms``
+    fragment of "DeepEP V2 ElasticBuffer architecture" with num_groups = R,
+    R * (1 - C(E - E/R, K) / C(E, K)) (exact binomials, one float division)."""
+    return R * (1 - math.comb(E - E // R, K) / math.comb(E, K))
+
+
+def theoretical_num_sms(H, K, E, R, hbm_gbs, fp8=False, combine=False, sm_read_gbs=200.0,
+                        sm_write_gbs=50.0, prefer_overlap=True, device_sms=152):
+    """The SM count rule of the ``get_theoretical_num_sms`` fragment ("DeepEP
+    V2 ElasticBuffer architecture"), read for ranks that share one HBM: the
+    bounding link is the HBM, whose traffic is everything the SMs read and
+    write.  Steps in the fragment's order:
+
+    1. bandwidth of the bounding link: hbm_gbs;
+    2. expected ranks per token g (``expected_ranks_per_token``);
+    3. traffic per token: dispatch reads the 2H-byte source row and writes g
+       rows (2H bytes bf16, H + 4H/128 FP8); combine reads g bf16 rows and
+       writes one;
+    4. the link is the bottleneck: time per token = (read + write) / hbm_gbs;
+    5. SMs to read / write at sm_read_gbs / sm_write_gbs per SM in that time,
+       the larger of the two, x 1.25, at least 4, rounded up to even, at least
+       64 unless overlapping with compute, at most device_sms.
+
+    Returns (count, n) with n the unrounded count of step 5."""
+    g = expected_ranks_per_token(E, K, R)
+    row = (H + 4 * (H // 128)) if fp8 and not combine else 2 * H
+    if combine:
+        read, write = g * 2 * H, 2 * H
+    else:
+        read, write = 2 * H, g * row
+    traffic = read + write
+    n = max(hbm_gbs / traffic * read / sm_read_gbs, hbm_gbs / traffic * write / sm_write_gbs)
+    count = max(4, math.ceil(n * 1.25))
+    count = (count + 1) // 2 * 2
+    if not prefer_overlap:
+        count = max(count, 64)
+    return min(count, device_sms), n

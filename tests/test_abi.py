@@ -31,7 +31,7 @@ def test_header_declares_the_entry_points():
     for n in ("ep_get_layout", "ep_dispatch", "ep_combine", "ep_layout_workspace_bytes",
               "ep_recv_capacity_bound", "ep_status_string", "ep_abi_version", "ep_dispatch_expanded",
               "ep_combine_expanded", "ep_expanded_capacity_bound", "ep_combine_topk_weights",
-              "ep_accumulate_expert_stats"):
+              "ep_accumulate_expert_stats", "ep_theoretical_num_sms"):
         assert n in names
 
 
@@ -52,7 +52,7 @@ def test_status_strings_and_sizes(lib):
     ws = lib.ep_layout_workspace_bytes(4096, 8, 256, 8, 0)
     tiles = 16
     assert ws >= 4 * tiles * (8 + 256 + 8 * 8)
-    assert lib.ep_abi_version() == 4
+    assert lib.ep_abi_version() == 5
 
 
 def test_host_checks_reject_before_any_launch(lib):
@@ -126,3 +126,52 @@ def test_host_checks_reject_before_any_launch(lib):
     assert c(*bad) == B.EP_ERR_INVALID_ARG
     bad = list(cargs); bad[0] = None                     # y missing with rows > 0
     assert c(*bad) == B.EP_ERR_INVALID_ARG
+
+
+def _sm_rule(lib):
+    f = lib.ep_theoretical_num_sms
+    f.restype = ctypes.c_int
+    f.argtypes = [ctypes.c_int] * 6 + [ctypes.c_double] * 3 + [ctypes.c_int] * 2
+    return f
+
+
+def test_sm_count_rule_matches_oracle(lib):
+    """The library's SM count rule against the oracle's over a grid; a case
+    whose unrounded 1.25 n sits within 1e-9 of an integer may round either
+    way (the two sides evaluate the binomial ratio in different orders)."""
+    import itertools
+    import math
+
+    import oracle
+    f = _sm_rule(lib)
+    checked = 0
+    for (H, K, E, R), fp8, comb, hbm, (rd, wr), ov, dev in itertools.product(
+            [(7168, 8, 256, 8), (7168, 8, 256, 64), (4096, 6, 64, 16), (128, 1, 16, 4), (2048, 32, 2048, 1024),
+             (256, 4, 8, 8), (1024, 8, 256, 1)],
+            [False, True], [False, True], [6677.2, 1000.0, 450.0], [(200.0, 50.0), (41.0, 50.0), (10.0, 10.0)],
+            [True, False], [152, 132, 16]):
+        want, n = oracle.theoretical_num_sms(H, K, E, R, hbm, fp8=fp8, combine=comb, sm_read_gbs=rd,
+                                             sm_write_gbs=wr, prefer_overlap=ov, device_sms=dev)
+        got = f(H, K, E, R, 1 if fp8 else 0, int(comb), hbm, rd, wr, int(ov), dev)
+        x = 1.25 * n
+        if abs(x - round(x)) < 1e-9 * max(1.0, x):
+            assert abs(got - want) <= 2
+            continue
+        assert got == want, (H, K, E, R, fp8, comb, hbm, rd, wr, ov, dev)
+        checked += 1
+    assert checked > 1000
+
+
+def test_sm_count_rule_rejects_bad_arguments(lib):
+    f = _sm_rule(lib)
+    ok = (7168, 8, 256, 8, 0, 0, 6677.0, 200.0, 50.0, 1, 152)
+    assert f(*ok) > 0
+    bad = [
+        (0,) + ok[1:], (100,) + ok[1:], (7176, 8, 256, 8, 1) + ok[5:],   # hidden: zero, not /8, FP8 not /128
+        ok[:1] + (0,) + ok[2:], ok[:1] + (33,) + ok[2:], (7168, 8, 4, 4) + ok[4:],    # K
+        ok[:3] + (7,) + ok[4:], ok[:4] + (2,) + ok[5:],                                # R does not divide E; dtype
+        ok[:6] + (0.0,) + ok[7:], ok[:7] + (-1.0,) + ok[8:], ok[:8] + (float("nan"),) + ok[9:],
+        ok[:10] + (0,),
+    ]
+    for a in bad:
+        assert f(*a) == 0, a
