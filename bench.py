@@ -218,9 +218,12 @@ def hbm_peak():
 
 
 def kernel_source_hash(kernel):
-    path = os.path.join(ROOT, "combine_ep_get_gb300", "csrc", "%s.cu" % kernel)
-    with open(path, "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()[:16]
+    """sha256[:16] of the kernel's source file followed by the shared device header."""
+    h = hashlib.sha256()
+    for name in ("%s.cu" % kernel, "ep_internal.cuh"):
+        with open(os.path.join(ROOT, "combine_ep_get_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
 
 
 def recorded_traffic(kernel, workload):
