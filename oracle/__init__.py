@@ -77,6 +77,17 @@ def _load():
                  "ep_oracle_float_to_bf16_array"):
         getattr(lib, name).restype = None
         getattr(lib, name).argtypes = [vp, ctypes.c_int64, vp]
+    lib.ep_oracle_double_to_bf16_array.restype = None
+    lib.ep_oracle_double_to_bf16_array.argtypes = [vp, ctypes.c_int64, vp]
+    lib.ep_oracle_node_rows.restype = ctypes.c_int
+    lib.ep_oracle_node_rows.argtypes = [vp] + [ctypes.c_int] * 5 + [vp, vp]
+    lib.ep_oracle_dispatch_hierarchical.restype = ctypes.c_int
+    lib.ep_oracle_dispatch_hierarchical.argtypes = (
+        [vp, vp, vp] + [ctypes.c_int] * 6 + [vp, vp, ctypes.c_int, ctypes.c_int64, vp, vp, vp, ctypes.c_int64,
+                                            ctypes.c_int, ctypes.c_int64, vp, vp, vp, vp, vp])
+    lib.ep_oracle_combine_hierarchical.restype = ctypes.c_int
+    lib.ep_oracle_combine_hierarchical.argtypes = (
+        [vp, ctypes.c_int64, vp, vp] + [ctypes.c_int] * 7 + [vp, vp, ctypes.c_int64, vp, vp, vp])
     _lib = lib
     return lib
 
@@ -310,6 +321,94 @@ def float_to_bf16(values):
     out = np.zeros(v.size, np.uint16)
     lib.ep_oracle_float_to_bf16_array(_p(v), v.size, _p(out))
     return out
+
+
+def double_to_bf16(values):
+    """float64 -> bf16 bit patterns in one rounding (RNE), elementwise, flattened."""
+    lib = _load()
+    v = np.ascontiguousarray(np.asarray(values, dtype=np.float64).ravel())
+    out = np.zeros(v.size, np.uint16)
+    lib.ep_oracle_double_to_bf16_array(_p(v), v.size, _p(out))
+    return out
+
+
+def node_rows(topk_idx, E, R, ranks_per_node):
+    """Rows of the per-node scale-out buffers (see ep_oracle_node_rows):
+    returns (node_offset int32 [nodes+1], node_row int32 [T, nodes], status)."""
+    lib = _load()
+    topk_idx = np.ascontiguousarray(topk_idx, dtype=np.int64)
+    T, K = topk_idx.shape
+    nodes = R // ranks_per_node
+    node_offset = np.zeros(nodes + 1, np.int32)
+    node_row = np.zeros((max(T, 1), nodes), np.int32)
+    status = lib.ep_oracle_node_rows(_p(topk_idx), T, K, E, R, ranks_per_node, _p(node_offset), _p(node_row))
+    return node_offset, node_row[:T], status
+
+
+def dispatch_hierarchical(x_bits, topk_idx, topk_weights, E, R, ranks_per_node, node_row, dst_row,
+                          node_capacity, recv_capacity, fp8=False, sf_col_major=False, sf_stride=None):
+    """Two-stage dispatch (see ep_oracle_dispatch_hierarchical).  Returns the
+    node buffers (node_x, node_sf, node_src_idx; unwritten node rows 0 / -1)
+    and the receive buffers (recv_*; unwritten rows 0), all sized by the
+    capacities."""
+    lib = _load()
+    x_bits = np.ascontiguousarray(x_bits, dtype=np.uint16)
+    topk_idx = np.ascontiguousarray(topk_idx, dtype=np.int64)
+    topk_weights = np.ascontiguousarray(topk_weights, dtype=np.float32)
+    node_row = np.ascontiguousarray(node_row, dtype=np.int32)
+    dst_row = np.ascontiguousarray(dst_row, dtype=np.int32)
+    T, H = x_bits.shape
+    K = topk_idx.shape[1]
+    row_bytes = H if fp8 else 2 * H
+    nb = H // 128
+    nc, rc = max(int(node_capacity), 1), max(int(recv_capacity), 1)
+    if sf_stride is None:
+        sf_stride = rc
+    node_x = np.zeros((nc, row_bytes), np.uint8)
+    node_sf = np.zeros((nc, max(nb, 1)), np.float32)
+    node_src_idx = np.full(nc, -1, np.int32)
+    recv_x = np.zeros((rc, row_bytes), np.uint8)
+    recv_sf = np.zeros(max(nb, 1) * sf_stride if sf_col_major else rc * max(nb, 1), np.float32)
+    recv_topk_idx = np.zeros((rc, K), np.int32)
+    recv_topk_weights = np.zeros((rc, K), np.float32)
+    recv_src_idx = np.zeros(rc, np.int32)
+    status = lib.ep_oracle_dispatch_hierarchical(
+        _p(x_bits), _p(topk_idx), _p(topk_weights), T, H, K, E, R, ranks_per_node, _p(node_row), _p(dst_row),
+        1 if fp8 else 0, int(node_capacity), _p(node_x), _p(node_sf), _p(node_src_idx), int(recv_capacity),
+        1 if sf_col_major else 0, sf_stride, _p(recv_x), _p(recv_sf), _p(recv_topk_idx),
+        _p(recv_topk_weights), _p(recv_src_idx))
+    n, r = int(node_capacity), int(recv_capacity)
+    res = dict(node_x=node_x[:n], node_src_idx=node_src_idx[:n], recv_x=recv_x[:r],
+               recv_topk_idx=recv_topk_idx[:r], recv_topk_weights=recv_topk_weights[:r],
+               recv_src_idx=recv_src_idx[:r], status=status)
+    if fp8:
+        res["node_sf"] = node_sf[:n]
+        res["recv_sf"] = recv_sf if sf_col_major else recv_sf.reshape(rc, nb)[:r]
+    return res
+
+
+def combine_hierarchical(y_bits, topk_idx, topk_weights, E, R, ranks_per_node, node_row, dst_row,
+                         node_capacity, weighted=False):
+    """Two-stage combine (see ep_oracle_combine_hierarchical): returns
+    (node_y uint16 bf16 bits [node_capacity, H], out float64 [T, H], status)."""
+    lib = _load()
+    y_bits = np.ascontiguousarray(y_bits, dtype=np.uint16)
+    topk_idx = np.ascontiguousarray(topk_idx, dtype=np.int64)
+    T, K = topk_idx.shape
+    H = y_bits.shape[1]
+    if topk_weights is None:
+        topk_weights = np.zeros((T, K), np.float32)
+    topk_weights = np.ascontiguousarray(topk_weights, dtype=np.float32)
+    node_row = np.ascontiguousarray(node_row, dtype=np.int32)
+    dst_row = np.ascontiguousarray(dst_row, dtype=np.int32)
+    nc = max(int(node_capacity), 1)
+    node_y = np.zeros((nc, H), np.uint16)
+    out = np.zeros((max(T, 1), H), np.float64)
+    scratch = np.zeros(max(H, 1), np.float64)
+    status = lib.ep_oracle_combine_hierarchical(
+        _p(y_bits), y_bits.shape[0], _p(topk_idx), _p(topk_weights), 1 if weighted else 0, T, H, K, E, R,
+        ranks_per_node, _p(node_row), _p(dst_row), int(node_capacity), _p(node_y), _p(out), _p(scratch))
+    return node_y[:int(node_capacity)], out[:T], status
 
 
 def bf16_to_float(bits):

@@ -515,3 +515,197 @@ void ep_oracle_accumulate_expert_stats(const int32_t* num_tokens_per_expert, int
 {
     for (int e = 0; e < E; ++e) stats[e] += num_tokens_per_expert[e];
 }
+
+/* ------------------------------------------------------------------------ */
+/* Hierarchical (two-stage) path: [P2] hybrid_dispatch / hybrid_combine,    */
+/* chosen when there is more than one scale-out domain, and the             */
+/* WorkspaceLayout fragment (scale-out rank counts kept beside the          */
+/* scale-up ones); [P3 section 3.2] node = rank / ranks_per_node.           */
+/* Readings: node n holds ranks [n*rpn, (n+1)*rpn); a token crosses the     */
+/* scale-out link once per node that holds any of its experts (node-level   */
+/* deduplication) and is then copied inside the node to each rank that      */
+/* needs it.  Node n's scale-out buffer holds its tokens in ascending t.    */
+/* Combine runs the other way: a scale-up reduce per (token, node) stored   */
+/* as bf16 (the data type on the link), then a scale-out reduce of the      */
+/* token's node partials.                                                   */
+/* ------------------------------------------------------------------------ */
+
+/* fp64 -> nearest bf16, ties to even, in one rounding (finite inputs inside */
+/* bf16's range).  |v| = m * 2^e with m in [0.5, 1): the bf16 quantum is    */
+/* 2^(e-8), and below the smallest normal (e < -125) the fixed subnormal    */
+/* quantum 2^-133.  nearbyint rounds ties to even in the default mode.      */
+uint16_t ep_oracle_double_to_bf16(double v)
+{
+    int neg = signbit(v) ? 1 : 0;
+    double a = fabs(v);
+    uint16_t b = 0;
+    if (a != 0.0) {
+        int e;
+        (void)frexp(a, &e);
+        if (e < -125) e = -125;
+        double q = nearbyint(ldexp(a, 8 - e));      /* integer, at most 2^8 */
+        float f = (float)ldexp(q, e - 8);           /* exact: <= 8 significant bits */
+        uint32_t u;
+        memcpy(&u, &f, sizeof u);
+        b = (uint16_t)(u >> 16);
+    }
+    return neg ? (uint16_t)(b | 0x8000u) : b;
+}
+
+void ep_oracle_double_to_bf16_array(const double* v, int64_t n, uint16_t* out)
+{
+    for (int64_t i = 0; i < n; ++i) out[i] = ep_oracle_double_to_bf16(v[i]);
+}
+
+/* Node rows: node_row[t, n] = row of token t in node n's scale-out buffer   */
+/* (node_offset[n] + number of earlier tokens reaching n) or -1;             */
+/* node_offset is the exclusive prefix of the per-node token counts.        */
+int ep_oracle_node_rows(const int64_t* topk_idx, int T, int K, int E, int R, int rpn,
+                        int32_t* node_offset, int32_t* node_row)
+{
+    int status = OR_OK;
+    int nodes = R / rpn;
+    int experts_per_rank = E / R;
+    node_offset[0] = 0;
+    for (int n = 0; n < nodes; ++n) {
+        int32_t count = 0;
+        for (int t = 0; t < T; ++t) {
+            int hit = 0;
+            for (int k = 0; k < K; ++k) {
+                int64_t e = topk_idx[(int64_t)t * K + k];
+                if (e < -1 || e >= E) { status |= OR_INVALID_INDEX; continue; }
+                if (e >= 0 && (int)(e / experts_per_rank) / rpn == n) hit = 1;
+            }
+            node_row[(int64_t)t * nodes + n] = hit ? node_offset[n] + count : -1;
+            count += hit;
+        }
+        node_offset[n + 1] = node_offset[n] + count;
+    }
+    return status;
+}
+
+/* Hierarchical dispatch.  Stage 1 (scale-out): node_x[node_row[t,n]] = x[t]  */
+/* (bf16 copy, or the FP8 cast with row-major node_sf), node_src_idx = t.   */
+/* Stage 2 (scale-up): every node row j of node n is forwarded to each rank */
+/* r of n with dst_row[t,r] >= 0 (t = node_src_idx[j]): recv_x / recv_sf   */
+/* copied from the node row, metadata as in ep_oracle_dispatch.             */
+int ep_oracle_dispatch_hierarchical(const uint16_t* x, const int64_t* topk_idx,
+                                    const float* topk_weights, int T, int H, int K, int E, int R,
+                                    int rpn, const int32_t* node_row, const int32_t* dst_row, int fp8,
+                                    int64_t node_capacity, uint8_t* node_x, float* node_sf,
+                                    int32_t* node_src_idx, int64_t recv_capacity, int sf_col_major,
+                                    int64_t sf_stride, uint8_t* recv_x, float* recv_sf,
+                                    int32_t* recv_topk_idx, float* recv_topk_weights,
+                                    int32_t* recv_src_idx)
+{
+    int status = OR_OK;
+    int nodes = R / rpn;
+    int experts_per_rank = E / R;
+    size_t row_bytes = fp8 ? (size_t)H : (size_t)H * 2;
+    int nb = H / 128;
+    uint8_t q_tmp[65536];
+    float sf_tmp[512];
+
+    /* stage 1: one copy of each token per node it reaches */
+    for (int t = 0; t < T; ++t)
+        for (int n = 0; n < nodes; ++n) {
+            int32_t j = node_row[(int64_t)t * nodes + n];
+            if (j < 0) continue;
+            if ((int64_t)j >= node_capacity) { status |= OR_CAPACITY; continue; }
+            const uint16_t* src = x + (int64_t)t * H;
+            if (fp8) {
+                ep_oracle_fp8_cast_row(src, H, q_tmp, sf_tmp);
+                memcpy(node_x + (int64_t)j * (int64_t)row_bytes, q_tmp, row_bytes);
+                for (int b = 0; b < nb; ++b) node_sf[(int64_t)j * nb + b] = sf_tmp[b];
+            } else {
+                memcpy(node_x + (int64_t)j * (int64_t)row_bytes, src, row_bytes);
+            }
+            node_src_idx[j] = t;
+        }
+
+    /* stage 2: each node row to the ranks of its node that need the token */
+    for (int n = 0; n < nodes; ++n)
+        for (int t0 = 0; t0 < T; ++t0) {
+            int32_t j = node_row[(int64_t)t0 * nodes + n];
+            if (j < 0 || (int64_t)j >= node_capacity) continue;
+            int t = node_src_idx[j];
+            for (int r = n * rpn; r < (n + 1) * rpn; ++r) {
+                int32_t d = dst_row[(int64_t)t * R + r];
+                if (d < 0) continue;
+                if ((int64_t)d >= recv_capacity) { status |= OR_CAPACITY; continue; }
+                memcpy(recv_x + (int64_t)d * (int64_t)row_bytes, node_x + (int64_t)j * (int64_t)row_bytes,
+                       row_bytes);
+                if (fp8 && recv_sf)
+                    for (int b = 0; b < nb; ++b) {
+                        float s = node_sf[(int64_t)j * nb + b];
+                        if (sf_col_major) recv_sf[(int64_t)b * sf_stride + d] = s;
+                        else recv_sf[(int64_t)d * nb + b] = s;
+                    }
+                for (int k = 0; k < K; ++k) {
+                    int64_t e = topk_idx[(int64_t)t * K + k];
+                    int on_r = (e >= 0 && e < E && (int)(e / experts_per_rank) == r);
+                    if (recv_topk_idx)
+                        recv_topk_idx[(int64_t)d * K + k] = on_r ? (int32_t)(e - (int64_t)r * experts_per_rank) : -1;
+                    if (recv_topk_weights)
+                        recv_topk_weights[(int64_t)d * K + k] = on_r ? topk_weights[(int64_t)t * K + k] : 0.0f;
+                }
+                if (recv_src_idx) recv_src_idx[d] = t;
+            }
+        }
+    return status;
+}
+
+/* Hierarchical combine.  Stage 1 (scale-up reduce): for every (t, n) with   */
+/* j = node_row[t,n] >= 0, node_y[j] = bf16( sum over ranks r of n,         */
+/* ascending, with dst_row[t,r] >= 0 of c(t,r) * y[dst_row[t,r]] ) (fp64    */
+/* sum, one rounding; c as in ep_oracle_combine).  Stage 2 (scale-out       */
+/* reduce): out[t] = sum over nodes n ascending with j >= 0 of node_y[j]    */
+/* (fp64, returned unrounded).                                               */
+int ep_oracle_combine_hierarchical(const uint16_t* y, int64_t num_y_rows, const int64_t* topk_idx,
+                                   const float* topk_weights, int weighted, int T, int H, int K, int E,
+                                   int R, int rpn, const int32_t* node_row, const int32_t* dst_row,
+                                   int64_t node_capacity, uint16_t* node_y, double* out,
+                                   double* scratch /* [H] */)
+{
+    int status = OR_OK;
+    int nodes = R / rpn;
+    int experts_per_rank = E / R;
+
+    /* stage 1 */
+    for (int t = 0; t < T; ++t)
+        for (int n = 0; n < nodes; ++n) {
+            int32_t j = node_row[(int64_t)t * nodes + n];
+            if (j < 0) continue;
+            if ((int64_t)j >= node_capacity) { status |= OR_CAPACITY; continue; }
+            for (int h = 0; h < H; ++h) scratch[h] = 0.0;
+            for (int r = n * rpn; r < (n + 1) * rpn; ++r) {
+                int32_t d = dst_row[(int64_t)t * R + r];
+                if (d < 0) continue;
+                if ((int64_t)d >= num_y_rows) { status |= OR_CAPACITY; continue; }
+                double c = 1.0;
+                if (weighted) {
+                    c = 0.0;
+                    for (int k = 0; k < K; ++k) {
+                        int64_t e = topk_idx[(int64_t)t * K + k];
+                        if (e >= 0 && e < E && (int)(e / experts_per_rank) == r)
+                            c += (double)topk_weights[(int64_t)t * K + k];
+                    }
+                }
+                const uint16_t* yr = y + (int64_t)d * H;
+                for (int h = 0; h < H; ++h) scratch[h] += c * (double)ep_oracle_bf16_to_float(yr[h]);
+            }
+            for (int h = 0; h < H; ++h) node_y[(int64_t)j * H + h] = ep_oracle_double_to_bf16(scratch[h]);
+        }
+
+    /* stage 2 */
+    for (int t = 0; t < T; ++t) {
+        double* o = out + (int64_t)t * H;
+        for (int h = 0; h < H; ++h) o[h] = 0.0;
+        for (int n = 0; n < nodes; ++n) {
+            int32_t j = node_row[(int64_t)t * nodes + n];
+            if (j < 0 || (int64_t)j >= node_capacity) continue;
+            for (int h = 0; h < H; ++h) o[h] += (double)ep_oracle_bf16_to_float(node_y[(int64_t)j * H + h]);
+        }
+    }
+    return status;
+}
