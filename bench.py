@@ -36,11 +36,12 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 L2_FLUSH_BYTES = 256 << 20
-def kernels_per_step(T, R, expanded=False):
+def kernels_per_step(T, R, expanded=False, hierarchical=False):
     """Launches of this library per step: the layout is one cluster kernel, or
-    three tiled kernels when T*R is large or expanded rows are wanted;
-    dispatch and combine one each."""
-    return (1 if T * R <= (1 << 19) and not expanded else 3) + 2
+    three tiled kernels when T*R is large or expanded or node rows are wanted;
+    dispatch and combine one each, two each on the hierarchical path."""
+    tiled = expanded or hierarchical or T * R > (1 << 19)
+    return (3 if tiled else 1) + (4 if hierarchical else 2)
 
 
 def parse_args(argv=None):
@@ -50,9 +51,12 @@ def parse_args(argv=None):
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="dsv3")
-    ap.add_argument("--path", choices=["rank", "expanded"], default="rank",
+    ap.add_argument("--path", choices=["rank", "expanded", "hierarchical"], default="rank",
                     help="rank: one receive row per (token, rank); expanded: one per valid (token, k), "
-                         "grouped by expert (weighted combine)")
+                         "grouped by expert (weighted combine); hierarchical: two-stage dispatch and "
+                         "combine through per-node buffers")
+    ap.add_argument("--ranks-per-node", type=int, default=0,
+                    help="hierarchical path: ranks per node (default: the workload's, else R/2)")
     ap.add_argument("--no-graph", action="store_true", help="launch eagerly instead of CUDA graphs")
     ap.add_argument("--num-sms", default="0",
                     help="SM-limited dispatch and combine (persistent grid of this many CTAs); 0 = whole "
@@ -85,6 +89,29 @@ def algorithmic_bytes_expanded(T, H, K, E, R, M, fp8=False):
     layout = T * K * 8 + T * R * 5 + T * K * 4 + 4 * (3 * E + 3 * R + 2)
     dispatch = T * H * 2 + T * K * 12 + T * K * 4 + M * (H * b_out + s + 8)
     combine = M * H * 2 + T * K * 8 + T * H * 2
+    return dict(layout=layout, dispatch=dispatch, combine=combine, total=layout + dispatch + combine)
+
+
+def algorithmic_bytes_hierarchical(T, H, K, E, R, nodes, N, M, weighted=False, fp8=False):
+    """Bytes per step of the two-stage path, M = node rows (token, node pairs).
+
+    layout:   as the rank path, plus node rows [T, nodes] written.
+    dispatch: stage 1 reads x, topk_idx and the node rows and writes M node
+              rows (+ FP8 scales) and their source index; stage 2 reads the
+              node rows and dst_row, topk_idx and topk_weights, and writes N
+              rows with their metadata.
+    combine:  stage 1 reads dst_row and N rows (+ topk for weighting) and
+              writes M node partials; stage 2 reads the node rows and the M
+              partials and writes T rows.
+    """
+    b_out = 1 if fp8 else 2
+    s = 4 * (H // 128) if fp8 else 0
+    layout = T * K * 8 + T * R * 5 + T * nodes * 4 + 4 * (3 * E + 3 * R + 2 * nodes + 3)
+    stage1 = T * H * 2 + T * K * 8 + T * nodes * 4 + M * (H * b_out + s + 4)
+    stage2 = T * nodes * 4 + T * R * 4 + T * K * 12 + M * (H * b_out + s) + N * (H * b_out + s + 8 * K + 4)
+    reduce1 = T * nodes * 4 + T * R * 4 + N * H * 2 + M * H * 2 + (T * K * 12 if weighted else 0)
+    reduce2 = T * nodes * 4 + M * H * 2 + T * H * 2
+    dispatch, combine = stage1 + stage2, reduce1 + reduce2
     return dict(layout=layout, dispatch=dispatch, combine=combine, total=layout + dispatch + combine)
 
 
@@ -269,11 +296,14 @@ def run_ours(args):
     w = w_host.to(dev)
 
     expanded = args.path == "expanded"
-    lay = B.alloc_layout(T, E, R, cfg.ranks_per_node, device=dev, K=K if expanded else None)
-    ws = torch.empty(B.ep_layout_workspace_bytes(T, K, E, R, cfg.ranks_per_node), dtype=torch.uint8,
-                     device=dev)
+    hierarchical = args.path == "hierarchical"
+    rpn = cfg.ranks_per_node
+    if hierarchical:
+        rpn = args.ranks_per_node or cfg.ranks_per_node or max(1, R // 2)
+    lay = B.alloc_layout(T, E, R, rpn, device=dev, K=K if expanded else None, node_rows=hierarchical)
+    ws = torch.empty(B.ep_layout_workspace_bytes(T, K, E, R, rpn), dtype=torch.uint8, device=dev)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
-    B.ep_get_layout(idx, E, R, lay, ws, status, cfg.ranks_per_node)
+    B.ep_get_layout(idx, E, R, lay, ws, status, rpn)
     # one host read of the row count (rank_offset[R], or expert_offset[E] for the
     # expanded rows), before any timing
     N = int(lay.expert_offset[-1].item()) if expanded else lay.num_recv
@@ -298,6 +328,13 @@ def run_ours(args):
     if expanded:
         weighted = True            # the expanded combine weights every (token, k) output
         recv_weight = torch.empty((N,), dtype=torch.float32, device=dev)
+    hier = None
+    if hierarchical:
+        M = int(lay.node_offset[-1].item())
+        hier = dict(rpn=rpn, M=M, node_src=torch.empty((M,), dtype=torch.int32, device=dev),
+                    node_y=torch.empty((M, H), dtype=torch.bfloat16, device=dev),
+                    node_x=torch.empty((M, H), dtype=torch.uint8 if fp8 else torch.bfloat16, device=dev),
+                    node_sf=torch.empty((M * (H // 128),), dtype=torch.float32, device=dev) if fp8 else None)
 
     if args.num_sms == "rule":
         hbm, _ = hbm_peak()
@@ -313,10 +350,15 @@ def run_ours(args):
         sms_config = sms_dispatch or "all"
 
     def do_layout():
-        B.ep_get_layout(idx, E, R, lay, ws, status, cfg.ranks_per_node)
+        B.ep_get_layout(idx, E, R, lay, ws, status, rpn)
 
     def do_dispatch():
-        if expanded:
+        if hierarchical:
+            B.ep_dispatch_hierarchical(x, idx, w, E, R, rpn, lay, hier["node_x"], recv_x, status,
+                                       node_sf=hier["node_sf"], node_src_idx=hier["node_src"], recv_sf=recv_sf,
+                                       recv_topk_idx=recv_idx, recv_topk_weights=recv_w, recv_src_idx=recv_src,
+                                       out_dtype=dtype_code)
+        elif expanded:
             B.ep_dispatch_expanded(x, idx, w, E, R, lay, recv_x, recv_src, recv_weight, status,
                                    recv_sf=recv_sf, out_dtype=dtype_code, num_sms=sms_dispatch)
         else:
@@ -324,7 +366,9 @@ def run_ours(args):
                           recv_sf=recv_sf, out_dtype=dtype_code, num_sms=sms_dispatch)
 
     def do_combine():
-        if expanded:
+        if hierarchical:
+            B.ep_combine_hierarchical(y, idx, w_comb, E, R, rpn, lay, hier["node_y"], out, status)
+        elif expanded:
             B.ep_combine_expanded(y, w, K, E, R, lay, out, status, num_sms=sms_combine)
         else:
             B.ep_combine(y, idx, w_comb, E, R, lay, out, status, num_sms=sms_combine)
@@ -440,6 +484,8 @@ def run_ours(args):
 
     if expanded:
         nbytes = algorithmic_bytes_expanded(T, H, K, E, R, int((idx >= 0).sum().item()), fp8=fp8)
+    elif hierarchical:
+        nbytes = algorithmic_bytes_hierarchical(T, H, K, E, R, R // rpn, N, hier["M"], weighted=weighted, fp8=fp8)
     else:
         nbytes = algorithmic_bytes(T, H, K, E, R, N, weighted=weighted, fp8=fp8)
     value_bps = replica_value(nbytes["total"], args.steps, max_total, world)
@@ -463,7 +509,7 @@ def run_ours(args):
 
     # end to end through the public API with host buffers
     e2e = run_e2e(args, B, torch, dev, x_host, idx_host, w_host, lay, ws, status, recv_x, recv_sf, y,
-                  recv_idx, recv_w, recv_src, out, cfg, nbytes, world)
+                  recv_idx, recv_w, recv_src, out, cfg, nbytes, world, rpn, hier)
 
     result = {
         "metric": "dispatch+combine GB/s and tokens/s on 1 GB300; % of HBM roofline",
@@ -482,6 +528,7 @@ def run_ours(args):
         "config": {
             "workload": cfg.description,
             "T": T, "H": H, "E": E, "K": K, "R": R, "N": N, "path": args.path,
+            **({"ranks_per_node": rpn, "node_rows": hier["M"]} if hierarchical else {}),
             "num_sms": sms_config,
             "bytes_per_step": nbytes,
             "parallelism": "replicas" if world > 1 else "single",
@@ -492,15 +539,19 @@ def run_ours(args):
                            "stand-in expert rows, weighted, fp32 accumulate, bf16 out" if fp8 else
                            "bf16 row copies; combine of the dispatched rows (identity expert), "
                            "%s, fp32 accumulate, bf16 out" % ("weighted" if weighted else "unweighted")) +
-                          ("; expanded rows: one per valid (token, k), grouped by expert" if expanded else ""),
+                          ("; expanded rows: one per valid (token, k), grouped by expert" if expanded else "") +
+                          ("; two stages: each token once per node into per-node buffers, then fanned out to "
+                           "the node's ranks; combine partials per (token, node) stored as bf16"
+                           if hierarchical else ""),
         },
         "per_kernel": per_kernel,
         "roofline": {"bound": "hbm", "kernel": dominant, "achieved": achieved, "peak": peak,
                      "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / peak,
-                     "traffic": recorded_traffic(dominant, args.workload),
+                     # recorded DRAM traffic is of the rank path's kernels only
+                     "traffic": recorded_traffic(dominant, args.workload) if args.path == "rank" else None,
                      "algorithmic_bytes_per_launch": nbytes[dominant], "timed_in": source[dominant]},
         "e2e": e2e,
-        "gpu_launches": kernels_per_step(T, R, expanded) * args.steps,
+        "gpu_launches": kernels_per_step(T, R, expanded, hierarchical) * args.steps,
         "clocks": clocks,
     }
     if world == 1 and rank == 0 and not args.no_cpu_baseline:
@@ -513,7 +564,7 @@ def run_ours(args):
 
 
 def run_e2e(args, B, torch, dev, x_host, idx_host, w_host, lay, ws, status, recv_x, recv_sf, y, recv_idx,
-            recv_w, recv_src, out, cfg, nbytes, world):
+            recv_w, recv_src, out, cfg, nbytes, world, rpn, hier):
     """End to end through the public calls with host buffers.
 
     Every step copies its inputs (x, topk_idx, topk_weights) from pinned host
@@ -547,9 +598,16 @@ def run_e2e(args, B, torch, dev, x_host, idx_host, w_host, lay, ws, status, recv
             ev_in[b].record(s_in)
         s_comp.wait_event(ev_in[b])
         s_comp.wait_event(ev_out[b])             # step i-2's output has been copied out
-        B.ep_get_layout(idd[b], E, R, lay, ws, status, cfg.ranks_per_node, stream=s_comp)
+        B.ep_get_layout(idd[b], E, R, lay, ws, status, rpn, stream=s_comp)
         dtype_code = B.EP_FP8_E4M3 if cfg.fp8 else B.EP_BF16
-        if args.path == "expanded":
+        if args.path == "hierarchical":
+            B.ep_dispatch_hierarchical(xd[b], idd[b], wd[b], E, R, rpn, lay, hier["node_x"], recv_x, status,
+                                       node_sf=hier["node_sf"], node_src_idx=hier["node_src"], recv_sf=recv_sf,
+                                       recv_topk_idx=recv_idx, recv_topk_weights=recv_w, recv_src_idx=recv_src,
+                                       out_dtype=dtype_code, stream=s_comp)
+            B.ep_combine_hierarchical(y, idd[b], wd[b] if cfg.weighted else None, E, R, rpn, lay, hier["node_y"],
+                                      outd[b], status, stream=s_comp)
+        elif args.path == "expanded":
             B.ep_dispatch_expanded(xd[b], idd[b], wd[b], E, R, lay, recv_x, recv_src, None, status,
                                    recv_sf=recv_sf, out_dtype=dtype_code, stream=s_comp)
             B.ep_combine_expanded(y, wd[b], idd[b].shape[1], E, R, lay, outd[b], status, stream=s_comp)

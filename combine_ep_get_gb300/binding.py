@@ -38,7 +38,7 @@ class ep_layout_t(ctypes.Structure):
     _fields_ = [("num_tokens_per_rank", _vp), ("num_tokens_per_node", _vp),
                 ("num_tokens_per_expert", _vp), ("is_token_in_rank", _vp), ("rank_offset", _vp),
                 ("expert_offset", _vp), ("dst_row", _vp), ("src_dst_count", _vp),
-                ("token_offset", _vp), ("expanded_row", _vp)]
+                ("token_offset", _vp), ("expanded_row", _vp), ("node_offset", _vp), ("node_row", _vp)]
 
 
 _lib.ep_layout_workspace_bytes.restype = ctypes.c_size_t
@@ -74,6 +74,12 @@ _lib.ep_status_string.restype = ctypes.c_char_p
 _lib.ep_status_string.argtypes = [ctypes.c_int32]
 _lib.ep_abi_version.restype = _i
 _lib.ep_abi_version.argtypes = []
+_lib.ep_dispatch_hierarchical.restype = ctypes.c_int32
+_lib.ep_dispatch_hierarchical.argtypes = [_vp, _vp, _vp, _i, _i, _i, _i, _i, _i, ctypes.POINTER(ep_layout_t), _i,
+                                          _i64, _vp, _vp, _vp, _i64, _vp, _vp, _i, _vp, _vp, _vp, _vp, _vp]
+_lib.ep_combine_hierarchical.restype = ctypes.c_int32
+_lib.ep_combine_hierarchical.argtypes = [_vp, _i64, _vp, _vp, _i, _i, _i, _i, _i, _i, ctypes.POINTER(ep_layout_t),
+                                         _i64, _vp, _vp, _vp, _vp]
 _lib.ep_theoretical_num_sms.restype = _i
 _lib.ep_theoretical_num_sms.argtypes = [_i, _i, _i, _i, _i, _i, ctypes.c_double, ctypes.c_double,
                                         ctypes.c_double, _i, _i]
@@ -133,7 +139,7 @@ def ep_theoretical_num_sms(hidden, num_topk, num_experts, num_ranks, hbm_gbs, ou
 class Layout:
     """Device tensors of one routing layout plus their ep_layout_t view."""
 
-    def __init__(self, T, E, R, ranks_per_node=0, with_src_dst=True, device="cuda", K=None):
+    def __init__(self, T, E, R, ranks_per_node=0, with_src_dst=True, device="cuda", K=None, node_rows=False):
         i32 = dict(dtype=torch.int32, device=device)
         nodes = R // ranks_per_node if ranks_per_node > 0 else 0
         self.T, self.E, self.R, self.ranks_per_node = T, E, R, ranks_per_node
@@ -148,6 +154,9 @@ class Layout:
         self.token_offset = torch.empty(T + 1, **i32)
         # expanded (per-expert) rows are produced when K is given
         self.expanded_row = torch.empty((T, K), **i32) if K is not None else None
+        # per-node scale-out rows (hierarchical path) when node_rows is set
+        self.node_offset = torch.empty(nodes + 1, **i32) if (node_rows and nodes) else None
+        self.node_row = torch.empty((T, nodes), **i32) if (node_rows and nodes) else None
         self.c = ep_layout_t(*[_ptr(getattr(self, f)) for f, _ in ep_layout_t._fields_])
 
     @property
@@ -156,9 +165,10 @@ class Layout:
         return int(self.rank_offset[-1].item())
 
 
-def alloc_layout(T, E, R, ranks_per_node=0, with_src_dst=True, device="cuda", K=None) -> Layout:
-    """Device arrays of a layout; pass K to also get the expanded rows."""
-    return Layout(T, E, R, ranks_per_node, with_src_dst, device, K)
+def alloc_layout(T, E, R, ranks_per_node=0, with_src_dst=True, device="cuda", K=None, node_rows=False) -> Layout:
+    """Device arrays of a layout; pass K to also get the expanded rows, and
+    node_rows=True (with ranks_per_node > 0) for the hierarchical path's node rows."""
+    return Layout(T, E, R, ranks_per_node, with_src_dst, device, K, node_rows)
 
 
 def ep_expanded_capacity_bound(num_tokens, num_topk, num_experts, expert_alignment=1) -> int:
@@ -253,3 +263,34 @@ def ep_combine(y, topk_idx, topk_weights, num_experts, num_ranks, layout, out, d
                            num_experts, num_ranks, ctypes.byref(layout.c), _ptr(out), num_sms,
                            _ptr(d_status), _stream(stream))
     return _check(code, "ep_combine")
+
+
+def ep_dispatch_hierarchical(x, topk_idx, topk_weights, num_experts, num_ranks, ranks_per_node, layout, node_x,
+                             recv_x, d_status, node_sf=None, node_src_idx=None, recv_sf=None, recv_topk_idx=None,
+                             recv_topk_weights=None, recv_src_idx=None, out_dtype=EP_BF16, sf_col_major=False,
+                             stream=None):
+    """Two-stage dispatch: node_x / node_sf / node_src_idx are the per-node
+    scale-out buffers (node_capacity = node_x.shape[0]); recv_* as ep_dispatch."""
+    T, H = x.shape
+    K = topk_idx.shape[1]
+    assert x.element_size() == 2 and x.is_contiguous() and recv_x.is_contiguous() and node_x.is_contiguous()
+    code = _lib.ep_dispatch_hierarchical(_ptr(x), _ptr(topk_idx), _ptr(topk_weights), T, H, K, num_experts,
+                                         num_ranks, ranks_per_node, ctypes.byref(layout.c), out_dtype,
+                                         node_x.shape[0], _ptr(node_x), _ptr(node_sf), _ptr(node_src_idx),
+                                         recv_x.shape[0], _ptr(recv_x), _ptr(recv_sf), int(sf_col_major),
+                                         _ptr(recv_topk_idx), _ptr(recv_topk_weights), _ptr(recv_src_idx),
+                                         _ptr(d_status), _stream(stream))
+    return _check(code, "ep_dispatch_hierarchical")
+
+
+def ep_combine_hierarchical(y, topk_idx, topk_weights, num_experts, num_ranks, ranks_per_node, layout, node_y,
+                            out, d_status, stream=None):
+    """Two-stage combine: node_y (bf16 [node_capacity, H]) receives the
+    per-(token, node) partials; out the combined rows."""
+    T, K = topk_idx.shape
+    H = out.shape[1]
+    assert y.element_size() == 2 and out.element_size() == 2 and node_y.element_size() == 2
+    code = _lib.ep_combine_hierarchical(_ptr(y), y.shape[0], _ptr(topk_idx), _ptr(topk_weights), T, H, K,
+                                        num_experts, num_ranks, ranks_per_node, ctypes.byref(layout.c),
+                                        node_y.shape[0], _ptr(node_y), _ptr(out), _ptr(d_status), _stream(stream))
+    return _check(code, "ep_combine_hierarchical")

@@ -50,7 +50,7 @@ ep_status_t check_shape(int T, int K, int E, int R) {
 
 extern "C" {
 
-int ep_abi_version(void) { return 5; }
+int ep_abi_version(void) { return 6; }
 
 size_t ep_layout_workspace_bytes(int num_tokens, int num_topk, int num_experts, int num_ranks,
                                  int ranks_per_node) {
@@ -111,6 +111,10 @@ ep_status_t ep_get_layout(const int64_t* topk_idx, int T, int K, int E, int R, i
     if (out->src_dst_count && (!aligned16(out->src_dst_count) || T % R != 0)) return EP_ERR_INVALID_ARG;
     if (out->token_offset && !aligned16(out->token_offset)) return EP_ERR_INVALID_ARG;
     if (out->expanded_row && !aligned16(out->expanded_row)) return EP_ERR_INVALID_ARG;
+    if ((out->node_row != nullptr) != (out->node_offset != nullptr)) return EP_ERR_INVALID_ARG;
+    if (out->node_row && (ranks_per_node <= 0 || !ok_ptr(out->num_tokens_per_node) ||
+                          !aligned16(out->node_row) || !aligned16(out->node_offset)))
+        return EP_ERR_INVALID_ARG;
     const int nodes_ws = ranks_per_node > 0 ? R / ranks_per_node : 0;
     const epg::LayoutWorkspace w = epg::layout_workspace(T, E, R, nodes_ws);
     if (!ok_ptr(workspace) || ws_bytes < w.total) return EP_ERR_INVALID_ARG;
@@ -136,6 +140,8 @@ ep_status_t ep_get_layout(const int64_t* topk_idx, int T, int K, int E, int R, i
     p.src_dst_count = out->src_dst_count;
     p.token_offset = out->token_offset;
     p.expanded_row = T > 0 ? out->expanded_row : nullptr;
+    p.node_offset = out->node_offset;
+    p.node_row = out->node_row;
     char* ws = static_cast<char*>(workspace);
     p.ws_rank = reinterpret_cast<int32_t*>(ws + w.off_rank);
     p.ws_expert = reinterpret_cast<int32_t*>(ws + w.off_expert);
@@ -202,6 +208,151 @@ ep_status_t ep_dispatch(const void* x, const int64_t* topk_idx, const float* top
     const cudaError_t e = out_dtype == EP_BF16 ? epg::launch_dispatch_bf16(p, st)
                                                : epg::launch_dispatch_fp8(p, st);
     return e == cudaSuccess ? EP_OK : EP_ERR_CUDA;
+}
+
+ep_status_t ep_dispatch_hierarchical(const void* x, const int64_t* topk_idx, const float* topk_weights, int T,
+                                     int H, int K, int E, int R, int rpn, const ep_layout_t* layout,
+                                     int out_dtype, int64_t node_capacity, void* node_x, float* node_sf,
+                                     int32_t* node_src_idx, int64_t recv_capacity, void* recv_x, float* recv_sf,
+                                     int sf_col_major, int32_t* recv_topk_idx, float* recv_topk_weights,
+                                     int32_t* recv_src_idx, int32_t* d_status, void* cuda_stream) {
+    if (!layout || !d_status) return EP_ERR_INVALID_ARG;
+    ep_status_t s = check_shape(T, K, E, R);
+    if (s != EP_OK) return s;
+    if (rpn < 1 || R % rpn != 0) return EP_ERR_INVALID_ARG;
+    const bool fp8 = out_dtype == EP_FP8_E4M3;
+    if (H < 1) return EP_ERR_INVALID_ARG;
+    if (out_dtype == EP_BF16) {
+        if (H % 8 != 0) return EP_ERR_INVALID_ARG;
+    } else if (fp8) {
+        if (H % 128 != 0) return EP_ERR_INVALID_ARG;
+        if (H > 65536) return EP_ERR_UNSUPPORTED;
+    } else {
+        return EP_ERR_INVALID_ARG;
+    }
+    if (recv_capacity < 0 || recv_capacity > INT32_MAX) return EP_ERR_INVALID_ARG;
+    if (node_capacity < 0 || node_capacity > INT32_MAX) return EP_ERR_INVALID_ARG;
+    if (static_cast<int64_t>(H) * 2 > UINT32_MAX / 2) return EP_ERR_UNSUPPORTED;
+    if (T > 0 && (!ok_ptr(x) || !ok_ptr(topk_idx) || !ok_ptr(layout->dst_row) || !ok_ptr(layout->node_row)))
+        return EP_ERR_INVALID_ARG;
+    if (node_capacity > 0 && (!ok_ptr(node_x) || (fp8 && !ok_ptr(node_sf)))) return EP_ERR_INVALID_ARG;
+    if (node_src_idx && !aligned16(node_src_idx)) return EP_ERR_INVALID_ARG;
+    if (recv_capacity > 0 && !ok_ptr(recv_x)) return EP_ERR_INVALID_ARG;
+    if (fp8 && recv_capacity > 0 && !ok_ptr(recv_sf)) return EP_ERR_INVALID_ARG;
+    if (recv_topk_weights && T > 0 && !ok_ptr(topk_weights)) return EP_ERR_INVALID_ARG;
+    if ((recv_topk_idx && !aligned16(recv_topk_idx)) || (recv_topk_weights && !aligned16(recv_topk_weights)) ||
+        (recv_src_idx && !aligned16(recv_src_idx)))
+        return EP_ERR_INVALID_ARG;
+    if (T == 0) return EP_OK;
+    const int nodes = R / rpn;
+    cudaStream_t st = static_cast<cudaStream_t>(cuda_stream);
+
+    // stage 1: the ordinary dispatch with the node table as destinations
+    epg::DispatchParams p{};
+    p.x = static_cast<const uint8_t*>(x);
+    p.topk_idx = topk_idx;
+    p.topk_weights = topk_weights;
+    p.dst_row = layout->node_row;
+    p.T = T;
+    p.H = H;
+    p.K = K;
+    p.E = E;
+    p.R = nodes;
+    p.experts_per_rank = E / R;
+    p.capacity = node_capacity;
+    p.recv_x = static_cast<uint8_t*>(node_x);
+    p.recv_sf = node_sf;
+    p.sf_col_major = 0;
+    p.sf_stride = node_capacity;
+    p.recv_src_idx = node_src_idx;
+    p.status = d_status;
+    cudaError_t e = fp8 ? epg::launch_dispatch_fp8(p, st) : epg::launch_dispatch_bf16(p, st);
+    if (e != cudaSuccess) return EP_ERR_CUDA;
+
+    // stage 2: node rows to the ranks of their node
+    epg::HierParams h{};
+    h.node_x = static_cast<const uint8_t*>(node_x);
+    h.node_sf = node_sf;
+    h.topk_idx = topk_idx;
+    h.topk_weights = topk_weights;
+    h.dst_row = layout->dst_row;
+    h.node_row = layout->node_row;
+    h.T = T;
+    h.H = H;
+    h.K = K;
+    h.E = E;
+    h.R = R;
+    h.experts_per_rank = E / R;
+    h.ranks_per_node = rpn;
+    h.num_nodes = nodes;
+    h.node_capacity = node_capacity;
+    h.capacity = recv_capacity;
+    h.recv_x = static_cast<uint8_t*>(recv_x);
+    h.recv_sf = recv_sf;
+    h.sf_col_major = sf_col_major ? 1 : 0;
+    h.sf_stride = (recv_capacity + 3) / 4 * 4;
+    h.recv_topk_idx = recv_topk_idx;
+    h.recv_topk_weights = recv_topk_weights;
+    h.recv_src_idx = recv_src_idx;
+    h.status = d_status;
+    return epg::launch_forward_scaleup(h, fp8, st) == cudaSuccess ? EP_OK : EP_ERR_CUDA;
+}
+
+ep_status_t ep_combine_hierarchical(const void* y, int64_t num_y_rows, const int64_t* topk_idx,
+                                    const float* topk_weights, int T, int H, int K, int E, int R, int rpn,
+                                    const ep_layout_t* layout, int64_t node_capacity, void* node_y, void* out,
+                                    int32_t* d_status, void* cuda_stream) {
+    if (!layout || !d_status) return EP_ERR_INVALID_ARG;
+    ep_status_t s = check_shape(T, K, E, R);
+    if (s != EP_OK) return s;
+    if (rpn < 1 || R % rpn != 0) return EP_ERR_INVALID_ARG;
+    if (H < 1 || H % 8 != 0) return EP_ERR_INVALID_ARG;
+    if (num_y_rows < 0 || num_y_rows > INT32_MAX) return EP_ERR_INVALID_ARG;
+    if (node_capacity < 0 || node_capacity > INT32_MAX) return EP_ERR_INVALID_ARG;
+    if (num_y_rows > 0 && !ok_ptr(y)) return EP_ERR_INVALID_ARG;
+    if (node_capacity > 0 && !ok_ptr(node_y)) return EP_ERR_INVALID_ARG;
+    if (T > 0 && (!ok_ptr(out) || !ok_ptr(layout->dst_row) || !ok_ptr(layout->node_row))) return EP_ERR_INVALID_ARG;
+    if (topk_weights && T > 0 && (!ok_ptr(topk_weights) || !ok_ptr(topk_idx))) return EP_ERR_INVALID_ARG;
+    if (T == 0) return EP_OK;
+    const int nodes = R / rpn;
+    cudaStream_t st = static_cast<cudaStream_t>(cuda_stream);
+
+    // stage 1: per (token, node) partial sums of the node's ranks
+    epg::HierParams h{};
+    h.topk_idx = topk_idx;
+    h.topk_weights = topk_weights;
+    h.dst_row = layout->dst_row;
+    h.node_row = layout->node_row;
+    h.T = T;
+    h.H = H;
+    h.K = K;
+    h.E = E;
+    h.R = R;
+    h.experts_per_rank = E / R;
+    h.ranks_per_node = rpn;
+    h.num_nodes = nodes;
+    h.node_capacity = node_capacity;
+    h.y = static_cast<const uint8_t*>(y);
+    h.num_y_rows = num_y_rows;
+    h.node_y = static_cast<uint8_t*>(node_y);
+    h.status = d_status;
+    if (epg::launch_reduce_scaleup(h, topk_weights != nullptr, st) != cudaSuccess) return EP_ERR_CUDA;
+
+    // stage 2: the ordinary unweighted combine over the node rows
+    epg::CombineParams p{};
+    p.y = static_cast<const uint8_t*>(node_y);
+    p.num_y_rows = node_capacity;
+    p.topk_idx = topk_idx;
+    p.dst_row = layout->node_row;
+    p.T = T;
+    p.H = H;
+    p.K = K;
+    p.E = E;
+    p.R = nodes;
+    p.experts_per_rank = E / R;
+    p.out = static_cast<uint8_t*>(out);
+    p.status = d_status;
+    return epg::launch_combine(p, false, st) == cudaSuccess ? EP_OK : EP_ERR_CUDA;
 }
 
 ep_status_t ep_combine(const void* y, int64_t num_y_rows, const int64_t* topk_idx,

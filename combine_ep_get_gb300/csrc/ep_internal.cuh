@@ -32,6 +32,8 @@ struct LayoutParams {
     int32_t* src_dst_count;
     int32_t* token_offset;
     int32_t* expanded_row;   // [T][K] or null
+    int32_t* node_offset;    // [num_nodes + 1] or null (set together with node_row)
+    int32_t* node_row;       // [T][num_nodes] or null
     // workspace
     int32_t* ws_rank;      // [R][num_tiles]: tile counts, then exclusive tile prefix
     int32_t* ws_expert;    // [E][num_tiles]
@@ -80,6 +82,36 @@ struct CombineParams {
     int num_sms;            // > 0: SM-limited mode (persistent CTAs, one per SM)
 };
 
+// Hierarchical path, the scale-up halves (the scale-out halves reuse the
+// dispatch and combine kernels with node_row in place of dst_row).
+struct HierParams {
+    const uint8_t* node_x;        // forward: node rows, row_bytes each
+    const float* node_sf;         // forward, FP8: [node_capacity][H/128]
+    const int64_t* topk_idx;
+    const float* topk_weights;
+    const int32_t* dst_row;       // [T][R]
+    const int32_t* node_row;      // [T][num_nodes]
+    int T, H, K, E, R, experts_per_rank, ranks_per_node, num_nodes;
+    int64_t node_capacity;
+    // forward (dispatch stage 2)
+    int64_t capacity;
+    uint8_t* recv_x;
+    float* recv_sf;
+    int sf_col_major;
+    int64_t sf_stride;
+    int32_t* recv_topk_idx;
+    float* recv_topk_weights;
+    int32_t* recv_src_idx;
+    // reduce (combine stage 1)
+    const uint8_t* y;
+    int64_t num_y_rows;
+    uint8_t* node_y;
+    int32_t* status;
+    int chunks;             // pieces per row
+    uint32_t chunk_bytes;   // forward: bytes per piece (multiple of 16)
+    int chunk_vecs;         // reduce: 16-byte vectors per piece
+};
+
 struct CombineWeightsParams {
     const float* recv_topk_weights;
     int64_t num_rows;
@@ -105,6 +137,8 @@ cudaError_t launch_dispatch_fp8(DispatchParams p, cudaStream_t stream);
 cudaError_t launch_combine(CombineParams p, bool weighted, cudaStream_t stream);
 cudaError_t launch_combine_topk_weights(const CombineWeightsParams& p, cudaStream_t stream);
 cudaError_t launch_accumulate_expert_stats(const int32_t* counts, int E, int64_t* stats, cudaStream_t stream);
+cudaError_t launch_forward_scaleup(HierParams p, bool fp8, cudaStream_t stream);
+cudaError_t launch_reduce_scaleup(HierParams p, bool weighted, cudaStream_t stream);
 
 // Launch with programmatic dependent launch allowed: the kernel may begin
 // while the previous kernel on the stream is still running, and must call

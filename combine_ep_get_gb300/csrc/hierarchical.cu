@@ -1,0 +1,268 @@
+// Scale-up halves of the hierarchical (two-stage) path ("DeepEP V2
+// ElasticBuffer architecture": hybrid_dispatch / hybrid_combine, used when
+// there is more than one scale-out domain; node = rank / ranks_per_node as in
+// "V1 Buffer initialisation" section 3.2).
+//
+// Dispatch stage 1 (scale-out) sends each token once to every node holding
+// one of its experts: the ordinary dispatch kernels run with node_row as the
+// destination table.  Stage 2 (here, forward_scaleup_kernel) copies each node
+// row to the ranks of that node that need the token and writes the same
+// per-row metadata as the single-stage dispatch, so the receive buffers come
+// out identical.
+//
+// Combine stage 1 (here, reduce_scaleup_kernel) sums, per (token, node), the
+// rows of the node's ranks (fp32, weighted or not) into one bf16 node row;
+// stage 2 (scale-out) is the ordinary unweighted combine over node_row.
+//
+// Both kernels take one CTA per (token, piece) and walk the token's nodes in
+// order; all stores are 16-byte vectors.
+#include <cuda_bf16.h>
+
+#include "ep_internal.cuh"
+
+namespace epg {
+namespace {
+
+constexpr int kFwdThreads = 256;
+constexpr int kFwdUnroll = 4;
+constexpr int kRedThreads = 128;
+constexpr int kRedBatch = 4;
+
+// Metadata of token t's rows in ranks [r0, r1) (one warp, lane k < K).
+__device__ __forceinline__ void forward_metadata(const HierParams& p, int t, int r0, int r1, int lane) {
+    const int K = p.K;
+    const int64_t e_l = lane < K ? p.topk_idx[static_cast<int64_t>(t) * K + lane] : -1;
+    const float w_l = (lane < K && p.recv_topk_weights) ? p.topk_weights[static_cast<int64_t>(t) * K + lane] : 0.0f;
+    for (int r = r0; r < r1; ++r) {
+        const int d = p.dst_row[static_cast<int64_t>(t) * p.R + r];   // uniform over the warp
+        if (d < 0 || d >= p.capacity) continue;
+        if (lane < K) {
+            const bool on = e_l >= 0 && e_l < p.E && static_cast<int>(e_l) / p.experts_per_rank == r;
+            if (p.recv_topk_idx)
+                p.recv_topk_idx[static_cast<int64_t>(d) * K + lane] =
+                    on ? static_cast<int32_t>(e_l) - r * p.experts_per_rank : -1;
+            if (p.recv_topk_weights) p.recv_topk_weights[static_cast<int64_t>(d) * K + lane] = on ? w_l : 0.0f;
+        }
+        if (lane == 0 && p.recv_src_idx) p.recv_src_idx[d] = t;
+    }
+}
+
+template <bool kFp8>
+__global__ void __launch_bounds__(kFwdThreads, 6) forward_scaleup_kernel(const HierParams p) {
+    const int gtid = threadIdx.x;
+    const int warp = gtid >> 5;
+    const int lane = gtid & 31;
+    pdl_wait();   // node rows come from the previous kernel
+    const int t = static_cast<int>(blockIdx.x / p.chunks);
+    const int c = static_cast<int>(blockIdx.x - static_cast<unsigned>(t) * p.chunks);
+    const uint32_t row_bytes = kFp8 ? static_cast<uint32_t>(p.H) : static_cast<uint32_t>(p.H) * 2u;
+    const uint32_t off = static_cast<uint32_t>(c) * p.chunk_bytes;
+    const int nvec = static_cast<int>(min(p.chunk_bytes, row_bytes - off) / 16);
+    const int nb = p.H / 128;
+    const int rpn = p.ranks_per_node;
+    bool cap_bad = false;
+    for (int n = 0; n < p.num_nodes; ++n) {
+        const int j = p.node_row[static_cast<int64_t>(t) * p.num_nodes + n];   // uniform over the CTA
+        if (j < 0) continue;
+        if (j >= p.node_capacity) {
+            cap_bad = true;
+            continue;
+        }
+        const int r0 = n * rpn;
+        if (c == 0 && warp == 1) forward_metadata(p, t, r0, r0 + rpn, lane);
+        if (kFp8 && c == 0 && warp == 2 && p.recv_sf) {
+            for (int r = r0; r < r0 + rpn; ++r) {
+                const int d = p.dst_row[static_cast<int64_t>(t) * p.R + r];
+                if (d < 0 || d >= p.capacity) continue;
+                for (int b = lane; b < nb; b += 32) {
+                    const float s = p.node_sf[static_cast<int64_t>(j) * nb + b];
+                    const int64_t si = p.sf_col_major ? static_cast<int64_t>(b) * p.sf_stride + d
+                                                      : static_cast<int64_t>(d) * nb + b;
+                    p.recv_sf[si] = s;
+                }
+            }
+        }
+        const uint8_t* src = p.node_x + static_cast<int64_t>(j) * row_bytes + off;
+        const int32_t* drow = p.dst_row + static_cast<int64_t>(t) * p.R + r0;
+        for (int base = 0; base < nvec; base += kFwdUnroll * kFwdThreads) {
+            uint4 u[kFwdUnroll];
+#pragma unroll
+            for (int k = 0; k < kFwdUnroll; ++k) {
+                const int v = base + gtid + k * kFwdThreads;
+                if (v < nvec) u[k] = ld_stream_v4(src + static_cast<size_t>(v) * 16);
+            }
+            for (int rb = 0; rb < rpn; rb += 32) {
+                const int d = rb + lane < rpn ? drow[rb + lane] : -1;
+                if (d >= p.capacity && c == 0 && base == 0) cap_bad = true;
+                unsigned m = __ballot_sync(0xffffffffu, d >= 0 && d < p.capacity);
+                while (m) {
+                    const int sl = __ffs(m) - 1;
+                    m &= m - 1;
+                    uint8_t* dst = p.recv_x + static_cast<int64_t>(__shfl_sync(0xffffffffu, d, sl)) * row_bytes + off;
+#pragma unroll
+                    for (int k = 0; k < kFwdUnroll; ++k) {
+                        const int v = base + gtid + k * kFwdThreads;
+                        if (v < nvec) st_v4(dst + static_cast<size_t>(v) * 16, u[k]);
+                    }
+                }
+            }
+        }
+    }
+    // every warp sees the same rows; warp 0 of the first piece reports
+    if (warp == 0 && c == 0 && __any_sync(0xffffffffu, cap_bad) && lane == 0) atomicOr(p.status, EP_ERR_CAPACITY);
+}
+
+template <bool kWeighted>
+__global__ void __launch_bounds__(kRedThreads, 12) reduce_scaleup_kernel(const HierParams p) {
+    __shared__ int s_rows[EP_MAX_TOPK];
+    __shared__ float s_coef[EP_MAX_TOPK];
+    __shared__ int s_n;
+    const int gtid = threadIdx.x;
+    pdl_wait();
+    const int t = static_cast<int>(blockIdx.x / p.chunks);
+    const int c = static_cast<int>(blockIdx.x - static_cast<unsigned>(t) * p.chunks);
+    const int rpn = p.ranks_per_node;
+    const int n_vec = p.H / 8;
+    const int v_begin = c * p.chunk_vecs;
+    const int v_end = min(n_vec, v_begin + p.chunk_vecs);
+    const int64_t row_bytes = static_cast<int64_t>(p.H) * 2;
+    for (int nd = 0; nd < p.num_nodes; ++nd) {
+        const int j = p.node_row[static_cast<int64_t>(t) * p.num_nodes + nd];   // uniform over the CTA
+        if (j < 0) continue;
+        if (j >= p.node_capacity) {
+            if (gtid == 0 && c == 0) atomicOr(p.status, EP_ERR_CAPACITY);
+            continue;
+        }
+        if (gtid < 32) {
+            const int lane = gtid;
+            int64_t e_l = -1;
+            float w_l = 0.0f;
+            if (kWeighted && lane < p.K) {
+                e_l = p.topk_idx[static_cast<int64_t>(t) * p.K + lane];
+                w_l = p.topk_weights[static_cast<int64_t>(t) * p.K + lane];
+            }
+            int n = 0;
+            bool cap_bad = false;
+            const int32_t* srow = p.dst_row + static_cast<int64_t>(t) * p.R + nd * rpn;
+            for (int rb = 0; rb < rpn; rb += 32) {
+                const int r = rb + lane;
+                const int d = r < rpn ? srow[r] : -1;
+                const bool ok = d >= 0 && d < p.num_y_rows;
+                if (d >= p.num_y_rows) cap_bad = true;
+                float coef = 1.0f;
+                if (kWeighted) {
+                    coef = 0.0f;
+                    const int rank = nd * rpn + r;
+                    for (int k = 0; k < p.K; ++k) {
+                        const int64_t e = __shfl_sync(0xffffffffu, e_l, k);
+                        const float w = __shfl_sync(0xffffffffu, w_l, k);
+                        if (e >= 0 && e < p.E && static_cast<int>(e) / p.experts_per_rank == rank) coef += w;
+                    }
+                }
+                const unsigned m = __ballot_sync(0xffffffffu, ok);
+                const int pos = n + __popc(m & ((1u << lane) - 1u));
+                if (ok && pos < EP_MAX_TOPK) {
+                    s_rows[pos] = d;
+                    s_coef[pos] = coef;
+                }
+                n += __popc(m);
+            }
+            if (n > EP_MAX_TOPK) {
+                if (lane == 0) atomicOr(p.status, EP_ERR_INVALID_INDEX);
+                n = EP_MAX_TOPK;
+            }
+            if (lane == 0) s_n = n;
+            if (__any_sync(0xffffffffu, cap_bad) && lane == 0 && c == 0) atomicOr(p.status, EP_ERR_CAPACITY);
+        }
+        __syncthreads();
+        const int n = s_n;
+        uint8_t* orow = p.node_y + static_cast<int64_t>(j) * row_bytes;
+        for (int v = v_begin + gtid; v < v_end; v += kRedThreads) {
+            float acc[8];
+#pragma unroll
+            for (int q = 0; q < 8; ++q) acc[q] = 0.0f;
+            const int64_t voff = static_cast<int64_t>(v) * 16;
+            for (int m0 = 0; m0 < n; m0 += kRedBatch) {
+                uint4 buf[kRedBatch];
+#pragma unroll
+                for (int i = 0; i < kRedBatch; ++i)
+                    if (m0 + i < n) buf[i] = ld_stream_v4(p.y + static_cast<int64_t>(s_rows[m0 + i]) * row_bytes + voff);
+#pragma unroll
+                for (int i = 0; i < kRedBatch; ++i) {
+                    if (m0 + i < n) {
+                        const uint32_t w[4] = {buf[i].x, buf[i].y, buf[i].z, buf[i].w};
+                        const float cf = kWeighted ? s_coef[m0 + i] : 1.0f;
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            if (kWeighted) {
+                                acc[2 * q] = fmaf(cf, __uint_as_float(w[q] << 16), acc[2 * q]);
+                                acc[2 * q + 1] = fmaf(cf, __uint_as_float(w[q] & 0xffff0000u), acc[2 * q + 1]);
+                            } else {
+                                acc[2 * q] += __uint_as_float(w[q] << 16);
+                                acc[2 * q + 1] += __uint_as_float(w[q] & 0xffff0000u);
+                            }
+                        }
+                    }
+                }
+            }
+            uint4 o;
+            uint32_t* ow = reinterpret_cast<uint32_t*>(&o);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const __nv_bfloat162 h = __floats2bfloat162_rn(acc[2 * q], acc[2 * q + 1]);
+                ow[q] = *reinterpret_cast<const uint32_t*>(&h);
+            }
+            st_v4(orow + voff, o);
+        }
+        __syncthreads();   // the row list is rebuilt for the next node
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_forward_scaleup(HierParams p, bool fp8, cudaStream_t stream) {
+    const DeviceInfo& di = device_info();
+    const uint32_t row_bytes = fp8 ? static_cast<uint32_t>(p.H) : static_cast<uint32_t>(p.H) * 2u;
+    // pieces of at most 16 KB; more pieces when there are few tokens
+    int chunks = static_cast<int>((row_bytes + 16383u) / 16384u);
+    const int want_items = 4 * di.num_sms;
+    if (p.T > 0 && static_cast<int64_t>(p.T) * chunks < want_items) {
+        const int more = (want_items + p.T - 1) / p.T;
+        const int max_chunks = static_cast<int>(row_bytes / 1024u) > 0 ? static_cast<int>(row_bytes / 1024u) : 1;
+        chunks = more < max_chunks ? more : max_chunks;
+        if (chunks < 1) chunks = 1;
+    }
+    uint32_t cb = (row_bytes + chunks - 1) / chunks;
+    cb = (cb + 15u) / 16u * 16u;
+    p.chunks = static_cast<int>((row_bytes + cb - 1) / cb);
+    p.chunk_bytes = cb;
+    const int64_t items = static_cast<int64_t>(p.T) * p.chunks;
+    if (items < 1) return cudaSuccess;
+    const dim3 grid(static_cast<unsigned>(items)), block(kFwdThreads);
+    if (fp8) return launch_pdl(forward_scaleup_kernel<true>, grid, block, 0, stream, p);
+    return launch_pdl(forward_scaleup_kernel<false>, grid, block, 0, stream, p);
+}
+
+cudaError_t launch_reduce_scaleup(HierParams p, bool weighted, cudaStream_t stream) {
+    const DeviceInfo& di = device_info();
+    const int n_vec = p.H / 8;
+    int chunks = (n_vec + 2 * kRedThreads - 1) / (2 * kRedThreads);
+    const int want_items = 4 * di.num_sms;
+    if (p.T > 0 && static_cast<int64_t>(p.T) * chunks < want_items) {
+        const int more = (want_items + p.T - 1) / p.T;
+        const int max_chunks = (n_vec + 31) / 32;
+        chunks = more < max_chunks ? more : max_chunks;
+        if (chunks < 1) chunks = 1;
+    }
+    int chunk_vecs = (n_vec + chunks - 1) / chunks;
+    chunks = (n_vec + chunk_vecs - 1) / chunk_vecs;
+    p.chunks = chunks;
+    p.chunk_vecs = chunk_vecs;
+    const int64_t items = static_cast<int64_t>(p.T) * chunks;
+    if (items < 1) return cudaSuccess;
+    const dim3 grid(static_cast<unsigned>(items)), block(kRedThreads);
+    if (weighted) return launch_pdl(reduce_scaleup_kernel<true>, grid, block, 0, stream, p);
+    return launch_pdl(reduce_scaleup_kernel<false>, grid, block, 0, stream, p);
+}
+
+}  // namespace epg

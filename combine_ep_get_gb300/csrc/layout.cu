@@ -154,6 +154,7 @@ __global__ void __launch_bounds__(kThreads) layout_scan_kernel(const LayoutParam
         const int n = col - p.R - p.E;
         row = p.ws_node + static_cast<size_t>(n) * p.num_tiles;
         total = p.num_tokens_per_node + n;
+        scan = p.node_row != nullptr;        // tile prefix per node for the node rows
     }
     int carry = 0;
     for (int base = 0; base < p.num_tiles; base += 32) {
@@ -261,6 +262,49 @@ __device__ void expanded_rows_of_tile(const LayoutParams& p, int tile, int t0, i
     }
 }
 
+// Node rows of one tile: a token is in node n when any rank of n holds it,
+// so node n's membership word is the OR of its ranks' words; node n's rows
+// are node_offset[n] + (its tokens in earlier tiles) + popc below the token.
+// Needs (num_nodes + 1) + 2 * kTileWords * num_nodes shared ints; ends with a
+// block barrier so the caller may reuse them.
+__device__ void node_rows_of_tile(const LayoutParams& p, int tile, int t0, int nt, const uint32_t* s_bm, int* sm,
+                                  int* s_warp) {
+    const int NN = p.num_nodes, R = p.R, rpn = p.ranks_per_node;
+    int* s_nbase = sm;                                                 // [NN + 1]
+    uint32_t* s_nbm = reinterpret_cast<uint32_t*>(s_nbase + NN + 1);   // [kTileWords][NN]
+    int* s_nwpre = reinterpret_cast<int*>(s_nbm + NN * kTileWords);    // [kTileWords][NN]
+    const int32_t* cn = p.num_tokens_per_node;
+    block_exclusive_scan(NN, [&](int i) { return cn[i]; }, [&](int i, int v) { s_nbase[i] = v; }, s_warp);
+    for (int n = threadIdx.x; n < NN; n += kThreads) s_nbase[n] += p.ws_node[static_cast<size_t>(n) * p.num_tiles + tile];
+    for (int i = threadIdx.x; i < NN * kTileWords; i += kThreads) {
+        const int w = i / NN;
+        const int n = i - w * NN;
+        uint32_t word = 0u;
+        for (int r = n * rpn; r < (n + 1) * rpn; ++r) word |= s_bm[w * R + r];
+        s_nbm[i] = word;
+    }
+    __syncthreads();
+    for (int n = threadIdx.x; n < NN; n += kThreads) {
+        int run = 0;
+#pragma unroll
+        for (int w = 0; w < kTileWords; ++w) {
+            s_nwpre[w * NN + n] = run;
+            run += __popc(s_nbm[w * NN + n]);
+        }
+    }
+    __syncthreads();
+    int32_t* out = p.node_row + static_cast<size_t>(t0) * NN;
+    for (int j = threadIdx.x; j < nt * NN; j += kThreads) {
+        const int tl = j / NN;
+        const int n = j - tl * NN;
+        const int w = tl >> 5;
+        const uint32_t word = s_nbm[w * NN + n];
+        const uint32_t b = static_cast<uint32_t>(tl & 31);
+        out[j] = ((word >> b) & 1u) ? s_nbase[n] + s_nwpre[w * NN + n] + __popc(word & ((1u << b) - 1u)) : -1;
+    }
+    __syncthreads();
+}
+
 __global__ void __launch_bounds__(kThreads) layout_rows_kernel(const LayoutParams p) {
     extern __shared__ __align__(16) uint32_t smem[];
     __shared__ int s_warp[kThreads / 32];
@@ -283,6 +327,12 @@ __global__ void __launch_bounds__(kThreads) layout_rows_kernel(const LayoutParam
         block_exclusive_scan(
             p.E, [&](int i) { return (ce[i] + a - 1) / a * a; }, [&](int i, int v) { eo[i] = v; },
             s_warp);
+        if (p.node_row) {
+            const int32_t* cn = p.num_tokens_per_node;
+            int32_t* no = p.node_offset;
+            block_exclusive_scan(p.num_nodes, [&](int i) { return cn[i]; }, [&](int i, int v) { no[i] = v; },
+                                 s_warp);
+        }
     }
     if (tile >= p.num_tiles) {
         if (p.token_offset && p.num_tiles == 0 && threadIdx.x == 0) p.token_offset[0] = 0;
@@ -370,6 +420,7 @@ __global__ void __launch_bounds__(kThreads) layout_rows_kernel(const LayoutParam
         }
     }
 
+    if (p.node_row) node_rows_of_tile(p, tile, t0, nt, s_bm, reinterpret_cast<int*>(s_wpre + R * kTileWords), s_warp);
     if (p.expanded_row) expanded_rows_of_tile(p, tile, t0, nt, s_wpre + R * kTileWords, s_warp);
 }
 
@@ -732,9 +783,10 @@ cudaError_t launch_layout(const LayoutParams& p, cudaStream_t stream) {
         configured_device = di.device;
     }
 
-    // the expanded rows are produced by the tiled path only
-    const ClusterPlan plan =
-        (cluster_ok && p.expanded_row == nullptr) ? plan_cluster(p, cluster_smem_max) : ClusterPlan{0, 0, 0};
+    // the expanded rows and the node rows are produced by the tiled path only
+    const ClusterPlan plan = (cluster_ok && p.expanded_row == nullptr && p.node_row == nullptr)
+                                 ? plan_cluster(p, cluster_smem_max)
+                                 : ClusterPlan{0, 0, 0};
     if (plan.ctas > 0) {
         cudaLaunchConfig_t cfg = {};
         cudaLaunchAttribute attr[2];
@@ -764,8 +816,14 @@ cudaError_t launch_layout(const LayoutParams& p, cudaStream_t stream) {
     const size_t smem_count =
         4 * (static_cast<size_t>(p.R) * kTileWords + static_cast<size_t>(p.num_nodes) * kTileWords + p.E);
     size_t smem_rows = 4 * (static_cast<size_t>(p.R) + 1 + 2 * static_cast<size_t>(p.R) * kTileWords);
-    if (p.expanded_row)
-        smem_rows += 4 * (static_cast<size_t>(kTileTokens) * p.K + 9 * static_cast<size_t>(p.E));
+    // node rows, then expanded rows, reuse the same region after the rank arrays
+    size_t extra = 0;
+    if (p.node_row) extra = 4 * (static_cast<size_t>(p.num_nodes) + 1 + 2 * static_cast<size_t>(kTileWords) * p.num_nodes);
+    if (p.expanded_row) {
+        const size_t ex = 4 * (static_cast<size_t>(kTileTokens) * p.K + 9 * static_cast<size_t>(p.E));
+        if (ex > extra) extra = ex;
+    }
+    smem_rows += extra;
     const int grid_tiles = p.num_tiles > 0 ? p.num_tiles : 1;
     cudaError_t e = launch_pdl(layout_count_kernel, dim3(grid_tiles), dim3(kThreads), smem_count, stream, p);
     if (e != cudaSuccess) return e;

@@ -101,6 +101,14 @@ typedef struct ep_layout {
     int32_t* expanded_row;          /* [T,K] expanded (per-expert) row of each valid
                                              (t, k), -1 if masked, or NULL; see
                                              ep_dispatch_expanded                        */
+    int32_t* node_offset;           /* [nodes+1] exclusive prefix of num_tokens_per_node
+                                             (nodes = R / ranks_per_node), or NULL       */
+    int32_t* node_row;              /* [T,nodes] row of token t in node n's scale-out
+                                             buffer or -1; rows of node n are
+                                             node_offset[n] + 0, 1, ... in ascending t.
+                                             NULL, or set together with node_offset and
+                                             num_tokens_per_node (ranks_per_node > 0);
+                                             see ep_dispatch_hierarchical              */
 } ep_layout_t;
 
 /* Bytes of device workspace ep_get_layout needs for these sizes (>= 16). */
@@ -300,6 +308,61 @@ ep_status_t ep_combine_topk_weights(const float* recv_topk_weights, int64_t num_
  */
 ep_status_t ep_accumulate_expert_stats(const ep_layout_t* layout, int num_experts, int64_t* stats,
                                        void* cuda_stream);
+
+/*
+ * Hierarchical (two-stage) dispatch ("DeepEP V2 ElasticBuffer architecture":
+ * hybrid_dispatch, the path taken when there is more than one scale-out
+ * domain; the WorkspaceLayout fragment keeps scale-out rank counts beside the
+ * scale-up ones; node = rank / ranks_per_node as in "V1 Buffer
+ * initialisation" section 3.2).  Node n holds ranks [n*rpn, (n+1)*rpn).
+ *
+ * Stage 1 (scale-out): each token goes once to every node holding one of its
+ * experts:  node_x[j] = x[t] (bf16) or its FP8 cast (codes, with row-major
+ * scales node_sf[j, H/128]), node_src_idx[j] = t, for j = node_row[t,n] >= 0.
+ * Stage 2 (scale-up): each node row is copied to the ranks r of its node with
+ * dst_row[t,r] >= 0, with the per-row metadata of ep_dispatch.  recv_* end up
+ * identical to ep_dispatch's (same arguments, layout and capacity).
+ *
+ * layout          from ep_get_layout with node_row / node_offset set (same
+ *                 ranks_per_node).
+ * node_capacity   rows of node_x / node_sf / node_src_idx; node_offset[nodes]
+ *                 rows are used, at most T * min(K, nodes)
+ *                 (= ep_recv_capacity_bound(T, K, nodes)).  Rows at or beyond
+ *                 it set EP_ERR_CAPACITY and are skipped.
+ * node_x          bf16 [node_capacity, H] or FP8 codes [node_capacity, H];
+ *                 node_sf fp32 [node_capacity, H/128] (FP8, required);
+ *                 node_src_idx int32 [node_capacity] or NULL.
+ * Other arguments and errors as ep_dispatch (no SM-limited mode).  Two kernel
+ * launches on the stream; the node buffers are the caller's.
+ */
+ep_status_t ep_dispatch_hierarchical(const void* x, const int64_t* topk_idx, const float* topk_weights,
+                                     int num_tokens, int hidden, int num_topk, int num_experts,
+                                     int num_ranks, int ranks_per_node, const ep_layout_t* layout,
+                                     int out_dtype, int64_t node_capacity, void* node_x, float* node_sf,
+                                     int32_t* node_src_idx, int64_t recv_capacity, void* recv_x,
+                                     float* recv_sf, int sf_col_major, int32_t* recv_topk_idx,
+                                     float* recv_topk_weights, int32_t* recv_src_idx, int32_t* d_status,
+                                     void* cuda_stream);
+
+/*
+ * Hierarchical (two-stage) combine ("DeepEP V2 ElasticBuffer architecture":
+ * hybrid_combine), the reverse of ep_dispatch_hierarchical.
+ * Stage 1 (scale-up reduce): for every (t, n) with j = node_row[t,n] >= 0,
+ *   node_y[j] = bf16( sum over ranks r of node n holding t of c(t,r) *
+ *   y[dst_row[t,r]] ), fp32 accumulation, c as in ep_combine.
+ * Stage 2 (scale-out reduce): out[t] = bf16( sum over nodes of node_y[j] ),
+ *   fp32 accumulation.
+ * The node partial is rounded to bf16 (the data type on the scale-out link),
+ * so the result may differ from ep_combine by the rounding of each partial.
+ * y bf16 [num_y_rows, H]; node_y bf16 [node_capacity, H] (the caller's
+ * buffer); out bf16 [T, H].  Rows beyond num_y_rows or node_capacity set
+ * EP_ERR_CAPACITY and are skipped.  Other arguments as ep_combine.
+ */
+ep_status_t ep_combine_hierarchical(const void* y, int64_t num_y_rows, const int64_t* topk_idx,
+                                    const float* topk_weights, int num_tokens, int hidden, int num_topk,
+                                    int num_experts, int num_ranks, int ranks_per_node,
+                                    const ep_layout_t* layout, int64_t node_capacity, void* node_y, void* out,
+                                    int32_t* d_status, void* cuda_stream);
 
 /*
  * SM count rule for the SM-limited mode ("DeepEP V2 ElasticBuffer

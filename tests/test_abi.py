@@ -31,7 +31,8 @@ def test_header_declares_the_entry_points():
     for n in ("ep_get_layout", "ep_dispatch", "ep_combine", "ep_layout_workspace_bytes",
               "ep_recv_capacity_bound", "ep_status_string", "ep_abi_version", "ep_dispatch_expanded",
               "ep_combine_expanded", "ep_expanded_capacity_bound", "ep_combine_topk_weights",
-              "ep_accumulate_expert_stats", "ep_theoretical_num_sms"):
+              "ep_accumulate_expert_stats", "ep_theoretical_num_sms",
+              "ep_dispatch_hierarchical", "ep_combine_hierarchical"):
         assert n in names
 
 
@@ -52,7 +53,7 @@ def test_status_strings_and_sizes(lib):
     ws = lib.ep_layout_workspace_bytes(4096, 8, 256, 8, 0)
     tiles = 16
     assert ws >= 4 * tiles * (8 + 256 + 8 * 8)
-    assert lib.ep_abi_version() == 5
+    assert lib.ep_abi_version() == 6
 
 
 def test_host_checks_reject_before_any_launch(lib):
@@ -175,3 +176,52 @@ def test_sm_count_rule_rejects_bad_arguments(lib):
     ]
     for a in bad:
         assert f(*a) == 0, a
+
+
+def test_hierarchical_host_checks(lib):
+    """Node rows and the two-stage calls reject bad arguments before any launch."""
+    from combine_ep_get_gb300 import binding as B
+    vp = ctypes.c_void_p
+    st = vp(16)
+    f = lib.ep_get_layout
+    f.restype = ctypes.c_int32
+    f.argtypes = [vp, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                  ctypes.c_int, ctypes.POINTER(B.ep_layout_t), vp, ctypes.c_size_t, vp, vp]
+    fields = dict(num_tokens_per_rank=16, num_tokens_per_node=128, num_tokens_per_expert=32, is_token_in_rank=48,
+                  rank_offset=64, expert_offset=80, dst_row=96, node_offset=144, node_row=160)
+    ok = B.ep_layout_t(**fields)
+    assert f(vp(16), 10, 8, 256, 8, 4, 1, ctypes.byref(B.ep_layout_t(**{**fields, "node_offset": None})),
+             vp(256), 1 << 20, st, None) == B.EP_ERR_INVALID_ARG          # node_row without node_offset
+    assert f(vp(16), 10, 8, 256, 8, 0, 1, ctypes.byref(ok), vp(256), 1 << 20, st, None) == B.EP_ERR_INVALID_ARG
+    assert f(vp(16), 10, 8, 256, 8, 4, 1, ctypes.byref(B.ep_layout_t(**{**fields, "num_tokens_per_node": None})),
+             vp(256), 1 << 20, st, None) == B.EP_ERR_INVALID_ARG          # no node counts
+    assert f(vp(16), 10, 8, 256, 8, 4, 1, ctypes.byref(B.ep_layout_t(**{**fields, "node_row": 161})),
+             vp(256), 1 << 20, st, None) == B.EP_ERR_INVALID_ARG          # misaligned
+    d = lib.ep_dispatch_hierarchical
+    d.restype = ctypes.c_int32
+    d.argtypes = [vp, vp, vp] + [ctypes.c_int] * 6 + [ctypes.POINTER(B.ep_layout_t), ctypes.c_int, ctypes.c_int64,
+                                                       vp, vp, vp, ctypes.c_int64, vp, vp, ctypes.c_int, vp, vp, vp,
+                                                       vp, vp]
+    args = [vp(16), vp(32), vp(48), 10, 7168, 8, 256, 8, 4, ctypes.byref(ok), B.EP_BF16, 20, vp(64), None, None,
+            100, vp(80), None, 0, None, None, None, st, None]
+    bad = list(args); bad[8] = 3                                             # rpn does not divide R
+    assert d(*bad) == B.EP_ERR_INVALID_ARG
+    bad = list(args); bad[9] = ctypes.byref(B.ep_layout_t(**{**fields, "node_row": None}))
+    assert d(*bad) == B.EP_ERR_INVALID_ARG                                   # layout without node rows
+    bad = list(args); bad[10] = B.EP_FP8_E4M3; bad[16] = vp(80); bad[17] = vp(96)
+    assert d(*bad) == B.EP_ERR_INVALID_ARG                                   # FP8 needs node_sf
+    bad = list(args); bad[12] = None                                         # node_x missing
+    assert d(*bad) == B.EP_ERR_INVALID_ARG
+    bad = list(args); bad[11] = -1                                           # node capacity
+    assert d(*bad) == B.EP_ERR_INVALID_ARG
+    c = lib.ep_combine_hierarchical
+    c.restype = ctypes.c_int32
+    c.argtypes = [vp, ctypes.c_int64, vp, vp] + [ctypes.c_int] * 6 + [ctypes.POINTER(B.ep_layout_t),
+                                                                       ctypes.c_int64, vp, vp, vp, vp]
+    cargs = [vp(16), 100, vp(32), None, 10, 7168, 8, 256, 8, 4, ctypes.byref(ok), 20, vp(48), vp(64), st, None]
+    bad = list(cargs); bad[12] = None                                        # node_y missing
+    assert c(*bad) == B.EP_ERR_INVALID_ARG
+    bad = list(cargs); bad[9] = 0                                            # rpn
+    assert c(*bad) == B.EP_ERR_INVALID_ARG
+    bad = list(cargs); bad[10] = ctypes.byref(B.ep_layout_t(**{**fields, "node_row": None}))
+    assert c(*bad) == B.EP_ERR_INVALID_ARG
