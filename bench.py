@@ -10,9 +10,12 @@ logical ranks in one GPU's memory.  Inputs are seeded synthetic data.
 The metric is throughput in GB/s of algorithmic bytes (what the method must
 read and write: see ``algorithmic_bytes``) per step, with tokens/s beside it
 and the dominant kernel's HBM roofline fraction against the measured copy
-bandwidth.  L2 (129 MB) is flushed by a 256 MiB write before the layout and
-again before the combine (in a real layer, expert GEMMs run between them), and
-the flushes are outside the timed events.
+bandwidth.  L2 (129 MB) is flushed before the layout and again before the
+combine (in a real layer, expert GEMMs run between them), outside the timed
+events: a 256 MiB buffer is written and then a second one of 256 MiB is read,
+so the flush's own dirty lines are written back before the timed kernel starts
+(``--flush write`` keeps only the write, leaving ~129 MB of dirty lines for the
+timed kernel to write back).
 
 Multi-GPU: the path does not shard (ranks are partitions of one GPU), so
 ``--gpus N`` under torchrun runs N independent replicas; the time is the max
@@ -64,6 +67,9 @@ def parse_args(argv=None):
                          "HBM peak and the per-SM rates below")
     ap.add_argument("--sm-read-gbs", type=float, default=200.0, help="per-SM read rate of the SM count rule")
     ap.add_argument("--sm-write-gbs", type=float, default=50.0, help="per-SM write rate of the SM count rule")
+    ap.add_argument("--flush", choices=["write+read", "write"], default="write+read",
+                    help="L2 flush before layout and combine: write 256 MiB then read another 256 MiB "
+                         "(clean L2), or the write alone (dirty L2)")
     ap.add_argument("--e2e-steps", type=int, default=200)
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
                     help="CPU time budget of the oracle baseline (rank 0, N=1)")
@@ -313,6 +319,13 @@ def run_ours(args):
     recv_src = torch.empty((N,), dtype=torch.int32, device=dev)
     out = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    flush_rd = torch.zeros(L2_FLUSH_BYTES // 8, dtype=torch.int64, device=dev)
+    flush_sink = torch.zeros((), dtype=torch.int64, device=dev)
+
+    def flush_l2():
+        flush.zero_()
+        if args.flush == "write+read":
+            torch.sum(flush_rd, dim=0, out=flush_sink)
     if fp8:
         # FP8 dispatch; the combine reads a bf16 stand-in for the expert outputs
         recv_x = torch.empty((N, H), dtype=torch.uint8, device=dev)
@@ -389,14 +402,14 @@ def run_ours(args):
         # split: an extra event between layout and dispatch (per-kernel
         # breakdown); without it the dispatch launch overlaps the layout's
         # tail (programmatic dependent launch), as in a real layer
-        flush.zero_()
+        flush_l2()
         ev[0].record()
         do_layout()
         if split:
             ev[4].record()
         do_dispatch()
         ev[1].record()
-        flush.zero_()
+        flush_l2()
         ev[2].record()
         do_combine()
         ev[3].record()
@@ -532,7 +545,9 @@ def run_ours(args):
             "num_sms": sms_config,
             "bytes_per_step": nbytes,
             "parallelism": "replicas" if world > 1 else "single",
-            "l2": "flushed (256 MiB write) before layout and before combine, outside the timed events",
+            "l2": ("flushed before layout and before combine, outside the timed events: 256 MiB written, "
+                   "then another 256 MiB read (the flush's dirty lines drained)" if args.flush == "write+read"
+                   else "flushed (256 MiB write) before layout and before combine, outside the timed events"),
             "launch": ("one CUDA graph per step (flushes, calls and timing events inside)"
                        if use_graph else "eager"),
             "arithmetic": ("fp8 e4m3 dispatch with fp32 per-128-channel scales; combine of bf16 "

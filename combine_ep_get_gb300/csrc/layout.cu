@@ -473,6 +473,26 @@ __device__ int smem_exclusive_scan(int* a, int n, int* s_warp) {
     return total;
 }
 
+// Exclusive scan of a[0, n) in shared memory by one warp (each lane a
+// contiguous run of at most kWarpScanMax / 32 values); returns the total.
+constexpr int kWarpScanMax = 256;
+__device__ int warp_exclusive_scan_smem(int* a, int n) {
+    const int lane = threadIdx.x & 31;
+    const int per = (n + 31) / 32;
+    const int begin = min(n, lane * per);
+    const int end = min(n, begin + per);
+    int local = 0;
+    for (int i = begin; i < end; ++i) local += a[i];
+    const int incl = warp_inclusive_scan(local);
+    int run = incl - local;
+    for (int i = begin; i < end; ++i) {
+        const int v = a[i];
+        a[i] = run;
+        run += v;
+    }
+    return __shfl_sync(0xffffffffu, incl, 31);
+}
+
 __global__ void __launch_bounds__(kClusterThreads, 1)
     layout_cluster_kernel(const LayoutParams p, int tokens_per_cta) {
     namespace cg = cooperative_groups;
@@ -496,6 +516,7 @@ __global__ void __launch_bounds__(kClusterThreads, 1)
     int* s_wtok = s_ntok + 32 * W;                                  // [W] rows of earlier words
     __shared__ int s_rows_total;                                    // read by later CTAs
     __shared__ int s_cta_base;
+    __shared__ int s_totals[2];                                     // N, expert rows
     const int tid = threadIdx.x;
     const int t0 = me * tokens_per_cta;
     const int nt = max(0, min(tokens_per_cta, p.T - t0));
@@ -574,7 +595,8 @@ __global__ void __launch_bounds__(kClusterThreads, 1)
     }
     cluster.sync();   // counts of every CTA visible; src_dst_count zeroed
 
-    // Phase 2: rank totals, this CTA's base per rank, and (two CTAs) the outputs.
+    // Phase 2: rank totals and this CTA's base per rank (every CTA), expert and
+    // node totals (the last CTA), all from the other CTAs' shared memory.
     // Remote loads are issued for all CTAs before any is summed (one latency).
     for (int r = tid; r < R; r += kClusterThreads) {
         int v[kMaxClusterCtas];
@@ -595,23 +617,18 @@ __global__ void __launch_bounds__(kClusterThreads, 1)
         const int sum = warp_inclusive_scan(v);
         if (lane == 31) s_cta_base = sum;
     }
-    // expert totals: CTA c sums experts [c E / C, (c+1) E / C) over all CTAs
-    for (int e = me * E / C + tid; e < (me + 1) * E / C; e += kClusterThreads) {
-        int v[kMaxClusterCtas];
-#pragma unroll
-        for (int c = 0; c < kMaxClusterCtas; ++c) v[c] = c < C ? cluster.map_shared_rank(s_hist, c)[e] : 0;
-        int tot = 0;
-#pragma unroll
-        for (int c = 0; c < kMaxClusterCtas; ++c) tot += v[c];
-        p.num_tokens_per_expert[e] = tot;
-    }
-    __syncthreads();
-    const int n_recv = smem_exclusive_scan(s_tot, R, s_warp);   // s_tot = rank_offset
-    if (me == 0) {
-        for (int r = tid; r < R; r += kClusterThreads) p.rank_offset[r] = s_tot[r];
-        if (tid == 0) p.rank_offset[R] = n_recv;
-    }
     if (me == C - 1) {
+        // only this CTA reads any s_hist, and each e is read and rewritten by one thread
+        for (int e = tid; e < E; e += kClusterThreads) {
+            int v[kMaxClusterCtas];
+#pragma unroll
+            for (int c = 0; c < kMaxClusterCtas; ++c) v[c] = c < C ? cluster.map_shared_rank(s_hist, c)[e] : 0;
+            int tot = 0;
+#pragma unroll
+            for (int c = 0; c < kMaxClusterCtas; ++c) tot += v[c];
+            p.num_tokens_per_expert[e] = tot;
+            s_hist[e] = (tot + p.alignment - 1) / p.alignment * p.alignment;
+        }
         for (int n = tid; n < NN; n += kClusterThreads) {
             int v[kMaxClusterCtas];
 #pragma unroll
@@ -622,24 +639,42 @@ __global__ void __launch_bounds__(kClusterThreads, 1)
             p.num_tokens_per_node[n] = tot;
         }
     }
-    cluster.sync();   // every remote read done; every CTA's expert totals are in global memory
-    if (me == C - 1) {
-        for (int e = tid; e < E; e += kClusterThreads) {
-            const int tot = __ldcg(p.num_tokens_per_expert + e);
-            s_hist[e] = (tot + p.alignment - 1) / p.alignment * p.alignment;
+    __syncthreads();
+    // Exclusive scans: s_tot becomes rank_offset (every CTA), s_hist
+    // expert_offset (last CTA); one warp each when short, else the block.
+    if (R <= kWarpScanMax) {
+        if (warp_id == 0) {
+            const int tot = warp_exclusive_scan_smem(s_tot, R);
+            if (lane == 0) s_totals[0] = tot;
         }
-        __syncthreads();
-        const int tot = smem_exclusive_scan(s_hist, E, s_warp);
-        for (int e = tid; e < E; e += kClusterThreads) p.expert_offset[e] = s_hist[e];
-        if (tid == 0) p.expert_offset[E] = tot;
+    } else {
+        const int tot = smem_exclusive_scan(s_tot, R, s_warp);
+        if (tid == 0) s_totals[0] = tot;
     }
-
-    // Phase 3: dst_row and is_token_in_rank of this CTA's [nt, R] block.
-    for (int i = tid; i < R * W; i += kClusterThreads) {
-        const int r = i % R;
-        s_wbase[i] += s_tot[r] + s_before[r];
+    if (me == C - 1) {
+        if (E <= kWarpScanMax) {
+            if (warp_id == 2) {
+                const int tot = warp_exclusive_scan_smem(s_hist, E);
+                if (lane == 0) s_totals[1] = tot;
+            }
+        } else {
+            const int tot = smem_exclusive_scan(s_hist, E, s_warp);
+            if (tid == 0) s_totals[1] = tot;
+        }
     }
     __syncthreads();
+    const int n_recv = s_totals[0];
+    if (me == 0) {
+        for (int r = tid; r < R; r += kClusterThreads) p.rank_offset[r] = s_tot[r];
+        if (tid == 0) p.rank_offset[R] = n_recv;
+    }
+    if (me == C - 1) {
+        for (int e = tid; e < E; e += kClusterThreads) p.expert_offset[e] = s_hist[e];
+        if (tid == 0) p.expert_offset[E] = s_totals[1];
+    }
+
+    // Phase 3: dst_row and is_token_in_rank of this CTA's [nt, R] block:
+    // rank_offset + rows of earlier CTAs + rows of earlier words + popc below.
     const int n_el = nt * R;
     int32_t* drow = p.dst_row + static_cast<int64_t>(t0) * R;
     uint8_t* inr = p.is_token_in_rank + static_cast<int64_t>(t0) * R;
@@ -657,7 +692,7 @@ __global__ void __launch_bounds__(kClusterThreads, 1)
                 const uint32_t word = s_bm[w * R + r];
                 const uint32_t b = static_cast<uint32_t>(tl & 31);
                 if ((word >> b) & 1u) {
-                    v[u] = s_wbase[w * R + r] + __popc(word & ((1u << b) - 1u));
+                    v[u] = s_tot[r] + s_before[r] + s_wbase[w * R + r] + __popc(word & ((1u << b) - 1u));
                     in4 |= 1u << (8 * u);
                 }
             }
@@ -703,6 +738,8 @@ __global__ void __launch_bounds__(kClusterThreads, 1)
             if (c) atomicAdd(&p.src_dst_count[s * R + r], c);
         }
     }
+    // No CTA may exit (releasing its shared memory) while another still reads it.
+    cluster.sync();
 }
 
 size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
