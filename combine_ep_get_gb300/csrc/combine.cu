@@ -12,6 +12,13 @@
 // accumulating (64 bytes of reads in flight per thread, 12 CTAs per SM).  The
 // reduced vector is rounded to bf16 and stored once.  HBM-bound: reads are
 // ~n(t) times the writes.
+//
+// SM-limited mode (num_sms > 0): CTAs of 8 groups of 128 threads, one per SM,
+// each group looping over items with 8 source rows of loads in flight per
+// thread (same order and arithmetic, so results are bit-identical).  A
+// bulk-copy ring (one producer warp filling 13 shared-memory slots, eight
+// consumer warps) measured ~30% slower: per 14 KB slot its consumers spent
+// more instructions on the ring handshake than register loads cost.
 #include <cuda_bf16.h>
 
 #include "ep_internal.cuh"
@@ -31,6 +38,9 @@ constexpr int kThreads = EP_COMBINE_THREADS;
 #define EP_COMBINE_BATCH 4
 #endif
 constexpr int kBatch = EP_COMBINE_BATCH;
+#ifndef EP_COMBINE_SM_BATCH
+#define EP_COMBINE_SM_BATCH 8        // SM-limited mode: rows of loads in flight per thread
+#endif
 
 // SM-limited mode: CTAs of kSmGroups x kThreads threads, one per SM, each
 // group looping over (token, piece) items.
@@ -105,13 +115,14 @@ __device__ __forceinline__ void combine_item(const CombineParams& p, int64_t it,
 #pragma unroll
         for (int q = 0; q < 8; ++q) acc[q] = 0.0f;
         const int64_t off = static_cast<int64_t>(v) * 16;
-        for (int m0 = 0; m0 < n; m0 += kBatch) {
-            uint4 buf[kBatch];
+        constexpr int kB = kGroups == 1 ? kBatch : EP_COMBINE_SM_BATCH;
+        for (int m0 = 0; m0 < n; m0 += kB) {
+            uint4 buf[kB];
 #pragma unroll
-            for (int j = 0; j < kBatch; ++j)
+            for (int j = 0; j < kB; ++j)
                 if (m0 + j < n) buf[j] = ld_stream_v4(p.y + static_cast<int64_t>(s_rows[m0 + j]) * row_bytes + off);
 #pragma unroll
-            for (int j = 0; j < kBatch; ++j) {
+            for (int j = 0; j < kB; ++j) {
                 if (m0 + j < n) {
                     const uint32_t w[4] = {buf[j].x, buf[j].y, buf[j].z, buf[j].w};
                     if (kWeighted) {

@@ -19,7 +19,10 @@
 //   a row never passes through registers; warps 1-3 write the metadata.  With
 //   token_offset it splits the receive rows evenly over the CTAs.  On GB300 it
 //   measured ~7% slower than the register path for every stage count, piece
-//   size and L2 hint tried, so it is not the default.
+//   size and L2 hint tried, so it is not the default over the whole GPU; it is
+//   the SM-limited mode (num_sms > 0), one CTA per SM with a 12-slot ring,
+//   where it reaches the SM's store limit (~61 GB/s on GB300) that the
+//   register copies miss by ~20%.
 //
 // FP8 path: one CTA per (token, piece of 128-channel blocks); each half-warp
 //   owns one 128-channel block, loads it with 16-byte vectors, takes amax by
@@ -57,8 +60,13 @@ namespace {
 #endif
 
 constexpr int kBf16Threads = 128;
-constexpr int kStages = EP_DISPATCH_STAGES;
-constexpr int kStoreDepth = EP_DISPATCH_STORE_DEPTH;
+constexpr int kBulkStages = EP_DISPATCH_STAGES;
+constexpr int kBulkStoreDepth = EP_DISPATCH_STORE_DEPTH;
+// SM-limited mode: one persistent CTA per SM whose shared-memory ring keeps
+// 12 row loads in flight (a CTA's stores are bounded by the SM's write port,
+// ~61 GB/s on GB300, which this ring reaches; register copies reach ~50).
+constexpr int kSmBulkStages = 12;
+constexpr int kSmBulkStoreDepth = 4;
 
 // The work of one CTA.  Strided mode: items first, first + stride, ... of the
 // (token, piece) list, every destination stored.  Balanced mode (rows
@@ -166,6 +174,7 @@ __device__ __forceinline__ void write_metadata(const DispatchParams& p, int t, i
     }
 }
 
+template <int kStages, int kStoreDepth>
 __global__ void __launch_bounds__(kBf16Threads) dispatch_bf16_kernel(const DispatchParams p) {
     extern __shared__ __align__(128) uint8_t smem[];
     __shared__ CtaWork s_work;
@@ -516,13 +525,63 @@ __global__ void __launch_bounds__(kFp8Threads * kGroups) dispatch_fp8_kernel(con
     }
 }
 
+// Bulk-copy path: the default alternative (EP_DISPATCH_IMPL=0) and the
+// SM-limited mode (num_sms > 0, one CTA per SM with a deeper ring).
+template <int kStages, int kStoreDepth>
+cudaError_t launch_dispatch_bulk_t(DispatchParams p, int max_ctas, cudaStream_t stream) {
+    const DeviceInfo& di = device_info();
+    const uint32_t row_bytes = static_cast<uint32_t>(p.H) * 2u;
+    int chunks = static_cast<int>((row_bytes + EP_DISPATCH_PIECE_MAX - 1) / EP_DISPATCH_PIECE_MAX);
+    const int want_items = 2 * di.num_sms;
+    if (p.T > 0 && static_cast<int64_t>(p.T) * chunks < want_items) {
+        const int more = (want_items + p.T - 1) / p.T;
+        const int max_chunks = static_cast<int>(row_bytes / 1024u) > 0 ? static_cast<int>(row_bytes / 1024u) : 1;
+        chunks = more < max_chunks ? more : max_chunks;
+        if (chunks < 1) chunks = 1;
+    }
+    uint32_t chunk_bytes = (row_bytes + chunks - 1) / chunks;
+    chunk_bytes = (chunk_bytes + 15u) / 16u * 16u;
+    chunks = static_cast<int>((row_bytes + chunk_bytes - 1) / chunk_bytes);
+    p.chunks = chunks;
+    p.chunk_bytes = chunk_bytes;
+    const size_t smem = 128 + static_cast<size_t>(kStages) * chunk_bytes;
+
+    static thread_local int configured_device = -1;
+    static thread_local int blocks_per_sm = 1;
+    static thread_local size_t configured_smem = 0;
+    if (configured_device != di.device || configured_smem != smem) {
+        cudaError_t e = cudaFuncSetAttribute(dispatch_bf16_kernel<kStages, kStoreDepth>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             static_cast<int>(smem));
+        if (e != cudaSuccess) return e;
+        int nb = 0;
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, dispatch_bf16_kernel<kStages, kStoreDepth>,
+                                                          kBf16Threads, smem);
+        if (e != cudaSuccess) return e;
+        blocks_per_sm = nb > 0 ? nb : 1;
+        configured_device = di.device;
+        configured_smem = smem;
+    }
+    const int64_t num_items = static_cast<int64_t>(p.T) * chunks;
+    int64_t grid = static_cast<int64_t>(di.num_sms) * blocks_per_sm;
+    if (max_ctas > 0 && grid > max_ctas) grid = max_ctas;
+    if (grid > num_items) grid = num_items;
+    if (grid < 1) return cudaSuccess;
+    return launch_pdl(dispatch_bf16_kernel<kStages, kStoreDepth>, dim3(static_cast<unsigned>(grid)),
+                      dim3(kBf16Threads), smem, stream, p);
+}
+
 }  // namespace
 
 cudaError_t launch_dispatch_bf16(DispatchParams p, cudaStream_t stream) {
     const DeviceInfo& di = device_info();
     const uint32_t row_bytes = static_cast<uint32_t>(p.H) * 2u;
-    // Pieces: at most 16 KB each; more pieces when there are few tokens so
-    // that every SM gets work.
+    if (p.num_sms > 0 && p.expanded_row == nullptr) {
+        // SM-limited rank-row dispatch: the bulk-copy kernel with the deep
+        // ring; at most num_sms CTAs (one per SM for rows of 6 KB or more)
+        const int n = p.num_sms < di.num_sms ? p.num_sms : di.num_sms;
+        return launch_dispatch_bulk_t<kSmBulkStages, kSmBulkStoreDepth>(p, n, stream);
+    }
     if (EP_DISPATCH_IMPL == 1 || p.expanded_row != nullptr) {
         // register path (the expanded mode always takes it): one CTA per (token, piece of <= 16 KB); more pieces for few tokens
         int chunks = static_cast<int>((row_bytes + 16383u) / 16384u);
@@ -551,42 +610,7 @@ cudaError_t launch_dispatch_bf16(DispatchParams p, cudaStream_t stream) {
         if (p.expanded_row) return launch_pdl(dispatch_bf16_regs_kernel<true, 1>, grid, block, 0, stream, p);
         return launch_pdl(dispatch_bf16_regs_kernel<false, 1>, grid, block, 0, stream, p);
     }
-    int chunks = static_cast<int>((row_bytes + EP_DISPATCH_PIECE_MAX - 1) / EP_DISPATCH_PIECE_MAX);
-    const int want_items = 2 * di.num_sms;
-    if (p.T > 0 && static_cast<int64_t>(p.T) * chunks < want_items) {
-        const int more = (want_items + p.T - 1) / p.T;
-        const int max_chunks = static_cast<int>(row_bytes / 1024u) > 0 ? static_cast<int>(row_bytes / 1024u) : 1;
-        chunks = more < max_chunks ? more : max_chunks;
-        if (chunks < 1) chunks = 1;
-    }
-    uint32_t chunk_bytes = (row_bytes + chunks - 1) / chunks;
-    chunk_bytes = (chunk_bytes + 15u) / 16u * 16u;
-    chunks = static_cast<int>((row_bytes + chunk_bytes - 1) / chunk_bytes);
-    p.chunks = chunks;
-    p.chunk_bytes = chunk_bytes;
-    const size_t smem = 128 + static_cast<size_t>(kStages) * chunk_bytes;
-
-    static thread_local int configured_device = -1;
-    static thread_local int blocks_per_sm = 1;
-    static thread_local size_t configured_smem = 0;
-    if (configured_device != di.device || configured_smem != smem) {
-        cudaError_t e = cudaFuncSetAttribute(dispatch_bf16_kernel,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             static_cast<int>(smem));
-        if (e != cudaSuccess) return e;
-        int nb = 0;
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, dispatch_bf16_kernel, kBf16Threads, smem);
-        if (e != cudaSuccess) return e;
-        blocks_per_sm = nb > 0 ? nb : 1;
-        configured_device = di.device;
-        configured_smem = smem;
-    }
-    const int64_t num_items = static_cast<int64_t>(p.T) * chunks;
-    int64_t grid = static_cast<int64_t>(di.num_sms) * blocks_per_sm;
-    if (grid > num_items) grid = num_items;
-    if (grid < 1) return cudaSuccess;
-    return launch_pdl(dispatch_bf16_kernel, dim3(static_cast<unsigned>(grid)), dim3(kBf16Threads), smem, stream,
-                      p);
+    return launch_dispatch_bulk_t<kBulkStages, kBulkStoreDepth>(p, 0, stream);
 }
 
 cudaError_t launch_dispatch_fp8(DispatchParams p, cudaStream_t stream) {
