@@ -61,6 +61,9 @@ def parse_args(argv=None):
     ap.add_argument("--ranks-per-node", type=int, default=0,
                     help="hierarchical path: ranks per node (default: the workload's, else R/2)")
     ap.add_argument("--no-graph", action="store_true", help="launch eagerly instead of CUDA graphs")
+    ap.add_argument("--fp8", action="store_true",
+                    help="FP8 e4m3 dispatch (per-128-channel scales) on any workload; the combine then reads "
+                         "bf16 stand-in expert rows")
     ap.add_argument("--num-sms", default="0",
                     help="SM-limited dispatch and combine (persistent grid of this many CTAs); 0 = whole "
                          "GPU; 'rule' = each phase's count from ep_theoretical_num_sms with the measured "
@@ -290,6 +293,9 @@ def run_ours(args):
     from combine_ep_get_gb300.inputs import CONFIGS, make_config, make_rows
 
     cfg = CONFIGS[args.workload]
+    if args.fp8 and not cfg.fp8:
+        import dataclasses
+        cfg = dataclasses.replace(cfg, fp8=True, description=cfg.description.replace(" bf16", "") + ", FP8 dispatch")
     data = make_config(cfg)
     T, H, E, K, R = cfg.T, cfg.H, cfg.E, cfg.K, cfg.R
     dev = torch.device("cuda", local)

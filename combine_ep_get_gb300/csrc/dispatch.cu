@@ -24,11 +24,13 @@
 //   where it reaches the SM's store limit (~61 GB/s on GB300) that the
 //   register copies miss by ~20%.
 //
-// FP8 path: one CTA per (token, piece of 128-channel blocks); each half-warp
-//   owns one 128-channel block, loads it with 16-byte vectors, takes amax by
-//   shuffles, scales with IEEE divides and converts with cvt.rn.satfinite
-//   e4m3x2, then stores the 8-byte code vectors and the scale to every
-//   destination row.
+// FP8 path: one CTA of 256 threads per (token, piece of up to 64 128-channel
+//   blocks), barrier-free like the bf16 register path: all 16-byte loads of
+//   the piece are issued first and each warp ballots the destination rows
+//   itself; then each quarter-warp owns one block per round (16 channels per
+//   lane), takes amax by shuffles, scales with IEEE divides and converts with
+//   cvt.rn.satfinite e4m3x2, and stores a 16-byte code vector per lane and
+//   the scale to every destination row.
 #include <climits>
 
 #include "ep_internal.cuh"
@@ -410,119 +412,126 @@ __device__ __forceinline__ uint32_t pack_e4m3x4(float a, float b, float c, float
 }
 
 constexpr int kFp8Threads = 256;
+constexpr int kFp8Rounds = 2;                        // 32 blocks per round: up to 64 blocks per item
+constexpr int kFp8BlocksPerRound = kFp8Threads / 8;  // one quarter-warp (8 lanes x 16 channels) per block
 
-// One group of kFp8Threads threads casts one (token, piece) item per
-// iteration; kGroups > 1 (SM-limited mode): several groups per CTA, each
-// looping over items and synchronising on its own named barrier.
-template <bool kExpanded, int kGroups>
-__global__ void __launch_bounds__(kFp8Threads * kGroups) dispatch_fp8_kernel(const DispatchParams p) {
-    __shared__ int s_rows_all[kGroups][EP_MAX_TOPK];
-    __shared__ int s_n_all[kGroups];
-    const int group = kGroups == 1 ? 0 : static_cast<int>(threadIdx.x) / kFp8Threads;
-    const int gtid = kGroups == 1 ? static_cast<int>(threadIdx.x) : static_cast<int>(threadIdx.x) % kFp8Threads;
-    const int warp = gtid >> 5;
-    const int lane = threadIdx.x & 31;
-    int* s_rows = s_rows_all[group];
-    const int64_t n_items = static_cast<int64_t>(p.T) * p.chunks;
-    pdl_wait();
-
-    for (int64_t it = static_cast<int64_t>(blockIdx.x) * kGroups + group; it < n_items;
-         it += static_cast<int64_t>(gridDim.x) * kGroups) {
-        const int t = static_cast<int>(it / p.chunks);
-        const int c = static_cast<int>(it - static_cast<int64_t>(t) * p.chunks);
-        if (kGroups > 1) named_barrier(1 + group, kFp8Threads);   // previous list consumed
-
-        if (warp == 0) {
-            int n = 0;
-            bool cap_bad = false;
-            const int n_dst = kExpanded ? p.K : p.R;
-            const int32_t* drow = kExpanded ? p.expanded_row + static_cast<int64_t>(t) * p.K
-                                            : p.dst_row + static_cast<int64_t>(t) * p.R;
-            for (int rb = 0; rb < n_dst; rb += 32) {
-                const int r = rb + lane;
-                const int d = r < n_dst ? drow[r] : -1;
-                const bool ok = d >= 0 && d < p.capacity;
-                if (d >= p.capacity) cap_bad = true;
-                const unsigned m = __ballot_sync(0xffffffffu, ok);
-                const int pos = n + __popc(m & ((1u << lane) - 1u));
-                // A layout from ep_get_layout has at most K <= 32 ranks per token;
-                // a foreign dst_row with more is cut off and flagged.
-                if (ok && pos < EP_MAX_TOPK) s_rows[pos] = d;
-                n += __popc(m);
-            }
-            if (n > EP_MAX_TOPK) {
-                if (lane == 0) atomicOr(p.status, EP_ERR_INVALID_INDEX);
-                n = EP_MAX_TOPK;
-            }
-            if (lane == 0) s_n_all[group] = n;
-            if (__any_sync(0xffffffffu, cap_bad) && lane == 0 && c == 0) atomicOr(p.status, EP_ERR_CAPACITY);
-        } else if (warp == 1 && c == 0) {
-            if (kExpanded) {
-                write_expanded_metadata(p, t, lane);
-            } else {
-                CtaWork all;
-                all.first = 0;
-                all.count = 0;
-                all.stride = 1;
-                all.lo = INT32_MIN;
-                all.hi = INT32_MAX;
-                all.balanced = 0;
-                write_metadata(p, t, lane, all);
-            }
+// One (token, piece) FP8 item, by one group of 256 threads, barrier-free.
+// Every thread first issues its loads of the piece (16 channels, two 16-byte
+// vectors, of one 128-channel block per round); each warp reads the token's
+// destination rows itself (one lane per rank, ballot) while they are in
+// flight.  Then per round each quarter-warp reduces its block's amax by
+// shuffles, forms the scale and 16 codes per lane, and stores the 16-byte
+// code vector (and, lane 0 of the quarter, the scale) to every destination.
+template <bool kExpanded>
+__device__ __forceinline__ void dispatch_fp8_item(const DispatchParams& p, int64_t it, int gtid, int lane,
+                                                  bool& cap_bad) {
+    const int t = static_cast<int>(it / p.chunks);
+    const int c = static_cast<int>(it - static_cast<int64_t>(t) * p.chunks);
+    const int warp_g = gtid >> 5;
+    const int quarter = lane >> 3;
+    const int sub = lane & 7;
+    const int nb = p.H / 128;
+    const int b_begin = c * p.chunk_blocks;
+    const int b_end = min(nb, b_begin + p.chunk_blocks);
+    const uint8_t* xrow = p.x + static_cast<int64_t>(t) * p.H * 2;
+    uint4 v[kFp8Rounds][2];
+#pragma unroll
+    for (int q = 0; q < kFp8Rounds; ++q) {
+        const int b = b_begin + q * kFp8BlocksPerRound + 4 * warp_g + quarter;
+        const uint8_t* src = xrow + static_cast<size_t>(b) * 256 + sub * 32;
+        v[q][0] = b < b_end ? ld_stream_v4(src) : make_uint4(0, 0, 0, 0);
+        v[q][1] = b < b_end ? ld_stream_v4(src + 16) : make_uint4(0, 0, 0, 0);
+    }
+    const int n_dst = kExpanded ? p.K : p.R;
+    const int32_t* drow = kExpanded ? p.expanded_row + static_cast<int64_t>(t) * p.K
+                                    : p.dst_row + static_cast<int64_t>(t) * p.R;
+    const int d0 = lane < n_dst ? drow[lane] : -1;
+    const int d1 = 32 + lane < n_dst ? drow[32 + lane] : -1;   // ranks 32..63, same latency
+    if (warp_g == 1 && c == 0) {
+        if (kExpanded) {
+            write_expanded_metadata(p, t, lane);
+        } else {
+            CtaWork all;
+            all.first = 0;
+            all.count = 0;
+            all.stride = 1;
+            all.lo = INT32_MIN;
+            all.hi = INT32_MAX;
+            all.balanced = 0;
+            write_metadata(p, t, lane, all);
         }
-        if (kGroups > 1)
-            named_barrier(1 + group, kFp8Threads);
-        else
-            __syncthreads();
-
-        const int n = s_n_all[group];
-        const int nb = p.H / 128;
-        const int b_begin = c * p.chunk_blocks;
-        const int b_end = min(nb, b_begin + p.chunk_blocks);
-        const int half = lane >> 4;
-        const int sub = lane & 15;
-        const uint8_t* xrow = p.x + static_cast<int64_t>(t) * p.H * 2;
-        for (int b0 = b_begin + 2 * warp; b0 < b_end; b0 += 2 * (kFp8Threads / 32)) {
-            const int b = b0 + half;
-            const bool valid = b < b_end;
-            uint4 v = make_uint4(0, 0, 0, 0);
-            if (valid) v = ld_stream_v4(xrow + static_cast<size_t>(b) * 256 + sub * 16);
-            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-            float f[8];
+    }
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                f[2 * q] = __uint_as_float(w[q] << 16);
-                f[2 * q + 1] = __uint_as_float(w[q] & 0xffff0000u);
-            }
-            float amax = 0.0f;
+    for (int q = 0; q < kFp8Rounds; ++q) {
+        const int b = b_begin + q * kFp8BlocksPerRound + 4 * warp_g + quarter;
+        if (b_begin + q * kFp8BlocksPerRound + 4 * warp_g >= b_end) break;   // the warp has no block left
+        const bool valid = b < b_end;
+        const uint32_t w[8] = {v[q][0].x, v[q][0].y, v[q][0].z, v[q][0].w,
+                               v[q][1].x, v[q][1].y, v[q][1].z, v[q][1].w};
+        float f[16];
 #pragma unroll
-            for (int q = 0; q < 8; ++q) amax = fmaxf(amax, fabsf(f[q]));
+        for (int e = 0; e < 8; ++e) {
+            f[2 * e] = __uint_as_float(w[e] << 16);
+            f[2 * e + 1] = __uint_as_float(w[e] & 0xffff0000u);
+        }
+        float amax = 0.0f;
 #pragma unroll
-            for (int o = 8; o >= 1; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-            float sf = 1.0f, mult = 0.0f;
-            if (amax > 0.0f) {
-                sf = __fdiv_rn(amax, 448.0f);
-                mult = __fdiv_rn(448.0f, amax);
-            }
-            float g[8];
+        for (int e = 0; e < 16; ++e) amax = fmaxf(amax, fabsf(f[e]));
 #pragma unroll
-            for (int q = 0; q < 8; ++q) g[q] = __fmul_rn(f[q], mult);
-            uint2 code;
-            code.x = pack_e4m3x4(g[0], g[1], g[2], g[3]);
-            code.y = pack_e4m3x4(g[4], g[5], g[6], g[7]);
-            if (valid) {
-                for (int m = 0; m < n; ++m) {
-                    const int64_t d = s_rows[m];
-                    *reinterpret_cast<uint2*>(p.recv_x + d * p.H + static_cast<int64_t>(b) * 128 + sub * 8) = code;
+        for (int o = 4; o >= 1; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+        float sf = 1.0f, mult = 0.0f;
+        if (amax > 0.0f) {
+            sf = __fdiv_rn(amax, 448.0f);
+            mult = __fdiv_rn(448.0f, amax);
+        }
+        uint4 code;
+        code.x = pack_e4m3x4(__fmul_rn(f[0], mult), __fmul_rn(f[1], mult), __fmul_rn(f[2], mult),
+                             __fmul_rn(f[3], mult));
+        code.y = pack_e4m3x4(__fmul_rn(f[4], mult), __fmul_rn(f[5], mult), __fmul_rn(f[6], mult),
+                             __fmul_rn(f[7], mult));
+        code.z = pack_e4m3x4(__fmul_rn(f[8], mult), __fmul_rn(f[9], mult), __fmul_rn(f[10], mult),
+                             __fmul_rn(f[11], mult));
+        code.w = pack_e4m3x4(__fmul_rn(f[12], mult), __fmul_rn(f[13], mult), __fmul_rn(f[14], mult),
+                             __fmul_rn(f[15], mult));
+        const int64_t col = static_cast<int64_t>(b) * 128 + sub * 16;
+        for (int rb = 0; rb < n_dst; rb += 32) {
+            const int d = rb == 0 ? d0 : rb == 32 ? d1 : (rb + lane < n_dst ? drow[rb + lane] : -1);
+            if (d >= p.capacity && c == 0 && q == 0) cap_bad = true;
+            unsigned m = __ballot_sync(0xffffffffu, d >= 0 && d < p.capacity);
+            while (m) {
+                const int sl = __ffs(m) - 1;
+                m &= m - 1;
+                const int64_t dd = __shfl_sync(0xffffffffu, d, sl);
+                if (valid) {
+                    st_v4(p.recv_x + dd * p.H + col, code);
                     if (sub == 0 && p.recv_sf) {
-                        const int64_t si = p.sf_col_major ? static_cast<int64_t>(b) * p.sf_stride + d
-                                                          : d * nb + b;
+                        const int64_t si = p.sf_col_major ? static_cast<int64_t>(b) * p.sf_stride + dd : dd * nb + b;
                         p.recv_sf[si] = sf;
                     }
                 }
             }
         }
     }
+}
+
+// kGroups == 1: one CTA per item.  kGroups > 1 (SM-limited mode): several
+// independent groups per CTA, each looping over items with a stride.
+template <bool kExpanded, int kGroups>
+__global__ void __launch_bounds__(kFp8Threads * kGroups, kGroups == 1 ? 4 : 1) dispatch_fp8_kernel(const DispatchParams p) {
+    const int gtid = static_cast<int>(threadIdx.x) % kFp8Threads;
+    const int lane = threadIdx.x & 31;
+    bool cap_bad = false;
+    pdl_wait();   // before any global access: the previous kernel may write x
+    if (kGroups == 1) {
+        dispatch_fp8_item<kExpanded>(p, blockIdx.x, gtid, lane, cap_bad);
+    } else {
+        const int64_t n_items = static_cast<int64_t>(p.T) * p.chunks;
+        const int group = static_cast<int>(threadIdx.x) / kFp8Threads;
+        for (int64_t it = static_cast<int64_t>(blockIdx.x) * kGroups + group; it < n_items;
+             it += static_cast<int64_t>(gridDim.x) * kGroups)
+            dispatch_fp8_item<kExpanded>(p, it, gtid, lane, cap_bad);
+    }
+    if ((gtid >> 5) == 0 && __any_sync(0xffffffffu, cap_bad) && lane == 0) atomicOr(p.status, EP_ERR_CAPACITY);
 }
 
 // Bulk-copy path: the default alternative (EP_DISPATCH_IMPL=0) and the
@@ -616,13 +625,13 @@ cudaError_t launch_dispatch_bf16(DispatchParams p, cudaStream_t stream) {
 cudaError_t launch_dispatch_fp8(DispatchParams p, cudaStream_t stream) {
     const DeviceInfo& di = device_info();
     const int nb = p.H / 128;
-    // One CTA per (token, piece); pieces of up to 16 blocks (2048 channels),
+    // One CTA per (token, piece); pieces of up to 64 blocks (8192 channels),
     // split further when there are few tokens.
-    int chunks = (nb + 15) / 16;
+    int chunks = (nb + kFp8Rounds * kFp8BlocksPerRound - 1) / (kFp8Rounds * kFp8BlocksPerRound);
     const int want_items = 4 * di.num_sms;
     if (p.T > 0 && static_cast<int64_t>(p.T) * chunks < want_items) {
         const int more = (want_items + p.T - 1) / p.T;
-        const int max_chunks = (nb + 1) / 2;  // keep >= 2 blocks (one warp) per piece
+        const int max_chunks = (nb + 3) / 4;  // keep >= 4 blocks (one warp) per piece
         chunks = more < max_chunks ? more : max_chunks;
         if (chunks < 1) chunks = 1;
     }
