@@ -60,6 +60,12 @@ namespace {
 #ifndef EP_DISPATCH_STORE_CS
 #define EP_DISPATCH_STORE_CS 0        // register path: streaming (.cs) stores
 #endif
+#ifndef EP_DISPATCH_FP8_MIN_BLOCKS
+#define EP_DISPATCH_FP8_MIN_BLOCKS 4      // FP8 path: __launch_bounds__ minimum resident CTAs per SM
+#endif
+#ifndef EP_DISPATCH_FP8_PIECE_BLOCKS
+#define EP_DISPATCH_FP8_PIECE_BLOCKS 64   // FP8 path: 128-channel blocks per piece (<= 64)
+#endif
 
 constexpr int kBf16Threads = 128;
 constexpr int kBulkStages = EP_DISPATCH_STAGES;
@@ -517,7 +523,8 @@ __device__ __forceinline__ void dispatch_fp8_item(const DispatchParams& p, int64
 // kGroups == 1: one CTA per item.  kGroups > 1 (SM-limited mode): several
 // independent groups per CTA, each looping over items with a stride.
 template <bool kExpanded, int kGroups>
-__global__ void __launch_bounds__(kFp8Threads * kGroups, kGroups == 1 ? 4 : 1) dispatch_fp8_kernel(const DispatchParams p) {
+__global__ void __launch_bounds__(kFp8Threads * kGroups, kGroups == 1 ? EP_DISPATCH_FP8_MIN_BLOCKS : 1)
+    dispatch_fp8_kernel(const DispatchParams p) {
     const int gtid = static_cast<int>(threadIdx.x) % kFp8Threads;
     const int lane = threadIdx.x & 31;
     bool cap_bad = false;
@@ -627,7 +634,7 @@ cudaError_t launch_dispatch_fp8(DispatchParams p, cudaStream_t stream) {
     const int nb = p.H / 128;
     // One CTA per (token, piece); pieces of up to 64 blocks (8192 channels),
     // split further when there are few tokens.
-    int chunks = (nb + kFp8Rounds * kFp8BlocksPerRound - 1) / (kFp8Rounds * kFp8BlocksPerRound);
+    int chunks = (nb + EP_DISPATCH_FP8_PIECE_BLOCKS - 1) / EP_DISPATCH_FP8_PIECE_BLOCKS;
     const int want_items = 4 * di.num_sms;
     if (p.T > 0 && static_cast<int64_t>(p.T) * chunks < want_items) {
         const int more = (want_items + p.T - 1) / p.T;
