@@ -39,6 +39,7 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kUnroll = 4;
+constexpr int kStageUnroll = 8;   // global loads in flight per thread when staging into shared memory
 
 // Sum of v over the block (blockDim a multiple of 32, at most 1024); s_red
 // holds 33 ints.  Every thread gets the total.
@@ -197,35 +198,82 @@ __device__ void block_exclusive_scan(int n, Get get, Put put, int* s_warp) {
     __syncthreads();
 }
 
+// Per-thread register slices for the rows kernel's scans: thread tid holds
+// elements tid * per + j (j < per, per = ceil(n / kThreads)) of an n-vector.
+constexpr int kMaxRankSlice = (EP_MAX_RANKS + kThreads - 1) / kThreads;
+constexpr int kMaxExpertSlice = (EP_MAX_EXPERTS + kThreads - 1) / kThreads;
+
+// v[j] = enable ? get(tid * per + j) : 0 for the thread's slice, all loads
+// issued before any use.
+template <int kMax, class Get>
+__device__ __forceinline__ void load_slice(int (&v)[kMax], int n, int per, bool enable, Get get) {
+#pragma unroll
+    for (int j = 0; j < kMax; ++j) {
+        const int i = static_cast<int>(threadIdx.x) * per + j;
+        v[j] = (enable && j < per && i < n) ? get(i) : 0;
+    }
+}
+
+// Exclusive scan of an n-vector held in register slices (see load_slice):
+// out[j] = sum of the elements before element tid * per + j.  Returns the
+// total.  Called by all kThreads threads; s_warp holds 8 ints.
+template <int kMax>
+__device__ int block_exclusive_scan_slice(const int (&v)[kMax], int (&out)[kMax], int per, int* s_warp) {
+    const int tid = threadIdx.x;
+    int local = 0;
+#pragma unroll
+    for (int j = 0; j < kMax; ++j) local += j < per ? v[j] : 0;
+    const int incl = warp_inclusive_scan(local);
+    const int lane = tid & 31, warp = tid >> 5;
+    if (lane == 31) s_warp[warp] = incl;
+    __syncthreads();
+    int before = 0, total = 0;
+#pragma unroll
+    for (int w = 0; w < kThreads / 32; ++w) {
+        const int x = s_warp[w];
+        if (w < warp) before += x;
+        total += x;
+    }
+    int run = before + incl - local;
+#pragma unroll
+    for (int j = 0; j < kMax; ++j) {
+        out[j] = run;
+        run += j < per ? v[j] : 0;
+    }
+    __syncthreads();
+    return total;
+}
+
 // Expanded (per-expert) rows of one tile's (token, k) entries: expert e's
 // entries take rows expert_offset[e] + (entries of e in earlier tiles) + their
 // stable rank in the tile, in (token, k) order.  The tile's entries are staged
 // in shared memory; each warp ranks a contiguous slice of them twice with
 // __match_any_sync (count, then place) around a per-(warp, expert) prefix, so
-// the order never depends on timing.  Needs 256 K + E + 8 E shared ints.
-__device__ void expanded_rows_of_tile(const LayoutParams& p, int tile, int t0, int nt, int* sm, int* s_warp) {
+// the order never depends on timing.  s_eb holds each expert's base row
+// for this tile; needs 256 K + 8 E shared ints.
+__device__ void expanded_rows_of_tile(const LayoutParams& p, int t0, int nt, const int* s_eb, int* sm,
+                                      const int64_t (&key0)[kStageUnroll]) {
     constexpr int kWarps = kThreads / 32;
     const int E = p.E;
     const int n_ent = nt * p.K;
-    int* s_key = sm;                      // [256 K] expert of each entry, or a unique negative
-    int* s_eb = s_key + kTileTokens * p.K;  // [E] base row of each expert for this tile
-    int* s_wc = s_eb + E;                 // [kWarps][E] per-warp counts, then per-warp bases
+    int* s_key = sm;                        // [256 K] expert of each entry, or a unique negative
+    int* s_wc = s_key + kTileTokens * p.K;  // [kWarps][E] per-warp counts, then per-warp bases
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int64_t* src = p.topk_idx + static_cast<int64_t>(t0) * p.K;
-    for (int i = threadIdx.x; i < n_ent; i += kThreads) {
-        const int64_t e = src[i];
-        s_key[i] = (e >= 0 && e < E) ? static_cast<int>(e) : -1 - (i & 31);
+    for (int base = 0; base < n_ent; base += kStageUnroll * kThreads) {
+        int64_t e[kStageUnroll];
+#pragma unroll
+        for (int u = 0; u < kStageUnroll; ++u) {   // the first batch was loaded at kernel entry
+            const int i = base + u * kThreads + threadIdx.x;
+            e[u] = base == 0 ? key0[u] : (i < n_ent ? src[i] : -1);
+        }
+#pragma unroll
+        for (int u = 0; u < kStageUnroll; ++u) {
+            const int i = base + u * kThreads + threadIdx.x;
+            if (i < n_ent) s_key[i] = (e[u] >= 0 && e[u] < E) ? static_cast<int>(e[u]) : -1 - (i & 31);
+        }
     }
     for (int i = threadIdx.x; i < kWarps * E; i += kThreads) s_wc[i] = 0;
-    const int a = p.alignment;
-    const int32_t* ce = p.num_tokens_per_expert;
-    block_exclusive_scan(
-        E, [&](int i) { return (ce[i] + a - 1) / a * a; },
-        [&](int i, int v) {
-            if (i < E) s_eb[i] = v;
-        },
-        s_warp);
-    for (int e = threadIdx.x; e < E; e += kThreads) s_eb[e] += p.ws_expert[static_cast<size_t>(e) * p.num_tiles + tile];
     __syncthreads();
     // each warp owns entries [w0, w1), whole 32-entry chunks
     const int chunks = (n_ent + 31) / 32;
@@ -264,18 +312,14 @@ __device__ void expanded_rows_of_tile(const LayoutParams& p, int tile, int t0, i
 
 // Node rows of one tile: a token is in node n when any rank of n holds it,
 // so node n's membership word is the OR of its ranks' words; node n's rows
-// are node_offset[n] + (its tokens in earlier tiles) + popc below the token.
-// Needs (num_nodes + 1) + 2 * kTileWords * num_nodes shared ints; ends with a
-// block barrier so the caller may reuse them.
-__device__ void node_rows_of_tile(const LayoutParams& p, int tile, int t0, int nt, const uint32_t* s_bm, int* sm,
-                                  int* s_warp) {
+// are s_nbase[n] (node_offset[n] + its tokens in earlier tiles) + popc below
+// the token.  Needs 2 * kTileWords * num_nodes shared ints; ends with a block
+// barrier so the caller may reuse them.
+__device__ void node_rows_of_tile(const LayoutParams& p, int t0, int nt, const uint32_t* s_bm, const int* s_nbase,
+                                  int* sm) {
     const int NN = p.num_nodes, R = p.R, rpn = p.ranks_per_node;
-    int* s_nbase = sm;                                                 // [NN + 1]
-    uint32_t* s_nbm = reinterpret_cast<uint32_t*>(s_nbase + NN + 1);   // [kTileWords][NN]
+    uint32_t* s_nbm = reinterpret_cast<uint32_t*>(sm);                // [kTileWords][NN]
     int* s_nwpre = reinterpret_cast<int*>(s_nbm + NN * kTileWords);    // [kTileWords][NN]
-    const int32_t* cn = p.num_tokens_per_node;
-    block_exclusive_scan(NN, [&](int i) { return cn[i]; }, [&](int i, int v) { s_nbase[i] = v; }, s_warp);
-    for (int n = threadIdx.x; n < NN; n += kThreads) s_nbase[n] += p.ws_node[static_cast<size_t>(n) * p.num_tiles + tile];
     for (int i = threadIdx.x; i < NN * kTileWords; i += kThreads) {
         const int w = i / NN;
         const int n = i - w * NN;
@@ -308,42 +352,121 @@ __device__ void node_rows_of_tile(const LayoutParams& p, int tile, int t0, int n
 __global__ void __launch_bounds__(kThreads) layout_rows_kernel(const LayoutParams p) {
     extern __shared__ __align__(16) uint32_t smem[];
     __shared__ int s_warp[kThreads / 32];
-    const int R = p.R;
-    int* s_base = reinterpret_cast<int*>(smem);                 // [R+1]
-    uint32_t* s_bm = smem + (R + 1);                             // [kTileWords][R]
-    int* s_wpre = reinterpret_cast<int*>(s_bm + R * kTileWords);  // [kTileWords][R]
+    const int R = p.R, E = p.E, NN = p.num_nodes;
     const int tile = blockIdx.x;
+    const bool has_tile = tile < p.num_tiles;
+    const bool expanded = p.expanded_row != nullptr && has_tile;
+    const bool nodes = p.node_row != nullptr;
+    int* s_base = reinterpret_cast<int*>(smem);                    // [R+1]
+    uint32_t* s_bm = smem + (R + 1);                                // [kTileWords][R]
+    int* s_wpre = reinterpret_cast<int*>(s_bm + R * kTileWords);    // [kTileWords][R]
+    int* s_eb = s_wpre + R * kTileWords;                            // [E] expanded: expert bases
+    int* s_nbase = s_eb + (p.expanded_row ? E : 0);                 // [NN] node bases
+    int* s_extra = s_nbase + (nodes ? NN : 0);                      // node rows, then expanded rows
     pdl_wait();
     pdl_launch_dependents();   // the next kernel may be scheduled; it waits for our completion
 
-    const int32_t* cnt = p.num_tokens_per_rank;
-    block_exclusive_scan(R, [&](int i) { return cnt[i]; }, [&](int i, int v) { s_base[i] = v; },
-                         s_warp);
-    if (tile == 0) {
-        for (int i = threadIdx.x; i <= R; i += kThreads) p.rank_offset[i] = s_base[i];
-        const int a = p.alignment;
-        const int32_t* ce = p.num_tokens_per_expert;
-        int32_t* eo = p.expert_offset;
-        block_exclusive_scan(
-            p.E, [&](int i) { return (ce[i] + a - 1) / a * a; }, [&](int i, int v) { eo[i] = v; },
-            s_warp);
-        if (p.node_row) {
-            const int32_t* cn = p.num_tokens_per_node;
-            int32_t* no = p.node_offset;
-            block_exclusive_scan(p.num_nodes, [&](int i) { return cn[i]; }, [&](int i, int v) { no[i] = v; },
-                                 s_warp);
+    // Every independent global value this CTA needs, loaded at once (one
+    // round trip): rank totals and this tile's rank prefixes, expert totals
+    // (block 0: expert_offset; expanded: the ranking's bases) and this tile's
+    // expert prefixes, node totals and prefixes, the tile's first top-k
+    // entries, then its membership bitmaps.
+    const int per_r = (R + kThreads - 1) / kThreads;
+    const int per_e = (E + kThreads - 1) / kThreads;
+    const int per_n = (NN + kThreads - 1) / kThreads;
+    const bool want_e = tile == 0 || expanded;
+    const bool want_n = nodes && (tile == 0 || has_tile);
+    int v_cnt[kMaxRankSlice], v_wsr[kMaxRankSlice];
+    int v_ce[kMaxExpertSlice], v_wse[kMaxExpertSlice];
+    int v_cn[kMaxRankSlice], v_wsn[kMaxRankSlice];
+    load_slice(v_cnt, R, per_r, true, [&](int i) { return p.num_tokens_per_rank[i]; });
+    load_slice(v_wsr, R, per_r, has_tile, [&](int i) { return p.ws_rank[static_cast<size_t>(i) * p.num_tiles + tile]; });
+    load_slice(v_ce, E, per_e, want_e, [&](int i) { return p.num_tokens_per_expert[i]; });
+    load_slice(v_wse, E, per_e, expanded,
+               [&](int i) { return p.ws_expert[static_cast<size_t>(i) * p.num_tiles + tile]; });
+    load_slice(v_cn, NN, per_n, want_n, [&](int i) { return p.num_tokens_per_node[i]; });
+    load_slice(v_wsn, NN, per_n, nodes && has_tile,
+               [&](int i) { return p.ws_node[static_cast<size_t>(i) * p.num_tiles + tile]; });
+    const int t0 = tile * kTileTokens;
+    const int nt = has_tile ? min(kTileTokens, p.T - t0) : 0;
+    int64_t key0[kStageUnroll];
+    {
+        const int n_ent = nt * p.K;
+        const int64_t* src = p.topk_idx + static_cast<int64_t>(t0) * p.K;
+#pragma unroll
+        for (int u = 0; u < kStageUnroll; ++u) {
+            const int i = u * kThreads + static_cast<int>(threadIdx.x);
+            key0[u] = (expanded && i < n_ent) ? src[i] : -1;
         }
     }
-    if (tile >= p.num_tiles) {
+    if (has_tile) {
+        const uint32_t* g_bm = p.ws_bitmap + static_cast<size_t>(tile) * R * kTileWords;
+        for (int base = 0; base < R * kTileWords; base += kStageUnroll * kThreads) {
+            uint32_t v[kStageUnroll];
+#pragma unroll
+            for (int u = 0; u < kStageUnroll; ++u) {   // all loads in flight before any use
+                const int i = base + u * kThreads + threadIdx.x;
+                v[u] = i < R * kTileWords ? g_bm[i] : 0u;
+            }
+#pragma unroll
+            for (int u = 0; u < kStageUnroll; ++u) {
+                const int i = base + u * kThreads + threadIdx.x;
+                if (i < R * kTileWords) s_bm[i] = v[u];
+            }
+        }
+    }
+
+    // rank offsets, then this tile's base per rank
+    {
+        int pre[kMaxRankSlice];
+        const int n_recv = block_exclusive_scan_slice(v_cnt, pre, per_r, s_warp);
+#pragma unroll
+        for (int j = 0; j < kMaxRankSlice; ++j) {
+            const int i = static_cast<int>(threadIdx.x) * per_r + j;
+            if (j < per_r && i < R) {
+                if (tile == 0) p.rank_offset[i] = pre[j];
+                s_base[i] = pre[j] + v_wsr[j];
+            }
+        }
+        if (tile == 0 && threadIdx.x == 0) p.rank_offset[R] = n_recv;
+    }
+    // expert offsets (aligned counts): block 0 writes them; the expanded
+    // ranking starts each expert at its offset plus this tile's prefix
+    if (want_e) {
+        const int a = p.alignment;
+        int al[kMaxExpertSlice], pre[kMaxExpertSlice];
+#pragma unroll
+        for (int j = 0; j < kMaxExpertSlice; ++j) al[j] = (v_ce[j] + a - 1) / a * a;
+        const int n_exp = block_exclusive_scan_slice(al, pre, per_e, s_warp);
+#pragma unroll
+        for (int j = 0; j < kMaxExpertSlice; ++j) {
+            const int i = static_cast<int>(threadIdx.x) * per_e + j;
+            if (j < per_e && i < E) {
+                if (tile == 0) p.expert_offset[i] = pre[j];
+                if (expanded) s_eb[i] = pre[j] + v_wse[j];
+            }
+        }
+        if (tile == 0 && threadIdx.x == 0) p.expert_offset[E] = n_exp;
+    }
+    // node offsets and this tile's base per node
+    if (want_n) {
+        int pre[kMaxRankSlice];
+        const int n_node = block_exclusive_scan_slice(v_cn, pre, per_n, s_warp);
+#pragma unroll
+        for (int j = 0; j < kMaxRankSlice; ++j) {
+            const int i = static_cast<int>(threadIdx.x) * per_n + j;
+            if (j < per_n && i < NN) {
+                if (tile == 0) p.node_offset[i] = pre[j];
+                s_nbase[i] = pre[j] + v_wsn[j];
+            }
+        }
+        if (tile == 0 && threadIdx.x == 0) p.node_offset[NN] = n_node;
+    }
+    if (!has_tile) {
         if (p.token_offset && p.num_tiles == 0 && threadIdx.x == 0) p.token_offset[0] = 0;
         return;
     }
-
-    for (int r = threadIdx.x; r < R; r += kThreads)
-        s_base[r] += p.ws_rank[static_cast<size_t>(r) * p.num_tiles + tile];
-    const uint32_t* g_bm = p.ws_bitmap + static_cast<size_t>(tile) * R * kTileWords;
-    for (int i = threadIdx.x; i < R * kTileWords; i += kThreads) s_bm[i] = g_bm[i];
-    __syncthreads();
+    __syncthreads();   // s_base, s_bm (and the bases) visible
     for (int r = threadIdx.x; r < R; r += kThreads) {
         int run = 0;
 #pragma unroll
@@ -354,20 +477,43 @@ __global__ void __launch_bounds__(kThreads) layout_rows_kernel(const LayoutParam
     }
     __syncthreads();
 
-    const int t0 = tile * kTileTokens;
-    const int nt = min(kTileTokens, p.T - t0);
+    // dst_row and is_token_in_rank of the tile's contiguous [nt, R] block,
+    // four entries per thread-step (16-byte / 4-byte stores)
     const int n_el = nt * R;
     int32_t* drow = p.dst_row + static_cast<size_t>(t0) * R;
     uint8_t* inr = p.is_token_in_rank + static_cast<size_t>(t0) * R;
-    for (int j = threadIdx.x; j < n_el; j += kThreads) {
-        const int tl = j / R;
-        const int r = j - tl * R;
-        const int w = tl >> 5;
-        const uint32_t word = s_bm[w * R + r];
-        const uint32_t b = static_cast<uint32_t>(tl & 31);
-        const bool in = (word >> b) & 1u;
-        drow[j] = in ? s_base[r] + s_wpre[w * R + r] + __popc(word & ((1u << b) - 1u)) : -1;
-        inr[j] = in ? 1 : 0;
+    for (int q = threadIdx.x; q * 4 < n_el; q += kThreads) {
+        const int j0 = q * 4;
+        int tl = j0 / R;
+        int r = j0 - tl * R;
+        int v[4];
+        uint32_t in4 = 0;
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            v[u] = -1;
+            if (j0 + u < n_el) {
+                const int w = tl >> 5;
+                const uint32_t word = s_bm[w * R + r];
+                const uint32_t b = static_cast<uint32_t>(tl & 31);
+                if ((word >> b) & 1u) {
+                    v[u] = s_base[r] + s_wpre[w * R + r] + __popc(word & ((1u << b) - 1u));
+                    in4 |= 1u << (8 * u);
+                }
+            }
+            if (++r == R) {
+                r = 0;
+                ++tl;
+            }
+        }
+        if (j0 + 4 <= n_el) {
+            *reinterpret_cast<int4*>(drow + j0) = make_int4(v[0], v[1], v[2], v[3]);
+            *reinterpret_cast<uint32_t*>(inr + j0) = in4;
+        } else {
+            for (int u = 0; u < 4 && j0 + u < n_el; ++u) {
+                drow[j0 + u] = v[u];
+                inr[j0 + u] = static_cast<uint8_t>((in4 >> (8 * u)) & 1u);
+            }
+        }
     }
 
     // token_offset: rows numbered token by token.  The rows of tokens before
@@ -420,8 +566,8 @@ __global__ void __launch_bounds__(kThreads) layout_rows_kernel(const LayoutParam
         }
     }
 
-    if (p.node_row) node_rows_of_tile(p, tile, t0, nt, s_bm, reinterpret_cast<int*>(s_wpre + R * kTileWords), s_warp);
-    if (p.expanded_row) expanded_rows_of_tile(p, tile, t0, nt, s_wpre + R * kTileWords, s_warp);
+    if (nodes) node_rows_of_tile(p, t0, nt, s_bm, s_nbase, s_extra);
+    if (expanded) expanded_rows_of_tile(p, t0, nt, s_eb, s_extra, key0);
 }
 
 // ---------------------------------------------------------------------------
@@ -853,11 +999,13 @@ cudaError_t launch_layout(const LayoutParams& p, cudaStream_t stream) {
     const size_t smem_count =
         4 * (static_cast<size_t>(p.R) * kTileWords + static_cast<size_t>(p.num_nodes) * kTileWords + p.E);
     size_t smem_rows = 4 * (static_cast<size_t>(p.R) + 1 + 2 * static_cast<size_t>(p.R) * kTileWords);
-    // node rows, then expanded rows, reuse the same region after the rank arrays
+    if (p.expanded_row) smem_rows += 4 * static_cast<size_t>(p.E);       // expert bases
+    if (p.node_row) smem_rows += 4 * static_cast<size_t>(p.num_nodes);   // node bases
+    // node rows, then expanded rows, reuse the same region after those
     size_t extra = 0;
-    if (p.node_row) extra = 4 * (static_cast<size_t>(p.num_nodes) + 1 + 2 * static_cast<size_t>(kTileWords) * p.num_nodes);
+    if (p.node_row) extra = 4 * (2 * static_cast<size_t>(kTileWords) * p.num_nodes);
     if (p.expanded_row) {
-        const size_t ex = 4 * (static_cast<size_t>(kTileTokens) * p.K + 9 * static_cast<size_t>(p.E));
+        const size_t ex = 4 * (static_cast<size_t>(kTileTokens) * p.K + 8 * static_cast<size_t>(p.E));
         if (ex > extra) extra = ex;
     }
     smem_rows += extra;
