@@ -418,35 +418,40 @@ __device__ __forceinline__ uint32_t pack_e4m3x4(float a, float b, float c, float
 }
 
 constexpr int kFp8Threads = 256;
-constexpr int kFp8Rounds = 2;                        // 32 blocks per round: up to 64 blocks per item
-constexpr int kFp8BlocksPerRound = kFp8Threads / 8;  // one quarter-warp (8 lanes x 16 channels) per block
+constexpr int kFp8Rounds = 2;   // rounds of blocks per item (loads of every round issued first)
 
 // One (token, piece) FP8 item, by one group of 256 threads, barrier-free.
-// Every thread first issues its loads of the piece (16 channels, two 16-byte
-// vectors, of one 128-channel block per round); each warp reads the token's
-// destination rows itself (one lane per rank, ballot) while they are in
-// flight.  Then per round each quarter-warp reduces its block's amax by
-// shuffles, forms the scale and 16 codes per lane, and stores the 16-byte
-// code vector (and, lane 0 of the quarter, the scale) to every destination.
-template <bool kExpanded>
+// kLanes lanes share one 128-channel block (each lane 128 / kLanes channels):
+// 8 (two 16-byte loads and a 16-byte code store per lane, fewer instructions
+// per byte: many tokens) or 16 (one load, an 8-byte store, half the work per
+// lane on the dependent path: few tokens).  Every thread first issues its
+// loads of the piece; each warp reads the token's destination rows itself
+// (one lane per rank, ballot) while they are in flight.  Then per round each
+// group of kLanes lanes reduces its block's amax by shuffles, forms the scale
+// and the codes, and stores the code vector (and, its first lane, the scale)
+// to every destination.
+template <bool kExpanded, int kLanes>
 __device__ __forceinline__ void dispatch_fp8_item(const DispatchParams& p, int64_t it, int gtid, int lane,
                                                   bool& cap_bad) {
+    constexpr int kVec = 128 / kLanes / 8;                     // 16-byte input vectors per lane per block
+    constexpr int kBlocksPerWarp = 32 / kLanes;
+    constexpr int kBlocksPerRound = kBlocksPerWarp * (kFp8Threads / 32);
     const int t = static_cast<int>(it / p.chunks);
     const int c = static_cast<int>(it - static_cast<int64_t>(t) * p.chunks);
     const int warp_g = gtid >> 5;
-    const int quarter = lane >> 3;
-    const int sub = lane & 7;
+    const int grp = lane / kLanes;
+    const int sub = lane % kLanes;
     const int nb = p.H / 128;
     const int b_begin = c * p.chunk_blocks;
     const int b_end = min(nb, b_begin + p.chunk_blocks);
     const uint8_t* xrow = p.x + static_cast<int64_t>(t) * p.H * 2;
-    uint4 v[kFp8Rounds][2];
+    uint4 v[kFp8Rounds][kVec];
 #pragma unroll
     for (int q = 0; q < kFp8Rounds; ++q) {
-        const int b = b_begin + q * kFp8BlocksPerRound + 4 * warp_g + quarter;
-        const uint8_t* src = xrow + static_cast<size_t>(b) * 256 + sub * 32;
-        v[q][0] = b < b_end ? ld_stream_v4(src) : make_uint4(0, 0, 0, 0);
-        v[q][1] = b < b_end ? ld_stream_v4(src + 16) : make_uint4(0, 0, 0, 0);
+        const int b = b_begin + q * kBlocksPerRound + kBlocksPerWarp * warp_g + grp;
+        const uint8_t* src = xrow + static_cast<size_t>(b) * 256 + sub * (16 * kVec);
+#pragma unroll
+        for (int u = 0; u < kVec; ++u) v[q][u] = b < b_end ? ld_stream_v4(src + 16 * u) : make_uint4(0, 0, 0, 0);
     }
     const int n_dst = kExpanded ? p.K : p.R;
     const int32_t* drow = kExpanded ? p.expanded_row + static_cast<int64_t>(t) * p.K
@@ -469,37 +474,35 @@ __device__ __forceinline__ void dispatch_fp8_item(const DispatchParams& p, int64
     }
 #pragma unroll
     for (int q = 0; q < kFp8Rounds; ++q) {
-        const int b = b_begin + q * kFp8BlocksPerRound + 4 * warp_g + quarter;
-        if (b_begin + q * kFp8BlocksPerRound + 4 * warp_g >= b_end) break;   // the warp has no block left
+        const int b = b_begin + q * kBlocksPerRound + kBlocksPerWarp * warp_g + grp;
+        if (b_begin + q * kBlocksPerRound + kBlocksPerWarp * warp_g >= b_end) break;   // the warp has no block left
         const bool valid = b < b_end;
-        const uint32_t w[8] = {v[q][0].x, v[q][0].y, v[q][0].z, v[q][0].w,
-                               v[q][1].x, v[q][1].y, v[q][1].z, v[q][1].w};
-        float f[16];
+        float f[8 * kVec];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-            f[2 * e] = __uint_as_float(w[e] << 16);
-            f[2 * e + 1] = __uint_as_float(w[e] & 0xffff0000u);
+        for (int u = 0; u < kVec; ++u) {
+            const uint32_t w[4] = {v[q][u].x, v[q][u].y, v[q][u].z, v[q][u].w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                f[8 * u + 2 * e] = __uint_as_float(w[e] << 16);
+                f[8 * u + 2 * e + 1] = __uint_as_float(w[e] & 0xffff0000u);
+            }
         }
         float amax = 0.0f;
 #pragma unroll
-        for (int e = 0; e < 16; ++e) amax = fmaxf(amax, fabsf(f[e]));
+        for (int e = 0; e < 8 * kVec; ++e) amax = fmaxf(amax, fabsf(f[e]));
 #pragma unroll
-        for (int o = 4; o >= 1; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+        for (int o = kLanes / 2; o >= 1; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
         float sf = 1.0f, mult = 0.0f;
         if (amax > 0.0f) {
             sf = __fdiv_rn(amax, 448.0f);
             mult = __fdiv_rn(448.0f, amax);
         }
-        uint4 code;
-        code.x = pack_e4m3x4(__fmul_rn(f[0], mult), __fmul_rn(f[1], mult), __fmul_rn(f[2], mult),
-                             __fmul_rn(f[3], mult));
-        code.y = pack_e4m3x4(__fmul_rn(f[4], mult), __fmul_rn(f[5], mult), __fmul_rn(f[6], mult),
-                             __fmul_rn(f[7], mult));
-        code.z = pack_e4m3x4(__fmul_rn(f[8], mult), __fmul_rn(f[9], mult), __fmul_rn(f[10], mult),
-                             __fmul_rn(f[11], mult));
-        code.w = pack_e4m3x4(__fmul_rn(f[12], mult), __fmul_rn(f[13], mult), __fmul_rn(f[14], mult),
-                             __fmul_rn(f[15], mult));
-        const int64_t col = static_cast<int64_t>(b) * 128 + sub * 16;
+        uint32_t code[2 * kVec];
+#pragma unroll
+        for (int e = 0; e < 2 * kVec; ++e)
+            code[e] = pack_e4m3x4(__fmul_rn(f[4 * e], mult), __fmul_rn(f[4 * e + 1], mult),
+                                  __fmul_rn(f[4 * e + 2], mult), __fmul_rn(f[4 * e + 3], mult));
+        const int64_t col = static_cast<int64_t>(b) * 128 + sub * (8 * kVec);
         for (int rb = 0; rb < n_dst; rb += 32) {
             const int d = rb == 0 ? d0 : rb == 32 ? d1 : (rb + lane < n_dst ? drow[rb + lane] : -1);
             if (d >= p.capacity && c == 0 && q == 0) cap_bad = true;
@@ -509,7 +512,11 @@ __device__ __forceinline__ void dispatch_fp8_item(const DispatchParams& p, int64
                 m &= m - 1;
                 const int64_t dd = __shfl_sync(0xffffffffu, d, sl);
                 if (valid) {
-                    st_v4(p.recv_x + dd * p.H + col, code);
+                    uint8_t* dst = p.recv_x + dd * p.H + col;
+                    if (kVec == 2)
+                        st_v4(dst, make_uint4(code[0], code[1], code[2 % (2 * kVec)], code[3 % (2 * kVec)]));
+                    else
+                        *reinterpret_cast<uint2*>(dst) = make_uint2(code[0], code[1]);
                     if (sub == 0 && p.recv_sf) {
                         const int64_t si = p.sf_col_major ? static_cast<int64_t>(b) * p.sf_stride + dd : dd * nb + b;
                         p.recv_sf[si] = sf;
@@ -522,7 +529,7 @@ __device__ __forceinline__ void dispatch_fp8_item(const DispatchParams& p, int64
 
 // kGroups == 1: one CTA per item.  kGroups > 1 (SM-limited mode): several
 // independent groups per CTA, each looping over items with a stride.
-template <bool kExpanded, int kGroups>
+template <bool kExpanded, int kGroups, int kLanes>
 __global__ void __launch_bounds__(kFp8Threads * kGroups, kGroups == 1 ? EP_DISPATCH_FP8_MIN_BLOCKS : 1)
     dispatch_fp8_kernel(const DispatchParams p) {
     const int gtid = static_cast<int>(threadIdx.x) % kFp8Threads;
@@ -530,13 +537,13 @@ __global__ void __launch_bounds__(kFp8Threads * kGroups, kGroups == 1 ? EP_DISPA
     bool cap_bad = false;
     pdl_wait();   // before any global access: the previous kernel may write x
     if (kGroups == 1) {
-        dispatch_fp8_item<kExpanded>(p, blockIdx.x, gtid, lane, cap_bad);
+        dispatch_fp8_item<kExpanded, kLanes>(p, blockIdx.x, gtid, lane, cap_bad);
     } else {
         const int64_t n_items = static_cast<int64_t>(p.T) * p.chunks;
         const int group = static_cast<int>(threadIdx.x) / kFp8Threads;
         for (int64_t it = static_cast<int64_t>(blockIdx.x) * kGroups + group; it < n_items;
              it += static_cast<int64_t>(gridDim.x) * kGroups)
-            dispatch_fp8_item<kExpanded>(p, it, gtid, lane, cap_bad);
+            dispatch_fp8_item<kExpanded, kLanes>(p, it, gtid, lane, cap_bad);
     }
     if ((gtid >> 5) == 0 && __any_sync(0xffffffffu, cap_bad) && lane == 0) atomicOr(p.status, EP_ERR_CAPACITY);
 }
@@ -629,16 +636,37 @@ cudaError_t launch_dispatch_bf16(DispatchParams p, cudaStream_t stream) {
     return launch_dispatch_bulk_t<kBulkStages, kBulkStoreDepth>(p, 0, stream);
 }
 
+template <int kLanes>
+cudaError_t launch_dispatch_fp8_t(DispatchParams p, int num_sms, cudaStream_t stream) {
+    const int64_t items = static_cast<int64_t>(p.T) * p.chunks;
+    if (num_sms > 0) {
+        int64_t g = (items + kSmGroups - 1) / kSmGroups;
+        if (g > num_sms) g = num_sms;
+        const dim3 grid(static_cast<unsigned>(g)), block(kFp8Threads * kSmGroups);
+        if (p.expanded_row) return launch_pdl(dispatch_fp8_kernel<true, kSmGroups, kLanes>, grid, block, 0, stream, p);
+        return launch_pdl(dispatch_fp8_kernel<false, kSmGroups, kLanes>, grid, block, 0, stream, p);
+    }
+    const dim3 grid(static_cast<unsigned>(items)), block(kFp8Threads);
+    if (p.expanded_row) return launch_pdl(dispatch_fp8_kernel<true, 1, kLanes>, grid, block, 0, stream, p);
+    return launch_pdl(dispatch_fp8_kernel<false, 1, kLanes>, grid, block, 0, stream, p);
+}
+
 cudaError_t launch_dispatch_fp8(DispatchParams p, cudaStream_t stream) {
     const DeviceInfo& di = device_info();
     const int nb = p.H / 128;
-    // One CTA per (token, piece); pieces of up to 64 blocks (8192 channels),
-    // split further when there are few tokens.
-    int chunks = (nb + EP_DISPATCH_FP8_PIECE_BLOCKS - 1) / EP_DISPATCH_FP8_PIECE_BLOCKS;
+    // Many tokens: 8 lanes per block (fewer instructions per byte); few tokens
+    // (fewer than 8 per SM): 16 lanes per block (shorter dependent path).
+    const bool wide = static_cast<int64_t>(p.T) >= 8 * static_cast<int64_t>(di.num_sms);
+    const int blocks_per_round = (wide ? 4 : 2) * (kFp8Threads / 32);
+    // One CTA per (token, piece); pieces of up to kFp8Rounds rounds of blocks
+    // (at most EP_DISPATCH_FP8_PIECE_BLOCKS), split further when there are few tokens.
+    int piece_max = kFp8Rounds * blocks_per_round;
+    if (piece_max > EP_DISPATCH_FP8_PIECE_BLOCKS) piece_max = EP_DISPATCH_FP8_PIECE_BLOCKS;
+    int chunks = (nb + piece_max - 1) / piece_max;
     const int want_items = 4 * di.num_sms;
     if (p.T > 0 && static_cast<int64_t>(p.T) * chunks < want_items) {
         const int more = (want_items + p.T - 1) / p.T;
-        const int max_chunks = (nb + 3) / 4;  // keep >= 4 blocks (one warp) per piece
+        const int max_chunks = (nb + blocks_per_round / 8 - 1) / (blocks_per_round / 8);   // >= one warp's blocks per piece
         chunks = more < max_chunks ? more : max_chunks;
         if (chunks < 1) chunks = 1;
     }
@@ -649,16 +677,7 @@ cudaError_t launch_dispatch_fp8(DispatchParams p, cudaStream_t stream) {
     const int64_t items = static_cast<int64_t>(p.T) * chunks;
     if (items < 1) return cudaSuccess;
     const int num_sms = p.num_sms > 0 ? (p.num_sms < di.num_sms ? p.num_sms : di.num_sms) : 0;
-    if (num_sms > 0) {
-        int64_t g = (items + kSmGroups - 1) / kSmGroups;
-        if (g > num_sms) g = num_sms;
-        const dim3 grid(static_cast<unsigned>(g)), block(kFp8Threads * kSmGroups);
-        if (p.expanded_row) return launch_pdl(dispatch_fp8_kernel<true, kSmGroups>, grid, block, 0, stream, p);
-        return launch_pdl(dispatch_fp8_kernel<false, kSmGroups>, grid, block, 0, stream, p);
-    }
-    const dim3 grid(static_cast<unsigned>(items)), block(kFp8Threads);
-    if (p.expanded_row) return launch_pdl(dispatch_fp8_kernel<true, 1>, grid, block, 0, stream, p);
-    return launch_pdl(dispatch_fp8_kernel<false, 1>, grid, block, 0, stream, p);
+    return wide ? launch_dispatch_fp8_t<8>(p, num_sms, stream) : launch_dispatch_fp8_t<16>(p, num_sms, stream);
 }
 
 }  // namespace epg
