@@ -39,6 +39,23 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 L2_FLUSH_BYTES = 256 << 20
+HBM_NOMINAL_GBS = 7900.0   # GB300 HBM3e nominal bandwidth (context beside the measured copy peak)
+
+
+def host_cpu():
+    """Host core count and CPU model (as far as /proc/cpuinfo names it)."""
+    import platform
+    model = platform.machine()
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                key = line.split(":")[0].strip().lower()
+                if key in ("model name", "cpu model", "hardware"):
+                    model = line.split(":", 1)[1].strip()
+                    break
+    except OSError:
+        pass
+    return {"host_cores": os.cpu_count(), "cpu_model": model}
 def kernels_per_step(T, R, expanded=False, hierarchical=False):
     """Launches of this library per step: the layout is one cluster kernel, or
     three tiled kernels when T*R is large or expanded or node rows are wanted;
@@ -568,8 +585,10 @@ def run_ours(args):
         "per_kernel": per_kernel,
         "roofline": {"bound": "hbm", "kernel": dominant, "achieved": achieved, "peak": peak,
                      "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / peak,
-                     # recorded DRAM traffic is of the rank path's kernels only
-                     "traffic": recorded_traffic(dominant, args.workload) if args.path == "rank" else None,
+                     "frac_of_nominal": achieved / HBM_NOMINAL_GBS,
+                     # recorded DRAM traffic is of the rank path's bf16 kernels only
+                     "traffic": (recorded_traffic(dominant, args.workload)
+                                 if args.path == "rank" and not args.fp8 else None),
                      "algorithmic_bytes_per_launch": nbytes[dominant], "timed_in": source[dominant]},
         "e2e": e2e,
         "gpu_launches": kernels_per_step(T, R, expanded, hierarchical) * args.steps,
@@ -708,7 +727,7 @@ def cpu_baseline(cfg, data, nbytes, N, seconds):
     return {"value": moved / el / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
             "sample": "%d full step(s) of the workload (all %d tokens), single-threaded C oracle"
                       % (done, cfg.T),
-            "tokens_per_s": done * cfg.T / el}
+            "tokens_per_s": done * cfg.T / el, **host_cpu()}
 
 
 def run_reference(args):
@@ -752,7 +771,8 @@ def run_reference(args):
         "data": "synthetic", "tokens_per_s": args.steps * n_tok / el,
         "config": {"workload": cfg.description, "T": cfg.T, "H": cfg.H, "E": cfg.E, "K": cfg.K,
                    "R": cfg.R, "l2": "n/a (host)"},
-        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": sample},
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": sample,
+                         **host_cpu()},
         "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }))
 
