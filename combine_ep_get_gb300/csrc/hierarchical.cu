@@ -14,8 +14,10 @@
 // rows of the node's ranks (fp32, weighted or not) into one bf16 node row;
 // stage 2 (scale-out) is the ordinary unweighted combine over node_row.
 //
-// Both kernels take one CTA per (token, piece) and walk the token's nodes in
-// order; all stores are 16-byte vectors.
+// Both kernels take one CTA per (token, piece); the forwarder walks the
+// token's nodes in order, the reduce compacts all the token's source rows at
+// once (ascending rank, hence grouped by node) and streams them in batches
+// across node boundaries.  All stores are 16-byte vectors.
 #include <cuda_bf16.h>
 
 #include "ep_internal.cuh"
@@ -116,105 +118,126 @@ template <bool kWeighted>
 __global__ void __launch_bounds__(kRedThreads, 12) reduce_scaleup_kernel(const HierParams p) {
     __shared__ int s_rows[EP_MAX_TOPK];
     __shared__ float s_coef[EP_MAX_TOPK];
+    __shared__ int s_dst[EP_MAX_TOPK];   // node row (partial) each source row adds into
     __shared__ int s_n;
     const int gtid = threadIdx.x;
     pdl_wait();
     const int t = static_cast<int>(blockIdx.x / p.chunks);
     const int c = static_cast<int>(blockIdx.x - static_cast<unsigned>(t) * p.chunks);
     const int rpn = p.ranks_per_node;
+    // Warp 0: the token's source rows over all ranks in ascending order, which
+    // groups them by node; each entry carries its node's row in node_y.
+    if (gtid < 32) {
+        const int lane = gtid;
+        int64_t e_l = -1;
+        float w_l = 0.0f;
+        if (kWeighted && lane < p.K) {
+            e_l = p.topk_idx[static_cast<int64_t>(t) * p.K + lane];
+            w_l = p.topk_weights[static_cast<int64_t>(t) * p.K + lane];
+        }
+        const int32_t* nrow = p.node_row + static_cast<int64_t>(t) * p.num_nodes;
+        const int j_lane = lane < p.num_nodes ? nrow[lane] : -1;   // nodes 0..31, with the rank rows
+        const int32_t* srow = p.dst_row + static_cast<int64_t>(t) * p.R;
+        int n = 0;
+        bool cap_bad = false;
+        for (int rb = 0; rb < p.R; rb += 32) {
+            const int r = rb + lane;
+            const int d = r < p.R ? srow[r] : -1;
+            const int nd = r / rpn;
+            int j = -1;
+            if (nd < 32) {
+                j = __shfl_sync(0xffffffffu, j_lane, nd & 31);
+            } else if (d >= 0) {
+                j = nrow[nd];
+            }
+            // a row beyond num_y_rows stays in the list as a null entry (never
+            // loaded), so its node's partial is still written from the others
+            bool ok = d >= 0;
+            if (d >= p.num_y_rows) cap_bad = true;
+            if (ok && (j < 0 || j >= p.node_capacity)) {   // the node's partial row does not exist
+                if (j >= p.node_capacity) cap_bad = true;
+                ok = false;
+            }
+            float coef = 1.0f;
+            if (kWeighted) {
+                coef = 0.0f;
+                for (int k = 0; k < p.K; ++k) {
+                    const int64_t e = __shfl_sync(0xffffffffu, e_l, k);
+                    const float w = __shfl_sync(0xffffffffu, w_l, k);
+                    if (e >= 0 && e < p.E && static_cast<int>(e) / p.experts_per_rank == r) coef += w;
+                }
+            }
+            const unsigned m = __ballot_sync(0xffffffffu, ok);
+            const int pos = n + __popc(m & ((1u << lane) - 1u));
+            if (ok && pos < EP_MAX_TOPK) {
+                s_rows[pos] = d < p.num_y_rows ? d : -1;
+                s_coef[pos] = coef;
+                s_dst[pos] = j;
+            }
+            n += __popc(m);
+        }
+        if (n > EP_MAX_TOPK) {
+            if (lane == 0) atomicOr(p.status, EP_ERR_INVALID_INDEX);
+            n = EP_MAX_TOPK;
+        }
+        if (lane == 0) s_n = n;
+        if (__any_sync(0xffffffffu, cap_bad) && lane == 0 && c == 0) atomicOr(p.status, EP_ERR_CAPACITY);
+    }
+    __syncthreads();
+
+    const int n = s_n;
     const int n_vec = p.H / 8;
     const int v_begin = c * p.chunk_vecs;
     const int v_end = min(n_vec, v_begin + p.chunk_vecs);
     const int64_t row_bytes = static_cast<int64_t>(p.H) * 2;
-    for (int nd = 0; nd < p.num_nodes; ++nd) {
-        const int j = p.node_row[static_cast<int64_t>(t) * p.num_nodes + nd];   // uniform over the CTA
-        if (j < 0) continue;
-        if (j >= p.node_capacity) {
-            if (gtid == 0 && c == 0) atomicOr(p.status, EP_ERR_CAPACITY);
-            continue;
-        }
-        if (gtid < 32) {
-            const int lane = gtid;
-            int64_t e_l = -1;
-            float w_l = 0.0f;
-            if (kWeighted && lane < p.K) {
-                e_l = p.topk_idx[static_cast<int64_t>(t) * p.K + lane];
-                w_l = p.topk_weights[static_cast<int64_t>(t) * p.K + lane];
+    for (int v = v_begin + gtid; v < v_end; v += kRedThreads) {
+        float acc[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) acc[q] = 0.0f;
+        const int64_t voff = static_cast<int64_t>(v) * 16;
+        // rows of all the token's nodes in batches; a node's partial is stored
+        // after its last row, then the sum restarts
+        for (int m0 = 0; m0 < n; m0 += kRedBatch) {
+            uint4 buf[kRedBatch];
+#pragma unroll
+            for (int i = 0; i < kRedBatch; ++i) {
+                const int d = m0 + i < n ? s_rows[m0 + i] : -1;
+                buf[i] = d >= 0 ? ld_stream_v4(p.y + static_cast<int64_t>(d) * row_bytes + voff) : make_uint4(0, 0, 0, 0);
             }
-            int n = 0;
-            bool cap_bad = false;
-            const int32_t* srow = p.dst_row + static_cast<int64_t>(t) * p.R + nd * rpn;
-            for (int rb = 0; rb < rpn; rb += 32) {
-                const int r = rb + lane;
-                const int d = r < rpn ? srow[r] : -1;
-                const bool ok = d >= 0 && d < p.num_y_rows;
-                if (d >= p.num_y_rows) cap_bad = true;
-                float coef = 1.0f;
-                if (kWeighted) {
-                    coef = 0.0f;
-                    const int rank = nd * rpn + r;
-                    for (int k = 0; k < p.K; ++k) {
-                        const int64_t e = __shfl_sync(0xffffffffu, e_l, k);
-                        const float w = __shfl_sync(0xffffffffu, w_l, k);
-                        if (e >= 0 && e < p.E && static_cast<int>(e) / p.experts_per_rank == rank) coef += w;
-                    }
-                }
-                const unsigned m = __ballot_sync(0xffffffffu, ok);
-                const int pos = n + __popc(m & ((1u << lane) - 1u));
-                if (ok && pos < EP_MAX_TOPK) {
-                    s_rows[pos] = d;
-                    s_coef[pos] = coef;
-                }
-                n += __popc(m);
-            }
-            if (n > EP_MAX_TOPK) {
-                if (lane == 0) atomicOr(p.status, EP_ERR_INVALID_INDEX);
-                n = EP_MAX_TOPK;
-            }
-            if (lane == 0) s_n = n;
-            if (__any_sync(0xffffffffu, cap_bad) && lane == 0 && c == 0) atomicOr(p.status, EP_ERR_CAPACITY);
-        }
-        __syncthreads();
-        const int n = s_n;
-        uint8_t* orow = p.node_y + static_cast<int64_t>(j) * row_bytes;
-        for (int v = v_begin + gtid; v < v_end; v += kRedThreads) {
-            float acc[8];
 #pragma unroll
-            for (int q = 0; q < 8; ++q) acc[q] = 0.0f;
-            const int64_t voff = static_cast<int64_t>(v) * 16;
-            for (int m0 = 0; m0 < n; m0 += kRedBatch) {
-                uint4 buf[kRedBatch];
+            for (int i = 0; i < kRedBatch; ++i) {
+                const int m = m0 + i;
+                if (m < n) {
+                    const uint32_t w[4] = {buf[i].x, buf[i].y, buf[i].z, buf[i].w};
+                    const float cf = kWeighted ? s_coef[m] : 1.0f;
+                    const bool live = s_rows[m] >= 0;
 #pragma unroll
-                for (int i = 0; i < kRedBatch; ++i)
-                    if (m0 + i < n) buf[i] = ld_stream_v4(p.y + static_cast<int64_t>(s_rows[m0 + i]) * row_bytes + voff);
-#pragma unroll
-                for (int i = 0; i < kRedBatch; ++i) {
-                    if (m0 + i < n) {
-                        const uint32_t w[4] = {buf[i].x, buf[i].y, buf[i].z, buf[i].w};
-                        const float cf = kWeighted ? s_coef[m0 + i] : 1.0f;
-#pragma unroll
-                        for (int q = 0; q < 4; ++q) {
-                            if (kWeighted) {
-                                acc[2 * q] = fmaf(cf, __uint_as_float(w[q] << 16), acc[2 * q]);
-                                acc[2 * q + 1] = fmaf(cf, __uint_as_float(w[q] & 0xffff0000u), acc[2 * q + 1]);
-                            } else {
-                                acc[2 * q] += __uint_as_float(w[q] << 16);
-                                acc[2 * q + 1] += __uint_as_float(w[q] & 0xffff0000u);
-                            }
+                    for (int q = 0; q < 4; ++q) {
+                        if (!live) {
+                        } else if (kWeighted) {
+                            acc[2 * q] = fmaf(cf, __uint_as_float(w[q] << 16), acc[2 * q]);
+                            acc[2 * q + 1] = fmaf(cf, __uint_as_float(w[q] & 0xffff0000u), acc[2 * q + 1]);
+                        } else {
+                            acc[2 * q] += __uint_as_float(w[q] << 16);
+                            acc[2 * q + 1] += __uint_as_float(w[q] & 0xffff0000u);
                         }
                     }
+                    const int j = s_dst[m];
+                    if (m == n - 1 || s_dst[m + 1] != j) {
+                        uint4 o;
+                        uint32_t* ow = reinterpret_cast<uint32_t*>(&o);
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            const __nv_bfloat162 h = __floats2bfloat162_rn(acc[2 * q], acc[2 * q + 1]);
+                            ow[q] = *reinterpret_cast<const uint32_t*>(&h);
+                            acc[2 * q] = 0.0f;
+                            acc[2 * q + 1] = 0.0f;
+                        }
+                        st_v4(p.node_y + static_cast<int64_t>(j) * row_bytes + voff, o);
+                    }
                 }
             }
-            uint4 o;
-            uint32_t* ow = reinterpret_cast<uint32_t*>(&o);
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const __nv_bfloat162 h = __floats2bfloat162_rn(acc[2 * q], acc[2 * q + 1]);
-                ow[q] = *reinterpret_cast<const uint32_t*>(&h);
-            }
-            st_v4(orow + voff, o);
         }
-        __syncthreads();   // the row list is rebuilt for the next node
     }
 }
 

@@ -257,3 +257,43 @@ def test_hierarchical_node_capacity_overflow():
     assert int(g["status"].item()) & oracle.EP_ERR_CAPACITY
     _, _, st = _combine(B, g["recv_x"], idx, None, E, R, rpn, lay, M - 10, T, H)
     assert int(st.item()) & oracle.EP_ERR_CAPACITY
+
+
+@pytest.mark.parametrize("weighted", [False, True])
+def test_combine_hierarchical_short_y(weighted):
+    """Expert rows beyond num_y_rows are skipped: each node partial is the sum
+    of the node's remaining rows (zero when none remain), as in the oracle;
+    the capacity bit is set."""
+    from gpu_path import B, bf16_bits, x_tensor
+    T, H, E, K, R, rpn = 400, 512, 64, 6, 16, 4
+    d = make_inputs(T, H, E, K, R, seed=31, mask_frac=0.05, with_x=False)
+    idx, lay, _ = _layout(d["topk_idx"], E, R, rpn)
+    w = torch.from_numpy(d["topk_weights"]).cuda()
+    N, M = lay.num_recv, int(lay.node_offset[-1].item())
+    n_y = N - 300
+    y_bits = make_rows(n_y, H, seed=32)
+    node_y, out, st = _combine(B, x_tensor(y_bits), idx, w if weighted else None, E, R, rpn, lay, M, T, H)
+    assert int(st.item()) & oracle.EP_ERR_CAPACITY
+    L = oracle.layout(d["topk_idx"], E, R)
+    _, rows, _ = oracle.node_rows(d["topk_idx"], E, R, rpn)
+    ony, oout, ost = oracle.combine_hierarchical(y_bits, d["topk_idx"], d["topk_weights"], E, R, rpn, rows,
+                                                 L.dst_row, M, weighted=weighted)
+    assert ost & oracle.EP_ERR_CAPACITY
+    yf = oracle.bf16_to_float(y_bits).astype(np.float64)
+    el = E // R
+    scale_node = np.zeros((M, H))
+    scale_tok = np.zeros((T, H))
+    tt, rr = np.nonzero((L.dst_row >= 0) & (L.dst_row < n_y))
+    for t, r in zip(tt, rr):
+        c = 1.0
+        if weighted:
+            c = sum(abs(float(d["topk_weights"][t, k])) for k in range(K)
+                    if d["topk_idx"][t, k] >= 0 and d["topk_idx"][t, k] // el == r)
+        a = c * np.abs(yf[L.dst_row[t, r]])
+        scale_node[rows[t, r // rpn]] += a
+        scale_tok[t] += a
+    g_node = oracle.bf16_to_float(bf16_bits(node_y).reshape(M, H)).astype(np.float64)
+    want_node = oracle.bf16_to_float(ony).astype(np.float64)
+    assert (np.abs(g_node - want_node) <= 1e-2 * scale_node).all()
+    g_out = oracle.bf16_to_float(bf16_bits(out).reshape(T, H)).astype(np.float64)
+    assert (np.abs(g_out - oout) <= 1e-2 * scale_tok).all()
