@@ -622,12 +622,11 @@ cudaError_t launch_dispatch_bf16(DispatchParams p, cudaStream_t stream) {
         const int64_t items = static_cast<int64_t>(p.T) * p.chunks;
         if (items < 1) return cudaSuccess;
         const int num_sms = p.num_sms > 0 ? (p.num_sms < di.num_sms ? p.num_sms : di.num_sms) : 0;
-        if (num_sms > 0) {
+        if (num_sms > 0) {   // only the expanded mode reaches here (rank rows took the bulk path)
             int64_t g = (items + kSmGroups - 1) / kSmGroups;
             if (g > num_sms) g = num_sms;
             const dim3 grid(static_cast<unsigned>(g)), block(kRegThreads * kSmGroups);
-            if (p.expanded_row) return launch_pdl(dispatch_bf16_regs_kernel<true, kSmGroups>, grid, block, 0, stream, p);
-            return launch_pdl(dispatch_bf16_regs_kernel<false, kSmGroups>, grid, block, 0, stream, p);
+            return launch_pdl(dispatch_bf16_regs_kernel<true, kSmGroups>, grid, block, 0, stream, p);
         }
         const dim3 grid(static_cast<unsigned>(items)), block(kRegThreads);
         if (p.expanded_row) return launch_pdl(dispatch_bf16_regs_kernel<true, 1>, grid, block, 0, stream, p);
