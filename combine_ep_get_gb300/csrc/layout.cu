@@ -244,21 +244,62 @@ __device__ int block_exclusive_scan_slice(const int (&v)[kMax], int (&out)[kMax]
     return total;
 }
 
+// Ranks entries [0, n_ent) per expert in index order: entry i with key
+// e >= 0 (s_key[i]; negative keys are unique per lane and never match) gets
+// out[i] = s_eb[e] + (entries of e before i), else -1.  Warps 0..7 each rank
+// a contiguous slice of 32-entry chunks twice with __match_any_sync (count,
+// then place) around per-(warp, expert) bases in s_wc [nw][E] (warps
+// 0..nw-1 rank), which the caller has zeroed; the order never depends on
+// timing.  Every thread of the block calls it (block barriers inside).
+constexpr int kRankWarps = 8;
+__device__ void rank_entries(const int* s_key, int n_ent, int E, const int* s_eb, int* s_wc, int32_t* out,
+                             int nw) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int chunks = (n_ent + 31) / 32;
+    const int per = (chunks + nw - 1) / nw;
+    const int c0 = warp < nw ? min(chunks, warp * per) : 0;
+    const int c1 = warp < nw ? min(chunks, c0 + per) : 0;
+    for (int c = c0; c < c1; ++c) {                     // pass 1: per-(warp, expert) counts
+        const int i = c * 32 + lane;
+        const int key = i < n_ent ? s_key[i] : -1 - lane;
+        const unsigned g = __match_any_sync(0xffffffffu, key);
+        if (key >= 0 && lane == __ffs(g) - 1) s_wc[warp * E + key] += __popc(g);
+        __syncwarp();
+    }
+    __syncthreads();
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {   // per-warp bases, warps in entry order
+        int run = s_eb[e];
+        for (int w = 0; w < nw; ++w) {
+            const int v = s_wc[w * E + e];
+            s_wc[w * E + e] = run;
+            run += v;
+        }
+    }
+    __syncthreads();
+    for (int c = c0; c < c1; ++c) {                     // pass 2: place
+        const int i = c * 32 + lane;
+        const int key = i < n_ent ? s_key[i] : -1 - lane;
+        const unsigned g = __match_any_sync(0xffffffffu, key);
+        int pos = -1;
+        if (key >= 0) pos = s_wc[warp * E + key] + __popc(g & ((1u << lane) - 1u));
+        __syncwarp();
+        if (key >= 0 && lane == __ffs(g) - 1) s_wc[warp * E + key] += __popc(g);
+        __syncwarp();
+        if (i < n_ent) out[i] = pos;
+    }
+}
+
 // Expanded (per-expert) rows of one tile's (token, k) entries: expert e's
-// entries take rows expert_offset[e] + (entries of e in earlier tiles) + their
-// stable rank in the tile, in (token, k) order.  The tile's entries are staged
-// in shared memory; each warp ranks a contiguous slice of them twice with
-// __match_any_sync (count, then place) around a per-(warp, expert) prefix, so
-// the order never depends on timing.  s_eb holds each expert's base row
-// for this tile; needs 256 K + 8 E shared ints.
+// entries take rows s_eb[e] (expert_offset[e] + entries of e in earlier
+// tiles) + their stable rank in the tile, in (token, k) order.  The tile's
+// entries are staged in shared memory (the first batch was loaded at kernel
+// entry).  Needs 256 K + 8 E shared ints.
 __device__ void expanded_rows_of_tile(const LayoutParams& p, int t0, int nt, const int* s_eb, int* sm,
                                       const int64_t (&key0)[kStageUnroll]) {
-    constexpr int kWarps = kThreads / 32;
     const int E = p.E;
     const int n_ent = nt * p.K;
     int* s_key = sm;                        // [256 K] expert of each entry, or a unique negative
-    int* s_wc = s_key + kTileTokens * p.K;  // [kWarps][E] per-warp counts, then per-warp bases
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int* s_wc = s_key + kTileTokens * p.K;  // [8][E] per-warp counts, then per-warp bases
     const int64_t* src = p.topk_idx + static_cast<int64_t>(t0) * p.K;
     for (int base = 0; base < n_ent; base += kStageUnroll * kThreads) {
         int64_t e[kStageUnroll];
@@ -273,41 +314,9 @@ __device__ void expanded_rows_of_tile(const LayoutParams& p, int t0, int nt, con
             if (i < n_ent) s_key[i] = (e[u] >= 0 && e[u] < E) ? static_cast<int>(e[u]) : -1 - (i & 31);
         }
     }
-    for (int i = threadIdx.x; i < kWarps * E; i += kThreads) s_wc[i] = 0;
+    for (int i = threadIdx.x; i < kRankWarps * E; i += kThreads) s_wc[i] = 0;
     __syncthreads();
-    // each warp owns entries [w0, w1), whole 32-entry chunks
-    const int chunks = (n_ent + 31) / 32;
-    const int per = (chunks + kWarps - 1) / kWarps;
-    const int c0 = min(chunks, warp * per), c1 = min(chunks, c0 + per);
-    for (int c = c0; c < c1; ++c) {                     // pass 1: per-(warp, expert) counts
-        const int i = c * 32 + lane;
-        const int key = i < n_ent ? s_key[i] : -1 - lane;
-        const unsigned g = __match_any_sync(0xffffffffu, key);
-        if (key >= 0 && lane == __ffs(g) - 1) s_wc[warp * E + key] += __popc(g);
-        __syncwarp();
-    }
-    __syncthreads();
-    for (int e = threadIdx.x; e < E; e += kThreads) {   // per-warp bases, warps in entry order
-        int run = s_eb[e];
-        for (int w = 0; w < kWarps; ++w) {
-            const int v = s_wc[w * E + e];
-            s_wc[w * E + e] = run;
-            run += v;
-        }
-    }
-    __syncthreads();
-    int32_t* out = p.expanded_row + static_cast<int64_t>(t0) * p.K;
-    for (int c = c0; c < c1; ++c) {                     // pass 2: place
-        const int i = c * 32 + lane;
-        const int key = i < n_ent ? s_key[i] : -1 - lane;
-        const unsigned g = __match_any_sync(0xffffffffu, key);
-        int pos = -1;
-        if (key >= 0) pos = s_wc[warp * E + key] + __popc(g & ((1u << lane) - 1u));
-        __syncwarp();
-        if (key >= 0 && lane == __ffs(g) - 1) s_wc[warp * E + key] += __popc(g);
-        __syncwarp();
-        if (i < n_ent) out[i] = pos;
-    }
+    rank_entries(s_key, n_ent, E, s_eb, s_wc, p.expanded_row + static_cast<int64_t>(t0) * p.K, kRankWarps);
 }
 
 // Node rows of one tile: a token is in node n when any rank of n holds it,
@@ -584,9 +593,15 @@ constexpr int kMaxClusterCtas = 16;
 constexpr int64_t kClusterMaxTokenRanks = EP_LAYOUT_CLUSTER_MAX_TOKEN_RANKS;
 
 // Shared-memory words of one cluster CTA for W bitmap words per rank.
-size_t cluster_smem_words(int R, int E, int nodes, int W) {
-    return 2 * static_cast<size_t>(R) * W + static_cast<size_t>(nodes) * W + R + E + nodes + (R + 1) +
-           R + 33 * static_cast<size_t>(W) + 64;
+// Warps that rank the expanded entries in a cluster CTA: all 32 while their
+// [warps][E] counters stay small, else 8.
+__host__ __device__ inline int cluster_rank_warps(int E) { return E <= 512 ? 32 : kRankWarps; }
+
+size_t cluster_smem_words(int R, int E, int nodes, int W, int K, bool expanded) {
+    size_t w = 2 * static_cast<size_t>(R) * W + static_cast<size_t>(nodes) * W + R + E + nodes + (R + 1) + R +
+               33 * static_cast<size_t>(W) + 64;
+    if (expanded) w += 32 * static_cast<size_t>(W) * K + (1 + cluster_rank_warps(E)) * static_cast<size_t>(E);
+    return w;
 }
 
 // In-place exclusive scan of a[0, n) in shared memory by all kClusterThreads
@@ -660,6 +675,10 @@ __global__ void __launch_bounds__(kClusterThreads, 1)
     int* s_before = s_tot + R + 1;                                  // [R]
     int* s_ntok = s_before + R;                                     // [32 W] token's row within its word
     int* s_wtok = s_ntok + 32 * W;                                  // [W] rows of earlier words
+    const bool expanded = p.expanded_row != nullptr;
+    int* s_key = s_wtok + W;                                        // expanded: [32 W K] expert of each entry
+    int* s_eb = s_key + (expanded ? 32 * W * p.K : 0);              // expanded: [E] expert bases
+    int* s_wc = s_eb + (expanded ? E : 0);                          // expanded: [8][E] ranking counters
     __shared__ int s_rows_total;                                    // read by later CTAs
     __shared__ int s_cta_base;
     __shared__ int s_totals[2];                                     // N, expert rows
@@ -689,6 +708,13 @@ __global__ void __launch_bounds__(kClusterThreads, 1)
         for (int u = 0; u < kClusterUnroll; ++u) {
             const int i = base + u * kClusterThreads + tid;
             e[u] = i < n_ent ? src[i] : -1;
+        }
+        if (expanded) {
+#pragma unroll
+            for (int u = 0; u < kClusterUnroll; ++u) {
+                const int i = base + u * kClusterThreads + tid;
+                if (i < n_ent) s_key[i] = (e[u] >= 0 && e[u] < E) ? static_cast<int>(e[u]) : -1 - (i & 31);
+            }
         }
 #pragma unroll
         for (int u = 0; u < kClusterUnroll; ++u) {
@@ -763,9 +789,27 @@ __global__ void __launch_bounds__(kClusterThreads, 1)
         const int sum = warp_inclusive_scan(v);
         if (lane == 31) s_cta_base = sum;
     }
+    if (expanded) {
+        // every CTA needs each expert's total (for the offsets) and its count in
+        // earlier CTAs; the histograms stay untouched (others read them too)
+        for (int e = tid; e < E; e += kClusterThreads) {
+            int v[kMaxClusterCtas];
+#pragma unroll
+            for (int c = 0; c < kMaxClusterCtas; ++c) v[c] = c < C ? cluster.map_shared_rank(s_hist, c)[e] : 0;
+            int tot = 0, before = 0;
+#pragma unroll
+            for (int c = 0; c < kMaxClusterCtas; ++c) {
+                tot += v[c];
+                if (c < me) before += v[c];
+            }
+            if (me == C - 1) p.num_tokens_per_expert[e] = tot;
+            s_eb[e] = (tot + p.alignment - 1) / p.alignment * p.alignment;
+            s_wc[e] = before;
+        }
+    }
     if (me == C - 1) {
         // only this CTA reads any s_hist, and each e is read and rewritten by one thread
-        for (int e = tid; e < E; e += kClusterThreads) {
+        for (int e = tid; e < E && !expanded; e += kClusterThreads) {
             int v[kMaxClusterCtas];
 #pragma unroll
             for (int c = 0; c < kMaxClusterCtas; ++c) v[c] = c < C ? cluster.map_shared_rank(s_hist, c)[e] : 0;
@@ -797,14 +841,15 @@ __global__ void __launch_bounds__(kClusterThreads, 1)
         const int tot = smem_exclusive_scan(s_tot, R, s_warp);
         if (tid == 0) s_totals[0] = tot;
     }
-    if (me == C - 1) {
+    int* s_escan = expanded ? s_eb : s_hist;   // aligned expert totals -> expert_offset
+    if (expanded || me == C - 1) {
         if (E <= kWarpScanMax) {
             if (warp_id == 2) {
-                const int tot = warp_exclusive_scan_smem(s_hist, E);
+                const int tot = warp_exclusive_scan_smem(s_escan, E);
                 if (lane == 0) s_totals[1] = tot;
             }
         } else {
-            const int tot = smem_exclusive_scan(s_hist, E, s_warp);
+            const int tot = smem_exclusive_scan(s_escan, E, s_warp);
             if (tid == 0) s_totals[1] = tot;
         }
     }
@@ -815,7 +860,7 @@ __global__ void __launch_bounds__(kClusterThreads, 1)
         if (tid == 0) p.rank_offset[R] = n_recv;
     }
     if (me == C - 1) {
-        for (int e = tid; e < E; e += kClusterThreads) p.expert_offset[e] = s_hist[e];
+        for (int e = tid; e < E; e += kClusterThreads) p.expert_offset[e] = s_escan[e];
         if (tid == 0) p.expert_offset[E] = s_totals[1];
     }
 
@@ -884,6 +929,18 @@ __global__ void __launch_bounds__(kClusterThreads, 1)
             if (c) atomicAdd(&p.src_dst_count[s * R + r], c);
         }
     }
+    // Expanded rows: expert e's entries of this CTA start at expert_offset[e] +
+    // its entries in earlier CTAs and are ranked in (token, k) order.
+    if (expanded) {
+        const int nw = cluster_rank_warps(E);
+        for (int e = tid; e < E; e += kClusterThreads) {
+            s_eb[e] += s_wc[e];   // each thread owns column e of s_wc here
+            for (int w = 0; w < nw; ++w) s_wc[w * E + e] = 0;
+        }
+        __syncthreads();
+        rank_entries(s_key, n_ent, E, s_eb, s_wc, p.expanded_row + static_cast<int64_t>(t0) * p.K, nw);
+    }
+
     // No CTA may exit (releasing its shared memory) while another still reads it.
     cluster.sync();
 }
@@ -908,7 +965,7 @@ ClusterPlan plan_cluster(const LayoutParams& p, int smem_max) {
     if (tpc < 32) tpc = 32;
     ctas = (p.T + tpc - 1) / tpc;
     if (ctas < 1) ctas = 1;
-    const size_t smem = 4 * cluster_smem_words(p.R, p.E, p.num_nodes, tpc / 32);
+    const size_t smem = 4 * cluster_smem_words(p.R, p.E, p.num_nodes, tpc / 32, p.K, p.expanded_row != nullptr);
     if (smem > static_cast<size_t>(smem_max)) return plan;
     // Large [T, R] outputs are written faster by the many-CTA path.
     if (static_cast<int64_t>(p.T) * p.R > kClusterMaxTokenRanks) return plan;
@@ -966,8 +1023,8 @@ cudaError_t launch_layout(const LayoutParams& p, cudaStream_t stream) {
         configured_device = di.device;
     }
 
-    // the expanded rows and the node rows are produced by the tiled path only
-    const ClusterPlan plan = (cluster_ok && p.expanded_row == nullptr && p.node_row == nullptr)
+    // the node rows are produced by the tiled path only
+    const ClusterPlan plan = (cluster_ok && p.node_row == nullptr)
                                  ? plan_cluster(p, cluster_smem_max)
                                  : ClusterPlan{0, 0, 0};
     if (plan.ctas > 0) {
