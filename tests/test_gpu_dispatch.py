@@ -161,3 +161,35 @@ def test_dispatch_fp8_shapes(T, H, E, K, R):
         np.testing.assert_array_equal(g[k], o[k], err_msg=k)
     sf = res["recv_sf"].cpu().numpy()[:n * (H // 128)].reshape(n, -1)
     np.testing.assert_array_equal(sf, o["recv_sf"])
+
+
+@pytest.mark.parametrize("sf_col_major", [False, True])
+def test_dispatch_fp8_wide_full_size(sf_col_major):
+    """FP8 dispatch with many tokens (8 lanes per 128-channel block, the mode
+    timed on the DeepSeek-V3-shaped workload): codes and scales of sampled
+    tokens against the oracle's compact dispatch, metadata of every row."""
+    import dataclasses
+    from combine_ep_get_gb300.inputs import CONFIGS
+    d = make_config(dataclasses.replace(CONFIGS["dsv3"], fp8=True))
+    c = d["cfg"]
+    lay, res, n, _, _ = _run(d, c.E, c.R, fp8=True, sf_col_major=sf_col_major)
+    assert int(res["status"].item()) == 0
+    L = oracle.layout(d["topk_idx"], c.E, c.R)
+    stand_in = np.zeros((c.T, 16), np.uint16)
+    om = oracle.dispatch(stand_in, d["topk_idx"], d["topk_weights"], c.E, c.R, L.dst_row)
+    np.testing.assert_array_equal(res["recv_src_idx"][:n].cpu().numpy(), om["recv_src_idx"])
+    np.testing.assert_array_equal(res["recv_topk_idx"][:n].cpu().numpy(), om["recv_topk_idx"])
+    rng = np.random.Generator(np.random.PCG64(7))
+    toks = np.unique(np.concatenate([[0, c.T - 1], rng.choice(c.T, 40, replace=False)])).astype(np.int32)
+    os_ = oracle.dispatch(d["x_bits"], d["topk_idx"], d["topk_weights"], c.E, c.R, L.dst_row, fp8=True,
+                          tokens=toks)
+    rows = os_["rows"].astype(np.int64)
+    np.testing.assert_array_equal(res["recv_x"][torch.from_numpy(rows).cuda()].cpu().numpy(), os_["recv_x"])
+    nb = c.H // 128
+    sf = res["recv_sf"].cpu().numpy()
+    if sf_col_major:
+        stride = (n + 3) // 4 * 4
+        got = sf[:nb * stride].reshape(nb, stride)[:, rows].T
+    else:
+        got = sf[:n * nb].reshape(n, nb)[rows]
+    np.testing.assert_array_equal(got, os_["recv_sf"])

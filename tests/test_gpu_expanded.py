@@ -148,3 +148,28 @@ def test_expanded_round_trip_closed_form():
     n_valid = (idx >= 0).sum(dim=1).float()
     want = (x.float() * n_valid[:, None]).to(torch.bfloat16)
     assert torch.equal(out.float(), want.float())
+
+
+def test_expanded_dispatch_fp8_wide():
+    """Expanded FP8 dispatch in the many-token mode against the oracle."""
+    from gpu_path import B, x_tensor
+    T, H, E, K, R = 2048, 1024, 64, 6, 8
+    d = make_inputs(T, H, E, K, R, seed=19, mask_frac=0.05)
+    idx, lay, _ = _layout(d["topk_idx"], E, R, 1)
+    w = torch.from_numpy(d["topk_weights"]).cuda()
+    cap = int(lay.expert_offset[-1].item())
+    rx = torch.full((cap, H), 0x55, dtype=torch.uint8, device="cuda")
+    rsf = torch.full((cap * (H // 128),), -1.0, dtype=torch.float32, device="cuda")
+    rs = torch.full((cap,), -1, dtype=torch.int32, device="cuda")
+    rw = torch.full((cap,), -9.0, dtype=torch.float32, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    B.ep_dispatch_expanded(x_tensor(d["x_bits"]), idx, w, E, R, lay, rx, rs, rw, st, recv_sf=rsf,
+                           out_dtype=B.EP_FP8_E4M3)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    _, rows, _ = _oracle_rows(d["topk_idx"], E, R, 1)
+    o = oracle.dispatch_expanded(d["x_bits"], d["topk_weights"], rows, cap, fp8=True)
+    valid = np.unique(rows[rows >= 0])
+    np.testing.assert_array_equal(rx.cpu().numpy()[valid], o["recv_x"][valid])
+    np.testing.assert_array_equal(rsf.cpu().numpy().reshape(cap, -1)[valid], o["recv_sf"][valid])
+    np.testing.assert_array_equal(rs.cpu().numpy(), o["recv_src_idx"])

@@ -100,3 +100,19 @@ def test_sm_limited_against_oracle():
     nt = L.is_token_in_rank.sum(axis=1)
     want = (x.float() * torch.from_numpy(nt).cuda().float()[:, None]).to(torch.bfloat16)
     assert torch.equal(out.float(), want.float())
+
+
+@pytest.mark.parametrize("expanded", [False, True])
+@pytest.mark.parametrize("num_sms", [16, 100])
+def test_fp8_wide_sm_limited_matches_default(expanded, num_sms):
+    """FP8 dispatch in the many-token mode (T >= 8 tokens per SM): the
+    SM-limited grid gives exactly the default mode's codes, scales and
+    metadata."""
+    from gpu_path import B
+    T, H, E, K, R = 2048, 1024, 64, 6, 8
+    d, idx, w, x, lay = _setup(T, H, E, K, R, seed=8, expanded=expanded)
+    n = int(lay.expert_offset[-1].item()) if expanded else lay.num_recv
+    ref = _dispatch(B, x, idx, w, E, R, lay, n, H, K, True, 0, expanded)
+    got = _dispatch(B, x, idx, w, E, R, lay, n, H, K, True, num_sms, expanded)
+    for a, b in zip(ref, got):
+        assert torch.equal(a, b)
