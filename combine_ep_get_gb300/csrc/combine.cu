@@ -200,7 +200,11 @@ cudaError_t launch_combine(CombineParams p, bool weighted, cudaStream_t stream) 
     int chunks = (n_vec + 2 * kThreads - 1) / (2 * kThreads);
     const int want_items = 4 * di.num_sms;
     if (p.T > 0 && static_cast<int64_t>(p.T) * chunks < want_items) {
-        const int more = (want_items + p.T - 1) / p.T;
+        // few tokens: latency-bound, so at most one vector per thread (each
+        // CTA then waits for one batch of row loads per 4 rows, not two)
+        int more = (want_items + p.T - 1) / p.T;
+        const int one_vec = (n_vec + kThreads - 1) / kThreads;
+        if (more < one_vec) more = one_vec;
         const int max_chunks = (n_vec + 31) / 32;
         chunks = more < max_chunks ? more : max_chunks;
         if (chunks < 1) chunks = 1;

@@ -654,6 +654,9 @@ __device__ int warp_exclusive_scan_smem(int* a, int n) {
     return __shfl_sync(0xffffffffu, incl, 31);
 }
 
+// kExpanded: also the expanded per-expert rows (a separate instantiation, so
+// the plain layout carries none of that work).
+template <bool kExpanded>
 __global__ void __launch_bounds__(kClusterThreads, 1)
     layout_cluster_kernel(const LayoutParams p, int tokens_per_cta) {
     namespace cg = cooperative_groups;
@@ -675,7 +678,7 @@ __global__ void __launch_bounds__(kClusterThreads, 1)
     int* s_before = s_tot + R + 1;                                  // [R]
     int* s_ntok = s_before + R;                                     // [32 W] token's row within its word
     int* s_wtok = s_ntok + 32 * W;                                  // [W] rows of earlier words
-    const bool expanded = p.expanded_row != nullptr;
+    constexpr bool expanded = kExpanded;
     int* s_key = s_wtok + W;                                        // expanded: [32 W K] expert of each entry
     int* s_eb = s_key + (expanded ? 32 * W * p.K : 0);              // expanded: [E] expert bases
     int* s_wc = s_eb + (expanded ? E : 0);                          // expanded: [8][E] ranking counters
@@ -1011,13 +1014,22 @@ cudaError_t launch_layout(const LayoutParams& p, cudaStream_t stream) {
         e = cudaFuncSetAttribute(layout_rows_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  di.max_smem_optin - static_cast<int>(fa.sharedSizeBytes));
         if (e != cudaSuccess) return e;
-        e = cudaFuncGetAttributes(&fa, layout_cluster_kernel);
+        cudaFuncAttributes fa0{}, fa1{};
+        e = cudaFuncGetAttributes(&fa0, layout_cluster_kernel<false>);
         if (e != cudaSuccess) return e;
-        cluster_smem_max = di.max_smem_optin - static_cast<int>(fa.sharedSizeBytes);
+        e = cudaFuncGetAttributes(&fa1, layout_cluster_kernel<true>);
+        if (e != cudaSuccess) return e;
+        const int static_smem =
+            static_cast<int>(fa0.sharedSizeBytes > fa1.sharedSizeBytes ? fa0.sharedSizeBytes : fa1.sharedSizeBytes);
+        cluster_smem_max = di.max_smem_optin - static_smem;
         cluster_ok =
-            cudaFuncSetAttribute(layout_cluster_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+            cudaFuncSetAttribute(layout_cluster_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  cluster_smem_max) == cudaSuccess &&
-            cudaFuncSetAttribute(layout_cluster_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed,
+            cudaFuncSetAttribute(layout_cluster_kernel<false>, cudaFuncAttributeNonPortableClusterSizeAllowed,
+                                 1) == cudaSuccess &&
+            cudaFuncSetAttribute(layout_cluster_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 cluster_smem_max) == cudaSuccess &&
+            cudaFuncSetAttribute(layout_cluster_kernel<true>, cudaFuncAttributeNonPortableClusterSizeAllowed,
                                  1) == cudaSuccess;
         cudaGetLastError();   // a refused attribute only disables the cluster path
         configured_device = di.device;
@@ -1044,11 +1056,14 @@ cudaError_t launch_layout(const LayoutParams& p, cudaStream_t stream) {
         cfg.numAttrs = 2;
         int max_clusters = 0;
         cfg.numAttrs = 1;   // the occupancy query takes the cluster shape only
-        const bool fits = cudaOccupancyMaxActiveClusters(&max_clusters, layout_cluster_kernel, &cfg) == cudaSuccess;
+        const bool expanded = p.expanded_row != nullptr;
+        const bool fits = (expanded ? cudaOccupancyMaxActiveClusters(&max_clusters, layout_cluster_kernel<true>, &cfg)
+                                    : cudaOccupancyMaxActiveClusters(&max_clusters, layout_cluster_kernel<false>, &cfg)) ==
+                          cudaSuccess;
         cfg.numAttrs = 2;
-        if (fits &&
-            max_clusters >= 1) {
-            return cudaLaunchKernelEx(&cfg, layout_cluster_kernel, p, plan.tokens_per_cta);
+        if (fits && max_clusters >= 1) {
+            if (expanded) return cudaLaunchKernelEx(&cfg, layout_cluster_kernel<true>, p, plan.tokens_per_cta);
+            return cudaLaunchKernelEx(&cfg, layout_cluster_kernel<false>, p, plan.tokens_per_cta);
         }
         cudaGetLastError();   // fall back to the tiled path
     }
