@@ -597,10 +597,11 @@ constexpr int64_t kClusterMaxTokenRanks = EP_LAYOUT_CLUSTER_MAX_TOKEN_RANKS;
 // [warps][E] counters stay small, else 8.
 __host__ __device__ inline int cluster_rank_warps(int E) { return E <= 512 ? 32 : kRankWarps; }
 
-size_t cluster_smem_words(int R, int E, int nodes, int W, int K, bool expanded) {
+size_t cluster_smem_words(int R, int E, int nodes, int W, int K, bool expanded, bool node_rows) {
     size_t w = 2 * static_cast<size_t>(R) * W + static_cast<size_t>(nodes) * W + R + E + nodes + (R + 1) + R +
                33 * static_cast<size_t>(W) + 64;
     if (expanded) w += 32 * static_cast<size_t>(W) * K + (1 + cluster_rank_warps(E)) * static_cast<size_t>(E);
+    if (node_rows) w += 2 * static_cast<size_t>(nodes) + 1 + static_cast<size_t>(W) * nodes;
     return w;
 }
 
@@ -654,9 +655,10 @@ __device__ int warp_exclusive_scan_smem(int* a, int n) {
     return __shfl_sync(0xffffffffu, incl, 31);
 }
 
-// kExpanded: also the expanded per-expert rows (a separate instantiation, so
-// the plain layout carries none of that work).
-template <bool kExpanded>
+// kExpanded: also the expanded per-expert rows; kNodeRows: also the node rows
+// of the hierarchical path (separate instantiations, so the plain layout
+// carries none of that work).
+template <bool kExpanded, bool kNodeRows>
 __global__ void __launch_bounds__(kClusterThreads, 1)
     layout_cluster_kernel(const LayoutParams p, int tokens_per_cta) {
     namespace cg = cooperative_groups;
@@ -682,9 +684,12 @@ __global__ void __launch_bounds__(kClusterThreads, 1)
     int* s_key = s_wtok + W;                                        // expanded: [32 W K] expert of each entry
     int* s_eb = s_key + (expanded ? 32 * W * p.K : 0);              // expanded: [E] expert bases
     int* s_wc = s_eb + (expanded ? E : 0);                          // expanded: [8][E] ranking counters
+    int* s_ntot = s_wc + (expanded ? cluster_rank_warps(E) * E : 0);  // node rows: [NN+1] totals -> node_offset
+    int* s_nbefore = s_ntot + (kNodeRows ? NN + 1 : 0);             // node rows: [NN] tokens of earlier CTAs
+    int* s_nwbase = s_nbefore + (kNodeRows ? NN : 0);               // node rows: [W][NN] earlier words
     __shared__ int s_rows_total;                                    // read by later CTAs
     __shared__ int s_cta_base;
-    __shared__ int s_totals[2];                                     // N, expert rows
+    __shared__ int s_totals[3];                                     // N, expert rows, node rows
     const int tid = threadIdx.x;
     const int t0 = me * tokens_per_cta;
     const int nt = max(0, min(tokens_per_cta, p.T - t0));
@@ -744,7 +749,10 @@ __global__ void __launch_bounds__(kClusterThreads, 1)
     }
     for (int n = tid; n < NN; n += kClusterThreads) {
         int c = 0;
-        for (int w = 0; w < W; ++w) c += __popc(s_bmn[w * NN + n]);
+        for (int w = 0; w < W; ++w) {
+            if (kNodeRows) s_nwbase[w * NN + n] = c;
+            c += __popc(s_bmn[w * NN + n]);
+        }
         s_ncnt[n] = c;
     }
     // Rows numbered token by token: one warp per 32-token word, lane = token.
@@ -822,7 +830,7 @@ __global__ void __launch_bounds__(kClusterThreads, 1)
             p.num_tokens_per_expert[e] = tot;
             s_hist[e] = (tot + p.alignment - 1) / p.alignment * p.alignment;
         }
-        for (int n = tid; n < NN; n += kClusterThreads) {
+        for (int n = tid; n < NN && !kNodeRows; n += kClusterThreads) {
             int v[kMaxClusterCtas];
 #pragma unroll
             for (int c = 0; c < kMaxClusterCtas; ++c) v[c] = c < C ? cluster.map_shared_rank(s_ncnt, c)[n] : 0;
@@ -830,6 +838,24 @@ __global__ void __launch_bounds__(kClusterThreads, 1)
 #pragma unroll
             for (int c = 0; c < kMaxClusterCtas; ++c) tot += v[c];
             p.num_tokens_per_node[n] = tot;
+        }
+    }
+    if (kNodeRows) {
+        // every CTA needs each node's total (for node_offset) and its tokens in
+        // earlier CTAs
+        for (int n = tid; n < NN; n += kClusterThreads) {
+            int v[kMaxClusterCtas];
+#pragma unroll
+            for (int c = 0; c < kMaxClusterCtas; ++c) v[c] = c < C ? cluster.map_shared_rank(s_ncnt, c)[n] : 0;
+            int tot = 0, before = 0;
+#pragma unroll
+            for (int c = 0; c < kMaxClusterCtas; ++c) {
+                tot += v[c];
+                if (c < me) before += v[c];
+            }
+            if (me == C - 1) p.num_tokens_per_node[n] = tot;
+            s_ntot[n] = tot;
+            s_nbefore[n] = before;
         }
     }
     __syncthreads();
@@ -856,6 +882,17 @@ __global__ void __launch_bounds__(kClusterThreads, 1)
             if (tid == 0) s_totals[1] = tot;
         }
     }
+    if (kNodeRows) {   // s_ntot becomes node_offset
+        if (NN <= kWarpScanMax) {
+            if (warp_id == 4) {
+                const int tot = warp_exclusive_scan_smem(s_ntot, NN);
+                if (lane == 0) s_totals[2] = tot;
+            }
+        } else {
+            const int tot = smem_exclusive_scan(s_ntot, NN, s_warp);
+            if (tid == 0) s_totals[2] = tot;
+        }
+    }
     __syncthreads();
     const int n_recv = s_totals[0];
     if (me == 0) {
@@ -865,6 +902,10 @@ __global__ void __launch_bounds__(kClusterThreads, 1)
     if (me == C - 1) {
         for (int e = tid; e < E; e += kClusterThreads) p.expert_offset[e] = s_escan[e];
         if (tid == 0) p.expert_offset[E] = s_totals[1];
+        if (kNodeRows) {
+            for (int n = tid; n < NN; n += kClusterThreads) p.node_offset[n] = s_ntot[n];
+            if (tid == 0) p.node_offset[NN] = s_totals[2];
+        }
     }
 
     // Phase 3: dst_row and is_token_in_rank of this CTA's [nt, R] block:
@@ -900,6 +941,22 @@ __global__ void __launch_bounds__(kClusterThreads, 1)
                 drow[j0 + u] = v[u];
                 inr[j0 + u] = static_cast<uint8_t>((in4 >> (8 * u)) & 1u);
             }
+        }
+    }
+
+    // Node rows of this CTA's [nt, nodes] block: node_offset + tokens of
+    // earlier CTAs + tokens of earlier words + popc below.
+    if (kNodeRows) {
+        int32_t* nrow = p.node_row + static_cast<int64_t>(t0) * NN;
+        for (int j = tid; j < nt * NN; j += kClusterThreads) {
+            const int tl = j / NN;
+            const int n = j - tl * NN;
+            const int w = tl >> 5;
+            const uint32_t word = s_bmn[w * NN + n];
+            const uint32_t b = static_cast<uint32_t>(tl & 31);
+            nrow[j] = ((word >> b) & 1u)
+                          ? s_ntot[n] + s_nbefore[n] + s_nwbase[w * NN + n] + __popc(word & ((1u << b) - 1u))
+                          : -1;
         }
     }
 
@@ -957,6 +1014,23 @@ struct ClusterPlan {
     size_t smem;
 };
 
+// Largest static shared memory of the cluster kernel instantiations so far.
+template <bool kX, bool kN>
+cudaError_t cluster_static_smem(int& bytes) {
+    cudaFuncAttributes fa{};
+    const cudaError_t e = cudaFuncGetAttributes(&fa, layout_cluster_kernel<kX, kN>);
+    if (e == cudaSuccess && static_cast<int>(fa.sharedSizeBytes) > bytes) bytes = static_cast<int>(fa.sharedSizeBytes);
+    return e;
+}
+
+template <bool kX, bool kN>
+bool configure_cluster(int smem_max) {
+    return cudaFuncSetAttribute(layout_cluster_kernel<kX, kN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                smem_max) == cudaSuccess &&
+           cudaFuncSetAttribute(layout_cluster_kernel<kX, kN>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) ==
+               cudaSuccess;
+}
+
 ClusterPlan plan_cluster(const LayoutParams& p, int smem_max) {
     ClusterPlan plan{0, 0, 0};
     // One CTA per 256 tokens up to 16; ranges are whole 32-token words.
@@ -968,7 +1042,8 @@ ClusterPlan plan_cluster(const LayoutParams& p, int smem_max) {
     if (tpc < 32) tpc = 32;
     ctas = (p.T + tpc - 1) / tpc;
     if (ctas < 1) ctas = 1;
-    const size_t smem = 4 * cluster_smem_words(p.R, p.E, p.num_nodes, tpc / 32, p.K, p.expanded_row != nullptr);
+    const size_t smem = 4 * cluster_smem_words(p.R, p.E, p.num_nodes, tpc / 32, p.K, p.expanded_row != nullptr,
+                                               p.node_row != nullptr);
     if (smem > static_cast<size_t>(smem_max)) return plan;
     // Large [T, R] outputs are written faster by the many-CTA path.
     if (static_cast<int64_t>(p.T) * p.R > kClusterMaxTokenRanks) return plan;
@@ -1014,31 +1089,21 @@ cudaError_t launch_layout(const LayoutParams& p, cudaStream_t stream) {
         e = cudaFuncSetAttribute(layout_rows_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  di.max_smem_optin - static_cast<int>(fa.sharedSizeBytes));
         if (e != cudaSuccess) return e;
-        cudaFuncAttributes fa0{}, fa1{};
-        e = cudaFuncGetAttributes(&fa0, layout_cluster_kernel<false>);
+        int static_smem = 0;
+        e = cluster_static_smem<false, false>(static_smem);
+        if (e == cudaSuccess) e = cluster_static_smem<true, false>(static_smem);
+        if (e == cudaSuccess) e = cluster_static_smem<false, true>(static_smem);
+        if (e == cudaSuccess) e = cluster_static_smem<true, true>(static_smem);
         if (e != cudaSuccess) return e;
-        e = cudaFuncGetAttributes(&fa1, layout_cluster_kernel<true>);
-        if (e != cudaSuccess) return e;
-        const int static_smem =
-            static_cast<int>(fa0.sharedSizeBytes > fa1.sharedSizeBytes ? fa0.sharedSizeBytes : fa1.sharedSizeBytes);
         cluster_smem_max = di.max_smem_optin - static_smem;
-        cluster_ok =
-            cudaFuncSetAttribute(layout_cluster_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 cluster_smem_max) == cudaSuccess &&
-            cudaFuncSetAttribute(layout_cluster_kernel<false>, cudaFuncAttributeNonPortableClusterSizeAllowed,
-                                 1) == cudaSuccess &&
-            cudaFuncSetAttribute(layout_cluster_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 cluster_smem_max) == cudaSuccess &&
-            cudaFuncSetAttribute(layout_cluster_kernel<true>, cudaFuncAttributeNonPortableClusterSizeAllowed,
-                                 1) == cudaSuccess;
+        cluster_ok = configure_cluster<false, false>(cluster_smem_max) &&
+                     configure_cluster<true, false>(cluster_smem_max) &&
+                     configure_cluster<false, true>(cluster_smem_max) && configure_cluster<true, true>(cluster_smem_max);
         cudaGetLastError();   // a refused attribute only disables the cluster path
         configured_device = di.device;
     }
 
-    // the node rows are produced by the tiled path only
-    const ClusterPlan plan = (cluster_ok && p.node_row == nullptr)
-                                 ? plan_cluster(p, cluster_smem_max)
-                                 : ClusterPlan{0, 0, 0};
+    const ClusterPlan plan = cluster_ok ? plan_cluster(p, cluster_smem_max) : ClusterPlan{0, 0, 0};
     if (plan.ctas > 0) {
         cudaLaunchConfig_t cfg = {};
         cudaLaunchAttribute attr[2];
@@ -1056,15 +1121,12 @@ cudaError_t launch_layout(const LayoutParams& p, cudaStream_t stream) {
         cfg.numAttrs = 2;
         int max_clusters = 0;
         cfg.numAttrs = 1;   // the occupancy query takes the cluster shape only
-        const bool expanded = p.expanded_row != nullptr;
-        const bool fits = (expanded ? cudaOccupancyMaxActiveClusters(&max_clusters, layout_cluster_kernel<true>, &cfg)
-                                    : cudaOccupancyMaxActiveClusters(&max_clusters, layout_cluster_kernel<false>, &cfg)) ==
-                          cudaSuccess;
+        const bool expanded = p.expanded_row != nullptr, nodes = p.node_row != nullptr;
+        auto kernel = expanded ? (nodes ? layout_cluster_kernel<true, true> : layout_cluster_kernel<true, false>)
+                               : (nodes ? layout_cluster_kernel<false, true> : layout_cluster_kernel<false, false>);
+        const bool fits = cudaOccupancyMaxActiveClusters(&max_clusters, kernel, &cfg) == cudaSuccess;
         cfg.numAttrs = 2;
-        if (fits && max_clusters >= 1) {
-            if (expanded) return cudaLaunchKernelEx(&cfg, layout_cluster_kernel<true>, p, plan.tokens_per_cta);
-            return cudaLaunchKernelEx(&cfg, layout_cluster_kernel<false>, p, plan.tokens_per_cta);
-        }
+        if (fits && max_clusters >= 1) return cudaLaunchKernelEx(&cfg, kernel, p, plan.tokens_per_cta);
         cudaGetLastError();   // fall back to the tiled path
     }
 
