@@ -417,6 +417,17 @@ __device__ __forceinline__ uint32_t pack_e4m3x4(float a, float b, float c, float
     return static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
 }
 
+// (a * m, b * m), each product rounded to nearest even as by a scalar
+// multiply, in one packed fp32x2 instruction.
+__device__ __forceinline__ float2 mul2_rn(float a, float b, uint64_t mm) {
+    uint64_t x, r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(x) : "f"(a), "f"(b));
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(x), "l"(mm));
+    float2 y;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(y.x), "=f"(y.y) : "l"(r));
+    return y;
+}
+
 constexpr int kFp8Threads = 256;
 constexpr int kFp8Rounds = 2;   // rounds of blocks per item (loads of every round issued first)
 
@@ -472,11 +483,20 @@ __device__ __forceinline__ void dispatch_fp8_item(const DispatchParams& p, int64
             write_metadata(p, t, lane, all);
         }
     }
+    // Many tokens (kLanes 8): codes and scales of every round first, then one
+    // pass over the destinations stores all of them (one shuffle and one row
+    // address per destination instead of one per round).  Few tokens (kLanes
+    // 16): each round is stored as soon as it is cast, which keeps the first
+    // stores early on the short, latency-bound grid.
+    constexpr bool kMerged = kLanes == 8;
+    const int b0 = b_begin + kBlocksPerWarp * warp_g + grp;   // this lane's block in round 0
+    uint32_t code[kFp8Rounds][2 * kVec];
+    float sfq[kFp8Rounds];
+    auto warp_has_round = [&](int q) { return b_begin + q * kBlocksPerRound + kBlocksPerWarp * warp_g < b_end; };
+    auto cast_round = [&](int q) {
+        sfq[q] = 1.0f;
 #pragma unroll
-    for (int q = 0; q < kFp8Rounds; ++q) {
-        const int b = b_begin + q * kBlocksPerRound + kBlocksPerWarp * warp_g + grp;
-        if (b_begin + q * kBlocksPerRound + kBlocksPerWarp * warp_g >= b_end) break;   // the warp has no block left
-        const bool valid = b < b_end;
+        for (int e = 0; e < 2 * kVec; ++e) code[q][e] = 0u;
         float f[8 * kVec];
 #pragma unroll
         for (int u = 0; u < kVec; ++u) {
@@ -492,37 +512,70 @@ __device__ __forceinline__ void dispatch_fp8_item(const DispatchParams& p, int64
         for (int e = 0; e < 8 * kVec; ++e) amax = fmaxf(amax, fabsf(f[e]));
 #pragma unroll
         for (int o = kLanes / 2; o >= 1; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-        float sf = 1.0f, mult = 0.0f;
+        float mult = 0.0f;
         if (amax > 0.0f) {
-            sf = __fdiv_rn(amax, 448.0f);
+            sfq[q] = __fdiv_rn(amax, 448.0f);
             mult = __fdiv_rn(448.0f, amax);
         }
-        uint32_t code[2 * kVec];
+        if (kMerged) {   // packed products: fewer instructions on the issue-heavy many-token grid
+            uint64_t mm;
+            asm("mov.b64 %0, {%1, %1};" : "=l"(mm) : "f"(mult));
 #pragma unroll
-        for (int e = 0; e < 2 * kVec; ++e)
-            code[e] = pack_e4m3x4(__fmul_rn(f[4 * e], mult), __fmul_rn(f[4 * e + 1], mult),
-                                  __fmul_rn(f[4 * e + 2], mult), __fmul_rn(f[4 * e + 3], mult));
-        const int64_t col = static_cast<int64_t>(b) * 128 + sub * (8 * kVec);
+            for (int e = 0; e < 2 * kVec; ++e) {
+                const float2 lo = mul2_rn(f[4 * e], f[4 * e + 1], mm);
+                const float2 hi = mul2_rn(f[4 * e + 2], f[4 * e + 3], mm);
+                code[q][e] = pack_e4m3x4(lo.x, lo.y, hi.x, hi.y);
+            }
+        } else {
+#pragma unroll
+            for (int e = 0; e < 2 * kVec; ++e)
+                code[q][e] = pack_e4m3x4(__fmul_rn(f[4 * e], mult), __fmul_rn(f[4 * e + 1], mult),
+                                         __fmul_rn(f[4 * e + 2], mult), __fmul_rn(f[4 * e + 3], mult));
+        }
+    };
+    const int sub_col = sub * (8 * kVec);
+    // stores rounds [q_lo, q_hi) to every destination
+    auto store_rounds = [&](int q_lo, int q_hi) {
         for (int rb = 0; rb < n_dst; rb += 32) {
             const int d = rb == 0 ? d0 : rb == 32 ? d1 : (rb + lane < n_dst ? drow[rb + lane] : -1);
-            if (d >= p.capacity && c == 0 && q == 0) cap_bad = true;
+            if (d >= p.capacity && c == 0 && q_lo == 0) cap_bad = true;
             unsigned m = __ballot_sync(0xffffffffu, d >= 0 && d < p.capacity);
             while (m) {
                 const int sl = __ffs(m) - 1;
                 m &= m - 1;
                 const int64_t dd = __shfl_sync(0xffffffffu, d, sl);
-                if (valid) {
-                    uint8_t* dst = p.recv_x + dd * p.H + col;
-                    if (kVec == 2)
-                        st_v4(dst, make_uint4(code[0], code[1], code[2 % (2 * kVec)], code[3 % (2 * kVec)]));
-                    else
-                        *reinterpret_cast<uint2*>(dst) = make_uint2(code[0], code[1]);
-                    if (sub == 0 && p.recv_sf) {
-                        const int64_t si = p.sf_col_major ? static_cast<int64_t>(b) * p.sf_stride + dd : dd * nb + b;
-                        p.recv_sf[si] = sf;
+                uint8_t* row = p.recv_x + dd * p.H + sub_col;
+#pragma unroll
+                for (int q = 0; q < kFp8Rounds; ++q) {
+                    const int b = b0 + q * kBlocksPerRound;
+                    if (q >= q_lo && q < q_hi && b < b_end) {
+                        uint8_t* dst = row + static_cast<int64_t>(b) * 128;
+                        if (kVec == 2)
+                            st_v4(dst, make_uint4(code[q][0], code[q][1], code[q][2 % (2 * kVec)],
+                                                  code[q][3 % (2 * kVec)]));
+                        else
+                            *reinterpret_cast<uint2*>(dst) = make_uint2(code[q][0], code[q][1]);
+                        if (sub == 0 && p.recv_sf) {
+                            const int64_t si =
+                                p.sf_col_major ? static_cast<int64_t>(b) * p.sf_stride + dd : dd * nb + b;
+                            p.recv_sf[si] = sfq[q];
+                        }
                     }
                 }
             }
+        }
+    };
+    if (kMerged) {
+#pragma unroll
+        for (int q = 0; q < kFp8Rounds; ++q)
+            if (warp_has_round(q)) cast_round(q);   // warp-uniform
+        store_rounds(0, kFp8Rounds);
+    } else {
+#pragma unroll
+        for (int q = 0; q < kFp8Rounds; ++q) {
+            if (!warp_has_round(q)) break;   // warp-uniform
+            cast_round(q);
+            store_rounds(q, q + 1);
         }
     }
 }

@@ -136,6 +136,43 @@ def test_dispatch_fp8_special_blocks():
     np.testing.assert_array_equal(sf, o["recv_sf"])
 
 
+def _every_amax_x(T, H, seed):
+    """bf16 rows whose 128-channel blocks take, in order, every finite bf16
+    magnitude 0x0000..0x7f7f as their amax (at a random channel, random sign);
+    the block's other channels are random magnitudes up to it."""
+    rng = np.random.default_rng(seed)
+    nb = H // 128
+    amax = np.arange(0x7F80, dtype=np.int64)
+    blocks = np.zeros((T * nb, 128), np.int64)
+    n = min(len(amax), T * nb)
+    blocks[:n] = (rng.random((n, 128)) * (amax[:n, None] + 1)).astype(np.int64)
+    pos = rng.integers(0, 128, n)
+    blocks[np.arange(n), pos] = amax[:n]
+    blocks |= rng.integers(0, 2, blocks.shape) << 15
+    return blocks.reshape(T, H).astype(np.uint16)
+
+
+@pytest.mark.parametrize("H,many_tokens", [(2048, True), (7168, False)])
+def test_dispatch_fp8_every_amax(H, many_tokens):
+    """Codes and scales bit-exact for blocks covering every finite bf16 amax,
+    in the many-token mode (8 lanes per block) and the few-token mode (16)."""
+    nb = H // 128
+    T = (0x7F80 + nb - 1) // nb
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    assert (T >= 8 * sms) == many_tokens
+    E, K, R = 64, 4, 8
+    d = make_inputs(T, H, E, K, R, seed=40 + nb)
+    d["x_bits"] = _every_amax_x(T, H, seed=41 + nb)
+    lay, res, n, _, _ = _run(d, E, R, fp8=True)
+    assert int(res["status"].item()) == 0
+    g = _host(res, True, n)
+    L = oracle.layout(d["topk_idx"], E, R)
+    o = oracle.dispatch(d["x_bits"], d["topk_idx"], d["topk_weights"], E, R, L.dst_row, fp8=True)
+    np.testing.assert_array_equal(g["recv_x"], o["recv_x"])
+    sf = res["recv_sf"].cpu().numpy()[:n * nb].reshape(n, -1)
+    np.testing.assert_array_equal(sf, o["recv_sf"])
+
+
 def test_dispatch_capacity_overflow():
     T, H, E, K, R = 400, 512, 64, 4, 8
     d = make_inputs(T, H, E, K, R, seed=12)
