@@ -63,6 +63,9 @@ namespace {
 #ifndef EP_DISPATCH_FP8_MIN_BLOCKS
 #define EP_DISPATCH_FP8_MIN_BLOCKS 4      // FP8 path: __launch_bounds__ minimum resident CTAs per SM
 #endif
+#ifndef EP_DISPATCH_FP8_WIDE_MIN_BLOCKS
+#define EP_DISPATCH_FP8_WIDE_MIN_BLOCKS 5   // same, many-token rank-row mode (fits 48 registers unspilled)
+#endif
 #ifndef EP_DISPATCH_FP8_PIECE_BLOCKS
 #define EP_DISPATCH_FP8_PIECE_BLOCKS 64   // FP8 path: 128-channel blocks per piece (<= 64)
 #endif
@@ -582,8 +585,14 @@ __device__ __forceinline__ void dispatch_fp8_item(const DispatchParams& p, int64
 
 // kGroups == 1: one CTA per item.  kGroups > 1 (SM-limited mode): several
 // independent groups per CTA, each looping over items with a stride.
+// The many-token rank-row instantiation runs 5 CTAs per SM (more loads in
+// flight; 4 for the few-token and expanded ones, which the cap would slow or
+// spill).
 template <bool kExpanded, int kGroups, int kLanes>
-__global__ void __launch_bounds__(kFp8Threads * kGroups, kGroups == 1 ? EP_DISPATCH_FP8_MIN_BLOCKS : 1)
+__global__ void __launch_bounds__(kFp8Threads * kGroups,
+                                  kGroups > 1 ? 1
+                                  : (kLanes == 8 && !kExpanded) ? EP_DISPATCH_FP8_WIDE_MIN_BLOCKS
+                                                                : EP_DISPATCH_FP8_MIN_BLOCKS)
     dispatch_fp8_kernel(const DispatchParams p) {
     const int gtid = static_cast<int>(threadIdx.x) % kFp8Threads;
     const int lane = threadIdx.x & 31;
