@@ -41,6 +41,12 @@ constexpr int kBatch = EP_COMBINE_BATCH;
 #ifndef EP_COMBINE_SM_BATCH
 #define EP_COMBINE_SM_BATCH 8        // SM-limited mode: rows of loads in flight per thread
 #endif
+#ifndef EP_COMBINE_FEW_BATCH
+#define EP_COMBINE_FEW_BATCH 8       // few tokens: rows of loads in flight per thread
+#endif
+#ifndef EP_COMBINE_FEW_MIN_BLOCKS
+#define EP_COMBINE_FEW_MIN_BLOCKS 6  // few tokens: minimum resident CTAs per SM (78 registers, unspilled)
+#endif
 
 // SM-limited mode: CTAs of kSmGroups x kThreads threads, one per SM, each
 // group looping over (token, piece) items.
@@ -48,8 +54,9 @@ constexpr int kSmGroups = 8;
 
 // One (token, piece) item, by one group of kThreads threads.  kExpanded: the
 // token's source rows are its expanded rows (one per valid top-k slot,
-// coefficient = that slot's weight) instead of one row per rank.
-template <bool kWeighted, bool kExpanded, int kGroups>
+// coefficient = that slot's weight) instead of one row per rank.  kB: source
+// rows of loads in flight per thread.
+template <bool kWeighted, bool kExpanded, int kGroups, int kB>
 __device__ __forceinline__ void combine_item(const CombineParams& p, int64_t it, int group, int gtid,
                                              int* s_rows, float* s_coef, int* s_n) {
     const int t = static_cast<int>(it / p.chunks);
@@ -115,7 +122,6 @@ __device__ __forceinline__ void combine_item(const CombineParams& p, int64_t it,
 #pragma unroll
         for (int q = 0; q < 8; ++q) acc[q] = 0.0f;
         const int64_t off = static_cast<int64_t>(v) * 16;
-        constexpr int kB = kGroups == 1 ? kBatch : EP_COMBINE_SM_BATCH;
         for (int m0 = 0; m0 < n; m0 += kB) {
             uint4 buf[kB];
 #pragma unroll
@@ -155,17 +161,19 @@ __device__ __forceinline__ void combine_item(const CombineParams& p, int64_t it,
 
 // kGroups == 1: one CTA per item.  kGroups > 1 (SM-limited mode): several
 // groups per CTA, each looping over items with a stride and synchronising on
-// its own named barrier.
-template <bool kWeighted, bool kExpanded, int kGroups>
-__global__ void __launch_bounds__(kThreads * kGroups, kGroups == 1 ? EP_COMBINE_MIN_BLOCKS : 1)
+// its own named barrier.  kB > kBatch with kGroups == 1: the few-token grid,
+// where one round trip for all of a token's rows matters more than occupancy.
+template <bool kWeighted, bool kExpanded, int kGroups, int kB>
+__global__ void __launch_bounds__(kThreads * kGroups,
+                                  kGroups > 1 ? 1 : (kB > kBatch ? EP_COMBINE_FEW_MIN_BLOCKS : EP_COMBINE_MIN_BLOCKS))
     combine_kernel(const CombineParams p) {
     __shared__ int s_rows_all[kGroups][EP_MAX_TOPK];
     __shared__ float s_coef_all[kGroups][EP_MAX_TOPK];
     __shared__ int s_n_all[kGroups];
     pdl_wait();
     if (kGroups == 1) {
-        combine_item<kWeighted, kExpanded, 1>(p, blockIdx.x, 0, threadIdx.x, s_rows_all[0], s_coef_all[0],
-                                               &s_n_all[0]);
+        combine_item<kWeighted, kExpanded, 1, kB>(p, blockIdx.x, 0, threadIdx.x, s_rows_all[0], s_coef_all[0],
+                                                  &s_n_all[0]);
     } else {
         const int group = static_cast<int>(threadIdx.x) / kThreads;
         const int gtid = static_cast<int>(threadIdx.x) % kThreads;
@@ -173,22 +181,25 @@ __global__ void __launch_bounds__(kThreads * kGroups, kGroups == 1 ? EP_COMBINE_
         for (int64_t it = static_cast<int64_t>(blockIdx.x) * kGroups + group; it < n_items;
              it += static_cast<int64_t>(gridDim.x) * kGroups) {
             named_barrier(1 + group, kThreads);   // the previous item's list is consumed
-            combine_item<kWeighted, kExpanded, kGroups>(p, it, group, gtid, s_rows_all[group], s_coef_all[group],
-                                                        &s_n_all[group]);
+            combine_item<kWeighted, kExpanded, kGroups, kB>(p, it, group, gtid, s_rows_all[group],
+                                                            s_coef_all[group], &s_n_all[group]);
         }
     }
 }
 
 template <bool kWeighted, bool kExpanded>
-cudaError_t launch_combine_t(const CombineParams& p, int64_t items, int num_sms, cudaStream_t stream) {
+cudaError_t launch_combine_t(const CombineParams& p, int64_t items, int num_sms, bool few, cudaStream_t stream) {
     if (num_sms > 0) {
         int64_t grid = (items + kSmGroups - 1) / kSmGroups;
         if (grid > num_sms) grid = num_sms;
-        return launch_pdl(combine_kernel<kWeighted, kExpanded, kSmGroups>, dim3(static_cast<unsigned>(grid)),
-                          dim3(kThreads * kSmGroups), 0, stream, p);
+        return launch_pdl(combine_kernel<kWeighted, kExpanded, kSmGroups, EP_COMBINE_SM_BATCH>,
+                          dim3(static_cast<unsigned>(grid)), dim3(kThreads * kSmGroups), 0, stream, p);
     }
-    return launch_pdl(combine_kernel<kWeighted, kExpanded, 1>, dim3(static_cast<unsigned>(items)), dim3(kThreads), 0,
-                      stream, p);
+    if (few)
+        return launch_pdl(combine_kernel<kWeighted, kExpanded, 1, EP_COMBINE_FEW_BATCH>,
+                          dim3(static_cast<unsigned>(items)), dim3(kThreads), 0, stream, p);
+    return launch_pdl(combine_kernel<kWeighted, kExpanded, 1, kBatch>, dim3(static_cast<unsigned>(items)),
+                      dim3(kThreads), 0, stream, p);
 }
 
 }  // namespace
@@ -199,7 +210,8 @@ cudaError_t launch_combine(CombineParams p, bool weighted, cudaStream_t stream) 
     // Pieces of up to 2 vectors per thread; more pieces when there are few tokens.
     int chunks = (n_vec + 2 * kThreads - 1) / (2 * kThreads);
     const int want_items = 4 * di.num_sms;
-    if (p.T > 0 && static_cast<int64_t>(p.T) * chunks < want_items) {
+    const bool few = p.T > 0 && static_cast<int64_t>(p.T) * chunks < want_items;
+    if (few) {
         // few tokens: latency-bound, so at most one vector per thread (each
         // CTA then waits for one batch of row loads per 4 rows, not two)
         int more = (want_items + p.T - 1) / p.T;
@@ -217,11 +229,11 @@ cudaError_t launch_combine(CombineParams p, bool weighted, cudaStream_t stream) 
     if (items < 1) return cudaSuccess;
     const int num_sms = p.num_sms > 0 ? (p.num_sms < di.num_sms ? p.num_sms : di.num_sms) : 0;
     if (p.expanded_row) {
-        if (weighted) return launch_combine_t<true, true>(p, items, num_sms, stream);
-        return launch_combine_t<false, true>(p, items, num_sms, stream);
+        if (weighted) return launch_combine_t<true, true>(p, items, num_sms, few, stream);
+        return launch_combine_t<false, true>(p, items, num_sms, few, stream);
     }
-    if (weighted) return launch_combine_t<true, false>(p, items, num_sms, stream);
-    return launch_combine_t<false, false>(p, items, num_sms, stream);
+    if (weighted) return launch_combine_t<true, false>(p, items, num_sms, few, stream);
+    return launch_combine_t<false, false>(p, items, num_sms, few, stream);
 }
 
 }  // namespace epg
