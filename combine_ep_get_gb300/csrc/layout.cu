@@ -1014,6 +1014,199 @@ struct ClusterPlan {
     size_t smem;
 };
 
+// Few tokens (T <= 1024, R <= 32, K <= 16, no expanded or node rows): one CTA
+// of 1024 threads and no cluster.  Every phase is spread over all 32 warps,
+// whatever T: the top-k entries one per thread (shared atomics build the
+// [word][rank] bitmaps and the expert histogram), one warp per rank for its
+// prefix over words and one per word for its tokens' rows, then (token, rank)
+// quads of dst_row and is_token_in_rank per thread.  Three block barriers, no
+// cluster barrier and no remote read.
+#ifndef EP_LAYOUT_SMALL_MAX_TOKENS
+#define EP_LAYOUT_SMALL_MAX_TOKENS 1024   // 0 disables the single-CTA path
+#endif
+constexpr int kSmallMaxTokens = EP_LAYOUT_SMALL_MAX_TOKENS <= 1024 ? EP_LAYOUT_SMALL_MAX_TOKENS : 1024;
+constexpr int kSmallMaxRanks = 32;
+constexpr int kSmallMaxTopk = 16;
+constexpr int kSmallEntries = kSmallMaxTopk;   // entries per thread: <= 1024 tokens x 16 over 1024 threads
+
+__global__ void __launch_bounds__(1024, 1) layout_small_kernel(const LayoutParams p) {
+    __shared__ uint32_t s_bm[32][kSmallMaxRanks + 1];    // [word][rank] membership
+    __shared__ int s_base[32][kSmallMaxRanks + 1];       // [word][rank] rows in earlier words
+    __shared__ uint32_t s_bmn[32][kSmallMaxRanks + 1];   // [word][node] membership
+    __shared__ int s_tot[kSmallMaxRanks];                // rows of each rank
+    __shared__ int s_ntok[1024];                         // token's row within its word
+    __shared__ int s_wtok[32];                           // rows of each word
+    __shared__ int s_echunk[64];                         // aligned rows of each 32-expert chunk
+    __shared__ int s_bad;
+    extern __shared__ int s_hist[];                      // [E] entries per expert
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int T = p.T, K = p.K, E = p.E, R = p.R, NN = p.num_nodes;
+    const int W = (T + 31) >> 5;
+    const int n_ent = T * K;
+    pdl_wait();
+    pdl_launch_dependents();
+
+    // this thread's top-k entries, in flight while shared memory is cleared
+    int64_t v[kSmallEntries];
+#pragma unroll
+    for (int u = 0; u < kSmallEntries; ++u) {
+        const int i = u * 1024 + tid;
+        v[u] = i < n_ent ? p.topk_idx[i] : -1;
+    }
+    for (int i = tid; i < 32 * (kSmallMaxRanks + 1); i += 1024) {
+        (&s_bm[0][0])[i] = 0u;
+        (&s_bmn[0][0])[i] = 0u;
+    }
+    for (int i = tid; i < E; i += 1024) s_hist[i] = 0;
+    if (tid == 0) s_bad = 0;
+    __syncthreads();
+
+    // Phase 1: bitmaps and expert histogram.
+    bool bad = false;
+#pragma unroll
+    for (int u = 0; u < kSmallEntries; ++u) {
+        const int64_t e = v[u];
+        if (e == -1) continue;
+        if (e < -1 || e >= E) {
+            bad = true;
+            continue;
+        }
+        const int tk = (u * 1024 + tid) / K;
+        const int r = static_cast<int>(e) / p.experts_per_rank;
+        const uint32_t bit = 1u << (tk & 31);
+        atomicAdd(&s_hist[e], 1);
+        atomicOr(&s_bm[tk >> 5][r], bit);
+        if (NN) atomicOr(&s_bmn[tk >> 5][r / p.ranks_per_node], bit);
+    }
+    if (bad) s_bad = 1;
+    __syncthreads();
+
+    // Phase 2: warp r scans rank r over the words (and fills column r of
+    // src_dst_count), warp n totals node n, warp w numbers word w's tokens,
+    // and warp c scans the aligned counts of experts [32c, 32c + 32).
+    if (warp < R) {
+        const int r = warp;
+        const int c = lane < W ? __popc(s_bm[lane][r]) : 0;
+        const int incl = warp_inclusive_scan(c);
+        if (lane < W) s_base[lane][r] = incl - c;
+        if (lane == 31) {
+            s_tot[r] = incl;
+            p.num_tokens_per_rank[r] = incl;
+        }
+        if (p.src_dst_count && lane < R) {   // src_dst_count[s][r], s = lane (R | T)
+            const int ts = T / R;
+            const int a = lane * ts, b = a + ts;
+            int cnt = 0;
+            for (int w = a >> 5; w < W && w * 32 < b; ++w) {
+                const int lo = max(a - w * 32, 0), hi = min(b - w * 32, 32);
+                const uint32_t upper = hi >= 32 ? 0xffffffffu : ((1u << hi) - 1u);
+                cnt += __popc(s_bm[w][r] & upper & ~((1u << lo) - 1u));
+            }
+            p.src_dst_count[lane * R + r] = cnt;
+        }
+    }
+    if (warp < NN) {
+        const int c = lane < W ? __popc(s_bmn[lane][warp]) : 0;
+        const int tot = static_cast<int>(__reduce_add_sync(0xffffffffu, static_cast<unsigned>(c)));
+        if (lane == 0) p.num_tokens_per_node[warp] = tot;
+    }
+    if (warp < W) {
+        int n = 0;
+        for (int r = 0; r < R; ++r) n += (s_bm[warp][r] >> lane) & 1u;
+        const int incl = warp_inclusive_scan(n);
+        s_ntok[warp * 32 + lane] = incl - n;
+        if (lane == 31) s_wtok[warp] = incl;
+    }
+    const int n_chunks = (E + 31) >> 5;   // <= 64
+    for (int c = warp; c < n_chunks; c += 32) {
+        const int e = c * 32 + lane;
+        const int cnt = e < E ? s_hist[e] : 0;
+        if (e < E) p.num_tokens_per_expert[e] = cnt;
+        const int al = (cnt + p.alignment - 1) / p.alignment * p.alignment;
+        const int incl = warp_inclusive_scan(al);
+        if (e < E) s_hist[e] = incl - al;   // exclusive within the chunk
+        if (lane == 31) s_echunk[c] = incl;
+    }
+    __syncthreads();
+
+    // Phase 3: every warp forms rank_offset (lane r) and the words' row bases
+    // (lane w) by shuffles, then writes (token, rank) quads and token offsets.
+    const int tv = lane < R ? s_tot[lane] : 0;
+    const int tincl = warp_inclusive_scan(tv);
+    const int ro = tincl - tv;
+    const int n_recv = __shfl_sync(0xffffffffu, tincl, 31);
+    const int wv = lane < W ? s_wtok[lane] : 0;
+    const int wincl = warp_inclusive_scan(wv);
+    const int wbase = wincl - wv;
+    // expert offsets: chunk bases (chunks lane and 32 + lane) + row within the chunk
+    if (warp < n_chunks) {
+        const int c0 = lane < n_chunks ? s_echunk[lane] : 0;
+        const int c1 = 32 + lane < n_chunks ? s_echunk[32 + lane] : 0;
+        const int i0 = warp_inclusive_scan(c0);
+        const int t0 = __shfl_sync(0xffffffffu, i0, 31);
+        const int i1 = warp_inclusive_scan(c1);
+        for (int c = warp; c < n_chunks; c += 32) {   // warp-uniform
+            const int base = c < 32 ? __shfl_sync(0xffffffffu, i0 - c0, c)
+                                    : t0 + __shfl_sync(0xffffffffu, i1 - c1, c - 32);
+            const int e = c * 32 + lane;
+            if (e < E) p.expert_offset[e] = base + s_hist[e];
+        }
+        const int t1 = __shfl_sync(0xffffffffu, i1, 31);
+        if (warp == 0 && lane == 0) p.expert_offset[E] = t0 + t1;
+    }
+    if (warp == 0) {
+        if (lane < R) p.rank_offset[lane] = ro;
+        if (lane == 0) {
+            p.rank_offset[R] = n_recv;
+            if (p.token_offset) p.token_offset[T] = n_recv;
+            if (s_bad) atomicOr(p.status, EP_ERR_INVALID_INDEX);
+        }
+    }
+    if (p.token_offset) {
+        for (int t0 = warp * 32; t0 < T; t0 += 1024) {   // warp-uniform
+            const int base = __shfl_sync(0xffffffffu, wbase, (t0 >> 5) & 31);
+            if (t0 + lane < T) p.token_offset[t0 + lane] = base + s_ntok[t0 + lane];
+        }
+    }
+    const int n_el = T * R;
+    // j / R as a multiply-high: m = ceil(2^32 / R) is exact for j < 2^27
+    const uint32_t m_r = R > 1 ? 0xffffffffu / static_cast<uint32_t>(R) + 1u : 0u;
+    for (int q0 = warp * 128; q0 < n_el; q0 += 4096) {   // warp-uniform; 4 outputs per lane
+        const int j0 = q0 + lane * 4;
+        int tl = R > 1 ? static_cast<int>(__umulhi(static_cast<uint32_t>(j0), m_r)) : j0;
+        int r = j0 - tl * R;
+        int d[4];
+        uint32_t in4 = 0;
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int ror = __shfl_sync(0xffffffffu, ro, r & 31);
+            d[u] = -1;
+            if (j0 + u < n_el) {
+                const int w = tl >> 5;
+                const uint32_t word = s_bm[w][r];
+                const uint32_t b = static_cast<uint32_t>(tl & 31);
+                if ((word >> b) & 1u) {
+                    d[u] = ror + s_base[w][r] + __popc(word & ((1u << b) - 1u));
+                    in4 |= 1u << (8 * u);
+                }
+            }
+            if (++r == R) {
+                r = 0;
+                ++tl;
+            }
+        }
+        if (j0 + 4 <= n_el) {
+            *reinterpret_cast<int4*>(p.dst_row + j0) = make_int4(d[0], d[1], d[2], d[3]);
+            *reinterpret_cast<uint32_t*>(p.is_token_in_rank + j0) = in4;
+        } else {
+            for (int u = 0; u < 4 && j0 + u < n_el; ++u) {
+                p.dst_row[j0 + u] = d[u];
+                p.is_token_in_rank[j0 + u] = static_cast<uint8_t>((in4 >> (8 * u)) & 1u);
+            }
+        }
+    }
+}
+
 // Largest static shared memory of the cluster kernel instantiations so far.
 template <bool kX, bool kN>
 cudaError_t cluster_static_smem(int& bytes) {
@@ -1102,6 +1295,10 @@ cudaError_t launch_layout(const LayoutParams& p, cudaStream_t stream) {
         cudaGetLastError();   // a refused attribute only disables the cluster path
         configured_device = di.device;
     }
+
+    if (p.T <= kSmallMaxTokens && p.R <= kSmallMaxRanks && p.K <= kSmallMaxTopk && p.expanded_row == nullptr &&
+        p.node_row == nullptr)
+        return launch_pdl(layout_small_kernel, dim3(1), dim3(1024), static_cast<size_t>(p.E) * sizeof(int), stream, p);
 
     const ClusterPlan plan = cluster_ok ? plan_cluster(p, cluster_smem_max) : ClusterPlan{0, 0, 0};
     if (plan.ctas > 0) {

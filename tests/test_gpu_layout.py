@@ -47,6 +47,14 @@ def test_layout_workloads_full_size(name):
     (4096, 8, 2048, 1024, 0, 1, 0.0),     # many (token, rank) outputs: tiled path
     (32768, 8, 256, 128, 16, 1, 0.01),    # tiled path with node and source counts
     (9000, 8, 256, 256, 32, 3, 0.0),      # tiled path, ragged last tile
+    # single-CTA path (T <= 1024, R <= 32, K <= 16) at and around its limits
+    (1024, 16, 512, 32, 8, 1, 0.1),       # 32 words x 32 ranks, K = 16
+    (1025, 8, 256, 32, 0, 1, 0.0),        # one token over: cluster path
+    (1000, 17, 256, 8, 0, 1, 0.0),        # K = 17: cluster path
+    (200, 5, 30, 3, 0, 1, 0.1),           # R = 3: byte-wise rows of is_token_in_rank
+    (96, 8, 256, 32, 32, 1, 0.0),         # one node; source ranks of 3 tokens cross words
+    (33, 8, 64, 32, 1, 2, 0.0),           # 32 nodes of one rank, ragged second word
+    (500, 8, 2048, 32, 4, 5, 0.05),       # 64 expert chunks, alignment 5
 ])
 def test_layout_shapes(T, K, E, R, rpn, align, mask):
     idx = make_inputs(T, 8, E, K, R, seed=T + K + E + R, mask_frac=mask, with_x=False)["topk_idx"]
