@@ -63,6 +63,9 @@ namespace {
 #ifndef EP_DISPATCH_FP8_MIN_BLOCKS
 #define EP_DISPATCH_FP8_MIN_BLOCKS 4      // FP8 path: __launch_bounds__ minimum resident CTAs per SM
 #endif
+#ifndef EP_DISPATCH_PREFETCH
+#define EP_DISPATCH_PREFETCH 2   // x pieces a CTA of the first wave prefetches into L2 before its wait
+#endif
 #ifndef EP_DISPATCH_FP8_WIDE_MIN_BLOCKS
 #define EP_DISPATCH_FP8_WIDE_MIN_BLOCKS 5   // same, many-token rank-row mode (fits 48 registers unspilled)
 #endif
@@ -309,6 +312,31 @@ __device__ __forceinline__ void write_expanded_metadata(const DispatchParams& p,
     if (p.recv_weight) p.recv_weight[d] = p.topk_weights[static_cast<int64_t>(t) * p.K + lane];
 }
 
+// Before waiting on the previous kernel (normally the layout, which leaves
+// HBM idle for several microseconds), thread 0 of a first-wave CTA asks L2 to
+// fetch the x pieces of its own item and of the items that will follow on
+// the same slot (b + j * prefetch_ctas).  A prefetch only fills L2, the
+// coherence point, and x is still read after the wait, so a producer of x
+// that is still running cannot make the kernel read stale data.
+__device__ __forceinline__ void prefetch_l2(const void* ptr, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(ptr), "r"(bytes) : "memory");
+}
+
+template <bool kFp8>
+__device__ __forceinline__ void prefetch_x(const DispatchParams& p) {
+    if (threadIdx.x != 0 || static_cast<int>(blockIdx.x) >= p.prefetch_ctas) return;
+    const uint32_t row_bytes = static_cast<uint32_t>(p.H) * 2u;
+    const uint32_t piece = kFp8 ? static_cast<uint32_t>(p.chunk_blocks) * 256u : p.chunk_bytes;
+    const int64_t n_items = static_cast<int64_t>(p.T) * p.chunks;
+    for (int j = 0; j < p.prefetch_items; ++j) {
+        const int64_t it = static_cast<int64_t>(blockIdx.x) + static_cast<int64_t>(j) * p.prefetch_ctas;
+        if (it >= n_items) return;
+        const int t = static_cast<int>(it / p.chunks);
+        const uint32_t off = static_cast<uint32_t>(it - static_cast<int64_t>(t) * p.chunks) * piece;
+        prefetch_l2(p.x + static_cast<int64_t>(t) * row_bytes + off, min(piece, row_bytes - off));
+    }
+}
+
 constexpr int kRegThreads = 256;
 constexpr int kRegUnroll = 4;
 
@@ -399,7 +427,8 @@ __global__ void __launch_bounds__(kRegThreads * kGroups, kGroups == 1 ? 6 : 1)
     const int warp_g = gtid >> 5;   // warp within the group
     const int lane = threadIdx.x & 31;
     bool cap_bad = false;
-    pdl_wait();   // before any global access: the previous kernel may write x
+    if (kGroups == 1) prefetch_x<false>(p);
+    pdl_wait();   // before any load: the previous kernel may write x
     if (kGroups == 1) {
         dispatch_regs_item<kExpanded>(p, blockIdx.x, gtid, warp_g, lane, cap_bad);
     } else {
@@ -597,7 +626,8 @@ __global__ void __launch_bounds__(kFp8Threads * kGroups,
     const int gtid = static_cast<int>(threadIdx.x) % kFp8Threads;
     const int lane = threadIdx.x & 31;
     bool cap_bad = false;
-    pdl_wait();   // before any global access: the previous kernel may write x
+    if (kGroups == 1) prefetch_x<true>(p);
+    pdl_wait();   // before any load: the previous kernel may write x
     if (kGroups == 1) {
         dispatch_fp8_item<kExpanded, kLanes>(p, blockIdx.x, gtid, lane, cap_bad);
     } else {
@@ -691,6 +721,8 @@ cudaError_t launch_dispatch_bf16(DispatchParams p, cudaStream_t stream) {
             return launch_pdl(dispatch_bf16_regs_kernel<true, kSmGroups>, grid, block, 0, stream, p);
         }
         const dim3 grid(static_cast<unsigned>(items)), block(kRegThreads);
+        p.prefetch_ctas = di.num_sms * 6;   // the first wave (6 CTAs per SM)
+        p.prefetch_items = EP_DISPATCH_PREFETCH;
         if (p.expanded_row) return launch_pdl(dispatch_bf16_regs_kernel<true, 1>, grid, block, 0, stream, p);
         return launch_pdl(dispatch_bf16_regs_kernel<false, 1>, grid, block, 0, stream, p);
     }
@@ -708,6 +740,9 @@ cudaError_t launch_dispatch_fp8_t(DispatchParams p, int num_sms, cudaStream_t st
         return launch_pdl(dispatch_fp8_kernel<false, kSmGroups, kLanes>, grid, block, 0, stream, p);
     }
     const dim3 grid(static_cast<unsigned>(items)), block(kFp8Threads);
+    p.prefetch_ctas = device_info().num_sms * ((kLanes == 8 && !p.expanded_row) ? EP_DISPATCH_FP8_WIDE_MIN_BLOCKS
+                                                                              : EP_DISPATCH_FP8_MIN_BLOCKS);
+    p.prefetch_items = EP_DISPATCH_PREFETCH;
     if (p.expanded_row) return launch_pdl(dispatch_fp8_kernel<true, 1, kLanes>, grid, block, 0, stream, p);
     return launch_pdl(dispatch_fp8_kernel<false, 1, kLanes>, grid, block, 0, stream, p);
 }

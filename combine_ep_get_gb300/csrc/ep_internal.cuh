@@ -65,6 +65,11 @@ struct DispatchParams {
     int chunks;
     uint32_t chunk_bytes;   // bf16 path: bytes per piece (multiple of 16)
     int chunk_blocks;       // fp8 path: 128-channel blocks per piece
+    // L2 prefetch of x before the wait on the previous kernel: CTA b <
+    // prefetch_ctas prefetches the pieces of items b + j * prefetch_ctas,
+    // j < prefetch_items (0: none)
+    int prefetch_ctas;
+    int prefetch_items;
 };
 
 struct CombineParams {
