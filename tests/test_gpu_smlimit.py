@@ -83,6 +83,38 @@ def test_combine_sm_limited_matches_default(expanded, weighted, num_sms):
     assert torch.equal(outs[0], outs[1])
 
 
+@pytest.mark.parametrize("T,H,E,K,R,num_sms", [
+    (300, 7168, 256, 32, 64, 5),    # 32 rows per item: 1 KB pieces
+    (257, 4104, 64, 4, 16, 3),      # 8 KB pieces, a 16-byte last piece
+    (40, 16, 8, 2, 4, 2),           # rows shorter than a piece
+])
+def test_combine_ring_shapes_and_empty_tokens(T, H, E, K, R, num_sms):
+    """The SM-limited combine (shared-memory ring) against the oracle, with
+    tokens whose entries are all masked (items without source rows)."""
+    from gpu_path import B, bf16_bits, combine_tolerance, to_dev, x_tensor
+    d = make_inputs(T, H, E, K, R, seed=T + K, mask_frac=0.1, with_x=False)
+    d["topk_idx"][[0, T // 2, T - 1]] = -1
+    idx, w = to_dev(d["topk_idx"]), to_dev(d["topk_weights"])
+    lay = B.alloc_layout(T, E, R)
+    ws = torch.empty(B.ep_layout_workspace_bytes(T, K, E, R, 0), dtype=torch.uint8, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    B.ep_get_layout(idx, E, R, lay, ws, st)
+    n = lay.num_recv
+    y_bits = make_rows(n, H, seed=T + 1)
+    L = oracle.layout(d["topk_idx"], E, R)
+    for weighted in (False, True):
+        out = torch.full((T, H), 3.0, dtype=torch.bfloat16, device="cuda")
+        st.zero_()
+        B.ep_combine(x_tensor(y_bits), idx, w if weighted else None, E, R, lay, out, st, num_sms=num_sms)
+        torch.cuda.synchronize()
+        assert int(st.item()) == 0
+        ref, _ = oracle.combine(y_bits, d["topk_idx"], d["topk_weights"], E, R, L.dst_row, weighted=weighted)
+        bound = combine_tolerance(y_bits, d["topk_idx"], d["topk_weights"], E, R, L.dst_row, weighted)
+        g = (bf16_bits(out).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+        assert (np.abs(g - ref) <= bound).all()
+        assert (bf16_bits(out)[[0, T // 2, T - 1]] == 0).all()
+
+
 def test_sm_limited_against_oracle():
     from gpu_path import B, bf16_bits
     T, H, E, K, R = 1000, 7168, 256, 8, 8
