@@ -1028,7 +1028,18 @@ constexpr int kSmallMaxTokens = EP_LAYOUT_SMALL_MAX_TOKENS <= 1024 ? EP_LAYOUT_S
 constexpr int kSmallMaxRanks = 32;
 constexpr int kSmallMaxTopk = 16;
 constexpr int kSmallEntries = kSmallMaxTopk;   // entries per thread: <= 1024 tokens x 16 over 1024 threads
+constexpr int kSmallRankWarps = 8;             // warps ranking the expanded entries
 
+// Dynamic shared memory of the single-CTA kernel, in ints: the expert
+// histogram, and with expanded rows the entries' experts and the ranking's
+// per-(warp, expert) counters.
+inline size_t small_smem_ints(int E, int n_ent, bool expanded) {
+    return static_cast<size_t>(E) + (expanded ? static_cast<size_t>(n_ent) + static_cast<size_t>(kSmallRankWarps) * E : 0);
+}
+
+// kExpanded: also the expanded rows (each valid (t, k) numbered within its
+// expert in (token, k) order from expert_offset), ranked after the offsets.
+template <bool kExpanded>
 __global__ void __launch_bounds__(1024, 1) layout_small_kernel(const LayoutParams p) {
     __shared__ uint32_t s_bm[32][kSmallMaxRanks + 1];    // [word][rank] membership
     __shared__ int s_base[32][kSmallMaxRanks + 1];       // [word][rank] rows in earlier words
@@ -1043,6 +1054,8 @@ __global__ void __launch_bounds__(1024, 1) layout_small_kernel(const LayoutParam
     const int T = p.T, K = p.K, E = p.E, R = p.R, NN = p.num_nodes;
     const int W = (T + 31) >> 5;
     const int n_ent = T * K;
+    int* s_key = s_hist + E;                              // expanded: [n_ent] expert of each entry
+    int* s_wc = s_key + (kExpanded ? n_ent : 0);          // expanded: [8][E] ranking counters
     pdl_wait();
     pdl_launch_dependents();
 
@@ -1058,6 +1071,8 @@ __global__ void __launch_bounds__(1024, 1) layout_small_kernel(const LayoutParam
         (&s_bmn[0][0])[i] = 0u;
     }
     for (int i = tid; i < E; i += 1024) s_hist[i] = 0;
+    if (kExpanded)
+        for (int i = tid; i < kSmallRankWarps * E; i += 1024) s_wc[i] = 0;
     if (tid == 0) s_bad = 0;
     __syncthreads();
 
@@ -1066,6 +1081,10 @@ __global__ void __launch_bounds__(1024, 1) layout_small_kernel(const LayoutParam
 #pragma unroll
     for (int u = 0; u < kSmallEntries; ++u) {
         const int64_t e = v[u];
+        if (kExpanded) {
+            const int i = u * 1024 + tid;
+            if (i < n_ent) s_key[i] = (e >= 0 && e < E) ? static_cast<int>(e) : -1 - (i & 31);
+        }
         if (e == -1) continue;
         if (e < -1 || e >= E) {
             bad = true;
@@ -1149,7 +1168,10 @@ __global__ void __launch_bounds__(1024, 1) layout_small_kernel(const LayoutParam
             const int base = c < 32 ? __shfl_sync(0xffffffffu, i0 - c0, c)
                                     : t0 + __shfl_sync(0xffffffffu, i1 - c1, c - 32);
             const int e = c * 32 + lane;
-            if (e < E) p.expert_offset[e] = base + s_hist[e];
+            if (e < E) {
+                p.expert_offset[e] = base + s_hist[e];
+                if (kExpanded) s_hist[e] += base;   // now expert_offset, the ranking's bases
+            }
         }
         const int t1 = __shfl_sync(0xffffffffu, i1, 31);
         if (warp == 0 && lane == 0) p.expert_offset[E] = t0 + t1;
@@ -1204,6 +1226,10 @@ __global__ void __launch_bounds__(1024, 1) layout_small_kernel(const LayoutParam
                 p.is_token_in_rank[j0 + u] = static_cast<uint8_t>((in4 >> (8 * u)) & 1u);
             }
         }
+    }
+    if (kExpanded) {
+        __syncthreads();   // s_hist now holds expert_offset
+        rank_entries(s_key, n_ent, E, s_hist, s_wc, p.expanded_row, kSmallRankWarps);
     }
 }
 
@@ -1289,6 +1315,10 @@ cudaError_t launch_layout(const LayoutParams& p, cudaStream_t stream) {
         if (e == cudaSuccess) e = cluster_static_smem<true, true>(static_smem);
         if (e != cudaSuccess) return e;
         cluster_smem_max = di.max_smem_optin - static_smem;
+        // the single-CTA kernel with expanded rows: up to ~140 KB at the limits
+        e = cudaFuncSetAttribute(layout_small_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(4 * small_smem_ints(EP_MAX_EXPERTS, kSmallMaxTokens * kSmallMaxTopk, true)));
+        if (e != cudaSuccess) return e;
         cluster_ok = configure_cluster<false, false>(cluster_smem_max) &&
                      configure_cluster<true, false>(cluster_smem_max) &&
                      configure_cluster<false, true>(cluster_smem_max) && configure_cluster<true, true>(cluster_smem_max);
@@ -1296,9 +1326,12 @@ cudaError_t launch_layout(const LayoutParams& p, cudaStream_t stream) {
         configured_device = di.device;
     }
 
-    if (p.T <= kSmallMaxTokens && p.R <= kSmallMaxRanks && p.K <= kSmallMaxTopk && p.expanded_row == nullptr &&
-        p.node_row == nullptr)
-        return launch_pdl(layout_small_kernel, dim3(1), dim3(1024), static_cast<size_t>(p.E) * sizeof(int), stream, p);
+    if (p.T <= kSmallMaxTokens && p.R <= kSmallMaxRanks && p.K <= kSmallMaxTopk && p.node_row == nullptr) {
+        const bool expanded = p.expanded_row != nullptr;
+        const size_t smem = 4 * small_smem_ints(p.E, p.T * p.K, expanded);
+        if (expanded) return launch_pdl(layout_small_kernel<true>, dim3(1), dim3(1024), smem, stream, p);
+        return launch_pdl(layout_small_kernel<false>, dim3(1), dim3(1024), smem, stream, p);
+    }
 
     const ClusterPlan plan = cluster_ok ? plan_cluster(p, cluster_smem_max) : ClusterPlan{0, 0, 0};
     if (plan.ctas > 0) {

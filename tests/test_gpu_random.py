@@ -89,3 +89,31 @@ def test_random_layout_dispatch_combine(i):
     ref, _ = oracle.combine(y_bits, idx_h, w_h, E, R, L.dst_row, weighted=c["weighted"])
     bound = combine_tolerance(y_bits, idx_h, w_h, E, R, L.dst_row, c["weighted"])
     _close(bf16_bits(out), ref, bound)
+
+
+@pytest.mark.parametrize("i", range(N_CASES))
+def test_random_expanded_layout(i):
+    """The same shapes with expanded rows requested: the whole layout (rank
+    rows and offsets unchanged) plus expanded_row against the oracle."""
+    import torch
+    from gpu_path import B, layout_host, to_dev
+    c = _draw_case(i)
+    T, E, K, R = c["T"], c["E"], c["K"], c["R"]
+    d = make_inputs(T, 8, E, K, R, seed=c["seed"], mask_frac=c["mask"], with_x=False)
+    idx_h = d["topk_idx"]
+    lay = B.alloc_layout(T, E, R, c["rpn"], K=K)
+    ws = torch.empty(B.ep_layout_workspace_bytes(T, K, E, R, c["rpn"]), dtype=torch.uint8, device="cuda")
+    ws.fill_(0xA5)
+    lay.expanded_row.fill_(-7)
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    B.ep_get_layout(to_dev(idx_h), E, R, lay, ws, st, c["rpn"], c["align"])
+    torch.cuda.synchronize()
+    g = layout_host(lay)
+    L = oracle.layout(idx_h, E, R, c["rpn"], c["align"])
+    for f in ("num_tokens_per_rank", "num_tokens_per_expert", "is_token_in_rank", "rank_offset",
+              "expert_offset", "dst_row"):
+        np.testing.assert_array_equal(g[f], getattr(L, f), err_msg="%s %s" % (f, c))
+    want, _ = oracle.expanded_rows(idx_h, E, L.expert_offset)
+    np.testing.assert_array_equal(lay.expanded_row.cpu().numpy(), want, err_msg=str(c))
+    assert int(st.item()) == 0, c
+
