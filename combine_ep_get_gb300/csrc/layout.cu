@@ -7,6 +7,10 @@
 // expert).  Receive order inside a rank is ascending token index, so every
 // output is a pure function of topk_idx: no atomic decides an order.
 //
+// Few tokens (T <= 1024, R <= 32, K <= 16): one CTA, no cluster (see
+// layout_small_kernel), since at that size the cluster's fixed phases cost more
+// than the work.
+//
 // Main path: ONE launch of one thread-block cluster (up to 16 CTAs of 1024
 // threads, one per SM).  CTA c owns a contiguous token range; it builds the
 // membership bitmaps [words][R] and the expert histogram of its range in
@@ -1014,13 +1018,14 @@ struct ClusterPlan {
     size_t smem;
 };
 
-// Few tokens (T <= 1024, R <= 32, K <= 16, no expanded or node rows): one CTA
-// of 1024 threads and no cluster.  Every phase is spread over all 32 warps,
-// whatever T: the top-k entries one per thread (shared atomics build the
-// [word][rank] bitmaps and the expert histogram), one warp per rank for its
-// prefix over words and one per word for its tokens' rows, then (token, rank)
-// quads of dst_row and is_token_in_rank per thread.  Three block barriers, no
-// cluster barrier and no remote read.
+// Few tokens (T <= 1024, R <= 32, K <= 16, no node rows): one CTA of 1024
+// threads and no cluster.  Every phase is spread over all 32 warps, whatever
+// T: the top-k entries one per thread (shared atomics build the [word][rank]
+// bitmaps and the expert histogram), one warp per rank for its prefix over
+// words, one per word for its tokens' rows and one per 32 experts for their
+// aligned counts, then (token, rank) quads of dst_row and is_token_in_rank
+// per thread.  Three block barriers (a fourth and the ranking's two with
+// expanded rows), no cluster barrier and no remote read.
 #ifndef EP_LAYOUT_SMALL_MAX_TOKENS
 #define EP_LAYOUT_SMALL_MAX_TOKENS 1024   // 0 disables the single-CTA path
 #endif
