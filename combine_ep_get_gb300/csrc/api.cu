@@ -111,9 +111,12 @@ ep_status_t ep_get_layout(const int64_t* topk_idx, int T, int K, int E, int R, i
     if (out->src_dst_count && (!aligned16(out->src_dst_count) || T % R != 0)) return EP_ERR_INVALID_ARG;
     if (out->token_offset && !aligned16(out->token_offset)) return EP_ERR_INVALID_ARG;
     if (out->expanded_row && !aligned16(out->expanded_row)) return EP_ERR_INVALID_ARG;
-    if ((out->node_row != nullptr) != (out->node_offset != nullptr)) return EP_ERR_INVALID_ARG;
-    if (out->node_row && (ranks_per_node <= 0 || !ok_ptr(out->num_tokens_per_node) ||
-                          !aligned16(out->node_row) || !aligned16(out->node_offset)))
+    // node rows: node_offset and node_row together (node_row may be NULL, an
+    // empty array, when there are no tokens)
+    if (out->node_row && !out->node_offset) return EP_ERR_INVALID_ARG;
+    if (out->node_offset && !out->node_row && T > 0) return EP_ERR_INVALID_ARG;
+    if (out->node_offset && (ranks_per_node <= 0 || !ok_ptr(out->num_tokens_per_node) ||
+                             !aligned16(out->node_row) || !aligned16(out->node_offset)))
         return EP_ERR_INVALID_ARG;
     const int nodes_ws = ranks_per_node > 0 ? R / ranks_per_node : 0;
     const epg::LayoutWorkspace w = epg::layout_workspace(T, E, R, nodes_ws);
@@ -141,15 +144,20 @@ ep_status_t ep_get_layout(const int64_t* topk_idx, int T, int K, int E, int R, i
     p.token_offset = out->token_offset;
     p.expanded_row = T > 0 ? out->expanded_row : nullptr;
     p.node_offset = out->node_offset;
-    p.node_row = out->node_row;
+    p.node_row = T > 0 ? out->node_row : nullptr;
     char* ws = static_cast<char*>(workspace);
     p.ws_rank = reinterpret_cast<int32_t*>(ws + w.off_rank);
     p.ws_expert = reinterpret_cast<int32_t*>(ws + w.off_expert);
     p.ws_node = reinterpret_cast<int32_t*>(ws + w.off_node);
     p.ws_bitmap = reinterpret_cast<uint32_t*>(ws + w.off_bitmap);
     p.status = d_status;
-    return epg::launch_layout(p, static_cast<cudaStream_t>(cuda_stream)) == cudaSuccess ? EP_OK
-                                                                                      : EP_ERR_CUDA;
+    const cudaStream_t stream = static_cast<cudaStream_t>(cuda_stream);
+    if (epg::launch_layout(p, stream) != cudaSuccess) return EP_ERR_CUDA;
+    // no tokens: the node-row kernels are not launched, node_offset is all zero
+    if (T == 0 && out->node_offset &&
+        cudaMemsetAsync(out->node_offset, 0, sizeof(int32_t) * (R / ranks_per_node + 1), stream) != cudaSuccess)
+        return EP_ERR_CUDA;
+    return EP_OK;
 }
 
 ep_status_t ep_dispatch(const void* x, const int64_t* topk_idx, const float* topk_weights, int T,

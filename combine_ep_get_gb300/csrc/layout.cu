@@ -1044,11 +1044,15 @@ inline size_t small_smem_ints(int E, int n_ent, bool expanded) {
 
 // kExpanded: also the expanded rows (each valid (t, k) numbered within its
 // expert in (token, k) order from expert_offset), ranked after the offsets.
-template <bool kExpanded>
+// kNodeRows: also node_offset and the node rows, formed like the rank rows
+// from the [word][node] bitmaps.
+template <bool kExpanded, bool kNodeRows>
 __global__ void __launch_bounds__(1024, 1) layout_small_kernel(const LayoutParams p) {
     __shared__ uint32_t s_bm[32][kSmallMaxRanks + 1];    // [word][rank] membership
     __shared__ int s_base[32][kSmallMaxRanks + 1];       // [word][rank] rows in earlier words
     __shared__ uint32_t s_bmn[32][kSmallMaxRanks + 1];   // [word][node] membership
+    __shared__ int s_nbase[kNodeRows ? 32 : 1][kSmallMaxRanks + 1];   // [word][node] tokens in earlier words
+    __shared__ int s_ntot[kSmallMaxRanks];               // node rows: tokens of each node
     __shared__ int s_tot[kSmallMaxRanks];                // rows of each rank
     __shared__ int s_ntok[1024];                         // token's row within its word
     __shared__ int s_wtok[32];                           // rows of each word
@@ -1131,8 +1135,17 @@ __global__ void __launch_bounds__(1024, 1) layout_small_kernel(const LayoutParam
     }
     if (warp < NN) {
         const int c = lane < W ? __popc(s_bmn[lane][warp]) : 0;
-        const int tot = static_cast<int>(__reduce_add_sync(0xffffffffu, static_cast<unsigned>(c)));
-        if (lane == 0) p.num_tokens_per_node[warp] = tot;
+        if (kNodeRows) {   // warp n: node n's prefix over the words
+            const int incl = warp_inclusive_scan(c);
+            if (lane < W) s_nbase[lane][warp] = incl - c;
+            if (lane == 31) {
+                s_ntot[warp] = incl;
+                p.num_tokens_per_node[warp] = incl;
+            }
+        } else {
+            const int tot = static_cast<int>(__reduce_add_sync(0xffffffffu, static_cast<unsigned>(c)));
+            if (lane == 0) p.num_tokens_per_node[warp] = tot;
+        }
     }
     if (warp < W) {
         int n = 0;
@@ -1232,6 +1245,44 @@ __global__ void __launch_bounds__(1024, 1) layout_small_kernel(const LayoutParam
             }
         }
     }
+    if (kNodeRows) {   // node_offset (lane n) by shuffles, then (token, node) quads
+        const int nv = lane < NN ? s_ntot[lane] : 0;
+        const int nincl = warp_inclusive_scan(nv);
+        const int no = nincl - nv;
+        if (warp == 0) {
+            if (lane < NN) p.node_offset[lane] = no;
+            const int n_node = __shfl_sync(0xffffffffu, nincl, 31);
+            if (lane == 0) p.node_offset[NN] = n_node;
+        }
+        const int n_eln = T * NN;
+        const uint32_t m_n = NN > 1 ? 0xffffffffu / static_cast<uint32_t>(NN) + 1u : 0u;
+        for (int q0 = warp * 128; q0 < n_eln; q0 += 4096) {   // warp-uniform
+            const int j0 = q0 + lane * 4;
+            int tl = NN > 1 ? static_cast<int>(__umulhi(static_cast<uint32_t>(j0), m_n)) : j0;
+            int n = j0 - tl * NN;
+            int d[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int nor = __shfl_sync(0xffffffffu, no, n & 31);
+                d[u] = -1;
+                if (j0 + u < n_eln) {
+                    const int w = tl >> 5;
+                    const uint32_t word = s_bmn[w][n];
+                    const uint32_t b = static_cast<uint32_t>(tl & 31);
+                    if ((word >> b) & 1u) d[u] = nor + s_nbase[w][n] + __popc(word & ((1u << b) - 1u));
+                }
+                if (++n == NN) {
+                    n = 0;
+                    ++tl;
+                }
+            }
+            if (j0 + 4 <= n_eln) {
+                *reinterpret_cast<int4*>(p.node_row + j0) = make_int4(d[0], d[1], d[2], d[3]);
+            } else {
+                for (int u = 0; u < 4 && j0 + u < n_eln; ++u) p.node_row[j0 + u] = d[u];
+            }
+        }
+    }
     if (kExpanded) {
         __syncthreads();   // s_hist now holds expert_offset
         rank_entries(s_key, n_ent, E, s_hist, s_wc, p.expanded_row, kSmallRankWarps);
@@ -1321,8 +1372,10 @@ cudaError_t launch_layout(const LayoutParams& p, cudaStream_t stream) {
         if (e != cudaSuccess) return e;
         cluster_smem_max = di.max_smem_optin - static_smem;
         // the single-CTA kernel with expanded rows: up to ~140 KB at the limits
-        e = cudaFuncSetAttribute(layout_small_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 static_cast<int>(4 * small_smem_ints(EP_MAX_EXPERTS, kSmallMaxTokens * kSmallMaxTopk, true)));
+        const int small_max = static_cast<int>(4 * small_smem_ints(EP_MAX_EXPERTS, kSmallMaxTokens * kSmallMaxTopk, true));
+        e = cudaFuncSetAttribute(layout_small_kernel<true, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, small_max);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(layout_small_kernel<true, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, small_max);
         if (e != cudaSuccess) return e;
         cluster_ok = configure_cluster<false, false>(cluster_smem_max) &&
                      configure_cluster<true, false>(cluster_smem_max) &&
@@ -1331,11 +1384,12 @@ cudaError_t launch_layout(const LayoutParams& p, cudaStream_t stream) {
         configured_device = di.device;
     }
 
-    if (p.T <= kSmallMaxTokens && p.R <= kSmallMaxRanks && p.K <= kSmallMaxTopk && p.node_row == nullptr) {
-        const bool expanded = p.expanded_row != nullptr;
+    if (p.T <= kSmallMaxTokens && p.R <= kSmallMaxRanks && p.K <= kSmallMaxTopk) {
+        const bool expanded = p.expanded_row != nullptr, nodes = p.node_row != nullptr;
         const size_t smem = 4 * small_smem_ints(p.E, p.T * p.K, expanded);
-        if (expanded) return launch_pdl(layout_small_kernel<true>, dim3(1), dim3(1024), smem, stream, p);
-        return launch_pdl(layout_small_kernel<false>, dim3(1), dim3(1024), smem, stream, p);
+        auto kernel = expanded ? (nodes ? layout_small_kernel<true, true> : layout_small_kernel<true, false>)
+                               : (nodes ? layout_small_kernel<false, true> : layout_small_kernel<false, false>);
+        return launch_pdl(kernel, dim3(1), dim3(1024), smem, stream, p);
     }
 
     const ClusterPlan plan = cluster_ok ? plan_cluster(p, cluster_smem_max) : ClusterPlan{0, 0, 0};

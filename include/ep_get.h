@@ -107,7 +107,9 @@ typedef struct ep_layout {
                                              buffer or -1; rows of node n are
                                              node_offset[n] + 0, 1, ... in ascending t.
                                              NULL, or set together with node_offset and
-                                             num_tokens_per_node (ranks_per_node > 0);
+                                             num_tokens_per_node (ranks_per_node > 0;
+                                             with no tokens node_row may be NULL and
+                                             node_offset is all zero);
                                              see ep_dispatch_hierarchical              */
 } ep_layout_t;
 

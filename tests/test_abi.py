@@ -192,6 +192,8 @@ def test_hierarchical_host_checks(lib):
     ok = B.ep_layout_t(**fields)
     assert f(vp(16), 10, 8, 256, 8, 4, 1, ctypes.byref(B.ep_layout_t(**{**fields, "node_offset": None})),
              vp(256), 1 << 20, st, None) == B.EP_ERR_INVALID_ARG          # node_row without node_offset
+    assert f(vp(16), 10, 8, 256, 8, 4, 1, ctypes.byref(B.ep_layout_t(**{**fields, "node_row": None})),
+             vp(256), 1 << 20, st, None) == B.EP_ERR_INVALID_ARG          # node_offset without node_row, T > 0
     assert f(vp(16), 10, 8, 256, 8, 0, 1, ctypes.byref(ok), vp(256), 1 << 20, st, None) == B.EP_ERR_INVALID_ARG
     assert f(vp(16), 10, 8, 256, 8, 4, 1, ctypes.byref(B.ep_layout_t(**{**fields, "num_tokens_per_node": None})),
              vp(256), 1 << 20, st, None) == B.EP_ERR_INVALID_ARG          # no node counts

@@ -39,7 +39,7 @@ def _layout(idx_np, E, R, rpn):
 @pytest.mark.parametrize("T,K,E,R,rpn,mode", [
     (300, 8, 256, 64, 8, "uniform"), (777, 6, 96, 12, 3, "replace"), (513, 5, 40, 8, 2, "invalid"),
     (1000, 8, 256, 8, 1, "masked"), (200, 8, 256, 16, 16, "uniform"), (1, 4, 16, 4, 2, "uniform"),
-    (300, 32, 2048, 1024, 32, "uniform"),
+    (300, 32, 2048, 1024, 32, "uniform"), (1024, 8, 256, 32, 1, "masked"),
 ])
 def test_node_rows(T, K, E, R, rpn, mode):
     rng = np.random.Generator(np.random.PCG64(T + K + R))

@@ -93,15 +93,15 @@ def test_random_layout_dispatch_combine(i):
 
 @pytest.mark.parametrize("i", range(N_CASES))
 def test_random_expanded_layout(i):
-    """The same shapes with expanded rows requested: the whole layout (rank
-    rows and offsets unchanged) plus expanded_row against the oracle."""
+    """The same shapes with expanded rows (and node rows where there are node
+    groups) requested: the whole layout against the oracle."""
     import torch
     from gpu_path import B, layout_host, to_dev
     c = _draw_case(i)
     T, E, K, R = c["T"], c["E"], c["K"], c["R"]
     d = make_inputs(T, 8, E, K, R, seed=c["seed"], mask_frac=c["mask"], with_x=False)
     idx_h = d["topk_idx"]
-    lay = B.alloc_layout(T, E, R, c["rpn"], K=K)
+    lay = B.alloc_layout(T, E, R, c["rpn"], K=K, node_rows=c["rpn"] > 0)
     ws = torch.empty(B.ep_layout_workspace_bytes(T, K, E, R, c["rpn"]), dtype=torch.uint8, device="cuda")
     ws.fill_(0xA5)
     lay.expanded_row.fill_(-7)
@@ -115,5 +115,9 @@ def test_random_expanded_layout(i):
         np.testing.assert_array_equal(g[f], getattr(L, f), err_msg="%s %s" % (f, c))
     want, _ = oracle.expanded_rows(idx_h, E, L.expert_offset)
     np.testing.assert_array_equal(lay.expanded_row.cpu().numpy(), want, err_msg=str(c))
+    if c["rpn"]:
+        off, rows, _ = oracle.node_rows(idx_h, E, R, c["rpn"])
+        np.testing.assert_array_equal(lay.node_row.cpu().numpy(), rows, err_msg=str(c))
+        np.testing.assert_array_equal(lay.node_offset.cpu().numpy(), off, err_msg=str(c))
     assert int(st.item()) == 0, c
 
