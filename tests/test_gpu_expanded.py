@@ -72,8 +72,12 @@ def test_expanded_rows_workloads(name):
     (500, 1024, 64, 6, 8, 16, 0.1), (64, 7168, 256, 8, 32, 1, 0.0), (1000, 256, 256, 8, 8, 128, 0.02),
 ])
 def test_expanded_dispatch(fp8, T, H, E, K, R, align, mask):
+    _check_expanded_dispatch(fp8, T, H, E, K, R, align, mask, seed=T + H)
+
+
+def _check_expanded_dispatch(fp8, T, H, E, K, R, align, mask, seed):
     from gpu_path import B, bf16_bits, x_tensor
-    d = make_inputs(T, H, E, K, R, seed=T + H, mask_frac=mask)
+    d = make_inputs(T, H, E, K, R, seed=seed, mask_frac=mask)
     idx, lay, _ = _layout(d["topk_idx"], E, R, align)
     w = torch.from_numpy(d["topk_weights"]).cuda()
     cap = int(lay.expert_offset[-1].item())
@@ -93,12 +97,12 @@ def test_expanded_dispatch(fp8, T, H, E, K, R, align, mask):
     L, rows, _ = _oracle_rows(d["topk_idx"], E, R, align)
     o = oracle.dispatch_expanded(d["x_bits"], d["topk_weights"], rows, cap, fp8=fp8)
     valid = np.unique(rows[rows >= 0])
-    gx = rx.cpu().numpy() if fp8 else bf16_bits(rx).view(np.uint8).reshape(cap, -1)
+    gx = rx.cpu().numpy() if fp8 else bf16_bits(rx).view(np.uint8).reshape(cap, 2 * H)
     np.testing.assert_array_equal(gx[valid], o["recv_x"][valid])
     np.testing.assert_array_equal(rs.cpu().numpy(), o["recv_src_idx"])       # padding stays -1
     np.testing.assert_array_equal(rw.cpu().numpy()[valid], o["recv_weight"][valid])
     if fp8:
-        np.testing.assert_array_equal(rsf.cpu().numpy().reshape(cap, -1)[valid], o["recv_sf"][valid])
+        np.testing.assert_array_equal(rsf.cpu().numpy().reshape(cap, H // 128)[valid], o["recv_sf"][valid])
 
 
 @pytest.mark.parametrize("weighted", [False, True])
@@ -106,8 +110,12 @@ def test_expanded_dispatch(fp8, T, H, E, K, R, align, mask):
     (500, 1024, 64, 6, 8, 16, 0.1), (4096, 7168, 256, 8, 8, 1, 0.0), (200, 256, 2048, 32, 1024, 4, 0.1),
 ])
 def test_expanded_combine(weighted, T, H, E, K, R, align, mask):
+    _check_expanded_combine(weighted, T, H, E, K, R, align, mask, seed=T + 2 * H)
+
+
+def _check_expanded_combine(weighted, T, H, E, K, R, align, mask, seed):
     from gpu_path import B, bf16_bits, x_tensor
-    d = make_inputs(T, H, E, K, R, seed=T + 2 * H, mask_frac=mask, with_x=False)
+    d = make_inputs(T, H, E, K, R, seed=seed, mask_frac=mask, with_x=False)
     idx, lay, _ = _layout(d["topk_idx"], E, R, align)
     w = torch.from_numpy(d["topk_weights"]).cuda()
     cap = int(lay.expert_offset[-1].item())
@@ -171,5 +179,17 @@ def test_expanded_dispatch_fp8_wide():
     o = oracle.dispatch_expanded(d["x_bits"], d["topk_weights"], rows, cap, fp8=True)
     valid = np.unique(rows[rows >= 0])
     np.testing.assert_array_equal(rx.cpu().numpy()[valid], o["recv_x"][valid])
-    np.testing.assert_array_equal(rsf.cpu().numpy().reshape(cap, -1)[valid], o["recv_sf"][valid])
+    np.testing.assert_array_equal(rsf.cpu().numpy().reshape(cap, H // 128)[valid], o["recv_sf"][valid])
     np.testing.assert_array_equal(rs.cpu().numpy(), o["recv_src_idx"])
+
+
+@pytest.mark.parametrize("i", range(24))
+def test_random_expanded_dispatch_combine(i):
+    """Expanded dispatch and weighted / unweighted combine on the random
+    sweep's shapes and alignments."""
+    from test_gpu_random import _draw_case
+    c = _draw_case(i)
+    _check_expanded_dispatch(c["fp8"], c["T"], c["H"], c["E"], c["K"], c["R"], c["align"], c["mask"], seed=c["seed"])
+    _check_expanded_combine(c["weighted"], c["T"], c["H"], c["E"], c["K"], c["R"], c["align"], c["mask"],
+                            seed=c["seed"] + 3)
+

@@ -92,7 +92,7 @@ def _bytes(t):
     from gpu_path import bf16_bits
     if t.dtype == torch.uint8:
         return t.cpu().numpy()
-    return bf16_bits(t).view(np.uint8).reshape(t.shape[0], -1)
+    return bf16_bits(t).view(np.uint8).reshape(t.shape[0], 2 * t.shape[1])
 
 
 @pytest.mark.parametrize("fp8,col", [(False, False), (True, False), (True, True)])
@@ -101,8 +101,12 @@ def _bytes(t):
     (200, 512, 2048, 32, 1024, 32, 0.1), (33, 4096, 128, 8, 8, 8, 0.05),
 ])
 def test_dispatch_hierarchical(fp8, col, T, H, E, K, R, rpn, mask):
+    _check_dispatch_hierarchical(fp8, col, T, H, E, K, R, rpn, mask, seed=T + H + R)
+
+
+def _check_dispatch_hierarchical(fp8, col, T, H, E, K, R, rpn, mask, seed):
     from gpu_path import B, x_tensor
-    d = make_inputs(T, H, E, K, R, seed=T + H + R, mask_frac=mask)
+    d = make_inputs(T, H, E, K, R, seed=seed, mask_frac=mask)
     idx, lay, _ = _layout(d["topk_idx"], E, R, rpn)
     w = torch.from_numpy(d["topk_weights"]).cuda()
     N, M = lay.num_recv, int(lay.node_offset[-1].item())
@@ -121,13 +125,13 @@ def test_dispatch_hierarchical(fp8, col, T, H, E, K, R, rpn, mask):
     for k in ("recv_topk_idx", "recv_topk_weights", "recv_src_idx"):
         np.testing.assert_array_equal(g[k].cpu().numpy(), one[k], err_msg=k)
     if fp8:
-        np.testing.assert_array_equal(g["node_sf"].cpu().numpy().reshape(M, -1), two["node_sf"])
+        np.testing.assert_array_equal(g["node_sf"].cpu().numpy().reshape(M, H // 128), two["node_sf"])
         if col:
             nb = H // 128
             got = g["recv_sf"].cpu().numpy()[:nb * stride].reshape(nb, stride)[:, :N]
             want = one["recv_sf"][:nb * stride].reshape(nb, stride)[:, :N]
         else:
-            got, want = g["recv_sf"].cpu().numpy().reshape(N, -1), one["recv_sf"]
+            got, want = g["recv_sf"].cpu().numpy().reshape(N, H // 128), one["recv_sf"]
         np.testing.assert_array_equal(got, want)
 
 
@@ -172,8 +176,12 @@ def _combine(B, y, idx, w, E, R, rpn, lay, M, T, H):
     (64, 512, 32, 4, 8, 8, 0.0),
 ])
 def test_combine_hierarchical(weighted, T, H, E, K, R, rpn, mask):
+    _check_combine_hierarchical(weighted, T, H, E, K, R, rpn, mask, seed=T + 3 * H)
+
+
+def _check_combine_hierarchical(weighted, T, H, E, K, R, rpn, mask, seed):
     from gpu_path import B, bf16_bits, x_tensor
-    d = make_inputs(T, H, E, K, R, seed=T + 3 * H, mask_frac=mask, with_x=False)
+    d = make_inputs(T, H, E, K, R, seed=seed, mask_frac=mask, with_x=False)
     idx, lay, _ = _layout(d["topk_idx"], E, R, rpn)
     w = torch.from_numpy(d["topk_weights"]).cuda()
     N, M = lay.num_recv, int(lay.node_offset[-1].item())
@@ -297,3 +305,19 @@ def test_combine_hierarchical_short_y(weighted):
     assert (np.abs(g_node - want_node) <= 1e-2 * scale_node).all()
     g_out = oracle.bf16_to_float(bf16_bits(out).reshape(T, H)).astype(np.float64)
     assert (np.abs(g_out - oout) <= 1e-2 * scale_tok).all()
+
+
+@pytest.mark.parametrize("i", range(24))
+def test_random_hierarchical(i):
+    """Two-stage dispatch and combine on the random sweep's shapes (node
+    groups of the case, else a middle divisor of R): node buffers and receive
+    buffers exact, combine within tolerance."""
+    from test_gpu_random import _draw_case
+    c = _draw_case(i)
+    R = c["R"]
+    divisors = [d for d in range(1, R + 1) if R % d == 0]
+    rpn = c["rpn"] or divisors[len(divisors) // 2]
+    _check_dispatch_hierarchical(c["fp8"], c["fp8"] and i % 2 == 1, c["T"], c["H"], c["E"], c["K"], R, rpn, c["mask"],
+                                 seed=c["seed"])
+    _check_combine_hierarchical(c["weighted"], c["T"], c["H"], c["E"], c["K"], R, rpn, c["mask"], seed=c["seed"] + 7)
+
