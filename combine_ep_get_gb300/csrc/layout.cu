@@ -248,16 +248,38 @@ __device__ int block_exclusive_scan_slice(const int (&v)[kMax], int (&out)[kMax]
     return total;
 }
 
+// The lanes of the warp whose key equals this lane's (what the warp match
+// instruction returns), through a per-(warp, key) word in shared memory: each
+// lane ORs its bit in, the warp reads the word back, and the group's first
+// lane clears it.  kb: this warp's [E] words, zero on entry and left zero.
+// Negative keys are unique per lane.  When every warp of an SM ranks at once
+// the match instruction serialises (~2 us for two passes over 64 chunks);
+// a shared atomic, a load and a store per lane do not.
+__device__ __forceinline__ unsigned match_key(int key, uint32_t* kb, int lane) {
+    if (key >= 0) atomicOr(&kb[key], 1u << lane);
+    __syncwarp();
+    const unsigned g = key >= 0 ? kb[key] : (1u << lane);
+    __syncwarp();
+    if (key >= 0 && lane == __ffs(g) - 1) kb[key] = 0u;
+    return g;
+}
+
 // Ranks entries [0, n_ent) per expert in index order: entry i with key
 // e >= 0 (s_key[i]; negative keys are unique per lane and never match) gets
-// out[i] = s_eb[e] + (entries of e before i), else -1.  Warps 0..7 each rank
-// a contiguous slice of 32-entry chunks twice with __match_any_sync (count,
-// then place) around per-(warp, expert) bases in s_wc [nw][E] (warps
-// 0..nw-1 rank), which the caller has zeroed; the order never depends on
-// timing.  Every thread of the block calls it (block barriers inside).
+// out[i] = s_eb[e] + (entries of e before i), else -1.  Warps 0..nw-1 each
+// rank a contiguous slice of 32-entry chunks twice (count, then place) with
+// equal keys grouped by match_key, around per-(warp, expert) bases in s_wc
+// [nw][E]; s_wc and the key groups [nw][E] that follow it in shared memory
+// are zero on entry (the key groups are left zero).  The
+// order never depends on timing.  Every thread of the block calls it (block
+// barriers inside).
 constexpr int kRankWarps = 8;
+// Rank warps of the tiled path: 4 above 1024 experts, so that its counters and
+// key groups (2 x warps x E ints) fit beside the staged entries.
+__host__ __device__ inline int tiled_rank_warps(int E) { return E > 1024 ? kRankWarps / 2 : kRankWarps; }
 __device__ void rank_entries(const int* s_key, int n_ent, int E, const int* s_eb, int* s_wc, int32_t* out,
                              int nw) {
+    uint32_t* s_kb = reinterpret_cast<uint32_t*>(s_wc + nw * E);
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int chunks = (n_ent + 31) / 32;
     const int per = (chunks + nw - 1) / nw;
@@ -266,7 +288,7 @@ __device__ void rank_entries(const int* s_key, int n_ent, int E, const int* s_eb
     for (int c = c0; c < c1; ++c) {                     // pass 1: per-(warp, expert) counts
         const int i = c * 32 + lane;
         const int key = i < n_ent ? s_key[i] : -1 - lane;
-        const unsigned g = __match_any_sync(0xffffffffu, key);
+        const unsigned g = match_key(key, s_kb + warp * E, lane);
         if (key >= 0 && lane == __ffs(g) - 1) s_wc[warp * E + key] += __popc(g);
         __syncwarp();
     }
@@ -283,7 +305,7 @@ __device__ void rank_entries(const int* s_key, int n_ent, int E, const int* s_eb
     for (int c = c0; c < c1; ++c) {                     // pass 2: place
         const int i = c * 32 + lane;
         const int key = i < n_ent ? s_key[i] : -1 - lane;
-        const unsigned g = __match_any_sync(0xffffffffu, key);
+        const unsigned g = match_key(key, s_kb + warp * E, lane);
         int pos = -1;
         if (key >= 0) pos = s_wc[warp * E + key] + __popc(g & ((1u << lane) - 1u));
         __syncwarp();
@@ -297,13 +319,15 @@ __device__ void rank_entries(const int* s_key, int n_ent, int E, const int* s_eb
 // entries take rows s_eb[e] (expert_offset[e] + entries of e in earlier
 // tiles) + their stable rank in the tile, in (token, k) order.  The tile's
 // entries are staged in shared memory (the first batch was loaded at kernel
-// entry).  Needs 256 K + 8 E shared ints.
+// entry).  Needs 256 K + 2 x tiled_rank_warps(E) x E shared ints.
 __device__ void expanded_rows_of_tile(const LayoutParams& p, int t0, int nt, const int* s_eb, int* sm,
                                       const int64_t (&key0)[kStageUnroll]) {
     const int E = p.E;
     const int n_ent = nt * p.K;
     int* s_key = sm;                        // [256 K] expert of each entry, or a unique negative
-    int* s_wc = s_key + kTileTokens * p.K;  // [8][E] per-warp counts, then per-warp bases
+    const int nw = tiled_rank_warps(E);
+    int* s_wc = s_key + kTileTokens * p.K;  // [nw][E] per-warp counts, then per-warp bases
+    uint32_t* s_kb = reinterpret_cast<uint32_t*>(s_wc + nw * E);   // [nw][E] key groups
     const int64_t* src = p.topk_idx + static_cast<int64_t>(t0) * p.K;
     for (int base = 0; base < n_ent; base += kStageUnroll * kThreads) {
         int64_t e[kStageUnroll];
@@ -318,9 +342,12 @@ __device__ void expanded_rows_of_tile(const LayoutParams& p, int t0, int nt, con
             if (i < n_ent) s_key[i] = (e[u] >= 0 && e[u] < E) ? static_cast<int>(e[u]) : -1 - (i & 31);
         }
     }
-    for (int i = threadIdx.x; i < kRankWarps * E; i += kThreads) s_wc[i] = 0;
+    for (int i = threadIdx.x; i < nw * E; i += kThreads) {
+        s_wc[i] = 0;
+        s_kb[i] = 0u;
+    }
     __syncthreads();
-    rank_entries(s_key, n_ent, E, s_eb, s_wc, p.expanded_row + static_cast<int64_t>(t0) * p.K, kRankWarps);
+    rank_entries(s_key, n_ent, E, s_eb, s_wc, p.expanded_row + static_cast<int64_t>(t0) * p.K, nw);
 }
 
 // Node rows of one tile: a token is in node n when any rank of n holds it,
@@ -604,7 +631,7 @@ __host__ __device__ inline int cluster_rank_warps(int E) { return E <= 512 ? 32 
 size_t cluster_smem_words(int R, int E, int nodes, int W, int K, bool expanded, bool node_rows) {
     size_t w = 2 * static_cast<size_t>(R) * W + static_cast<size_t>(nodes) * W + R + E + nodes + (R + 1) + R +
                33 * static_cast<size_t>(W) + 64;
-    if (expanded) w += 32 * static_cast<size_t>(W) * K + (1 + cluster_rank_warps(E)) * static_cast<size_t>(E);
+    if (expanded) w += 32 * static_cast<size_t>(W) * K + (1 + 2 * cluster_rank_warps(E)) * static_cast<size_t>(E);
     if (node_rows) w += 2 * static_cast<size_t>(nodes) + 1 + static_cast<size_t>(W) * nodes;
     return w;
 }
@@ -688,7 +715,8 @@ __global__ void __launch_bounds__(kClusterThreads, 1)
     int* s_key = s_wtok + W;                                        // expanded: [32 W K] expert of each entry
     int* s_eb = s_key + (expanded ? 32 * W * p.K : 0);              // expanded: [E] expert bases
     int* s_wc = s_eb + (expanded ? E : 0);                          // expanded: [8][E] ranking counters
-    int* s_ntot = s_wc + (expanded ? cluster_rank_warps(E) * E : 0);  // node rows: [NN+1] totals -> node_offset
+    uint32_t* s_kb = reinterpret_cast<uint32_t*>(s_wc + (expanded ? cluster_rank_warps(E) * E : 0));   // expanded: [nw][E] key groups
+    int* s_ntot = reinterpret_cast<int*>(s_kb) + (expanded ? cluster_rank_warps(E) * E : 0);  // node rows: [NN+1] totals -> node_offset
     int* s_nbefore = s_ntot + (kNodeRows ? NN + 1 : 0);             // node rows: [NN] tokens of earlier CTAs
     int* s_nwbase = s_nbefore + (kNodeRows ? NN : 0);               // node rows: [W][NN] earlier words
     __shared__ int s_rows_total;                                    // read by later CTAs
@@ -999,7 +1027,10 @@ __global__ void __launch_bounds__(kClusterThreads, 1)
         const int nw = cluster_rank_warps(E);
         for (int e = tid; e < E; e += kClusterThreads) {
             s_eb[e] += s_wc[e];   // each thread owns column e of s_wc here
-            for (int w = 0; w < nw; ++w) s_wc[w * E + e] = 0;
+            for (int w = 0; w < nw; ++w) {
+                s_wc[w * E + e] = 0;
+                s_kb[w * E + e] = 0u;
+            }
         }
         __syncthreads();
         rank_entries(s_key, n_ent, E, s_eb, s_wc, p.expanded_row + static_cast<int64_t>(t0) * p.K, nw);
@@ -1039,7 +1070,7 @@ constexpr int kSmallRankWarps = 8;             // warps ranking the expanded ent
 // histogram, and with expanded rows the entries' experts and the ranking's
 // per-(warp, expert) counters.
 inline size_t small_smem_ints(int E, int n_ent, bool expanded) {
-    return static_cast<size_t>(E) + (expanded ? static_cast<size_t>(n_ent) + static_cast<size_t>(kSmallRankWarps) * E : 0);
+    return static_cast<size_t>(E) + (expanded ? static_cast<size_t>(n_ent) + 2 * static_cast<size_t>(kSmallRankWarps) * E : 0);
 }
 
 // kExpanded: also the expanded rows (each valid (t, k) numbered within its
@@ -1065,6 +1096,7 @@ __global__ void __launch_bounds__(1024, 1) layout_small_kernel(const LayoutParam
     const int n_ent = T * K;
     int* s_key = s_hist + E;                              // expanded: [n_ent] expert of each entry
     int* s_wc = s_key + (kExpanded ? n_ent : 0);          // expanded: [8][E] ranking counters
+    uint32_t* s_kb = reinterpret_cast<uint32_t*>(s_wc + (kExpanded ? kSmallRankWarps * E : 0));   // expanded: [8][E] key groups
     pdl_wait();
     pdl_launch_dependents();
 
@@ -1081,7 +1113,10 @@ __global__ void __launch_bounds__(1024, 1) layout_small_kernel(const LayoutParam
     }
     for (int i = tid; i < E; i += 1024) s_hist[i] = 0;
     if (kExpanded)
-        for (int i = tid; i < kSmallRankWarps * E; i += 1024) s_wc[i] = 0;
+        for (int i = tid; i < kSmallRankWarps * E; i += 1024) {
+            s_wc[i] = 0;
+            s_kb[i] = 0u;
+        }
     if (tid == 0) s_bad = 0;
     __syncthreads();
 
@@ -1428,7 +1463,8 @@ cudaError_t launch_layout(const LayoutParams& p, cudaStream_t stream) {
     size_t extra = 0;
     if (p.node_row) extra = 4 * (2 * static_cast<size_t>(kTileWords) * p.num_nodes);
     if (p.expanded_row) {
-        const size_t ex = 4 * (static_cast<size_t>(kTileTokens) * p.K + 8 * static_cast<size_t>(p.E));
+        const size_t ex = 4 * (static_cast<size_t>(kTileTokens) * p.K +
+                               2 * static_cast<size_t>(tiled_rank_warps(p.E)) * static_cast<size_t>(p.E));
         if (ex > extra) extra = ex;
     }
     smem_rows += extra;
