@@ -14,11 +14,12 @@
 // ~n(t) times the writes.
 //
 // SM-limited mode (num_sms > 0): CTAs of 8 groups of 128 threads, one per SM,
-// each group looping over items with 8 source rows of loads in flight per
-// thread (same order and arithmetic, so results are bit-identical).  A
-// bulk-copy ring (one producer warp filling 13 shared-memory slots, eight
-// consumer warps) measured ~30% slower: per 14 KB slot its consumers spent
-// more instructions on the ring handshake than register loads cost.
+// each group looping over whole-row items (pieces only when there are fewer
+// rows than groups) with 8 source rows of loads in flight per thread (same
+// order and arithmetic, so results are bit-identical).  Shared-memory rings
+// fed by bulk copies (per-row slots, or per-item stages with one to four
+// producer warps) measured 30% to 2.8x slower: their handshakes cost more than
+// register loads.
 #include <cuda_bf16.h>
 
 #include "ep_internal.cuh"
@@ -207,14 +208,18 @@ cudaError_t launch_combine_t(const CombineParams& p, int64_t items, int num_sms,
 cudaError_t launch_combine(CombineParams p, bool weighted, cudaStream_t stream) {
     const DeviceInfo& di = device_info();
     const int n_vec = p.H / 8;
-    // Pieces of up to 2 vectors per thread; more pieces when there are few tokens.
-    int chunks = (n_vec + 2 * kThreads - 1) / (2 * kThreads);
-    const int want_items = 4 * di.num_sms;
+    const int num_sms = p.num_sms > 0 ? (p.num_sms < di.num_sms ? p.num_sms : di.num_sms) : 0;
+    // Pieces of up to 2 vectors per thread; more pieces when there are few
+    // tokens.  SM-limited: whole rows (each group's item then waits on one
+    // routing load per row instead of one per quarter row: +40-55% at 16-64
+    // SMs), unless there are fewer rows than groups.
+    int chunks = num_sms > 0 ? 1 : (n_vec + 2 * kThreads - 1) / (2 * kThreads);
+    const int64_t want_items = num_sms > 0 ? static_cast<int64_t>(num_sms) * kSmGroups : 4 * di.num_sms;
     const bool few = p.T > 0 && static_cast<int64_t>(p.T) * chunks < want_items;
     if (few) {
         // few tokens: latency-bound, so at most one vector per thread (each
         // CTA then waits for one batch of row loads per 4 rows, not two)
-        int more = (want_items + p.T - 1) / p.T;
+        int more = static_cast<int>((want_items + p.T - 1) / p.T);
         const int one_vec = (n_vec + kThreads - 1) / kThreads;
         if (more < one_vec) more = one_vec;
         const int max_chunks = (n_vec + 31) / 32;
@@ -227,7 +232,6 @@ cudaError_t launch_combine(CombineParams p, bool weighted, cudaStream_t stream) 
     p.chunk_vecs = chunk_vecs;
     const int64_t items = static_cast<int64_t>(p.T) * chunks;
     if (items < 1) return cudaSuccess;
-    const int num_sms = p.num_sms > 0 ? (p.num_sms < di.num_sms ? p.num_sms : di.num_sms) : 0;
     if (p.expanded_row) {
         if (weighted) return launch_combine_t<true, true>(p, items, num_sms, few, stream);
         return launch_combine_t<false, true>(p, items, num_sms, few, stream);
