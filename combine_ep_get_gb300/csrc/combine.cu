@@ -57,6 +57,30 @@ constexpr int kSmGroups = 8;
 // token's source rows are its expanded rows (one per valid top-k slot,
 // coefficient = that slot's weight) instead of one row per rank.  kB: source
 // rows of loads in flight per thread.
+// Pairs of fp32 in one 64-bit register, added or fused-multiply-added by the
+// packed fp32x2 instructions: each element is rounded as by the scalar
+// instruction, so sums are bit-identical to scalar code, with half the adds.
+__device__ __forceinline__ uint64_t f2_pack(uint32_t lo_bits, uint32_t hi_bits) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "r"(lo_bits), "r"(hi_bits));
+    return r;
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+    uint64_t r;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t r;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+    return r;
+}
+__device__ __forceinline__ float2 f2_unpack(uint64_t v) {
+    float2 f;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(f.x), "=f"(f.y) : "l"(v));
+    return f;
+}
+
 template <bool kWeighted, bool kExpanded, int kGroups, int kB>
 __device__ __forceinline__ void combine_item(const CombineParams& p, int64_t it, int group, int gtid,
                                              int* s_rows, float* s_coef, int* s_n) {
@@ -119,9 +143,7 @@ __device__ __forceinline__ void combine_item(const CombineParams& p, int64_t it,
     const int v_end = min(n_vec, v_begin + p.chunk_vecs);
     const int64_t row_bytes = static_cast<int64_t>(p.H) * 2;
     for (int v = v_begin + gtid; v < v_end; v += kThreads) {
-        float acc[8];
-#pragma unroll
-        for (int q = 0; q < 8; ++q) acc[q] = 0.0f;
+        uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};   // channel pairs (2q, 2q + 1), +0.0f each
         const int64_t off = static_cast<int64_t>(v) * 16;
         for (int m0 = 0; m0 < n; m0 += kB) {
             uint4 buf[kB];
@@ -133,18 +155,14 @@ __device__ __forceinline__ void combine_item(const CombineParams& p, int64_t it,
                 if (m0 + j < n) {
                     const uint32_t w[4] = {buf[j].x, buf[j].y, buf[j].z, buf[j].w};
                     if (kWeighted) {
-                        const float cf = s_coef[m0 + j];
+                        const uint32_t cb = __float_as_uint(s_coef[m0 + j]);
+                        const uint64_t cf2 = f2_pack(cb, cb);
 #pragma unroll
-                        for (int q = 0; q < 4; ++q) {
-                            acc[2 * q] = fmaf(cf, __uint_as_float(w[q] << 16), acc[2 * q]);
-                            acc[2 * q + 1] = fmaf(cf, __uint_as_float(w[q] & 0xffff0000u), acc[2 * q + 1]);
-                        }
+                        for (int q = 0; q < 4; ++q)
+                            acc[q] = f2_fma(cf2, f2_pack(w[q] << 16, w[q] & 0xffff0000u), acc[q]);
                     } else {
 #pragma unroll
-                        for (int q = 0; q < 4; ++q) {
-                            acc[2 * q] += __uint_as_float(w[q] << 16);
-                            acc[2 * q + 1] += __uint_as_float(w[q] & 0xffff0000u);
-                        }
+                        for (int q = 0; q < 4; ++q) acc[q] = f2_add(acc[q], f2_pack(w[q] << 16, w[q] & 0xffff0000u));
                     }
                 }
             }
@@ -153,7 +171,8 @@ __device__ __forceinline__ void combine_item(const CombineParams& p, int64_t it,
         uint32_t* ow = reinterpret_cast<uint32_t*>(&o);
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
-            const __nv_bfloat162 h = __floats2bfloat162_rn(acc[2 * q], acc[2 * q + 1]);
+            const float2 a = f2_unpack(acc[q]);
+            const __nv_bfloat162 h = __floats2bfloat162_rn(a.x, a.y);
             ow[q] = *reinterpret_cast<const uint32_t*>(&h);
         }
         st_v4(p.out + static_cast<int64_t>(t) * row_bytes + off, o);
