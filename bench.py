@@ -57,10 +57,13 @@ def host_cpu():
         pass
     return {"host_cores": os.cpu_count(), "cpu_model": model}
 def kernels_per_step(T, R, expanded=False, hierarchical=False):
-    """Launches of this library per step: the layout is one cluster kernel, or
-    three tiled kernels when T*R is large or expanded or node rows are wanted;
-    dispatch and combine one each, two each on the hierarchical path."""
-    tiled = expanded or hierarchical or T * R > (1 << 19)
+    """Launches of this library per step: the layout is one kernel (the
+    single-CTA kernel for few tokens, else one cluster), or three tiled kernels
+    when T*R passes 2^19 (expanded and node rows ride on the same kernels; the
+    tiled fallback for a cluster whose shared memory would not fit does not
+    occur on these workloads); dispatch and combine one each, two each on the
+    hierarchical path."""
+    tiled = T * R > (1 << 19)
     return (3 if tiled else 1) + (4 if hierarchical else 2)
 
 
