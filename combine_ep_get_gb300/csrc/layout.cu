@@ -267,18 +267,18 @@ __device__ __forceinline__ unsigned match_key(int key, uint32_t* kb, int lane) {
 // Ranks entries [0, n_ent) per expert in index order: entry i with key
 // e >= 0 (s_key[i]; negative keys are unique per lane and never match) gets
 // out[i] = s_eb[e] + (entries of e before i), else -1.  Warps 0..nw-1 each
-// rank a contiguous slice of 32-entry chunks twice (count, then place) with
-// equal keys grouped by match_key, around per-(warp, expert) bases in s_wc
-// [nw][E]; s_wc and the key groups [nw][E] that follow it in shared memory
-// are zero on entry (the key groups are left zero).  The
-// order never depends on timing.  Every thread of the block calls it (block
-// barriers inside).
+// rank a contiguous slice of 32-entry chunks twice around per-(warp, expert)
+// bases in s_wc [nw][E]: pass 1 groups equal keys by match_key, counts them
+// per expert and overwrites s_key[i] with (key, group size, rank in group)
+// packed in 22 bits (E <= 2048); pass 2 places from that record.  s_wc and the
+// key groups [nw][E] that follow it in shared memory are zero on entry (the
+// key groups are left zero).  The order never depends on timing.  Every
+// thread of the block calls it (block barriers inside).
 constexpr int kRankWarps = 8;
 // Rank warps of the tiled path: 4 above 1024 experts, so that its counters and
 // key groups (2 x warps x E ints) fit beside the staged entries.
 __host__ __device__ inline int tiled_rank_warps(int E) { return E > 1024 ? kRankWarps / 2 : kRankWarps; }
-__device__ void rank_entries(const int* s_key, int n_ent, int E, const int* s_eb, int* s_wc, int32_t* out,
-                             int nw) {
+__device__ void rank_entries(int* s_key, int n_ent, int E, const int* s_eb, int* s_wc, int32_t* out, int nw) {
     uint32_t* s_kb = reinterpret_cast<uint32_t*>(s_wc + nw * E);
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int chunks = (n_ent + 31) / 32;
@@ -290,6 +290,7 @@ __device__ void rank_entries(const int* s_key, int n_ent, int E, const int* s_eb
         const int key = i < n_ent ? s_key[i] : -1 - lane;
         const unsigned g = match_key(key, s_kb + warp * E, lane);
         if (key >= 0 && lane == __ffs(g) - 1) s_wc[warp * E + key] += __popc(g);
+        if (key >= 0 && i < n_ent) s_key[i] = (key << 11) | (__popc(g) << 5) | __popc(g & ((1u << lane) - 1u));
         __syncwarp();
     }
     __syncthreads();
@@ -304,12 +305,12 @@ __device__ void rank_entries(const int* s_key, int n_ent, int E, const int* s_eb
     __syncthreads();
     for (int c = c0; c < c1; ++c) {                     // pass 2: place
         const int i = c * 32 + lane;
-        const int key = i < n_ent ? s_key[i] : -1 - lane;
-        const unsigned g = match_key(key, s_kb + warp * E, lane);
+        const int rec = i < n_ent ? s_key[i] : -1;   // key << 11 | group size << 5 | rank in group
+        const int key = rec >> 11;
         int pos = -1;
-        if (key >= 0) pos = s_wc[warp * E + key] + __popc(g & ((1u << lane) - 1u));
+        if (rec >= 0) pos = s_wc[warp * E + key] + (rec & 31);
         __syncwarp();
-        if (key >= 0 && lane == __ffs(g) - 1) s_wc[warp * E + key] += __popc(g);
+        if (rec >= 0 && (rec & 31) == 0) s_wc[warp * E + key] += (rec >> 5) & 63;
         __syncwarp();
         if (i < n_ent) out[i] = pos;
     }
