@@ -148,3 +148,39 @@ def test_fp8_wide_sm_limited_matches_default(expanded, num_sms):
     got = _dispatch(B, x, idx, w, E, R, lay, n, H, K, True, num_sms, expanded)
     for a, b in zip(ref, got):
         assert torch.equal(a, b)
+
+
+@pytest.mark.parametrize("num_sms", [3, 40])
+@pytest.mark.parametrize("fp8", [False, True])
+def test_sm_limited_capacity_overflow(num_sms, fp8):
+    """SM-limited dispatch into too few receive rows, and combine from too few
+    expert-output rows: the capacity bit is set and every row that fits is
+    what the default mode writes."""
+    from gpu_path import B, x_tensor
+    T, H, E, K, R = 600, 1024, 64, 6, 8
+    d, idx, w, x, lay = _setup(T, H, E, K, R, seed=31)
+    n = lay.num_recv
+    cap = n - 57
+    outs = []
+    for ns in (0, num_sms):
+        rx = torch.zeros((cap, H), dtype=torch.uint8 if fp8 else torch.bfloat16, device="cuda")
+        rsf = torch.zeros((cap * (H // 128),), dtype=torch.float32, device="cuda") if fp8 else None
+        rs = torch.full((cap,), -1, dtype=torch.int32, device="cuda")
+        st = torch.zeros(1, dtype=torch.int32, device="cuda")
+        B.ep_dispatch(x, idx, w, E, R, lay, rx, None, None, rs, st, recv_sf=rsf,
+                      out_dtype=B.EP_FP8_E4M3 if fp8 else B.EP_BF16, num_sms=ns)
+        torch.cuda.synchronize()
+        assert int(st.item()) & B.EP_ERR_CAPACITY
+        outs.append((rx.view(torch.uint8).clone(), rs.clone()))
+    assert torch.equal(outs[0][0], outs[1][0]) and torch.equal(outs[0][1], outs[1][1])
+    y = x_tensor(make_rows(cap, H, seed=32))
+    res = []
+    for ns in (0, num_sms):
+        out = torch.zeros((T, H), dtype=torch.bfloat16, device="cuda")
+        st = torch.zeros(1, dtype=torch.int32, device="cuda")
+        B.ep_combine(y, idx, w, E, R, lay, out, st, num_sms=ns)
+        torch.cuda.synchronize()
+        assert int(st.item()) & B.EP_ERR_CAPACITY
+        res.append(out.view(torch.int16).clone())
+    assert torch.equal(res[0], res[1])
+
