@@ -64,7 +64,8 @@ def _load():
     lib.ep_oracle_expanded_rows.argtypes = [vp, ctypes.c_int, ctypes.c_int, ctypes.c_int, vp, vp, vp]
     lib.ep_oracle_dispatch_expanded.restype = ctypes.c_int
     lib.ep_oracle_dispatch_expanded.argtypes = [vp, vp, ctypes.c_int, ctypes.c_int, ctypes.c_int, vp,
-                                                ctypes.c_int64, ctypes.c_int, vp, vp, vp, vp]
+                                                ctypes.c_int64, ctypes.c_int, ctypes.c_int, ctypes.c_int64,
+                                                vp, vp, vp, vp]
     lib.ep_oracle_combine_expanded.restype = ctypes.c_int
     lib.ep_oracle_combine_expanded.argtypes = [vp, ctypes.c_int64, vp, ctypes.c_int, ctypes.c_int,
                                                ctypes.c_int, ctypes.c_int, vp, vp]
@@ -224,8 +225,15 @@ def expanded_rows(topk_idx, E, expert_offset):
     return out, status
 
 
-def dispatch_expanded(x_bits, topk_weights, expanded_row, capacity, fp8=False):
-    """Expanded dispatch (see ep_oracle_dispatch_expanded); arrays sized by capacity."""
+def dispatch_expanded(x_bits, topk_weights, expanded_row, capacity, fp8=False, sf_col_major=False,
+                      sf_stride=None, sf_fill=0.0):
+    """Expanded dispatch (see ep_oracle_dispatch_expanded); arrays sized by capacity.
+
+    FP8 scales come back as [capacity, H/128] (row-major) or, with
+    ``sf_col_major``, as the flat column-major array of H/128 columns of
+    ``sf_stride`` entries (default: capacity).  Entries no row writes (expert
+    padding rows, the stride's tail) keep ``sf_fill``.
+    """
     lib = _load()
     x_bits = np.ascontiguousarray(x_bits, dtype=np.uint16)
     T, H = x_bits.shape
@@ -234,17 +242,24 @@ def dispatch_expanded(x_bits, topk_weights, expanded_row, capacity, fp8=False):
     K = expanded_row.shape[1]
     n = max(int(capacity), 1)
     row_bytes = H if fp8 else 2 * H
+    nb = H // 128
+    if sf_stride is None:
+        sf_stride = int(capacity)
+    assert sf_stride >= capacity
     recv_x = np.zeros((n, row_bytes), np.uint8)
-    recv_sf = np.zeros((n, H // 128), np.float32) if fp8 else None
+    recv_sf = None
+    if fp8:
+        recv_sf = np.full(max(nb * sf_stride, 1) if sf_col_major else n * nb, sf_fill, np.float32)
     recv_src_idx = np.full(n, -1, np.int32)
     recv_weight = np.zeros(n, np.float32)
     status = lib.ep_oracle_dispatch_expanded(_p(x_bits), _p(topk_weights), T, H, K, _p(expanded_row),
-                                             int(capacity), 1 if fp8 else 0, _p(recv_x), _p(recv_sf),
+                                             int(capacity), 1 if fp8 else 0, 1 if sf_col_major else 0,
+                                             int(sf_stride), _p(recv_x), _p(recv_sf),
                                              _p(recv_src_idx), _p(recv_weight))
     res = dict(recv_x=recv_x[:capacity], recv_src_idx=recv_src_idx[:capacity],
                recv_weight=recv_weight[:capacity], status=status)
     if fp8:
-        res["recv_sf"] = recv_sf[:capacity]
+        res["recv_sf"] = recv_sf[:nb * sf_stride] if sf_col_major else recv_sf.reshape(n, nb)[:capacity]
     return res
 
 

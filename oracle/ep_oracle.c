@@ -432,8 +432,13 @@ int ep_oracle_expanded_rows(const int64_t* topk_idx, int T, int K, int E,
 
 /* Expanded dispatch: row expanded_row[t,k] receives x[t] (bf16 copy or the  */
 /* FP8 cast), its source token t and its weight topk_weights[t,k].         */
+/* FP8 scales: row-major [row][block], or with sf_col_major the TMA-aligned  */
+/* column-major form of [P2 SF-layout fragment] / [P1 section 6.1]          */
+/* (sf_token_stride = 1, sf_hidden_stride = sf_stride): scale (row, b) at   */
+/* b * sf_stride + row.  Padding rows of an expert block are not written.   */
 int ep_oracle_dispatch_expanded(const uint16_t* x, const float* topk_weights, int T, int H, int K,
                                 const int32_t* expanded_row, int64_t capacity, int fp8,
+                                int sf_col_major, int64_t sf_stride,
                                 uint8_t* recv_x, float* recv_sf, int32_t* recv_src_idx,
                                 float* recv_weight)
 {
@@ -452,7 +457,10 @@ int ep_oracle_dispatch_expanded(const uint16_t* x, const float* topk_weights, in
                 ep_oracle_fp8_cast_row(src, H, q_tmp, sf_tmp);
                 memcpy(recv_x + (int64_t)d * (int64_t)row_bytes, q_tmp, row_bytes);
                 if (recv_sf)
-                    for (int b = 0; b < nb; ++b) recv_sf[(int64_t)d * nb + b] = sf_tmp[b];
+                    for (int b = 0; b < nb; ++b) {
+                        if (sf_col_major) recv_sf[(int64_t)b * sf_stride + d] = sf_tmp[b];
+                        else recv_sf[(int64_t)d * nb + b] = sf_tmp[b];
+                    }
             } else {
                 memcpy(recv_x + (int64_t)d * (int64_t)row_bytes, src, row_bytes);
             }

@@ -102,3 +102,38 @@ def test_combine_against_scatter_add():
     np.add.at(ref, t_of, d["topk_weights"][t_of, k_of].astype(np.float64)[:, None] * yf[rows[t_of, k_of]])
     out, _ = oracle.combine_expanded(y, d["topk_weights"], rows, weighted=True)
     np.testing.assert_allclose(out, ref, rtol=1e-12, atol=1e-12)
+
+
+@pytest.mark.parametrize("align", [1, 16])
+def test_dispatch_fp8_col_major_scales_are_the_transpose(align):
+    """Column-major FP8 scales of the expanded dispatch (the TMA-aligned
+    scale layout a grouped GEMM loads): scale (row, b) sits at
+    b * stride + row, with stride = capacity rounded up to 4.  Against the
+    row-major result of the same call: every written row's scales are its
+    row-major scales, and the entries of padding rows and of the stride's
+    tail keep the fill value."""
+    T, H, E, K, R = 90, 512, 32, 5, 4
+    d = make_inputs(T, H, E, K, R, seed=11 + align, mask_frac=0.1)
+    L = oracle.layout(d["topk_idx"], E, R, 0, align)
+    rows, _ = oracle.expanded_rows(d["topk_idx"], E, L.expert_offset)
+    cap = int(L.expert_offset[-1])
+    stride = (cap + 3) // 4 * 4
+    nb = H // 128
+    rm = oracle.dispatch_expanded(d["x_bits"], d["topk_weights"], rows, cap, fp8=True)
+    cm = oracle.dispatch_expanded(d["x_bits"], d["topk_weights"], rows, cap, fp8=True, sf_col_major=True,
+                                  sf_stride=stride, sf_fill=-5.0)
+    assert rm["status"] == 0 and cm["status"] == 0
+    np.testing.assert_array_equal(cm["recv_x"], rm["recv_x"])
+    written = np.unique(rows[rows >= 0])
+    cols = cm["recv_sf"].reshape(nb, stride)
+    np.testing.assert_array_equal(cols[:, written].T, rm["recv_sf"][written])
+    unwritten = np.setdiff1d(np.arange(stride), written)
+    if align > 1:
+        assert len(unwritten) > stride - cap        # padding rows exist inside the columns
+    assert (cols[:, unwritten] == -5.0).all()
+    # the scales themselves follow the single-row cast
+    for t in (0, T // 2, T - 1):
+        for k in range(K):
+            if rows[t, k] >= 0:
+                _, sf = oracle.fp8_cast_row(d["x_bits"][t])
+                np.testing.assert_array_equal(cols[:, rows[t, k]], sf)
