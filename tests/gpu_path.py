@@ -82,24 +82,3 @@ def run_combine(y_dev, idx_dev, w_dev, E, R, lay, T, H):
 
 def bf16_bits(t):
     return t.contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
-
-
-def combine_tolerance(y_bits, idx, w, E, R, dst_row, weighted, tokens=None):
-    """Elementwise bound 1e-2 * sum_r |c(t,r) * y[dst_row[t,r]]| (fp64, host)."""
-    T, K = idx.shape
-    el = E // R
-    toks = np.arange(T) if tokens is None else np.asarray(tokens)
-    H = y_bits.shape[1]
-    yf = (y_bits.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
-    bound = np.zeros((len(toks), H))
-    for i, t in enumerate(toks):
-        for r in range(R):
-            d = dst_row[t, r]
-            if d < 0:
-                continue
-            if weighted:
-                c = sum(float(w[t, k]) for k in range(K) if idx[t, k] >= 0 and idx[t, k] // el == r)
-            else:
-                c = 1.0
-            bound[i] += np.abs(c * yf[d])
-    return 1e-2 * bound

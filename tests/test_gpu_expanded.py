@@ -9,6 +9,7 @@ import torch
 
 import oracle
 from combine_ep_get_gb300.inputs import CONFIGS, make_config, make_inputs, make_rows
+from tolerance import check_close, combine_bounds, expanded_sources
 
 pytestmark = pytest.mark.gpu
 
@@ -75,15 +76,17 @@ def test_expanded_dispatch(fp8, T, H, E, K, R, align, mask):
     _check_expanded_dispatch(fp8, T, H, E, K, R, align, mask, seed=T + H)
 
 
-def _check_expanded_dispatch(fp8, T, H, E, K, R, align, mask, seed):
+def _check_expanded_dispatch(fp8, T, H, E, K, R, align, mask, seed, sf_col_major=False, num_sms=0):
     from gpu_path import B, bf16_bits, x_tensor
     d = make_inputs(T, H, E, K, R, seed=seed, mask_frac=mask)
     idx, lay, _ = _layout(d["topk_idx"], E, R, align)
     w = torch.from_numpy(d["topk_weights"]).cuda()
     cap = int(lay.expert_offset[-1].item())
+    sf_stride = (cap + 3) // 4 * 4      # the library's column stride: capacity rounded up to 4
     if fp8:
         rx = torch.full((cap, H), 0x55, dtype=torch.uint8, device="cuda")
-        rsf = torch.full((cap * (H // 128),), -1.0, dtype=torch.float32, device="cuda")
+        n_sf = (H // 128) * sf_stride if sf_col_major else cap * (H // 128)
+        rsf = torch.full((max(n_sf, 1),), -1.0, dtype=torch.float32, device="cuda")
     else:
         rx = torch.full((cap, H), -3.0, dtype=torch.bfloat16, device="cuda")
         rsf = None
@@ -91,18 +94,41 @@ def _check_expanded_dispatch(fp8, T, H, E, K, R, align, mask, seed):
     rw = torch.full((cap,), -9.0, dtype=torch.float32, device="cuda")
     st = torch.zeros(1, dtype=torch.int32, device="cuda")
     B.ep_dispatch_expanded(x_tensor(d["x_bits"]), idx, w, E, R, lay, rx, rs, rw, st, recv_sf=rsf,
-                           out_dtype=B.EP_FP8_E4M3 if fp8 else B.EP_BF16)
+                           out_dtype=B.EP_FP8_E4M3 if fp8 else B.EP_BF16, sf_col_major=sf_col_major,
+                           num_sms=num_sms)
     torch.cuda.synchronize()
     assert int(st.item()) == 0
     L, rows, _ = _oracle_rows(d["topk_idx"], E, R, align)
-    o = oracle.dispatch_expanded(d["x_bits"], d["topk_weights"], rows, cap, fp8=fp8)
+    o = oracle.dispatch_expanded(d["x_bits"], d["topk_weights"], rows, cap, fp8=fp8, sf_col_major=sf_col_major,
+                                 sf_stride=sf_stride, sf_fill=-1.0)
     valid = np.unique(rows[rows >= 0])
     gx = rx.cpu().numpy() if fp8 else bf16_bits(rx).view(np.uint8).reshape(cap, 2 * H)
     np.testing.assert_array_equal(gx[valid], o["recv_x"][valid])
     np.testing.assert_array_equal(rs.cpu().numpy(), o["recv_src_idx"])       # padding stays -1
     np.testing.assert_array_equal(rw.cpu().numpy()[valid], o["recv_weight"][valid])
-    if fp8:
-        np.testing.assert_array_equal(rsf.cpu().numpy().reshape(cap, H // 128)[valid], o["recv_sf"][valid])
+    if fp8 and sf_col_major:
+        # the whole column-major array: written rows' scales, and the fill of
+        # padding rows and of the stride's tail, untouched
+        np.testing.assert_array_equal(rsf.cpu().numpy()[:(H // 128) * sf_stride], o["recv_sf"])
+    elif fp8:
+        np.testing.assert_array_equal(rsf.cpu().numpy()[:cap * (H // 128)].reshape(cap, H // 128)[valid],
+                                      o["recv_sf"][valid])
+
+
+@pytest.mark.parametrize("T,H,E,K,R,align,mask,num_sms", [
+    (64, 7168, 256, 8, 32, 1, 0.0, 0),        # few-token lane mode (16 lanes per block)
+    (500, 1024, 64, 6, 8, 16, 0.1, 0),        # expert padding rows inside the scale columns
+    (1000, 256, 256, 8, 8, 128, 0.02, 0),     # mostly padding (alignment 128)
+    (2048, 1024, 64, 6, 8, 4, 0.05, 0),       # many-token lane mode (8 lanes per block)
+    (2048, 1024, 64, 6, 8, 4, 0.05, 16),      # SM-limited, many-token
+    (333, 2048, 96, 5, 12, 7, 0.1, 36),       # SM-limited, few-token, odd alignment
+    (3, 128, 16, 4, 4, 3, 0.0, 0),            # capacity not a multiple of 4: ragged stride tail
+])
+def test_expanded_dispatch_fp8_col_major(T, H, E, K, R, align, mask, num_sms):
+    """Expanded FP8 dispatch with TMA-aligned column-major scales (stride =
+    capacity rounded up to 4) against the oracle, element by element over the
+    whole scale array."""
+    _check_expanded_dispatch(True, T, H, E, K, R, align, mask, seed=T + 3 * H, sf_col_major=True, num_sms=num_sms)
 
 
 @pytest.mark.parametrize("weighted", [False, True])
@@ -128,12 +154,9 @@ def _check_expanded_combine(weighted, T, H, E, K, R, align, mask, seed):
     _, rows, _ = _oracle_rows(d["topk_idx"], E, R, align)
     toks = np.arange(T) if T <= 1000 else np.unique(np.concatenate([[0, T - 1], np.arange(0, T, 97)]))
     ref, _ = oracle.combine_expanded(y_bits, d["topk_weights"][toks], rows[toks], weighted=weighted)
-    yf = (y_bits.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
-    r = rows[toks]
-    c = d["topk_weights"][toks].astype(np.float64) if weighted else np.ones(r.shape)
-    bound = 1e-2 * (np.where(r >= 0, np.abs(c), 0.0)[:, :, None] * np.abs(yf[np.maximum(r, 0)])).sum(axis=1)
-    g = (bf16_bits(out)[toks].astype(np.uint32) << 16).view(np.float32).astype(np.float64)
-    assert (np.abs(g - ref) <= bound).all()
+    srows, c, a, m = expanded_sources(rows, d["topk_weights"], weighted, tokens=toks)
+    loose, tight = combine_bounds(y_bits, srows, c, a, ref, m)
+    check_close(bf16_bits(out)[toks], ref, loose, tight)
 
 
 def test_expanded_round_trip_closed_form():
@@ -185,11 +208,13 @@ def test_expanded_dispatch_fp8_wide():
 
 @pytest.mark.parametrize("i", range(24))
 def test_random_expanded_dispatch_combine(i):
-    """Expanded dispatch and weighted / unweighted combine on the random
-    sweep's shapes and alignments."""
+    """Expanded dispatch (FP8 cases alternate row- and column-major scales)
+    and weighted / unweighted combine on the random sweep's shapes and
+    alignments."""
     from test_gpu_random import _draw_case
     c = _draw_case(i)
-    _check_expanded_dispatch(c["fp8"], c["T"], c["H"], c["E"], c["K"], c["R"], c["align"], c["mask"], seed=c["seed"])
+    _check_expanded_dispatch(c["fp8"], c["T"], c["H"], c["E"], c["K"], c["R"], c["align"], c["mask"], seed=c["seed"],
+                             sf_col_major=c["fp8"] and i % 2 == 1)
     _check_expanded_combine(c["weighted"], c["T"], c["H"], c["E"], c["K"], c["R"], c["align"], c["mask"],
                             seed=c["seed"] + 3)
 

@@ -206,17 +206,44 @@ def _check_combine_hierarchical(weighted, T, H, E, K, R, rpn, mask, seed):
         coef[tt, rr] = 1.0
     scale_node = np.zeros((M, H))
     scale_tok = np.zeros((T, H))
+    n_node = np.zeros(M)
     for t, r in zip(tt, rr):
         a = coef[t, r] * np.abs(yf[L.dst_row[t, r]])
         scale_node[rows[t, r // rpn]] += a
         scale_tok[t] += a
+        n_node[rows[t, r // rpn]] += 1
     g_node = oracle.bf16_to_float(bf16_bits(node_y).reshape(M, H)).astype(np.float64)
     want_node = oracle.bf16_to_float(ony).astype(np.float64)
     assert (np.abs(g_node - want_node) <= 1e-2 * scale_node).all()
+    _check_two_stage_tight(g_node, want_node, n_node, scale_node, K if weighted else 0, rows, bf16_bits(out), T, H)
     g_out = oracle.bf16_to_float(bf16_bits(out).reshape(T, H)).astype(np.float64)
     assert (np.abs(g_out - oout) <= 1e-2 * scale_tok).all()
     empty = L.is_token_in_rank.sum(axis=1) == 0
     assert (g_out[empty] == 0).all()
+
+
+def _check_two_stage_tight(g_node, want_node, n_node, scale_node, m, node_rows, out_bits, T, H):
+    """fp32-accumulation bounds of both stages (tests/tolerance.py).
+    Stage 1: the GPU's node partial bf16(P32) and the oracle's bf16(P) are
+    each within 2^-8 |P| (+ the fp32 error of P32) of the exact partial P,
+    and |P| <= |bf16(P)| / (1 - 2^-8).  Stage 2: the output is bf16 of the
+    fp32 sum of the GPU's own node partials."""
+    from tolerance import BF16_MIN_SUBNORMAL, U32, U_BF16, bf16_bits_to_f64, sum_bound
+    p_abs = np.abs(want_node) / (1.0 - U_BF16)
+    tight_node = (2.0 * U_BF16 * p_abs + 2.0 * (n_node[:, None] + m + 1) * U32 * scale_node
+                  + 2.0 * BF16_MIN_SUBNORMAL)
+    assert (np.abs(g_node - want_node) <= tight_node).all()
+    exact = np.zeros((T, H))
+    mag = np.zeros((T, H))
+    n_parts = np.zeros(T)
+    for n in range(node_rows.shape[1]):
+        ok = node_rows[:, n] >= 0
+        part = g_node[node_rows[ok, n]]
+        exact[ok] += part
+        mag[ok] += np.abs(part)
+        n_parts += ok
+    g_out = bf16_bits_to_f64(out_bits.reshape(T, H))
+    assert (np.abs(g_out - exact) <= sum_bound(exact, mag, n_parts)).all()
 
 
 def test_combine_hierarchical_identity_full_size():
@@ -291,6 +318,7 @@ def test_combine_hierarchical_short_y(weighted):
     el = E // R
     scale_node = np.zeros((M, H))
     scale_tok = np.zeros((T, H))
+    n_node = np.zeros(M)
     tt, rr = np.nonzero((L.dst_row >= 0) & (L.dst_row < n_y))
     for t, r in zip(tt, rr):
         c = 1.0
@@ -300,9 +328,11 @@ def test_combine_hierarchical_short_y(weighted):
         a = c * np.abs(yf[L.dst_row[t, r]])
         scale_node[rows[t, r // rpn]] += a
         scale_tok[t] += a
+        n_node[rows[t, r // rpn]] += 1
     g_node = oracle.bf16_to_float(bf16_bits(node_y).reshape(M, H)).astype(np.float64)
     want_node = oracle.bf16_to_float(ony).astype(np.float64)
     assert (np.abs(g_node - want_node) <= 1e-2 * scale_node).all()
+    _check_two_stage_tight(g_node, want_node, n_node, scale_node, K if weighted else 0, rows, bf16_bits(out), T, H)
     g_out = oracle.bf16_to_float(bf16_bits(out).reshape(T, H)).astype(np.float64)
     assert (np.abs(g_out - oout) <= 1e-2 * scale_tok).all()
 

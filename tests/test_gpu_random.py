@@ -38,16 +38,10 @@ def _draw_case(i):
                 seed=2000 + i)
 
 
-def _close(gpu_bits, ref, bound):
-    g = (gpu_bits.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
-    bad = np.abs(g - ref) > bound
-    assert not bad.any(), (np.argwhere(bad)[:5], g[bad][:5], ref[bad][:5])
-
-
 @pytest.mark.parametrize("i", range(N_CASES))
 def test_random_layout_dispatch_combine(i):
-    from gpu_path import (bf16_bits, combine_tolerance, layout_host, run_combine, run_dispatch, run_layout,
-                          to_dev, x_tensor)
+    from gpu_path import bf16_bits, layout_host, run_combine, run_dispatch, run_layout, to_dev, x_tensor
+    from tolerance import check_close, rank_combine_bounds
     c = _draw_case(i)
     T, H, E, K, R = c["T"], c["H"], c["E"], c["K"], c["R"]
     d = make_inputs(T, H, E, K, R, seed=c["seed"], mask_frac=c["mask"])
@@ -87,8 +81,8 @@ def test_random_layout_dispatch_combine(i):
     out, st = run_combine(x_tensor(y_bits), idx, w if c["weighted"] else None, E, R, lay, T, H)
     assert int(st.item()) == 0, c
     ref, _ = oracle.combine(y_bits, idx_h, w_h, E, R, L.dst_row, weighted=c["weighted"])
-    bound = combine_tolerance(y_bits, idx_h, w_h, E, R, L.dst_row, c["weighted"])
-    _close(bf16_bits(out), ref, bound)
+    loose, tight = rank_combine_bounds(y_bits, idx_h, w_h, E, R, L.dst_row, c["weighted"], ref)
+    check_close(bf16_bits(out), ref, loose, tight)
 
 
 @pytest.mark.parametrize("i", range(N_CASES))

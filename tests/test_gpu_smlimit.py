@@ -91,7 +91,8 @@ def test_combine_sm_limited_matches_default(expanded, weighted, num_sms):
 def test_combine_ring_shapes_and_empty_tokens(T, H, E, K, R, num_sms):
     """The SM-limited combine (shared-memory ring) against the oracle, with
     tokens whose entries are all masked (items without source rows)."""
-    from gpu_path import B, bf16_bits, combine_tolerance, to_dev, x_tensor
+    from gpu_path import B, bf16_bits, to_dev, x_tensor
+    from tolerance import check_close, rank_combine_bounds
     d = make_inputs(T, H, E, K, R, seed=T + K, mask_frac=0.1, with_x=False)
     d["topk_idx"][[0, T // 2, T - 1]] = -1
     idx, w = to_dev(d["topk_idx"]), to_dev(d["topk_weights"])
@@ -109,9 +110,9 @@ def test_combine_ring_shapes_and_empty_tokens(T, H, E, K, R, num_sms):
         torch.cuda.synchronize()
         assert int(st.item()) == 0
         ref, _ = oracle.combine(y_bits, d["topk_idx"], d["topk_weights"], E, R, L.dst_row, weighted=weighted)
-        bound = combine_tolerance(y_bits, d["topk_idx"], d["topk_weights"], E, R, L.dst_row, weighted)
-        g = (bf16_bits(out).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
-        assert (np.abs(g - ref) <= bound).all()
+        loose, tight = rank_combine_bounds(y_bits, d["topk_idx"], d["topk_weights"], E, R, L.dst_row, weighted,
+                                           ref)
+        check_close(bf16_bits(out), ref, loose, tight)
         assert (bf16_bits(out)[[0, T // 2, T - 1]] == 0).all()
 
 
