@@ -69,6 +69,9 @@ namespace {
 #ifndef EP_DISPATCH_FP8_WIDE_MIN_BLOCKS
 #define EP_DISPATCH_FP8_WIDE_MIN_BLOCKS 5   // same, many-token rank-row mode (fits 48 registers unspilled)
 #endif
+#ifndef EP_DISPATCH_FP8_FIT_WARPS
+#define EP_DISPATCH_FP8_FIT_WARPS 1       // FP8 many-token mode: CTA warps fitted to the piece's blocks
+#endif
 #ifndef EP_DISPATCH_FP8_PIECE_BLOCKS
 #define EP_DISPATCH_FP8_PIECE_BLOCKS 64   // FP8 path: 128-channel blocks per piece (<= 64)
 #endif
@@ -482,10 +485,10 @@ constexpr int kFp8Rounds = 2;   // rounds of blocks per item (loads of every rou
 // to every destination.
 template <bool kExpanded, int kLanes>
 __device__ __forceinline__ void dispatch_fp8_item(const DispatchParams& p, int64_t it, int gtid, int lane,
-                                                  bool& cap_bad) {
+                                                  int group_warps, bool& cap_bad) {
     constexpr int kVec = 128 / kLanes / 8;                     // 16-byte input vectors per lane per block
     constexpr int kBlocksPerWarp = 32 / kLanes;
-    constexpr int kBlocksPerRound = kBlocksPerWarp * (kFp8Threads / 32);
+    const int blocks_per_round = kBlocksPerWarp * group_warps;
     const int t = static_cast<int>(it / p.chunks);
     const int c = static_cast<int>(it - static_cast<int64_t>(t) * p.chunks);
     const int warp_g = gtid >> 5;
@@ -498,7 +501,7 @@ __device__ __forceinline__ void dispatch_fp8_item(const DispatchParams& p, int64
     uint4 v[kFp8Rounds][kVec];
 #pragma unroll
     for (int q = 0; q < kFp8Rounds; ++q) {
-        const int b = b_begin + q * kBlocksPerRound + kBlocksPerWarp * warp_g + grp;
+        const int b = b_begin + q * blocks_per_round + kBlocksPerWarp * warp_g + grp;
         const uint8_t* src = xrow + static_cast<size_t>(b) * 256 + sub * (16 * kVec);
 #pragma unroll
         for (int u = 0; u < kVec; ++u) v[q][u] = b < b_end ? ld_stream_v4(src + 16 * u) : make_uint4(0, 0, 0, 0);
@@ -531,7 +534,7 @@ __device__ __forceinline__ void dispatch_fp8_item(const DispatchParams& p, int64
     const int b0 = b_begin + kBlocksPerWarp * warp_g + grp;   // this lane's block in round 0
     uint32_t code[kFp8Rounds][2 * kVec];
     float sfq[kFp8Rounds];
-    auto warp_has_round = [&](int q) { return b_begin + q * kBlocksPerRound + kBlocksPerWarp * warp_g < b_end; };
+    auto warp_has_round = [&](int q) { return b_begin + q * blocks_per_round + kBlocksPerWarp * warp_g < b_end; };
     auto cast_round = [&](int q) {
         sfq[q] = 1.0f;
 #pragma unroll
@@ -586,7 +589,7 @@ __device__ __forceinline__ void dispatch_fp8_item(const DispatchParams& p, int64
                 uint8_t* row = p.recv_x + dd * p.H + sub_col;
 #pragma unroll
                 for (int q = 0; q < kFp8Rounds; ++q) {
-                    const int b = b0 + q * kBlocksPerRound;
+                    const int b = b0 + q * blocks_per_round;
                     if (q >= q_lo && q < q_hi && b < b_end) {
                         uint8_t* dst = row + static_cast<int64_t>(b) * 128;
                         if (kVec == 2)
@@ -630,19 +633,21 @@ __global__ void __launch_bounds__(kFp8Threads * kGroups,
                                   : (kLanes == 8 && !kExpanded) ? EP_DISPATCH_FP8_WIDE_MIN_BLOCKS
                                                                 : EP_DISPATCH_FP8_MIN_BLOCKS)
     dispatch_fp8_kernel(const DispatchParams p) {
-    const int gtid = static_cast<int>(threadIdx.x) % kFp8Threads;
+    // one CTA per item: blockDim.x / 32 warps (up to 8, as many as the
+    // piece's blocks need); SM-limited groups: 8 warps each
+    const int gtid = kGroups == 1 ? static_cast<int>(threadIdx.x) : static_cast<int>(threadIdx.x) % kFp8Threads;
     const int lane = threadIdx.x & 31;
     bool cap_bad = false;
     if (kGroups == 1) prefetch_x<true>(p);
     pdl_wait();   // before any load: the previous kernel may write x
     if (kGroups == 1) {
-        dispatch_fp8_item<kExpanded, kLanes>(p, blockIdx.x, gtid, lane, cap_bad);
+        dispatch_fp8_item<kExpanded, kLanes>(p, blockIdx.x, gtid, lane, static_cast<int>(blockDim.x) / 32, cap_bad);
     } else {
         const int64_t n_items = static_cast<int64_t>(p.T) * p.chunks;
         const int group = static_cast<int>(threadIdx.x) / kFp8Threads;
         for (int64_t it = static_cast<int64_t>(blockIdx.x) * kGroups + group; it < n_items;
              it += static_cast<int64_t>(gridDim.x) * kGroups)
-            dispatch_fp8_item<kExpanded, kLanes>(p, it, gtid, lane, cap_bad);
+            dispatch_fp8_item<kExpanded, kLanes>(p, it, gtid, lane, kFp8Threads / 32, cap_bad);
     }
     if ((gtid >> 5) == 0 && __any_sync(0xffffffffu, cap_bad) && lane == 0) atomicOr(p.status, EP_ERR_CAPACITY);
 }
@@ -746,12 +751,32 @@ cudaError_t launch_dispatch_fp8_t(DispatchParams p, int num_sms, cudaStream_t st
         if (p.expanded_row) return launch_pdl(dispatch_fp8_kernel<true, kSmGroups, kLanes>, grid, block, 0, stream, p);
         return launch_pdl(dispatch_fp8_kernel<false, kSmGroups, kLanes>, grid, block, 0, stream, p);
     }
-    const dim3 grid(static_cast<unsigned>(items)), block(kFp8Threads);
-    p.prefetch_ctas = device_info().num_sms * ((kLanes == 8 && !p.expanded_row) ? EP_DISPATCH_FP8_WIDE_MIN_BLOCKS
-                                                                              : EP_DISPATCH_FP8_MIN_BLOCKS);
+    // Many tokens: as many warps per CTA as the piece's blocks need (a warp
+    // casts 4 blocks per round), so a 56-block row (H = 7168) runs 7 warps
+    // with no idle lanes and fits 6 CTAs per SM instead of 5.
+    int warps = kFp8Threads / 32;
+    if (kLanes == 8 && EP_DISPATCH_FP8_FIT_WARPS) {
+        warps = (p.chunk_blocks + kFp8Rounds * 4 - 1) / (kFp8Rounds * 4);
+        if (warps > kFp8Threads / 32) warps = kFp8Threads / 32;
+        if (warps < 2) warps = 2;   // warp 1 writes the metadata
+    }
+    const dim3 grid(static_cast<unsigned>(items)), block(32 * warps);
+    auto kernel = p.expanded_row ? dispatch_fp8_kernel<true, 1, kLanes> : dispatch_fp8_kernel<false, 1, kLanes>;
+    // CTAs resident per SM at this size: the first wave, which prefetches
+    static thread_local int occ_device = -1, occ_threads = 0, occ_expanded = -1, occ_ctas = 1;
+    const int dev = device_info().device;
+    if (occ_device != dev || occ_threads != 32 * warps || occ_expanded != (p.expanded_row != nullptr)) {
+        int nb_sm = 0;
+        const cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb_sm, kernel, 32 * warps, 0);
+        if (e != cudaSuccess) return e;
+        occ_ctas = nb_sm > 0 ? nb_sm : 1;
+        occ_device = dev;
+        occ_threads = 32 * warps;
+        occ_expanded = p.expanded_row != nullptr;
+    }
+    p.prefetch_ctas = device_info().num_sms * occ_ctas;
     p.prefetch_items = EP_DISPATCH_PREFETCH;
-    if (p.expanded_row) return launch_pdl(dispatch_fp8_kernel<true, 1, kLanes>, grid, block, 0, stream, p);
-    return launch_pdl(dispatch_fp8_kernel<false, 1, kLanes>, grid, block, 0, stream, p);
+    return launch_pdl(kernel, grid, block, 0, stream, p);
 }
 
 cudaError_t launch_dispatch_fp8(DispatchParams p, cudaStream_t stream) {

@@ -216,6 +216,7 @@ def test_dispatch_fp8_wide_full_size(sf_col_major):
     om = oracle.dispatch(stand_in, d["topk_idx"], d["topk_weights"], c.E, c.R, L.dst_row)
     np.testing.assert_array_equal(res["recv_src_idx"][:n].cpu().numpy(), om["recv_src_idx"])
     np.testing.assert_array_equal(res["recv_topk_idx"][:n].cpu().numpy(), om["recv_topk_idx"])
+    np.testing.assert_array_equal(res["recv_topk_weights"][:n].cpu().numpy(), om["recv_topk_weights"])
     rng = np.random.Generator(np.random.PCG64(7))
     toks = np.unique(np.concatenate([[0, c.T - 1], rng.choice(c.T, 40, replace=False)])).astype(np.int32)
     os_ = oracle.dispatch(d["x_bits"], d["topk_idx"], d["topk_weights"], c.E, c.R, L.dst_row, fp8=True,
@@ -230,3 +231,33 @@ def test_dispatch_fp8_wide_full_size(sf_col_major):
     else:
         got = sf[:n * nb].reshape(n, nb)[rows]
     np.testing.assert_array_equal(got, os_["recv_sf"])
+
+
+@pytest.mark.parametrize("T,H,E,K,R,mask,sf_col_major", [
+    (1300, 9216, 256, 8, 128, 0.05, False),   # two passes of blocks per row; ranks beyond 64
+    (2000, 128, 64, 6, 8, 0.0, True),         # one block per row: most consumer warps idle
+    (1216, 16384, 64, 4, 64, 0.1, False),     # 32 KB rows: a shorter ring
+    (1500, 1024, 32, 32, 32, 0.3, True),      # top-32, masked entries
+])
+def test_dispatch_fp8_many_token_shapes(T, H, E, K, R, mask, sf_col_major):
+    """FP8 dispatch with at least 8 tokens per SM (the persistent ring kernel)
+    on shapes beside the timed one: every code, scale and metadata entry
+    against the oracle."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    assert T >= 8 * sms
+    d = make_inputs(T, H, E, K, R, seed=T + H + K, mask_frac=mask)
+    lay, res, n, _, _ = _run(d, E, R, fp8=True, sf_col_major=sf_col_major)
+    assert int(res["status"].item()) == 0
+    g = _host(res, True, n)
+    L = oracle.layout(d["topk_idx"], E, R)
+    o = oracle.dispatch(d["x_bits"], d["topk_idx"], d["topk_weights"], E, R, L.dst_row, fp8=True,
+                        sf_col_major=sf_col_major, sf_stride=(n + 3) // 4 * 4)
+    for k in ("recv_x", "recv_topk_idx", "recv_topk_weights", "recv_src_idx"):
+        np.testing.assert_array_equal(g[k], o[k], err_msg=k)
+    nb = H // 128
+    if sf_col_major:
+        stride = (n + 3) // 4 * 4
+        np.testing.assert_array_equal(res["recv_sf"].cpu().numpy()[:nb * stride].reshape(nb, stride)[:, :n],
+                                      o["recv_sf"][:nb * stride].reshape(nb, stride)[:, :n])
+    else:
+        np.testing.assert_array_equal(res["recv_sf"].cpu().numpy()[:n * nb].reshape(n, -1), o["recv_sf"])
