@@ -35,9 +35,41 @@ def _load():
     global _lib
     if _lib is not None:
         return _lib
-    path = _build.build()
-    lib = ctypes.CDLL(path)
+    _lib = _configure(ctypes.CDLL(_build.build()))
+    return _lib
+
+
+_lib_omp = None
+
+
+class threads:
+    """``with oracle.threads() as n:`` -- the calls inside run on the OpenMP
+    build of the same C source (token loops of dispatch and combine split
+    over ``n`` host threads; the layout stays sequential).  n is None, and
+    the single-threaded build stays in use, when no OpenMP build exists.
+    For the benchmark's all-cores CPU baseline."""
+
+    def __enter__(self):
+        global _lib, _lib_omp
+        self._saved = _load()
+        if _lib_omp is None:
+            path = _build.build_omp()
+            if path is None:
+                return None
+            _lib_omp = _configure(ctypes.CDLL(path))
+        _lib = _lib_omp
+        return int(_lib_omp.ep_oracle_threads())
+
+    def __exit__(self, *exc):
+        global _lib
+        _lib = self._saved
+        return False
+
+
+def _configure(lib):
     vp = ctypes.c_void_p
+    lib.ep_oracle_threads.restype = ctypes.c_int
+    lib.ep_oracle_threads.argtypes = []
     lib.ep_oracle_layout.restype = ctypes.c_int
     lib.ep_oracle_layout.argtypes = [vp, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                      ctypes.c_int, ctypes.c_int] + [vp] * 11
@@ -89,7 +121,6 @@ def _load():
     lib.ep_oracle_combine_hierarchical.restype = ctypes.c_int
     lib.ep_oracle_combine_hierarchical.argtypes = (
         [vp, ctypes.c_int64, vp, vp] + [ctypes.c_int] * 7 + [vp, vp, ctypes.c_int64, vp, vp, vp])
-    _lib = lib
     return lib
 
 

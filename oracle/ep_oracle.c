@@ -40,16 +40,32 @@
  *
  * Build: gcc -O2 -std=c11 -ffp-contract=off -shared -fPIC (see build.py).
  * -ffp-contract=off keeps every multiply and add separately rounded on both
- * x86-64 and aarch64.
+ * x86-64 and aarch64.  A second build with -fopenmp splits the token loops
+ * of dispatch (non-compact form) and combine over host threads, for the
+ * benchmark's all-cores CPU baseline; the arithmetic is the same code.
  */
 #include <stdint.h>
 #include <stddef.h>
 #include <string.h>
 #include <math.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
 
 #define OR_OK            0
 #define OR_INVALID_INDEX 4
 #define OR_CAPACITY      8
+
+/* Threads the dispatch and combine loops may use: 1, or OpenMP's count in  */
+/* a build with -fopenmp (the benchmark's all-cores CPU baseline).          */
+int ep_oracle_threads(void)
+{
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
 
 /* ------------------------------------------------------------------------ */
 /* bf16 <-> float.  A bf16 is the upper 16 bits of an IEEE binary32.        */
@@ -298,11 +314,15 @@ int ep_oracle_dispatch(const uint16_t* x, const int64_t* topk_idx, const float* 
     int64_t j = 0;
     size_t row_bytes = fp8 ? (size_t)H : (size_t)H * 2;
     int nb = H / 128;
-    uint8_t q_tmp[65536];
-    float sf_tmp[512];
 
+    /* Tokens write disjoint rows when not compact, so a build with OpenMP
+     * (the all-cores timing of the benchmark) may split this loop over
+     * threads; without OpenMP the pragma is ignored.  Same work either way. */
+#pragma omp parallel for schedule(static) reduction(|:status) if(!compact)
     for (int i = 0; i < n_list; ++i) {
         int t = tokens ? tokens[i] : i;
+        uint8_t q_tmp[65536];
+        float sf_tmp[512];
         for (int r = 0; r < R; ++r) {
             int32_t d = dst_row[(int64_t)t * R + r];
             if (d < 0) continue;
@@ -356,6 +376,8 @@ int ep_oracle_combine(const uint16_t* y, int64_t num_y_rows,
     int status = OR_OK;
     int experts_per_rank = E / R;
     int n_list = tokens ? num_listed : T;
+    /* one output row per listed token: threads may share the tokens (OpenMP build) */
+#pragma omp parallel for schedule(static) reduction(|:status)
     for (int i = 0; i < n_list; ++i) {
         int t = tokens ? tokens[i] : i;
         double* o = out + (int64_t)i * H;

@@ -181,3 +181,34 @@ def test_expert_stats_accumulate():
     oracle.accumulate_expert_stats(L.num_tokens_per_expert, stats)
     oracle.accumulate_expert_stats(L.num_tokens_per_expert, stats)
     np.testing.assert_array_equal(stats, 2 * np.bincount(d["topk_idx"][d["topk_idx"] >= 0], minlength=16))
+
+
+def test_openmp_build_gives_the_same_results():
+    """The oracle's OpenMP build (token loops of dispatch and combine split
+    over host threads, used for the all-cores CPU baseline) returns exactly
+    what the single-threaded build returns."""
+    T, H, E, K, R = 300, 512, 64, 6, 8
+    d = make_inputs(T, H, E, K, R, seed=21, mask_frac=0.1)
+    L = oracle.layout(d["topk_idx"], E, R)
+    outs = []
+    for parallel in (False, True):
+        if parallel:
+            with oracle.threads() as n:
+                if n is None:
+                    pytest.skip("no OpenMP build on this host")
+                res = _dispatch_and_combine(d, E, R, L)
+        else:
+            res = _dispatch_and_combine(d, E, R, L)
+        outs.append(res)
+    for a, b in zip(outs[0], outs[1]):
+        np.testing.assert_array_equal(a, b)
+
+
+def _dispatch_and_combine(d, E, R, L):
+    o = oracle.dispatch(d["x_bits"], d["topk_idx"], d["topk_weights"], E, R, L.dst_row, capacity=L.num_recv)
+    f = oracle.dispatch(d["x_bits"], d["topk_idx"], d["topk_weights"], E, R, L.dst_row, capacity=L.num_recv,
+                        fp8=True)
+    c, st = oracle.combine(o["recv_x"].view(np.uint16), d["topk_idx"], d["topk_weights"], E, R, L.dst_row,
+                           weighted=True)
+    return [o["recv_x"], o["recv_topk_idx"], o["recv_topk_weights"], o["recv_src_idx"], f["recv_x"], f["recv_sf"],
+            c, np.array([o["status"], st])]
