@@ -10,7 +10,7 @@ load the library.
 """
 
 _BINDING_NAMES = (
-    "ep_get_layout", "ep_dispatch", "ep_combine", "ep_layout_workspace_bytes",
+    "ep_get_layout", "ep_dispatch", "ep_combine", "ep_layout_and_dispatch", "ep_layout_workspace_bytes",
     "ep_recv_capacity_bound", "ep_status_string", "Layout", "alloc_layout",
     "ep_get_layout_static_scratch", "ep_dispatch_expanded", "ep_combine_expanded",
     "ep_expanded_capacity_bound", "ep_combine_topk_weights", "ep_accumulate_expert_stats",

@@ -54,6 +54,9 @@ _lib.ep_get_layout_static_scratch.argtypes = [_vp, _i, _i, _i, _i, _i, _i, ctype
 _lib.ep_dispatch.restype = ctypes.c_int32
 _lib.ep_dispatch.argtypes = [_vp, _vp, _vp, _i, _i, _i, _i, _i, ctypes.POINTER(ep_layout_t), _i,
                              _i64, _vp, _vp, _i, _vp, _vp, _vp, _i, _vp, _vp]
+_lib.ep_layout_and_dispatch.restype = ctypes.c_int32
+_lib.ep_layout_and_dispatch.argtypes = [_vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, ctypes.POINTER(ep_layout_t), _vp,
+                                        ctypes.c_size_t, _i, _i64, _vp, _vp, _i, _vp, _vp, _vp, _vp, _vp]
 _lib.ep_combine.restype = ctypes.c_int32
 _lib.ep_combine.argtypes = [_vp, _i64, _vp, _vp, _i, _i, _i, _i, _i, ctypes.POINTER(ep_layout_t),
                             _vp, _i, _vp, _vp]
@@ -252,6 +255,22 @@ def ep_accumulate_expert_stats(layout, num_experts, stats, stream=None):
     assert stats.dtype == torch.int64 and stats.is_contiguous()
     code = _lib.ep_accumulate_expert_stats(ctypes.byref(layout.c), num_experts, _ptr(stats), _stream(stream))
     return _check(code, "ep_accumulate_expert_stats")
+
+
+def ep_layout_and_dispatch(x, topk_idx, topk_weights, num_experts, num_ranks, layout, workspace, recv_x,
+                           recv_topk_idx, recv_topk_weights, recv_src_idx, d_status, recv_sf=None,
+                           out_dtype=EP_BF16, sf_col_major=False, ranks_per_node=0, expert_alignment=1,
+                           stream=None):
+    T, H = x.shape
+    K = topk_idx.shape[1]
+    assert x.element_size() == 2 and x.is_contiguous() and recv_x.is_contiguous()
+    assert topk_idx.dtype == torch.int64 and topk_idx.is_contiguous()
+    code = _lib.ep_layout_and_dispatch(_ptr(x), _ptr(topk_idx), _ptr(topk_weights), T, H, K, num_experts, num_ranks,
+                                       ranks_per_node, expert_alignment, ctypes.byref(layout.c), _ptr(workspace),
+                                       workspace.numel() * workspace.element_size(), out_dtype, recv_x.shape[0],
+                                       _ptr(recv_x), _ptr(recv_sf), 1 if sf_col_major else 0, _ptr(recv_topk_idx),
+                                       _ptr(recv_topk_weights), _ptr(recv_src_idx), _ptr(d_status), _stream(stream))
+    return _check(code, "ep_layout_and_dispatch")
 
 
 def ep_combine(y, topk_idx, topk_weights, num_experts, num_ranks, layout, out, d_status, num_sms=0,

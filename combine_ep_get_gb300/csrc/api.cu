@@ -50,7 +50,7 @@ ep_status_t check_shape(int T, int K, int E, int R) {
 
 extern "C" {
 
-int ep_abi_version(void) { return 6; }
+int ep_abi_version(void) { return 7; }
 
 size_t ep_layout_workspace_bytes(int num_tokens, int num_topk, int num_experts, int num_ranks,
                                  int ranks_per_node) {
@@ -93,9 +93,14 @@ int64_t ep_recv_capacity_bound(int num_tokens, int num_topk, int num_ranks) {
     return static_cast<int64_t>(num_tokens) * (num_topk < num_ranks ? num_topk : num_ranks);
 }
 
-ep_status_t ep_get_layout(const int64_t* topk_idx, int T, int K, int E, int R, int ranks_per_node,
-                          int expert_alignment, const ep_layout_t* out, void* workspace,
-                          size_t ws_bytes, int32_t* d_status, void* cuda_stream) {
+}  // extern "C"
+
+namespace {
+
+// Host checks of ep_get_layout and its parameter block (no launch).
+ep_status_t layout_params(const int64_t* topk_idx, int T, int K, int E, int R, int ranks_per_node,
+                          int expert_alignment, const ep_layout_t* out, void* workspace, size_t ws_bytes,
+                          int32_t* d_status, epg::LayoutParams& p) {
     if (!out || !d_status) return EP_ERR_INVALID_ARG;
     ep_status_t s = check_shape(T, K, E, R);
     if (s != EP_OK) return s;
@@ -122,7 +127,7 @@ ep_status_t ep_get_layout(const int64_t* topk_idx, int T, int K, int E, int R, i
     const epg::LayoutWorkspace w = epg::layout_workspace(T, E, R, nodes_ws);
     if (!ok_ptr(workspace) || ws_bytes < w.total) return EP_ERR_INVALID_ARG;
 
-    epg::LayoutParams p{};
+    p = epg::LayoutParams{};
     p.topk_idx = topk_idx;
     p.T = T;
     p.K = K;
@@ -151,6 +156,20 @@ ep_status_t ep_get_layout(const int64_t* topk_idx, int T, int K, int E, int R, i
     p.ws_node = reinterpret_cast<int32_t*>(ws + w.off_node);
     p.ws_bitmap = reinterpret_cast<uint32_t*>(ws + w.off_bitmap);
     p.status = d_status;
+    return EP_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+ep_status_t ep_get_layout(const int64_t* topk_idx, int T, int K, int E, int R, int ranks_per_node,
+                          int expert_alignment, const ep_layout_t* out, void* workspace,
+                          size_t ws_bytes, int32_t* d_status, void* cuda_stream) {
+    epg::LayoutParams p{};
+    const ep_status_t s = layout_params(topk_idx, T, K, E, R, ranks_per_node, expert_alignment, out, workspace,
+                                        ws_bytes, d_status, p);
+    if (s != EP_OK) return s;
     const cudaStream_t stream = static_cast<cudaStream_t>(cuda_stream);
     if (epg::launch_layout(p, stream) != cudaSuccess) return EP_ERR_CUDA;
     // no tokens: the node-row kernels are not launched, node_offset is all zero
@@ -160,11 +179,18 @@ ep_status_t ep_get_layout(const int64_t* topk_idx, int T, int K, int E, int R, i
     return EP_OK;
 }
 
-ep_status_t ep_dispatch(const void* x, const int64_t* topk_idx, const float* topk_weights, int T,
-                        int H, int K, int E, int R, const ep_layout_t* layout, int out_dtype,
-                        int64_t recv_capacity, void* recv_x, float* recv_sf, int sf_col_major,
-                        int32_t* recv_topk_idx, float* recv_topk_weights, int32_t* recv_src_idx,
-                        int num_sms, int32_t* d_status, void* cuda_stream) {
+}  // extern "C"
+
+namespace {
+
+// Shared by ep_dispatch and ep_layout_and_dispatch.  self_layout (few
+// tokens, ep_layout_and_dispatch): no layout kernel has run; the dispatch
+// kernel computes the rows itself and writes the layout arrays of `lp`.
+ep_status_t dispatch_impl(const void* x, const int64_t* topk_idx, const float* topk_weights, int T, int H, int K,
+                          int E, int R, const ep_layout_t* layout, int out_dtype, int64_t recv_capacity,
+                          void* recv_x, float* recv_sf, int sf_col_major, int32_t* recv_topk_idx,
+                          float* recv_topk_weights, int32_t* recv_src_idx, int num_sms, int32_t* d_status,
+                          void* cuda_stream, const epg::LayoutParams* self_layout) {
     if (!layout || !d_status || num_sms < 0) return EP_ERR_INVALID_ARG;
     ep_status_t s = check_shape(T, K, E, R);
     if (s != EP_OK) return s;
@@ -212,10 +238,81 @@ ep_status_t ep_dispatch(const void* x, const int64_t* topk_idx, const float* top
     p.recv_src_idx = recv_src_idx;
     p.num_sms = num_sms;
     p.status = d_status;
+    if (self_layout) {
+        p.self_route = 1;
+        p.l_num_tokens_per_rank = self_layout->num_tokens_per_rank;
+        p.l_num_tokens_per_node = self_layout->num_nodes > 0 ? self_layout->num_tokens_per_node : nullptr;
+        p.l_num_tokens_per_expert = self_layout->num_tokens_per_expert;
+        p.l_is_token_in_rank = self_layout->is_token_in_rank;
+        p.l_rank_offset = self_layout->rank_offset;
+        p.l_expert_offset = self_layout->expert_offset;
+        p.l_dst_row = self_layout->dst_row;
+        p.l_src_dst_count = self_layout->src_dst_count;
+        p.l_token_offset = self_layout->token_offset;
+        p.l_alignment = self_layout->alignment;
+        p.l_ranks_per_node = self_layout->ranks_per_node;
+        p.l_num_nodes = self_layout->num_nodes;
+    }
     cudaStream_t st = static_cast<cudaStream_t>(cuda_stream);
     const cudaError_t e = out_dtype == EP_BF16 ? epg::launch_dispatch_bf16(p, st)
                                                : epg::launch_dispatch_fp8(p, st);
     return e == cudaSuccess ? EP_OK : EP_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+ep_status_t ep_dispatch(const void* x, const int64_t* topk_idx, const float* topk_weights, int T,
+                        int H, int K, int E, int R, const ep_layout_t* layout, int out_dtype,
+                        int64_t recv_capacity, void* recv_x, float* recv_sf, int sf_col_major,
+                        int32_t* recv_topk_idx, float* recv_topk_weights, int32_t* recv_src_idx,
+                        int num_sms, int32_t* d_status, void* cuda_stream) {
+    return dispatch_impl(x, topk_idx, topk_weights, T, H, K, E, R, layout, out_dtype, recv_capacity, recv_x, recv_sf,
+                         sf_col_major, recv_topk_idx, recv_topk_weights, recv_src_idx, num_sms, d_status, cuda_stream,
+                         nullptr);
+}
+
+ep_status_t ep_layout_and_dispatch(const void* x, const int64_t* topk_idx, const float* topk_weights, int T, int H,
+                                   int K, int E, int R, int ranks_per_node, int expert_alignment,
+                                   const ep_layout_t* layout, void* workspace, size_t ws_bytes, int out_dtype,
+                                   int64_t recv_capacity, void* recv_x, float* recv_sf, int sf_col_major,
+                                   int32_t* recv_topk_idx, float* recv_topk_weights, int32_t* recv_src_idx,
+                                   int32_t* d_status, void* cuda_stream) {
+    // the dispatch's host checks first, so that a rejected call launches nothing
+    if (!layout || !d_status) return EP_ERR_INVALID_ARG;
+    ep_status_t s = check_shape(T, K, E, R);
+    if (s != EP_OK) return s;
+    if (H < 1 || (out_dtype != EP_BF16 && out_dtype != EP_FP8_E4M3)) return EP_ERR_INVALID_ARG;
+    if (H % (out_dtype == EP_BF16 ? 8 : 128) != 0) return EP_ERR_INVALID_ARG;
+    if (out_dtype == EP_FP8_E4M3 && H > 65536) return EP_ERR_UNSUPPORTED;
+    if (recv_capacity < 0 || recv_capacity > INT32_MAX) return EP_ERR_INVALID_ARG;
+    if (static_cast<int64_t>(H) * 2 > UINT32_MAX / 2) return EP_ERR_UNSUPPORTED;
+    if (T > 0 && (!ok_ptr(x) || !ok_ptr(topk_idx))) return EP_ERR_INVALID_ARG;
+    if (recv_capacity > 0 && !ok_ptr(recv_x)) return EP_ERR_INVALID_ARG;
+    if (out_dtype == EP_FP8_E4M3 && recv_capacity > 0 && !ok_ptr(recv_sf)) return EP_ERR_INVALID_ARG;
+    if (recv_topk_weights && T > 0 && !ok_ptr(topk_weights)) return EP_ERR_INVALID_ARG;
+    if ((recv_topk_idx && !aligned16(recv_topk_idx)) || (recv_topk_weights && !aligned16(recv_topk_weights)) ||
+        (recv_src_idx && !aligned16(recv_src_idx)))
+        return EP_ERR_INVALID_ARG;
+    epg::LayoutParams lp{};
+    s = layout_params(topk_idx, T, K, E, R, ranks_per_node, expert_alignment, layout, workspace, ws_bytes, d_status,
+                      lp);
+    if (s != EP_OK) return s;
+    // Few tokens: one kernel; its CTAs derive the rows themselves and write
+    // the layout (expanded rows and node rows need the layout kernel).
+    const bool one_kernel = T >= 1 && T <= epg::kSelfRouteMaxTokens && R <= 32 && K <= epg::kSelfRouteMaxTopk &&
+                            E <= epg::kSelfRouteMaxExperts && !lp.expanded_row && !lp.node_row && !lp.node_offset;
+    if (!one_kernel) {
+        if (epg::launch_layout(lp, static_cast<cudaStream_t>(cuda_stream)) != cudaSuccess) return EP_ERR_CUDA;
+        if (T == 0 && layout->node_offset &&
+            cudaMemsetAsync(layout->node_offset, 0, sizeof(int32_t) * (R / ranks_per_node + 1),
+                            static_cast<cudaStream_t>(cuda_stream)) != cudaSuccess)
+            return EP_ERR_CUDA;
+    }
+    return dispatch_impl(x, topk_idx, topk_weights, T, H, K, E, R, layout, out_dtype, recv_capacity, recv_x, recv_sf,
+                         sf_col_major, recv_topk_idx, recv_topk_weights, recv_src_idx, 0, d_status, cuda_stream,
+                         one_kernel ? &lp : nullptr);
 }
 
 ep_status_t ep_dispatch_hierarchical(const void* x, const int64_t* topk_idx, const float* topk_weights, int T,

@@ -347,8 +347,187 @@ __device__ __forceinline__ void prefetch_x(const DispatchParams& p) {
     }
 }
 
+// Few-token layout inside the dispatch (ep_layout_and_dispatch): each CTA
+// derives the destination row of its token on every rank from topk_idx
+// alone, as the layout defines it ("DeepEP Symmetric Memory" section 6.1:
+// the per-rank prefix sum of received tokens plus the destination slot
+// index):
+//   dst_row[t, r] = rank_offset[r] + #{t' < t : t' has an expert on r},
+//   rank_offset = exclusive prefix of the per-rank token counts,
+// with masked (-1) and invalid ids counting for no rank, so no layout kernel
+// has to run first.  The CTA of piece 0 of token t also writes the token's
+// layout rows (dst_row, is_token_in_rank, token_offset[t]).  One extra CTA
+// of the grid (kLayoutCta, no dispatch work) writes the counts and offsets
+// (per rank, per expert with the alignment, per node, src_dst_count,
+// rank_offset, expert_offset, token_offset[T]) and flags invalid ids, beside
+// the dispatch CTAs.  CTA-wide: every thread calls it, with blockDim.x ==
+// 256, T <= kSelfMaxTokens, R <= 32, K <= kSelfMaxTopk and
+// E <= kSelfMaxExperts.  Returns in lane r of every warp the row of rank r
+// for token t, or -1.
+constexpr int kSelfMaxTokens = kSelfRouteMaxTokens;
+constexpr int kSelfMaxTopk = kSelfRouteMaxTopk;
+constexpr int kSelfMaxExperts = kSelfRouteMaxExperts;
+static_assert(kSelfMaxTokens <= 256, "self_route_layout: one thread per token in a 256-thread CTA");
+struct SelfRouteSmem {
+    uint32_t mask[kSelfMaxTokens];           // ranks holding each token (bit r)
+    uint32_t bal[kSelfMaxTokens / 32][32];   // [word of 32 tokens][rank]: membership bits
+    int hist[kSelfMaxExperts];               // CTA 0: entries per expert, then offsets in the chunk
+    int chunk[kSelfMaxExperts / 32];         // CTA 0: aligned entries per 32 experts, then their prefix
+};
+
+// The CTA's one SelfRouteSmem (a function-scope __shared__ object exists
+// once per CTA), shared by the dispatch items and the layout CTA.
+__device__ __forceinline__ SelfRouteSmem& self_smem() {
+    __shared__ SelfRouteSmem s;
+    return s;
+}
+
+template <bool kLayoutCta>
+__device__ int self_route_layout(const DispatchParams& p, int t, int c, SelfRouteSmem& s) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    constexpr bool cta0 = kLayoutCta;
+    int64_t e[kSelfMaxTopk];
+    if (tid < p.T) {   // one thread per token: all K entries in flight at once
+#pragma unroll
+        for (int k = 0; k < kSelfMaxTopk; ++k) e[k] = k < p.K ? p.topk_idx[static_cast<int64_t>(tid) * p.K + k] : -1;
+        uint32_t m = 0;
+#pragma unroll
+        for (int k = 0; k < kSelfMaxTopk; ++k)
+            if (e[k] >= 0 && e[k] < p.E) m |= 1u << (static_cast<int>(e[k]) / p.experts_per_rank);
+        s.mask[tid] = m;
+    }
+    if (cta0)
+        for (int i = tid; i < p.E; i += blockDim.x) s.hist[i] = 0;
+    __syncthreads();
+    if (cta0 && tid < p.T) {
+        bool bad = false;
+#pragma unroll
+        for (int k = 0; k < kSelfMaxTopk; ++k) {
+            if (k >= p.K) break;
+            if (e[k] >= 0 && e[k] < p.E) atomicAdd(&s.hist[e[k]], 1);
+            else if (e[k] != -1) bad = true;
+        }
+        if (bad) atomicOr(p.status, EP_ERR_INVALID_INDEX);
+    }
+    const int n_words = (p.T + 31) >> 5;
+    if (warp < n_words) {
+        const int j = (warp << 5) + lane;
+        const uint32_t m = j < p.T ? s.mask[j] : 0u;
+        for (int r = 0; r < p.R; ++r) {
+            const uint32_t b = __ballot_sync(0xffffffffu, (m >> r) & 1u);
+            if (lane == r) s.bal[warp][r] = b;
+        }
+    }
+    __syncthreads();
+    int total = 0, before = 0;
+    if (lane < p.R) {
+        const int tw = t >> 5;
+        for (int w = 0; w < n_words; ++w) {
+            const uint32_t b = s.bal[w][lane];
+            total += __popc(b);
+            if (w < tw) before += __popc(b);
+            else if (w == tw) before += __popc(b & ((1u << (t & 31)) - 1u));
+        }
+    }
+    const int incl = warp_inclusive_scan(total);   // lanes >= R add 0
+    const int offset = incl - total;
+    const bool in = lane < p.R && ((s.mask[t] >> lane) & 1u);
+    const int d = in ? offset + before : -1;
+
+    // the token's layout rows
+    if (!kLayoutCta && c == 0 && warp == 0) {
+        if (lane < p.R) {
+            p.l_dst_row[static_cast<int64_t>(t) * p.R + lane] = d;
+            p.l_is_token_in_rank[static_cast<int64_t>(t) * p.R + lane] = in ? 1 : 0;
+        }
+        const int rows_before = static_cast<int>(__reduce_add_sync(0xffffffffu, static_cast<unsigned>(before)));
+        if (lane == 0 && p.l_token_offset) p.l_token_offset[t] = rows_before;
+    }
+    if (cta0) {
+        const int n_rows = __shfl_sync(0xffffffffu, incl, 31);
+        if (warp == 0) {
+            if (lane < p.R) {
+                p.l_num_tokens_per_rank[lane] = total;
+                p.l_rank_offset[lane] = offset;
+            }
+            if (lane == 0) {
+                p.l_rank_offset[p.R] = n_rows;
+                if (p.l_token_offset) p.l_token_offset[p.T] = n_rows;
+            }
+        }
+        // per-expert counts, rounded up to the alignment, scanned
+        const int n_chunks = (p.E + 31) >> 5;
+        for (int ch = warp; ch < n_chunks; ch += blockDim.x >> 5) {
+            const int ex = ch * 32 + lane;
+            const int cnt = ex < p.E ? s.hist[ex] : 0;
+            if (ex < p.E) p.l_num_tokens_per_expert[ex] = cnt;
+            const int al = (cnt + p.l_alignment - 1) / p.l_alignment * p.l_alignment;
+            const int ci = warp_inclusive_scan(al);
+            if (ex < p.E) s.hist[ex] = ci - al;
+            if (lane == 31) s.chunk[ch] = ci;
+        }
+        // src_dst_count[src][r]: tokens of source rank src (T / R each) on rank r
+        if (p.l_src_dst_count) {
+            const int per_src = p.T / p.R;
+            for (int j = tid; j < p.R * p.R; j += blockDim.x) {
+                const int src = j / p.R, r = j - src * p.R;
+                int cnt = 0;
+                for (int u = src * per_src; u < (src + 1) * per_src; ++u) cnt += (s.mask[u] >> r) & 1u;
+                p.l_src_dst_count[j] = cnt;
+            }
+        }
+        // tokens reaching each node (ranks [n * rpn, (n + 1) * rpn))
+        if (p.l_num_tokens_per_node) {
+            for (int n = tid; n < p.l_num_nodes; n += blockDim.x) {
+                const uint32_t node_bits = (p.l_ranks_per_node >= 32 ? 0xffffffffu
+                                                                     : ((1u << p.l_ranks_per_node) - 1u))
+                                           << (n * p.l_ranks_per_node);
+                int cnt = 0;
+                for (int u = 0; u < p.T; ++u) cnt += (s.mask[u] & node_bits) != 0u;
+                p.l_num_tokens_per_node[n] = cnt;
+            }
+        }
+        __syncthreads();   // CTA-uniform branch
+        if (warp == 0) {   // exclusive prefix of the chunk totals (at most 64 chunks)
+            const int a = lane < n_chunks ? s.chunk[lane] : 0;
+            const int b = 32 + lane < n_chunks ? s.chunk[32 + lane] : 0;
+            const int ia = warp_inclusive_scan(a);
+            const int ib = warp_inclusive_scan(b) + __shfl_sync(0xffffffffu, ia, 31);
+            if (lane < n_chunks) s.chunk[lane] = ia - a;
+            if (32 + lane < n_chunks) s.chunk[32 + lane] = ib - b;
+            if (lane == 31) p.l_expert_offset[p.E] = ib;
+        }
+        __syncthreads();
+        for (int ex = tid; ex < p.E; ex += blockDim.x) p.l_expert_offset[ex] = s.chunk[ex >> 5] + s.hist[ex];
+    }
+    return d;
+}
+
+// Metadata of token t with its destination rows in registers (lane r holds
+// rank r's row, R <= 32); one warp.  Same entries as write_metadata.
+__device__ __forceinline__ void write_metadata_lanes(const DispatchParams& p, int t, int lane, int d) {
+    const int K = p.K;
+    const int64_t e_l = lane < K ? p.topk_idx[static_cast<int64_t>(t) * K + lane] : -1;
+    const float w_l =
+        (lane < K && p.recv_topk_weights) ? p.topk_weights[static_cast<int64_t>(t) * K + lane] : 0.0f;
+    unsigned m = __ballot_sync(0xffffffffu, d >= 0 && d < p.capacity);
+    while (m) {
+        const int rr = __ffs(m) - 1;
+        m &= m - 1;
+        const int64_t dd = __shfl_sync(0xffffffffu, d, rr);
+        if (lane < K) {
+            const bool on = e_l >= 0 && e_l < p.E && static_cast<int>(e_l) / p.experts_per_rank == rr;
+            if (p.recv_topk_idx)
+                p.recv_topk_idx[dd * K + lane] = on ? static_cast<int32_t>(e_l) - rr * p.experts_per_rank : -1;
+            if (p.recv_topk_weights) p.recv_topk_weights[dd * K + lane] = on ? w_l : 0.0f;
+        }
+        if (lane == 0 && p.recv_src_idx) p.recv_src_idx[dd] = t;
+    }
+}
+
 constexpr int kRegThreads = 256;
 constexpr int kRegUnroll = 4;
+constexpr int kSelfRegBlocks = 4;   // self-routing bf16 CTAs per SM (registers for the top-k entries, no spills)
 
 // SM-limited mode: CTAs of kSmGroups groups, one per SM, each group looping
 // over (token, piece) items.
@@ -362,7 +541,7 @@ constexpr int kSmGroups = 4;
 // expanded rows (one per valid top-k slot) instead of one row per rank.
 // kGroups > 1 (SM-limited mode): several groups per CTA looping over items.
 // One (token, piece) item of the register path, by one group of 256 threads.
-template <bool kExpanded>
+template <bool kExpanded, bool kSelf>
 __device__ __forceinline__ void dispatch_regs_item(const DispatchParams& p, int64_t it, int gtid, int warp_g,
                                                    int lane, bool& cap_bad) {
     const uint32_t row_bytes = static_cast<uint32_t>(p.H) * 2u;
@@ -382,11 +561,19 @@ __device__ __forceinline__ void dispatch_regs_item(const DispatchParams& p, int6
     const int n_dst = kExpanded ? p.K : p.R;
     const int32_t* drow = kExpanded ? p.expanded_row + static_cast<int64_t>(t) * p.K
                                     : p.dst_row + static_cast<int64_t>(t) * p.R;
-    const int d0 = lane < n_dst ? drow[lane] : -1;
-    const int d1 = 32 + lane < n_dst ? drow[32 + lane] : -1;   // ranks 32..63, same latency
+    int d0, d1;
+    if constexpr (kSelf) {
+        d0 = self_route_layout<false>(p, t, c, self_smem());   // R <= 32
+        d1 = -1;
+    } else {
+        d0 = lane < n_dst ? drow[lane] : -1;
+        d1 = 32 + lane < n_dst ? drow[32 + lane] : -1;   // ranks 32..63, same latency
+    }
     if (warp_g == 1 && c == 0) {
         if (kExpanded) {
             write_expanded_metadata(p, t, lane);
+        } else if (kSelf) {
+            write_metadata_lanes(p, t, lane, d0);
         } else {
             CtaWork all;
             all.first = 0;
@@ -430,23 +617,32 @@ __device__ __forceinline__ void dispatch_regs_item(const DispatchParams& p, int6
     }
 }
 
-template <bool kExpanded, int kGroups>
-__global__ void __launch_bounds__(kRegThreads * kGroups, kGroups == 1 ? 6 : 1)
+// kSelf (ep_layout_and_dispatch, few tokens, one CTA per item): there is no
+// layout kernel in front; each CTA derives its token's destination rows
+// itself and writes the token's layout rows, and CTA 0 the layout's counts
+// and offsets (self_route_layout).
+template <bool kExpanded, int kGroups, bool kSelf = false>
+__global__ void __launch_bounds__(kRegThreads * kGroups, kGroups > 1 ? 1 : kSelf ? kSelfRegBlocks : 6)
     dispatch_bf16_regs_kernel(const DispatchParams p) {
     const int gtid = static_cast<int>(threadIdx.x) % kRegThreads;
     const int warp_g = gtid >> 5;   // warp within the group
     const int lane = threadIdx.x & 31;
     bool cap_bad = false;
+    if (kSelf && blockIdx.x == gridDim.x - 1) {   // the layout's counts and offsets
+        pdl_wait();
+        self_route_layout<true>(p, 0, 1, self_smem());
+        return;
+    }
     if (kGroups == 1) prefetch_x<false>(p);
     pdl_wait();   // before any load: the previous kernel may write x
     if (kGroups == 1) {
-        dispatch_regs_item<kExpanded>(p, blockIdx.x, gtid, warp_g, lane, cap_bad);
+        dispatch_regs_item<kExpanded, kSelf>(p, blockIdx.x, gtid, warp_g, lane, cap_bad);
     } else {
         const int64_t n_items = static_cast<int64_t>(p.T) * p.chunks;
         const int group = static_cast<int>(threadIdx.x) / kRegThreads;
         for (int64_t it = static_cast<int64_t>(blockIdx.x) * kGroups + group; it < n_items;
              it += static_cast<int64_t>(gridDim.x) * kGroups)
-            dispatch_regs_item<kExpanded>(p, it, gtid, warp_g, lane, cap_bad);
+            dispatch_regs_item<kExpanded, false>(p, it, gtid, warp_g, lane, cap_bad);
     }
     if (warp_g == 0 && __any_sync(0xffffffffu, cap_bad) && lane == 0) atomicOr(p.status, EP_ERR_CAPACITY);
 }
@@ -483,7 +679,7 @@ constexpr int kFp8Rounds = 2;   // rounds of blocks per item (loads of every rou
 // group of kLanes lanes reduces its block's amax by shuffles, forms the scale
 // and the codes, and stores the code vector (and, its first lane, the scale)
 // to every destination.
-template <bool kExpanded, int kLanes>
+template <bool kExpanded, int kLanes, bool kSelf>
 __device__ __forceinline__ void dispatch_fp8_item(const DispatchParams& p, int64_t it, int gtid, int lane,
                                                   int group_warps, bool& cap_bad) {
     constexpr int kVec = 128 / kLanes / 8;                     // 16-byte input vectors per lane per block
@@ -509,11 +705,19 @@ __device__ __forceinline__ void dispatch_fp8_item(const DispatchParams& p, int64
     const int n_dst = kExpanded ? p.K : p.R;
     const int32_t* drow = kExpanded ? p.expanded_row + static_cast<int64_t>(t) * p.K
                                     : p.dst_row + static_cast<int64_t>(t) * p.R;
-    const int d0 = lane < n_dst ? drow[lane] : -1;
-    const int d1 = 32 + lane < n_dst ? drow[32 + lane] : -1;   // ranks 32..63, same latency
+    int d0, d1;
+    if constexpr (kSelf) {
+        d0 = self_route_layout<false>(p, t, c, self_smem());   // R <= 32
+        d1 = -1;
+    } else {
+        d0 = lane < n_dst ? drow[lane] : -1;
+        d1 = 32 + lane < n_dst ? drow[32 + lane] : -1;   // ranks 32..63, same latency
+    }
     if (warp_g == 1 && c == 0) {
         if (kExpanded) {
             write_expanded_metadata(p, t, lane);
+        } else if (kSelf) {
+            write_metadata_lanes(p, t, lane, d0);
         } else {
             CtaWork all;
             all.first = 0;
@@ -627,7 +831,7 @@ __device__ __forceinline__ void dispatch_fp8_item(const DispatchParams& p, int64
 // The many-token rank-row instantiation runs 5 CTAs per SM (more loads in
 // flight; 4 for the few-token and expanded ones, which the cap would slow or
 // spill).
-template <bool kExpanded, int kGroups, int kLanes>
+template <bool kExpanded, int kGroups, int kLanes, bool kSelf = false>
 __global__ void __launch_bounds__(kFp8Threads * kGroups,
                                   kGroups > 1 ? 1
                                   : (kLanes == 8 && !kExpanded) ? EP_DISPATCH_FP8_WIDE_MIN_BLOCKS
@@ -638,16 +842,22 @@ __global__ void __launch_bounds__(kFp8Threads * kGroups,
     const int gtid = kGroups == 1 ? static_cast<int>(threadIdx.x) : static_cast<int>(threadIdx.x) % kFp8Threads;
     const int lane = threadIdx.x & 31;
     bool cap_bad = false;
+    if (kSelf && blockIdx.x == gridDim.x - 1) {   // the layout's counts and offsets
+        pdl_wait();
+        self_route_layout<true>(p, 0, 1, self_smem());
+        return;
+    }
     if (kGroups == 1) prefetch_x<true>(p);
     pdl_wait();   // before any load: the previous kernel may write x
     if (kGroups == 1) {
-        dispatch_fp8_item<kExpanded, kLanes>(p, blockIdx.x, gtid, lane, static_cast<int>(blockDim.x) / 32, cap_bad);
+        dispatch_fp8_item<kExpanded, kLanes, kSelf>(p, blockIdx.x, gtid, lane, static_cast<int>(blockDim.x) / 32,
+                                                    cap_bad);
     } else {
         const int64_t n_items = static_cast<int64_t>(p.T) * p.chunks;
         const int group = static_cast<int>(threadIdx.x) / kFp8Threads;
         for (int64_t it = static_cast<int64_t>(blockIdx.x) * kGroups + group; it < n_items;
              it += static_cast<int64_t>(gridDim.x) * kGroups)
-            dispatch_fp8_item<kExpanded, kLanes>(p, it, gtid, lane, kFp8Threads / 32, cap_bad);
+            dispatch_fp8_item<kExpanded, kLanes, false>(p, it, gtid, lane, kFp8Threads / 32, cap_bad);
     }
     if ((gtid >> 5) == 0 && __any_sync(0xffffffffu, cap_bad) && lane == 0) atomicOr(p.status, EP_ERR_CAPACITY);
 }
@@ -714,7 +924,9 @@ cudaError_t launch_dispatch_bf16(DispatchParams p, cudaStream_t stream) {
         int chunks = static_cast<int>((row_bytes + 16383u) / 16384u);
         const int want_items = 4 * di.num_sms;
         if (p.T > 0 && static_cast<int64_t>(p.T) * chunks < want_items) {
-            const int more = (want_items + p.T - 1) / p.T;
+            // a CTA that derives its rows itself (self_route) pays that
+            // latency once per wave: keep it to one wave of 4 CTAs per SM
+            const int more = p.self_route ? di.num_sms * kSelfRegBlocks / p.T : (want_items + p.T - 1) / p.T;
             const int max_chunks = static_cast<int>(row_bytes / 1024u) > 0 ? static_cast<int>(row_bytes / 1024u) : 1;
             chunks = more < max_chunks ? more : max_chunks;
             if (chunks < 1) chunks = 1;
@@ -732,10 +944,12 @@ cudaError_t launch_dispatch_bf16(DispatchParams p, cudaStream_t stream) {
             const dim3 grid(static_cast<unsigned>(g)), block(kRegThreads * kSmGroups);
             return launch_pdl(dispatch_bf16_regs_kernel<true, kSmGroups>, grid, block, 0, stream, p);
         }
-        const dim3 grid(static_cast<unsigned>(items)), block(kRegThreads);
+        // self routing: one more CTA, which writes the layout's counts and offsets
+        const dim3 grid(static_cast<unsigned>(items + (p.self_route ? 1 : 0))), block(kRegThreads);
         p.prefetch_ctas = di.num_sms * 6;   // the first wave (6 CTAs per SM)
         p.prefetch_items = EP_DISPATCH_PREFETCH;
         if (p.expanded_row) return launch_pdl(dispatch_bf16_regs_kernel<true, 1>, grid, block, 0, stream, p);
+        if (p.self_route) return launch_pdl(dispatch_bf16_regs_kernel<false, 1, true>, grid, block, 0, stream, p);
         return launch_pdl(dispatch_bf16_regs_kernel<false, 1>, grid, block, 0, stream, p);
     }
     return launch_dispatch_bulk_t<kBulkStages, kBulkStoreDepth>(p, 0, stream);
@@ -760,19 +974,25 @@ cudaError_t launch_dispatch_fp8_t(DispatchParams p, int num_sms, cudaStream_t st
         if (warps > kFp8Threads / 32) warps = kFp8Threads / 32;
         if (warps < 2) warps = 2;   // warp 1 writes the metadata
     }
-    const dim3 grid(static_cast<unsigned>(items)), block(32 * warps);
-    auto kernel = p.expanded_row ? dispatch_fp8_kernel<true, 1, kLanes> : dispatch_fp8_kernel<false, 1, kLanes>;
+    // self routing (few tokens, the 16-lane mode): one more CTA, which writes
+    // the layout's counts and offsets
+    const bool self = kLanes == 16 && p.self_route && !p.expanded_row;
+    const dim3 grid(static_cast<unsigned>(items + (self ? 1 : 0))), block(32 * warps);
+    auto kernel = p.expanded_row ? dispatch_fp8_kernel<true, 1, kLanes>
+                  : (kLanes == 16 && p.self_route) ? dispatch_fp8_kernel<false, 1, 16, true>
+                                                   : dispatch_fp8_kernel<false, 1, kLanes>;
     // CTAs resident per SM at this size: the first wave, which prefetches
-    static thread_local int occ_device = -1, occ_threads = 0, occ_expanded = -1, occ_ctas = 1;
+    static thread_local int occ_device = -1, occ_threads = 0, occ_kind = -1, occ_ctas = 1;
     const int dev = device_info().device;
-    if (occ_device != dev || occ_threads != 32 * warps || occ_expanded != (p.expanded_row != nullptr)) {
+    const int kind = p.expanded_row ? 1 : p.self_route ? 2 : 0;
+    if (occ_device != dev || occ_threads != 32 * warps || occ_kind != kind) {
         int nb_sm = 0;
         const cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb_sm, kernel, 32 * warps, 0);
         if (e != cudaSuccess) return e;
         occ_ctas = nb_sm > 0 ? nb_sm : 1;
         occ_device = dev;
         occ_threads = 32 * warps;
-        occ_expanded = p.expanded_row != nullptr;
+        occ_kind = kind;
     }
     p.prefetch_ctas = device_info().num_sms * occ_ctas;
     p.prefetch_items = EP_DISPATCH_PREFETCH;
@@ -793,7 +1013,9 @@ cudaError_t launch_dispatch_fp8(DispatchParams p, cudaStream_t stream) {
     int chunks = (nb + piece_max - 1) / piece_max;
     const int want_items = 4 * di.num_sms;
     if (p.T > 0 && static_cast<int64_t>(p.T) * chunks < want_items) {
-        const int more = (want_items + p.T - 1) / p.T;
+        // a CTA that derives its rows itself (self_route) pays that latency
+        // once per wave: keep it to one wave of 4 CTAs per SM
+        const int more = p.self_route ? want_items / p.T : (want_items + p.T - 1) / p.T;
         const int max_chunks = (nb + blocks_per_round / 8 - 1) / (blocks_per_round / 8);   // >= one warp's blocks per piece
         chunks = more < max_chunks ? more : max_chunks;
         if (chunks < 1) chunks = 1;

@@ -17,6 +17,12 @@ namespace epg {
 // ---------------------------------------------------------------------------
 
 constexpr int kTileTokens = 256;               // tokens per layout tile (one per thread)
+// ep_layout_and_dispatch: one kernel computes layout and dispatch (each CTA
+// derives its token's rows itself) for at most this many tokens, top-k
+// entries per token and experts, with R <= 32
+constexpr int kSelfRouteMaxTokens = 256;
+constexpr int kSelfRouteMaxTopk = 16;
+constexpr int kSelfRouteMaxExperts = 2048;
 constexpr int kTileWords = kTileTokens / 32;   // 32-bit membership words per rank per tile
 
 struct LayoutParams {
@@ -70,6 +76,20 @@ struct DispatchParams {
     // j < prefetch_items (0: none)
     int prefetch_ctas;
     int prefetch_items;
+    // 1: ep_layout_and_dispatch with few tokens: no layout kernel runs; each
+    // CTA derives its token's destination rows from topk_idx, writes that
+    // token's layout rows, and CTA 0 the layout's counts and offsets, into:
+    int self_route;
+    int32_t* l_num_tokens_per_rank;     // [R]
+    int32_t* l_num_tokens_per_node;     // [R / ranks_per_node] or null
+    int32_t* l_num_tokens_per_expert;   // [E]
+    uint8_t* l_is_token_in_rank;        // [T][R]
+    int32_t* l_rank_offset;             // [R + 1]
+    int32_t* l_expert_offset;           // [E + 1]
+    int32_t* l_dst_row;                 // [T][R]
+    int32_t* l_src_dst_count;           // [R][R] or null
+    int32_t* l_token_offset;            // [T + 1] or null
+    int l_alignment, l_ranks_per_node, l_num_nodes;
 };
 
 struct CombineParams {

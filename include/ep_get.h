@@ -225,6 +225,38 @@ ep_status_t ep_dispatch(const void* x, const int64_t* topk_idx, const float* top
                         int num_sms, int32_t* d_status, void* cuda_stream);
 
 /*
+ * Layout and dispatch in one call: the pages' dispatch, which computes the
+ * routing handle itself ("DeepEP Symmetric Memory" section 9.2,
+ * dispatch(x, topk_idx, topk_weights, num_experts, ...) -> (recv_x, ...,
+ * handle); section 6.1 for the prefix sums it launches with).
+ *
+ * Same results as ep_get_layout followed by ep_dispatch with num_sms = 0:
+ * `layout` receives every array ep_get_layout writes, and the receive arrays
+ * what ep_dispatch writes.  Arguments are those two calls' arguments
+ * (num_tokens .. num_ranks, ranks_per_node and expert_alignment as in
+ * ep_get_layout; out_dtype .. recv_src_idx as in ep_dispatch), checked on the
+ * host before anything is launched.  Since N is not known before the
+ * layout, size the receive arrays with ep_recv_capacity_bound.
+ *
+ * With few tokens (1 <= num_tokens <= 256, num_ranks <= 32, num_topk <= 16,
+ * num_experts <= 2048, and no expanded or node rows requested in `layout`)
+ * the call launches a single kernel: each dispatch CTA derives its token's
+ * destination rows from topk_idx by the layout's definition (rank offset plus
+ * the number of earlier tokens on that rank) and writes the token's layout
+ * rows, and one CTA writes the layout's counts and offsets, so no layout
+ * kernel runs in front of the dispatch (the workspace is then not touched).
+ * This shortens the latency-bound decode step.  Otherwise the call launches
+ * the layout kernel(s) and then the dispatch, as the two separate calls do.
+ */
+ep_status_t ep_layout_and_dispatch(const void* x, const int64_t* topk_idx, const float* topk_weights,
+                                   int num_tokens, int hidden, int num_topk, int num_experts,
+                                   int num_ranks, int ranks_per_node, int expert_alignment,
+                                   const ep_layout_t* layout, void* workspace, size_t ws_bytes,
+                                   int out_dtype, int64_t recv_capacity, void* recv_x, float* recv_sf,
+                                   int sf_col_major, int32_t* recv_topk_idx, float* recv_topk_weights,
+                                   int32_t* recv_src_idx, int32_t* d_status, void* cuda_stream);
+
+/*
  * Combine ("DeepEP Symmetric Memory" section 9.2: combine(x, handle,
  * topk_weights) -> combined_x).  For every token t:
  *   out[t] = bf16_rne( sum over r with dst_row[t,r] = d >= 0 of c(t,r) * y[d] )

@@ -32,7 +32,7 @@ def test_header_declares_the_entry_points():
               "ep_recv_capacity_bound", "ep_status_string", "ep_abi_version", "ep_dispatch_expanded",
               "ep_combine_expanded", "ep_expanded_capacity_bound", "ep_combine_topk_weights",
               "ep_accumulate_expert_stats", "ep_theoretical_num_sms",
-              "ep_dispatch_hierarchical", "ep_combine_hierarchical"):
+              "ep_dispatch_hierarchical", "ep_combine_hierarchical", "ep_layout_and_dispatch"):
         assert n in names
 
 
@@ -53,7 +53,7 @@ def test_status_strings_and_sizes(lib):
     ws = lib.ep_layout_workspace_bytes(4096, 8, 256, 8, 0)
     tiles = 16
     assert ws >= 4 * tiles * (8 + 256 + 8 * 8)
-    assert lib.ep_abi_version() == 6
+    assert lib.ep_abi_version() == 7
 
 
 def test_host_checks_reject_before_any_launch(lib):
@@ -113,6 +113,30 @@ def test_host_checks_reject_before_any_launch(lib):
     assert d(*bad) == B.EP_ERR_INVALID_ARG
     bad = list(args); bad[17] = -1                       # negative SM count
     assert d(*bad) == B.EP_ERR_INVALID_ARG
+    # layout + dispatch: the dispatch's checks run before the layout is launched
+    f2 = lib.ep_layout_and_dispatch
+    f2.restype = ctypes.c_int32
+    f2.argtypes = [vp, vp, vp] + [ctypes.c_int] * 7 + [ctypes.POINTER(B.ep_layout_t), vp, ctypes.c_size_t,
+                                                      ctypes.c_int, ctypes.c_int64, vp, vp, ctypes.c_int, vp, vp, vp,
+                                                      vp, vp]
+    fargs = [vp(16), vp(32), vp(48), 10, 7168, 8, 256, 8, 0, 1, ctypes.byref(L2), vp(256), 1 << 20, B.EP_BF16, 100,
+             vp(64), None, 0, None, None, None, st, None]
+    bad = list(fargs); bad[4] = 7164                     # H % 8
+    assert f2(*bad) == B.EP_ERR_INVALID_ARG
+    bad = list(fargs); bad[13] = B.EP_FP8_E4M3           # FP8 needs recv_sf
+    assert f2(*bad) == B.EP_ERR_INVALID_ARG
+    bad = list(fargs); bad[15] = None                    # recv_x missing
+    assert f2(*bad) == B.EP_ERR_INVALID_ARG
+    bad = list(fargs); bad[0] = vp(18)                   # x misaligned
+    assert f2(*bad) == B.EP_ERR_INVALID_ARG
+    bad = list(fargs); bad[21] = None                    # status missing
+    assert f2(*bad) == B.EP_ERR_INVALID_ARG
+    bad = list(fargs); bad[7] = 4096                     # more experts than the limit
+    assert f2(*bad) == B.EP_ERR_UNSUPPORTED
+    bad = list(fargs); bad[10] = ctypes.byref(L4)        # layout check: src_dst_count needs R | T
+    assert f2(*bad) == B.EP_ERR_INVALID_ARG
+    bad = list(fargs); bad[11] = None                    # workspace missing (layout check)
+    assert f2(*bad) == B.EP_ERR_INVALID_ARG
     # combine
     c = lib.ep_combine
     c.restype = ctypes.c_int32
