@@ -95,12 +95,11 @@ int64_t ep_recv_capacity_bound(int num_tokens, int num_topk, int num_ranks) {
 
 }  // extern "C"
 
-namespace {
+namespace epg {
 
-// Host checks of ep_get_layout and its parameter block (no launch).
 ep_status_t layout_params(const int64_t* topk_idx, int T, int K, int E, int R, int ranks_per_node,
                           int expert_alignment, const ep_layout_t* out, void* workspace, size_t ws_bytes,
-                          int32_t* d_status, epg::LayoutParams& p) {
+                          int32_t* d_status, bool check_workspace, LayoutParams& p) {
     if (!out || !d_status) return EP_ERR_INVALID_ARG;
     ep_status_t s = check_shape(T, K, E, R);
     if (s != EP_OK) return s;
@@ -125,6 +124,7 @@ ep_status_t layout_params(const int64_t* topk_idx, int T, int K, int E, int R, i
         return EP_ERR_INVALID_ARG;
     const int nodes_ws = ranks_per_node > 0 ? R / ranks_per_node : 0;
     const epg::LayoutWorkspace w = epg::layout_workspace(T, E, R, nodes_ws);
+    if (!check_workspace) return EP_OK;
     if (!ok_ptr(workspace) || ws_bytes < w.total) return EP_ERR_INVALID_ARG;
 
     p = epg::LayoutParams{};
@@ -159,7 +159,7 @@ ep_status_t layout_params(const int64_t* topk_idx, int T, int K, int E, int R, i
     return EP_OK;
 }
 
-}  // namespace
+}  // namespace epg
 
 extern "C" {
 
@@ -167,8 +167,8 @@ ep_status_t ep_get_layout(const int64_t* topk_idx, int T, int K, int E, int R, i
                           int expert_alignment, const ep_layout_t* out, void* workspace,
                           size_t ws_bytes, int32_t* d_status, void* cuda_stream) {
     epg::LayoutParams p{};
-    const ep_status_t s = layout_params(topk_idx, T, K, E, R, ranks_per_node, expert_alignment, out, workspace,
-                                        ws_bytes, d_status, p);
+    const ep_status_t s = epg::layout_params(topk_idx, T, K, E, R, ranks_per_node, expert_alignment, out, workspace,
+                                             ws_bytes, d_status, true, p);
     if (s != EP_OK) return s;
     const cudaStream_t stream = static_cast<cudaStream_t>(cuda_stream);
     if (epg::launch_layout(p, stream) != cudaSuccess) return EP_ERR_CUDA;
@@ -296,8 +296,8 @@ ep_status_t ep_layout_and_dispatch(const void* x, const int64_t* topk_idx, const
         (recv_src_idx && !aligned16(recv_src_idx)))
         return EP_ERR_INVALID_ARG;
     epg::LayoutParams lp{};
-    s = layout_params(topk_idx, T, K, E, R, ranks_per_node, expert_alignment, layout, workspace, ws_bytes, d_status,
-                      lp);
+    s = epg::layout_params(topk_idx, T, K, E, R, ranks_per_node, expert_alignment, layout, workspace, ws_bytes,
+                           d_status, true, lp);
     if (s != EP_OK) return s;
     // Few tokens: one kernel; its CTAs derive the rows themselves and write
     // the layout (expanded rows and node rows need the layout kernel).

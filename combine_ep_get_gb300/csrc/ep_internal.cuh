@@ -185,6 +185,12 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
     return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
+// Host checks of ep_get_layout (every argument; the workspace too when
+// check_workspace) and its parameter block, without a launch.
+ep_status_t layout_params(const int64_t* topk_idx, int T, int K, int E, int R, int ranks_per_node,
+                          int expert_alignment, const ep_layout_t* out, void* workspace, size_t ws_bytes,
+                          int32_t* d_status, bool check_workspace, LayoutParams& p);
+
 // Workspace carve-up shared by the size query and the launcher.
 struct LayoutWorkspace {
     size_t off_rank, off_expert, off_node, off_bitmap, total;
@@ -195,8 +201,12 @@ LayoutWorkspace layout_workspace(int T, int E, int R, int num_nodes);
 // Device helpers
 // ---------------------------------------------------------------------------
 
-// A bounded wait gives up after this many nanoseconds of %globaltimer.
-constexpr uint64_t kWaitTimeoutNs = 2000000000ull;
+// A bounded wait gives up after this many nanoseconds of %globaltimer (the
+// failure-path test builds a copy of the library with a shorter limit).
+#ifndef EP_WAIT_TIMEOUT_NS
+#define EP_WAIT_TIMEOUT_NS 2000000000ull
+#endif
+constexpr uint64_t kWaitTimeoutNs = EP_WAIT_TIMEOUT_NS;
 
 // Wait until the kernel this one depends on (previous on the stream) has
 // completed and its writes are visible; returns at once without a dependency.

@@ -9,8 +9,6 @@
 // point serves them: the workspace is a file-scope device array compiled into
 // the library, so the call allocates nothing.  It forwards to ep_get_layout
 // with that array as the workspace; results are identical.
-#include <mutex>
-
 #include "ep_internal.cuh"
 
 namespace {
@@ -21,25 +19,14 @@ namespace {
 // address: host code must use the address from cudaGetSymbolAddress below.
 static __device__ __align__(256) unsigned char g_layout_scratch[EP_LAYOUT_STATIC_SCRATCH_BYTES];
 
-constexpr int kMaxDevices = 64;
-std::mutex g_mu;
-void* g_scratch_addr[kMaxDevices] = {};
-
-// Device address of g_layout_scratch on the current device, resolved once
-// per device (with that device current) and cached.
+// Device address of g_layout_scratch on the current device, looked up on
+// every call (with that device current; cheap, allocates nothing), so that it
+// stays right if the device was reset and the module loaded again.
 cudaError_t scratch_address(void** out) {
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
+    void* p = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_layout_scratch);
     if (e != cudaSuccess) return e;
-    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-    std::lock_guard<std::mutex> lock(g_mu);
-    if (g_scratch_addr[dev] == nullptr) {
-        void* p = nullptr;
-        e = cudaGetSymbolAddress(&p, g_layout_scratch);
-        if (e != cudaSuccess) return e;
-        g_scratch_addr[dev] = p;
-    }
-    *out = g_scratch_addr[dev];
+    *out = p;
     return cudaSuccess;
 }
 
@@ -50,8 +37,13 @@ extern "C" ep_status_t ep_get_layout_static_scratch(const int64_t* topk_idx, int
                                                     int ranks_per_node, int expert_alignment,
                                                     const ep_layout_t* out, int32_t* d_status,
                                                     void* cuda_stream) {
-    if (num_tokens < 0 || num_experts < 1 || num_ranks < 1 || ranks_per_node < 0)
-        return EP_ERR_INVALID_ARG;
+    // every argument check of ep_get_layout first, so a bad argument gives the
+    // same code as there; then the size of the built-in scratch
+    epg::LayoutParams unused{};
+    const ep_status_t s = epg::layout_params(topk_idx, num_tokens, num_topk, num_experts, num_ranks,
+                                             ranks_per_node, expert_alignment, out, nullptr, 0, d_status,
+                                             false, unused);
+    if (s != EP_OK) return s;
     const size_t need =
         ep_layout_workspace_bytes(num_tokens, num_topk, num_experts, num_ranks, ranks_per_node);
     if (need > EP_LAYOUT_STATIC_SCRATCH_BYTES) return EP_ERR_UNSUPPORTED;

@@ -166,16 +166,18 @@ ep_status_t ep_get_layout(const int64_t* topk_idx, int num_tokens, int num_topk,
  * the library, which every GPU that loads the library holds until the process
  * exits.  The call allocates nothing.
  *
- * Limit: returns EP_ERR_UNSUPPORTED, before any launch, when
+ * Arguments are checked exactly as by ep_get_layout (same codes); then, before
+ * any launch, the call returns EP_ERR_UNSUPPORTED when
  * ep_layout_workspace_bytes(num_tokens, num_topk, num_experts, num_ranks,
  * ranks_per_node) > EP_LAYOUT_STATIC_SCRATCH_BYTES (for example T=32768,
  * E=256, R=64 needs about 0.43 MB; T=16384, E=2048, R=1024 about 2.9 MB).
- * The first call on a device looks up the array's device address (with that
- * device current) and returns EP_ERR_CUDA if that fails; make that first call
- * before any stream capture.  All calls share the one array, and every call
- * overwrites the scratch words it reads, so nothing needs clearing between
- * calls; but calls whose kernels overlap on the GPU (on unordered streams)
- * race on it and give wrong layouts: order them.
+ * Every call looks up the array's device address on the current device
+ * (cudaGetSymbolAddress, which allocates nothing) and returns EP_ERR_CUDA if
+ * that fails; the first call on a device also loads the library's device
+ * code there, so make it before any stream capture.  All calls share the one
+ * array, and every call overwrites the scratch words it reads, so nothing
+ * needs clearing between calls; but calls whose kernels overlap on the GPU
+ * (on unordered streams) race on it and give wrong layouts: order them.
  */
 ep_status_t ep_get_layout_static_scratch(const int64_t* topk_idx, int num_tokens, int num_topk,
                                          int num_experts, int num_ranks, int ranks_per_node,

@@ -4,9 +4,11 @@ a process whose device memory is all reserved up front by a pooling
 allocator).  It uses a device array built into the library instead of a
 caller workspace.
 
-Called here through the C ABI (ctypes), twice in a row on different inputs,
-each result checked against the workspace entry point ep_get_layout on the
-same input (integer outputs: exact).  This file is collected last.
+Called here through the C ABI (ctypes) several times in a row on different
+inputs -- a smaller call after a larger one too, which finds the most stale
+scratch -- each result checked against the workspace entry point
+ep_get_layout on the same input (integer outputs: exact).  This file is
+collected last.
 """
 import ctypes
 
@@ -42,6 +44,7 @@ def test_static_scratch_matches_workspace_entry_point_twice():
     cases = [
         (4096, 8, 256, 8, 0, 1),           # DeepSeek-V3-shaped routing
         (32768, 8, 256, 64, 8, 2),         # large, node counts, src x dst counts
+        (128, 8, 256, 32, 0, 3),           # smaller after larger: decode-shaped, single-CTA path
     ]
     for T, K, E, R, rpn, seed in cases:
         idx = to_dev(make_inputs(T, 8, E, K, R, seed=seed, mask_frac=0.03, with_x=False)["topk_idx"])
@@ -61,7 +64,25 @@ def test_static_scratch_rejects_sizes_beyond_its_array():
     from gpu_path import B
     T, K, E, R = 65536, 8, 2048, 1024
     assert B.ep_layout_workspace_bytes(T, K, E, R, 0) > (4 << 20)
-    lay = B.ep_layout_t()
+    # valid-looking 16-byte-aligned stand-in addresses: every argument check
+    # passes, the size check rejects the call before anything is launched
+    vp = ctypes.c_void_p
+    lay = B.ep_layout_t(16, None, 32, 48, 64, 80, 96, None, None)
     fn = B.library().ep_get_layout_static_scratch
-    code = fn(None, T, K, E, R, 0, 1, ctypes.byref(lay), None, None)
+    code = fn(vp(16), T, K, E, R, 0, 1, ctypes.byref(lay), vp(16), None)
     assert code == B.EP_ERR_UNSUPPORTED
+
+
+def test_static_scratch_argument_errors_match_the_workspace_entry_point():
+    """A bad argument gives the code ep_get_layout gives, even for sizes the
+    built-in scratch could not hold (checked on the host, nothing launched)."""
+    from gpu_path import B
+    lay = B.ep_layout_t()
+    st = ctypes.c_void_p(16)             # a stand-in device address; never dereferenced here
+    fn = B.library().ep_get_layout_static_scratch
+    for args in [(None, 10, 8, 256, 7, 0, 1),            # R does not divide E
+                 (None, 65536, 8, 2048, 1024, 3, 1),     # too large, and rpn does not divide R
+                 (None, 10, 33, 256, 8, 0, 1)]:          # top-33
+        want = B.library().ep_get_layout(args[0], *args[1:], ctypes.byref(lay), None, 0, st, None)
+        got = fn(args[0], *args[1:], ctypes.byref(lay), st, None)
+        assert got == want != B.EP_OK
