@@ -68,5 +68,33 @@ def build(force: bool = False, verbose: bool = False) -> str:
     return LIB
 
 
+def build_variant(name: str, defines, recompile=("dispatch.cu",)) -> str:
+    """A test-only copy of the library: the files in `recompile` compiled
+    again with `defines` (e.g. ["-DEP_WAIT_TIMEOUT_NS=1000000ull"]) and linked
+    with the product build's other objects into _build/<name>/libep_get_<name>.so.
+    Never the product library: only tests load it, by path."""
+    build()
+    out_dir = os.path.join(BUILD, name)
+    os.makedirs(out_dir, exist_ok=True)
+    lib = os.path.join(out_dir, "libep_get_%s.so" % name)
+    nvcc = _nvcc()
+    objs = []
+    for src in sources():
+        base = os.path.basename(src)
+        obj = os.path.join(BUILD, base + ".o")
+        if base in recompile:
+            obj = os.path.join(out_dir, base + ".o")
+            cmd = [nvcc] + ARCH + NVCC_FLAGS + list(defines) + ["-c", src, "-o", obj]
+            r = subprocess.run(cmd, capture_output=True, text=True)
+            if r.returncode != 0:
+                raise RuntimeError("nvcc failed for %s:\n%s\n%s" % (src, r.stdout, r.stderr))
+        objs.append(obj)
+    r = subprocess.run([nvcc] + ARCH + ["-shared", "-Xlinker", "-Bsymbolic", "-o", lib] + objs,
+                       capture_output=True, text=True)
+    if r.returncode != 0:
+        raise RuntimeError("link failed:\n%s\n%s" % (r.stdout, r.stderr))
+    return lib
+
+
 if __name__ == "__main__":
     print(build(force="--force" in sys.argv, verbose=True))

@@ -227,6 +227,12 @@ __global__ void __launch_bounds__(kBf16Threads) dispatch_bf16_kernel(const Dispa
             const uint32_t bytes = min(p.chunk_bytes, row_bytes - off);
             const int slot = static_cast<int>(i % kStages);
             mbar_arrive_expect_tx(&bars[slot], bytes);
+#ifdef EP_TEST_DROP_FIRST_LOAD
+            // failure-path test build only: CTA 0 announces its first load
+            // and never issues it, so that slot's wait runs out (no copy is
+            // in flight for it, every access stays in bounds)
+            if (blockIdx.x == 0 && i == 0) return;
+#endif
             bulk_load(stage + static_cast<size_t>(slot) * p.chunk_bytes, p.x + t * row_bytes + off,
                       bytes, &bars[slot]);
         };
