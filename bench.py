@@ -1,9 +1,10 @@
 #!/usr/bin/env python
 """Benchmark of the MoE dispatch / combine hot path on GB300.
 
-One step = routing layout (ep_get_layout) -> bf16 dispatch (ep_dispatch) ->
-identity expert (the combine reads the dispatched rows) -> unweighted combine
-(ep_combine), on the DeepSeek-V3-shaped prefill workload: T=4096 tokens,
+One step = routing layout and bf16 dispatch (ep_layout_and_dispatch: the
+layout kernel, then the dispatch kernel) -> identity expert (the combine reads
+the dispatched rows) -> unweighted combine (ep_combine), on the
+DeepSeek-V3-shaped prefill workload: T=4096 tokens,
 H=7168 bf16, E=256 experts, top-8 distinct uniform experts per token, R=8
 logical ranks in one GPU's memory.  Inputs are seeded synthetic data.
 
@@ -283,7 +284,11 @@ def kernel_source_hash(kernel):
 
 
 def recorded_traffic(kernel, workload):
-    """DRAM bytes per launch from an ncu capture, if recorded for this source."""
+    """DRAM bytes per launch from an ncu capture, if recorded for this source
+    ("layout+dispatch": the sum of the two kernels' records)."""
+    if "+" in kernel:
+        parts = [recorded_traffic(k, workload) for k in kernel.split("+")]
+        return None if any(p is None for p in parts) else sum(parts)
     try:
         with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
             rec = json.load(f)[workload][kernel]
@@ -346,6 +351,7 @@ def run_ours(args):
     out = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     flush_rd = torch.zeros(L2_FLUSH_BYTES // 8, dtype=torch.int64, device=dev)
+    flush_rd2 = torch.zeros(L2_FLUSH_BYTES // 8, dtype=torch.int64, device=dev)
     flush_sink = torch.zeros((), dtype=torch.int64, device=dev)
 
     def flush_l2():
@@ -391,6 +397,20 @@ def run_ours(args):
     def do_layout():
         B.ep_get_layout(idx, E, R, lay, ws, status, rpn)
 
+    # The rank path over the whole GPU runs layout and dispatch as one call
+    # (ep_layout_and_dispatch): with few tokens the dispatch then derives its
+    # rows itself and runs beside the layout; with many it is the same two
+    # launches as the separate calls.
+    fused = args.path == "rank" and sms_dispatch == 0
+
+    def do_layout_dispatch():
+        if fused:
+            B.ep_layout_and_dispatch(x, idx, w, E, R, lay, ws, recv_x, recv_idx, recv_w, recv_src, status,
+                                     recv_sf=recv_sf, out_dtype=dtype_code, ranks_per_node=rpn)
+        else:
+            do_layout()
+            do_dispatch()
+
     def do_dispatch():
         if hierarchical:
             B.ep_dispatch_hierarchical(x, idx, w, E, R, rpn, lay, hier["node_x"], recv_x, status,
@@ -417,6 +437,8 @@ def run_ours(args):
         do_layout()
         do_dispatch()
         do_combine()
+        do_layout_dispatch()
+        do_combine()
     torch.cuda.synchronize()
     st = int(status.item())
     if st != 0:
@@ -425,25 +447,35 @@ def run_ours(args):
     use_graph = not args.no_graph
 
     def step_body(ev, split):
-        # split: an extra event between layout and dispatch (per-kernel
-        # breakdown); without it the dispatch launch overlaps the layout's
-        # tail (programmatic dependent launch), as in a real layer
+        # split (per-kernel breakdown): separate calls with an event between
+        # layout and dispatch, and after the combine two read passes over
+        # different 256 MiB buffers: the first also writes back what the
+        # combine left dirty in L2, the second finds only clean lines.
+        # Without split the dispatch launch overlaps the layout (programmatic
+        # dependent launch), as in a real layer.
         flush_l2()
         ev[0].record()
-        do_layout()
         if split:
+            do_layout()
             ev[4].record()
-        do_dispatch()
+            do_dispatch()
+        else:
+            do_layout_dispatch()
         ev[1].record()
         flush_l2()
         ev[2].record()
         do_combine()
         ev[3].record()
+        if split:
+            torch.sum(flush_rd, dim=0, out=flush_sink)
+            ev[5].record()
+            torch.sum(flush_rd2, dim=0, out=flush_sink)
+            ev[6].record()
 
     def new_events():
         if use_graph:
-            return [torch.cuda.Event(enable_timing=True, external=True) for _ in range(5)]
-        return [torch.cuda.Event(enable_timing=True) for _ in range(5)]
+            return [torch.cuda.Event(enable_timing=True, external=True) for _ in range(7)]
+        return [torch.cuda.Event(enable_timing=True) for _ in range(7)]
 
     # One CUDA graph per step holds the flushes, the three calls and the timing
     # events; n_graphs instances rotate so the GPU never waits for the host
@@ -474,10 +506,11 @@ def run_ours(args):
 
         def harvest(k):
             ev = slots[k][1]
-            ev[3].synchronize()
+            ev[6 if split else 3].synchronize()
             t = [ev[0].elapsed_time(ev[1]), ev[2].elapsed_time(ev[3])]
             if split:
-                t += [ev[0].elapsed_time(ev[4]), ev[4].elapsed_time(ev[1])]
+                t += [ev[0].elapsed_time(ev[4]), ev[4].elapsed_time(ev[1]),
+                      ev[3].elapsed_time(ev[5]) - ev[5].elapsed_time(ev[6])]
             times.append(t)
 
         for i in range(warm):
@@ -531,15 +564,23 @@ def run_ours(args):
     tokens_ps = replica_value(T, args.steps, max_total, world)
     ms_per_step = max_total / args.steps
 
-    avg = {"layout": statistics.mean(t[2] for t in split_times),
-           "dispatch": statistics.mean(t[3] for t in split_times),
+    # Timed region: the layout+dispatch call(s) and the combine, each between
+    # its own events.  Breakdown pass: layout and dispatch apart, and the
+    # combine plus the write-back of its dirty L2 lines (the extra time a
+    # 256 MiB read pass right after it takes over one over clean L2).
+    avg = {"layout+dispatch": statistics.mean(t_ld),
            "combine": statistics.mean(t_combine),
-           "layout+dispatch": statistics.mean(t_ld)}
-    source = {"layout": "breakdown pass", "dispatch": "breakdown pass", "combine": "timed region",
-              "layout+dispatch": "timed region"}
-    dominant = "dispatch" if avg["dispatch"] >= avg["combine"] else "combine"
-    peak, peak_kind = hbm_peak()
+           "layout": statistics.mean(t[2] for t in split_times),
+           "dispatch": statistics.mean(t[3] for t in split_times),
+           "combine_with_writeback": statistics.mean(t[1] + max(t[4], 0.0) for t in split_times)}
+    source = {"layout+dispatch": "timed region", "combine": "timed region", "layout": "breakdown pass",
+              "dispatch": "breakdown pass",
+              "combine_with_writeback": "breakdown pass: combine + write-back of its dirty L2 lines"}
     nbytes["layout+dispatch"] = nbytes["layout"] + nbytes["dispatch"]
+    nbytes["combine_with_writeback"] = nbytes["combine"]
+    # the roofline's kernel: the longer of the two timed-region intervals
+    dominant = "layout+dispatch" if avg["layout+dispatch"] >= avg["combine"] else "combine"
+    peak, peak_kind = hbm_peak()
     achieved = nbytes[dominant] / (avg[dominant] * 1e-3) / 1e9
     per_kernel = {k: {"ms": avg[k], "gbs": nbytes[k] / (avg[k] * 1e-3) / 1e9,
                       "frac_of_" + peak_kind: nbytes[k] / (avg[k] * 1e-3) / 1e9 / peak,
@@ -586,7 +627,11 @@ def run_ours(args):
                            if hierarchical else ""),
         },
         "per_kernel": per_kernel,
-        "roofline": {"bound": "hbm", "kernel": dominant, "achieved": achieved, "peak": peak,
+        "roofline": {"bound": "hbm",
+                     "kernel": ("layout+dispatch (%s: the layout kernel, then the dispatch kernel launched "
+                                "during it)" % ("ep_layout_and_dispatch" if fused else "ep_get_layout, ep_dispatch")
+                                if dominant == "layout+dispatch" else "combine"),
+                     "achieved": achieved, "peak": peak,
                      "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / peak,
                      "frac_of_nominal": achieved / HBM_NOMINAL_GBS,
                      # recorded DRAM traffic is of the rank path's bf16 kernels only
@@ -599,6 +644,7 @@ def run_ours(args):
     }
     if world == 1 and rank == 0 and not args.no_cpu_baseline:
         result["cpu_baseline"] = cpu_baseline(cfg, data, nbytes, N, args.cpu_seconds)
+        result["cpu_baseline_all_cores"] = cpu_baseline_all_cores(cfg, data, N, args.cpu_seconds)
     if rank == 0:
         print(json.dumps(result))
     if world > 1:
@@ -611,7 +657,8 @@ def run_e2e(args, B, torch, dev, x_host, idx_host, w_host, lay, ws, status, recv
     """End to end through the public calls with host buffers.
 
     Every step copies its inputs (x, topk_idx, topk_weights) from pinned host
-    memory to the device, runs ep_get_layout, ep_dispatch and ep_combine, and
+    memory to the device, runs ep_layout_and_dispatch (the rank path; the
+    other paths ep_get_layout and their dispatch) and the combine, and
     copies the combined rows back to pinned host memory.  Steps are pipelined
     on three streams with double-buffered device inputs and outputs: the
     copy-in of step i+1 and the copy-out of step i-1 overlap the kernels of
@@ -641,8 +688,9 @@ def run_e2e(args, B, torch, dev, x_host, idx_host, w_host, lay, ws, status, recv
             ev_in[b].record(s_in)
         s_comp.wait_event(ev_in[b])
         s_comp.wait_event(ev_out[b])             # step i-2's output has been copied out
-        B.ep_get_layout(idd[b], E, R, lay, ws, status, rpn, stream=s_comp)
         dtype_code = B.EP_FP8_E4M3 if cfg.fp8 else B.EP_BF16
+        if args.path != "rank":
+            B.ep_get_layout(idd[b], E, R, lay, ws, status, rpn, stream=s_comp)
         if args.path == "hierarchical":
             B.ep_dispatch_hierarchical(xd[b], idd[b], wd[b], E, R, rpn, lay, hier["node_x"], recv_x, status,
                                        node_sf=hier["node_sf"], node_src_idx=hier["node_src"], recv_sf=recv_sf,
@@ -655,8 +703,9 @@ def run_e2e(args, B, torch, dev, x_host, idx_host, w_host, lay, ws, status, recv
                                    recv_sf=recv_sf, out_dtype=dtype_code, stream=s_comp)
             B.ep_combine_expanded(y, wd[b], idd[b].shape[1], E, R, lay, outd[b], status, stream=s_comp)
         else:
-            B.ep_dispatch(xd[b], idd[b], wd[b], E, R, lay, recv_x, recv_idx, recv_w, recv_src, status,
-                          recv_sf=recv_sf, out_dtype=dtype_code, stream=s_comp)
+            B.ep_layout_and_dispatch(xd[b], idd[b], wd[b], E, R, lay, ws, recv_x, recv_idx, recv_w, recv_src,
+                                     status, recv_sf=recv_sf, out_dtype=dtype_code, ranks_per_node=rpn,
+                                     stream=s_comp)
             B.ep_combine(y, idd[b], wd[b] if cfg.weighted else None, E, R, lay, outd[b], status,
                          stream=s_comp)
         ev_comp[b].record(s_comp)
@@ -730,6 +779,34 @@ def cpu_baseline(cfg, data, nbytes, N, seconds):
     return {"value": moved / el / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
             "sample": "%d full step(s) of the workload (all %d tokens), single-threaded C oracle"
                       % (done, cfg.T),
+            "tokens_per_s": done * cfg.T / el, **host_cpu()}
+
+
+def cpu_baseline_all_cores(cfg, data, N, seconds):
+    """The oracle's OpenMP build (same C source, token loops of dispatch and
+    combine split over the host's cores; the layout stays sequential) on
+    whole steps of the workload: layout, dispatch of every token into its
+    rows, combine of the dispatched rows."""
+    import numpy as np
+    import oracle
+    idx, w, xb = data["topk_idx"], data["topk_weights"], data["x_bits"]
+    with oracle.threads() as n:
+        if n is None:
+            return {"unavailable": "no OpenMP build of the oracle on this host"}
+        done, moved = 0, 0
+        t0 = time.perf_counter()
+        while True:
+            L = oracle.layout(idx, cfg.E, cfg.R, cfg.ranks_per_node)
+            d = oracle.dispatch(xb, idx, w, cfg.E, cfg.R, L.dst_row, capacity=L.num_recv)
+            oracle.combine(d["recv_x"].view(np.uint16), idx, None, cfg.E, cfg.R, L.dst_row)
+            done += 1
+            moved += _sample_bytes(cfg, cfg.T, L.num_recv)
+            if time.perf_counter() - t0 >= seconds:
+                break
+        el = time.perf_counter() - t0
+    return {"value": moved / el / 1e9, "unit": "GB/s", "cores": n, "kind": "oracle",
+            "sample": "%d full step(s) of the workload (all %d tokens), OpenMP build of the C oracle on %d "
+                      "threads" % (done, cfg.T, n),
             "tokens_per_s": done * cfg.T / el, **host_cpu()}
 
 
