@@ -69,6 +69,9 @@ namespace {
 #ifndef EP_DISPATCH_FP8_WIDE_MIN_BLOCKS
 #define EP_DISPATCH_FP8_WIDE_MIN_BLOCKS 5   // same, many-token rank-row mode (fits 48 registers unspilled)
 #endif
+#ifndef EP_DISPATCH_FP8_HOISTED
+#define EP_DISPATCH_FP8_HOISTED 1         // FP8 many-token mode: store pass with offsets hoisted out of the loop
+#endif
 #ifndef EP_DISPATCH_FP8_FIT_WARPS
 #define EP_DISPATCH_FP8_FIT_WARPS 1       // FP8 many-token mode: CTA warps fitted to the piece's blocks
 #endif
@@ -817,7 +820,49 @@ __device__ __forceinline__ void dispatch_fp8_item(const DispatchParams& p, int64
             }
         }
     };
-    if (kMerged) {
+    if constexpr (kMerged && EP_DISPATCH_FP8_HOISTED) {
+#pragma unroll
+        for (int q = 0; q < kFp8Rounds; ++q)
+            if (warp_has_round(q)) cast_round(q);   // warp-uniform
+        // Every per-lane offset, predicate and base pointer is formed once,
+        // outside the destination loop, which then costs one row address,
+        // two predicated 16-byte code stores and, on a block's first lane,
+        // two predicated scale stores per destination.
+        static_assert(kFp8Rounds == 2 && kVec == 2, "the hoisted store pass handles two rounds of 16-byte codes");
+        const int bq0 = b0, bq1 = b0 + blocks_per_round;
+        const bool ok0 = bq0 < b_end, ok1 = bq1 < b_end;
+        const int64_t co0 = static_cast<int64_t>(bq0) * 128 + sub_col;
+        const int64_t co1 = static_cast<int64_t>(bq1) * 128 + sub_col;
+        uint8_t* const rx = p.recv_x;
+        float* const rsf = p.recv_sf;
+        const int64_t H = p.H, cap = p.capacity;
+        const bool sf_lane = sub == 0 && rsf != nullptr;
+        const bool col = p.sf_col_major != 0;
+        const int64_t sfs = col ? 1 : nb;                                   // scale index = dd * sfs + so_q
+        const int64_t so0 = col ? static_cast<int64_t>(bq0) * p.sf_stride : bq0;
+        const int64_t so1 = col ? static_cast<int64_t>(bq1) * p.sf_stride : bq1;
+        const uint4 c0 = make_uint4(code[0][0], code[0][1], code[0][2], code[0][3]);
+        const uint4 c1 = make_uint4(code[1][0], code[1][1], code[1][2], code[1][3]);
+        const float s0 = sfq[0], s1 = sfq[1];
+        for (int rb = 0; rb < n_dst; rb += 32) {
+            const int d = rb == 0 ? d0 : rb == 32 ? d1 : (rb + lane < n_dst ? drow[rb + lane] : -1);
+            if (d >= cap && c == 0) cap_bad = true;
+            unsigned m = __ballot_sync(0xffffffffu, d >= 0 && d < cap);
+            while (m) {
+                const int sl = __ffs(m) - 1;
+                m &= m - 1;
+                const int64_t dd = __shfl_sync(0xffffffffu, d, sl);
+                uint8_t* row = rx + dd * H;
+                if (ok0) *reinterpret_cast<uint4*>(row + co0) = c0;
+                if (ok1) *reinterpret_cast<uint4*>(row + co1) = c1;
+                if (sf_lane) {
+                    float* srow = rsf + dd * sfs;
+                    if (ok0) srow[so0] = s0;
+                    if (ok1) srow[so1] = s1;
+                }
+            }
+        }
+    } else if constexpr (kMerged) {
 #pragma unroll
         for (int q = 0; q < kFp8Rounds; ++q)
             if (warp_has_round(q)) cast_round(q);   // warp-uniform
