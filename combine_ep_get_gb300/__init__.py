@@ -14,7 +14,7 @@ _BINDING_NAMES = (
     "ep_recv_capacity_bound", "ep_status_string", "Layout", "alloc_layout",
     "ep_get_layout_static_scratch", "ep_dispatch_expanded", "ep_combine_expanded",
     "ep_expanded_capacity_bound", "ep_combine_topk_weights", "ep_accumulate_expert_stats",
-    "EP_BF16", "EP_FP8_E4M3",
+    "ep_bounds_checked", "EP_BF16", "EP_FP8_E4M3",
 )
 
 

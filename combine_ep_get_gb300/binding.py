@@ -11,11 +11,14 @@ import os
 import torch
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_HERE, "libep_get.so")
+# EP_GET_LIBRARY names another build of the same library to load instead:
+# the bounds-checked copy that the tests build (ep_bounds_checked() says which
+# one is loaded).  Unset, the product library.
+LIB_PATH = os.environ.get("EP_GET_LIBRARY") or os.path.join(_HERE, "libep_get.so")
 
 if not os.path.exists(LIB_PATH):
-    raise ImportError("libep_get.so is not built; run `python -c \"import __graft_entry__ as g; "
-                      "g.build()\"` or `python combine_ep_get_gb300/build.py`")
+    raise ImportError("%s is not built; run `python -c \"import __graft_entry__ as g; "
+                      "g.build()\"` or `python combine_ep_get_gb300/build.py`" % LIB_PATH)
 
 _lib = ctypes.CDLL(LIB_PATH)
 
@@ -26,6 +29,7 @@ EP_ERR_INVALID_INDEX = 4
 EP_ERR_CAPACITY = 8
 EP_ERR_TIMEOUT = 16
 EP_ERR_CUDA = 32
+EP_ERR_OUT_OF_BOUNDS = 64
 EP_BF16 = 0
 EP_FP8_E4M3 = 1
 
@@ -77,6 +81,8 @@ _lib.ep_status_string.restype = ctypes.c_char_p
 _lib.ep_status_string.argtypes = [ctypes.c_int32]
 _lib.ep_abi_version.restype = _i
 _lib.ep_abi_version.argtypes = []
+_lib.ep_bounds_checked.restype = _i
+_lib.ep_bounds_checked.argtypes = []
 _lib.ep_dispatch_hierarchical.restype = ctypes.c_int32
 _lib.ep_dispatch_hierarchical.argtypes = [_vp, _vp, _vp, _i, _i, _i, _i, _i, _i, ctypes.POINTER(ep_layout_t), _i,
                                           _i64, _vp, _vp, _vp, _i64, _vp, _vp, _i, _vp, _vp, _vp, _vp, _vp]
@@ -91,6 +97,11 @@ _lib.ep_theoretical_num_sms.argtypes = [_i, _i, _i, _i, _i, _i, ctypes.c_double,
 def library():
     """The loaded ctypes library (for callers that marshal raw pointers)."""
     return _lib
+
+
+def ep_bounds_checked() -> bool:
+    """True when the loaded library is the bounds-checked build."""
+    return bool(_lib.ep_bounds_checked())
 
 
 def _ptr(t):

@@ -69,30 +69,45 @@ def build(force: bool = False, verbose: bool = False) -> str:
 
 
 def build_variant(name: str, defines, recompile=("dispatch.cu",)) -> str:
-    """A test-only copy of the library: the files in `recompile` compiled
-    again with `defines` (e.g. ["-DEP_WAIT_TIMEOUT_NS=1000000ull"]) and linked
-    with the product build's other objects into _build/<name>/libep_get_<name>.so.
-    Never the product library: only tests load it, by path."""
+    """A test-only copy of the library: the files in `recompile` (or every
+    source, for recompile="all") compiled again with `defines` (e.g.
+    ["-DEP_WAIT_TIMEOUT_NS=1000000ull"]) and linked with the product build's
+    other objects into _build/<name>/libep_get_<name>.so.  Never the product
+    library: only tests load it, by path.  Rebuilt when a source, a header or
+    the defines changed."""
     build()
     out_dir = os.path.join(BUILD, name)
     os.makedirs(out_dir, exist_ok=True)
     lib = os.path.join(out_dir, "libep_get_%s.so" % name)
+    stamp = os.path.join(out_dir, "defines.txt")
+    want = " ".join(defines) + " | " + (recompile if isinstance(recompile, str) else " ".join(recompile))
+    if (os.path.exists(lib) and os.path.exists(stamp) and open(stamp).read() == want
+            and os.path.getmtime(lib) >= os.path.getmtime(LIB)
+            and all(os.path.getmtime(f) <= os.path.getmtime(lib) for f in sources() + HEADERS + [__file__])):
+        return lib
     nvcc = _nvcc()
-    objs = []
-    for src in sources():
+
+    def obj_of(src):
         base = os.path.basename(src)
-        obj = os.path.join(BUILD, base + ".o")
-        if base in recompile:
-            obj = os.path.join(out_dir, base + ".o")
-            cmd = [nvcc] + ARCH + NVCC_FLAGS + list(defines) + ["-c", src, "-o", obj]
-            r = subprocess.run(cmd, capture_output=True, text=True)
-            if r.returncode != 0:
-                raise RuntimeError("nvcc failed for %s:\n%s\n%s" % (src, r.stdout, r.stderr))
-        objs.append(obj)
-    r = subprocess.run([nvcc] + ARCH + ["-shared", "-Xlinker", "-Bsymbolic", "-o", lib] + objs,
+        if recompile != "all" and base not in recompile:
+            return os.path.join(BUILD, base + ".o")
+        obj = os.path.join(out_dir, base + ".o")
+        cmd = [nvcc] + ARCH + NVCC_FLAGS + list(defines) + ["-c", src, "-o", obj]
+        r = subprocess.run(cmd, capture_output=True, text=True)
+        if r.returncode != 0:
+            raise RuntimeError("nvcc failed for %s:\n%s\n%s" % (src, r.stdout, r.stderr))
+        return obj
+
+    with ThreadPoolExecutor(max_workers=len(sources())) as ex:
+        objs = list(ex.map(obj_of, sources()))
+    tmp = lib + ".tmp.%d" % os.getpid()
+    r = subprocess.run([nvcc] + ARCH + ["-shared", "-Xlinker", "-Bsymbolic", "-o", tmp] + objs,
                        capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError("link failed:\n%s\n%s" % (r.stdout, r.stderr))
+    os.replace(tmp, lib)
+    with open(stamp, "w") as f:
+        f.write(want)
     return lib
 
 

@@ -50,7 +50,9 @@ ep_status_t check_shape(int T, int K, int E, int R) {
 
 extern "C" {
 
-int ep_abi_version(void) { return 7; }
+int ep_abi_version(void) { return 8; }
+
+int ep_bounds_checked(void) { return EP_GET_CHECKED ? 1 : 0; }
 
 size_t ep_layout_workspace_bytes(int num_tokens, int num_topk, int num_experts, int num_ranks,
                                  int ranks_per_node) {
@@ -619,15 +621,15 @@ ep_status_t ep_accumulate_expert_stats(const ep_layout_t* layout, int E, int64_t
 }
 
 const char* ep_status_string(int32_t status) {
-    static const char* const kNames[6] = {"invalid_arg", "unsupported", "invalid_index",
-                                          "capacity",    "timeout",     "cuda"};
-    static std::string table[64];
+    static const char* const kNames[7] = {"invalid_arg", "unsupported", "invalid_index", "capacity",
+                                          "timeout",     "cuda",        "out_of_bounds"};
+    static std::string table[128];
     static std::once_flag once;
     std::call_once(once, [] {
         table[0] = "ok";
-        for (int v = 1; v < 64; ++v) {
+        for (int v = 1; v < 128; ++v) {
             std::string sname;
-            for (int b = 0; b < 6; ++b)
+            for (int b = 0; b < 7; ++b)
                 if (v & (1 << b)) {
                     if (!sname.empty()) sname += "|";
                     sname += kNames[b];
@@ -635,7 +637,7 @@ const char* ep_status_string(int32_t status) {
             table[v] = sname;
         }
     });
-    if (status < 0 || status >= 64) return "unknown";
+    if (status < 0 || status >= 128) return "unknown";
     return table[status].c_str();
 }
 

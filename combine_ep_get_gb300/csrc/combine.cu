@@ -90,18 +90,19 @@ __device__ __forceinline__ void combine_item(const CombineParams& p, int64_t it,
         const int lane = gtid;
         int64_t e_l = -1;
         float w_l = 0.0f;
-        if (kWeighted && lane < p.K) {
+        if (kWeighted && lane < p.K && EP_IN(static_cast<int64_t>(t) * p.K + lane, static_cast<int64_t>(p.T) * p.K)) {
             if (!kExpanded) e_l = p.topk_idx[static_cast<int64_t>(t) * p.K + lane];
             w_l = p.topk_weights[static_cast<int64_t>(t) * p.K + lane];
         }
         int n = 0;
         bool cap_bad = false;
         const int n_src = kExpanded ? p.K : p.R;
-        const int32_t* srow = kExpanded ? p.expanded_row + static_cast<int64_t>(t) * p.K
-                                        : p.dst_row + static_cast<int64_t>(t) * p.R;
+        const int64_t srow0 = static_cast<int64_t>(t) * n_src, n_srow = static_cast<int64_t>(p.T) * n_src;
+        const int32_t* srow = (kExpanded ? p.expanded_row : p.dst_row) + srow0;
         for (int rb = 0; rb < n_src; rb += 32) {
             const int r = rb + lane;
-            const int d = r < n_src ? srow[r] : -1;
+            const int d = (r < n_src && EP_IN(srow0 + r, n_srow)) ? srow[r] : -1;
+            (void)EP_ROW_OK(d);
             const bool ok = d >= 0 && d < p.num_y_rows;
             if (d >= p.num_y_rows) cap_bad = true;
             float coef = 1.0f;
@@ -142,6 +143,7 @@ __device__ __forceinline__ void combine_item(const CombineParams& p, int64_t it,
     const int v_begin = c * p.chunk_vecs;
     const int v_end = min(n_vec, v_begin + p.chunk_vecs);
     const int64_t row_bytes = static_cast<int64_t>(p.H) * 2;
+    const int64_t y_bytes = p.num_y_rows * row_bytes, out_bytes = static_cast<int64_t>(p.T) * row_bytes;
     for (int v = v_begin + gtid; v < v_end; v += kThreads) {
         uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};   // channel pairs (2q, 2q + 1), +0.0f each
         const int64_t off = static_cast<int64_t>(v) * 16;
@@ -149,7 +151,10 @@ __device__ __forceinline__ void combine_item(const CombineParams& p, int64_t it,
             uint4 buf[kB];
 #pragma unroll
             for (int j = 0; j < kB; ++j)
-                if (m0 + j < n) buf[j] = ld_stream_v4(p.y + static_cast<int64_t>(s_rows[m0 + j]) * row_bytes + off);
+                if (m0 + j < n) {
+                    const int64_t yo = static_cast<int64_t>(s_rows[m0 + j]) * row_bytes + off;
+                    buf[j] = EP_IN_BYTES(yo, 16, y_bytes) ? ld_stream_v4(p.y + yo) : make_uint4(0, 0, 0, 0);
+                }
 #pragma unroll
             for (int j = 0; j < kB; ++j) {
                 if (m0 + j < n) {
@@ -175,7 +180,8 @@ __device__ __forceinline__ void combine_item(const CombineParams& p, int64_t it,
             const __nv_bfloat162 h = __floats2bfloat162_rn(a.x, a.y);
             ow[q] = *reinterpret_cast<const uint32_t*>(&h);
         }
-        st_v4(p.out + static_cast<int64_t>(t) * row_bytes + off, o);
+        if (EP_IN_BYTES(static_cast<int64_t>(t) * row_bytes + off, 16, out_bytes))
+            st_v4(p.out + static_cast<int64_t>(t) * row_bytes + off, o);
     }
 }
 

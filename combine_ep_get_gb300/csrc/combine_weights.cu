@@ -22,7 +22,8 @@ __global__ void __launch_bounds__(kWeightThreads) combine_topk_weights_kernel(co
     bool cap_bad = false;
     for (int rb = 0; rb < p.R; rb += 32) {
         const int r = rb + lane;
-        const int d = r < p.R ? p.dst_row[t * p.R + r] : -1;
+        const int d = (r < p.R && EP_IN(t * p.R + r, static_cast<int64_t>(p.T) * p.R)) ? p.dst_row[t * p.R + r] : -1;
+        (void)EP_ROW_OK(d);
         const bool ok = d >= 0 && d < p.num_rows;
         if (d >= p.num_rows) cap_bad = true;
         unsigned m = __ballot_sync(0xffffffffu, ok);
@@ -30,10 +31,10 @@ __global__ void __launch_bounds__(kWeightThreads) combine_topk_weights_kernel(co
             const int sl = __ffs(m) - 1;
             m &= m - 1u;
             const int64_t dd = __shfl_sync(0xffffffffu, d, sl);
-            if (lane < p.K) acc += p.recv_topk_weights[dd * p.K + lane];
+            if (lane < p.K && EP_IN(dd * p.K + lane, p.num_rows * p.K)) acc += p.recv_topk_weights[dd * p.K + lane];
         }
     }
-    if (lane < p.K) p.combined[t * p.K + lane] = acc;
+    if (lane < p.K && EP_IN(t * p.K + lane, static_cast<int64_t>(p.T) * p.K)) p.combined[t * p.K + lane] = acc;
     if (__any_sync(0xffffffffu, cap_bad) && lane == 0) atomicOr(p.status, EP_ERR_CAPACITY);
 }
 

@@ -143,7 +143,7 @@ __device__ void cta_work(const DispatchParams& p, int lane, CtaWork& w) {
     }
     w.balanced = 1;
     w.stride = 1;
-    const int N = p.token_offset[p.T];
+    const int N = EP_IN(p.T, p.T + 1) ? p.token_offset[p.T] : 0;
     const int64_t G = gridDim.x, b = blockIdx.x;
     w.lo = static_cast<int>(b * N / G);
     w.hi = static_cast<int>((b + 1) * N / G);
@@ -164,14 +164,20 @@ __device__ void cta_work(const DispatchParams& p, int lane, CtaWork& w) {
 __device__ __forceinline__ void write_metadata(const DispatchParams& p, int t, int lane,
                                                const CtaWork& w) {
     const int K = p.K;
-    const int64_t e_l = lane < K ? p.topk_idx[static_cast<int64_t>(t) * K + lane] : -1;
-    const float w_l =
-        (lane < K && p.recv_topk_weights) ? p.topk_weights[static_cast<int64_t>(t) * K + lane] : 0.0f;
-    const int tok_off = w.balanced ? p.token_offset[t] : 0;
+    const int64_t e_l = (lane < K && EP_IN(static_cast<int64_t>(t) * K + lane, static_cast<int64_t>(p.T) * K))
+                            ? p.topk_idx[static_cast<int64_t>(t) * K + lane]
+                            : -1;
+    const float w_l = (lane < K && p.recv_topk_weights && EP_IN(static_cast<int64_t>(t) * K + lane, static_cast<int64_t>(p.T) * K))
+                          ? p.topk_weights[static_cast<int64_t>(t) * K + lane]
+                          : 0.0f;
+    const int tok_off = (w.balanced && EP_IN(t, p.T + 1)) ? p.token_offset[t] : 0;
     int m_base = 0;
     for (int rb = 0; rb < p.R; rb += 32) {
         const int r = rb + lane;
-        const int d = r < p.R ? p.dst_row[static_cast<int64_t>(t) * p.R + r] : -1;
+        const int d = (r < p.R && EP_IN(static_cast<int64_t>(t) * p.R + r, static_cast<int64_t>(p.T) * p.R))
+                          ? p.dst_row[static_cast<int64_t>(t) * p.R + r]
+                          : -1;
+        (void)EP_ROW_OK(d);
         const unsigned members = __ballot_sync(0xffffffffu, d >= 0);
         const int row_tm = tok_off + m_base + __popc(members & ((1u << lane) - 1u));
         m_base += __popc(members);
@@ -182,14 +188,14 @@ __device__ __forceinline__ void write_metadata(const DispatchParams& p, int t, i
             m &= m - 1;
             const int64_t dd = __shfl_sync(0xffffffffu, d, src);
             const int rr = rb + src;
-            if (lane < K) {
+            if (lane < K && EP_IN(dd * K + lane, p.capacity * K)) {
                 const bool on = e_l >= 0 && e_l < p.E && static_cast<int>(e_l) / p.experts_per_rank == rr;
                 if (p.recv_topk_idx)
                     p.recv_topk_idx[dd * K + lane] =
                         on ? static_cast<int32_t>(e_l) - rr * p.experts_per_rank : -1;
                 if (p.recv_topk_weights) p.recv_topk_weights[dd * K + lane] = on ? w_l : 0.0f;
             }
-            if (lane == 0 && p.recv_src_idx) p.recv_src_idx[dd] = t;
+            if (lane == 0 && p.recv_src_idx && EP_IN(dd, p.capacity)) p.recv_src_idx[dd] = t;
         }
     }
 }
@@ -230,6 +236,11 @@ __global__ void __launch_bounds__(kBf16Threads) dispatch_bf16_kernel(const Dispa
             const uint32_t bytes = min(p.chunk_bytes, row_bytes - off);
             const int slot = static_cast<int>(i % kStages);
             mbar_arrive_expect_tx(&bars[slot], bytes);
+#if EP_GET_CHECKED
+            // an out-of-range piece is not loaded; its wait then runs out
+            // (bounded) and the CTA winds down
+            if (!EP_IN_BYTES(t * row_bytes + off, bytes, static_cast<int64_t>(p.T) * row_bytes)) return;
+#endif
 #ifdef EP_TEST_DROP_FIRST_LOAD
             // failure-path test build only: CTA 0 announces its first load
             // and never issues it, so that slot's wait runs out (no copy is
@@ -253,8 +264,9 @@ __global__ void __launch_bounds__(kBf16Threads) dispatch_bf16_kernel(const Dispa
             const uint32_t bytes = min(p.chunk_bytes, row_bytes - off);
             // destination rows of the first 32 ranks and the token's first row
             // number: loaded before the wait so their latency overlaps it
-            const int d0 = lane < p.R ? p.dst_row[t * p.R + lane] : -1;
-            const int tok_off = w.balanced ? p.token_offset[t] : 0;
+            const int64_t n_tr = static_cast<int64_t>(p.T) * p.R;
+            const int d0 = (lane < p.R && EP_IN(t * p.R + lane, n_tr)) ? p.dst_row[t * p.R + lane] : -1;
+            const int tok_off = (w.balanced && EP_IN(t, p.T + 1)) ? p.token_offset[t] : 0;
             const bool landed = mbar_wait_bounded(&bars[slot], static_cast<uint32_t>((i / kStages) & 1));
             if (!__all_sync(0xffffffffu, landed)) {
                 ok = false;
@@ -264,12 +276,14 @@ __global__ void __launch_bounds__(kBf16Threads) dispatch_bf16_kernel(const Dispa
             int m_base = 0;
             for (int rb = 0; rb < p.R; rb += 32) {
                 const int r = rb + lane;
-                const int d = rb == 0 ? d0 : (r < p.R ? p.dst_row[t * p.R + r] : -1);
+                const int d = rb == 0 ? d0 : ((r < p.R && EP_IN(t * p.R + r, n_tr)) ? p.dst_row[t * p.R + r] : -1);
+                (void)EP_ROW_OK(d);
                 const unsigned members = __ballot_sync(0xffffffffu, d >= 0);
                 const int row_tm = tok_off + m_base + __popc(members & ((1u << lane) - 1u));
                 m_base += __popc(members);
                 if (d >= 0 && row_tm >= w.lo && row_tm < w.hi) {
-                    if (d < p.capacity) {
+                    if (d < p.capacity &&
+                        EP_IN_BYTES(static_cast<int64_t>(d) * row_bytes + off, bytes, p.capacity * row_bytes)) {
 #if EP_DISPATCH_EVICT_FIRST
                         bulk_store_evict_first(p.recv_x + static_cast<int64_t>(d) * row_bytes + off, src,
                                                bytes, policy);
@@ -318,10 +332,13 @@ __global__ void __launch_bounds__(kBf16Threads) dispatch_bf16_kernel(const Dispa
 // row gets the source token and the weight of that top-k slot.
 __device__ __forceinline__ void write_expanded_metadata(const DispatchParams& p, int t, int lane) {
     if (lane >= p.K) return;
-    const int d = p.expanded_row[static_cast<int64_t>(t) * p.K + lane];
+    const int64_t ek = static_cast<int64_t>(t) * p.K + lane, n_tk = static_cast<int64_t>(p.T) * p.K;
+    if (!EP_IN(ek, n_tk)) return;
+    const int d = p.expanded_row[ek];
+    (void)EP_ROW_OK(d);
     if (d < 0 || d >= p.capacity) return;
     if (p.recv_src_idx) p.recv_src_idx[d] = t;
-    if (p.recv_weight) p.recv_weight[d] = p.topk_weights[static_cast<int64_t>(t) * p.K + lane];
+    if (p.recv_weight) p.recv_weight[d] = p.topk_weights[ek];
 }
 
 // Before waiting on the previous kernel (normally the layout, which leaves
@@ -398,7 +415,10 @@ __device__ int self_route_layout(const DispatchParams& p, int t, int c, SelfRout
     int64_t e[kSelfMaxTopk];
     if (tid < p.T) {   // one thread per token: all K entries in flight at once
 #pragma unroll
-        for (int k = 0; k < kSelfMaxTopk; ++k) e[k] = k < p.K ? p.topk_idx[static_cast<int64_t>(tid) * p.K + k] : -1;
+        for (int k = 0; k < kSelfMaxTopk; ++k) {
+            const int64_t i = static_cast<int64_t>(tid) * p.K + k;
+            e[k] = (k < p.K && EP_IN(i, static_cast<int64_t>(p.T) * p.K)) ? p.topk_idx[i] : -1;
+        }
         uint32_t m = 0;
 #pragma unroll
         for (int k = 0; k < kSelfMaxTopk; ++k)
@@ -445,23 +465,24 @@ __device__ int self_route_layout(const DispatchParams& p, int t, int c, SelfRout
 
     // the token's layout rows
     if (!kLayoutCta && c == 0 && warp == 0) {
-        if (lane < p.R) {
-            p.l_dst_row[static_cast<int64_t>(t) * p.R + lane] = d;
-            p.l_is_token_in_rank[static_cast<int64_t>(t) * p.R + lane] = in ? 1 : 0;
+        const int64_t tr = static_cast<int64_t>(t) * p.R + lane;
+        if (lane < p.R && EP_IN(tr, static_cast<int64_t>(p.T) * p.R)) {
+            p.l_dst_row[tr] = d;
+            p.l_is_token_in_rank[tr] = in ? 1 : 0;
         }
         const int rows_before = static_cast<int>(__reduce_add_sync(0xffffffffu, static_cast<unsigned>(before)));
-        if (lane == 0 && p.l_token_offset) p.l_token_offset[t] = rows_before;
+        if (lane == 0 && p.l_token_offset && EP_IN(t, p.T + 1)) p.l_token_offset[t] = rows_before;
     }
     if (cta0) {
         const int n_rows = __shfl_sync(0xffffffffu, incl, 31);
         if (warp == 0) {
-            if (lane < p.R) {
+            if (lane < p.R && EP_IN(lane, p.R)) {
                 p.l_num_tokens_per_rank[lane] = total;
                 p.l_rank_offset[lane] = offset;
             }
             if (lane == 0) {
-                p.l_rank_offset[p.R] = n_rows;
-                if (p.l_token_offset) p.l_token_offset[p.T] = n_rows;
+                if (EP_IN(p.R, p.R + 1)) p.l_rank_offset[p.R] = n_rows;
+                if (p.l_token_offset && EP_IN(p.T, p.T + 1)) p.l_token_offset[p.T] = n_rows;
             }
         }
         // per-expert counts, rounded up to the alignment, scanned
@@ -469,7 +490,7 @@ __device__ int self_route_layout(const DispatchParams& p, int t, int c, SelfRout
         for (int ch = warp; ch < n_chunks; ch += blockDim.x >> 5) {
             const int ex = ch * 32 + lane;
             const int cnt = ex < p.E ? s.hist[ex] : 0;
-            if (ex < p.E) p.l_num_tokens_per_expert[ex] = cnt;
+            if (ex < p.E && EP_IN(ex, p.E)) p.l_num_tokens_per_expert[ex] = cnt;
             const int al = (cnt + p.l_alignment - 1) / p.l_alignment * p.l_alignment;
             const int ci = warp_inclusive_scan(al);
             if (ex < p.E) s.hist[ex] = ci - al;
@@ -482,7 +503,7 @@ __device__ int self_route_layout(const DispatchParams& p, int t, int c, SelfRout
                 const int src = j / p.R, r = j - src * p.R;
                 int cnt = 0;
                 for (int u = src * per_src; u < (src + 1) * per_src; ++u) cnt += (s.mask[u] >> r) & 1u;
-                p.l_src_dst_count[j] = cnt;
+                if (EP_IN(j, p.R * p.R)) p.l_src_dst_count[j] = cnt;
             }
         }
         // tokens reaching each node (ranks [n * rpn, (n + 1) * rpn))
@@ -493,7 +514,7 @@ __device__ int self_route_layout(const DispatchParams& p, int t, int c, SelfRout
                                            << (n * p.l_ranks_per_node);
                 int cnt = 0;
                 for (int u = 0; u < p.T; ++u) cnt += (s.mask[u] & node_bits) != 0u;
-                p.l_num_tokens_per_node[n] = cnt;
+                if (EP_IN(n, p.l_num_nodes)) p.l_num_tokens_per_node[n] = cnt;
             }
         }
         __syncthreads();   // CTA-uniform branch
@@ -504,10 +525,11 @@ __device__ int self_route_layout(const DispatchParams& p, int t, int c, SelfRout
             const int ib = warp_inclusive_scan(b) + __shfl_sync(0xffffffffu, ia, 31);
             if (lane < n_chunks) s.chunk[lane] = ia - a;
             if (32 + lane < n_chunks) s.chunk[32 + lane] = ib - b;
-            if (lane == 31) p.l_expert_offset[p.E] = ib;
+            if (lane == 31 && EP_IN(p.E, p.E + 1)) p.l_expert_offset[p.E] = ib;
         }
         __syncthreads();
-        for (int ex = tid; ex < p.E; ex += blockDim.x) p.l_expert_offset[ex] = s.chunk[ex >> 5] + s.hist[ex];
+        for (int ex = tid; ex < p.E; ex += blockDim.x)
+            if (EP_IN(ex, p.E + 1)) p.l_expert_offset[ex] = s.chunk[ex >> 5] + s.hist[ex];
     }
     return d;
 }
@@ -516,21 +538,21 @@ __device__ int self_route_layout(const DispatchParams& p, int t, int c, SelfRout
 // rank r's row, R <= 32); one warp.  Same entries as write_metadata.
 __device__ __forceinline__ void write_metadata_lanes(const DispatchParams& p, int t, int lane, int d) {
     const int K = p.K;
-    const int64_t e_l = lane < K ? p.topk_idx[static_cast<int64_t>(t) * K + lane] : -1;
-    const float w_l =
-        (lane < K && p.recv_topk_weights) ? p.topk_weights[static_cast<int64_t>(t) * K + lane] : 0.0f;
+    const int64_t ek = static_cast<int64_t>(t) * K + lane, n_tk = static_cast<int64_t>(p.T) * K;
+    const int64_t e_l = (lane < K && EP_IN(ek, n_tk)) ? p.topk_idx[ek] : -1;
+    const float w_l = (lane < K && p.recv_topk_weights && EP_IN(ek, n_tk)) ? p.topk_weights[ek] : 0.0f;
     unsigned m = __ballot_sync(0xffffffffu, d >= 0 && d < p.capacity);
     while (m) {
         const int rr = __ffs(m) - 1;
         m &= m - 1;
         const int64_t dd = __shfl_sync(0xffffffffu, d, rr);
-        if (lane < K) {
+        if (lane < K && EP_IN(dd * K + lane, p.capacity * K)) {
             const bool on = e_l >= 0 && e_l < p.E && static_cast<int>(e_l) / p.experts_per_rank == rr;
             if (p.recv_topk_idx)
                 p.recv_topk_idx[dd * K + lane] = on ? static_cast<int32_t>(e_l) - rr * p.experts_per_rank : -1;
             if (p.recv_topk_weights) p.recv_topk_weights[dd * K + lane] = on ? w_l : 0.0f;
         }
-        if (lane == 0 && p.recv_src_idx) p.recv_src_idx[dd] = t;
+        if (lane == 0 && p.recv_src_idx && EP_IN(dd, p.capacity)) p.recv_src_idx[dd] = t;
     }
 }
 
@@ -559,24 +581,29 @@ __device__ __forceinline__ void dispatch_regs_item(const DispatchParams& p, int6
     const uint32_t off = static_cast<uint32_t>(c) * p.chunk_bytes;
     const uint32_t bytes = min(p.chunk_bytes, row_bytes - off);
     const int nvec = static_cast<int>(bytes / 16);
-    const uint8_t* src = p.x + static_cast<int64_t>(t) * row_bytes + off;
+    const int64_t src_off = static_cast<int64_t>(t) * row_bytes + off;   // in x (T rows)
+    const int64_t x_bytes = static_cast<int64_t>(p.T) * row_bytes, rx_bytes = p.capacity * row_bytes;
+    const uint8_t* src = p.x + src_off;
     // this thread's loads and the warp's destination rows, all in flight together
     uint4 u[kRegUnroll];
 #pragma unroll
     for (int k = 0; k < kRegUnroll; ++k) {
         const int v = gtid + k * kRegThreads;
-        if (v < nvec) u[k] = ld_stream_v4(src + static_cast<size_t>(v) * 16);
+        if (v < nvec && EP_IN_BYTES(src_off + static_cast<int64_t>(v) * 16, 16, x_bytes))
+            u[k] = ld_stream_v4(src + static_cast<size_t>(v) * 16);
     }
     const int n_dst = kExpanded ? p.K : p.R;
-    const int32_t* drow = kExpanded ? p.expanded_row + static_cast<int64_t>(t) * p.K
-                                    : p.dst_row + static_cast<int64_t>(t) * p.R;
+    const int64_t drow0 = static_cast<int64_t>(t) * n_dst, n_drow = static_cast<int64_t>(p.T) * n_dst;
+    const int32_t* drow = (kExpanded ? p.expanded_row : p.dst_row) + drow0;
     int d0, d1;
     if constexpr (kSelf) {
         d0 = self_route_layout<false>(p, t, c, self_smem());   // R <= 32
         d1 = -1;
     } else {
-        d0 = lane < n_dst ? drow[lane] : -1;
-        d1 = 32 + lane < n_dst ? drow[32 + lane] : -1;   // ranks 32..63, same latency
+        d0 = (lane < n_dst && EP_IN(drow0 + lane, n_drow)) ? drow[lane] : -1;
+        d1 = (32 + lane < n_dst && EP_IN(drow0 + 32 + lane, n_drow)) ? drow[32 + lane] : -1;   // ranks 32..63
+        (void)EP_ROW_OK(d0);
+        (void)EP_ROW_OK(d1);
     }
     if (warp_g == 1 && c == 0) {
         if (kExpanded) {
@@ -599,21 +626,26 @@ __device__ __forceinline__ void dispatch_regs_item(const DispatchParams& p, int6
 #pragma unroll
             for (int k = 0; k < kRegUnroll; ++k) {
                 const int v = base + gtid + k * kRegThreads;
-                if (v < nvec) u[k] = ld_stream_v4(src + static_cast<size_t>(v) * 16);
+                if (v < nvec && EP_IN_BYTES(src_off + static_cast<int64_t>(v) * 16, 16, x_bytes))
+                    u[k] = ld_stream_v4(src + static_cast<size_t>(v) * 16);
             }
         }
         for (int rb = 0; rb < n_dst; rb += 32) {
-            const int d = rb == 0 ? d0 : rb == 32 ? d1 : (rb + lane < n_dst ? drow[rb + lane] : -1);
+            const int d = rb == 0    ? d0
+                          : rb == 32 ? d1
+                                     : ((rb + lane < n_dst && EP_IN(drow0 + rb + lane, n_drow)) ? drow[rb + lane] : -1);
+            if (rb >= 64) (void)EP_ROW_OK(d);
             if (d >= p.capacity && c == 0) cap_bad = true;
             unsigned m = __ballot_sync(0xffffffffu, d >= 0 && d < p.capacity);
             while (m) {
                 const int sl = __ffs(m) - 1;
                 m &= m - 1;
-                uint8_t* dst = p.recv_x + static_cast<int64_t>(__shfl_sync(0xffffffffu, d, sl)) * row_bytes + off;
+                const int64_t dst_off = static_cast<int64_t>(__shfl_sync(0xffffffffu, d, sl)) * row_bytes + off;
+                uint8_t* dst = p.recv_x + dst_off;
 #pragma unroll
                 for (int k = 0; k < kRegUnroll; ++k) {
                     const int v = base + gtid + k * kRegThreads;
-                    if (v < nvec) {
+                    if (v < nvec && EP_IN_BYTES(dst_off + static_cast<int64_t>(v) * 16, 16, rx_bytes)) {
 #if EP_DISPATCH_STORE_CS
                         st_cs_v4(dst + static_cast<size_t>(v) * 16, u[k]);
 #else
@@ -702,26 +734,34 @@ __device__ __forceinline__ void dispatch_fp8_item(const DispatchParams& p, int64
     const int nb = p.H / 128;
     const int b_begin = c * p.chunk_blocks;
     const int b_end = min(nb, b_begin + p.chunk_blocks);
-    const uint8_t* xrow = p.x + static_cast<int64_t>(t) * p.H * 2;
+    const int64_t xrow_off = static_cast<int64_t>(t) * p.H * 2, x_bytes = static_cast<int64_t>(p.T) * p.H * 2;
+    const uint8_t* xrow = p.x + xrow_off;
     uint4 v[kFp8Rounds][kVec];
 #pragma unroll
     for (int q = 0; q < kFp8Rounds; ++q) {
         const int b = b_begin + q * blocks_per_round + kBlocksPerWarp * warp_g + grp;
-        const uint8_t* src = xrow + static_cast<size_t>(b) * 256 + sub * (16 * kVec);
+        const int64_t so = static_cast<int64_t>(b) * 256 + sub * (16 * kVec);
+        const uint8_t* src = xrow + so;
 #pragma unroll
-        for (int u = 0; u < kVec; ++u) v[q][u] = b < b_end ? ld_stream_v4(src + 16 * u) : make_uint4(0, 0, 0, 0);
+        for (int u = 0; u < kVec; ++u)
+            v[q][u] = (b < b_end && EP_IN_BYTES(xrow_off + so + 16 * u, 16, x_bytes)) ? ld_stream_v4(src + 16 * u)
+                                                                                      : make_uint4(0, 0, 0, 0);
     }
     const int n_dst = kExpanded ? p.K : p.R;
-    const int32_t* drow = kExpanded ? p.expanded_row + static_cast<int64_t>(t) * p.K
-                                    : p.dst_row + static_cast<int64_t>(t) * p.R;
+    const int64_t drow0 = static_cast<int64_t>(t) * n_dst, n_drow = static_cast<int64_t>(p.T) * n_dst;
+    const int32_t* drow = (kExpanded ? p.expanded_row : p.dst_row) + drow0;
     int d0, d1;
     if constexpr (kSelf) {
         d0 = self_route_layout<false>(p, t, c, self_smem());   // R <= 32
         d1 = -1;
     } else {
-        d0 = lane < n_dst ? drow[lane] : -1;
-        d1 = 32 + lane < n_dst ? drow[32 + lane] : -1;   // ranks 32..63, same latency
+        d0 = (lane < n_dst && EP_IN(drow0 + lane, n_drow)) ? drow[lane] : -1;
+        d1 = (32 + lane < n_dst && EP_IN(drow0 + 32 + lane, n_drow)) ? drow[32 + lane] : -1;   // ranks 32..63
+        (void)EP_ROW_OK(d0);
+        (void)EP_ROW_OK(d1);
     }
+    const int64_t rx_bytes = p.capacity * p.H;   // FP8 codes: one byte per channel
+    const int64_t sf_n = p.sf_col_major ? static_cast<int64_t>(nb) * p.sf_stride : p.capacity * nb;
     if (warp_g == 1 && c == 0) {
         if (kExpanded) {
             write_expanded_metadata(p, t, lane);
@@ -792,7 +832,10 @@ __device__ __forceinline__ void dispatch_fp8_item(const DispatchParams& p, int64
     // stores rounds [q_lo, q_hi) to every destination
     auto store_rounds = [&](int q_lo, int q_hi) {
         for (int rb = 0; rb < n_dst; rb += 32) {
-            const int d = rb == 0 ? d0 : rb == 32 ? d1 : (rb + lane < n_dst ? drow[rb + lane] : -1);
+            const int d = rb == 0    ? d0
+                          : rb == 32 ? d1
+                                     : ((rb + lane < n_dst && EP_IN(drow0 + rb + lane, n_drow)) ? drow[rb + lane] : -1);
+            if (rb >= 64) (void)EP_ROW_OK(d);
             if (d >= p.capacity && c == 0 && q_lo == 0) cap_bad = true;
             unsigned m = __ballot_sync(0xffffffffu, d >= 0 && d < p.capacity);
             while (m) {
@@ -803,7 +846,8 @@ __device__ __forceinline__ void dispatch_fp8_item(const DispatchParams& p, int64
 #pragma unroll
                 for (int q = 0; q < kFp8Rounds; ++q) {
                     const int b = b0 + q * blocks_per_round;
-                    if (q >= q_lo && q < q_hi && b < b_end) {
+                    if (q >= q_lo && q < q_hi && b < b_end &&
+                        EP_IN_BYTES(dd * p.H + sub_col + static_cast<int64_t>(b) * 128, 8 * kVec, rx_bytes)) {
                         uint8_t* dst = row + static_cast<int64_t>(b) * 128;
                         if (kVec == 2)
                             st_v4(dst, make_uint4(code[q][0], code[q][1], code[q][2 % (2 * kVec)],
@@ -813,7 +857,7 @@ __device__ __forceinline__ void dispatch_fp8_item(const DispatchParams& p, int64
                         if (sub == 0 && p.recv_sf) {
                             const int64_t si =
                                 p.sf_col_major ? static_cast<int64_t>(b) * p.sf_stride + dd : dd * nb + b;
-                            p.recv_sf[si] = sfq[q];
+                            if (EP_IN(si, sf_n)) p.recv_sf[si] = sfq[q];
                         }
                     }
                 }
@@ -845,7 +889,10 @@ __device__ __forceinline__ void dispatch_fp8_item(const DispatchParams& p, int64
         const uint4 c1 = make_uint4(code[1][0], code[1][1], code[1][2], code[1][3]);
         const float s0 = sfq[0], s1 = sfq[1];
         for (int rb = 0; rb < n_dst; rb += 32) {
-            const int d = rb == 0 ? d0 : rb == 32 ? d1 : (rb + lane < n_dst ? drow[rb + lane] : -1);
+            const int d = rb == 0    ? d0
+                          : rb == 32 ? d1
+                                     : ((rb + lane < n_dst && EP_IN(drow0 + rb + lane, n_drow)) ? drow[rb + lane] : -1);
+            if (rb >= 64) (void)EP_ROW_OK(d);
             if (d >= cap && c == 0) cap_bad = true;
             unsigned m = __ballot_sync(0xffffffffu, d >= 0 && d < cap);
             while (m) {
@@ -853,12 +900,12 @@ __device__ __forceinline__ void dispatch_fp8_item(const DispatchParams& p, int64
                 m &= m - 1;
                 const int64_t dd = __shfl_sync(0xffffffffu, d, sl);
                 uint8_t* row = rx + dd * H;
-                if (ok0) *reinterpret_cast<uint4*>(row + co0) = c0;
-                if (ok1) *reinterpret_cast<uint4*>(row + co1) = c1;
+                if (ok0 && EP_IN_BYTES(dd * H + co0, 16, rx_bytes)) *reinterpret_cast<uint4*>(row + co0) = c0;
+                if (ok1 && EP_IN_BYTES(dd * H + co1, 16, rx_bytes)) *reinterpret_cast<uint4*>(row + co1) = c1;
                 if (sf_lane) {
                     float* srow = rsf + dd * sfs;
-                    if (ok0) srow[so0] = s0;
-                    if (ok1) srow[so1] = s1;
+                    if (ok0 && EP_IN(dd * sfs + so0, sf_n)) srow[so0] = s0;
+                    if (ok1 && EP_IN(dd * sfs + so1, sf_n)) srow[so1] = s1;
                 }
             }
         }

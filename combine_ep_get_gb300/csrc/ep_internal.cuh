@@ -201,6 +201,34 @@ LayoutWorkspace layout_workspace(int T, int E, int R, int num_nodes);
 // Device helpers
 // ---------------------------------------------------------------------------
 
+// Bounds-checked build (compiled with -DEP_GET_CHECKED=1; a test-only copy of
+// the library, never the product): in_bounds(i, n, status) is true when
+// 0 <= i < n; otherwise it ORs EP_ERR_OUT_OF_BOUNDS into *status and is
+// false, and the caller skips the access.  The product build compiles it to
+// the constant true, so its code is unchanged.
+#ifndef EP_GET_CHECKED
+#define EP_GET_CHECKED 0
+#endif
+__device__ __forceinline__ bool in_bounds(int64_t i, int64_t n, int32_t* status) {
+#if EP_GET_CHECKED
+    if (i >= 0 && i < n) return true;
+    atomicOr(status, EP_ERR_OUT_OF_BOUNDS);
+    return false;
+#else
+    (void)i;
+    (void)n;
+    (void)status;
+    return true;
+#endif
+}
+// Element i of an array of n, and a byte range [off, off + len) of an
+// array of n bytes, against the kernel's parameter block `p` (its status).
+#define EP_IN(i, n) ::epg::in_bounds(static_cast<int64_t>(i), static_cast<int64_t>(n), p.status)
+#define EP_IN_BYTES(off, len, n) \
+    ::epg::in_bounds(static_cast<int64_t>(off), static_cast<int64_t>(n) - static_cast<int64_t>(len) + 1, p.status)
+// A row index read from dst_row / expanded_row / node_row: -1 (absent) or >= 0.
+#define EP_ROW_OK(d) ((d) >= -1 || ::epg::in_bounds(-1, 0, p.status))
+
 // A bounded wait gives up after this many nanoseconds of %globaltimer (the
 // failure-path test builds a copy of the library with a shorter limit).
 #ifndef EP_WAIT_TIMEOUT_NS

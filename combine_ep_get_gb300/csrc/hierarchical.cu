@@ -33,12 +33,18 @@ constexpr int kRedBatch = 4;
 // Metadata of token t's rows in ranks [r0, r1) (one warp, lane k < K).
 __device__ __forceinline__ void forward_metadata(const HierParams& p, int t, int r0, int r1, int lane) {
     const int K = p.K;
-    const int64_t e_l = lane < K ? p.topk_idx[static_cast<int64_t>(t) * K + lane] : -1;
-    const float w_l = (lane < K && p.recv_topk_weights) ? p.topk_weights[static_cast<int64_t>(t) * K + lane] : 0.0f;
+    const int64_t e_l = (lane < K && EP_IN(static_cast<int64_t>(t) * K + lane, static_cast<int64_t>(p.T) * K))
+                            ? p.topk_idx[static_cast<int64_t>(t) * K + lane]
+                            : -1;
+    const float w_l = (lane < K && p.recv_topk_weights && EP_IN(static_cast<int64_t>(t) * K + lane, static_cast<int64_t>(p.T) * K))
+                          ? p.topk_weights[static_cast<int64_t>(t) * K + lane]
+                          : 0.0f;
     for (int r = r0; r < r1; ++r) {
-        const int d = p.dst_row[static_cast<int64_t>(t) * p.R + r];   // uniform over the warp
+        const int64_t dr = static_cast<int64_t>(t) * p.R + r;
+        const int d = EP_IN(dr, static_cast<int64_t>(p.T) * p.R) ? p.dst_row[dr] : -1;   // uniform over the warp
+        (void)EP_ROW_OK(d);
         if (d < 0 || d >= p.capacity) continue;
-        if (lane < K) {
+        if (lane < K && EP_IN(static_cast<int64_t>(d) * K + lane, p.capacity * K)) {
             const bool on = e_l >= 0 && e_l < p.E && static_cast<int>(e_l) / p.experts_per_rank == r;
             if (p.recv_topk_idx)
                 p.recv_topk_idx[static_cast<int64_t>(d) * K + lane] =
@@ -63,8 +69,12 @@ __global__ void __launch_bounds__(kFwdThreads, 6) forward_scaleup_kernel(const H
     const int nb = p.H / 128;
     const int rpn = p.ranks_per_node;
     bool cap_bad = false;
+    const int64_t row_in = static_cast<int64_t>(p.node_capacity) * row_bytes;
+    const int64_t row_out = p.capacity * row_bytes;
     for (int n = 0; n < p.num_nodes; ++n) {
-        const int j = p.node_row[static_cast<int64_t>(t) * p.num_nodes + n];   // uniform over the CTA
+        const int64_t nr = static_cast<int64_t>(t) * p.num_nodes + n;
+        const int j = EP_IN(nr, static_cast<int64_t>(p.T) * p.num_nodes) ? p.node_row[nr] : -1;   // uniform over the CTA
+        (void)EP_ROW_OK(j);
         if (j < 0) continue;
         if (j >= p.node_capacity) {
             cap_bad = true;
@@ -73,38 +83,48 @@ __global__ void __launch_bounds__(kFwdThreads, 6) forward_scaleup_kernel(const H
         const int r0 = n * rpn;
         if (c == 0 && warp == 1) forward_metadata(p, t, r0, r0 + rpn, lane);
         if (kFp8 && c == 0 && warp == 2 && p.recv_sf) {
+            const int64_t sf_n = p.sf_col_major ? static_cast<int64_t>(nb) * p.sf_stride : p.capacity * nb;
             for (int r = r0; r < r0 + rpn; ++r) {
-                const int d = p.dst_row[static_cast<int64_t>(t) * p.R + r];
+                const int64_t dr = static_cast<int64_t>(t) * p.R + r;
+                const int d = EP_IN(dr, static_cast<int64_t>(p.T) * p.R) ? p.dst_row[dr] : -1;
                 if (d < 0 || d >= p.capacity) continue;
                 for (int b = lane; b < nb; b += 32) {
+                    if (!EP_IN(static_cast<int64_t>(j) * nb + b, static_cast<int64_t>(p.node_capacity) * nb)) continue;
                     const float s = p.node_sf[static_cast<int64_t>(j) * nb + b];
                     const int64_t si = p.sf_col_major ? static_cast<int64_t>(b) * p.sf_stride + d
                                                       : static_cast<int64_t>(d) * nb + b;
-                    p.recv_sf[si] = s;
+                    if (EP_IN(si, sf_n)) p.recv_sf[si] = s;
                 }
             }
         }
-        const uint8_t* src = p.node_x + static_cast<int64_t>(j) * row_bytes + off;
-        const int32_t* drow = p.dst_row + static_cast<int64_t>(t) * p.R + r0;
+        const int64_t src_off = static_cast<int64_t>(j) * row_bytes + off;
+        const uint8_t* src = p.node_x + src_off;
+        const int64_t drow0 = static_cast<int64_t>(t) * p.R + r0;
+        const int32_t* drow = p.dst_row + drow0;
         for (int base = 0; base < nvec; base += kFwdUnroll * kFwdThreads) {
             uint4 u[kFwdUnroll];
 #pragma unroll
             for (int k = 0; k < kFwdUnroll; ++k) {
                 const int v = base + gtid + k * kFwdThreads;
-                if (v < nvec) u[k] = ld_stream_v4(src + static_cast<size_t>(v) * 16);
+                if (v < nvec && EP_IN_BYTES(src_off + static_cast<int64_t>(v) * 16, 16, row_in))
+                    u[k] = ld_stream_v4(src + static_cast<size_t>(v) * 16);
             }
             for (int rb = 0; rb < rpn; rb += 32) {
-                const int d = rb + lane < rpn ? drow[rb + lane] : -1;
+                const int d = (rb + lane < rpn && EP_IN(drow0 + rb + lane, static_cast<int64_t>(p.T) * p.R))
+                                  ? drow[rb + lane] : -1;
+                (void)EP_ROW_OK(d);
                 if (d >= p.capacity && c == 0 && base == 0) cap_bad = true;
                 unsigned m = __ballot_sync(0xffffffffu, d >= 0 && d < p.capacity);
                 while (m) {
                     const int sl = __ffs(m) - 1;
                     m &= m - 1;
-                    uint8_t* dst = p.recv_x + static_cast<int64_t>(__shfl_sync(0xffffffffu, d, sl)) * row_bytes + off;
+                    const int64_t dst_off = static_cast<int64_t>(__shfl_sync(0xffffffffu, d, sl)) * row_bytes + off;
+                    uint8_t* dst = p.recv_x + dst_off;
 #pragma unroll
                     for (int k = 0; k < kFwdUnroll; ++k) {
                         const int v = base + gtid + k * kFwdThreads;
-                        if (v < nvec) st_v4(dst + static_cast<size_t>(v) * 16, u[k]);
+                        if (v < nvec && EP_IN_BYTES(dst_off + static_cast<int64_t>(v) * 16, 16, row_out))
+                            st_v4(dst + static_cast<size_t>(v) * 16, u[k]);
                     }
                 }
             }
@@ -131,23 +151,27 @@ __global__ void __launch_bounds__(kRedThreads, 12) reduce_scaleup_kernel(const H
         const int lane = gtid;
         int64_t e_l = -1;
         float w_l = 0.0f;
-        if (kWeighted && lane < p.K) {
+        if (kWeighted && lane < p.K && EP_IN(static_cast<int64_t>(t) * p.K + lane, static_cast<int64_t>(p.T) * p.K)) {
             e_l = p.topk_idx[static_cast<int64_t>(t) * p.K + lane];
             w_l = p.topk_weights[static_cast<int64_t>(t) * p.K + lane];
         }
         const int32_t* nrow = p.node_row + static_cast<int64_t>(t) * p.num_nodes;
-        const int j_lane = lane < p.num_nodes ? nrow[lane] : -1;   // nodes 0..31, with the rank rows
+        const int j_lane = (lane < p.num_nodes && EP_IN(static_cast<int64_t>(t) * p.num_nodes + lane,
+                                                        static_cast<int64_t>(p.T) * p.num_nodes))
+                               ? nrow[lane]
+                               : -1;   // nodes 0..31, with the rank rows
         const int32_t* srow = p.dst_row + static_cast<int64_t>(t) * p.R;
         int n = 0;
         bool cap_bad = false;
         for (int rb = 0; rb < p.R; rb += 32) {
             const int r = rb + lane;
-            const int d = r < p.R ? srow[r] : -1;
+            const int d = (r < p.R && EP_IN(static_cast<int64_t>(t) * p.R + r, static_cast<int64_t>(p.T) * p.R)) ? srow[r] : -1;
+            (void)EP_ROW_OK(d);
             const int nd = r / rpn;
             int j = -1;
             if (nd < 32) {
                 j = __shfl_sync(0xffffffffu, j_lane, nd & 31);
-            } else if (d >= 0) {
+            } else if (d >= 0 && EP_IN(static_cast<int64_t>(t) * p.num_nodes + nd, static_cast<int64_t>(p.T) * p.num_nodes)) {
                 j = nrow[nd];
             }
             // a row beyond num_y_rows stays in the list as a null entry (never
@@ -202,7 +226,9 @@ __global__ void __launch_bounds__(kRedThreads, 12) reduce_scaleup_kernel(const H
 #pragma unroll
             for (int i = 0; i < kRedBatch; ++i) {
                 const int d = m0 + i < n ? s_rows[m0 + i] : -1;
-                buf[i] = d >= 0 ? ld_stream_v4(p.y + static_cast<int64_t>(d) * row_bytes + voff) : make_uint4(0, 0, 0, 0);
+                buf[i] = (d >= 0 && EP_IN_BYTES(static_cast<int64_t>(d) * row_bytes + voff, 16, p.num_y_rows * row_bytes))
+                             ? ld_stream_v4(p.y + static_cast<int64_t>(d) * row_bytes + voff)
+                             : make_uint4(0, 0, 0, 0);
             }
 #pragma unroll
             for (int i = 0; i < kRedBatch; ++i) {
@@ -233,7 +259,8 @@ __global__ void __launch_bounds__(kRedThreads, 12) reduce_scaleup_kernel(const H
                             acc[2 * q] = 0.0f;
                             acc[2 * q + 1] = 0.0f;
                         }
-                        st_v4(p.node_y + static_cast<int64_t>(j) * row_bytes + voff, o);
+                        if (EP_IN_BYTES(static_cast<int64_t>(j) * row_bytes + voff, 16, p.node_capacity * row_bytes))
+                            st_v4(p.node_y + static_cast<int64_t>(j) * row_bytes + voff, o);
                     }
                 }
             }

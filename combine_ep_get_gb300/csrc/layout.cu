@@ -81,7 +81,7 @@ __global__ void __launch_bounds__(kThreads) layout_count_kernel(const LayoutPara
     if (p.src_dst_count) {
         const int nn = R * R;
         for (int i = blockIdx.x * kThreads + threadIdx.x; i < nn; i += gridDim.x * kThreads)
-            p.src_dst_count[i] = 0;
+            if (EP_IN(i, nn)) p.src_dst_count[i] = 0;
     }
     if (tile >= p.num_tiles) return;
 
@@ -99,7 +99,8 @@ __global__ void __launch_bounds__(kThreads) layout_count_kernel(const LayoutPara
 #pragma unroll
         for (int u = 0; u < kUnroll; ++u) {
             const int i = base + u * kThreads + threadIdx.x;
-            e[u] = i < n_entries ? src[i] : -1;     // all loads in flight before any use
+            e[u] = (i < n_entries && EP_IN(static_cast<int64_t>(t0) * p.K + i, static_cast<int64_t>(p.T) * p.K))
+                       ? src[i] : -1;     // all loads in flight before any use
         }
 #pragma unroll
         for (int u = 0; u < kUnroll; ++u) {
@@ -117,21 +118,28 @@ __global__ void __launch_bounds__(kThreads) layout_count_kernel(const LayoutPara
     if (bad) s_bad = 1;
     __syncthreads();
 
-    uint32_t* g_bm = p.ws_bitmap + static_cast<size_t>(tile) * R * kTileWords;
-    for (int i = threadIdx.x; i < R * kTileWords; i += kThreads) g_bm[i] = s_bm[i];
+    const int64_t bm0 = static_cast<int64_t>(tile) * R * kTileWords;
+    const int64_t n_bm = static_cast<int64_t>(p.num_tiles) * R * kTileWords;
+    uint32_t* g_bm = p.ws_bitmap + bm0;
+    for (int i = threadIdx.x; i < R * kTileWords; i += kThreads)
+        if (EP_IN(bm0 + i, n_bm)) g_bm[i] = s_bm[i];
     for (int r = threadIdx.x; r < R; r += kThreads) {
         int c = 0;
 #pragma unroll
         for (int w = 0; w < kTileWords; ++w) c += __popc(s_bm[w * R + r]);
-        p.ws_rank[static_cast<size_t>(r) * p.num_tiles + tile] = c;
+        const int64_t wi = static_cast<int64_t>(r) * p.num_tiles + tile;
+        if (EP_IN(wi, static_cast<int64_t>(R) * p.num_tiles)) p.ws_rank[wi] = c;
     }
-    for (int e = threadIdx.x; e < p.E; e += kThreads)
-        p.ws_expert[static_cast<size_t>(e) * p.num_tiles + tile] = s_hist[e];
+    for (int e = threadIdx.x; e < p.E; e += kThreads) {
+        const int64_t wi = static_cast<int64_t>(e) * p.num_tiles + tile;
+        if (EP_IN(wi, static_cast<int64_t>(p.E) * p.num_tiles)) p.ws_expert[wi] = s_hist[e];
+    }
     for (int n = threadIdx.x; n < p.num_nodes; n += kThreads) {
         int c = 0;
 #pragma unroll
         for (int w = 0; w < kTileWords; ++w) c += __popc(s_bm_node[w * p.num_nodes + n]);
-        p.ws_node[static_cast<size_t>(n) * p.num_tiles + tile] = c;
+        const int64_t wi = static_cast<int64_t>(n) * p.num_tiles + tile;
+        if (EP_IN(wi, static_cast<int64_t>(p.num_nodes) * p.num_tiles)) p.ws_node[wi] = c;
     }
     if (threadIdx.x == 0 && s_bad) atomicOr(p.status, EP_ERR_INVALID_INDEX);
 }
@@ -146,6 +154,8 @@ __global__ void __launch_bounds__(kThreads) layout_scan_kernel(const LayoutParam
     int32_t* row;
     int32_t* total;
     bool scan = false;
+    // the column's workspace row and total stay inside their arrays
+    if (!EP_IN(col, n_cols)) return;
     if (col < p.R) {
         row = p.ws_rank + static_cast<size_t>(col) * p.num_tiles;
         total = p.num_tokens_per_rank + col;
@@ -278,7 +288,8 @@ constexpr int kRankWarps = 8;
 // Rank warps of the tiled path: 4 above 1024 experts, so that its counters and
 // key groups (2 x warps x E ints) fit beside the staged entries.
 __host__ __device__ inline int tiled_rank_warps(int E) { return E > 1024 ? kRankWarps / 2 : kRankWarps; }
-__device__ void rank_entries(int* s_key, int n_ent, int E, const int* s_eb, int* s_wc, int32_t* out, int nw) {
+__device__ void rank_entries(int* s_key, int n_ent, int E, const int* s_eb, int* s_wc, int32_t* out, int nw,
+                             int64_t out_n, int32_t* status) {
     uint32_t* s_kb = reinterpret_cast<uint32_t*>(s_wc + nw * E);
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int chunks = (n_ent + 31) / 32;
@@ -312,7 +323,7 @@ __device__ void rank_entries(int* s_key, int n_ent, int E, const int* s_eb, int*
         __syncwarp();
         if (rec >= 0 && (rec & 31) == 0) s_wc[warp * E + key] += (rec >> 5) & 63;
         __syncwarp();
-        if (i < n_ent) out[i] = pos;
+        if (i < n_ent && ::epg::in_bounds(i, out_n, status)) out[i] = pos;
     }
 }
 
@@ -335,7 +346,8 @@ __device__ void expanded_rows_of_tile(const LayoutParams& p, int t0, int nt, con
 #pragma unroll
         for (int u = 0; u < kStageUnroll; ++u) {   // the first batch was loaded at kernel entry
             const int i = base + u * kThreads + threadIdx.x;
-            e[u] = base == 0 ? key0[u] : (i < n_ent ? src[i] : -1);
+            e[u] = base == 0 ? key0[u]
+                             : ((i < n_ent && EP_IN(static_cast<int64_t>(t0) * p.K + i, static_cast<int64_t>(p.T) * p.K)) ? src[i] : -1);
         }
 #pragma unroll
         for (int u = 0; u < kStageUnroll; ++u) {
@@ -348,7 +360,8 @@ __device__ void expanded_rows_of_tile(const LayoutParams& p, int t0, int nt, con
         s_kb[i] = 0u;
     }
     __syncthreads();
-    rank_entries(s_key, n_ent, E, s_eb, s_wc, p.expanded_row + static_cast<int64_t>(t0) * p.K, nw);
+    rank_entries(s_key, n_ent, E, s_eb, s_wc, p.expanded_row + static_cast<int64_t>(t0) * p.K, nw,
+                 static_cast<int64_t>(p.T - t0) * p.K, p.status);
 }
 
 // Node rows of one tile: a token is in node n when any rank of n holds it,
@@ -385,6 +398,7 @@ __device__ void node_rows_of_tile(const LayoutParams& p, int t0, int nt, const u
         const int w = tl >> 5;
         const uint32_t word = s_nbm[w * NN + n];
         const uint32_t b = static_cast<uint32_t>(tl & 31);
+        if (!EP_IN(static_cast<int64_t>(t0) * NN + j, static_cast<int64_t>(p.T) * NN)) continue;
         out[j] = ((word >> b) & 1u) ? s_nbase[n] + s_nwpre[w * NN + n] + __popc(word & ((1u << b) - 1u)) : -1;
     }
     __syncthreads();
@@ -437,7 +451,8 @@ __global__ void __launch_bounds__(kThreads) layout_rows_kernel(const LayoutParam
 #pragma unroll
         for (int u = 0; u < kStageUnroll; ++u) {
             const int i = u * kThreads + static_cast<int>(threadIdx.x);
-            key0[u] = (expanded && i < n_ent) ? src[i] : -1;
+            key0[u] = (expanded && i < n_ent && EP_IN(static_cast<int64_t>(t0) * p.K + i, static_cast<int64_t>(p.T) * p.K))
+                          ? src[i] : -1;
         }
     }
     if (has_tile) {
@@ -447,7 +462,9 @@ __global__ void __launch_bounds__(kThreads) layout_rows_kernel(const LayoutParam
 #pragma unroll
             for (int u = 0; u < kStageUnroll; ++u) {   // all loads in flight before any use
                 const int i = base + u * kThreads + threadIdx.x;
-                v[u] = i < R * kTileWords ? g_bm[i] : 0u;
+                v[u] = (i < R * kTileWords && EP_IN(static_cast<int64_t>(tile) * R * kTileWords + i,
+                                                    static_cast<int64_t>(p.num_tiles) * R * kTileWords))
+                           ? g_bm[i] : 0u;
             }
 #pragma unroll
             for (int u = 0; u < kStageUnroll; ++u) {
@@ -465,11 +482,11 @@ __global__ void __launch_bounds__(kThreads) layout_rows_kernel(const LayoutParam
         for (int j = 0; j < kMaxRankSlice; ++j) {
             const int i = static_cast<int>(threadIdx.x) * per_r + j;
             if (j < per_r && i < R) {
-                if (tile == 0) p.rank_offset[i] = pre[j];
+                if (tile == 0 && EP_IN(i, R + 1)) p.rank_offset[i] = pre[j];
                 s_base[i] = pre[j] + v_wsr[j];
             }
         }
-        if (tile == 0 && threadIdx.x == 0) p.rank_offset[R] = n_recv;
+        if (tile == 0 && threadIdx.x == 0 && EP_IN(R, R + 1)) p.rank_offset[R] = n_recv;
     }
     // expert offsets (aligned counts): block 0 writes them; the expanded
     // ranking starts each expert at its offset plus this tile's prefix
@@ -483,11 +500,11 @@ __global__ void __launch_bounds__(kThreads) layout_rows_kernel(const LayoutParam
         for (int j = 0; j < kMaxExpertSlice; ++j) {
             const int i = static_cast<int>(threadIdx.x) * per_e + j;
             if (j < per_e && i < E) {
-                if (tile == 0) p.expert_offset[i] = pre[j];
+                if (tile == 0 && EP_IN(i, E + 1)) p.expert_offset[i] = pre[j];
                 if (expanded) s_eb[i] = pre[j] + v_wse[j];
             }
         }
-        if (tile == 0 && threadIdx.x == 0) p.expert_offset[E] = n_exp;
+        if (tile == 0 && threadIdx.x == 0 && EP_IN(E, E + 1)) p.expert_offset[E] = n_exp;
     }
     // node offsets and this tile's base per node
     if (want_n) {
@@ -497,11 +514,11 @@ __global__ void __launch_bounds__(kThreads) layout_rows_kernel(const LayoutParam
         for (int j = 0; j < kMaxRankSlice; ++j) {
             const int i = static_cast<int>(threadIdx.x) * per_n + j;
             if (j < per_n && i < NN) {
-                if (tile == 0) p.node_offset[i] = pre[j];
+                if (tile == 0 && EP_IN(i, NN + 1)) p.node_offset[i] = pre[j];
                 s_nbase[i] = pre[j] + v_wsn[j];
             }
         }
-        if (tile == 0 && threadIdx.x == 0) p.node_offset[NN] = n_node;
+        if (tile == 0 && threadIdx.x == 0 && EP_IN(NN, NN + 1)) p.node_offset[NN] = n_node;
     }
     if (!has_tile) {
         if (p.token_offset && p.num_tiles == 0 && threadIdx.x == 0) p.token_offset[0] = 0;
@@ -547,10 +564,13 @@ __global__ void __launch_bounds__(kThreads) layout_rows_kernel(const LayoutParam
             }
         }
         if (j0 + 4 <= n_el) {
-            *reinterpret_cast<int4*>(drow + j0) = make_int4(v[0], v[1], v[2], v[3]);
-            *reinterpret_cast<uint32_t*>(inr + j0) = in4;
+            if (EP_IN(static_cast<int64_t>(t0) * R + j0 + 3, static_cast<int64_t>(p.T) * R)) {
+                *reinterpret_cast<int4*>(drow + j0) = make_int4(v[0], v[1], v[2], v[3]);
+                *reinterpret_cast<uint32_t*>(inr + j0) = in4;
+            }
         } else {
             for (int u = 0; u < 4 && j0 + u < n_el; ++u) {
+                if (!EP_IN(static_cast<int64_t>(t0) * R + j0 + u, static_cast<int64_t>(p.T) * R)) continue;
                 drow[j0 + u] = v[u];
                 inr[j0 + u] = static_cast<uint8_t>((in4 >> (8 * u)) & 1u);
             }
@@ -564,7 +584,8 @@ __global__ void __launch_bounds__(kThreads) layout_rows_kernel(const LayoutParam
         __shared__ int s_ntok[kTileTokens];
         int before = 0;
         for (int r = threadIdx.x; r < R; r += kThreads)
-            before += p.ws_rank[static_cast<size_t>(r) * p.num_tiles + tile];
+            if (EP_IN(static_cast<int64_t>(r) * p.num_tiles + tile, static_cast<int64_t>(R) * p.num_tiles))
+                before += p.ws_rank[static_cast<size_t>(r) * p.num_tiles + tile];
         const int tile_base = block_sum(before, s_red);
         if (threadIdx.x < nt) {
             const int w = threadIdx.x >> 5;
@@ -579,7 +600,7 @@ __global__ void __launch_bounds__(kThreads) layout_rows_kernel(const LayoutParam
         block_exclusive_scan(
             nt, [&](int i) { return s_ntok[i]; },
             [&](int i, int v) {
-                if (i < nt || last) to[i] = tile_base + v;
+                if ((i < nt || last) && EP_IN(t0 + i, p.T + 1)) to[i] = tile_base + v;
             },
             s_warp);
     }
@@ -603,7 +624,7 @@ __global__ void __launch_bounds__(kThreads) layout_rows_kernel(const LayoutParam
                 const uint32_t mask = upper & ~((1u << lo) - 1u);
                 c += __popc(s_bm[w * R + r] & mask);
             }
-            if (c) atomicAdd(&p.src_dst_count[s * R + r], c);
+            if (c && EP_IN(s * R + r, R * R)) atomicAdd(&p.src_dst_count[s * R + r], c);
         }
     }
 
@@ -735,7 +756,7 @@ __global__ void __launch_bounds__(kClusterThreads, 1)
     if (tid == 0) s_bad = 0;
     if (p.src_dst_count) {
         for (int i = me * kClusterThreads + tid; i < R * R; i += C * kClusterThreads)
-            p.src_dst_count[i] = 0;
+            if (EP_IN(i, R * R)) p.src_dst_count[i] = 0;
     }
     __syncthreads();
 
@@ -748,7 +769,7 @@ __global__ void __launch_bounds__(kClusterThreads, 1)
 #pragma unroll
         for (int u = 0; u < kClusterUnroll; ++u) {
             const int i = base + u * kClusterThreads + tid;
-            e[u] = i < n_ent ? src[i] : -1;
+            e[u] = (i < n_ent && EP_IN(static_cast<int64_t>(t0) * p.K + i, static_cast<int64_t>(p.T) * p.K)) ? src[i] : -1;
         }
         if (expanded) {
 #pragma unroll
@@ -826,7 +847,7 @@ __global__ void __launch_bounds__(kClusterThreads, 1)
         }
         s_tot[r] = tot;
         s_before[r] = before;
-        if (me == 0) p.num_tokens_per_rank[r] = tot;
+        if (me == 0 && EP_IN(r, R)) p.num_tokens_per_rank[r] = tot;
     }
     if (warp_id == 1) {
         const int v = lane < me ? *cluster.map_shared_rank(&s_rows_total, lane) : 0;
@@ -846,7 +867,7 @@ __global__ void __launch_bounds__(kClusterThreads, 1)
                 tot += v[c];
                 if (c < me) before += v[c];
             }
-            if (me == C - 1) p.num_tokens_per_expert[e] = tot;
+            if (me == C - 1 && EP_IN(e, E)) p.num_tokens_per_expert[e] = tot;
             s_eb[e] = (tot + p.alignment - 1) / p.alignment * p.alignment;
             s_wc[e] = before;
         }
@@ -860,7 +881,7 @@ __global__ void __launch_bounds__(kClusterThreads, 1)
             int tot = 0;
 #pragma unroll
             for (int c = 0; c < kMaxClusterCtas; ++c) tot += v[c];
-            p.num_tokens_per_expert[e] = tot;
+            if (EP_IN(e, E)) p.num_tokens_per_expert[e] = tot;
             s_hist[e] = (tot + p.alignment - 1) / p.alignment * p.alignment;
         }
         for (int n = tid; n < NN && !kNodeRows; n += kClusterThreads) {
@@ -870,7 +891,7 @@ __global__ void __launch_bounds__(kClusterThreads, 1)
             int tot = 0;
 #pragma unroll
             for (int c = 0; c < kMaxClusterCtas; ++c) tot += v[c];
-            p.num_tokens_per_node[n] = tot;
+            if (EP_IN(n, NN)) p.num_tokens_per_node[n] = tot;
         }
     }
     if (kNodeRows) {
@@ -886,7 +907,7 @@ __global__ void __launch_bounds__(kClusterThreads, 1)
                 tot += v[c];
                 if (c < me) before += v[c];
             }
-            if (me == C - 1) p.num_tokens_per_node[n] = tot;
+            if (me == C - 1 && EP_IN(n, NN)) p.num_tokens_per_node[n] = tot;
             s_ntot[n] = tot;
             s_nbefore[n] = before;
         }
@@ -929,15 +950,18 @@ __global__ void __launch_bounds__(kClusterThreads, 1)
     __syncthreads();
     const int n_recv = s_totals[0];
     if (me == 0) {
-        for (int r = tid; r < R; r += kClusterThreads) p.rank_offset[r] = s_tot[r];
-        if (tid == 0) p.rank_offset[R] = n_recv;
+        for (int r = tid; r < R; r += kClusterThreads)
+            if (EP_IN(r, R + 1)) p.rank_offset[r] = s_tot[r];
+        if (tid == 0 && EP_IN(R, R + 1)) p.rank_offset[R] = n_recv;
     }
     if (me == C - 1) {
-        for (int e = tid; e < E; e += kClusterThreads) p.expert_offset[e] = s_escan[e];
-        if (tid == 0) p.expert_offset[E] = s_totals[1];
+        for (int e = tid; e < E; e += kClusterThreads)
+            if (EP_IN(e, E + 1)) p.expert_offset[e] = s_escan[e];
+        if (tid == 0 && EP_IN(E, E + 1)) p.expert_offset[E] = s_totals[1];
         if (kNodeRows) {
-            for (int n = tid; n < NN; n += kClusterThreads) p.node_offset[n] = s_ntot[n];
-            if (tid == 0) p.node_offset[NN] = s_totals[2];
+            for (int n = tid; n < NN; n += kClusterThreads)
+                if (EP_IN(n, NN + 1)) p.node_offset[n] = s_ntot[n];
+            if (tid == 0 && EP_IN(NN, NN + 1)) p.node_offset[NN] = s_totals[2];
         }
     }
 
@@ -967,10 +991,13 @@ __global__ void __launch_bounds__(kClusterThreads, 1)
             if (++r == R) { r = 0; ++tl; }
         }
         if (j0 + 4 <= n_el) {
-            *reinterpret_cast<int4*>(drow + j0) = make_int4(v[0], v[1], v[2], v[3]);
-            *reinterpret_cast<uint32_t*>(inr + j0) = in4;
+            if (EP_IN(static_cast<int64_t>(t0) * R + j0 + 3, static_cast<int64_t>(p.T) * R)) {
+                *reinterpret_cast<int4*>(drow + j0) = make_int4(v[0], v[1], v[2], v[3]);
+                *reinterpret_cast<uint32_t*>(inr + j0) = in4;
+            }
         } else {
             for (int u = 0; u < 4 && j0 + u < n_el; ++u) {
+                if (!EP_IN(static_cast<int64_t>(t0) * R + j0 + u, static_cast<int64_t>(p.T) * R)) continue;
                 drow[j0 + u] = v[u];
                 inr[j0 + u] = static_cast<uint8_t>((in4 >> (8 * u)) & 1u);
             }
@@ -987,6 +1014,7 @@ __global__ void __launch_bounds__(kClusterThreads, 1)
             const int w = tl >> 5;
             const uint32_t word = s_bmn[w * NN + n];
             const uint32_t b = static_cast<uint32_t>(tl & 31);
+            if (!EP_IN(static_cast<int64_t>(t0) * NN + j, static_cast<int64_t>(p.T) * NN)) continue;
             nrow[j] = ((word >> b) & 1u)
                           ? s_ntot[n] + s_nbefore[n] + s_nwbase[w * NN + n] + __popc(word & ((1u << b) - 1u))
                           : -1;
@@ -997,8 +1025,8 @@ __global__ void __launch_bounds__(kClusterThreads, 1)
     if (p.token_offset) {
         const int cta_base = s_cta_base;
         for (int tl = tid; tl < nt; tl += kClusterThreads)
-            p.token_offset[t0 + tl] = cta_base + s_wtok[tl >> 5] + s_ntok[tl];
-        if (me == C - 1 && tid == 0) p.token_offset[p.T] = n_recv;
+            if (EP_IN(t0 + tl, p.T + 1)) p.token_offset[t0 + tl] = cta_base + s_wtok[tl >> 5] + s_ntok[tl];
+        if (me == C - 1 && tid == 0 && EP_IN(p.T, p.T + 1)) p.token_offset[p.T] = n_recv;
     }
 
     // src_dst_count[s][r] += tokens of source rank s in this range that rank r receives.
@@ -1019,7 +1047,7 @@ __global__ void __launch_bounds__(kClusterThreads, 1)
                 const uint32_t upper = hi >= 32 ? 0xffffffffu : ((1u << hi) - 1u);
                 c += __popc(s_bm[w * R + r] & upper & ~((1u << lo) - 1u));
             }
-            if (c) atomicAdd(&p.src_dst_count[s * R + r], c);
+            if (c && EP_IN(s * R + r, R * R)) atomicAdd(&p.src_dst_count[s * R + r], c);
         }
     }
     // Expanded rows: expert e's entries of this CTA start at expert_offset[e] +
@@ -1034,7 +1062,8 @@ __global__ void __launch_bounds__(kClusterThreads, 1)
             }
         }
         __syncthreads();
-        rank_entries(s_key, n_ent, E, s_eb, s_wc, p.expanded_row + static_cast<int64_t>(t0) * p.K, nw);
+        rank_entries(s_key, n_ent, E, s_eb, s_wc, p.expanded_row + static_cast<int64_t>(t0) * p.K, nw,
+                     static_cast<int64_t>(p.T - t0) * p.K, p.status);
     }
 
     // No CTA may exit (releasing its shared memory) while another still reads it.
@@ -1321,7 +1350,8 @@ __global__ void __launch_bounds__(1024, 1) layout_small_kernel(const LayoutParam
     }
     if (kExpanded) {
         __syncthreads();   // s_hist now holds expert_offset
-        rank_entries(s_key, n_ent, E, s_hist, s_wc, p.expanded_row, kSmallRankWarps);
+        rank_entries(s_key, n_ent, E, s_hist, s_wc, p.expanded_row, kSmallRankWarps,
+                     static_cast<int64_t>(p.T) * p.K, p.status);
     }
 }
 

@@ -63,6 +63,12 @@ typedef int32_t ep_status_t;
 #define EP_ERR_CAPACITY      8   /* device: a row index >= the receive capacity */
 #define EP_ERR_TIMEOUT       16  /* device: a bounded wait gave up              */
 #define EP_ERR_CUDA          32  /* host: a CUDA launch failed                  */
+/* device, bounds-checked build only (compiled with EP_GET_CHECKED=1): an
+ * index failed the check against its array's extent, or a dst_row /
+ * expanded_row / node_row entry was below -1; the access was skipped,
+ * nothing traps.  The product build never sets it (it reads an entry below
+ * -1 as "absent", like -1). */
+#define EP_ERR_OUT_OF_BOUNDS 64
 
 /* Payload types of the receive buffer. */
 #define EP_BF16      0
@@ -432,6 +438,13 @@ const char* ep_status_string(int32_t status);
 
 /* ABI version of this header (bumped on any signature change). */
 int ep_abi_version(void);
+
+/* 1 when this copy of the library is the bounds-checked build (every kernel
+ * compiled with EP_GET_CHECKED=1: each global load and store is checked
+ * against the extent its arguments declare, a failing access is skipped and
+ * sets EP_ERR_OUT_OF_BOUNDS in *d_status), 0 for the product build.  The
+ * checked build computes the same results on valid input, more slowly. */
+int ep_bounds_checked(void);
 
 #ifdef __cplusplus
 }

@@ -32,7 +32,8 @@ def test_header_declares_the_entry_points():
               "ep_recv_capacity_bound", "ep_status_string", "ep_abi_version", "ep_dispatch_expanded",
               "ep_combine_expanded", "ep_expanded_capacity_bound", "ep_combine_topk_weights",
               "ep_accumulate_expert_stats", "ep_theoretical_num_sms",
-              "ep_dispatch_hierarchical", "ep_combine_hierarchical", "ep_layout_and_dispatch"):
+              "ep_dispatch_hierarchical", "ep_combine_hierarchical", "ep_layout_and_dispatch",
+              "ep_bounds_checked"):
         assert n in names
 
 
@@ -46,6 +47,7 @@ def test_status_strings_and_sizes(lib):
     assert lib.ep_status_string(0) == b"ok"
     assert lib.ep_status_string(4 | 8) == b"invalid_index|capacity"
     assert lib.ep_status_string(999) == b"unknown"
+    assert lib.ep_status_string(64 | 16) == b"timeout|out_of_bounds"
     lib.ep_recv_capacity_bound.restype = ctypes.c_int64
     assert lib.ep_recv_capacity_bound(4096, 8, 8) == 4096 * 8
     assert lib.ep_recv_capacity_bound(128, 8, 4) == 512
@@ -53,7 +55,8 @@ def test_status_strings_and_sizes(lib):
     ws = lib.ep_layout_workspace_bytes(4096, 8, 256, 8, 0)
     tiles = 16
     assert ws >= 4 * tiles * (8 + 256 + 8 * 8)
-    assert lib.ep_abi_version() == 7
+    assert lib.ep_abi_version() == 8
+    assert lib.ep_bounds_checked() == 0   # the product library
 
 
 def test_host_checks_reject_before_any_launch(lib):
