@@ -171,6 +171,9 @@ __device__ __forceinline__ void write_metadata(const DispatchParams& p, int t, i
                           ? p.topk_weights[static_cast<int64_t>(t) * K + lane]
                           : 0.0f;
     const int tok_off = (w.balanced && EP_IN(t, p.T + 1)) ? p.token_offset[t] : 0;
+    // the rank of this lane's expert and its index there, once (not per destination)
+    const int e_rank = (e_l >= 0 && e_l < p.E) ? static_cast<int>(e_l) / p.experts_per_rank : -1;
+    const int32_t e_local = static_cast<int32_t>(e_l) - e_rank * p.experts_per_rank;
     int m_base = 0;
     for (int rb = 0; rb < p.R; rb += 32) {
         const int r = rb + lane;
@@ -189,10 +192,10 @@ __device__ __forceinline__ void write_metadata(const DispatchParams& p, int t, i
             const int64_t dd = __shfl_sync(0xffffffffu, d, src);
             const int rr = rb + src;
             if (lane < K && EP_IN(dd * K + lane, p.capacity * K)) {
-                const bool on = e_l >= 0 && e_l < p.E && static_cast<int>(e_l) / p.experts_per_rank == rr;
+                const bool on = e_rank == rr;
                 if (p.recv_topk_idx)
                     p.recv_topk_idx[dd * K + lane] =
-                        on ? static_cast<int32_t>(e_l) - rr * p.experts_per_rank : -1;
+                        on ? e_local : -1;
                 if (p.recv_topk_weights) p.recv_topk_weights[dd * K + lane] = on ? w_l : 0.0f;
             }
             if (lane == 0 && p.recv_src_idx && EP_IN(dd, p.capacity)) p.recv_src_idx[dd] = t;
@@ -382,17 +385,21 @@ __device__ __forceinline__ void prefetch_x(const DispatchParams& p) {
 //   rank_offset = exclusive prefix of the per-rank token counts,
 // with masked (-1) and invalid ids counting for no rank, so no layout kernel
 // has to run first.  The CTA of piece 0 of token t also writes the token's
-// layout rows (dst_row, is_token_in_rank, token_offset[t]).  One extra CTA
-// of the grid (kLayoutCta, no dispatch work) writes the counts and offsets
-// (per rank, per expert with the alignment, per node, src_dst_count,
-// rank_offset, expert_offset, token_offset[T]) and flags invalid ids, beside
-// the dispatch CTAs.  CTA-wide: every thread calls it, with blockDim.x ==
-// 256, T <= kSelfMaxTokens, R <= 32, K <= kSelfMaxTopk and
-// E <= kSelfMaxExperts.  Returns in lane r of every warp the row of rank r
-// for token t, or -1.
+// layout rows (dst_row, is_token_in_rank, token_offset[t]).  Two extra CTAs
+// of the grid (kLayoutCta, no dispatch work; c selects the part) write the
+// counts and offsets beside the dispatch CTAs: part 0 per rank, per node,
+// src_dst_count, rank_offset and token_offset[T]; part 1 per expert with
+// the alignment and expert_offset, and flags invalid ids.  CTA-wide: every
+// thread calls it, with blockDim.x == 256, T <= kSelfMaxTokens, R <= 32,
+// K <= kSelfMaxTopk and E <= kSelfMaxExperts.  Returns in lane r of every
+// warp the row of rank r for token t, or -1 (dispatch CTAs).
 constexpr int kSelfMaxTokens = kSelfRouteMaxTokens;
 constexpr int kSelfMaxTopk = kSelfRouteMaxTopk;
 constexpr int kSelfMaxExperts = kSelfRouteMaxExperts;
+// Layout CTAs after the dispatch items: the last writes the per-rank counts
+// and offsets, src_dst_count and the per-node counts; the one before it the
+// per-expert counts and offsets (and flags invalid ids).
+constexpr int kSelfLayoutCtas = 2;
 static_assert(kSelfMaxTokens <= 256, "self_route_layout: one thread per token in a 256-thread CTA");
 struct SelfRouteSmem {
     uint32_t mask[kSelfMaxTokens];           // ranks holding each token (bit r)
@@ -408,12 +415,55 @@ __device__ __forceinline__ SelfRouteSmem& self_smem() {
     return s;
 }
 
+#ifndef EP_SELF_ROUTE_COALESCED
+#define EP_SELF_ROUTE_COALESCED 1   // 16-byte top-k loads in the dispatch CTAs' routing step
+#endif
+#ifndef EP_SELF_META_PIECE
+#define EP_SELF_META_PIECE 1        // piece whose warp 1 writes the receive metadata
+#endif
+#ifndef EP_SELF_META_SPREAD
+#define EP_SELF_META_SPREAD 1       // with four or more pieces, one metadata array per piece
+#endif
+#ifndef EP_SELF_EARLY_META
+#define EP_SELF_EARLY_META 1        // that warp loads the token's entries before the routing step
+#endif
+
 template <bool kLayoutCta>
 __device__ int self_route_layout(const DispatchParams& p, int t, int c, SelfRouteSmem& s) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     constexpr bool cta0 = kLayoutCta;
+    // layout CTAs: c is the part (0: ranks, 1: experts); CTA-uniform
+    const bool rank_part = !cta0 || c == 0;
+    const bool expert_part = cta0 && c == 1;
     int64_t e[kSelfMaxTopk];
-    if (tid < p.T) {   // one thread per token: all K entries in flight at once
+    // K in {2, 4, 8, 16} and a 16-byte aligned topk_idx: 16-byte loads (two
+    // entries each) over the whole [T, K] block, and the K / 2 lanes of a
+    // token OR their rank bits together (a quarter of the L2 requests of one
+    // thread per token, on a block that every CTA reads).  Thread tid holds
+    // entries 2 (j * 256 + tid) and the next in e[2 j], e[2 j + 1].
+    const int q = p.K >> 1;
+    const bool coalesced = EP_SELF_ROUTE_COALESCED && (p.K & (p.K - 1)) == 0 && p.K >= 2 &&
+                           (reinterpret_cast<uintptr_t>(p.topk_idx) & 15u) == 0;
+    const int n_pairs = p.T * q;
+    if (coalesced) {
+        static_assert(kSelfMaxTokens * kSelfMaxTopk / 2 <= 256 * (kSelfMaxTopk / 2), "entry pairs per thread");
+#pragma unroll
+        for (int j = 0; j < kSelfMaxTopk / 2; ++j) {
+            const int i = j * 256 + tid;   // blockDim.x == 256
+            e[2 * j] = e[2 * j + 1] = -1;
+            if (j * 256 >= n_pairs) continue;   // the same trips in every lane
+            uint32_t m = 0;
+            if (i < n_pairs && EP_IN(2 * static_cast<int64_t>(i) + 1, static_cast<int64_t>(p.T) * p.K)) {
+                const longlong2 v = *reinterpret_cast<const longlong2*>(p.topk_idx + 2 * static_cast<int64_t>(i));
+                e[2 * j] = v.x;
+                e[2 * j + 1] = v.y;
+                if (v.x >= 0 && v.x < p.E) m |= 1u << (static_cast<int>(v.x) / p.experts_per_rank);
+                if (v.y >= 0 && v.y < p.E) m |= 1u << (static_cast<int>(v.y) / p.experts_per_rank);
+            }
+            for (int o = 1; o < q; o <<= 1) m |= __shfl_xor_sync(0xffffffffu, m, o);
+            if (i < n_pairs && (i & (q - 1)) == 0) s.mask[i / q] = m;
+        }
+    } else if (tid < p.T) {   // one thread per token: all K entries in flight at once
 #pragma unroll
         for (int k = 0; k < kSelfMaxTopk; ++k) {
             const int64_t i = static_cast<int64_t>(tid) * p.K + k;
@@ -425,21 +475,21 @@ __device__ int self_route_layout(const DispatchParams& p, int t, int c, SelfRout
             if (e[k] >= 0 && e[k] < p.E) m |= 1u << (static_cast<int>(e[k]) / p.experts_per_rank);
         s.mask[tid] = m;
     }
-    if (cta0)
+    if (expert_part)
         for (int i = tid; i < p.E; i += blockDim.x) s.hist[i] = 0;
     __syncthreads();
-    if (cta0 && tid < p.T) {
+    if (expert_part && (coalesced || tid < p.T)) {   // every entry once: the expert histogram, invalid ids
         bool bad = false;
 #pragma unroll
         for (int k = 0; k < kSelfMaxTopk; ++k) {
-            if (k >= p.K) break;
+            if (!coalesced && k >= p.K) break;
             if (e[k] >= 0 && e[k] < p.E) atomicAdd(&s.hist[e[k]], 1);
             else if (e[k] != -1) bad = true;
         }
         if (bad) atomicOr(p.status, EP_ERR_INVALID_INDEX);
     }
     const int n_words = (p.T + 31) >> 5;
-    if (warp < n_words) {
+    if (rank_part && warp < n_words) {
         const int j = (warp << 5) + lane;
         const uint32_t m = j < p.T ? s.mask[j] : 0u;
         for (int r = 0; r < p.R; ++r) {
@@ -449,7 +499,7 @@ __device__ int self_route_layout(const DispatchParams& p, int t, int c, SelfRout
     }
     __syncthreads();
     int total = 0, before = 0;
-    if (lane < p.R) {
+    if (rank_part && lane < p.R) {
         const int tw = t >> 5;
         for (int w = 0; w < n_words; ++w) {
             const uint32_t b = s.bal[w][lane];
@@ -463,17 +513,22 @@ __device__ int self_route_layout(const DispatchParams& p, int t, int c, SelfRout
     const bool in = lane < p.R && ((s.mask[t] >> lane) & 1u);
     const int d = in ? offset + before : -1;
 
-    // the token's layout rows
-    if (!kLayoutCta && c == 0 && warp == 0) {
+    // the token's layout rows, one array per warp: on this short grid the
+    // first store into each array waits for its address translation, and on
+    // separate warps those waits overlap
+    if (!kLayoutCta && c == 0 && warp < 3) {
         const int64_t tr = static_cast<int64_t>(t) * p.R + lane;
-        if (lane < p.R && EP_IN(tr, static_cast<int64_t>(p.T) * p.R)) {
-            p.l_dst_row[tr] = d;
-            p.l_is_token_in_rank[tr] = in ? 1 : 0;
+        const bool ok = lane < p.R && EP_IN(tr, static_cast<int64_t>(p.T) * p.R);
+        if (warp == 0) {
+            if (ok) p.l_dst_row[tr] = d;
+        } else if (warp == 1) {
+            if (ok) p.l_is_token_in_rank[tr] = in ? 1 : 0;
+        } else {
+            const int rows_before = static_cast<int>(__reduce_add_sync(0xffffffffu, static_cast<unsigned>(before)));
+            if (lane == 0 && p.l_token_offset && EP_IN(t, p.T + 1)) p.l_token_offset[t] = rows_before;
         }
-        const int rows_before = static_cast<int>(__reduce_add_sync(0xffffffffu, static_cast<unsigned>(before)));
-        if (lane == 0 && p.l_token_offset && EP_IN(t, p.T + 1)) p.l_token_offset[t] = rows_before;
     }
-    if (cta0) {
+    if (cta0 && rank_part) {
         const int n_rows = __shfl_sync(0xffffffffu, incl, 31);
         if (warp == 0) {
             if (lane < p.R && EP_IN(lane, p.R)) {
@@ -484,17 +539,6 @@ __device__ int self_route_layout(const DispatchParams& p, int t, int c, SelfRout
                 if (EP_IN(p.R, p.R + 1)) p.l_rank_offset[p.R] = n_rows;
                 if (p.l_token_offset && EP_IN(p.T, p.T + 1)) p.l_token_offset[p.T] = n_rows;
             }
-        }
-        // per-expert counts, rounded up to the alignment, scanned
-        const int n_chunks = (p.E + 31) >> 5;
-        for (int ch = warp; ch < n_chunks; ch += blockDim.x >> 5) {
-            const int ex = ch * 32 + lane;
-            const int cnt = ex < p.E ? s.hist[ex] : 0;
-            if (ex < p.E && EP_IN(ex, p.E)) p.l_num_tokens_per_expert[ex] = cnt;
-            const int al = (cnt + p.l_alignment - 1) / p.l_alignment * p.l_alignment;
-            const int ci = warp_inclusive_scan(al);
-            if (ex < p.E) s.hist[ex] = ci - al;
-            if (lane == 31) s.chunk[ch] = ci;
         }
         // src_dst_count[src][r]: tokens of source rank src (T / R each) on rank r
         if (p.l_src_dst_count) {
@@ -509,13 +553,29 @@ __device__ int self_route_layout(const DispatchParams& p, int t, int c, SelfRout
         // tokens reaching each node (ranks [n * rpn, (n + 1) * rpn))
         if (p.l_num_tokens_per_node) {
             for (int n = tid; n < p.l_num_nodes; n += blockDim.x) {
-                const uint32_t node_bits = (p.l_ranks_per_node >= 32 ? 0xffffffffu
-                                                                     : ((1u << p.l_ranks_per_node) - 1u))
-                                           << (n * p.l_ranks_per_node);
+                // a token reaches node n when any rank of n holds it: OR the
+                // ranks' membership words, count the bits
                 int cnt = 0;
-                for (int u = 0; u < p.T; ++u) cnt += (s.mask[u] & node_bits) != 0u;
+                for (int w = 0; w < n_words; ++w) {
+                    uint32_t o = 0u;
+                    for (int r = n * p.l_ranks_per_node; r < (n + 1) * p.l_ranks_per_node; ++r) o |= s.bal[w][r];
+                    cnt += __popc(o);
+                }
                 if (EP_IN(n, p.l_num_nodes)) p.l_num_tokens_per_node[n] = cnt;
             }
+        }
+    }
+    if (expert_part) {
+        // per-expert counts, rounded up to the alignment, scanned
+        const int n_chunks = (p.E + 31) >> 5;
+        for (int ch = warp; ch < n_chunks; ch += blockDim.x >> 5) {
+            const int ex = ch * 32 + lane;
+            const int cnt = ex < p.E ? s.hist[ex] : 0;
+            if (ex < p.E && EP_IN(ex, p.E)) p.l_num_tokens_per_expert[ex] = cnt;
+            const int al = (cnt + p.l_alignment - 1) / p.l_alignment * p.l_alignment;
+            const int ci = warp_inclusive_scan(al);
+            if (ex < p.E) s.hist[ex] = ci - al;
+            if (lane == 31) s.chunk[ch] = ci;
         }
         __syncthreads();   // CTA-uniform branch
         if (warp == 0) {   // exclusive prefix of the chunk totals (at most 64 chunks)
@@ -534,25 +594,66 @@ __device__ int self_route_layout(const DispatchParams& p, int t, int c, SelfRout
     return d;
 }
 
-// Metadata of token t with its destination rows in registers (lane r holds
-// rank r's row, R <= 32); one warp.  Same entries as write_metadata.
-__device__ __forceinline__ void write_metadata_lanes(const DispatchParams& p, int t, int lane, int d) {
+// The token's top-k entries for its receive metadata, loaded where the
+// call stands (volatile: issued before the routing step, not sunk to the use).
+__device__ __forceinline__ void load_token_entries(const DispatchParams& p, int t, int lane, int64_t& e_l, float& w_l) {
+    const int64_t ek = static_cast<int64_t>(t) * p.K + lane, n_tk = static_cast<int64_t>(p.T) * p.K;
+    e_l = -1;
+    w_l = 0.0f;
+    if (lane < p.K && EP_IN(ek, n_tk)) {
+        asm volatile("ld.global.nc.s64 %0, [%1];" : "=l"(e_l) : "l"(p.topk_idx + ek));
+        if (p.recv_topk_weights) asm volatile("ld.global.nc.f32 %0, [%1];" : "=f"(w_l) : "l"(p.topk_weights + ek));
+    }
+}
+
+// The self-routed item's piece whose warps write the token's receive
+// metadata: piece 1 when there is one, so that piece 0 (which writes the
+// token's layout rows) and it each carry one extra chain of first touches.
+__device__ __forceinline__ int self_meta_piece(const DispatchParams& p) {
+    return EP_SELF_META_PIECE < p.chunks ? EP_SELF_META_PIECE : p.chunks - 1;
+}
+
+// Which receive-metadata part (0..2) warp warp_g (of nw) of piece c
+// writes, or -1.  The last warps take it: on the few-token FP8 grid the last
+// warp has no blocks of the piece to cast, so the metadata overlaps the
+// other warps' stores.  With at least four pieces each part has a piece of
+// its own (pieces 1, 2, 3, last warp); otherwise the last three warps of the
+// metadata piece write one part each.
+__device__ __forceinline__ int self_meta_part(const DispatchParams& p, int c, int warp_g, int nw) {
+    if (EP_SELF_META_SPREAD && p.chunks >= 4) return (warp_g == nw - 1 && c >= 1 && c <= 3) ? c - 1 : -1;
+    const int part = warp_g - (nw - 3);
+    return (c == self_meta_piece(p) && part >= 0 && part < 3) ? part : -1;
+}
+
+// One of the token's receive-metadata arrays (part 0: recv_topk_idx, 1:
+// recv_topk_weights, 2: recv_src_idx) for every destination (lane r of d:
+// rank r's row, R <= 32); one warp per part, so that the first stores into
+// the three arrays wait for their address translations side by side.  Same
+// entries as write_metadata.
+__device__ __forceinline__ void write_metadata_part(const DispatchParams& p, int t, int lane, int d, int64_t e_l,
+                                                    float w_l, int part) {
     const int K = p.K;
-    const int64_t ek = static_cast<int64_t>(t) * K + lane, n_tk = static_cast<int64_t>(p.T) * K;
-    const int64_t e_l = (lane < K && EP_IN(ek, n_tk)) ? p.topk_idx[ek] : -1;
-    const float w_l = (lane < K && p.recv_topk_weights && EP_IN(ek, n_tk)) ? p.topk_weights[ek] : 0.0f;
+    // the rank of this lane's expert and its index there, once (not per destination)
+    const int e_rank = (e_l >= 0 && e_l < p.E) ? static_cast<int>(e_l) / p.experts_per_rank : -1;
+    const int32_t e_local = static_cast<int32_t>(e_l) - e_rank * p.experts_per_rank;
     unsigned m = __ballot_sync(0xffffffffu, d >= 0 && d < p.capacity);
     while (m) {
         const int rr = __ffs(m) - 1;
         m &= m - 1;
         const int64_t dd = __shfl_sync(0xffffffffu, d, rr);
-        if (lane < K && EP_IN(dd * K + lane, p.capacity * K)) {
-            const bool on = e_l >= 0 && e_l < p.E && static_cast<int>(e_l) / p.experts_per_rank == rr;
-            if (p.recv_topk_idx)
-                p.recv_topk_idx[dd * K + lane] = on ? static_cast<int32_t>(e_l) - rr * p.experts_per_rank : -1;
-            if (p.recv_topk_weights) p.recv_topk_weights[dd * K + lane] = on ? w_l : 0.0f;
+        if (part < 2) {
+            if (lane < K && EP_IN(dd * K + lane, p.capacity * K)) {
+                const bool on = e_rank == rr;
+                if (part == 0) {
+                    if (p.recv_topk_idx)
+                        p.recv_topk_idx[dd * K + lane] = on ? e_local : -1;
+                } else if (p.recv_topk_weights) {
+                    p.recv_topk_weights[dd * K + lane] = on ? w_l : 0.0f;
+                }
+            }
+        } else if (lane == 0 && p.recv_src_idx && EP_IN(dd, p.capacity)) {
+            p.recv_src_idx[dd] = t;
         }
-        if (lane == 0 && p.recv_src_idx && EP_IN(dd, p.capacity)) p.recv_src_idx[dd] = t;
     }
 }
 
@@ -596,7 +697,11 @@ __device__ __forceinline__ void dispatch_regs_item(const DispatchParams& p, int6
     const int64_t drow0 = static_cast<int64_t>(t) * n_dst, n_drow = static_cast<int64_t>(p.T) * n_dst;
     const int32_t* drow = (kExpanded ? p.expanded_row : p.dst_row) + drow0;
     int d0, d1;
+    int64_t me_l = -1;   // self-routed: the token's entries, for the receive metadata
+    float mw_l = 0.0f;
     if constexpr (kSelf) {
+        if (EP_SELF_EARLY_META && static_cast<unsigned>(self_meta_part(p, c, warp_g, kRegThreads / 32)) < 2u)
+            load_token_entries(p, t, lane, me_l, mw_l);
         d0 = self_route_layout<false>(p, t, c, self_smem());   // R <= 32
         d1 = -1;
     } else {
@@ -605,11 +710,15 @@ __device__ __forceinline__ void dispatch_regs_item(const DispatchParams& p, int6
         (void)EP_ROW_OK(d0);
         (void)EP_ROW_OK(d1);
     }
-    if (warp_g == 1 && c == 0) {
+    if (kSelf) {
+        const int part = self_meta_part(p, c, warp_g, kRegThreads / 32);
+        if (part >= 0) {
+            if (!EP_SELF_EARLY_META && part < 2) load_token_entries(p, t, lane, me_l, mw_l);
+            write_metadata_part(p, t, lane, d0, me_l, mw_l, part);
+        }
+    } else if (warp_g == 1 && c == 0) {
         if (kExpanded) {
             write_expanded_metadata(p, t, lane);
-        } else if (kSelf) {
-            write_metadata_lanes(p, t, lane, d0);
         } else {
             CtaWork all;
             all.first = 0;
@@ -669,9 +778,9 @@ __global__ void __launch_bounds__(kRegThreads * kGroups, kGroups > 1 ? 1 : kSelf
     const int warp_g = gtid >> 5;   // warp within the group
     const int lane = threadIdx.x & 31;
     bool cap_bad = false;
-    if (kSelf && blockIdx.x == gridDim.x - 1) {   // the layout's counts and offsets
+    if (kSelf && blockIdx.x >= gridDim.x - kSelfLayoutCtas) {   // the layout's counts and offsets
         pdl_wait();
-        self_route_layout<true>(p, 0, 1, self_smem());
+        self_route_layout<true>(p, 0, static_cast<int>(gridDim.x - 1 - blockIdx.x), self_smem());
         return;
     }
     if (kGroups == 1) prefetch_x<false>(p);
@@ -744,14 +853,19 @@ __device__ __forceinline__ void dispatch_fp8_item(const DispatchParams& p, int64
         const uint8_t* src = xrow + so;
 #pragma unroll
         for (int u = 0; u < kVec; ++u)
-            v[q][u] = (b < b_end && EP_IN_BYTES(xrow_off + so + 16 * u, 16, x_bytes)) ? ld_stream_v4(src + 16 * u)
-                                                                                      : make_uint4(0, 0, 0, 0);
+            v[q][u] = (b < b_end && EP_IN_BYTES(xrow_off + so + 16 * u, 16, x_bytes))
+                          ? ld_stream_v4(src + 16 * u)
+                          : make_uint4(0, 0, 0, 0);
     }
     const int n_dst = kExpanded ? p.K : p.R;
     const int64_t drow0 = static_cast<int64_t>(t) * n_dst, n_drow = static_cast<int64_t>(p.T) * n_dst;
     const int32_t* drow = (kExpanded ? p.expanded_row : p.dst_row) + drow0;
     int d0, d1;
+    int64_t me_l = -1;   // self-routed: the token's entries, for the receive metadata
+    float mw_l = 0.0f;
     if constexpr (kSelf) {
+        if (EP_SELF_EARLY_META && static_cast<unsigned>(self_meta_part(p, c, warp_g, group_warps)) < 2u)
+            load_token_entries(p, t, lane, me_l, mw_l);
         d0 = self_route_layout<false>(p, t, c, self_smem());   // R <= 32
         d1 = -1;
     } else {
@@ -762,11 +876,15 @@ __device__ __forceinline__ void dispatch_fp8_item(const DispatchParams& p, int64
     }
     const int64_t rx_bytes = p.capacity * p.H;   // FP8 codes: one byte per channel
     const int64_t sf_n = p.sf_col_major ? static_cast<int64_t>(nb) * p.sf_stride : p.capacity * nb;
-    if (warp_g == 1 && c == 0) {
+    if (kSelf) {
+        const int part = self_meta_part(p, c, warp_g, group_warps);
+        if (part >= 0) {
+            if (!EP_SELF_EARLY_META && part < 2) load_token_entries(p, t, lane, me_l, mw_l);
+            write_metadata_part(p, t, lane, d0, me_l, mw_l, part);
+        }
+    } else if (warp_g == 1 && c == 0) {
         if (kExpanded) {
             write_expanded_metadata(p, t, lane);
-        } else if (kSelf) {
-            write_metadata_lanes(p, t, lane, d0);
         } else {
             CtaWork all;
             all.first = 0;
@@ -940,9 +1058,9 @@ __global__ void __launch_bounds__(kFp8Threads * kGroups,
     const int gtid = kGroups == 1 ? static_cast<int>(threadIdx.x) : static_cast<int>(threadIdx.x) % kFp8Threads;
     const int lane = threadIdx.x & 31;
     bool cap_bad = false;
-    if (kSelf && blockIdx.x == gridDim.x - 1) {   // the layout's counts and offsets
+    if (kSelf && blockIdx.x >= gridDim.x - kSelfLayoutCtas) {   // the layout's counts and offsets
         pdl_wait();
-        self_route_layout<true>(p, 0, 1, self_smem());
+        self_route_layout<true>(p, 0, static_cast<int>(gridDim.x - 1 - blockIdx.x), self_smem());
         return;
     }
     if (kGroups == 1) prefetch_x<true>(p);
@@ -1024,7 +1142,9 @@ cudaError_t launch_dispatch_bf16(DispatchParams p, cudaStream_t stream) {
         if (p.T > 0 && static_cast<int64_t>(p.T) * chunks < want_items) {
             // a CTA that derives its rows itself (self_route) pays that
             // latency once per wave: keep it to one wave of 4 CTAs per SM
-            const int more = p.self_route ? di.num_sms * kSelfRegBlocks / p.T : (want_items + p.T - 1) / p.T;
+            // (the layout CTAs included)
+            const int more = p.self_route ? (di.num_sms * kSelfRegBlocks - kSelfLayoutCtas) / p.T
+                                          : (want_items + p.T - 1) / p.T;
             const int max_chunks = static_cast<int>(row_bytes / 1024u) > 0 ? static_cast<int>(row_bytes / 1024u) : 1;
             chunks = more < max_chunks ? more : max_chunks;
             if (chunks < 1) chunks = 1;
@@ -1043,7 +1163,7 @@ cudaError_t launch_dispatch_bf16(DispatchParams p, cudaStream_t stream) {
             return launch_pdl(dispatch_bf16_regs_kernel<true, kSmGroups>, grid, block, 0, stream, p);
         }
         // self routing: one more CTA, which writes the layout's counts and offsets
-        const dim3 grid(static_cast<unsigned>(items + (p.self_route ? 1 : 0))), block(kRegThreads);
+        const dim3 grid(static_cast<unsigned>(items + (p.self_route ? kSelfLayoutCtas : 0))), block(kRegThreads);
         p.prefetch_ctas = di.num_sms * 6;   // the first wave (6 CTAs per SM)
         p.prefetch_items = EP_DISPATCH_PREFETCH;
         if (p.expanded_row) return launch_pdl(dispatch_bf16_regs_kernel<true, 1>, grid, block, 0, stream, p);
@@ -1072,10 +1192,10 @@ cudaError_t launch_dispatch_fp8_t(DispatchParams p, int num_sms, cudaStream_t st
         if (warps > kFp8Threads / 32) warps = kFp8Threads / 32;
         if (warps < 2) warps = 2;   // warp 1 writes the metadata
     }
-    // self routing (few tokens, the 16-lane mode): one more CTA, which writes
-    // the layout's counts and offsets
+    // self routing (few tokens, the 16-lane mode): kSelfLayoutCtas more CTAs,
+    // which write the layout's counts and offsets
     const bool self = kLanes == 16 && p.self_route && !p.expanded_row;
-    const dim3 grid(static_cast<unsigned>(items + (self ? 1 : 0))), block(32 * warps);
+    const dim3 grid(static_cast<unsigned>(items + (self ? kSelfLayoutCtas : 0))), block(32 * warps);
     auto kernel = p.expanded_row ? dispatch_fp8_kernel<true, 1, kLanes>
                   : (kLanes == 16 && p.self_route) ? dispatch_fp8_kernel<false, 1, 16, true>
                                                    : dispatch_fp8_kernel<false, 1, kLanes>;
@@ -1112,8 +1232,9 @@ cudaError_t launch_dispatch_fp8(DispatchParams p, cudaStream_t stream) {
     const int want_items = 4 * di.num_sms;
     if (p.T > 0 && static_cast<int64_t>(p.T) * chunks < want_items) {
         // a CTA that derives its rows itself (self_route) pays that latency
-        // once per wave: keep it to one wave of 4 CTAs per SM
-        const int more = p.self_route ? want_items / p.T : (want_items + p.T - 1) / p.T;
+        // once per wave: keep it to one wave of 4 CTAs per SM, the layout
+        // CTAs included
+        const int more = p.self_route ? (want_items - kSelfLayoutCtas) / p.T : (want_items + p.T - 1) / p.T;
         const int max_chunks = (nb + blocks_per_round / 8 - 1) / (blocks_per_round / 8);   // >= one warp's blocks per piece
         chunks = more < max_chunks ? more : max_chunks;
         if (chunks < 1) chunks = 1;

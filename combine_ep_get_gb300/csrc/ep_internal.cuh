@@ -78,7 +78,8 @@ struct DispatchParams {
     int prefetch_items;
     // 1: ep_layout_and_dispatch with few tokens: no layout kernel runs; each
     // CTA derives its token's destination rows from topk_idx, writes that
-    // token's layout rows, and CTA 0 the layout's counts and offsets, into:
+    // token's layout rows, and two extra CTAs the layout's counts and
+    // offsets, into:
     int self_route;
     int32_t* l_num_tokens_per_rank;     // [R]
     int32_t* l_num_tokens_per_node;     // [R / ranks_per_node] or null

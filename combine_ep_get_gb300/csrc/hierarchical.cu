@@ -39,16 +39,19 @@ __device__ __forceinline__ void forward_metadata(const HierParams& p, int t, int
     const float w_l = (lane < K && p.recv_topk_weights && EP_IN(static_cast<int64_t>(t) * K + lane, static_cast<int64_t>(p.T) * K))
                           ? p.topk_weights[static_cast<int64_t>(t) * K + lane]
                           : 0.0f;
+    // the rank of this lane's expert and its index there, once (not per destination)
+    const int e_rank = (e_l >= 0 && e_l < p.E) ? static_cast<int>(e_l) / p.experts_per_rank : -1;
+    const int32_t e_local = static_cast<int32_t>(e_l) - e_rank * p.experts_per_rank;
     for (int r = r0; r < r1; ++r) {
         const int64_t dr = static_cast<int64_t>(t) * p.R + r;
         const int d = EP_IN(dr, static_cast<int64_t>(p.T) * p.R) ? p.dst_row[dr] : -1;   // uniform over the warp
         (void)EP_ROW_OK(d);
         if (d < 0 || d >= p.capacity) continue;
         if (lane < K && EP_IN(static_cast<int64_t>(d) * K + lane, p.capacity * K)) {
-            const bool on = e_l >= 0 && e_l < p.E && static_cast<int>(e_l) / p.experts_per_rank == r;
+            const bool on = e_rank == r;
             if (p.recv_topk_idx)
                 p.recv_topk_idx[static_cast<int64_t>(d) * K + lane] =
-                    on ? static_cast<int32_t>(e_l) - r * p.experts_per_rank : -1;
+                    on ? e_local : -1;
             if (p.recv_topk_weights) p.recv_topk_weights[static_cast<int64_t>(d) * K + lane] = on ? w_l : 0.0f;
         }
         if (lane == 0 && p.recv_src_idx) p.recv_src_idx[d] = t;
