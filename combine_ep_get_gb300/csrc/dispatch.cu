@@ -94,6 +94,15 @@ constexpr int kSmBulkStoreDepth = 4;
 // [lo, hi) of that numbering, N / gridDim rows each, and the consecutive
 // tokens first .. first + count - 1 that hold them; only destinations whose
 // row number falls in [lo, hi) are stored by this CTA.
+// Warps (1 .. kMetaWarps) of a one-token item that write its receive
+// metadata: 3 puts recv_topk_idx, recv_topk_weights and recv_src_idx on
+// warps 1, 2, 3 (the chain of loads and stores a CTA's lifetime waits for
+// is a third as long), 1 puts all three on warp 1.
+#ifndef EP_DISPATCH_META_WARPS
+#define EP_DISPATCH_META_WARPS 3
+#endif
+constexpr int kMetaWarps = EP_DISPATCH_META_WARPS == 1 ? 1 : 3;
+
 struct CtaWork {
     int64_t first, count, stride;
     int lo, hi;
@@ -162,12 +171,15 @@ __device__ void cta_work(const DispatchParams& p, int lane, CtaWork& w) {
 
 // Metadata of token t for every destination row this CTA owns (one warp).
 __device__ __forceinline__ void write_metadata(const DispatchParams& p, int t, int lane,
-                                               const CtaWork& w) {
+                                               const CtaWork& w, int part = -1) {
     const int K = p.K;
-    const int64_t e_l = (lane < K && EP_IN(static_cast<int64_t>(t) * K + lane, static_cast<int64_t>(p.T) * K))
+    // part -1: every array; 0: recv_topk_idx, 1: recv_topk_weights, 2: recv_src_idx only
+    const bool want_idx = part < 0 || part == 0, want_w = part < 0 || part == 1, want_src = part < 0 || part == 2;
+    const int64_t e_l = (lane < K && (want_idx || want_w) &&
+                         EP_IN(static_cast<int64_t>(t) * K + lane, static_cast<int64_t>(p.T) * K))
                             ? p.topk_idx[static_cast<int64_t>(t) * K + lane]
                             : -1;
-    const float w_l = (lane < K && p.recv_topk_weights && EP_IN(static_cast<int64_t>(t) * K + lane, static_cast<int64_t>(p.T) * K))
+    const float w_l = (lane < K && want_w && p.recv_topk_weights && EP_IN(static_cast<int64_t>(t) * K + lane, static_cast<int64_t>(p.T) * K))
                           ? p.topk_weights[static_cast<int64_t>(t) * K + lane]
                           : 0.0f;
     const int tok_off = (w.balanced && EP_IN(t, p.T + 1)) ? p.token_offset[t] : 0;
@@ -193,12 +205,12 @@ __device__ __forceinline__ void write_metadata(const DispatchParams& p, int t, i
             const int rr = rb + src;
             if (lane < K && EP_IN(dd * K + lane, p.capacity * K)) {
                 const bool on = e_rank == rr;
-                if (p.recv_topk_idx)
+                if (want_idx && p.recv_topk_idx)
                     p.recv_topk_idx[dd * K + lane] =
                         on ? e_local : -1;
-                if (p.recv_topk_weights) p.recv_topk_weights[dd * K + lane] = on ? w_l : 0.0f;
+                if (want_w && p.recv_topk_weights) p.recv_topk_weights[dd * K + lane] = on ? w_l : 0.0f;
             }
-            if (lane == 0 && p.recv_src_idx && EP_IN(dd, p.capacity)) p.recv_src_idx[dd] = t;
+            if (want_src && lane == 0 && p.recv_src_idx && EP_IN(dd, p.capacity)) p.recv_src_idx[dd] = t;
         }
     }
 }
@@ -673,7 +685,7 @@ constexpr int kSmGroups = 4;
 // expanded rows (one per valid top-k slot) instead of one row per rank.
 // kGroups > 1 (SM-limited mode): several groups per CTA looping over items.
 // One (token, piece) item of the register path, by one group of 256 threads.
-template <bool kExpanded, bool kSelf>
+template <bool kExpanded, bool kSelf, int kMW = kMetaWarps>
 __device__ __forceinline__ void dispatch_regs_item(const DispatchParams& p, int64_t it, int gtid, int warp_g,
                                                    int lane, bool& cap_bad) {
     const uint32_t row_bytes = static_cast<uint32_t>(p.H) * 2u;
@@ -716,7 +728,7 @@ __device__ __forceinline__ void dispatch_regs_item(const DispatchParams& p, int6
             if (!EP_SELF_EARLY_META && part < 2) load_token_entries(p, t, lane, me_l, mw_l);
             write_metadata_part(p, t, lane, d0, me_l, mw_l, part);
         }
-    } else if (warp_g == 1 && c == 0) {
+    } else if (c == 0 && (kExpanded ? warp_g == 1 : (warp_g >= 1 && warp_g <= kMW))) {
         if (kExpanded) {
             write_expanded_metadata(p, t, lane);
         } else {
@@ -727,7 +739,8 @@ __device__ __forceinline__ void dispatch_regs_item(const DispatchParams& p, int6
             all.lo = INT32_MIN;
             all.hi = INT32_MAX;
             all.balanced = 0;
-            write_metadata(p, t, lane, all);
+            // one array per warp (kMW == 3), or all on warp 1
+            write_metadata(p, t, lane, all, kMW == 3 ? warp_g - 1 : -1);
         }
     }
     for (int base = 0; base < nvec; base += kRegUnroll * kRegThreads) {
@@ -792,7 +805,7 @@ __global__ void __launch_bounds__(kRegThreads * kGroups, kGroups > 1 ? 1 : kSelf
         const int group = static_cast<int>(threadIdx.x) / kRegThreads;
         for (int64_t it = static_cast<int64_t>(blockIdx.x) * kGroups + group; it < n_items;
              it += static_cast<int64_t>(gridDim.x) * kGroups)
-            dispatch_regs_item<kExpanded, false>(p, it, gtid, warp_g, lane, cap_bad);
+            dispatch_regs_item<kExpanded, false, 1>(p, it, gtid, warp_g, lane, cap_bad);
     }
     if (warp_g == 0 && __any_sync(0xffffffffu, cap_bad) && lane == 0) atomicOr(p.status, EP_ERR_CAPACITY);
 }
@@ -829,7 +842,7 @@ constexpr int kFp8Rounds = 2;   // rounds of blocks per item (loads of every rou
 // group of kLanes lanes reduces its block's amax by shuffles, forms the scale
 // and the codes, and stores the code vector (and, its first lane, the scale)
 // to every destination.
-template <bool kExpanded, int kLanes, bool kSelf>
+template <bool kExpanded, int kLanes, bool kSelf, int kMW = kMetaWarps>
 __device__ __forceinline__ void dispatch_fp8_item(const DispatchParams& p, int64_t it, int gtid, int lane,
                                                   int group_warps, bool& cap_bad) {
     constexpr int kVec = 128 / kLanes / 8;                     // 16-byte input vectors per lane per block
@@ -882,7 +895,7 @@ __device__ __forceinline__ void dispatch_fp8_item(const DispatchParams& p, int64
             if (!EP_SELF_EARLY_META && part < 2) load_token_entries(p, t, lane, me_l, mw_l);
             write_metadata_part(p, t, lane, d0, me_l, mw_l, part);
         }
-    } else if (warp_g == 1 && c == 0) {
+    } else if (c == 0 && (kExpanded ? warp_g == 1 : (warp_g >= 1 && warp_g <= kMW))) {
         if (kExpanded) {
             write_expanded_metadata(p, t, lane);
         } else {
@@ -893,7 +906,8 @@ __device__ __forceinline__ void dispatch_fp8_item(const DispatchParams& p, int64
             all.lo = INT32_MIN;
             all.hi = INT32_MAX;
             all.balanced = 0;
-            write_metadata(p, t, lane, all);
+            // one array per warp (kMW == 3), or all on warp 1
+            write_metadata(p, t, lane, all, kMW == 3 ? warp_g - 1 : -1);
         }
     }
     // Many tokens (kLanes 8): codes and scales of every round first, then one
@@ -1073,7 +1087,7 @@ __global__ void __launch_bounds__(kFp8Threads * kGroups,
         const int group = static_cast<int>(threadIdx.x) / kFp8Threads;
         for (int64_t it = static_cast<int64_t>(blockIdx.x) * kGroups + group; it < n_items;
              it += static_cast<int64_t>(gridDim.x) * kGroups)
-            dispatch_fp8_item<kExpanded, kLanes, false>(p, it, gtid, lane, kFp8Threads / 32, cap_bad);
+            dispatch_fp8_item<kExpanded, kLanes, false, 1>(p, it, gtid, lane, kFp8Threads / 32, cap_bad);
     }
     if ((gtid >> 5) == 0 && __any_sync(0xffffffffu, cap_bad) && lane == 0) atomicOr(p.status, EP_ERR_CAPACITY);
 }
@@ -1190,7 +1204,7 @@ cudaError_t launch_dispatch_fp8_t(DispatchParams p, int num_sms, cudaStream_t st
     if (kLanes == 8 && EP_DISPATCH_FP8_FIT_WARPS) {
         warps = (p.chunk_blocks + kFp8Rounds * 4 - 1) / (kFp8Rounds * 4);
         if (warps > kFp8Threads / 32) warps = kFp8Threads / 32;
-        if (warps < 2) warps = 2;   // warp 1 writes the metadata
+        if (warps < 1 + kMetaWarps) warps = 1 + kMetaWarps;   // warps 1 .. kMetaWarps write the metadata
     }
     // self routing (few tokens, the 16-lane mode): kSelfLayoutCtas more CTAs,
     // which write the layout's counts and offsets
