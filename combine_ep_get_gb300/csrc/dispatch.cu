@@ -57,14 +57,30 @@ namespace {
 #ifndef EP_DISPATCH_IMPL
 #define EP_DISPATCH_IMPL 1            // 1: 16-byte register copies, 0: bulk-copy engine
 #endif
+// bf16 register path and L2: the CTAs of the first wave prefetch x into L2
+// before their wait, as many generations of pieces as fit
+// EP_DISPATCH_PREFETCH_L2_BYTES (all of x for DeepSeek-V3 sizes: 59 MB read
+// while the layout kernel leaves HBM idle), with the evict-last policy; the
+// receive rows are stored evict-first, so the 311 MB of writes stream past
+// the prefetched rows instead of evicting them; a read piece of x goes back
+// to the normal priority.  DS-V3 layout + dispatch 65.6 -> 61.1 us.
 #ifndef EP_DISPATCH_STORE_CS
-#define EP_DISPATCH_STORE_CS 0        // register path: streaming (.cs) stores
+#define EP_DISPATCH_STORE_CS 2        // register path: 0 plain, 1 streaming (.cs), 2 L2 evict-first stores
+#endif
+#ifndef EP_DISPATCH_PREFETCH_EVICT_LAST
+#define EP_DISPATCH_PREFETCH_EVICT_LAST 1
+#endif
+#ifndef EP_DISPATCH_PREFETCH_L2_BYTES
+#define EP_DISPATCH_PREFETCH_L2_BYTES (64ll << 20)
+#endif
+#ifndef EP_DISPATCH_PREFETCH_MAX_GENS
+#define EP_DISPATCH_PREFETCH_MAX_GENS 16
 #endif
 #ifndef EP_DISPATCH_FP8_MIN_BLOCKS
 #define EP_DISPATCH_FP8_MIN_BLOCKS 4      // FP8 path: __launch_bounds__ minimum resident CTAs per SM
 #endif
 #ifndef EP_DISPATCH_PREFETCH
-#define EP_DISPATCH_PREFETCH 2   // x pieces a CTA of the first wave prefetches into L2 before its wait
+#define EP_DISPATCH_PREFETCH 2   // FP8: x pieces a CTA of the first wave prefetches into L2 before its wait
 #endif
 #ifndef EP_DISPATCH_FP8_WIDE_MIN_BLOCKS
 #define EP_DISPATCH_FP8_WIDE_MIN_BLOCKS 5   // same, many-token rank-row mode (fits 48 registers unspilled)
@@ -362,15 +378,21 @@ __device__ __forceinline__ void write_expanded_metadata(const DispatchParams& p,
 // the same slot (b + j * prefetch_ctas).  A prefetch only fills L2, the
 // coherence point, and x is still read after the wait, so a producer of x
 // that is still running cannot make the kernel read stale data.
-__device__ __forceinline__ void prefetch_l2(const void* ptr, uint32_t bytes) {
-    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(ptr), "r"(bytes) : "memory");
+__device__ __forceinline__ void prefetch_l2(const void* ptr, uint32_t bytes, bool evict_last = false) {
+    if (evict_last)
+        asm volatile("cp.async.bulk.prefetch.L2.global.L2::cache_hint [%0], %1, %2;" ::"l"(ptr), "r"(bytes),
+                     "l"(l2_policy_evict_last())
+                     : "memory");
+    else
+        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(ptr), "r"(bytes) : "memory");
 }
 
 // FP8 (latency-bound): later CTAs keep the distance, CTA b >= prefetch_ctas
 // fetching the piece of item b + (prefetch_items - 1) * prefetch_ctas, one
 // generation ahead (DS-V3 39.9 -> 38.1 us).  The bf16 copy, bound by HBM
-// writes, lost 2-6% to the extra L2 traffic, so there only the first wave
-// prefetches.
+// writes, lost 2-6% to that extra L2 traffic, so there only the first wave
+// prefetches: every generation that fits the L2 budget, evict-last (see
+// EP_DISPATCH_PREFETCH_EVICT_LAST).
 template <bool kFp8>
 __device__ __forceinline__ void prefetch_x(const DispatchParams& p) {
     if (threadIdx.x != 0 || p.prefetch_items <= 0) return;
@@ -384,7 +406,8 @@ __device__ __forceinline__ void prefetch_x(const DispatchParams& p) {
         if (it >= n_items) return;
         const int t = static_cast<int>(it / p.chunks);
         const uint32_t off = static_cast<uint32_t>(it - static_cast<int64_t>(t) * p.chunks) * piece;
-        prefetch_l2(p.x + static_cast<int64_t>(t) * row_bytes + off, min(piece, row_bytes - off));
+        prefetch_l2(p.x + static_cast<int64_t>(t) * row_bytes + off, min(piece, row_bytes - off),
+                    !kFp8 && EP_DISPATCH_PREFETCH_EVICT_LAST);
     }
 }
 
@@ -697,6 +720,9 @@ __device__ __forceinline__ void dispatch_regs_item(const DispatchParams& p, int6
     const int64_t src_off = static_cast<int64_t>(t) * row_bytes + off;   // in x (T rows)
     const int64_t x_bytes = static_cast<int64_t>(p.T) * row_bytes, rx_bytes = p.capacity * row_bytes;
     const uint8_t* src = p.x + src_off;
+#if EP_DISPATCH_STORE_CS == 2
+    const uint64_t store_pol = l2_policy_evict_first();
+#endif
     // this thread's loads and the warp's destination rows, all in flight together
     uint4 u[kRegUnroll];
 #pragma unroll
@@ -768,8 +794,10 @@ __device__ __forceinline__ void dispatch_regs_item(const DispatchParams& p, int6
                 for (int k = 0; k < kRegUnroll; ++k) {
                     const int v = base + gtid + k * kRegThreads;
                     if (v < nvec && EP_IN_BYTES(dst_off + static_cast<int64_t>(v) * 16, 16, rx_bytes)) {
-#if EP_DISPATCH_STORE_CS
+#if EP_DISPATCH_STORE_CS == 1
                         st_cs_v4(dst + static_cast<size_t>(v) * 16, u[k]);
+#elif EP_DISPATCH_STORE_CS == 2
+                        st_v4_hint(dst + static_cast<size_t>(v) * 16, u[k], store_pol);
 #else
                         st_v4(dst + static_cast<size_t>(v) * 16, u[k]);
 #endif
@@ -777,6 +805,19 @@ __device__ __forceinline__ void dispatch_regs_item(const DispatchParams& p, int6
                 }
             }
         }
+#if EP_DISPATCH_PREFETCH_EVICT_LAST
+        // These x vectors are read: the 128-byte lines they start (whole
+        // lines inside x only) go back to the normal eviction priority, so
+        // that x does not outlive the kernel in L2 ahead of other data.
+#pragma unroll
+        for (int k = 0; k < kRegUnroll; ++k) {
+            const int v = base + gtid + k * kRegThreads;
+            const uint8_t* a = src + static_cast<size_t>(v) * 16;
+            if (v < nvec && (reinterpret_cast<uintptr_t>(a) & 127u) == 0 &&
+                src_off + static_cast<int64_t>(v) * 16 + 128 <= x_bytes)
+                l2_priority_normal(a);
+        }
+#endif
     }
 }
 
@@ -1176,10 +1217,19 @@ cudaError_t launch_dispatch_bf16(DispatchParams p, cudaStream_t stream) {
             const dim3 grid(static_cast<unsigned>(g)), block(kRegThreads * kSmGroups);
             return launch_pdl(dispatch_bf16_regs_kernel<true, kSmGroups>, grid, block, 0, stream, p);
         }
-        // self routing: one more CTA, which writes the layout's counts and offsets
+        // self routing: kSelfLayoutCtas more CTAs, which write the layout's counts and offsets
         const dim3 grid(static_cast<unsigned>(items + (p.self_route ? kSelfLayoutCtas : 0))), block(kRegThreads);
         p.prefetch_ctas = di.num_sms * 6;   // the first wave (6 CTAs per SM)
-        p.prefetch_items = EP_DISPATCH_PREFETCH;
+        // the first wave prefetches the pieces of every generation while they
+        // fit the L2 budget (all of x on DeepSeek-V3-sized inputs)
+        {
+            const int64_t budget_items = static_cast<int64_t>(EP_DISPATCH_PREFETCH_L2_BYTES) / cb;
+            const int64_t n_pf = items < budget_items ? items : budget_items;
+            int64_t gens = n_pf / p.prefetch_ctas;
+            if (gens < 1) gens = 1;
+            if (gens > EP_DISPATCH_PREFETCH_MAX_GENS) gens = EP_DISPATCH_PREFETCH_MAX_GENS;
+            p.prefetch_items = static_cast<int>(gens);
+        }
         if (p.expanded_row) return launch_pdl(dispatch_bf16_regs_kernel<true, 1>, grid, block, 0, stream, p);
         if (p.self_route) return launch_pdl(dispatch_bf16_regs_kernel<false, 1, true>, grid, block, 0, stream, p);
         return launch_pdl(dispatch_bf16_regs_kernel<false, 1>, grid, block, 0, stream, p);

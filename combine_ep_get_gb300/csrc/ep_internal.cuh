@@ -324,6 +324,25 @@ __device__ __forceinline__ uint64_t l2_policy_evict_first() {
     return pol;
 }
 
+// L2 policy that keeps lines ahead of normal and evict-first ones.
+__device__ __forceinline__ uint64_t l2_policy_evict_last() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
+// Back to the normal eviction priority for the 128-byte L2 line at p.
+__device__ __forceinline__ void l2_priority_normal(const void* p) {
+    asm volatile("applypriority.global.L2::evict_normal [%0], 128;" ::"l"(p) : "memory");
+}
+
+// 16-byte store with an L2 cache policy.
+__device__ __forceinline__ void st_v4_hint(void* p, uint4 v, uint64_t policy) {
+    asm volatile("st.global.L2::cache_hint.v4.u32 [%0], {%1, %2, %3, %4}, %5;" ::"l"(p), "r"(v.x), "r"(v.y),
+                 "r"(v.z), "r"(v.w), "l"(policy)
+                 : "memory");
+}
+
 // Bulk copy shared -> global with an L2 cache policy.
 __device__ __forceinline__ void bulk_store_evict_first(void* dst, const void* src_smem, uint32_t bytes,
                                                        uint64_t policy) {
