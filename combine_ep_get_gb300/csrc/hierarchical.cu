@@ -30,31 +30,43 @@ constexpr int kFwdUnroll = 4;
 constexpr int kRedThreads = 128;
 constexpr int kRedBatch = 4;
 
-// Metadata of token t's rows in ranks [r0, r1) (one warp, lane k < K).
-__device__ __forceinline__ void forward_metadata(const HierParams& p, int t, int r0, int r1, int lane) {
+// One of the receive-metadata arrays of token t's rows on ranks [r0, r1)
+// (part 0: recv_topk_idx, 1: recv_topk_weights, 2: recv_src_idx), one warp
+// (lane k < K).  The rows of up to 32 ranks are loaded at once, one per lane.
+__device__ __forceinline__ void forward_metadata(const HierParams& p, int t, int r0, int r1, int lane, int part) {
     const int K = p.K;
-    const int64_t e_l = (lane < K && EP_IN(static_cast<int64_t>(t) * K + lane, static_cast<int64_t>(p.T) * K))
-                            ? p.topk_idx[static_cast<int64_t>(t) * K + lane]
-                            : -1;
-    const float w_l = (lane < K && p.recv_topk_weights && EP_IN(static_cast<int64_t>(t) * K + lane, static_cast<int64_t>(p.T) * K))
-                          ? p.topk_weights[static_cast<int64_t>(t) * K + lane]
-                          : 0.0f;
+    int64_t e_l = -1;
+    float w_l = 0.0f;
+    if (part < 2 && lane < K && EP_IN(static_cast<int64_t>(t) * K + lane, static_cast<int64_t>(p.T) * K)) {
+        e_l = p.topk_idx[static_cast<int64_t>(t) * K + lane];
+        if (part == 1 && p.recv_topk_weights) w_l = p.topk_weights[static_cast<int64_t>(t) * K + lane];
+    }
     // the rank of this lane's expert and its index there, once (not per destination)
     const int e_rank = (e_l >= 0 && e_l < p.E) ? static_cast<int>(e_l) / p.experts_per_rank : -1;
     const int32_t e_local = static_cast<int32_t>(e_l) - e_rank * p.experts_per_rank;
-    for (int r = r0; r < r1; ++r) {
-        const int64_t dr = static_cast<int64_t>(t) * p.R + r;
-        const int d = EP_IN(dr, static_cast<int64_t>(p.T) * p.R) ? p.dst_row[dr] : -1;   // uniform over the warp
+    for (int rb = r0; rb < r1; rb += 32) {
+        const int64_t dr = static_cast<int64_t>(t) * p.R + rb + lane;
+        const int d = (rb + lane < r1 && EP_IN(dr, static_cast<int64_t>(p.T) * p.R)) ? p.dst_row[dr] : -1;
         (void)EP_ROW_OK(d);
-        if (d < 0 || d >= p.capacity) continue;
-        if (lane < K && EP_IN(static_cast<int64_t>(d) * K + lane, p.capacity * K)) {
-            const bool on = e_rank == r;
-            if (p.recv_topk_idx)
-                p.recv_topk_idx[static_cast<int64_t>(d) * K + lane] =
-                    on ? e_local : -1;
-            if (p.recv_topk_weights) p.recv_topk_weights[static_cast<int64_t>(d) * K + lane] = on ? w_l : 0.0f;
+        unsigned m = __ballot_sync(0xffffffffu, d >= 0 && d < p.capacity);
+        while (m) {
+            const int sl = __ffs(m) - 1;
+            m &= m - 1;
+            const int64_t dd = __shfl_sync(0xffffffffu, d, sl);
+            const int r = rb + sl;
+            if (part < 2) {
+                if (lane < K && EP_IN(dd * K + lane, p.capacity * K)) {
+                    const bool on = e_rank == r;
+                    if (part == 0) {
+                        if (p.recv_topk_idx) p.recv_topk_idx[dd * K + lane] = on ? e_local : -1;
+                    } else if (p.recv_topk_weights) {
+                        p.recv_topk_weights[dd * K + lane] = on ? w_l : 0.0f;
+                    }
+                }
+            } else if (lane == 0 && p.recv_src_idx) {
+                p.recv_src_idx[dd] = t;
+            }
         }
-        if (lane == 0 && p.recv_src_idx) p.recv_src_idx[d] = t;
     }
 }
 
@@ -74,9 +86,13 @@ __global__ void __launch_bounds__(kFwdThreads, 6) forward_scaleup_kernel(const H
     bool cap_bad = false;
     const int64_t row_in = static_cast<int64_t>(p.node_capacity) * row_bytes;
     const int64_t row_out = p.capacity * row_bytes;
+    const uint64_t store_pol = l2_policy_evict_first();   // the rank rows stream out past L2
+    // the token's node rows of the first 32 nodes, one per lane, in one load
+    const int64_t nr0 = static_cast<int64_t>(t) * p.num_nodes, n_nr = static_cast<int64_t>(p.T) * p.num_nodes;
+    const int j_lane = (lane < p.num_nodes && EP_IN(nr0 + lane, n_nr)) ? p.node_row[nr0 + lane] : -1;
     for (int n = 0; n < p.num_nodes; ++n) {
-        const int64_t nr = static_cast<int64_t>(t) * p.num_nodes + n;
-        const int j = EP_IN(nr, static_cast<int64_t>(p.T) * p.num_nodes) ? p.node_row[nr] : -1;   // uniform over the CTA
+        const int j = n < 32 ? __shfl_sync(0xffffffffu, j_lane, n)
+                             : (EP_IN(nr0 + n, n_nr) ? p.node_row[nr0 + n] : -1);   // uniform over the CTA
         (void)EP_ROW_OK(j);
         if (j < 0) continue;
         if (j >= p.node_capacity) {
@@ -84,19 +100,25 @@ __global__ void __launch_bounds__(kFwdThreads, 6) forward_scaleup_kernel(const H
             continue;
         }
         const int r0 = n * rpn;
-        if (c == 0 && warp == 1) forward_metadata(p, t, r0, r0 + rpn, lane);
-        if (kFp8 && c == 0 && warp == 2 && p.recv_sf) {
+        // receive metadata: one array per warp (1, 2, 3); FP8 scales: warp 4
+        if (c == 0 && warp >= 1 && warp <= 3) forward_metadata(p, t, r0, r0 + rpn, lane, warp - 1);
+        if (kFp8 && c == 0 && warp == 4 && p.recv_sf) {
             const int64_t sf_n = p.sf_col_major ? static_cast<int64_t>(nb) * p.sf_stride : p.capacity * nb;
-            for (int r = r0; r < r0 + rpn; ++r) {
-                const int64_t dr = static_cast<int64_t>(t) * p.R + r;
-                const int d = EP_IN(dr, static_cast<int64_t>(p.T) * p.R) ? p.dst_row[dr] : -1;
-                if (d < 0 || d >= p.capacity) continue;
-                for (int b = lane; b < nb; b += 32) {
-                    if (!EP_IN(static_cast<int64_t>(j) * nb + b, static_cast<int64_t>(p.node_capacity) * nb)) continue;
-                    const float s = p.node_sf[static_cast<int64_t>(j) * nb + b];
-                    const int64_t si = p.sf_col_major ? static_cast<int64_t>(b) * p.sf_stride + d
-                                                      : static_cast<int64_t>(d) * nb + b;
-                    if (EP_IN(si, sf_n)) p.recv_sf[si] = s;
+            for (int rb = r0; rb < r0 + rpn; rb += 32) {
+                const int64_t dr = static_cast<int64_t>(t) * p.R + rb + lane;
+                const int d_l = (rb + lane < r0 + rpn && EP_IN(dr, static_cast<int64_t>(p.T) * p.R)) ? p.dst_row[dr] : -1;
+                unsigned m = __ballot_sync(0xffffffffu, d_l >= 0 && d_l < p.capacity);
+                while (m) {
+                    const int sl = __ffs(m) - 1;
+                    m &= m - 1;
+                    const int d = __shfl_sync(0xffffffffu, d_l, sl);
+                    for (int b = lane; b < nb; b += 32) {
+                        if (!EP_IN(static_cast<int64_t>(j) * nb + b, static_cast<int64_t>(p.node_capacity) * nb)) continue;
+                        const float s = p.node_sf[static_cast<int64_t>(j) * nb + b];
+                        const int64_t si = p.sf_col_major ? static_cast<int64_t>(b) * p.sf_stride + d
+                                                          : static_cast<int64_t>(d) * nb + b;
+                        if (EP_IN(si, sf_n)) p.recv_sf[si] = s;
+                    }
                 }
             }
         }
@@ -127,7 +149,7 @@ __global__ void __launch_bounds__(kFwdThreads, 6) forward_scaleup_kernel(const H
                     for (int k = 0; k < kFwdUnroll; ++k) {
                         const int v = base + gtid + k * kFwdThreads;
                         if (v < nvec && EP_IN_BYTES(dst_off + static_cast<int64_t>(v) * 16, 16, row_out))
-                            st_v4(dst + static_cast<size_t>(v) * 16, u[k]);
+                            st_v4_hint(dst + static_cast<size_t>(v) * 16, u[k], store_pol);
                     }
                 }
             }
