@@ -2,12 +2,54 @@
 // launches.  Declarations and the full contract are in include/ep_get.h.
 #include <algorithm>
 #include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <cxxabi.h>
 #include <mutex>
 #include <string>
 
 #include "ep_internal.cuh"
 
 namespace epg {
+
+bool debug_enabled() {
+    static const bool on = [] {
+        const char* v = std::getenv("EP_GET_DEBUG");
+        return v != nullptr && v[0] != '\0' && std::strcmp(v, "0") != 0;
+    }();
+    return on;
+}
+
+void debug_log(const char* fmt, ...) {
+    char line[512];
+    va_list ap;
+    va_start(ap, fmt);
+    std::vsnprintf(line, sizeof(line), fmt, ap);
+    va_end(ap);
+    std::fprintf(stderr, "[ep_get] %s\n", line);
+}
+
+void debug_launch(const void* kernel, dim3 grid, dim3 block, size_t smem, int cluster) {
+    const char* name = nullptr;
+    if (cudaFuncGetName(&name, kernel) != cudaSuccess || name == nullptr) {
+        cudaGetLastError();
+        name = "?";
+    }
+    int st = 0;
+    char* readable = abi::__cxa_demangle(name, nullptr, nullptr, &st);
+    debug_log("launch %s grid (%u, %u, %u) block (%u, %u, %u) smem %zu cluster %d",
+              (st == 0 && readable) ? readable : name, grid.x, grid.y, grid.z, block.x, block.y, block.z, smem,
+              cluster);
+    std::free(readable);
+}
+
+// A status a host check returns, logged (with the check's line) when it is an error.
+ep_status_t debug_ret(const char* fn, int line, ep_status_t s) {
+    if (s != EP_OK && debug_enabled()) debug_log("%s: %s (api.cu:%d)", fn, ep_status_string(s), line);
+    return s;
+}
 
 const DeviceInfo& device_info() {
     constexpr int kMaxDevices = 64;
@@ -30,6 +72,8 @@ const DeviceInfo& device_info() {
 
 }  // namespace epg
 
+#define EP_RET(s) ::epg::debug_ret(__func__, __LINE__, (s))
+
 namespace {
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -37,12 +81,12 @@ inline bool ok_ptr(const void* p) { return p != nullptr && aligned16(p); }
 
 // Shape checks shared by the three calls.
 ep_status_t check_shape(int T, int K, int E, int R) {
-    if (T < 0 || K < 1 || E < 1 || R < 1) return EP_ERR_INVALID_ARG;
-    if (K > EP_MAX_TOPK || R > EP_MAX_RANKS || E > EP_MAX_EXPERTS) return EP_ERR_UNSUPPORTED;
-    if (E % R != 0) return EP_ERR_INVALID_ARG;
-    if (E / R > EP_MAX_EXPERTS_PER_RANK) return EP_ERR_UNSUPPORTED;
+    if (T < 0 || K < 1 || E < 1 || R < 1) return EP_RET(EP_ERR_INVALID_ARG);
+    if (K > EP_MAX_TOPK || R > EP_MAX_RANKS || E > EP_MAX_EXPERTS) return EP_RET(EP_ERR_UNSUPPORTED);
+    if (E % R != 0) return EP_RET(EP_ERR_INVALID_ARG);
+    if (E / R > EP_MAX_EXPERTS_PER_RANK) return EP_RET(EP_ERR_UNSUPPORTED);
     if (static_cast<int64_t>(T) * R > INT32_MAX || static_cast<int64_t>(T) * K > INT32_MAX)
-        return EP_ERR_UNSUPPORTED;
+        return EP_RET(EP_ERR_UNSUPPORTED);
     return EP_OK;
 }
 
@@ -102,32 +146,32 @@ namespace epg {
 ep_status_t layout_params(const int64_t* topk_idx, int T, int K, int E, int R, int ranks_per_node,
                           int expert_alignment, const ep_layout_t* out, void* workspace, size_t ws_bytes,
                           int32_t* d_status, bool check_workspace, LayoutParams& p) {
-    if (!out || !d_status) return EP_ERR_INVALID_ARG;
+    if (!out || !d_status) return EP_RET(EP_ERR_INVALID_ARG);
     ep_status_t s = check_shape(T, K, E, R);
     if (s != EP_OK) return s;
     if (ranks_per_node < 0 || (ranks_per_node > 0 && R % ranks_per_node != 0))
-        return EP_ERR_INVALID_ARG;
-    if (expert_alignment < 1) return EP_ERR_INVALID_ARG;
+        return EP_RET(EP_ERR_INVALID_ARG);
+    if (expert_alignment < 1) return EP_RET(EP_ERR_INVALID_ARG);
     if (!ok_ptr(out->num_tokens_per_rank) || !ok_ptr(out->num_tokens_per_expert) ||
         !ok_ptr(out->rank_offset) || !ok_ptr(out->expert_offset))
-        return EP_ERR_INVALID_ARG;
+        return EP_RET(EP_ERR_INVALID_ARG);
     if (T > 0 && (!ok_ptr(topk_idx) || !ok_ptr(out->is_token_in_rank) || !ok_ptr(out->dst_row)))
-        return EP_ERR_INVALID_ARG;
-    if (out->num_tokens_per_node && !aligned16(out->num_tokens_per_node)) return EP_ERR_INVALID_ARG;
-    if (out->src_dst_count && (!aligned16(out->src_dst_count) || T % R != 0)) return EP_ERR_INVALID_ARG;
-    if (out->token_offset && !aligned16(out->token_offset)) return EP_ERR_INVALID_ARG;
-    if (out->expanded_row && !aligned16(out->expanded_row)) return EP_ERR_INVALID_ARG;
+        return EP_RET(EP_ERR_INVALID_ARG);
+    if (out->num_tokens_per_node && !aligned16(out->num_tokens_per_node)) return EP_RET(EP_ERR_INVALID_ARG);
+    if (out->src_dst_count && (!aligned16(out->src_dst_count) || T % R != 0)) return EP_RET(EP_ERR_INVALID_ARG);
+    if (out->token_offset && !aligned16(out->token_offset)) return EP_RET(EP_ERR_INVALID_ARG);
+    if (out->expanded_row && !aligned16(out->expanded_row)) return EP_RET(EP_ERR_INVALID_ARG);
     // node rows: node_offset and node_row together (node_row may be NULL, an
     // empty array, when there are no tokens)
-    if (out->node_row && !out->node_offset) return EP_ERR_INVALID_ARG;
-    if (out->node_offset && !out->node_row && T > 0) return EP_ERR_INVALID_ARG;
+    if (out->node_row && !out->node_offset) return EP_RET(EP_ERR_INVALID_ARG);
+    if (out->node_offset && !out->node_row && T > 0) return EP_RET(EP_ERR_INVALID_ARG);
     if (out->node_offset && (ranks_per_node <= 0 || !ok_ptr(out->num_tokens_per_node) ||
                              !aligned16(out->node_row) || !aligned16(out->node_offset)))
-        return EP_ERR_INVALID_ARG;
+        return EP_RET(EP_ERR_INVALID_ARG);
     const int nodes_ws = ranks_per_node > 0 ? R / ranks_per_node : 0;
     const epg::LayoutWorkspace w = epg::layout_workspace(T, E, R, nodes_ws);
     if (!check_workspace) return EP_OK;
-    if (!ok_ptr(workspace) || ws_bytes < w.total) return EP_ERR_INVALID_ARG;
+    if (!ok_ptr(workspace) || ws_bytes < w.total) return EP_RET(EP_ERR_INVALID_ARG);
 
     p = epg::LayoutParams{};
     p.topk_idx = topk_idx;
@@ -168,16 +212,19 @@ extern "C" {
 ep_status_t ep_get_layout(const int64_t* topk_idx, int T, int K, int E, int R, int ranks_per_node,
                           int expert_alignment, const ep_layout_t* out, void* workspace,
                           size_t ws_bytes, int32_t* d_status, void* cuda_stream) {
+    EP_DEBUG("ep_get_layout: T=%d K=%d E=%d R=%d ranks_per_node=%d alignment=%d%s%s",
+             T, K, E, R, ranks_per_node, expert_alignment, out && out->expanded_row ? " expanded_row" : "",
+             out && out->node_row ? " node_row" : "");
     epg::LayoutParams p{};
     const ep_status_t s = epg::layout_params(topk_idx, T, K, E, R, ranks_per_node, expert_alignment, out, workspace,
                                              ws_bytes, d_status, true, p);
     if (s != EP_OK) return s;
     const cudaStream_t stream = static_cast<cudaStream_t>(cuda_stream);
-    if (epg::launch_layout(p, stream) != cudaSuccess) return EP_ERR_CUDA;
+    if (epg::launch_layout(p, stream) != cudaSuccess) return EP_RET(EP_ERR_CUDA);
     // no tokens: the node-row kernels are not launched, node_offset is all zero
     if (T == 0 && out->node_offset &&
         cudaMemsetAsync(out->node_offset, 0, sizeof(int32_t) * (R / ranks_per_node + 1), stream) != cudaSuccess)
-        return EP_ERR_CUDA;
+        return EP_RET(EP_ERR_CUDA);
     return EP_OK;
 }
 
@@ -193,29 +240,29 @@ ep_status_t dispatch_impl(const void* x, const int64_t* topk_idx, const float* t
                           void* recv_x, float* recv_sf, int sf_col_major, int32_t* recv_topk_idx,
                           float* recv_topk_weights, int32_t* recv_src_idx, int num_sms, int32_t* d_status,
                           void* cuda_stream, const epg::LayoutParams* self_layout) {
-    if (!layout || !d_status || num_sms < 0) return EP_ERR_INVALID_ARG;
+    if (!layout || !d_status || num_sms < 0) return EP_RET(EP_ERR_INVALID_ARG);
     ep_status_t s = check_shape(T, K, E, R);
     if (s != EP_OK) return s;
-    if (H < 1) return EP_ERR_INVALID_ARG;
+    if (H < 1) return EP_RET(EP_ERR_INVALID_ARG);
     if (out_dtype == EP_BF16) {
-        if (H % 8 != 0) return EP_ERR_INVALID_ARG;
+        if (H % 8 != 0) return EP_RET(EP_ERR_INVALID_ARG);
     } else if (out_dtype == EP_FP8_E4M3) {
-        if (H % 128 != 0) return EP_ERR_INVALID_ARG;
-        if (H > 65536) return EP_ERR_UNSUPPORTED;
+        if (H % 128 != 0) return EP_RET(EP_ERR_INVALID_ARG);
+        if (H > 65536) return EP_RET(EP_ERR_UNSUPPORTED);
     } else {
-        return EP_ERR_INVALID_ARG;
+        return EP_RET(EP_ERR_INVALID_ARG);
     }
-    if (recv_capacity < 0 || recv_capacity > INT32_MAX) return EP_ERR_INVALID_ARG;
-    if (static_cast<int64_t>(H) * 2 > UINT32_MAX / 2) return EP_ERR_UNSUPPORTED;
+    if (recv_capacity < 0 || recv_capacity > INT32_MAX) return EP_RET(EP_ERR_INVALID_ARG);
+    if (static_cast<int64_t>(H) * 2 > UINT32_MAX / 2) return EP_RET(EP_ERR_UNSUPPORTED);
     if (T > 0 && (!ok_ptr(x) || !ok_ptr(topk_idx) || !ok_ptr(layout->dst_row)))
-        return EP_ERR_INVALID_ARG;
-    if (recv_capacity > 0 && !ok_ptr(recv_x)) return EP_ERR_INVALID_ARG;
-    if (out_dtype == EP_FP8_E4M3 && recv_capacity > 0 && !ok_ptr(recv_sf)) return EP_ERR_INVALID_ARG;
-    if (recv_topk_weights && T > 0 && !ok_ptr(topk_weights)) return EP_ERR_INVALID_ARG;
+        return EP_RET(EP_ERR_INVALID_ARG);
+    if (recv_capacity > 0 && !ok_ptr(recv_x)) return EP_RET(EP_ERR_INVALID_ARG);
+    if (out_dtype == EP_FP8_E4M3 && recv_capacity > 0 && !ok_ptr(recv_sf)) return EP_RET(EP_ERR_INVALID_ARG);
+    if (recv_topk_weights && T > 0 && !ok_ptr(topk_weights)) return EP_RET(EP_ERR_INVALID_ARG);
     if ((recv_topk_idx && !aligned16(recv_topk_idx)) ||
         (recv_topk_weights && !aligned16(recv_topk_weights)) ||
         (recv_src_idx && !aligned16(recv_src_idx)))
-        return EP_ERR_INVALID_ARG;
+        return EP_RET(EP_ERR_INVALID_ARG);
     if (T == 0) return EP_OK;
 
     epg::DispatchParams p{};
@@ -258,7 +305,7 @@ ep_status_t dispatch_impl(const void* x, const int64_t* topk_idx, const float* t
     cudaStream_t st = static_cast<cudaStream_t>(cuda_stream);
     const cudaError_t e = out_dtype == EP_BF16 ? epg::launch_dispatch_bf16(p, st)
                                                : epg::launch_dispatch_fp8(p, st);
-    return e == cudaSuccess ? EP_OK : EP_ERR_CUDA;
+    return e == cudaSuccess ? EP_OK : EP_RET(EP_ERR_CUDA);
 }
 
 }  // namespace
@@ -270,6 +317,9 @@ ep_status_t ep_dispatch(const void* x, const int64_t* topk_idx, const float* top
                         int64_t recv_capacity, void* recv_x, float* recv_sf, int sf_col_major,
                         int32_t* recv_topk_idx, float* recv_topk_weights, int32_t* recv_src_idx,
                         int num_sms, int32_t* d_status, void* cuda_stream) {
+    EP_DEBUG("ep_dispatch: T=%d H=%d K=%d E=%d R=%d %s capacity=%lld sf_col_major=%d num_sms=%d",
+             T, H, K, E, R, out_dtype == EP_FP8_E4M3 ? "fp8" : "bf16", static_cast<long long>(recv_capacity),
+             sf_col_major, num_sms);
     return dispatch_impl(x, topk_idx, topk_weights, T, H, K, E, R, layout, out_dtype, recv_capacity, recv_x, recv_sf,
                          sf_col_major, recv_topk_idx, recv_topk_weights, recv_src_idx, num_sms, d_status, cuda_stream,
                          nullptr);
@@ -281,22 +331,25 @@ ep_status_t ep_layout_and_dispatch(const void* x, const int64_t* topk_idx, const
                                    int64_t recv_capacity, void* recv_x, float* recv_sf, int sf_col_major,
                                    int32_t* recv_topk_idx, float* recv_topk_weights, int32_t* recv_src_idx,
                                    int32_t* d_status, void* cuda_stream) {
+    EP_DEBUG("ep_layout_and_dispatch: T=%d H=%d K=%d E=%d R=%d ranks_per_node=%d alignment=%d %s capacity=%lld",
+             T, H, K, E, R, ranks_per_node, expert_alignment, out_dtype == EP_FP8_E4M3 ? "fp8" : "bf16",
+             static_cast<long long>(recv_capacity));
     // the dispatch's host checks first, so that a rejected call launches nothing
-    if (!layout || !d_status) return EP_ERR_INVALID_ARG;
+    if (!layout || !d_status) return EP_RET(EP_ERR_INVALID_ARG);
     ep_status_t s = check_shape(T, K, E, R);
     if (s != EP_OK) return s;
-    if (H < 1 || (out_dtype != EP_BF16 && out_dtype != EP_FP8_E4M3)) return EP_ERR_INVALID_ARG;
-    if (H % (out_dtype == EP_BF16 ? 8 : 128) != 0) return EP_ERR_INVALID_ARG;
-    if (out_dtype == EP_FP8_E4M3 && H > 65536) return EP_ERR_UNSUPPORTED;
-    if (recv_capacity < 0 || recv_capacity > INT32_MAX) return EP_ERR_INVALID_ARG;
-    if (static_cast<int64_t>(H) * 2 > UINT32_MAX / 2) return EP_ERR_UNSUPPORTED;
-    if (T > 0 && (!ok_ptr(x) || !ok_ptr(topk_idx))) return EP_ERR_INVALID_ARG;
-    if (recv_capacity > 0 && !ok_ptr(recv_x)) return EP_ERR_INVALID_ARG;
-    if (out_dtype == EP_FP8_E4M3 && recv_capacity > 0 && !ok_ptr(recv_sf)) return EP_ERR_INVALID_ARG;
-    if (recv_topk_weights && T > 0 && !ok_ptr(topk_weights)) return EP_ERR_INVALID_ARG;
+    if (H < 1 || (out_dtype != EP_BF16 && out_dtype != EP_FP8_E4M3)) return EP_RET(EP_ERR_INVALID_ARG);
+    if (H % (out_dtype == EP_BF16 ? 8 : 128) != 0) return EP_RET(EP_ERR_INVALID_ARG);
+    if (out_dtype == EP_FP8_E4M3 && H > 65536) return EP_RET(EP_ERR_UNSUPPORTED);
+    if (recv_capacity < 0 || recv_capacity > INT32_MAX) return EP_RET(EP_ERR_INVALID_ARG);
+    if (static_cast<int64_t>(H) * 2 > UINT32_MAX / 2) return EP_RET(EP_ERR_UNSUPPORTED);
+    if (T > 0 && (!ok_ptr(x) || !ok_ptr(topk_idx))) return EP_RET(EP_ERR_INVALID_ARG);
+    if (recv_capacity > 0 && !ok_ptr(recv_x)) return EP_RET(EP_ERR_INVALID_ARG);
+    if (out_dtype == EP_FP8_E4M3 && recv_capacity > 0 && !ok_ptr(recv_sf)) return EP_RET(EP_ERR_INVALID_ARG);
+    if (recv_topk_weights && T > 0 && !ok_ptr(topk_weights)) return EP_RET(EP_ERR_INVALID_ARG);
     if ((recv_topk_idx && !aligned16(recv_topk_idx)) || (recv_topk_weights && !aligned16(recv_topk_weights)) ||
         (recv_src_idx && !aligned16(recv_src_idx)))
-        return EP_ERR_INVALID_ARG;
+        return EP_RET(EP_ERR_INVALID_ARG);
     epg::LayoutParams lp{};
     s = epg::layout_params(topk_idx, T, K, E, R, ranks_per_node, expert_alignment, layout, workspace, ws_bytes,
                            d_status, true, lp);
@@ -306,11 +359,11 @@ ep_status_t ep_layout_and_dispatch(const void* x, const int64_t* topk_idx, const
     const bool one_kernel = T >= 1 && T <= epg::kSelfRouteMaxTokens && R <= 32 && K <= epg::kSelfRouteMaxTopk &&
                             E <= epg::kSelfRouteMaxExperts && !lp.expanded_row && !lp.node_row && !lp.node_offset;
     if (!one_kernel) {
-        if (epg::launch_layout(lp, static_cast<cudaStream_t>(cuda_stream)) != cudaSuccess) return EP_ERR_CUDA;
+        if (epg::launch_layout(lp, static_cast<cudaStream_t>(cuda_stream)) != cudaSuccess) return EP_RET(EP_ERR_CUDA);
         if (T == 0 && layout->node_offset &&
             cudaMemsetAsync(layout->node_offset, 0, sizeof(int32_t) * (R / ranks_per_node + 1),
                             static_cast<cudaStream_t>(cuda_stream)) != cudaSuccess)
-            return EP_ERR_CUDA;
+            return EP_RET(EP_ERR_CUDA);
     }
     return dispatch_impl(x, topk_idx, topk_weights, T, H, K, E, R, layout, out_dtype, recv_capacity, recv_x, recv_sf,
                          sf_col_major, recv_topk_idx, recv_topk_weights, recv_src_idx, 0, d_status, cuda_stream,
@@ -323,33 +376,36 @@ ep_status_t ep_dispatch_hierarchical(const void* x, const int64_t* topk_idx, con
                                      int32_t* node_src_idx, int64_t recv_capacity, void* recv_x, float* recv_sf,
                                      int sf_col_major, int32_t* recv_topk_idx, float* recv_topk_weights,
                                      int32_t* recv_src_idx, int32_t* d_status, void* cuda_stream) {
-    if (!layout || !d_status) return EP_ERR_INVALID_ARG;
+    EP_DEBUG("ep_dispatch_hierarchical: T=%d H=%d K=%d E=%d R=%d ranks_per_node=%d %s node_capacity=%lld capacity=%lld",
+             T, H, K, E, R, rpn, out_dtype == EP_FP8_E4M3 ? "fp8" : "bf16", static_cast<long long>(node_capacity),
+             static_cast<long long>(recv_capacity));
+    if (!layout || !d_status) return EP_RET(EP_ERR_INVALID_ARG);
     ep_status_t s = check_shape(T, K, E, R);
     if (s != EP_OK) return s;
-    if (rpn < 1 || R % rpn != 0) return EP_ERR_INVALID_ARG;
+    if (rpn < 1 || R % rpn != 0) return EP_RET(EP_ERR_INVALID_ARG);
     const bool fp8 = out_dtype == EP_FP8_E4M3;
-    if (H < 1) return EP_ERR_INVALID_ARG;
+    if (H < 1) return EP_RET(EP_ERR_INVALID_ARG);
     if (out_dtype == EP_BF16) {
-        if (H % 8 != 0) return EP_ERR_INVALID_ARG;
+        if (H % 8 != 0) return EP_RET(EP_ERR_INVALID_ARG);
     } else if (fp8) {
-        if (H % 128 != 0) return EP_ERR_INVALID_ARG;
-        if (H > 65536) return EP_ERR_UNSUPPORTED;
+        if (H % 128 != 0) return EP_RET(EP_ERR_INVALID_ARG);
+        if (H > 65536) return EP_RET(EP_ERR_UNSUPPORTED);
     } else {
-        return EP_ERR_INVALID_ARG;
+        return EP_RET(EP_ERR_INVALID_ARG);
     }
-    if (recv_capacity < 0 || recv_capacity > INT32_MAX) return EP_ERR_INVALID_ARG;
-    if (node_capacity < 0 || node_capacity > INT32_MAX) return EP_ERR_INVALID_ARG;
-    if (static_cast<int64_t>(H) * 2 > UINT32_MAX / 2) return EP_ERR_UNSUPPORTED;
+    if (recv_capacity < 0 || recv_capacity > INT32_MAX) return EP_RET(EP_ERR_INVALID_ARG);
+    if (node_capacity < 0 || node_capacity > INT32_MAX) return EP_RET(EP_ERR_INVALID_ARG);
+    if (static_cast<int64_t>(H) * 2 > UINT32_MAX / 2) return EP_RET(EP_ERR_UNSUPPORTED);
     if (T > 0 && (!ok_ptr(x) || !ok_ptr(topk_idx) || !ok_ptr(layout->dst_row) || !ok_ptr(layout->node_row)))
-        return EP_ERR_INVALID_ARG;
-    if (node_capacity > 0 && (!ok_ptr(node_x) || (fp8 && !ok_ptr(node_sf)))) return EP_ERR_INVALID_ARG;
-    if (node_src_idx && !aligned16(node_src_idx)) return EP_ERR_INVALID_ARG;
-    if (recv_capacity > 0 && !ok_ptr(recv_x)) return EP_ERR_INVALID_ARG;
-    if (fp8 && recv_capacity > 0 && !ok_ptr(recv_sf)) return EP_ERR_INVALID_ARG;
-    if (recv_topk_weights && T > 0 && !ok_ptr(topk_weights)) return EP_ERR_INVALID_ARG;
+        return EP_RET(EP_ERR_INVALID_ARG);
+    if (node_capacity > 0 && (!ok_ptr(node_x) || (fp8 && !ok_ptr(node_sf)))) return EP_RET(EP_ERR_INVALID_ARG);
+    if (node_src_idx && !aligned16(node_src_idx)) return EP_RET(EP_ERR_INVALID_ARG);
+    if (recv_capacity > 0 && !ok_ptr(recv_x)) return EP_RET(EP_ERR_INVALID_ARG);
+    if (fp8 && recv_capacity > 0 && !ok_ptr(recv_sf)) return EP_RET(EP_ERR_INVALID_ARG);
+    if (recv_topk_weights && T > 0 && !ok_ptr(topk_weights)) return EP_RET(EP_ERR_INVALID_ARG);
     if ((recv_topk_idx && !aligned16(recv_topk_idx)) || (recv_topk_weights && !aligned16(recv_topk_weights)) ||
         (recv_src_idx && !aligned16(recv_src_idx)))
-        return EP_ERR_INVALID_ARG;
+        return EP_RET(EP_ERR_INVALID_ARG);
     if (T == 0) return EP_OK;
     const int nodes = R / rpn;
     cudaStream_t st = static_cast<cudaStream_t>(cuda_stream);
@@ -374,7 +430,7 @@ ep_status_t ep_dispatch_hierarchical(const void* x, const int64_t* topk_idx, con
     p.recv_src_idx = node_src_idx;
     p.status = d_status;
     cudaError_t e = fp8 ? epg::launch_dispatch_fp8(p, st) : epg::launch_dispatch_bf16(p, st);
-    if (e != cudaSuccess) return EP_ERR_CUDA;
+    if (e != cudaSuccess) return EP_RET(EP_ERR_CUDA);
 
     // stage 2: node rows to the ranks of their node
     epg::HierParams h{};
@@ -402,24 +458,28 @@ ep_status_t ep_dispatch_hierarchical(const void* x, const int64_t* topk_idx, con
     h.recv_topk_weights = recv_topk_weights;
     h.recv_src_idx = recv_src_idx;
     h.status = d_status;
-    return epg::launch_forward_scaleup(h, fp8, st) == cudaSuccess ? EP_OK : EP_ERR_CUDA;
+    return epg::launch_forward_scaleup(h, fp8, st) == cudaSuccess ? EP_OK : EP_RET(EP_ERR_CUDA);
 }
 
 ep_status_t ep_combine_hierarchical(const void* y, int64_t num_y_rows, const int64_t* topk_idx,
                                     const float* topk_weights, int T, int H, int K, int E, int R, int rpn,
                                     const ep_layout_t* layout, int64_t node_capacity, void* node_y, void* out,
                                     int32_t* d_status, void* cuda_stream) {
-    if (!layout || !d_status) return EP_ERR_INVALID_ARG;
+    EP_DEBUG("ep_combine_hierarchical: T=%d H=%d K=%d E=%d R=%d ranks_per_node=%d rows=%lld node_capacity=%lld %s",
+             T, H, K, E, R, rpn, static_cast<long long>(num_y_rows), static_cast<long long>(node_capacity),
+             topk_weights ? "weighted" : "unweighted");
+    if (!layout || !d_status) return EP_RET(EP_ERR_INVALID_ARG);
     ep_status_t s = check_shape(T, K, E, R);
     if (s != EP_OK) return s;
-    if (rpn < 1 || R % rpn != 0) return EP_ERR_INVALID_ARG;
-    if (H < 1 || H % 8 != 0) return EP_ERR_INVALID_ARG;
-    if (num_y_rows < 0 || num_y_rows > INT32_MAX) return EP_ERR_INVALID_ARG;
-    if (node_capacity < 0 || node_capacity > INT32_MAX) return EP_ERR_INVALID_ARG;
-    if (num_y_rows > 0 && !ok_ptr(y)) return EP_ERR_INVALID_ARG;
-    if (node_capacity > 0 && !ok_ptr(node_y)) return EP_ERR_INVALID_ARG;
-    if (T > 0 && (!ok_ptr(out) || !ok_ptr(layout->dst_row) || !ok_ptr(layout->node_row))) return EP_ERR_INVALID_ARG;
-    if (topk_weights && T > 0 && (!ok_ptr(topk_weights) || !ok_ptr(topk_idx))) return EP_ERR_INVALID_ARG;
+    if (rpn < 1 || R % rpn != 0) return EP_RET(EP_ERR_INVALID_ARG);
+    if (H < 1 || H % 8 != 0) return EP_RET(EP_ERR_INVALID_ARG);
+    if (num_y_rows < 0 || num_y_rows > INT32_MAX) return EP_RET(EP_ERR_INVALID_ARG);
+    if (node_capacity < 0 || node_capacity > INT32_MAX) return EP_RET(EP_ERR_INVALID_ARG);
+    if (num_y_rows > 0 && !ok_ptr(y)) return EP_RET(EP_ERR_INVALID_ARG);
+    if (node_capacity > 0 && !ok_ptr(node_y)) return EP_RET(EP_ERR_INVALID_ARG);
+    if (T > 0 && (!ok_ptr(out) || !ok_ptr(layout->dst_row) || !ok_ptr(layout->node_row)))
+        return EP_RET(EP_ERR_INVALID_ARG);
+    if (topk_weights && T > 0 && (!ok_ptr(topk_weights) || !ok_ptr(topk_idx))) return EP_RET(EP_ERR_INVALID_ARG);
     if (T == 0) return EP_OK;
     const int nodes = R / rpn;
     cudaStream_t st = static_cast<cudaStream_t>(cuda_stream);
@@ -443,7 +503,7 @@ ep_status_t ep_combine_hierarchical(const void* y, int64_t num_y_rows, const int
     h.num_y_rows = num_y_rows;
     h.node_y = static_cast<uint8_t*>(node_y);
     h.status = d_status;
-    if (epg::launch_reduce_scaleup(h, topk_weights != nullptr, st) != cudaSuccess) return EP_ERR_CUDA;
+    if (epg::launch_reduce_scaleup(h, topk_weights != nullptr, st) != cudaSuccess) return EP_RET(EP_ERR_CUDA);
 
     // stage 2: the ordinary unweighted combine over the node rows
     epg::CombineParams p{};
@@ -459,21 +519,23 @@ ep_status_t ep_combine_hierarchical(const void* y, int64_t num_y_rows, const int
     p.experts_per_rank = E / R;
     p.out = static_cast<uint8_t*>(out);
     p.status = d_status;
-    return epg::launch_combine(p, false, st) == cudaSuccess ? EP_OK : EP_ERR_CUDA;
+    return epg::launch_combine(p, false, st) == cudaSuccess ? EP_OK : EP_RET(EP_ERR_CUDA);
 }
 
 ep_status_t ep_combine(const void* y, int64_t num_y_rows, const int64_t* topk_idx,
                        const float* topk_weights, int T, int H, int K, int E, int R,
                        const ep_layout_t* layout, void* out, int num_sms, int32_t* d_status,
                        void* cuda_stream) {
-    if (!layout || !d_status || num_sms < 0) return EP_ERR_INVALID_ARG;
+    EP_DEBUG("ep_combine: T=%d H=%d K=%d E=%d R=%d rows=%lld %s num_sms=%d",
+             T, H, K, E, R, static_cast<long long>(num_y_rows), topk_weights ? "weighted" : "unweighted", num_sms);
+    if (!layout || !d_status || num_sms < 0) return EP_RET(EP_ERR_INVALID_ARG);
     ep_status_t s = check_shape(T, K, E, R);
     if (s != EP_OK) return s;
-    if (H < 1 || H % 8 != 0) return EP_ERR_INVALID_ARG;
-    if (num_y_rows < 0 || num_y_rows > INT32_MAX) return EP_ERR_INVALID_ARG;
-    if (num_y_rows > 0 && !ok_ptr(y)) return EP_ERR_INVALID_ARG;
-    if (T > 0 && (!ok_ptr(out) || !ok_ptr(layout->dst_row))) return EP_ERR_INVALID_ARG;
-    if (topk_weights && T > 0 && (!ok_ptr(topk_weights) || !ok_ptr(topk_idx))) return EP_ERR_INVALID_ARG;
+    if (H < 1 || H % 8 != 0) return EP_RET(EP_ERR_INVALID_ARG);
+    if (num_y_rows < 0 || num_y_rows > INT32_MAX) return EP_RET(EP_ERR_INVALID_ARG);
+    if (num_y_rows > 0 && !ok_ptr(y)) return EP_RET(EP_ERR_INVALID_ARG);
+    if (T > 0 && (!ok_ptr(out) || !ok_ptr(layout->dst_row))) return EP_RET(EP_ERR_INVALID_ARG);
+    if (topk_weights && T > 0 && (!ok_ptr(topk_weights) || !ok_ptr(topk_idx))) return EP_RET(EP_ERR_INVALID_ARG);
     if (T == 0) return EP_OK;
 
     epg::CombineParams p{};
@@ -493,7 +555,7 @@ ep_status_t ep_combine(const void* y, int64_t num_y_rows, const int64_t* topk_id
     p.status = d_status;
     const cudaError_t e =
         epg::launch_combine(p, topk_weights != nullptr, static_cast<cudaStream_t>(cuda_stream));
-    return e == cudaSuccess ? EP_OK : EP_ERR_CUDA;
+    return e == cudaSuccess ? EP_OK : EP_RET(EP_ERR_CUDA);
 }
 
 int64_t ep_expanded_capacity_bound(int num_tokens, int num_topk, int num_experts, int expert_alignment) {
@@ -506,26 +568,29 @@ ep_status_t ep_dispatch_expanded(const void* x, const int64_t* topk_idx, const f
                                  int64_t recv_capacity, void* recv_x, float* recv_sf, int sf_col_major,
                                  int32_t* recv_src_idx, float* recv_weight, int num_sms, int32_t* d_status,
                                  void* cuda_stream) {
-    if (!layout || !d_status || num_sms < 0) return EP_ERR_INVALID_ARG;
+    EP_DEBUG("ep_dispatch_expanded: T=%d H=%d K=%d E=%d R=%d %s capacity=%lld sf_col_major=%d num_sms=%d",
+             T, H, K, E, R, out_dtype == EP_FP8_E4M3 ? "fp8" : "bf16", static_cast<long long>(recv_capacity),
+             sf_col_major, num_sms);
+    if (!layout || !d_status || num_sms < 0) return EP_RET(EP_ERR_INVALID_ARG);
     ep_status_t s = check_shape(T, K, E, R);
     if (s != EP_OK) return s;
-    if (H < 1) return EP_ERR_INVALID_ARG;
+    if (H < 1) return EP_RET(EP_ERR_INVALID_ARG);
     if (out_dtype == EP_BF16) {
-        if (H % 8 != 0) return EP_ERR_INVALID_ARG;
+        if (H % 8 != 0) return EP_RET(EP_ERR_INVALID_ARG);
     } else if (out_dtype == EP_FP8_E4M3) {
-        if (H % 128 != 0) return EP_ERR_INVALID_ARG;
-        if (H > 65536) return EP_ERR_UNSUPPORTED;
+        if (H % 128 != 0) return EP_RET(EP_ERR_INVALID_ARG);
+        if (H > 65536) return EP_RET(EP_ERR_UNSUPPORTED);
     } else {
-        return EP_ERR_INVALID_ARG;
+        return EP_RET(EP_ERR_INVALID_ARG);
     }
-    if (recv_capacity < 0 || recv_capacity > INT32_MAX) return EP_ERR_INVALID_ARG;
-    if (static_cast<int64_t>(H) * 2 > UINT32_MAX / 2) return EP_ERR_UNSUPPORTED;
-    if (T > 0 && (!ok_ptr(x) || !ok_ptr(layout->expanded_row))) return EP_ERR_INVALID_ARG;
-    if (recv_capacity > 0 && !ok_ptr(recv_x)) return EP_ERR_INVALID_ARG;
-    if (out_dtype == EP_FP8_E4M3 && recv_capacity > 0 && !ok_ptr(recv_sf)) return EP_ERR_INVALID_ARG;
-    if (recv_weight && T > 0 && !ok_ptr(topk_weights)) return EP_ERR_INVALID_ARG;
+    if (recv_capacity < 0 || recv_capacity > INT32_MAX) return EP_RET(EP_ERR_INVALID_ARG);
+    if (static_cast<int64_t>(H) * 2 > UINT32_MAX / 2) return EP_RET(EP_ERR_UNSUPPORTED);
+    if (T > 0 && (!ok_ptr(x) || !ok_ptr(layout->expanded_row))) return EP_RET(EP_ERR_INVALID_ARG);
+    if (recv_capacity > 0 && !ok_ptr(recv_x)) return EP_RET(EP_ERR_INVALID_ARG);
+    if (out_dtype == EP_FP8_E4M3 && recv_capacity > 0 && !ok_ptr(recv_sf)) return EP_RET(EP_ERR_INVALID_ARG);
+    if (recv_weight && T > 0 && !ok_ptr(topk_weights)) return EP_RET(EP_ERR_INVALID_ARG);
     if ((recv_src_idx && !aligned16(recv_src_idx)) || (recv_weight && !aligned16(recv_weight)))
-        return EP_ERR_INVALID_ARG;
+        return EP_RET(EP_ERR_INVALID_ARG);
     if (T == 0) return EP_OK;
 
     epg::DispatchParams p{};
@@ -551,20 +616,22 @@ ep_status_t ep_dispatch_expanded(const void* x, const int64_t* topk_idx, const f
     cudaStream_t st = static_cast<cudaStream_t>(cuda_stream);
     const cudaError_t e = out_dtype == EP_BF16 ? epg::launch_dispatch_bf16(p, st)
                                                : epg::launch_dispatch_fp8(p, st);
-    return e == cudaSuccess ? EP_OK : EP_ERR_CUDA;
+    return e == cudaSuccess ? EP_OK : EP_RET(EP_ERR_CUDA);
 }
 
 ep_status_t ep_combine_expanded(const void* y, int64_t num_y_rows, const float* topk_weights, int T, int H,
                                 int K, int E, int R, const ep_layout_t* layout, void* out, int num_sms,
                                 int32_t* d_status, void* cuda_stream) {
-    if (!layout || !d_status || num_sms < 0) return EP_ERR_INVALID_ARG;
+    EP_DEBUG("ep_combine_expanded: T=%d H=%d K=%d E=%d R=%d rows=%lld %s num_sms=%d",
+             T, H, K, E, R, static_cast<long long>(num_y_rows), topk_weights ? "weighted" : "unweighted", num_sms);
+    if (!layout || !d_status || num_sms < 0) return EP_RET(EP_ERR_INVALID_ARG);
     ep_status_t s = check_shape(T, K, E, R);
     if (s != EP_OK) return s;
-    if (H < 1 || H % 8 != 0) return EP_ERR_INVALID_ARG;
-    if (num_y_rows < 0 || num_y_rows > INT32_MAX) return EP_ERR_INVALID_ARG;
-    if (num_y_rows > 0 && !ok_ptr(y)) return EP_ERR_INVALID_ARG;
-    if (T > 0 && (!ok_ptr(out) || !ok_ptr(layout->expanded_row))) return EP_ERR_INVALID_ARG;
-    if (topk_weights && T > 0 && !ok_ptr(topk_weights)) return EP_ERR_INVALID_ARG;
+    if (H < 1 || H % 8 != 0) return EP_RET(EP_ERR_INVALID_ARG);
+    if (num_y_rows < 0 || num_y_rows > INT32_MAX) return EP_RET(EP_ERR_INVALID_ARG);
+    if (num_y_rows > 0 && !ok_ptr(y)) return EP_RET(EP_ERR_INVALID_ARG);
+    if (T > 0 && (!ok_ptr(out) || !ok_ptr(layout->expanded_row))) return EP_RET(EP_ERR_INVALID_ARG);
+    if (topk_weights && T > 0 && !ok_ptr(topk_weights)) return EP_RET(EP_ERR_INVALID_ARG);
     if (T == 0) return EP_OK;
 
     epg::CombineParams p{};
@@ -583,18 +650,19 @@ ep_status_t ep_combine_expanded(const void* y, int64_t num_y_rows, const float* 
     p.status = d_status;
     const cudaError_t e =
         epg::launch_combine(p, topk_weights != nullptr, static_cast<cudaStream_t>(cuda_stream));
-    return e == cudaSuccess ? EP_OK : EP_ERR_CUDA;
+    return e == cudaSuccess ? EP_OK : EP_RET(EP_ERR_CUDA);
 }
 
 ep_status_t ep_combine_topk_weights(const float* recv_topk_weights, int64_t num_rows, int T, int K, int E,
                                    int R, const ep_layout_t* layout, float* combined_topk_weights,
                                    int32_t* d_status, void* cuda_stream) {
-    if (!layout || !d_status) return EP_ERR_INVALID_ARG;
+    EP_DEBUG("ep_combine_topk_weights: T=%d K=%d E=%d R=%d rows=%lld", T, K, E, R, static_cast<long long>(num_rows));
+    if (!layout || !d_status) return EP_RET(EP_ERR_INVALID_ARG);
     ep_status_t s = check_shape(T, K, E, R);
     if (s != EP_OK) return s;
-    if (num_rows < 0 || num_rows > INT32_MAX) return EP_ERR_INVALID_ARG;
-    if (num_rows > 0 && !ok_ptr(recv_topk_weights)) return EP_ERR_INVALID_ARG;
-    if (T > 0 && (!ok_ptr(combined_topk_weights) || !ok_ptr(layout->dst_row))) return EP_ERR_INVALID_ARG;
+    if (num_rows < 0 || num_rows > INT32_MAX) return EP_RET(EP_ERR_INVALID_ARG);
+    if (num_rows > 0 && !ok_ptr(recv_topk_weights)) return EP_RET(EP_ERR_INVALID_ARG);
+    if (T > 0 && (!ok_ptr(combined_topk_weights) || !ok_ptr(layout->dst_row))) return EP_RET(EP_ERR_INVALID_ARG);
     if (T == 0) return EP_OK;
     epg::CombineWeightsParams p{};
     p.recv_topk_weights = recv_topk_weights;
@@ -611,9 +679,10 @@ ep_status_t ep_combine_topk_weights(const float* recv_topk_weights, int64_t num_
 }
 
 ep_status_t ep_accumulate_expert_stats(const ep_layout_t* layout, int E, int64_t* stats, void* cuda_stream) {
-    if (!layout || E < 1) return EP_ERR_INVALID_ARG;
-    if (E > EP_MAX_EXPERTS) return EP_ERR_UNSUPPORTED;
-    if (!ok_ptr(layout->num_tokens_per_expert) || !ok_ptr(stats)) return EP_ERR_INVALID_ARG;
+    EP_DEBUG("ep_accumulate_expert_stats: E=%d", E);
+    if (!layout || E < 1) return EP_RET(EP_ERR_INVALID_ARG);
+    if (E > EP_MAX_EXPERTS) return EP_RET(EP_ERR_UNSUPPORTED);
+    if (!ok_ptr(layout->num_tokens_per_expert) || !ok_ptr(stats)) return EP_RET(EP_ERR_INVALID_ARG);
     return epg::launch_accumulate_expert_stats(layout->num_tokens_per_expert, E, stats,
                                                static_cast<cudaStream_t>(cuda_stream)) == cudaSuccess
                ? EP_OK

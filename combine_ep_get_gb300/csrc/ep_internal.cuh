@@ -166,6 +166,22 @@ cudaError_t launch_accumulate_expert_stats(const int32_t* counts, int E, int64_t
 cudaError_t launch_forward_scaleup(HierParams p, bool fp8, cudaStream_t stream);
 cudaError_t launch_reduce_scaleup(HierParams p, bool weighted, cudaStream_t stream);
 
+// Host-side logging, on when EP_GET_DEBUG is set to anything but "0" (read
+// once per process): one line on stderr per C-ABI call, per argument check
+// that rejects a call (with the check's line in api.cu) and per kernel launch
+// (kernel, grid, block, dynamic shared memory, cluster size).
+bool debug_enabled();
+void debug_log(const char* fmt, ...)
+#if defined(__GNUC__)
+    __attribute__((format(printf, 1, 2)))
+#endif
+    ;
+void debug_launch(const void* kernel, dim3 grid, dim3 block, size_t smem, int cluster);
+#define EP_DEBUG(...)                                                 \
+    do {                                                              \
+        if (::epg::debug_enabled()) ::epg::debug_log(__VA_ARGS__);   \
+    } while (0)
+
 // Launch with programmatic dependent launch allowed: the kernel may begin
 // while the previous kernel on the stream is still running, and must call
 // pdl_wait() before it reads anything that kernel writes.  After any other
@@ -183,6 +199,7 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
     cfg.stream = stream;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
+    if (debug_enabled()) debug_launch(reinterpret_cast<const void*>(kernel), grid, block, smem, 1);
     return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 

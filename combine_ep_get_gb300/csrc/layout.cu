@@ -1481,7 +1481,11 @@ cudaError_t launch_layout(const LayoutParams& p, cudaStream_t stream) {
                                : (nodes ? layout_cluster_kernel<false, true> : layout_cluster_kernel<false, false>);
         const bool fits = cudaOccupancyMaxActiveClusters(&max_clusters, kernel, &cfg) == cudaSuccess;
         cfg.numAttrs = 2;
-        if (fits && max_clusters >= 1) return cudaLaunchKernelEx(&cfg, kernel, p, plan.tokens_per_cta);
+        if (fits && max_clusters >= 1) {
+            if (debug_enabled())
+                debug_launch(reinterpret_cast<const void*>(kernel), cfg.gridDim, cfg.blockDim, plan.smem, plan.ctas);
+            return cudaLaunchKernelEx(&cfg, kernel, p, plan.tokens_per_cta);
+        }
         cudaGetLastError();   // fall back to the tiled path
     }
 

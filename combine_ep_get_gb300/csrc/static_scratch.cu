@@ -39,6 +39,7 @@ extern "C" ep_status_t ep_get_layout_static_scratch(const int64_t* topk_idx, int
                                                     void* cuda_stream) {
     // every argument check of ep_get_layout first, so a bad argument gives the
     // same code as there; then the size of the built-in scratch
+    EP_DEBUG("ep_get_layout_static_scratch: T=%d K=%d E=%d R=%d", num_tokens, num_topk, num_experts, num_ranks);
     epg::LayoutParams unused{};
     const ep_status_t s = epg::layout_params(topk_idx, num_tokens, num_topk, num_experts, num_ranks,
                                              ranks_per_node, expert_alignment, out, nullptr, 0, d_status,
@@ -46,9 +47,16 @@ extern "C" ep_status_t ep_get_layout_static_scratch(const int64_t* topk_idx, int
     if (s != EP_OK) return s;
     const size_t need =
         ep_layout_workspace_bytes(num_tokens, num_topk, num_experts, num_ranks, ranks_per_node);
-    if (need > EP_LAYOUT_STATIC_SCRATCH_BYTES) return EP_ERR_UNSUPPORTED;
+    if (need > EP_LAYOUT_STATIC_SCRATCH_BYTES) {
+        EP_DEBUG("ep_get_layout_static_scratch: needs %zu bytes of scratch, has %zu: unsupported", need,
+                 static_cast<size_t>(EP_LAYOUT_STATIC_SCRATCH_BYTES));
+        return EP_ERR_UNSUPPORTED;
+    }
     void* scratch = nullptr;
-    if (scratch_address(&scratch) != cudaSuccess) return EP_ERR_CUDA;
+    if (scratch_address(&scratch) != cudaSuccess) {
+        EP_DEBUG("ep_get_layout_static_scratch: cudaGetSymbolAddress failed");
+        return EP_ERR_CUDA;
+    }
     return ep_get_layout(topk_idx, num_tokens, num_topk, num_experts, num_ranks, ranks_per_node,
                          expert_alignment, out, scratch, EP_LAYOUT_STATIC_SCRATCH_BYTES, d_status,
                          cuda_stream);

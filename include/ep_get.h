@@ -37,6 +37,13 @@
  *    the stream has synchronised.  Nothing ever traps.
  *  - A return of EP_ERR_CUDA means a launch failed; cudaGetLastError() has
  *    the CUDA error.
+ *  - Logging: with the environment variable EP_GET_DEBUG set to anything but
+ *    "0" when the library is first used, every call writes one line on
+ *    stderr ("[ep_get] <entry point>: <shapes and options>"), every host check
+ *    that rejects a call one more (the status and the check's source line),
+ *    and every kernel launch one (kernel, grid, block, dynamic shared memory,
+ *    cluster size).  Unset, nothing is written.  The counterpart of the
+ *    EP_BUFFER_DEBUG switch ("DeepEP Symmetric Memory", App. B).
  *
  * Notation: T tokens (all source ranks together), H hidden channels, K top-k
  * slots per token, E experts, R ranks, E_l = E/R experts per rank; expert e
