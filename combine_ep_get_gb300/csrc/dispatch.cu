@@ -76,6 +76,9 @@ namespace {
 #ifndef EP_DISPATCH_PREFETCH_MAX_GENS
 #define EP_DISPATCH_PREFETCH_MAX_GENS 16
 #endif
+#ifndef EP_DISPATCH_FP8_L2
+#define EP_DISPATCH_FP8_L2 0   // FP8 rank-row path: the same L2 policy (code stores evict-first)
+#endif
 #ifndef EP_DISPATCH_FP8_MIN_BLOCKS
 #define EP_DISPATCH_FP8_MIN_BLOCKS 4      // FP8 path: __launch_bounds__ minimum resident CTAs per SM
 #endif
@@ -400,14 +403,14 @@ __device__ __forceinline__ void prefetch_x(const DispatchParams& p) {
     const uint32_t piece = kFp8 ? static_cast<uint32_t>(p.chunk_blocks) * 256u : p.chunk_bytes;
     const int64_t n_items = static_cast<int64_t>(p.T) * p.chunks;
     const int64_t b = blockIdx.x, g = p.prefetch_ctas;
-    const int j0 = b < g ? 0 : (kFp8 ? p.prefetch_items - 1 : p.prefetch_items);
+    const int j0 = b < g ? 0 : ((kFp8 && !p.prefetch_evict_last) ? p.prefetch_items - 1 : p.prefetch_items);
     for (int j = j0; j < p.prefetch_items; ++j) {
         const int64_t it = b + static_cast<int64_t>(j) * g;
         if (it >= n_items) return;
         const int t = static_cast<int>(it / p.chunks);
         const uint32_t off = static_cast<uint32_t>(it - static_cast<int64_t>(t) * p.chunks) * piece;
         prefetch_l2(p.x + static_cast<int64_t>(t) * row_bytes + off, min(piece, row_bytes - off),
-                    !kFp8 && EP_DISPATCH_PREFETCH_EVICT_LAST);
+                    p.prefetch_evict_last != 0);
     }
 }
 
@@ -1060,6 +1063,19 @@ __device__ __forceinline__ void dispatch_fp8_item(const DispatchParams& p, int64
         const int64_t so1 = col ? static_cast<int64_t>(bq1) * p.sf_stride : bq1;
         const uint4 c0 = make_uint4(code[0][0], code[0][1], code[0][2], code[0][3]);
         const uint4 c1 = make_uint4(code[1][0], code[1][1], code[1][2], code[1][3]);
+#if EP_DISPATCH_FP8_L2
+        const uint64_t code_pol = l2_policy_evict_first();
+        if (p.prefetch_evict_last) {   // this lane's x vectors are read: lines they start back to normal
+#pragma unroll
+            for (int q = 0; q < kFp8Rounds; ++q) {
+                const int b = b_begin + q * blocks_per_round + kBlocksPerWarp * warp_g + grp;
+                const uint8_t* a = xrow + static_cast<int64_t>(b) * 256 + sub * (16 * kVec);
+                if (b < b_end && (reinterpret_cast<uintptr_t>(a) & 127u) == 0 &&
+                    xrow_off + static_cast<int64_t>(b) * 256 + sub * (16 * kVec) + 128 <= x_bytes)
+                    l2_priority_normal(a);
+            }
+        }
+#endif
         const float s0 = sfq[0], s1 = sfq[1];
         for (int rb = 0; rb < n_dst; rb += 32) {
             const int d = rb == 0    ? d0
@@ -1073,8 +1089,13 @@ __device__ __forceinline__ void dispatch_fp8_item(const DispatchParams& p, int64
                 m &= m - 1;
                 const int64_t dd = __shfl_sync(0xffffffffu, d, sl);
                 uint8_t* row = rx + dd * H;
+#if EP_DISPATCH_FP8_L2
+                if (ok0 && EP_IN_BYTES(dd * H + co0, 16, rx_bytes)) st_v4_hint(row + co0, c0, code_pol);
+                if (ok1 && EP_IN_BYTES(dd * H + co1, 16, rx_bytes)) st_v4_hint(row + co1, c1, code_pol);
+#else
                 if (ok0 && EP_IN_BYTES(dd * H + co0, 16, rx_bytes)) *reinterpret_cast<uint4*>(row + co0) = c0;
                 if (ok1 && EP_IN_BYTES(dd * H + co1, 16, rx_bytes)) *reinterpret_cast<uint4*>(row + co1) = c1;
+#endif
                 if (sf_lane) {
                     float* srow = rsf + dd * sfs;
                     if (ok0 && EP_IN(dd * sfs + so0, sf_n)) srow[so0] = s0;
@@ -1229,6 +1250,7 @@ cudaError_t launch_dispatch_bf16(DispatchParams p, cudaStream_t stream) {
             if (gens < 1) gens = 1;
             if (gens > EP_DISPATCH_PREFETCH_MAX_GENS) gens = EP_DISPATCH_PREFETCH_MAX_GENS;
             p.prefetch_items = static_cast<int>(gens);
+            p.prefetch_evict_last = EP_DISPATCH_PREFETCH_EVICT_LAST;
         }
         if (p.expanded_row) return launch_pdl(dispatch_bf16_regs_kernel<true, 1>, grid, block, 0, stream, p);
         if (p.self_route) return launch_pdl(dispatch_bf16_regs_kernel<false, 1, true>, grid, block, 0, stream, p);
@@ -1278,6 +1300,19 @@ cudaError_t launch_dispatch_fp8_t(DispatchParams p, int num_sms, cudaStream_t st
     }
     p.prefetch_ctas = device_info().num_sms * occ_ctas;
     p.prefetch_items = EP_DISPATCH_PREFETCH;
+    p.prefetch_evict_last = 0;
+    if (EP_DISPATCH_FP8_L2 && !self && !p.expanded_row) {
+        // the bf16 path's L2 policy: every generation of pieces within the
+        // budget, prefetched evict-last by the first wave
+        const int64_t piece = static_cast<int64_t>(p.chunk_blocks) * 256;
+        const int64_t n_items = static_cast<int64_t>(p.T) * p.chunks;
+        const int64_t budget_items = static_cast<int64_t>(EP_DISPATCH_PREFETCH_L2_BYTES) / piece;
+        int64_t gens = (n_items < budget_items ? n_items : budget_items) / p.prefetch_ctas;
+        if (gens < 1) gens = 1;
+        if (gens > EP_DISPATCH_PREFETCH_MAX_GENS) gens = EP_DISPATCH_PREFETCH_MAX_GENS;
+        p.prefetch_items = static_cast<int>(gens);
+        p.prefetch_evict_last = 1;
+    }
     return launch_pdl(kernel, grid, block, 0, stream, p);
 }
 

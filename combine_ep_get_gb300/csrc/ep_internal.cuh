@@ -76,6 +76,8 @@ struct DispatchParams {
     // j < prefetch_items (0: none)
     int prefetch_ctas;
     int prefetch_items;
+    int prefetch_evict_last;   // 1: the prefetch is evict-last, only the first wave prefetches, and a
+                               // read piece of x goes back to the normal priority
     // 1: ep_layout_and_dispatch with few tokens: no layout kernel runs; each
     // CTA derives its token's destination rows from topk_idx, writes that
     // token's layout rows, and two extra CTAs the layout's counts and
