@@ -41,6 +41,18 @@ constexpr int kThreads = EP_COMBINE_THREADS;
 #ifndef EP_COMBINE_BATCH
 #define EP_COMBINE_BATCH 4
 #endif
+// Many tokens: 16-byte vectors per thread in a piece.  Rank rows (~5 per
+// token on DS-V3) take 2; expanded rows (K = 8 per token, two batches of
+// loads per vector) take 1, so that a CTA waits on fewer round trips
+// (DS-V3 expanded combine 78.1 -> 75.8 us; rank rows with 1: 53.6 -> 54.7 us).
+#ifndef EP_COMBINE_VECS
+#define EP_COMBINE_VECS 2
+#endif
+#ifndef EP_COMBINE_VECS_EXPANDED
+#define EP_COMBINE_VECS_EXPANDED 1
+#endif
+constexpr int kCombineVecs = EP_COMBINE_VECS;
+constexpr int kCombineVecsExpanded = EP_COMBINE_VECS_EXPANDED;
 constexpr int kBatch = EP_COMBINE_BATCH;
 #ifndef EP_COMBINE_SM_BATCH
 #define EP_COMBINE_SM_BATCH 8        // SM-limited mode: rows of loads in flight per thread
@@ -255,11 +267,12 @@ cudaError_t launch_combine(CombineParams p, bool weighted, cudaStream_t stream) 
     const DeviceInfo& di = device_info();
     const int n_vec = p.H / 8;
     const int num_sms = p.num_sms > 0 ? (p.num_sms < di.num_sms ? p.num_sms : di.num_sms) : 0;
-    // Pieces of up to 2 vectors per thread; more pieces when there are few
-    // tokens.  SM-limited: whole rows (each group's item then waits on one
+    // Pieces of up to kCombineVecs (rank rows) or kCombineVecsExpanded
+    // vectors per thread; more pieces when there are few tokens.  SM-limited: whole rows (each group's item then waits on one
     // routing load per row instead of one per quarter row: +40-55% at 16-64
     // SMs), unless there are fewer rows than groups.
-    int chunks = num_sms > 0 ? 1 : (n_vec + 2 * kThreads - 1) / (2 * kThreads);
+    const int vecs = p.expanded_row ? kCombineVecsExpanded : kCombineVecs;
+    int chunks = num_sms > 0 ? 1 : (n_vec + vecs * kThreads - 1) / (vecs * kThreads);
     const int64_t want_items = num_sms > 0 ? static_cast<int64_t>(num_sms) * kSmGroups : 4 * di.num_sms;
     const bool few = p.T > 0 && static_cast<int64_t>(p.T) * chunks < want_items;
     if (few) {
