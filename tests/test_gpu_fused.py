@@ -107,6 +107,8 @@ def test_fused_workloads(name, sf_col_major):
     (200, 512, 128, 8, 64, 0.0, False, 0, 1),    # 64 ranks: no self routing
     (100, 256, 256, 20, 32, 0.1, True, 0, 1),    # top-20: no self routing
     (2048, 1024, 64, 6, 8, 0.05, True, 0, 1),    # many tokens (FP8 many-token mode)
+    (160, 1024, 64, 2, 8, 0.1, True, 0, 1),      # K = 2 (one lane per token's pair), three pieces
+    (96, 2048, 32, 4, 16, 0.0, False, 2, 1),     # K = 4, bf16, four pieces (one metadata array each)
 ])
 def test_fused_shapes(T, H, E, K, R, mask, fp8, rpn, align):
     d = make_inputs(T, H, E, K, R, seed=T * 7 + K, mask_frac=mask)
