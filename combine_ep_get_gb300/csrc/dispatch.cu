@@ -6,11 +6,13 @@
 //
 // bf16 path (pure copy, HBM-bound, writes ~n(t) times the reads), default:
 //   one CTA of 256 threads per (token, piece of <= 16 KB).  Every thread first
-//   issues its 16-byte streaming loads of the piece (up to 4), warp 0 meanwhile
-//   compacts the token's destination rows (one lane per rank, ballot) into
-//   shared memory, warp 1 writes the per-row metadata, and after one barrier
-//   every thread stores its vectors to every destination row.  Thousands of
-//   short CTAs let the block scheduler balance the uneven fan-out n(t).
+//   issues its 16-byte streaming loads of the piece (up to 4), then each warp
+//   reads the token's destination rows itself (one lane per rank, ballot; no
+//   block barrier) and stores its vectors to every destination row; warps 1,
+//   2, 3 write the three per-row metadata arrays.  Thousands of short CTAs let
+//   the block scheduler balance the uneven fan-out n(t).  L2: while the layout
+//   kernel runs, the first wave prefetches x evict-last (all of it at
+//   DeepSeek-V3 sizes) and the rows are stored evict-first.
 //
 // bf16 alternative (EP_DISPATCH_IMPL=0): persistent CTAs whose warp 0 drives
 //   the bulk-copy engine: a ring of kStages shared-memory slots, each filled by
@@ -24,8 +26,8 @@
 //   where it reaches the SM's store limit (~61 GB/s on GB300) that the
 //   register copies miss by ~20%.
 //
-// FP8 path: one CTA of 256 threads per (token, piece of up to 64 128-channel
-//   blocks), barrier-free like the bf16 register path: all 16-byte loads of
+// FP8 path: one CTA of up to 256 threads per (token, piece of up to 64
+//   128-channel blocks), barrier-free like the bf16 register path: all 16-byte loads of
 //   the piece are issued first and each warp ballots the destination rows
 //   itself; then each quarter-warp owns one block per round (16 channels per
 //   lane), takes amax by shuffles, scales with IEEE divides and converts with
@@ -442,8 +444,8 @@ static_assert(kSelfMaxTokens <= 256, "self_route_layout: one thread per token in
 struct SelfRouteSmem {
     uint32_t mask[kSelfMaxTokens];           // ranks holding each token (bit r)
     uint32_t bal[kSelfMaxTokens / 32][32];   // [word of 32 tokens][rank]: membership bits
-    int hist[kSelfMaxExperts];               // CTA 0: entries per expert, then offsets in the chunk
-    int chunk[kSelfMaxExperts / 32];         // CTA 0: aligned entries per 32 experts, then their prefix
+    int hist[kSelfMaxExperts];               // expert layout CTA: entries per expert, then offsets in the chunk
+    int chunk[kSelfMaxExperts / 32];         // expert layout CTA: aligned entries per 32 experts, then their prefix
 };
 
 // The CTA's one SelfRouteSmem (a function-scope __shared__ object exists
@@ -457,7 +459,7 @@ __device__ __forceinline__ SelfRouteSmem& self_smem() {
 #define EP_SELF_ROUTE_COALESCED 1   // 16-byte top-k loads in the dispatch CTAs' routing step
 #endif
 #ifndef EP_SELF_META_PIECE
-#define EP_SELF_META_PIECE 1        // piece whose warp 1 writes the receive metadata
+#define EP_SELF_META_PIECE 1        // piece whose last warps write the receive metadata (fewer than four pieces)
 #endif
 #ifndef EP_SELF_META_SPREAD
 #define EP_SELF_META_SPREAD 1       // with four or more pieces, one metadata array per piece
@@ -826,8 +828,8 @@ __device__ __forceinline__ void dispatch_regs_item(const DispatchParams& p, int6
 
 // kSelf (ep_layout_and_dispatch, few tokens, one CTA per item): there is no
 // layout kernel in front; each CTA derives its token's destination rows
-// itself and writes the token's layout rows, and CTA 0 the layout's counts
-// and offsets (self_route_layout).
+// itself and writes the token's layout rows, and kSelfLayoutCtas extra CTAs
+// the layout's counts and offsets (self_route_layout).
 template <bool kExpanded, int kGroups, bool kSelf = false>
 __global__ void __launch_bounds__(kRegThreads * kGroups, kGroups > 1 ? 1 : kSelf ? kSelfRegBlocks : 6)
     dispatch_bf16_regs_kernel(const DispatchParams p) {
