@@ -274,12 +274,38 @@ def hbm_peak():
         return 6800.0, "fallback"
 
 
+def _code_only(text):
+    """C++ source without comments and with whitespace runs collapsed, so that
+    an edit of comments alone keeps the hash (string literals are kept)."""
+    out, i, n = [], 0, len(text)
+    while i < n:
+        c = text[i]
+        if c == '"':                       # string literal, copied as is
+            j = i + 1
+            while j < n and text[j] != '"':
+                j += 2 if text[j] == "\\" else 1
+            out.append(text[i:j + 1])
+            i = j + 1
+        elif text.startswith("//", i):
+            j = text.find("\n", i)
+            i = n if j < 0 else j
+        elif text.startswith("/*", i):
+            j = text.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+            out.append(" ")
+        else:
+            out.append(c)
+            i += 1
+    return " ".join("".join(out).split())
+
+
 def kernel_source_hash(kernel):
-    """sha256[:16] of the kernel's source file followed by the shared device header."""
+    """sha256[:16] of the kernel's source file followed by the shared device
+    header, comments and whitespace left out."""
     h = hashlib.sha256()
     for name in ("%s.cu" % kernel, "ep_internal.cuh"):
-        with open(os.path.join(ROOT, "combine_ep_get_gb300", "csrc", name), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, "combine_ep_get_gb300", "csrc", name), encoding="utf-8") as f:
+            h.update(_code_only(f.read()).encode())
     return h.hexdigest()[:16]
 
 
