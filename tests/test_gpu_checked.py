@@ -9,10 +9,11 @@ EP_ERR_OUT_OF_BOUNDS in the status word.  Nothing traps.  Two kinds of test:
 * the whole GPU suite again, in a child process that loads the checked copy
   (EP_GET_LIBRARY): every parity test there asserts status 0 and the oracle's
   results, so on valid input no check fires;
-* malformed row tables (an entry below -1 in dst_row or expanded_row) given to
-  dispatch and combine, run under both builds: the checked build reports
-  EP_ERR_OUT_OF_BOUNDS, the product build reads the entry as absent (as -1)
-  with status 0; every other row is the oracle's under both.
+* malformed row tables (an entry below -1 in dst_row, expanded_row or
+  node_row) given to the rank-row, expanded and two-stage dispatch and to the
+  rank-row and expanded combine, run under both builds: the checked build
+  reports EP_ERR_OUT_OF_BOUNDS, the product build reads the entry as absent
+  (as -1) with status 0; every other row is the oracle's under both.
 """
 import os
 import subprocess
@@ -153,3 +154,66 @@ def test_expanded_combine_with_rows_below_minus_one():
     src_rows, c, a, m = expanded_sources(read_as, d["topk_weights"], True)
     loose, tight = combine_bounds(y_bits, src_rows, c, a, ref, m)
     check_close(bf16_bits(out), ref, loose, tight)
+
+
+def test_expanded_dispatch_with_rows_below_minus_one():
+    from gpu_path import B, bf16_bits, to_dev, x_tensor
+    T, H, E, K, R = 200, 1024, 64, 6, 8
+    d = make_inputs(T, H, E, K, R, seed=29)
+    idx, w = to_dev(d["topk_idx"]), to_dev(d["topk_weights"])
+    lay = B.alloc_layout(T, E, R, 0, K=K)
+    ws = torch.empty(B.ep_layout_workspace_bytes(T, K, E, R, 0), dtype=torch.uint8, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    B.ep_get_layout(idx, E, R, lay, ws, st, 0, 1)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    cap = int(lay.expert_offset[-1].item())
+    bad, read_as, dropped = _plant(lay.expanded_row.cpu().numpy(), -4, seed=8)
+    lay.expanded_row.copy_(torch.from_numpy(bad))
+    rx = torch.full((cap, H), -3.0, dtype=torch.bfloat16, device="cuda")
+    rs = torch.full((cap,), -1, dtype=torch.int32, device="cuda")
+    rw = torch.full((cap,), -9.0, dtype=torch.float32, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    B.ep_dispatch_expanded(x_tensor(d["x_bits"]), idx, w, E, R, lay, rx, rs, rw, status)
+    torch.cuda.synchronize()
+    _expect(B, status)
+    o = oracle.dispatch_expanded(d["x_bits"], d["topk_weights"], read_as, cap)
+    valid = np.unique(read_as[read_as >= 0])
+    np.testing.assert_array_equal(bf16_bits(rx).view(np.uint8).reshape(cap, 2 * H)[valid], o["recv_x"][valid])
+    np.testing.assert_array_equal(rs.cpu().numpy(), o["recv_src_idx"])   # the dropped rows stay -1
+    assert (rs.cpu().numpy()[dropped] == -1).all()
+
+
+def test_two_stage_dispatch_with_node_rows_below_minus_one():
+    from gpu_path import B, bf16_bits, to_dev, x_tensor
+    T, H, E, K, R, rpn = 256, 1024, 64, 6, 8, 4
+    d = make_inputs(T, H, E, K, R, seed=31)
+    idx, w = to_dev(d["topk_idx"]), to_dev(d["topk_weights"])
+    lay = B.alloc_layout(T, E, R, rpn, node_rows=True)
+    ws = torch.empty(B.ep_layout_workspace_bytes(T, K, E, R, rpn), dtype=torch.uint8, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    B.ep_get_layout(idx, E, R, lay, ws, st, rpn)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    M = int(lay.node_offset[-1].item())
+    N = lay.num_recv
+    bad, read_as, _ = _plant(lay.node_row.cpu().numpy(), -6, seed=9)
+    lay.node_row.copy_(torch.from_numpy(bad))
+    node_x = torch.full((M, H), -5.0, dtype=torch.bfloat16, device="cuda")
+    recv_x = torch.full((N, H), -3.0, dtype=torch.bfloat16, device="cuda")
+    rs = torch.full((N,), -9, dtype=torch.int32, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    B.ep_dispatch_hierarchical(x_tensor(d["x_bits"]), idx, w, E, R, rpn, lay, node_x, recv_x, status,
+                               recv_src_idx=rs)
+    torch.cuda.synchronize()
+    _expect(B, status)
+    dst = lay.dst_row.cpu().numpy()
+    o = oracle.dispatch_hierarchical(d["x_bits"], d["topk_idx"], d["topk_weights"], E, R, rpn, read_as, dst, M, N)
+    # the rank rows reached through a node row the product reads as present
+    node_of = np.arange(R) // rpn
+    written = [dst[t, r] for t in range(T) for r in range(R) if dst[t, r] >= 0 and read_as[t, node_of[r]] >= 0]
+    written = np.array(sorted(written))
+    assert len(written) < N                    # some rows were dropped with their node row
+    got = bf16_bits(recv_x).view(np.uint8).reshape(N, 2 * H)
+    np.testing.assert_array_equal(got[written], o["recv_x"][written])
+    np.testing.assert_array_equal(rs.cpu().numpy()[written], o["recv_src_idx"][written])
