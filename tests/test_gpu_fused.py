@@ -179,3 +179,37 @@ def test_combine_right_after_the_fused_call_sees_the_layout():
         assert int(st.item()) == 0
         nt = lay.is_token_in_rank.sum(dim=1, dtype=torch.int32).float()
         assert torch.equal(out.float(), (x.float() * nt[:, None]).to(torch.bfloat16).float())
+
+
+def _random_fused_case(seed):
+    """A seeded shape inside the one-kernel limits (T <= 256, R <= 32, K <= 16,
+    E <= 2048): token counts around warp and piece edges, K of both top-k
+    loaders (powers of two: 16-byte pairs; others: one thread per token),
+    bf16 or FP8 of several widths, masks, invalid ids, node groups, alignment."""
+    rng = np.random.Generator(np.random.PCG64(1000 + seed))
+    T = int(rng.choice([1, 2, 31, 32, 33, 63, 64, 65, 100, 127, 128, 129, 152, 200, 255, 256]))
+    R = int(rng.choice([1, 2, 4, 8, 16, 32]))
+    E = R * int(rng.choice([1, 2, 4, 8, 16, 64]))
+    E = min(E, 2048 - 2048 % R)
+    K = int(rng.choice([k for k in (1, 2, 3, 4, 5, 6, 8, 12, 16) if k <= E]))
+    fp8 = bool(rng.integers(0, 2))
+    H = int(rng.choice([128, 256, 1024, 2048, 7168])) if fp8 else int(rng.choice([8, 64, 256, 1024, 7168]))
+    rpn = int(rng.choice([0] + [v for v in (1, 2, 4, 8) if R % v == 0]))
+    align = int(rng.choice([1, 1, 3, 16]))
+    mask = float(rng.choice([0.0, 0.05, 0.3]))
+    col = fp8 and bool(rng.integers(0, 2))
+    invalid = bool(rng.integers(0, 4) == 0)
+    return T, H, E, K, R, fp8, rpn, align, mask, col, invalid
+
+
+@pytest.mark.parametrize("seed", range(24))
+def test_fused_random(seed):
+    T, H, E, K, R, fp8, rpn, align, mask, col, invalid = _random_fused_case(seed)
+    d = make_inputs(T, H, E, K, R, seed=seed, mask_frac=mask)
+    if invalid:   # a few ids outside [-1, E): flagged, skipped, every other row intact
+        rng = np.random.Generator(np.random.PCG64(seed))
+        flat = d["topk_idx"].reshape(-1)
+        pick = rng.choice(flat.size, size=max(1, flat.size // 50), replace=False)
+        flat[pick] = rng.choice([-3, -2, E, E + 7], size=pick.size)
+    g = _fused(d, E, R, fp8=fp8, sf_col_major=col, rpn=rpn, align=align)
+    _check(d, E, R, g, fp8=fp8, sf_col_major=col, rpn=rpn, align=align)
