@@ -57,13 +57,21 @@ def host_cpu():
     except OSError:
         pass
     return {"host_cores": os.cpu_count(), "cpu_model": model}
-def kernels_per_step(T, R, expanded=False, hierarchical=False):
+# ep_layout_and_dispatch's one-kernel limits (include/ep_get.h)
+ONE_KERNEL_MAX_TOKENS, ONE_KERNEL_MAX_RANKS, ONE_KERNEL_MAX_TOPK, ONE_KERNEL_MAX_EXPERTS = 256, 32, 16, 2048
+
+
+def kernels_per_step(T, R, expanded=False, hierarchical=False, fused=False, K=0, E=0):
     """Launches of this library per step: the layout is one kernel (the
     single-CTA kernel for few tokens, else one cluster), or three tiled kernels
     when T*R passes 2^19 (expanded and node rows ride on the same kernels; the
     tiled fallback for a cluster whose shared memory would not fit does not
     occur on these workloads); dispatch and combine one each, two each on the
-    hierarchical path."""
+    hierarchical path.  ep_layout_and_dispatch (fused) with few tokens runs
+    layout and dispatch as one kernel."""
+    if (fused and not expanded and not hierarchical and 1 <= T <= ONE_KERNEL_MAX_TOKENS
+            and R <= ONE_KERNEL_MAX_RANKS and K <= ONE_KERNEL_MAX_TOPK and E <= ONE_KERNEL_MAX_EXPERTS):
+        return 1 + 1
     tiled = T * R > (1 << 19)
     return (3 if tiled else 1) + (4 if hierarchical else 2)
 
@@ -428,6 +436,7 @@ def run_ours(args):
     # rows itself and runs beside the layout; with many it is the same two
     # launches as the separate calls.
     fused = args.path == "rank" and sms_dispatch == 0
+    one_kernel = fused and kernels_per_step(T, R, False, False, True, K, E) == 2
 
     def do_layout_dispatch():
         if fused:
@@ -654,8 +663,10 @@ def run_ours(args):
         },
         "per_kernel": per_kernel,
         "roofline": {"bound": "hbm",
-                     "kernel": ("layout+dispatch (%s: the layout kernel, then the dispatch kernel launched "
-                                "during it)" % ("ep_layout_and_dispatch" if fused else "ep_get_layout, ep_dispatch")
+                     "kernel": (("layout+dispatch (ep_layout_and_dispatch: one kernel, the layout inside the "
+                                 "dispatch)" if one_kernel else
+                                 "layout+dispatch (%s: the layout kernel, then the dispatch kernel launched "
+                                 "during it)" % ("ep_layout_and_dispatch" if fused else "ep_get_layout, ep_dispatch"))
                                 if dominant == "layout+dispatch" else "combine"),
                      "achieved": achieved, "peak": peak,
                      "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / peak,
@@ -665,7 +676,7 @@ def run_ours(args):
                                  if args.path == "rank" and not args.fp8 else None),
                      "algorithmic_bytes_per_launch": nbytes[dominant], "timed_in": source[dominant]},
         "e2e": e2e,
-        "gpu_launches": kernels_per_step(T, R, expanded, hierarchical) * args.steps,
+        "gpu_launches": kernels_per_step(T, R, expanded, hierarchical, fused, K, E) * args.steps,
         "clocks": clocks,
     }
     if world == 1 and rank == 0 and not args.no_cpu_baseline:

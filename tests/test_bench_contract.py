@@ -8,6 +8,8 @@ import socket
 import subprocess
 import sys
 
+import pytest
+
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 ARGS = ["--impl", "reference", "--workload", "tiny", "--steps", "2", "--warmup", "3"]
 
@@ -51,3 +53,27 @@ def test_reference_arm_under_torchrun_two_ranks():
     lines = _lines(r.stdout)
     assert len(lines) == 1, r.stdout
     _check_line(json.loads(lines[0]), 2)
+
+
+@pytest.mark.gpu
+def test_our_arm_prints_the_contract_keys():
+    r = subprocess.run([sys.executable, "bench.py", "--workload", "tiny", "--steps", "5", "--warmup", "3",
+                        "--e2e-steps", "3", "--cpu-seconds", "0.5"], cwd=ROOT, capture_output=True, text=True,
+                       timeout=900)
+    assert r.returncode == 0, r.stderr[-3000:]
+    lines = _lines(r.stdout)
+    assert len(lines) == 1, r.stdout
+    d = json.loads(lines[0])
+    for k in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better", "scaling",
+              "vs_baseline", "dtype", "data", "config", "roofline", "cpu_baseline", "e2e", "gpu_launches", "clocks"):
+        assert k in d, k
+    assert d["n_gpus"] == 1 and d["steps"] == 5 and d["value"] > 0
+    roof = d["roofline"]
+    for k in ("bound", "achieved", "peak", "unit", "frac", "traffic"):
+        assert k in roof, k
+    assert roof["bound"] == "hbm" and roof["frac"] == pytest.approx(roof["achieved"] / roof["peak"])
+    e = d["e2e"]
+    assert e["value"] > 0 and e["h2d_bytes_per_step"] > 0 and e["d2h_bytes_per_step"] > 0
+    assert d["gpu_launches"] == 5 * 2                      # layout + dispatch in one kernel, combine
+    assert "sm_mhz" in d["clocks"] and "reasons" in d["clocks"]
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] == 1
