@@ -1,6 +1,8 @@
 // C ABI of libep_get.so: host-side argument checks, parameter blocks and
 // launches.  Declarations and the full contract are in include/ep_get.h.
 #include <algorithm>
+#include <atomic>
+#include <chrono>
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
@@ -232,6 +234,22 @@ ep_status_t ep_get_layout(const int64_t* topk_idx, int T, int K, int E, int R, i
 
 namespace {
 
+// A tag for the rows-ready signal, distinct for every call of the process:
+// the splitmix64 output function (Steele, Lea and Flood, "Fast splittable
+// pseudorandom number generators", 2014), a bijection of 64-bit words,
+// applied to a per-process offset plus an odd multiple of the call count.
+uint64_t next_rows_tag() {
+    static std::atomic<uint64_t> calls{0};
+    static const uint64_t salt =
+        static_cast<uint64_t>(std::chrono::steady_clock::now().time_since_epoch().count()) ^
+        static_cast<uint64_t>(reinterpret_cast<uintptr_t>(&calls));
+    uint64_t z = salt + 0x9e3779b97f4a7c15ull * (calls.fetch_add(1, std::memory_order_relaxed) + 1);
+    z = (z ^ (z >> 30)) * 0xbf58476d1ce4e5b9ull;
+    z = (z ^ (z >> 27)) * 0x94d049bb133111ebull;
+    z ^= z >> 31;
+    return z != 0 ? z : 1;
+}
+
 // Shared by ep_dispatch and ep_layout_and_dispatch.  self_layout (few
 // tokens, ep_layout_and_dispatch): no layout kernel has run; the dispatch
 // kernel computes the rows itself and writes the layout arrays of `lp`.
@@ -239,7 +257,8 @@ ep_status_t dispatch_impl(const void* x, const int64_t* topk_idx, const float* t
                           int E, int R, const ep_layout_t* layout, int out_dtype, int64_t recv_capacity,
                           void* recv_x, float* recv_sf, int sf_col_major, int32_t* recv_topk_idx,
                           float* recv_topk_weights, int32_t* recv_src_idx, int num_sms, int32_t* d_status,
-                          void* cuda_stream, const epg::LayoutParams* self_layout) {
+                          void* cuda_stream, const epg::LayoutParams* self_layout,
+                          const epg::RowsSignal* rows = nullptr) {
     if (!layout || !d_status || num_sms < 0) return EP_RET(EP_ERR_INVALID_ARG);
     ep_status_t s = check_shape(T, K, E, R);
     if (s != EP_OK) return s;
@@ -302,6 +321,12 @@ ep_status_t dispatch_impl(const void* x, const int64_t* topk_idx, const float* t
         p.l_ranks_per_node = self_layout->ranks_per_node;
         p.l_num_nodes = self_layout->num_nodes;
     }
+    if (rows && rows->slots) {
+        p.rows_ready = rows->slots;
+        p.rows_tag = rows->tag;
+        p.rows_tokens = rows->tokens;
+        p.rows_slots = rows->count;
+    }
     cudaStream_t st = static_cast<cudaStream_t>(cuda_stream);
     const cudaError_t e = out_dtype == EP_BF16 ? epg::launch_dispatch_bf16(p, st)
                                                : epg::launch_dispatch_fp8(p, st);
@@ -358,8 +383,19 @@ ep_status_t ep_layout_and_dispatch(const void* x, const int64_t* topk_idx, const
     // the layout (expanded rows and node rows need the layout kernel).
     const bool one_kernel = T >= 1 && T <= epg::kSelfRouteMaxTokens && R <= 32 && K <= epg::kSelfRouteMaxTopk &&
                             E <= epg::kSelfRouteMaxExperts && !lp.expanded_row && !lp.node_row && !lp.node_offset;
+    // Otherwise the layout kernel, and the dispatch waits for the rows-ready
+    // signal of the cluster layout (where the dispatch kernel is one of the
+    // two that read it) instead of the layout kernel's completion.
+    epg::RowsSignal rows{};
+    if (!one_kernel && T > 0 && epg::dispatch_reads_rows_signal(out_dtype == EP_FP8_E4M3) &&
+        (reinterpret_cast<uintptr_t>(workspace) & 127u) == 0) {
+        rows.slots = static_cast<uint64_t*>(workspace);
+        rows.tag = next_rows_tag();
+        rows.bytes = ws_bytes;
+    }
     if (!one_kernel) {
-        if (epg::launch_layout(lp, static_cast<cudaStream_t>(cuda_stream)) != cudaSuccess) return EP_RET(EP_ERR_CUDA);
+        if (epg::launch_layout(lp, static_cast<cudaStream_t>(cuda_stream), &rows) != cudaSuccess)
+            return EP_RET(EP_ERR_CUDA);
         if (T == 0 && layout->node_offset &&
             cudaMemsetAsync(layout->node_offset, 0, sizeof(int32_t) * (R / ranks_per_node + 1),
                             static_cast<cudaStream_t>(cuda_stream)) != cudaSuccess)
@@ -367,7 +403,7 @@ ep_status_t ep_layout_and_dispatch(const void* x, const int64_t* topk_idx, const
     }
     return dispatch_impl(x, topk_idx, topk_weights, T, H, K, E, R, layout, out_dtype, recv_capacity, recv_x, recv_sf,
                          sf_col_major, recv_topk_idx, recv_topk_weights, recv_src_idx, 0, d_status, cuda_stream,
-                         one_kernel ? &lp : nullptr);
+                         one_kernel ? &lp : nullptr, &rows);
 }
 
 ep_status_t ep_dispatch_hierarchical(const void* x, const int64_t* topk_idx, const float* topk_weights, int T,

@@ -33,6 +33,11 @@
 //   lane), takes amax by shuffles, scales with IEEE divides and converts with
 //   cvt.rn.satfinite e4m3x2, and stores a 16-byte code vector per lane and
 //   the scale to every destination row.
+//
+// Behind the one-cluster layout kernel (ep_layout_and_dispatch) the first
+// wave of either path waits for the rows-ready signal of its token's layout
+// CTA instead of the layout kernel's completion (wait_rows_ready), and the
+// grid's last CTA clears the signal for the next call (clear_rows_slots).
 #include <climits>
 
 #include "ep_internal.cuh"
@@ -55,6 +60,9 @@ namespace {
 #endif
 #ifndef EP_DISPATCH_EVICT_FIRST
 #define EP_DISPATCH_EVICT_FIRST 0     // L2 evict-first hint on the receive-row stores
+#endif
+#ifndef EP_ROWS_SIGNAL
+#define EP_ROWS_SIGNAL 3              // rows-ready signal behind the layout kernel: bit 0 bf16, bit 1 FP8
 #endif
 #ifndef EP_DISPATCH_IMPL
 #define EP_DISPATCH_IMPL 1            // 1: 16-byte register copies, 0: bulk-copy engine
@@ -697,6 +705,56 @@ __device__ __forceinline__ void write_metadata_part(const DispatchParams& p, int
     }
 }
 
+// Rows-ready wait (ep_layout_and_dispatch, cluster layout): thread 0 polls
+// the slot of the layout CTA that writes token t's rows until it holds the
+// call's tag, or waits for the layout kernel's completion after kRowsWaitNs,
+// then counts itself as a reader of the slot (a relaxed add that returns
+// nothing, so no wait: the count only tells the last CTA when it may clear
+// the tag, and a tag cleared early costs a reader the fallback, never a
+// wrong row); the CTA's barrier then releases the row loads, which are plain
+// loads: the layout CTA's release, this acquire and the barrier order them
+// after the rows' stores.  Every first-wave CTA calls this exactly once.
+__device__ __forceinline__ void wait_rows_ready(const DispatchParams& p, int t) {
+    if (threadIdx.x == 0) {
+        const int c = t / p.rows_tokens;
+        bool seen = false;
+        uint64_t* slot = p.rows_ready + static_cast<size_t>(c) * kReadyWords;
+        const bool ok = EP_IN(c, p.rows_slots);
+        if (ok) {
+            const uint64_t start = global_timer_ns();
+            while (!(seen = ld_acquire_u64(slot) == p.rows_tag)) {
+                if (global_timer_ns() - start > kRowsWaitNs) break;
+                __nanosleep(64);
+            }
+        }
+        if (!seen) pdl_wait();
+        if (ok) red_relaxed_add_u32(reinterpret_cast<uint32_t*>(slot + 1), 1u);
+    }
+    __syncthreads();
+}
+
+// The grid's last CTA, after its item: once the layout kernel has completed
+// (every tag published) and each slot has counted all its readers (the CTAs
+// of its tokens below rows_first_wave), clear the tags.  Should a count stay short for kRowsWaitNs
+// the tag is cleared all the same: a reader that then finds none waits for
+// the layout kernel's completion, which has already happened.
+__device__ __forceinline__ void clear_rows_slots(const DispatchParams& p) {
+    pdl_wait();
+    for (int c = threadIdx.x; c < p.rows_slots; c += blockDim.x) {
+        uint64_t* slot = p.rows_ready + static_cast<size_t>(c) * kReadyWords;
+        const int64_t first = static_cast<int64_t>(c) * p.rows_tokens * p.chunks;
+        const int64_t end = min(min(static_cast<int64_t>(c + 1) * p.rows_tokens, static_cast<int64_t>(p.T)) * p.chunks,
+                                static_cast<int64_t>(p.rows_first_wave));
+        const uint32_t readers = end > first ? static_cast<uint32_t>(end - first) : 0u;
+        const uint64_t start = global_timer_ns();
+        while (ld_acquire_u32(reinterpret_cast<const uint32_t*>(slot + 1)) < readers) {
+            if (global_timer_ns() - start > kRowsWaitNs) break;
+            __nanosleep(64);
+        }
+        *reinterpret_cast<volatile uint64_t*>(slot) = 0ull;
+    }
+}
+
 constexpr int kRegThreads = 256;
 constexpr int kRegUnroll = 4;
 constexpr int kSelfRegBlocks = 4;   // self-routing bf16 CTAs per SM (registers for the top-k entries, no spills)
@@ -715,7 +773,7 @@ constexpr int kSmGroups = 4;
 // One (token, piece) item of the register path, by one group of 256 threads.
 template <bool kExpanded, bool kSelf, int kMW = kMetaWarps>
 __device__ __forceinline__ void dispatch_regs_item(const DispatchParams& p, int64_t it, int gtid, int warp_g,
-                                                   int lane, bool& cap_bad) {
+                                                   int lane, bool& cap_bad, bool signal = false) {
     const uint32_t row_bytes = static_cast<uint32_t>(p.H) * 2u;
     const int t = static_cast<int>(it / p.chunks);
     const int c = static_cast<int>(it - static_cast<int64_t>(t) * p.chunks);
@@ -748,6 +806,7 @@ __device__ __forceinline__ void dispatch_regs_item(const DispatchParams& p, int6
         d0 = self_route_layout<false>(p, t, c, self_smem());   // R <= 32
         d1 = -1;
     } else {
+        if (signal) wait_rows_ready(p, t);   // x is already in flight
         d0 = (lane < n_dst && EP_IN(drow0 + lane, n_drow)) ? drow[lane] : -1;
         d1 = (32 + lane < n_dst && EP_IN(drow0 + 32 + lane, n_drow)) ? drow[32 + lane] : -1;   // ranks 32..63
         (void)EP_ROW_OK(d0);
@@ -843,9 +902,16 @@ __global__ void __launch_bounds__(kRegThreads * kGroups, kGroups > 1 ? 1 : kSelf
         return;
     }
     if (kGroups == 1) prefetch_x<false>(p);
-    pdl_wait();   // before any load: the previous kernel may write x
+    // With the rows-ready signal (first wave) x was complete before the
+    // layout kernel passed its own wait, and only dst_row waits (for the
+    // signal).  Later CTAs start once the layout kernel has ended: for them
+    // the wait on it costs nothing, and a poll would cost a round trip.
+    const bool signal_call = kGroups == 1 && !kSelf && !kExpanded && p.rows_ready != nullptr;
+    const bool signal = signal_call && static_cast<int>(blockIdx.x) < p.rows_first_wave;
+    if (!signal) pdl_wait();   // before any load: the previous kernel may write x
     if (kGroups == 1) {
-        dispatch_regs_item<kExpanded, kSelf>(p, blockIdx.x, gtid, warp_g, lane, cap_bad);
+        dispatch_regs_item<kExpanded, kSelf>(p, blockIdx.x, gtid, warp_g, lane, cap_bad, signal);
+        if (signal_call && blockIdx.x == gridDim.x - 1) clear_rows_slots(p);
     } else {
         const int64_t n_items = static_cast<int64_t>(p.T) * p.chunks;
         const int group = static_cast<int>(threadIdx.x) / kRegThreads;
@@ -890,7 +956,7 @@ constexpr int kFp8Rounds = 2;   // rounds of blocks per item (loads of every rou
 // to every destination.
 template <bool kExpanded, int kLanes, bool kSelf, int kMW = kMetaWarps>
 __device__ __forceinline__ void dispatch_fp8_item(const DispatchParams& p, int64_t it, int gtid, int lane,
-                                                  int group_warps, bool& cap_bad) {
+                                                  int group_warps, bool& cap_bad, bool signal = false) {
     constexpr int kVec = 128 / kLanes / 8;                     // 16-byte input vectors per lane per block
     constexpr int kBlocksPerWarp = 32 / kLanes;
     const int blocks_per_round = kBlocksPerWarp * group_warps;
@@ -928,6 +994,7 @@ __device__ __forceinline__ void dispatch_fp8_item(const DispatchParams& p, int64
         d0 = self_route_layout<false>(p, t, c, self_smem());   // R <= 32
         d1 = -1;
     } else {
+        if (signal) wait_rows_ready(p, t);   // x is already in flight
         d0 = (lane < n_dst && EP_IN(drow0 + lane, n_drow)) ? drow[lane] : -1;
         d1 = (32 + lane < n_dst && EP_IN(drow0 + 32 + lane, n_drow)) ? drow[32 + lane] : -1;   // ranks 32..63
         (void)EP_ROW_OK(d0);
@@ -1142,10 +1209,15 @@ __global__ void __launch_bounds__(kFp8Threads * kGroups,
         return;
     }
     if (kGroups == 1) prefetch_x<true>(p);
-    pdl_wait();   // before any load: the previous kernel may write x
+    // with the rows-ready signal (first wave) only dst_row waits (see the
+    // bf16 kernel)
+    const bool signal_call = kGroups == 1 && !kSelf && !kExpanded && p.rows_ready != nullptr;
+    const bool signal = signal_call && static_cast<int>(blockIdx.x) < p.rows_first_wave;
+    if (!signal) pdl_wait();   // before any load: the previous kernel may write x
     if (kGroups == 1) {
         dispatch_fp8_item<kExpanded, kLanes, kSelf>(p, blockIdx.x, gtid, lane, static_cast<int>(blockDim.x) / 32,
-                                                    cap_bad);
+                                                    cap_bad, signal);
+        if (signal_call && blockIdx.x == gridDim.x - 1) clear_rows_slots(p);
     } else {
         const int64_t n_items = static_cast<int64_t>(p.T) * p.chunks;
         const int group = static_cast<int>(threadIdx.x) / kFp8Threads;
@@ -1243,6 +1315,7 @@ cudaError_t launch_dispatch_bf16(DispatchParams p, cudaStream_t stream) {
         // self routing: kSelfLayoutCtas more CTAs, which write the layout's counts and offsets
         const dim3 grid(static_cast<unsigned>(items + (p.self_route ? kSelfLayoutCtas : 0))), block(kRegThreads);
         p.prefetch_ctas = di.num_sms * 6;   // the first wave (6 CTAs per SM)
+        p.rows_first_wave = p.prefetch_ctas;
         // the first wave prefetches the pieces of every generation while they
         // fit the L2 budget (all of x on DeepSeek-V3-sized inputs)
         {
@@ -1301,6 +1374,7 @@ cudaError_t launch_dispatch_fp8_t(DispatchParams p, int num_sms, cudaStream_t st
         occ_kind = kind;
     }
     p.prefetch_ctas = device_info().num_sms * occ_ctas;
+    p.rows_first_wave = p.prefetch_ctas;
     p.prefetch_items = EP_DISPATCH_PREFETCH;
     p.prefetch_evict_last = 0;
     if (EP_DISPATCH_FP8_L2 && !self && !p.expanded_row) {
@@ -1316,6 +1390,10 @@ cudaError_t launch_dispatch_fp8_t(DispatchParams p, int num_sms, cudaStream_t st
         p.prefetch_evict_last = 1;
     }
     return launch_pdl(kernel, grid, block, 0, stream, p);
+}
+
+bool dispatch_reads_rows_signal(bool fp8) {
+    return fp8 ? (EP_ROWS_SIGNAL & 2) != 0 : ((EP_ROWS_SIGNAL & 1) != 0 && EP_DISPATCH_IMPL == 1);
 }
 
 cudaError_t launch_dispatch_fp8(DispatchParams p, cudaStream_t stream) {

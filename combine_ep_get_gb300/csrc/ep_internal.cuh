@@ -25,6 +25,29 @@ constexpr int kSelfRouteMaxTopk = 16;
 constexpr int kSelfRouteMaxExperts = 2048;
 constexpr int kTileWords = kTileTokens / 32;   // 32-bit membership words per rank per tile
 
+// Rows-ready signal of ep_layout_and_dispatch on the cluster layout path, in
+// the caller's workspace (which that path does not otherwise use): one
+// 128-byte line per layout CTA.  Word 0 holds the call's tag once the CTA's
+// block of dst_row is written; the low 32 bits of word 1 count the dispatch
+// CTAs that have looked for it.  The layout CTA clears the count before it
+// publishes the tag; the dispatch grid's last CTA, once the layout kernel has
+// completed and every reader has counted itself, clears the tag, so a line
+// holds no tag between calls (a CUDA graph replays a call with the same
+// tag).  A dispatch CTA that sees no tag within kRowsWaitNs waits for the
+// layout kernel's completion instead.
+constexpr int kReadyWords = 16;   // 64-bit words per slot line
+#ifndef EP_ROWS_WAIT_NS
+#define EP_ROWS_WAIT_NS 200000ull
+#endif
+constexpr uint64_t kRowsWaitNs = EP_ROWS_WAIT_NS;
+struct RowsSignal {
+    uint64_t* slots;   // in: the workspace, or null for no signal; out: null when the layout does not publish
+    uint64_t tag;      // in: this call's tag (never 0)
+    size_t bytes;      // in: workspace bytes available for slot lines
+    int tokens;        // out: tokens per slot (one layout CTA's range)
+    int count;         // out: slots
+};
+
 struct LayoutParams {
     const int64_t* topk_idx;
     int T, K, E, R, experts_per_rank, ranks_per_node, num_nodes, alignment, num_tiles;
@@ -46,6 +69,8 @@ struct LayoutParams {
     int32_t* ws_node;      // [num_nodes][num_tiles]
     uint32_t* ws_bitmap;   // [num_tiles][kTileWords][R]
     int32_t* status;
+    uint64_t* rows_ready;  // cluster path: publish each CTA's rows here (null: no signal)
+    uint64_t rows_tag;
 };
 
 struct DispatchParams {
@@ -93,6 +118,13 @@ struct DispatchParams {
     int32_t* l_src_dst_count;           // [R][R] or null
     int32_t* l_token_offset;            // [T + 1] or null
     int l_alignment, l_ranks_per_node, l_num_nodes;
+    // rows-ready signal (one item per CTA, rank rows): the CTAs below
+    // rows_first_wave (the first wave, which starts while the layout kernel
+    // runs) wait for the tag in slot t / rows_tokens instead of the layout
+    // kernel's completion
+    uint64_t* rows_ready;
+    uint64_t rows_tag;
+    int rows_tokens, rows_slots, rows_first_wave;
 };
 
 struct CombineParams {
@@ -159,9 +191,14 @@ struct DeviceInfo {
 const DeviceInfo& device_info();
 
 // Launchers (host).  Each returns cudaSuccess or the launch error.
-cudaError_t launch_layout(const LayoutParams& p, cudaStream_t stream);
+// sig (ep_layout_and_dispatch): on the cluster path with room for its slot
+// lines the layout CTAs publish their rows; otherwise sig->slots is cleared.
+cudaError_t launch_layout(const LayoutParams& p, cudaStream_t stream, RowsSignal* sig = nullptr);
 cudaError_t launch_dispatch_bf16(DispatchParams p, cudaStream_t stream);
 cudaError_t launch_dispatch_fp8(DispatchParams p, cudaStream_t stream);
+// True when the dispatch that ep_layout_and_dispatch launches on the layout
+// kernel's rows (num_sms 0, not self-routed) waits for the rows-ready signal.
+bool dispatch_reads_rows_signal(bool fp8);
 cudaError_t launch_combine(CombineParams p, bool weighted, cudaStream_t stream);
 cudaError_t launch_combine_topk_weights(const CombineWeightsParams& p, cudaStream_t stream);
 cudaError_t launch_accumulate_expert_stats(const int32_t* counts, int E, int64_t* stats, cudaStream_t stream);
@@ -384,6 +421,25 @@ __device__ __forceinline__ void bulk_wait_read() {
 template <int N>
 __device__ __forceinline__ void bulk_wait_all() {
     asm volatile("cp.async.bulk.wait_group %0;" ::"n"(N) : "memory");
+}
+
+// Loads, stores and counts of the rows-ready signal (memory-model strong, at
+// GPU scope).
+__device__ __forceinline__ uint64_t ld_acquire_u64(const uint64_t* p) {
+    uint64_t v;
+    asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ void st_release_u64(uint64_t* p, uint64_t v) {
+    asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+__device__ __forceinline__ uint32_t ld_acquire_u32(const uint32_t* p) {
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ void red_relaxed_add_u32(uint32_t* p, uint32_t v) {
+    asm volatile("red.relaxed.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
 // 16-byte read-only streaming load that does not allocate in L1.

@@ -1004,6 +1004,20 @@ __global__ void __launch_bounds__(kClusterThreads, 1)
         }
     }
 
+    // Rows-ready signal: this CTA's dst_row block is complete.  The reader
+    // count is cleared before the tag goes out (readers count only once
+    // they have seen it), and the block's stores are ordered before the tag
+    // by the barrier and the fence.
+    if (p.rows_ready) {
+        __syncthreads();
+        if (tid == 0) {
+            uint64_t* slot = p.rows_ready + static_cast<size_t>(me) * kReadyWords;
+            *reinterpret_cast<volatile uint32_t*>(slot + 1) = 0u;
+            __threadfence();
+            st_release_u64(slot, p.rows_tag);
+        }
+    }
+
     // Node rows of this CTA's [nt, nodes] block: node_offset + tokens of
     // earlier CTAs + tokens of earlier words + popc below.
     if (kNodeRows) {
@@ -1412,8 +1426,15 @@ LayoutWorkspace layout_workspace(int T, int E, int R, int num_nodes) {
     return w;
 }
 
-cudaError_t launch_layout(const LayoutParams& p, cudaStream_t stream) {
+cudaError_t launch_layout(const LayoutParams& p_in, cudaStream_t stream, RowsSignal* sig) {
     const DeviceInfo& di = device_info();
+    LayoutParams p = p_in;
+    p.rows_ready = nullptr;   // only the cluster kernel publishes, when sig has room for its lines
+    p.rows_tag = 0;
+    if (sig) {
+        sig->tokens = 0;
+        sig->count = 0;
+    }
     static thread_local int configured_device = -1;
     static thread_local bool cluster_ok = false;
     static thread_local int cluster_smem_max = 0;
@@ -1455,6 +1476,7 @@ cudaError_t launch_layout(const LayoutParams& p, cudaStream_t stream) {
         const size_t smem = 4 * small_smem_ints(p.E, p.T * p.K, expanded);
         auto kernel = expanded ? (nodes ? layout_small_kernel<true, true> : layout_small_kernel<true, false>)
                                : (nodes ? layout_small_kernel<false, true> : layout_small_kernel<false, false>);
+        if (sig) sig->slots = nullptr;
         return launch_pdl(kernel, dim3(1), dim3(1024), smem, stream, p);
     }
 
@@ -1482,12 +1504,21 @@ cudaError_t launch_layout(const LayoutParams& p, cudaStream_t stream) {
         const bool fits = cudaOccupancyMaxActiveClusters(&max_clusters, kernel, &cfg) == cudaSuccess;
         cfg.numAttrs = 2;
         if (fits && max_clusters >= 1) {
+            if (sig && sig->slots && static_cast<size_t>(plan.ctas) * kReadyWords * 8 <= sig->bytes) {
+                p.rows_ready = sig->slots;
+                p.rows_tag = sig->tag;
+                sig->tokens = plan.tokens_per_cta;
+                sig->count = plan.ctas;
+            } else if (sig) {
+                sig->slots = nullptr;
+            }
             if (debug_enabled())
                 debug_launch(reinterpret_cast<const void*>(kernel), cfg.gridDim, cfg.blockDim, plan.smem, plan.ctas);
             return cudaLaunchKernelEx(&cfg, kernel, p, plan.tokens_per_cta);
         }
         cudaGetLastError();   // fall back to the tiled path
     }
+    if (sig) sig->slots = nullptr;
 
     const size_t smem_count =
         4 * (static_cast<size_t>(p.R) * kTileWords + static_cast<size_t>(p.num_nodes) * kTileWords + p.E);

@@ -258,10 +258,19 @@ ep_status_t ep_dispatch(const void* x, const int64_t* topk_idx, const float* top
  * the call launches a single kernel: each dispatch CTA derives its token's
  * destination rows from topk_idx by the layout's definition (rank offset plus
  * the number of earlier tokens on that rank) and writes the token's layout
- * rows, and one CTA writes the layout's counts and offsets, so no layout
- * kernel runs in front of the dispatch (the workspace is then not touched).
- * This shortens the latency-bound decode step.  Otherwise the call launches
- * the layout kernel(s) and then the dispatch, as the two separate calls do.
+ * rows, and two more CTAs write the layout's counts and offsets, so no
+ * layout kernel runs in front of the dispatch (the workspace is then not
+ * touched).  This shortens the latency-bound decode step.  Otherwise the call
+ * launches the layout kernel(s) and then the dispatch, as the two separate
+ * calls do.  Where the layout is the one-cluster kernel (up to 2^19 token-rank
+ * pairs beyond the few-token case) and the workspace is 128-byte aligned
+ * with room for one 128-byte line per cluster CTA (at most 2 KiB), each layout
+ * CTA also publishes in its line when its block of dst_row is written, and
+ * the dispatch CTAs of the first wave start on that instead of on the layout
+ * kernel's completion; the dispatch's last CTA clears the lines, so a CUDA
+ * graph may replay the call.  The workspace then belongs to the call until
+ * the dispatch completes, and its contents are garbage after, as for
+ * ep_get_layout.
  */
 ep_status_t ep_layout_and_dispatch(const void* x, const int64_t* topk_idx, const float* topk_weights,
                                    int num_tokens, int hidden, int num_topk, int num_experts,
