@@ -25,8 +25,9 @@
  * Conventions shared by every entry point:
  *  - All array arguments are DEVICE pointers owned by the caller; they must be
  *    16-byte aligned.  The library allocates nothing and keeps no state
- *    between calls other than per-device kernel attributes (and the built-in
- *    scratch array of ep_get_layout_static_scratch).
+ *    between calls other than per-device kernel attributes, the built-in
+ *    scratch array of ep_get_layout_static_scratch and a process-wide call
+ *    counter that numbers the rows-ready tags of ep_layout_and_dispatch.
  *  - Every call is asynchronous on `cuda_stream` (a cudaStream_t; NULL = the
  *    legacy default stream).  The caller orders streams.
  *  - Errors a host check can see (null or misaligned pointers, sizes out of
