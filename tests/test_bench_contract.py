@@ -1,7 +1,9 @@
 """The benchmark's output contract, checked on the host with the reference
 arm (the oracle on the host cores; no GPU): one JSON line with the keys the
 driver reads, and under torchrun with two ranks still exactly one line
-(rank 0 runs and prints, the other rank exits 0 without work)."""
+(rank 0 runs and prints, the other rank exits 0 without work).  Also the
+per-step launch count behind the line's gpu_launches, on every workload and
+path, and (on a GPU) our arm's line."""
 import json
 import os
 import socket
@@ -77,3 +79,26 @@ def test_our_arm_prints_the_contract_keys():
     assert d["gpu_launches"] == 5 * 2                      # layout + dispatch in one kernel, combine
     assert "sm_mhz" in d["clocks"] and "reasons" in d["clocks"]
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] == 1
+
+
+@pytest.mark.parametrize("cfg,path,per_step", [
+    ("tiny", "rank", 2),        # few tokens: layout and dispatch in one kernel, then the combine
+    ("decode", "rank", 2),
+    ("dsv3", "rank", 3),        # one-cluster layout, dispatch, combine
+    ("skewed", "rank", 3),
+    ("large", "rank", 5),       # T * R > 2^19: the tiled layout's three kernels
+    ("dsv3", "expanded", 3),
+    ("dsv3", "hierarchical", 5),
+    ("large", "hierarchical", 7),
+])
+def test_launches_per_step(cfg, path, per_step):
+    """The bench's gpu_launches claim per step, for the library's launch
+    plans (the one-kernel limits of ep_layout_and_dispatch, the tiled
+    layout beyond 2^19 token-rank pairs, two kernels per stage on the
+    two-stage path)."""
+    import bench
+    from combine_ep_get_gb300.inputs import CONFIGS
+    c = CONFIGS[cfg]
+    fused = path == "rank"
+    got = bench.kernels_per_step(c.T, c.R, path == "expanded", path == "hierarchical", fused, c.K, c.E)
+    assert got == per_step
