@@ -11,19 +11,23 @@
 // layout_small_kernel), since at that size the cluster's fixed phases cost more
 // than the work.
 //
-// Main path: ONE launch of one thread-block cluster (up to 16 CTAs of 1024
-// threads, one per SM).  CTA c owns a contiguous token range; it builds the
-// membership bitmaps [words][R] and the expert histogram of its range in
-// shared memory, then after a hardware cluster barrier every CTA reads the
-// other CTAs' per-rank counts through distributed shared memory to get its
-// base row per rank (rank_offset + earlier CTAs), CTA 0 writes the rank counts
-// and offsets and the last CTA the expert / node counts and expert offsets; a
-// second cluster barrier keeps every CTA's shared memory alive until all remote
-// reads are done, then each CTA writes dst_row and is_token_in_rank for its
-// range with 16-byte stores.  No global-memory synchronisation, no spin.
+// Main path (T * R <= 2^19): ONE launch of one thread-block cluster (up to
+// 16 CTAs of 1024 threads, one per SM).  CTA c owns a contiguous token range;
+// it builds the membership bitmaps [words][R] and the expert histogram of its
+// range in shared memory, then after a hardware cluster barrier every CTA
+// reads the other CTAs' per-rank counts through distributed shared memory to
+// get its base row per rank (rank_offset + earlier CTAs); CTA 0 writes the
+// rank counts and offsets and the last CTA gathers the expert / node counts
+// and writes them with the expert offsets.  Each CTA then writes dst_row and
+// is_token_in_rank for its range with 16-byte stores (behind
+// ep_layout_and_dispatch it then publishes a rows-ready tag in its workspace
+// line, on which the dispatch's first wave starts), then its token offsets
+// and src_dst_count; a closing cluster barrier keeps every CTA's shared
+// memory alive for the other CTAs' remote reads.  No global-memory
+// synchronisation and no spin inside the kernel.
 //
-// Fallback (when a CTA's bitmaps would not fit in shared memory): three
-// launches over tiles of 256 tokens:
+// Fallback (T * R > 2^19, or a CTA's bitmaps would not fit in shared memory):
+// three launches over tiles of 256 tokens:
 //   1. count:  per tile, a shared-memory membership bitmap [8 words][R]
 //              (bit t of rank r set when token t has an expert on r), built
 //              from coalesced top-k loads with shared atomics; per-tile rank,
