@@ -17,7 +17,6 @@ ep_dispatch), which share no signal:
 """
 import ctypes
 
-import numpy as np
 import pytest
 import torch
 
