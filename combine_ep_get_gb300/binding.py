@@ -272,6 +272,12 @@ def ep_layout_and_dispatch(x, topk_idx, topk_weights, num_experts, num_ranks, la
                            recv_topk_idx, recv_topk_weights, recv_src_idx, d_status, recv_sf=None,
                            out_dtype=EP_BF16, sf_col_major=False, ranks_per_node=0, expert_alignment=1,
                            stream=None):
+    """ep_get_layout and ep_dispatch in one call (see the C header): one kernel
+    for few tokens, else the layout kernel and the dispatch, whose first wave
+    starts on the layout's rows-ready signal in `workspace`.  Size `workspace`
+    with ep_layout_workspace_bytes and the receive arrays with
+    ep_recv_capacity_bound; the workspace belongs to the call until the
+    dispatch completes."""
     T, H = x.shape
     K = topk_idx.shape[1]
     assert x.element_size() == 2 and x.is_contiguous() and recv_x.is_contiguous()
